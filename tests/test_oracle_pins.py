@@ -1,0 +1,284 @@
+"""Pins for the CPU oracle: each test checks it against something other than itself.
+
+Sources of truth used here: closed forms of the rotation and of the softmax, library
+routines (torch rounding, torch.topk, torch matmul, torch scaled-dot-product attention),
+a brute-force dense formulation on tiny inputs, and the values the pages print about the
+IndexShare schedule (``tests/golden/indexshare_facts.json``).
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import brute
+from oracle import dsa_oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "indexshare_facts.json")
+
+
+def facts():
+    with open(GOLDEN) as f:
+        return json.load(f)
+
+
+# ---------------------------------------------------------------------------- bf16 rounding
+
+def test_round_to_bf16_matches_torch_rne():
+    rng = np.random.default_rng(0)
+    x = np.concatenate([rng.standard_normal(20000) * 10.0 ** rng.integers(-6, 6, 20000),
+                        [0.0, -0.0, 1.0, -1.0]]).astype(np.float32).astype(np.float64)
+    ref = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(O.round_to_bf16(x), ref)
+
+
+def test_round_to_bf16_halfway_goes_to_even():
+    # 1 + 2^-8 is halfway between 1 and 1 + 2^-7 -> even mantissa (1.0)
+    # 1 + 3*2^-8 is halfway between 1 + 2^-7 and 1 + 2^-6 -> even (1 + 2^-6)
+    x = np.array([1 + 2.0 ** -8, 1 + 3 * 2.0 ** -8, -(1 + 2.0 ** -8)])
+    np.testing.assert_array_equal(O.round_to_bf16(x), [1.0, 1 + 2.0 ** -6, -1.0])
+    ref = torch.tensor(x, dtype=torch.float32).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(O.round_to_bf16(x), ref)
+
+
+def test_bf16_bits_decode():
+    bits = np.array([0x3F80, 0xBF80, 0x4000, 0x0000, 0x3E80], dtype=np.uint16)
+    np.testing.assert_array_equal(O.bf16_bits_to_f64(bits), [1.0, -1.0, 2.0, 0.0, 0.25])
+
+
+# ---------------------------------------------------------------------------- RoPE
+
+def test_rope_zero_dims_is_identity():
+    x = np.random.default_rng(1).standard_normal((5, 3, 64))
+    np.testing.assert_array_equal(O.rope_rotate_f64(x, np.arange(5)[:, None], 0, 1e4), x)
+
+
+def test_rope_leaves_the_first_d_minus_r_dims_alone():
+    # RoPE sits in the LAST r dims of each index head (Megatron convention).
+    x = np.random.default_rng(2).standard_normal((7, 128))
+    y = O.rope_rotate_f64(x, np.arange(7) * 1000 + 3, 64, 8e6)
+    np.testing.assert_array_equal(y[:, :64], x[:, :64])
+    assert not np.allclose(y[:, 64:], x[:, 64:])
+
+
+def test_rope_closed_form_on_unit_vectors():
+    # e at rotary slot i of the first half -> (cos(p f_i), sin(p f_i)) at slots (i, i + r/2).
+    d, r, theta, p = 64, 16, 1e4, 37
+    f = {0: 1.0, 1: 1.0 / math.sqrt(10.0), 4: 0.01}     # 1e4^(-2i/16): i=1 -> 10^-0.5, i=4 -> 10^-2
+    for i, fi in f.items():
+        e = np.zeros(d)
+        e[d - r + i] = 1.0
+        y = O.rope_rotate_f64(e, np.array(p), r, theta)
+        expect = np.zeros(d)
+        expect[d - r + i] = math.cos(p * fi)
+        expect[d - r // 2 + i] = math.sin(p * fi)
+        np.testing.assert_allclose(y, expect, atol=1e-15)
+    # a unit vector in the second half rotates the other way: (-sin, cos)
+    e = np.zeros(d)
+    e[d - r // 2 + 1] = 1.0
+    y = O.rope_rotate_f64(e, np.array(p), r, theta)
+    assert y[d - r + 1] == pytest.approx(-math.sin(p * f[1]), abs=1e-15)
+    assert y[d - r // 2 + 1] == pytest.approx(math.cos(p * f[1]), abs=1e-15)
+
+
+def test_rope_preserves_norm_and_depends_on_relative_position_only():
+    rng = np.random.default_rng(3)
+    a, b = rng.standard_normal(128), rng.standard_normal(128)
+    r, th = 64, 8e6
+    ra = lambda v, p: O.rope_rotate_f64(v, np.array(p), r, th)
+    assert np.linalg.norm(ra(a, 123456)) == pytest.approx(np.linalg.norm(a), rel=1e-13)
+    d0 = ra(a, 1000) @ ra(b, 990)
+    for shift in (1, 77, 500000, 1048575 - 1000):
+        assert ra(a, 1000 + shift) @ ra(b, 990 + shift) == pytest.approx(d0, rel=1e-9, abs=1e-9)
+
+
+def test_apply_index_rope_rounds_to_bf16():
+    rng = np.random.default_rng(4)
+    x = O.round_to_bf16(rng.standard_normal((3, 4, 64)) / 8)
+    y = O.apply_index_rope(x, np.array([5, 6, 7])[:, None], 16, 1e4)
+    np.testing.assert_array_equal(y, O.round_to_bf16(y))
+    np.testing.assert_array_equal(y[..., :48], x[..., :48])
+
+
+# ---------------------------------------------------------------------------- indexer scores
+
+def test_scores_single_head_unit_weight_is_relu_matmul():
+    rng = np.random.default_rng(5)
+    q = rng.standard_normal((1, 32))
+    k = rng.standard_normal((50, 32))
+    s = O.indexer_scores_row(q, k, np.array([1.0]))
+    ref = torch.relu(torch.from_numpy(k) @ torch.from_numpy(q[0])).numpy()
+    np.testing.assert_allclose(s, ref, rtol=1e-14, atol=1e-14)
+
+
+def test_scores_weighted_head_sum_and_sign():
+    rng = np.random.default_rng(6)
+    q = rng.standard_normal((3, 16))
+    k = rng.standard_normal((20, 16))
+    s = O.indexer_scores_row(q, k, np.array([2.0, 0.0, -1.0]))
+    tq, tk = torch.from_numpy(q), torch.from_numpy(k)
+    ref = 2.0 * torch.relu(tk @ tq[0]) - torch.relu(tk @ tq[2])
+    np.testing.assert_allclose(s, ref.numpy(), rtol=1e-13, atol=1e-13)
+    # negative weights make negative scores possible
+    assert (s < 0).any()
+
+
+# ---------------------------------------------------------------------------- top-k
+
+def test_topk_distinct_scores_matches_torch_topk_set():
+    rng = np.random.default_rng(7)
+    for L, k in ((100, 10), (4096, 2048), (50, 49)):
+        s = rng.standard_normal(L)
+        got = O.topk_row(s, k)
+        ref = torch.topk(torch.from_numpy(s), k).indices.numpy()
+        assert set(got.tolist()) == set(ref.tolist())
+        assert np.all(np.diff(got) > 0)
+
+
+def test_topk_ties_go_to_lower_index():
+    s = np.array([1.0, 5.0, 3.0, 5.0, 3.0, 3.0, 0.0])
+    np.testing.assert_array_equal(O.topk_row(s, 3), [1, 2, 3])
+    np.testing.assert_array_equal(O.topk_row(s, 4), [1, 2, 3, 4])
+    np.testing.assert_array_equal(O.topk_row(np.zeros(6), 2), [0, 1])
+
+
+def test_topk_short_row_pads_with_minus_one():
+    pad = facts()["short_sequence_topk"]["pad_value"]
+    s = np.array([0.3, -2.0, 7.0])
+    np.testing.assert_array_equal(O.topk_row(s, 5), [0, 1, 2, pad, pad])
+    np.testing.assert_array_equal(O.topk_row(np.zeros(0), 3), [pad, pad, pad])
+
+
+def test_indexer_topk_causal_first_row_sees_only_itself():
+    rng = np.random.default_rng(8)
+    T, H, d = 6, 2, 16
+    q = O.round_to_bf16(rng.standard_normal((T, H, d)))
+    k = O.round_to_bf16(rng.standard_normal((T, d)))
+    w = rng.standard_normal((T, H))
+    pos = np.arange(T)
+    idx = O.indexer_topk(q, k, w, pos, pos, np.zeros(T, int), pos + 1, 4, 1e4, 3)
+    np.testing.assert_array_equal(idx[0], [0, -1, -1])
+    np.testing.assert_array_equal(idx[1], [0, 1, -1])
+    assert (idx[5] >= 0).sum() == 3 and idx[5].max() <= 5
+
+
+# ---------------------------------------------------------------------------- attention
+
+def test_attn_equal_logits_give_the_mean_of_v():
+    rng = np.random.default_rng(9)
+    kv = rng.standard_normal((30, 576))
+    q = np.zeros((2, 576))
+    idx = np.array([3, 7, 11, 29, -1, -1])
+    o, lse = O.sparse_attn_row(q, kv, idx, 0, 0.5)
+    np.testing.assert_allclose(o, np.broadcast_to(kv[[3, 7, 11, 29], :512].mean(0), (2, 512)), rtol=1e-13)
+    np.testing.assert_allclose(lse, [math.log(4)] * 2, rtol=1e-14)
+
+
+def test_attn_single_row_and_empty_row():
+    rng = np.random.default_rng(10)
+    kv = rng.standard_normal((10, 576))
+    q = rng.standard_normal((3, 576))
+    o, lse = O.sparse_attn_row(q, kv, np.array([-1, -1]), 4, 0.1)
+    assert np.all(o == 0) and np.all(np.isneginf(lse))
+    o, lse = O.sparse_attn_row(q, kv, np.array([2, -1]), 4, 0.1)      # row 4 + 2 = 6
+    np.testing.assert_allclose(o, np.broadcast_to(kv[6, :512], (3, 512)), rtol=1e-14)
+    np.testing.assert_allclose(lse, 0.1 * q @ kv[6], rtol=1e-13)
+
+
+def test_sparse_equals_dense_causal_when_k_covers_the_prefix():
+    # Short rows "degenerate to dense": with k >= L_t the selection is the whole prefix.
+    rng = np.random.default_rng(11)
+    T, H, scale = 40, 4, 1.0 / math.sqrt(576)
+    q = rng.standard_normal((T, H, 576))
+    kv = rng.standard_normal((T, 576))
+    idx = np.stack([O.topk_row(rng.standard_normal(t + 1), 64) for t in range(T)])
+    o, lse = O.sparse_attn(q, kv, idx, np.zeros(T, int), scale)
+    tq = torch.from_numpy(q).permute(1, 0, 2)                           # [H, T, 576]
+    tk = torch.from_numpy(kv)[None].expand(H, T, 576)
+    tv = torch.from_numpy(kv[:, :512])[None].expand(H, T, 512)
+    ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=True, scale=scale)
+    np.testing.assert_allclose(o, ref.permute(1, 0, 2).numpy(), rtol=1e-11, atol=1e-12)
+    # lse of the first row is its single logit
+    np.testing.assert_allclose(lse[0], scale * q[0] @ kv[0], rtol=1e-12)
+
+
+# ---------------------------------------------------------------------------- brute force
+
+@pytest.mark.parametrize("seed,T,H_I,d,r,k,H", [(0, 48, 4, 64, 16, 8, 4), (1, 64, 8, 32, 8, 16, 2),
+                                                  (2, 33, 1, 16, 0, 40, 3), (3, 64, 4, 64, 16, 32, 4)])
+def test_oracle_matches_brute_force(seed, T, H_I, d, r, k, H):
+    rng = np.random.default_rng(seed)
+    q_idx = O.round_to_bf16(rng.standard_normal((T, H_I, d)) / math.sqrt(d))
+    k_idx = O.round_to_bf16(rng.standard_normal((T, d)) / math.sqrt(d))
+    w = rng.standard_normal((T, H_I))
+    pos = np.arange(T)
+    ks, ke = np.zeros(T, int), pos + 1
+    idx, rows = O.indexer_topk(q_idx, k_idx, w, pos, pos, ks, ke, r, 1e4, k, return_scores=True)
+    # brute force: dense scores from the same rotated inputs, full argsort, mask
+    q_rot = O.apply_index_rope(q_idx, pos[:, None], r, 1e4)
+    k_rot = O.apply_index_rope(k_idx, pos, r, 1e4)
+    S = brute.dense_scores(q_rot, k_rot, w, ks, ke)
+    for t in range(T):
+        np.testing.assert_allclose(rows[t], S[t, :t + 1], rtol=1e-12, atol=1e-12)
+    mask = brute.topk_mask(S, ks, ke, k)
+    for t in range(T):
+        assert set(idx[t][idx[t] >= 0].tolist()) == set(np.nonzero(mask[t])[0].tolist())
+    q = rng.standard_normal((T, H, 576))
+    kv = rng.standard_normal((T, 576))
+    o, lse = O.sparse_attn(q, kv, idx, ks, 1 / math.sqrt(576))
+    ob, lseb = brute.dense_masked_attn(q, kv, mask, 1 / math.sqrt(576))
+    np.testing.assert_allclose(o, ob, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(lse, lseb, rtol=1e-12)
+
+
+# ---------------------------------------------------------------------------- IndexShare
+
+def test_donor_table_on_the_78_layer_fsss_schedule():
+    f = facts()["glm52_schedule"]
+    types = [O.FULL if l % 4 == 0 else O.SHARED for l in range(f["n_layers"])]
+    donors = O.donor_table(types)
+    full = [l for l in range(len(types)) if donors[l] == l]
+    assert len(full) == f["n_full"] and len(types) - len(full) == f["n_shared"]
+    assert full[:3] == f["full_layers_prefix"]
+    assert [l for l in range(8) if donors[l] != l] == f["shared_layers_prefix"]
+    assert round(100.0 * f["n_shared"] / f["n_layers"], 1) == f["pruned_percent_1dp"]
+    ex = facts()["donor_example"]
+    for l in ex["layers"]:
+        assert donors[l] == ex["donor"] != ex["wrong_donor"]
+
+
+def test_donor_table_follows_the_released_indexer_types():
+    types = facts()["released_config"]["indexer_types_prefix"]
+    assert O.donor_table(types) == [0, 1, 2, 2, 2, 2, 6, 6, 6, 6]
+
+
+def test_shared_layer_without_donor_is_an_error():
+    with pytest.raises(O.NoDonorError):
+        O.donor_table([O.SHARED, O.FULL])
+    with pytest.raises(ValueError):
+        O.donor_table([O.FULL, "sometimes"])
+
+
+def test_layers_forward_reuses_donor_indices_and_runs_own_attention():
+    rng = np.random.default_rng(12)
+    T, H_I, d, H = 24, 2, 32, 2
+    types = [O.FULL, O.SHARED, O.FULL, O.SHARED]
+    layers = []
+    for t in types:
+        L = {"q": rng.standard_normal((T, H, 576)), "kv": rng.standard_normal((T, 576))}
+        if t == O.FULL:
+            L.update(q_idx=O.round_to_bf16(rng.standard_normal((T, H_I, d))),
+                     k_idx=O.round_to_bf16(rng.standard_normal((T, d))),
+                     w=rng.standard_normal((T, H_I)))
+        layers.append(L)
+    pos = np.arange(T)
+    idx, o, lse = O.layers_forward(types, layers, pos, pos, np.zeros(T, int), pos + 1, 8, 1e4, 6,
+                                   1 / 24.0)
+    assert idx[1] is idx[0] and idx[3] is idx[2]
+    assert not np.array_equal(idx[0], idx[2])
+    assert not np.allclose(o[0], o[1])
+    # each layer's output is its own attention over the shared index set
+    o1, _ = O.sparse_attn(layers[1]["q"], layers[1]["kv"], idx[0], np.zeros(T, int), 1 / 24.0)
+    np.testing.assert_array_equal(o[1], o1)
