@@ -1,0 +1,388 @@
+"""Benchmark of the IndexShare DSA hot path on one GB300 (or N independent replicas).
+
+One step = one `indexshare_layers_forward` over the 8-layer T=4096 prefill workload
+(indexer_types F F F S S S F S, 32 index heads x 128 with the last 64 dims RoPE'd at
+theta 8e6, top-k 2048, 16 attention heads of 576/512): 4 lightning-indexer + fused top-k
+passes and 8 sparse-attention passes, every step of the path in libdsa's kernels.
+
+Prints one JSON line.  `value` = query tokens per second (whole job, inputs resident in
+HBM), `e2e` = the same through the C ABI with every input copied from pinned host memory
+and every layer output copied back inside the timed region.  `roofline` describes the
+dominant kernel (sparse attention); `cpu_baseline` times the float64 CPU oracle on a
+bounded sample of the same workload.  `--impl reference` times only that oracle.
+
+Timing: W warm-up steps, then K steps each bracketed by CUDA events on the launching
+stream; L2 is flushed (a 512 MiB write) between timed steps, outside the events.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "prefill_4k"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+# --------------------------------------------------------------------------- distributed
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(ws: int, backend: str):
+    if ws > 1 and not torch.distributed.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.distributed.init_process_group(backend=backend)
+
+
+def max_over_ranks(x: float, device) -> float:
+    """Max of a per-rank float over all ranks (identity for a single process)."""
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier():
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        torch.distributed.barrier()
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            p = [x.strip() for x in l.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                mx = max(mx, float(p[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, p[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- workload
+def build_inputs(w, geo, device):
+    from dsa_indexer_cross_gb300 import synth
+    layers = []
+    for l in range(len(w.layers)):
+        L = synth.layer_inputs(w, geo, l, device=device)
+        L["out"] = torch.empty((w.n_q, w.n_heads, w.d_v), dtype=torch.bfloat16, device=device)
+        L["lse"] = torch.empty((w.n_q, w.n_heads), dtype=torch.float32, device=device)
+        layers.append(L)
+    return layers
+
+
+def roofline_numbers(w, geo):
+    """Algorithmic work of one launch of each kernel (definitions in the design notes)."""
+    L = (geo.ke - geo.ks).astype(np.int64)
+    rows = np.minimum(L, w.topk).sum()                       # selected rows per layer
+    pairs = L.sum()                                          # causal (query, key) pairs
+    attn_gathered = rows * w.d_qk * 2 + w.n_q * w.n_heads * (w.d_qk + w.d_v) * 2 + w.n_q * w.topk * 4
+    attn_flops = 2.0 * rows * w.n_heads * (w.d_qk + w.d_v)
+    idx_flops = 2.0 * pairs * w.n_heads_idx * w.head_dim_idx
+    idx_bytes = (w.n_q * w.n_heads_idx * w.head_dim_idx * 2 + geo.n_kv * w.head_dim_idx * 2 + w.n_q * w.n_heads_idx * 4
+                 + w.n_q * w.topk * 4)
+    return dict(attn_gathered=float(attn_gathered), attn_flops=attn_flops, idx_flops=idx_flops,
+                idx_bytes=float(idx_bytes), rows=int(rows), pairs=int(pairs))
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained", d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# --------------------------------------------------------------------------- oracle timing
+def time_oracle(w, geo, layers_host, budget_s: float, max_rows: int = 512):
+    """Run the float64 oracle over all layers on growing row samples until ~budget_s of work."""
+    from dsa_indexer_cross_gb300 import synth
+    from oracle import dsa_oracle as O
+    rng = np.random.default_rng(7)
+    n = 4
+    spent, done_rows = 0.0, 0
+    while True:
+        rows = np.sort(rng.choice(w.n_q, size=min(n, w.n_q), replace=False))
+        t0 = time.perf_counter()
+        O.layers_forward(w.layers, layers_host, geo.q_pos, geo.k_pos, geo.ks, geo.ke, w.rope_dim, w.theta, w.topk,
+                         w.softmax_scale, rows=rows)
+        dt = time.perf_counter() - t0
+        spent += dt
+        done_rows += len(rows)
+        if spent >= budget_s or n >= max_rows:
+            break
+        n = min(max_rows, max(n * 2, int(n * budget_s / max(dt, 1e-3) * 0.5)))
+    return done_rows / spent, done_rows, spent
+
+
+def host_layers(layers):
+    from dsa_indexer_cross_gb300 import synth
+    out = []
+    for L in layers:
+        H = {k: synth.to_f64(v) for k, v in L.items() if k in ("q_idx", "k_idx", "w", "q", "kv")}
+        out.append(H)
+    return out
+
+
+# --------------------------------------------------------------------------- reference arm
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    from dsa_indexer_cross_gb300 import synth
+    w = synth.WORKLOADS[args.workload]
+    geo = synth.geometry(w)
+    layers = [synth.layer_inputs(w, geo, l, device="cpu") for l in range(len(w.layers))]
+    hl = host_layers(layers)
+    from oracle import dsa_oracle as O
+    rows_per_step = 8
+    rng = np.random.default_rng(11)
+    times = []
+    for s in range(args.warmup + args.steps):
+        rows = np.sort(rng.choice(w.n_q, size=rows_per_step, replace=False))
+        t0 = time.perf_counter()
+        O.layers_forward(w.layers, hl, geo.q_pos, geo.k_pos, geo.ks, geo.ke, w.rope_dim, w.theta, w.topk,
+                         w.softmax_scale, rows=rows)
+        if s >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    sec = sum(times) / len(times)
+    value = rows_per_step / sec
+    cores = os.cpu_count()
+    line = {"impl": "reference", "metric": "indexer+top-k and sparse-attn query-tokens/sec", "value": value,
+            "unit": "query_tokens/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic (seeded Gaussian, bf16 inputs)",
+            "config": {"workload": f"{w.name}: T={w.n_q}, {len(w.layers)} layers {''.join(t[0].upper() for t in w.layers)}, "
+                                   f"H_I={w.n_heads_idx}x{w.head_dim_idx}, topk={w.topk}, H={w.n_heads}",
+                       "sample": f"{rows_per_step} random query rows per step through all layers"},
+            "cpu_baseline": {"value": value, "unit": "query_tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{rows_per_step} query rows x {len(w.layers)} layers per step"},
+            "e2e": {"value": value, "unit": "query_tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# --------------------------------------------------------------------------- native arm
+def run_native(args):
+    ws_n, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(ws_n, "nccl")
+    from dsa_indexer_cross_gb300.build import build
+    build()
+    import dsa_indexer_cross_gb300 as D
+    from dsa_indexer_cross_gb300 import synth
+    w = synth.WORKLOADS[args.workload]
+    geo = synth.geometry(w)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    q_pos, k_pos, ks, ke = t(geo.q_pos), t(geo.k_pos), t(geo.ks), t(geo.ke)
+    layers = build_inputs(w, geo, dev)
+    cache = D.IndexCache(w.layers, w.n_q, w.topk, device=dev)
+    flags = D.DSA_IDX_ROPE_Q | (D.DSA_IDX_ROPE_K if w.rope_k else 0)
+    if w.kind == "decode":
+        flags |= D.DSA_IDX_INDEPENDENT_ROWS
+    idesc = D.indexer_desc(w.n_q, geo.n_kv, w.n_heads_idx, w.head_dim_idx, w.rope_dim, w.topk, geo.max_len, flags)
+    adesc = D.attn_desc(w.n_q, geo.n_kv, w.n_heads, w.topk, w.softmax_scale)
+    rope = D.dsa_rope_table(w.theta, w.rope_dim, geo.max_pos).to(dev)
+    ws = torch.empty(D.dsa_layers_workspace_size(idesc, adesc), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+
+    def step():
+        D.indexshare_layers_forward(idesc, adesc, w.layers, layers, ks, ke, q_pos, k_pos, rope, cache, ws=ws,
+                                    stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if D.dsa_workspace_status(ws) != 0:
+        raise RuntimeError("device status set during warm-up")
+
+    # ---------------- timed steps (device-resident inputs)
+    barrier()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        for a, b in evs:
+            flush.zero_()
+            a.record(stream)
+            step()
+            b.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    ms = [a.elapsed_time(b) for a, b in evs]
+    ms_step = max_over_ranks(sum(ms) / len(ms), dev)
+    value = ws_n * w.n_q / (ms_step / 1e3)
+
+    # ---------------- per-kernel timing of the dominant kernel (sparse attention) and the indexer
+    idx_full = cache.buffers[0]
+    attn_ws = torch.empty(D.dsa_sparse_attn_workspace_size(adesc), dtype=torch.uint8, device=dev)
+    idx_ws = torch.empty(D.dsa_indexer_workspace_size(idesc), dtype=torch.uint8, device=dev)
+    L0 = layers[0]
+
+    def time_call(fn, n):
+        e = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        fn()
+        for a, b in e:
+            flush.zero_()
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in e) / n
+
+    attn_ms = time_call(lambda: D.dsa_sparse_attn(adesc, L0["q"], L0["kv"], idx_full, ks, L0["out"], L0["lse"],
+                                                  ws=attn_ws, stream=stream), 10)
+    idx_ms = time_call(lambda: D.dsa_indexer_topk(idesc, L0["q_idx"], L0["k_idx"], L0["w"], q_pos, k_pos, ks, ke, rope,
+                                                  idx_full, None, ws=idx_ws, stream=stream), 10)
+
+    # ---------------- end to end through the C ABI from pinned host buffers
+    in_keys = ("q_idx", "k_idx", "w", "q", "kv")
+    host_in = [{k: v.cpu().pin_memory() for k, v in L.items() if k in in_keys} for L in layers]
+    host_out = [torch.empty(L["out"].shape, dtype=L["out"].dtype).pin_memory() for L in layers]
+    h2d = sum(v.numel() * v.element_size() for H in host_in for v in H.values())
+    d2h = sum(v.numel() * v.element_size() for v in host_out)
+    dev_in = [{k: torch.empty_like(v, device=dev) for k, v in H.items()} for H in host_in]
+    for l, L in enumerate(dev_in):
+        L["out"], L["lse"] = layers[l]["out"], layers[l]["lse"]
+
+    def e2e_step():
+        for H, Dd in zip(host_in, dev_in):
+            for k, v in H.items():
+                Dd[k].copy_(v, non_blocking=True)
+        D.indexshare_layers_forward(idesc, adesc, w.layers, dev_in, ks, ke, q_pos, k_pos, rope, cache, ws=ws,
+                                    stream=stream)
+        for L, Ho in zip(dev_in, host_out):
+            Ho.copy_(L["out"], non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(max(3, args.steps // 2))]
+    for a, b in e2e_ev:
+        a.record(stream)
+        e2e_step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in e2e_ev) / len(e2e_ev), dev)
+    if D.dsa_workspace_status(ws) != 0:
+        raise RuntimeError("device status set during the timed region")
+
+    hbm, tc_burst, tc_sus, peak_kind = peaks()
+    R = roofline_numbers(w, geo)
+    attn_gbs = R["attn_gathered"] / (attn_ms / 1e3) / 1e9
+    attn_strict_tflops = R["attn_flops"] / (attn_ms / 1e3) / 1e12
+    idx_tflops = R["idx_flops"] / (idx_ms / 1e3) / 1e12
+    gpu_launches = sum((3 if t == "full" else 0) + 2 for t in w.layers) + 2 * sum(t == "full" for t in w.layers)
+
+    line = {
+        "metric": "indexer+top-k and sparse-attn query-tokens/sec",
+        "value": value, "unit": "query_tokens/s", "n_gpus": ws_n, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 (fp32 accumulate)", "data": "synthetic (seeded Gaussian, bf16)",
+        "config": {"workload": f"{w.name}: T={w.n_q} prefill, {len(w.layers)} layers "
+                               f"{''.join(t[0].upper() for t in w.layers)}, H_I={w.n_heads_idx}x{w.head_dim_idx} "
+                               f"(rope {w.rope_dim}, theta {w.theta:g}), topk={w.topk}, H={w.n_heads} 576/512",
+                   "l2": "flushed between timed steps (512 MiB write outside the events)",
+                   "parallelism": "replicas" if ws_n > 1 else "single GPU"},
+        "e2e": {"value": ws_n * w.n_q / (e2e_ms / 1e3), "unit": "query_tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": gpu_launches * args.steps,
+        "roofline": {"kernel": "sparse_attn_kernel", "bound": "hbm", "achieved": attn_gbs, "peak": hbm, "unit": "GB/s",
+                     "frac": attn_gbs / hbm, "traffic": None, "peak_kind": peak_kind,
+                     "algorithmic_bytes_per_launch": R["attn_gathered"], "ms_per_launch": attn_ms,
+                     "strict_tensor_tflops": attn_strict_tflops, "strict_tensor_frac": attn_strict_tflops / tc_sus},
+        "roofline_indexer": {"kernel": "indexer (rope + tcgen05 scores/top-k + select)", "bound": "tensor",
+                             "achieved": idx_tflops, "peak": tc_burst, "unit": "TFLOP/s", "frac": idx_tflops / tc_burst,
+                             "algorithmic_flops_per_launch": R["idx_flops"], "ms_per_launch": idx_ms,
+                             "peak_kind": peak_kind},
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        hl = host_layers(layers)
+        rate, n_rows, spent = time_oracle(w, geo, hl, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": rate, "unit": "query_tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                                "sample": f"{n_rows} query rows through all {len(w.layers)} layers "
+                                          f"({spent:.1f} s of float64 NumPy)"}
+    if rank == 0:
+        print(json.dumps(line))
+    cache.close()
+    if torch.distributed.is_initialized():
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_native(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

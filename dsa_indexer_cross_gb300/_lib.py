@@ -1,0 +1,265 @@
+"""ctypes binding of libdsa.so (include/dsa.h).  Argument marshalling only.
+
+Every function keeps the C name.  Tensors are torch tensors on the GPU (their data pointers
+are passed through); the stream defaults to torch's current stream.  A non-OK status raises
+DsaError carrying the library's message.  There is no fallback: if the shared library is
+missing the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from typing import Optional, Sequence
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdsa.so")
+
+DSA_LAYER_SHARED = 0
+DSA_LAYER_FULL = 1
+DSA_IDX_ROPE_Q = 1 << 0
+DSA_IDX_ROPE_K = 1 << 1
+DSA_IDX_INDEPENDENT_ROWS = 1 << 2
+
+STATUS_NAMES = {0: "DSA_OK", 1: "DSA_ERR_ARG", 2: "DSA_ERR_SHAPE", 3: "DSA_ERR_NO_DONOR", 4: "DSA_ERR_UNSUPPORTED",
+                5: "DSA_ERR_CUDA", 6: "DSA_ERR_WORKSPACE", 7: "DSA_ERR_TIMEOUT", 8: "DSA_ERR_DEVICE"}
+EXPORTED = ("dsa_status_string", "dsa_last_error", "dsa_donor_table", "dsa_rope_table", "dsa_indexer_workspace_size",
+            "dsa_indexer_topk", "dsa_sparse_attn_workspace_size", "dsa_sparse_attn", "dsa_index_cache_create",
+            "dsa_index_cache_donor", "dsa_index_cache_indices", "dsa_index_cache_destroy",
+            "dsa_layers_workspace_size", "indexshare_layers_forward", "dsa_workspace_status")
+
+
+class DsaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        self.status = status
+        self.name = STATUS_NAMES.get(status, str(status))
+        super().__init__(f"{self.name}: {message}")
+
+
+class IndexerDesc(C.Structure):
+    _fields_ = [("n_q", C.c_int32), ("n_kv", C.c_int32), ("n_heads", C.c_int32), ("head_dim", C.c_int32),
+                ("rope_dim", C.c_int32), ("topk", C.c_int32), ("max_len", C.c_int32), ("flags", C.c_uint32)]
+
+
+class AttnDesc(C.Structure):
+    _fields_ = [("n_q", C.c_int32), ("n_kv", C.c_int32), ("n_heads", C.c_int32), ("d_qk", C.c_int32),
+                ("d_v", C.c_int32), ("topk", C.c_int32), ("softmax_scale", C.c_float), ("flags", C.c_uint32)]
+
+
+class LayerIO(C.Structure):
+    _fields_ = [("q_idx", C.c_void_p), ("k_idx", C.c_void_p), ("w", C.c_void_p), ("q", C.c_void_p),
+                ("kv", C.c_void_p), ("out", C.c_void_p), ("lse", C.c_void_p)]
+
+
+_lib: Optional[C.CDLL] = None
+
+
+def lib() -> C.CDLL:
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is not built: run dsa_indexer_cross_gb300.build.build() first")
+        L = C.CDLL(LIB_PATH)
+        st, vp, i32, u32, sz = C.c_int, C.c_void_p, C.c_int32, C.c_uint32, C.c_size_t
+        P = C.POINTER
+        L.dsa_status_string.restype = C.c_char_p
+        L.dsa_status_string.argtypes = [st]
+        L.dsa_last_error.restype = C.c_char_p
+        L.dsa_last_error.argtypes = []
+        L.dsa_donor_table.restype = st
+        L.dsa_donor_table.argtypes = [i32, P(C.c_uint8), P(i32)]
+        L.dsa_rope_table.restype = st
+        L.dsa_rope_table.argtypes = [C.c_double, i32, i32, P(C.c_float)]
+        L.dsa_indexer_workspace_size.restype = st
+        L.dsa_indexer_workspace_size.argtypes = [P(IndexerDesc), P(sz)]
+        L.dsa_indexer_topk.restype = st
+        L.dsa_indexer_topk.argtypes = [P(IndexerDesc), vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, sz, vp]
+        L.dsa_sparse_attn_workspace_size.restype = st
+        L.dsa_sparse_attn_workspace_size.argtypes = [P(AttnDesc), P(sz)]
+        L.dsa_sparse_attn.restype = st
+        L.dsa_sparse_attn.argtypes = [P(AttnDesc), vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.dsa_index_cache_create.restype = st
+        L.dsa_index_cache_create.argtypes = [i32, P(C.c_uint8), i32, i32, P(vp), P(vp)]
+        L.dsa_index_cache_donor.restype = st
+        L.dsa_index_cache_donor.argtypes = [vp, i32, P(i32)]
+        L.dsa_index_cache_indices.restype = vp
+        L.dsa_index_cache_indices.argtypes = [vp, i32]
+        L.dsa_index_cache_destroy.restype = None
+        L.dsa_index_cache_destroy.argtypes = [vp]
+        L.dsa_layers_workspace_size.restype = st
+        L.dsa_layers_workspace_size.argtypes = [P(IndexerDesc), P(AttnDesc), P(sz)]
+        L.indexshare_layers_forward.restype = st
+        L.indexshare_layers_forward.argtypes = [P(IndexerDesc), P(AttnDesc), i32, P(C.c_uint8), P(LayerIO), vp, vp,
+                                                vp, vp, vp, i32, vp, vp, sz, vp]
+        L.dsa_workspace_status.restype = st
+        L.dsa_workspace_status.argtypes = [vp, vp, P(u32)]
+        _lib = L
+    return _lib
+
+
+def _check(status: int) -> None:
+    if status != 0:
+        raise DsaError(status, lib().dsa_last_error().decode())
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to libdsa must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _u8(types: Sequence[int]):
+    return (C.c_uint8 * len(types))(*[int(x) for x in types])
+
+
+def types_to_u8(indexer_types: Sequence) -> list:
+    """'full'/'shared' strings (as in a released config) or 0/1 ints -> 0/1 ints."""
+    out = []
+    for t in indexer_types:
+        if isinstance(t, str):
+            out.append(DSA_LAYER_FULL if t == "full" else DSA_LAYER_SHARED if t == "shared" else 255)
+        else:
+            out.append(int(t))
+    return out
+
+
+# ------------------------------------------------------------------------------ schedule
+
+def dsa_donor_table(indexer_types: Sequence) -> list:
+    types = types_to_u8(indexer_types)
+    donors = (C.c_int32 * max(1, len(types)))()
+    _check(lib().dsa_donor_table(len(types), _u8(types), donors))
+    return list(donors)[:len(types)]
+
+
+def dsa_rope_table(theta: float, rope_dim: int, n_pos: int) -> torch.Tensor:
+    """Host float32 tensor [n_pos, rope_dim/2, 2] of (cos, sin)."""
+    out = torch.empty((n_pos, max(rope_dim // 2, 1), 2), dtype=torch.float32)
+    _check(lib().dsa_rope_table(float(theta), int(rope_dim), int(n_pos),
+                                C.cast(out.data_ptr(), C.POINTER(C.c_float))))
+    return out
+
+
+# ------------------------------------------------------------------------------ indexer
+
+def indexer_desc(n_q, n_kv, n_heads, head_dim, rope_dim, topk, max_len, flags) -> IndexerDesc:
+    return IndexerDesc(n_q, n_kv, n_heads, head_dim, rope_dim, topk, max_len, flags)
+
+
+def dsa_indexer_workspace_size(desc: IndexerDesc) -> int:
+    n = C.c_size_t(0)
+    _check(lib().dsa_indexer_workspace_size(C.byref(desc), C.byref(n)))
+    return n.value
+
+
+def dsa_indexer_topk(desc: IndexerDesc, q_idx, k_idx, w, q_pos, k_pos, ks, ke, rope_cs, idx_out, score_out=None,
+                     ws=None, stream=None) -> torch.Tensor:
+    if ws is None:
+        ws = torch.empty(dsa_indexer_workspace_size(desc), dtype=torch.uint8, device=idx_out.device)
+    n_pos = rope_cs.shape[0] if rope_cs is not None else 0
+    _check(lib().dsa_indexer_topk(C.byref(desc), _ptr(q_idx), _ptr(k_idx), _ptr(w), _ptr(q_pos), _ptr(k_pos),
+                                  _ptr(ks), _ptr(ke), _ptr(rope_cs), n_pos, _ptr(idx_out), _ptr(score_out),
+                                  _ptr(ws), ws.numel(), _stream(stream)))
+    return ws
+
+
+# ------------------------------------------------------------------------------ attention
+
+def attn_desc(n_q, n_kv, n_heads, topk, softmax_scale, d_qk=576, d_v=512) -> AttnDesc:
+    return AttnDesc(n_q, n_kv, n_heads, d_qk, d_v, topk, softmax_scale, 0)
+
+
+def dsa_sparse_attn_workspace_size(desc: AttnDesc) -> int:
+    n = C.c_size_t(0)
+    _check(lib().dsa_sparse_attn_workspace_size(C.byref(desc), C.byref(n)))
+    return n.value
+
+
+def dsa_sparse_attn(desc: AttnDesc, q, kv, idx, ks, out, lse=None, ws=None, stream=None) -> torch.Tensor:
+    if ws is None:
+        ws = torch.empty(dsa_sparse_attn_workspace_size(desc), dtype=torch.uint8, device=out.device)
+    _check(lib().dsa_sparse_attn(C.byref(desc), _ptr(q), _ptr(kv), _ptr(idx), _ptr(ks), _ptr(out), _ptr(lse),
+                                 _ptr(ws), ws.numel(), _stream(stream)))
+    return ws
+
+
+# ------------------------------------------------------------------------------ index cache
+
+class IndexCache:
+    """Owns a dsa_index_cache handle and the per-full-layer device index buffers."""
+
+    def __init__(self, indexer_types: Sequence, n_q: int, topk: int, device="cuda"):
+        self.types = types_to_u8(indexer_types)
+        self.n_q, self.topk = n_q, topk
+        self.buffers = [torch.full((n_q, topk), -1, dtype=torch.int32, device=device)
+                        if t == DSA_LAYER_FULL else None for t in self.types]
+        ptrs = (C.c_void_p * len(self.types))(*[b.data_ptr() if b is not None else None for b in self.buffers])
+        h = C.c_void_p()
+        _check(lib().dsa_index_cache_create(len(self.types), _u8(self.types), n_q, topk, ptrs, C.byref(h)))
+        self.handle = h
+
+    def donor(self, layer: int) -> int:
+        d = C.c_int32(0)
+        _check(lib().dsa_index_cache_donor(self.handle, layer, C.byref(d)))
+        return d.value
+
+    def indices_ptr(self, layer: int) -> int:
+        p = lib().dsa_index_cache_indices(self.handle, layer)
+        if not p:
+            raise DsaError(1, lib().dsa_last_error().decode())
+        return p
+
+    def indices(self, layer: int) -> torch.Tensor:
+        return self.buffers[self.donor(layer)]
+
+    def close(self):
+        if getattr(self, "handle", None):
+            lib().dsa_index_cache_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+# ------------------------------------------------------------------------------ layer loop
+
+def dsa_layers_workspace_size(idesc: IndexerDesc, adesc: AttnDesc) -> int:
+    n = C.c_size_t(0)
+    _check(lib().dsa_layers_workspace_size(C.byref(idesc), C.byref(adesc), C.byref(n)))
+    return n.value
+
+
+def indexshare_layers_forward(idesc: IndexerDesc, adesc: AttnDesc, indexer_types: Sequence, layers: Sequence[dict],
+                              ks, ke, q_pos, k_pos, rope_cs, cache: IndexCache, ws=None, stream=None):
+    """layers[l]: dict with 'q', 'kv', 'out' (+ 'lse') and, on full layers, 'q_idx', 'k_idx', 'w'."""
+    types = types_to_u8(indexer_types)
+    io = (LayerIO * len(layers))()
+    for l, L in enumerate(layers):
+        io[l] = LayerIO(_ptr(L.get("q_idx")), _ptr(L.get("k_idx")), _ptr(L.get("w")), _ptr(L["q"]), _ptr(L["kv"]),
+                        _ptr(L["out"]), _ptr(L.get("lse")))
+    if ws is None:
+        ws = torch.empty(dsa_layers_workspace_size(idesc, adesc), dtype=torch.uint8, device=layers[0]["q"].device)
+    n_pos = rope_cs.shape[0] if rope_cs is not None else 0
+    _check(lib().indexshare_layers_forward(C.byref(idesc), C.byref(adesc), len(types), _u8(types), io, _ptr(ks),
+                                           _ptr(ke), _ptr(q_pos), _ptr(k_pos), _ptr(rope_cs), n_pos, cache.handle,
+                                           _ptr(ws), ws.numel(), _stream(stream)))
+    return ws
+
+
+def dsa_workspace_status(ws: torch.Tensor, stream=None) -> int:
+    """Synchronise and read the device status bits of a workspace; raises on a device fault."""
+    bits = C.c_uint32(0)
+    _check(lib().dsa_workspace_status(_ptr(ws), _stream(stream), C.byref(bits)))
+    return bits.value

@@ -1,0 +1,487 @@
+// Host side of the C ABI declared in include/dsa.h: argument checks, workspace layout,
+// tensor maps, the IndexShare donor schedule and index cache, and the layer loop.
+// Nothing here computes a result on the host; every step of the path runs in a kernel.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <string>
+#include <vector>
+
+#include <cudaTypedefs.h>
+
+#include "../../include/dsa.h"
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace dsa {
+
+namespace {
+
+thread_local std::string g_err;
+
+dsa_status fail(dsa_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return s;
+}
+
+dsa_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(DSA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ------------------------------------------------------------------ device properties
+struct DevInfo {
+  int sms = 0;
+  int major = 0, minor = 0;
+};
+
+DevInfo dev_info() {
+  static std::mutex mu;
+  static std::vector<DevInfo> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DevInfo{};
+  std::lock_guard<std::mutex> lock(mu);
+  if (static_cast<int>(cache.size()) <= dev) cache.resize(dev + 1);
+  DevInfo& d = cache[dev];
+  if (d.sms == 0) {
+    cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev);
+  }
+  return d;
+}
+
+dsa_status check_device() {
+  const DevInfo d = dev_info();
+  if (d.sms == 0) return fail(DSA_ERR_UNSUPPORTED, "no CUDA device is available");
+  if (d.major != 10 || d.minor != 3)
+    return fail(DSA_ERR_UNSUPPORTED, "libdsa is built for sm_103a; the current device is sm_%d%d", d.major, d.minor);
+  return DSA_OK;
+}
+
+// ------------------------------------------------------------------ tensor maps
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor [rows][inner], 128-byte swizzled boxes of {64, box_rows}.
+dsa_status tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return fail(DSA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(DSA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+  return DSA_OK;
+}
+
+// ------------------------------------------------------------------ indexer plan
+bool supported_heads(int h) { return h == 4 || h == 8 || h == 16 || h == 32 || h == 64; }
+
+struct IndexerLayout {
+  IndexerPlan plan{};
+  size_t off_q = 0, off_k = 0, off_rr = 0, off_gr = 0, off_cnt = 0, off_key = 0, off_idx = 0, total = 0;
+};
+
+dsa_status check_indexer_desc(const dsa_indexer_desc* d) {
+  if (!d) return fail(DSA_ERR_ARG, "indexer descriptor is NULL");
+  if (d->n_q < 0 || d->n_kv < 0) return fail(DSA_ERR_ARG, "n_q and n_kv must be >= 0");
+  if (d->head_dim != 64 && d->head_dim != 128)
+    return fail(DSA_ERR_UNSUPPORTED, "index head_dim %d: supported values are 64 and 128", d->head_dim);
+  if (!supported_heads(d->n_heads))
+    return fail(DSA_ERR_UNSUPPORTED, "index n_heads %d: supported values are 4, 8, 16, 32, 64", d->n_heads);
+  if (d->rope_dim < 0 || d->rope_dim > d->head_dim || (d->rope_dim & 1))
+    return fail(DSA_ERR_ARG, "rope_dim %d must be even and within [0, head_dim]", d->rope_dim);
+  if (d->topk < 1 || d->topk > 2048) return fail(DSA_ERR_UNSUPPORTED, "topk %d: supported range is 1..2048", d->topk);
+  if (d->n_q > 0 && (d->max_len < 1 || d->max_len > d->n_kv))
+    return fail(DSA_ERR_ARG, "max_len %d must lie in [1, n_kv=%d]", d->max_len, d->n_kv);
+  if (d->flags & ~(DSA_IDX_ROPE_Q | DSA_IDX_ROPE_K | DSA_IDX_INDEPENDENT_ROWS))
+    return fail(DSA_ERR_ARG, "unknown indexer flags 0x%x", d->flags);
+  if (static_cast<long long>(d->n_q) * d->n_heads > 0x7FFFFFFFLL)
+    return fail(DSA_ERR_SHAPE, "n_q * n_heads exceeds the int32 range");
+  return DSA_OK;
+}
+
+IndexerLayout indexer_layout(const dsa_indexer_desc* d, int sms) {
+  IndexerLayout L;
+  IndexerPlan& p = L.plan;
+  const bool indep = (d->flags & DSA_IDX_INDEPENDENT_ROWS) != 0;
+  p.n_heads = d->n_heads;
+  p.head_dim = d->head_dim;
+  p.topk = d->topk;
+  p.group = indep ? (d->n_heads >= 32 ? 1 : 32 / d->n_heads) : 256 / d->n_heads;
+  p.n_groups = (d->n_q + p.group - 1) / p.group;
+  const long long max_len = d->max_len > 0 ? d->max_len : 1;
+  long long chunk;
+  if (p.n_groups >= 4LL * sms) {
+    chunk = max_len;
+  } else {
+    chunk = (max_len * p.n_groups + 4LL * sms - 1) / (4LL * sms);
+    if (chunk < 4096) chunk = 4096;
+  }
+  if (chunk > 262144) chunk = 262144;
+  chunk = (chunk + 127) / 128 * 128;
+  p.chunk = static_cast<int>(chunk);
+  p.n_chunks = static_cast<int>((max_len + chunk - 1) / chunk);
+  const int cap0 = d->topk * 2 > d->topk + 128 ? d->topk * 2 : d->topk + 128;
+  p.cap = (cap0 + 127) / 128 * 128;
+  const long long units = static_cast<long long>(p.n_groups) * p.n_chunks;
+  p.grid = static_cast<int>(units < sms ? units : sms);
+  if (p.grid < 1) p.grid = 1;
+
+  size_t off = kAlign;  // header
+  const bool rq = (d->flags & DSA_IDX_ROPE_Q) && d->rope_dim > 0;
+  const bool rk = (d->flags & DSA_IDX_ROPE_K) && d->rope_dim > 0;
+  L.off_q = off;
+  if (rq) off += align_up(static_cast<size_t>(d->n_q) * d->n_heads * d->head_dim * 2);
+  L.off_k = off;
+  if (rk) off += align_up(static_cast<size_t>(d->n_kv) * d->head_dim * 2);
+  L.off_rr = off;
+  off += align_up(static_cast<size_t>(d->n_q) * 8);
+  L.off_gr = off;
+  off += align_up(static_cast<size_t>(p.n_groups) * 8);
+  const size_t slots = static_cast<size_t>(d->n_q) * p.n_chunks;
+  L.off_cnt = off;
+  off += align_up(slots * 4);
+  L.off_key = off;
+  off += align_up(slots * p.cap * 4);
+  L.off_idx = off;
+  off += align_up(slots * p.cap * 4);
+  L.total = off;
+  return L;
+}
+
+dsa_status run_indexer(const dsa_indexer_desc* d, const void* q_idx, const void* k_idx, const float* w,
+                       const int32_t* q_pos, const int32_t* k_pos, const int32_t* ks, const int32_t* ke,
+                       const float* rope_cs, int32_t rope_n_pos, int32_t* idx_out, float* score_out, void* ws,
+                       size_t ws_bytes, cudaStream_t st, bool clear_status) {
+  dsa_status s = check_indexer_desc(d);
+  if (s != DSA_OK) return s;
+  if (d->n_q == 0) return DSA_OK;
+  const bool rq = (d->flags & DSA_IDX_ROPE_Q) && d->rope_dim > 0;
+  const bool rk = (d->flags & DSA_IDX_ROPE_K) && d->rope_dim > 0;
+  if (!q_idx || !k_idx || !w || !ks || !ke || !idx_out || !ws)
+    return fail(DSA_ERR_ARG, "q_idx, k_idx, w, ks, ke, idx_out and ws must be non-NULL");
+  if ((rq && !q_pos) || (rk && !k_pos) || ((rq || rk) && (!rope_cs || rope_n_pos < 1)))
+    return fail(DSA_ERR_ARG, "RoPE requested but q_pos/k_pos/rope_cs/rope_n_pos missing");
+  if (!aligned16(q_idx) || !aligned16(k_idx)) return fail(DSA_ERR_ARG, "q_idx and k_idx must be 16-byte aligned");
+  if (rope_cs && !aligned16(rope_cs)) return fail(DSA_ERR_ARG, "rope_cs must be 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(ws) % kAlign) return fail(DSA_ERR_ARG, "workspace must be 256-byte aligned");
+  if ((s = check_device()) != DSA_OK) return s;
+  const DevInfo di = dev_info();
+  const IndexerLayout L = indexer_layout(d, di.sms);
+  if (ws_bytes < L.total)
+    return fail(DSA_ERR_WORKSPACE, "indexer workspace too small: %zu < %zu bytes", ws_bytes, L.total);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  uint32_t* status = reinterpret_cast<uint32_t*>(base);
+  cudaError_t e;
+  if (clear_status && (e = cudaMemsetAsync(ws, 0, kAlign, st)) != cudaSuccess) return cuda_fail(e, "clear status");
+  const void* qr = q_idx;
+  const void* kr = k_idx;
+  if (rq) {
+    e = launch_rope_rows(q_idx, base + L.off_q, q_pos, static_cast<int64_t>(d->n_q) * d->n_heads, d->n_heads,
+                         d->head_dim, d->rope_dim, rope_cs, rope_n_pos, status, st);
+    if (e != cudaSuccess) return cuda_fail(e, "index q RoPE");
+    qr = base + L.off_q;
+  }
+  if (rk && d->n_kv > 0) {
+    e = launch_rope_rows(k_idx, base + L.off_k, k_pos, d->n_kv, 1, d->head_dim, d->rope_dim, rope_cs, rope_n_pos,
+                         status, st);
+    if (e != cudaSuccess) return cuda_fail(e, "index k RoPE");
+    kr = base + L.off_k;
+  }
+  const IndexerPlan& p = L.plan;
+  int2* rr = reinterpret_cast<int2*>(base + L.off_rr);
+  int2* gr = reinterpret_cast<int2*>(base + L.off_gr);
+  e = launch_ranges(ks, ke, d->n_q, p.group, d->n_kv, d->max_len, rr, gr, status, st);
+  if (e != cudaSuccess) return cuda_fail(e, "key ranges");
+  uint32_t* cnt = reinterpret_cast<uint32_t*>(base + L.off_cnt);
+  uint32_t* ck = reinterpret_cast<uint32_t*>(base + L.off_key);
+  int32_t* ci = reinterpret_cast<int32_t*>(base + L.off_idx);
+  if (d->n_kv > 0) {
+    CUtensorMap tq, tk;
+    if ((s = tmap_bf16(&tq, qr, d->head_dim, static_cast<uint64_t>(d->n_q) * d->n_heads,
+                       static_cast<uint32_t>(p.group * d->n_heads))) != DSA_OK)
+      return s;
+    if ((s = tmap_bf16(&tk, kr, d->head_dim, d->n_kv, 128)) != DSA_OK) return s;
+    e = launch_indexer(p, tq, tk, w, d->n_q, rr, gr, ck, ci, cnt, status, st);
+    if (e != cudaSuccess) return cuda_fail(e, "indexer kernel");
+  } else {
+    if ((e = cudaMemsetAsync(cnt, 0, static_cast<size_t>(d->n_q) * p.n_chunks * 4, st)) != cudaSuccess)
+      return cuda_fail(e, "clear counts");
+  }
+  e = launch_select(d->n_q, p.n_chunks, p.cap, d->topk, rr, ck, ci, cnt, idx_out, score_out, status, st);
+  if (e != cudaSuccess) return cuda_fail(e, "top-k select");
+  return DSA_OK;
+}
+
+// ------------------------------------------------------------------ sparse attention
+dsa_status check_attn_desc(const dsa_attn_desc* d) {
+  if (!d) return fail(DSA_ERR_ARG, "attention descriptor is NULL");
+  if (d->n_q < 0 || d->n_kv < 0) return fail(DSA_ERR_ARG, "n_q and n_kv must be >= 0");
+  if (d->d_qk != 576 || d->d_v != 512)
+    return fail(DSA_ERR_UNSUPPORTED, "d_qk/d_v %d/%d: this build supports 576/512", d->d_qk, d->d_v);
+  if (d->n_heads < 1 || d->n_heads > 128) return fail(DSA_ERR_UNSUPPORTED, "n_heads %d outside 1..128", d->n_heads);
+  if (d->topk < 1) return fail(DSA_ERR_ARG, "topk must be >= 1");
+  if (!(d->softmax_scale > 0.f) || !std::isfinite(d->softmax_scale))
+    return fail(DSA_ERR_ARG, "softmax_scale must be positive and finite");
+  if (d->flags != 0) return fail(DSA_ERR_ARG, "attention flags must be 0");
+  return DSA_OK;
+}
+
+size_t attn_ws_bytes(const dsa_attn_desc* d) { return kAlign + align_up(static_cast<size_t>(d->n_q) * 4); }
+
+// status: device status header (first two words: bits, bad-index count); row_nt: n_q int32.
+dsa_status run_attn(const dsa_attn_desc* d, const void* q, const void* kv, const int32_t* idx, const int32_t* ks,
+                    void* out, float* lse, void* ws, size_t ws_bytes, cudaStream_t st, bool clear_status,
+                    uint32_t* status_override = nullptr) {
+  dsa_status s = check_attn_desc(d);
+  if (s != DSA_OK) return s;
+  if (d->n_q == 0) return DSA_OK;
+  if (!q || !kv || !idx || !ks || !out || !ws) return fail(DSA_ERR_ARG, "q, kv, idx, ks, out and ws must be non-NULL");
+  if (!aligned16(q) || !aligned16(kv) || !aligned16(out)) return fail(DSA_ERR_ARG, "q, kv and out must be 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(ws) % kAlign) return fail(DSA_ERR_ARG, "workspace must be 256-byte aligned");
+  if ((s = check_device()) != DSA_OK) return s;
+  const size_t need = attn_ws_bytes(d);
+  if (ws_bytes < need) return fail(DSA_ERR_WORKSPACE, "attention workspace too small: %zu < %zu bytes", ws_bytes, need);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  cudaError_t e;
+  if (clear_status && (e = cudaMemsetAsync(ws, 0, kAlign, st)) != cudaSuccess) return cuda_fail(e, "clear status");
+  uint32_t* status = status_override ? status_override : reinterpret_cast<uint32_t*>(base);
+  e = launch_sparse_attn(d->n_q, d->n_kv, d->n_heads, d->topk, d->softmax_scale, q, kv, idx, ks, out, lse, status,
+                         reinterpret_cast<int32_t*>(base + kAlign), st);
+  if (e != cudaSuccess) return cuda_fail(e, "sparse attention kernel");
+  return DSA_OK;
+}
+
+}  // namespace
+
+int device_sm_count() { return dev_info().sms; }
+
+}  // namespace dsa
+
+// ====================================================================== C ABI
+using namespace dsa;
+
+struct dsa_index_cache {
+  std::vector<uint8_t> types;
+  std::vector<int32_t> donors;
+  std::vector<int32_t*> buffers;
+  int32_t n_q = 0, topk = 0;
+};
+
+extern "C" {
+
+const char* dsa_status_string(dsa_status s) {
+  switch (s) {
+    case DSA_OK: return "DSA_OK";
+    case DSA_ERR_ARG: return "DSA_ERR_ARG";
+    case DSA_ERR_SHAPE: return "DSA_ERR_SHAPE";
+    case DSA_ERR_NO_DONOR: return "DSA_ERR_NO_DONOR";
+    case DSA_ERR_UNSUPPORTED: return "DSA_ERR_UNSUPPORTED";
+    case DSA_ERR_CUDA: return "DSA_ERR_CUDA";
+    case DSA_ERR_WORKSPACE: return "DSA_ERR_WORKSPACE";
+    case DSA_ERR_TIMEOUT: return "DSA_ERR_TIMEOUT";
+    case DSA_ERR_DEVICE: return "DSA_ERR_DEVICE";
+  }
+  return "DSA_ERR_UNKNOWN";
+}
+
+const char* dsa_last_error(void) { return g_err.c_str(); }
+
+dsa_status dsa_donor_table(int32_t n_layers, const uint8_t* types, int32_t* donors) {
+  if (!types || !donors || n_layers < 1) return fail(DSA_ERR_ARG, "donor table: NULL array or n_layers < 1");
+  int32_t last_full = -1;
+  for (int32_t l = 0; l < n_layers; ++l) {
+    if (types[l] == DSA_LAYER_FULL) {
+      last_full = l;
+      donors[l] = l;
+    } else if (types[l] == DSA_LAYER_SHARED) {
+      if (last_full < 0) return fail(DSA_ERR_NO_DONOR, "layer %d is shared but no full layer precedes it", l);
+      donors[l] = last_full;
+    } else {
+      return fail(DSA_ERR_ARG, "layer %d: indexer type %u is neither shared (0) nor full (1)", l, types[l]);
+    }
+  }
+  return DSA_OK;
+}
+
+dsa_status dsa_rope_table(double theta, int32_t rope_dim, int32_t n_pos, float* host_out) {
+  if (!host_out || rope_dim < 0 || (rope_dim & 1) || n_pos < 1 || !(theta > 0.0))
+    return fail(DSA_ERR_ARG, "rope table: bad theta/rope_dim/n_pos or NULL output");
+  const int half = rope_dim / 2;
+  std::vector<double> inv(half);
+  for (int i = 0; i < half; ++i) inv[i] = std::pow(theta, -2.0 * i / rope_dim);
+  for (int64_t p = 0; p < n_pos; ++p) {
+    float* row = host_out + p * rope_dim;
+    for (int i = 0; i < half; ++i) {
+      const double a = static_cast<double>(p) * inv[i];
+      row[2 * i] = static_cast<float>(std::cos(a));
+      row[2 * i + 1] = static_cast<float>(std::sin(a));
+    }
+  }
+  return DSA_OK;
+}
+
+dsa_status dsa_indexer_workspace_size(const dsa_indexer_desc* desc, size_t* bytes) {
+  dsa_status s = check_indexer_desc(desc);
+  if (s != DSA_OK) return s;
+  if (!bytes) return fail(DSA_ERR_ARG, "bytes is NULL");
+  const DevInfo di = dev_info();
+  *bytes = indexer_layout(desc, di.sms > 0 ? di.sms : 148).total;
+  return DSA_OK;
+}
+
+dsa_status dsa_indexer_topk(const dsa_indexer_desc* desc, const void* q_idx, const void* k_idx, const float* w,
+                            const int32_t* q_pos, const int32_t* k_pos, const int32_t* ks, const int32_t* ke,
+                            const float* rope_cs, int32_t rope_n_pos, int32_t* idx_out, float* score_out, void* ws,
+                            size_t ws_bytes, void* stream) {
+  return run_indexer(desc, q_idx, k_idx, w, q_pos, k_pos, ks, ke, rope_cs, rope_n_pos, idx_out, score_out, ws,
+                     ws_bytes, static_cast<cudaStream_t>(stream), true);
+}
+
+dsa_status dsa_sparse_attn_workspace_size(const dsa_attn_desc* desc, size_t* bytes) {
+  dsa_status s = check_attn_desc(desc);
+  if (s != DSA_OK) return s;
+  if (!bytes) return fail(DSA_ERR_ARG, "bytes is NULL");
+  *bytes = attn_ws_bytes(desc);
+  return DSA_OK;
+}
+
+dsa_status dsa_sparse_attn(const dsa_attn_desc* desc, const void* q, const void* kv, const int32_t* idx,
+                           const int32_t* ks, void* out, float* lse, void* ws, size_t ws_bytes, void* stream) {
+  return run_attn(desc, q, kv, idx, ks, out, lse, ws, ws_bytes, static_cast<cudaStream_t>(stream), true);
+}
+
+dsa_status dsa_index_cache_create(int32_t n_layers, const uint8_t* types, int32_t n_q, int32_t topk,
+                                  int32_t* const* idx_buffers, dsa_index_cache** cache_out) {
+  if (!cache_out) return fail(DSA_ERR_ARG, "cache_out is NULL");
+  *cache_out = nullptr;
+  if (!idx_buffers || n_q < 0 || topk < 1) return fail(DSA_ERR_ARG, "index cache: NULL buffers or bad n_q/topk");
+  std::vector<int32_t> donors(n_layers > 0 ? n_layers : 0);
+  dsa_status s = dsa_donor_table(n_layers, types, donors.data());
+  if (s != DSA_OK) return s;
+  for (int32_t l = 0; l < n_layers; ++l)
+    if (types[l] == DSA_LAYER_FULL && !idx_buffers[l])
+      return fail(DSA_ERR_ARG, "index cache: full layer %d has no index buffer", l);
+  auto* c = new (std::nothrow) dsa_index_cache;
+  if (!c) return fail(DSA_ERR_ARG, "index cache: out of host memory");
+  c->types.assign(types, types + n_layers);
+  c->donors = donors;
+  c->buffers.assign(idx_buffers, idx_buffers + n_layers);
+  c->n_q = n_q;
+  c->topk = topk;
+  *cache_out = c;
+  return DSA_OK;
+}
+
+dsa_status dsa_index_cache_donor(const dsa_index_cache* c, int32_t layer, int32_t* donor) {
+  if (!c || !donor) return fail(DSA_ERR_ARG, "index cache or donor is NULL");
+  if (layer < 0 || layer >= static_cast<int32_t>(c->donors.size()))
+    return fail(DSA_ERR_ARG, "layer %d outside [0, %zu)", layer, c->donors.size());
+  *donor = c->donors[layer];
+  return DSA_OK;
+}
+
+int32_t* dsa_index_cache_indices(const dsa_index_cache* c, int32_t layer) {
+  if (!c || layer < 0 || layer >= static_cast<int32_t>(c->donors.size())) {
+    fail(DSA_ERR_ARG, "index cache NULL or layer %d out of range", layer);
+    return nullptr;
+  }
+  return c->buffers[c->donors[layer]];
+}
+
+void dsa_index_cache_destroy(dsa_index_cache* c) { delete c; }
+
+dsa_status dsa_layers_workspace_size(const dsa_indexer_desc* idx_desc, const dsa_attn_desc* attn_desc, size_t* bytes) {
+  size_t a = 0, b = 0;
+  dsa_status s = dsa_indexer_workspace_size(idx_desc, &a);
+  if (s != DSA_OK) return s;
+  if ((s = dsa_sparse_attn_workspace_size(attn_desc, &b)) != DSA_OK) return s;
+  *bytes = a + b;
+  return DSA_OK;
+}
+
+dsa_status indexshare_layers_forward(const dsa_indexer_desc* idx_desc, const dsa_attn_desc* attn_desc,
+                                     int32_t n_layers, const uint8_t* indexer_types, const dsa_layer_io* io,
+                                     const int32_t* ks, const int32_t* ke, const int32_t* q_pos,
+                                     const int32_t* k_pos, const float* rope_cs, int32_t rope_n_pos,
+                                     dsa_index_cache* cache, void* ws, size_t ws_bytes, void* stream) {
+  dsa_status s = check_indexer_desc(idx_desc);
+  if (s != DSA_OK) return s;
+  if ((s = check_attn_desc(attn_desc)) != DSA_OK) return s;
+  if (!io || !cache || !indexer_types || !ws) return fail(DSA_ERR_ARG, "layer_io, cache, indexer_types and ws must be non-NULL");
+  if (n_layers != static_cast<int32_t>(cache->types.size()))
+    return fail(DSA_ERR_SHAPE, "n_layers %d differs from the cache's %zu", n_layers, cache->types.size());
+  for (int32_t l = 0; l < n_layers; ++l)
+    if (indexer_types[l] != cache->types[l])
+      return fail(DSA_ERR_SHAPE, "indexer_types[%d] differs from the array the cache was built with", l);
+  if (idx_desc->n_q != attn_desc->n_q || idx_desc->topk != attn_desc->topk || idx_desc->n_kv != attn_desc->n_kv)
+    return fail(DSA_ERR_SHAPE, "indexer and attention descriptors disagree on n_q, n_kv or topk");
+  if (cache->n_q != idx_desc->n_q || cache->topk != idx_desc->topk)
+    return fail(DSA_ERR_SHAPE, "cache built for n_q=%d topk=%d", cache->n_q, cache->topk);
+  size_t need = 0;
+  if ((s = dsa_layers_workspace_size(idx_desc, attn_desc, &need)) != DSA_OK) return s;
+  if (ws_bytes < need) return fail(DSA_ERR_WORKSPACE, "layer workspace too small: %zu < %zu bytes", ws_bytes, need);
+  for (int32_t l = 0; l < n_layers; ++l) {
+    if (!io[l].q || !io[l].kv || !io[l].out) return fail(DSA_ERR_ARG, "layer %d: q, kv and out must be non-NULL", l);
+    if (cache->types[l] == DSA_LAYER_FULL && (!io[l].q_idx || !io[l].k_idx || !io[l].w))
+      return fail(DSA_ERR_ARG, "full layer %d: q_idx, k_idx and w must be non-NULL", l);
+  }
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  size_t idx_ws = 0;
+  dsa_indexer_workspace_size(idx_desc, &idx_ws);
+  uint8_t* attn_ws = static_cast<uint8_t*>(ws) + idx_ws;
+  if ((s = check_device()) != DSA_OK) return s;
+  cudaError_t e;
+  if ((e = cudaMemsetAsync(ws, 0, kAlign, st)) != cudaSuccess) return cuda_fail(e, "clear status");
+  for (int32_t l = 0; l < n_layers; ++l) {
+    if (cache->types[l] == DSA_LAYER_FULL) {
+      s = run_indexer(idx_desc, io[l].q_idx, io[l].k_idx, io[l].w, q_pos, k_pos, ks, ke, rope_cs, rope_n_pos,
+                      cache->buffers[l], nullptr, ws, idx_ws, st, false);
+      if (s != DSA_OK) return s;
+    }
+    s = run_attn(attn_desc, io[l].q, io[l].kv, cache->buffers[cache->donors[l]], ks, io[l].out, io[l].lse, attn_ws,
+                 ws_bytes - idx_ws, st, false, static_cast<uint32_t*>(ws));
+    if (s != DSA_OK) return s;
+  }
+  return DSA_OK;
+}
+
+dsa_status dsa_workspace_status(const void* ws, void* stream, uint32_t* device_bits) {
+  if (!ws) return fail(DSA_ERR_ARG, "workspace is NULL");
+  WsHeader h{};
+  cudaError_t e = cudaMemcpyAsync(&h, ws, sizeof(h), cudaMemcpyDeviceToHost, static_cast<cudaStream_t>(stream));
+  if (e == cudaSuccess) e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "read workspace status");
+  if (device_bits) *device_bits = h.status;
+  if (h.status & DEV_ERR_TIMEOUT) return fail(DSA_ERR_TIMEOUT, "a device pipeline wait ran past its bound");
+  if (h.status) return fail(DSA_ERR_DEVICE, "device status 0x%x (%u bad indices)", h.status, h.bad_count);
+  return DSA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,400 @@
+// Lightning-indexer score contraction on tcgen05 with a fused streaming causal top-k.
+//
+//   s[t, j] = sum_h w[t, h] * max(0, q[t, h] . k[j])            (q, k already rotated)
+//
+// ("GLM-5.2 IndexShare" explainer, section 1: the indexer scores the prefix tokens of each
+// query and keeps the top-k positions; the weighted ReLU head sum with one shared key head
+// follows "GLM-5/5.1/5.2 DSA + LoRA enablement", indexer RoPE half-swap commit.)
+//
+// Tiling.  A work unit is (group of G consecutive query rows, chunk of the group's key
+// range).  The MMA puts 128 KEYS in M and the G*H_I (query, head) pairs of the group in
+// N (<= 256), so one key tile is one tcgen05.mma chain of d_I/16 instructions:
+//     S^T[key, (g, h)] = K_tile[key, :] . Q_group[(g, h), :]
+// A thread of the epilogue owns one key (one TMEM lane) and reduces the heads of every
+// query in registers, so the head sum and the ReLU/weight epilogue never leave the SM and
+// the score matrix is never written anywhere.
+//
+// Streaming top-k.  Per (row, chunk) the kernel keeps a candidate buffer of `cap` entries
+// (order-preserving score key, key index) in the workspace and a running threshold tau in
+// shared memory.  A score is appended only when it beats tau.  When a buffer could
+// overflow on the next tile the 128 epilogue threads cut it back to exactly its top-k by
+// (score desc, index asc) and raise tau to the k-th key.  Keys of a unit are visited in
+// increasing index order, so "beats tau" is a strict comparison.
+//
+// Warp roles (192 threads): warp 0 = TMA producer, warp 1 = MMA issuer (owns TMEM),
+// warps 2..5 = epilogue (TMEM lane quarters 2, 3, 0, 1).  Q is single-buffered per unit,
+// K tiles go through a STAGES-deep ring, S^T is double-buffered in TMEM.
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+#include "topk.cuh"
+
+namespace dsa {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kEpiThreads = 128;
+constexpr int kKeyTile = 128;
+constexpr int kMaxPer = 32;  // cap / kEpiThreads <= 32  (cap <= 4096)
+
+template <int HI, int DI, int G>
+struct Cfg {
+  static constexpr int N = G * HI;                       // MMA N: (query, head) pairs
+  static constexpr int KB = DI / 64;                     // 128-byte K blocks per row
+  static constexpr int Q_BYTES = N * DI * 2;
+  static constexpr int K_STAGE_BYTES = kKeyTile * DI * 2;
+  static constexpr int SMEM_BUDGET = 232448 - 4096;      // dynamic budget after static smem
+  static constexpr int STAGES_FIT = (SMEM_BUDGET - 1024 - Q_BYTES) / K_STAGE_BYTES;
+  static constexpr int STAGES = STAGES_FIT > 6 ? 6 : STAGES_FIT;
+  static constexpr int DYN_SMEM = 1024 + Q_BYTES + STAGES * K_STAGE_BYTES;
+  static constexpr uint32_t TMEM_COLS = (2 * N <= 32) ? 32 : (2 * N <= 64) ? 64 : (2 * N <= 128) ? 128 : (2 * N <= 256) ? 256 : 512;
+  static_assert(N % 32 == 0 && N >= 32 && N <= 256, "MMA N (epilogue reads 32 columns at a time)");
+  static_assert(STAGES >= 2, "shared memory");
+};
+
+struct Shared {
+  uint64_t k_full[8], k_empty[8];
+  uint64_t q_full, q_empty;
+  uint64_t t_full[2], t_empty[2];
+  uint32_t tmem_base;
+  uint32_t abort_flag;
+  uint32_t hist[256];
+  int bc[4];
+  int warp_off[4];
+  float w_s[256];
+  uint32_t tau[64];
+  int cnt[64];
+  int2 rr[64];
+  int epi_abort;
+};
+
+struct UnitInfo {
+  int group, chunk, kbeg, kend, n_tiles;
+};
+
+__device__ __forceinline__ UnitInfo unit_info(int u, int n_groups, int chunk_len, const int2* group_range) {
+  UnitInfo ui;
+  ui.chunk = u / n_groups;
+  ui.group = n_groups - 1 - (u - ui.chunk * n_groups);  // later (longer) groups first
+  const int2 gr = group_range[ui.group];
+  const long long b = static_cast<long long>(gr.x) + static_cast<long long>(ui.chunk) * chunk_len;
+  const long long e = min(static_cast<long long>(gr.y), b + chunk_len);
+  ui.kbeg = static_cast<int>(b);
+  ui.kend = static_cast<int>(e > b ? e : b);
+  ui.n_tiles = e > b ? static_cast<int>((e - b + kKeyTile - 1) / kKeyTile) : 0;
+  return ui;
+}
+
+// Cut the candidate buffer of one (row, chunk) back to its top-K.  Called by the 128
+// epilogue threads together.  Returns the new threshold key.
+__device__ uint32_t compact_buffer(uint32_t* keys, int32_t* idxs, int n, int K, int tid, Shared& sh) {
+  uint32_t rk[kMaxPer];
+  int32_t ri[kMaxPer];
+#pragma unroll
+  for (int i = 0; i < kMaxPer; ++i) {
+    const int e = tid + i * kEpiThreads;
+    rk[i] = e < n ? keys[e] : 0u;
+    ri[i] = e < n ? idxs[e] : 0;
+  }
+  auto sync = [] { named_bar_sync(1, kEpiThreads); };
+  auto fe = [&](auto&& f) {
+#pragma unroll
+    for (int i = 0; i < kMaxPer; ++i)
+      if (tid + i * kEpiThreads < n) f(rk[i], ri[i]);
+  };
+  uint32_t v, cut;
+  radix_threshold<kEpiThreads>(sync, fe, tid, K, sh.hist, sh.bc, v, cut);
+  int keep = 0;
+#pragma unroll
+  for (int i = 0; i < kMaxPer; ++i)
+    if (tid + i * kEpiThreads < n && topk_keep(rk[i], ri[i], v, cut)) ++keep;
+  // block exclusive scan of `keep` over the 128 threads
+  const int lane = tid & 31, wq = tid >> 5;
+  int x = keep;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
+  }
+  if (lane == 31) sh.warp_off[wq] = x;
+  sync();
+  int base = 0;
+  for (int wv = 0; wv < wq; ++wv) base += sh.warp_off[wv];
+  int pos = base + x - keep;
+#pragma unroll
+  for (int i = 0; i < kMaxPer; ++i) {
+    if (tid + i * kEpiThreads < n && topk_keep(rk[i], ri[i], v, cut)) {
+      keys[pos] = rk[i];
+      idxs[pos] = ri[i];
+      ++pos;
+    }
+  }
+  __threadfence_block();
+  sync();
+  return v;
+}
+
+template <int HI, int DI, int G>
+__global__ void __launch_bounds__(kThreads, 1)
+    indexer_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                   const float* __restrict__ w, int n_q, const int2* __restrict__ row_range,
+                   const int2* __restrict__ group_range, int n_groups, int n_chunks, int chunk_len, int cap, int topk,
+                   uint32_t* __restrict__ cand_key, int32_t* __restrict__ cand_idx, uint32_t* __restrict__ cand_cnt,
+                   uint32_t* status) {
+  using C = Cfg<HI, DI, G>;
+  constexpr int N = C::N, KB = C::KB, STAGES = C::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ Shared sh;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sK = smem + C::Q_BYTES;
+  const int warp = threadIdx.x >> 5;
+  const int n_units = n_groups * n_chunks;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&sh.k_full[s], 1);
+      mbar_init(&sh.k_empty[s], 1);
+    }
+    mbar_init(&sh.q_full, 1);
+    mbar_init(&sh.q_empty, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sh.t_full[b], 1);
+      mbar_init(&sh.t_empty[b], kEpiThreads);
+    }
+    sh.abort_flag = 0;
+    sh.epi_abort = 0;
+    fence_mbar_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 1) {
+    tmem_alloc(&sh.tmem_base, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sh.tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (elect_lane0()) {
+      tma_prefetch_desc(&tmap_q);
+      tma_prefetch_desc(&tmap_k);
+      uint32_t kstage = 0, q_uses = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        const UnitInfo ui = unit_info(u, n_groups, chunk_len, group_range);
+        if (ui.n_tiles == 0) continue;
+        if (q_uses > 0) ok = mbar_wait(&sh.q_empty, (q_uses - 1) & 1, &sh.abort_flag, status);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&sh.q_full, C::Q_BYTES);
+        for (int b = 0; b < KB; ++b) tma_load_2d(sQ + b * N * 128, &tmap_q, &sh.q_full, b * 64, ui.group * N);
+        ++q_uses;
+        for (int i = 0; i < ui.n_tiles; ++i, ++kstage) {
+          const int s = kstage % STAGES;
+          if (kstage >= STAGES) {
+            ok = mbar_wait(&sh.k_empty[s], ((kstage / STAGES) - 1) & 1, &sh.abort_flag, status);
+            if (!ok) break;
+          }
+          mbar_arrive_expect_tx(&sh.k_full[s], C::K_STAGE_BYTES);
+          uint8_t* dst = sK + s * C::K_STAGE_BYTES;
+          for (int b = 0; b < KB; ++b)
+            tma_load_2d(dst + b * kKeyTile * 128, &tmap_k, &sh.k_full[s], b * 64, ui.kbeg + i * kKeyTile);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (elect_lane0()) {
+      constexpr uint32_t idesc = idesc_bf16_f32(128, N, 0, 0);
+      uint32_t kstage = 0, q_uses = 0, tile = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        const UnitInfo ui = unit_info(u, n_groups, chunk_len, group_range);
+        if (ui.n_tiles == 0) continue;
+        ok = mbar_wait(&sh.q_full, q_uses & 1, &sh.abort_flag, status);
+        if (!ok) break;
+        ++q_uses;
+        for (int i = 0; i < ui.n_tiles; ++i, ++kstage, ++tile) {
+          const int s = kstage % STAGES;
+          const int buf = tile & 1;
+          ok = mbar_wait(&sh.k_full[s], (kstage / STAGES) & 1, &sh.abort_flag, status);
+          if (ok && tile >= 2) ok = mbar_wait(&sh.t_empty[buf], ((tile >> 1) - 1) & 1, &sh.abort_flag, status);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sK + s * C::K_STAGE_BYTES);
+          const uint32_t b0 = smem_u32(sQ);
+#pragma unroll
+          for (int k = 0; k < DI / 16; ++k) {
+            const int kb = k >> 2, sub = k & 3;
+            const uint64_t ad = sdesc_sw128(a0 + kb * kKeyTile * 128 + sub * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(b0 + kb * N * 128 + sub * 32, 16, 1024);
+            umma_bf16(tmem + buf * N, ad, bd, idesc, k > 0 ? 1u : 0u);
+          }
+          umma_commit(&sh.k_empty[s]);
+          umma_commit(&sh.t_full[buf]);
+        }
+        if (ok) umma_commit(&sh.q_empty);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------------ epilogue
+    const int tid = threadIdx.x - 64;          // 0..127
+    const int quarter = warp & 3;              // TMEM lane quarter this warp may access
+    const int lane = threadIdx.x & 31;
+    const int row = quarter * 32 + lane;       // key within the tile
+    const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
+    // A failed (timed-out) wait is published through sh.epi_abort, written only before
+    // the first named barrier of a tile and read only between that barrier and the
+    // second one, so all four epilogue warps leave the loops at the same point.
+    uint32_t tile = 0;
+    bool stop = false;
+    for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
+      const UnitInfo ui = unit_info(u, n_groups, chunk_len, group_range);
+      const int t0 = ui.group * G;
+      // per-unit state
+      for (int i = tid; i < N; i += kEpiThreads) {
+        const int t = t0 + i / HI;
+        sh.w_s[i] = t < n_q ? __ldg(w + static_cast<size_t>(t) * HI + (i % HI)) : 0.f;
+      }
+      if (tid < G) {
+        const int t = t0 + tid;
+        sh.rr[tid] = t < n_q ? row_range[t] : make_int2(0, 0);
+        sh.tau[tid] = 0u;
+        sh.cnt[tid] = 0;
+      }
+      named_bar_sync(1, kEpiThreads);
+      for (int i = 0; i < ui.n_tiles; ++i, ++tile) {
+        const int buf = tile & 1;
+        bool ok = mbar_wait(&sh.t_full[buf], (tile >> 1) & 1, &sh.abort_flag, status);
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok) {
+          tc_fence_after();
+          float acc[G];
+#pragma unroll
+          for (int g = 0; g < G; ++g) acc[g] = 0.f;
+#pragma unroll
+          for (int c0 = 0; c0 < N; c0 += 32) {
+            uint32_t v[32];
+            tmem_ld32(tmem + t_lane + buf * N + c0, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {
+              const float4 wv = *reinterpret_cast<const float4*>(&sh.w_s[c0 + j]);
+              acc[(c0 + j) / HI] = fmaf(wv.x, fmaxf(__uint_as_float(v[j]), 0.f), acc[(c0 + j) / HI]);
+              acc[(c0 + j + 1) / HI] = fmaf(wv.y, fmaxf(__uint_as_float(v[j + 1]), 0.f), acc[(c0 + j + 1) / HI]);
+              acc[(c0 + j + 2) / HI] = fmaf(wv.z, fmaxf(__uint_as_float(v[j + 2]), 0.f), acc[(c0 + j + 2) / HI]);
+              acc[(c0 + j + 3) / HI] = fmaf(wv.w, fmaxf(__uint_as_float(v[j + 3]), 0.f), acc[(c0 + j + 3) / HI]);
+            }
+          }
+          tc_fence_before();
+          mbar_arrive(&sh.t_empty[buf]);
+          // append candidates that beat the running threshold
+          const int j = ui.kbeg + i * kKeyTile + row;
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            const int2 rr = sh.rr[g];
+            const uint32_t key = float_key(acc[g]);
+            const bool pass = j >= rr.x && j < rr.y && j < ui.kend && key > sh.tau[g];
+            const uint32_t m = __ballot_sync(0xffffffffu, pass);
+            if (m) {
+              int base = 0;
+              if (lane == 0) base = atomicAdd(&sh.cnt[g], __popc(m));
+              base = __shfl_sync(0xffffffffu, base, 0);
+              if (pass) {
+                const int pos = base + __popc(m & ((1u << lane) - 1u));
+                if (pos < cap) {
+                  const size_t off = (static_cast<size_t>(t0 + g) * n_chunks + ui.chunk) * cap + pos;
+                  cand_key[off] = key;
+                  cand_idx[off] = j;
+                }
+              }
+            }
+          }
+        } else if (lane == 0) {
+          sh.epi_abort = 1;
+        }
+        named_bar_sync(1, kEpiThreads);
+        stop = sh.epi_abort != 0;
+        if (!stop) {
+          // cut back buffers that could overflow on the next tile
+#pragma unroll 1
+          for (int g = 0; g < G; ++g) {
+            const int n = sh.cnt[g];
+            if (n > cap - kKeyTile) {
+              const size_t off = (static_cast<size_t>(t0 + g) * n_chunks + ui.chunk) * cap;
+              __threadfence_block();
+              const uint32_t v = compact_buffer(cand_key + off, cand_idx + off, n, topk, tid, sh);
+              if (tid == 0) {
+                sh.tau[g] = v;
+                sh.cnt[g] = topk;
+              }
+              named_bar_sync(1, kEpiThreads);
+            }
+          }
+        }
+        named_bar_sync(1, kEpiThreads);
+        if (stop) break;
+      }
+      if (stop) break;
+      if (tid < G && t0 + tid < n_q)
+        cand_cnt[static_cast<size_t>(t0 + tid) * n_chunks + ui.chunk] = static_cast<uint32_t>(min(sh.cnt[tid], cap));
+      named_bar_sync(1, kEpiThreads);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+template <int HI, int DI, int G>
+cudaError_t launch_t(const IndexerPlan& p, const CUtensorMap& tq, const CUtensorMap& tk, const float* w, int n_q,
+                     const int2* row_range, const int2* group_range, uint32_t* ck, int32_t* ci, uint32_t* cc,
+                     uint32_t* status, cudaStream_t st) {
+  using C = Cfg<HI, DI, G>;
+  auto kern = indexer_kernel<HI, DI, G>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::DYN_SMEM);
+  if (e != cudaSuccess) return e;
+  kern<<<p.grid, kThreads, C::DYN_SMEM, st>>>(tq, tk, w, n_q, row_range, group_range, p.n_groups, p.n_chunks,
+                                             p.chunk, p.cap, p.topk, ck, ci, cc, status);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+
+cudaError_t launch_indexer(const IndexerPlan& p, const CUtensorMap& tq, const CUtensorMap& tk, const float* w, int n_q,
+                           const int2* row_range, const int2* group_range, uint32_t* ck, int32_t* ci, uint32_t* cc,
+                           uint32_t* status, cudaStream_t st) {
+  if (p.n_groups * p.n_chunks == 0) return cudaSuccess;
+#define DSA_IDX_CASE(HI_, DI_, G_)                                                                      \
+  if (p.n_heads == HI_ && p.head_dim == DI_ && p.group == G_)                                           \
+    return launch_t<HI_, DI_, G_>(p, tq, tk, w, n_q, row_range, group_range, ck, ci, cc, status, st);
+  DSA_IDX_CASE(4, 64, 64)
+  DSA_IDX_CASE(8, 64, 32)
+  DSA_IDX_CASE(16, 64, 16)
+  DSA_IDX_CASE(32, 64, 8)
+  DSA_IDX_CASE(64, 64, 4)
+  DSA_IDX_CASE(4, 128, 64)
+  DSA_IDX_CASE(8, 128, 32)
+  DSA_IDX_CASE(16, 128, 16)
+  DSA_IDX_CASE(32, 128, 8)
+  DSA_IDX_CASE(64, 128, 4)
+  DSA_IDX_CASE(4, 64, 8)
+  DSA_IDX_CASE(8, 64, 4)
+  DSA_IDX_CASE(16, 64, 2)
+  DSA_IDX_CASE(32, 64, 1)
+  DSA_IDX_CASE(64, 64, 1)
+  DSA_IDX_CASE(4, 128, 8)
+  DSA_IDX_CASE(8, 128, 4)
+  DSA_IDX_CASE(16, 128, 2)
+  DSA_IDX_CASE(32, 128, 1)
+  DSA_IDX_CASE(64, 128, 1)
+#undef DSA_IDX_CASE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace dsa

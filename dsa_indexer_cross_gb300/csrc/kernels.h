@@ -1,0 +1,57 @@
+// Internal launch interface between the C-ABI layer (api.cu) and the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace dsa {
+
+// Layout of the 256-byte header at the start of every workspace.
+struct WsHeader {
+  uint32_t status;       // DEV_ERR_* bits
+  uint32_t bad_count;    // number of out-of-range indices met
+  uint32_t pad[62];
+};
+static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
+
+// ---------------------------------------------------------------------------- RoPE pre-pass
+// out[row] = in[row] with its last `rope` dims rotated at position pos[row / rows_per_pos].
+cudaError_t launch_rope_rows(const void* in, void* out, const int32_t* pos, int64_t n_rows, int rows_per_pos, int d,
+                             int rope, const float* cs, int n_pos, uint32_t* status, cudaStream_t st);
+
+// ---------------------------------------------------------------------------- indexer
+struct IndexerPlan {
+  int n_heads, head_dim, group;      // group = query rows sharing one key stream (G)
+  int n_groups, n_chunks, chunk;     // key chunking of every group's range
+  int cap;                           // candidate capacity per (row, chunk), multiple of 128
+  int grid;                          // persistent CTAs
+  int topk;
+};
+
+// Fills row_range[t] = (ks, ke) when valid, else (0, 0) and flags; group_range[g] = union.
+cudaError_t launch_ranges(const int32_t* ks, const int32_t* ke, int n_q, int group, int n_kv, int max_len,
+                          int2* row_range, int2* group_range, uint32_t* status, cudaStream_t st);
+
+// Scores + streaming top-k candidates.  tmap_q covers rotated q as [(n_q*H_I) x d_I] bf16,
+// tmap_k covers rotated k as [n_kv x d_I] bf16, both 128-byte swizzled, boxes {64, N} and
+// {64, 128}.
+cudaError_t launch_indexer(const IndexerPlan& p, const CUtensorMap& tmap_q, const CUtensorMap& tmap_k, const float* w,
+                           int n_q, const int2* row_range, const int2* group_range, uint32_t* cand_key,
+                           int32_t* cand_idx, uint32_t* cand_cnt, uint32_t* status, cudaStream_t st);
+
+// Exact top-k of every row from its candidates; writes offsets (ascending) and -1 padding.
+cudaError_t launch_select(int n_q, int n_chunks, int cap, int topk, const int2* row_range, const uint32_t* cand_key,
+                          const int32_t* cand_idx, const uint32_t* cand_cnt, int32_t* idx_out, float* score_out,
+                          uint32_t* status, cudaStream_t st);
+
+// ---------------------------------------------------------------------------- sparse attention
+// row_nt: n_q int32 of workspace (tiles of 64 index slots to visit per row).
+cudaError_t launch_sparse_attn(int n_q, int n_kv, int n_heads, int topk, float scale, const void* q, const void* kv,
+                               const int32_t* idx, const int32_t* ks, void* out, float* lse, uint32_t* status,
+                               int32_t* row_nt, cudaStream_t st);
+
+int device_sm_count();
+
+}  // namespace dsa

@@ -1,0 +1,163 @@
+// RoPE pre-pass of the index heads and the per-row / per-group key-range plan.
+//
+// Index RoPE rotates the LAST `rope` dims of every index head ("GLM-5/5.1/5.2 DSA + LoRA
+// enablement", indexer RoPE half-swap commit), pairing dim (d - r + i) with dim
+// (d - r/2 + i).  cos/sin come from a float32 table evaluated in float64 on the host; the
+// rotation runs in float32 and is rounded to bf16 (round-to-nearest-even), the precision
+// the tensor-core contraction consumes.
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace dsa {
+namespace {
+
+__device__ __forceinline__ float bf_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+__device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
+  const __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&p);
+}
+
+// Vector path: (d - rope) % 8 == 0 and (rope / 2) % 8 == 0.  One thread per unit of 8
+// copied elements or of 8 rotated pairs.
+__global__ void __launch_bounds__(256) rope_rows_vec(const uint16_t* __restrict__ in, uint16_t* __restrict__ out,
+                                                     const int32_t* __restrict__ pos, int64_t n_rows,
+                                                     int rows_per_pos, int d, int rope, const float* __restrict__ cs,
+                                                     int n_pos, uint32_t* status) {
+  const int copy_units = (d - rope) >> 3;
+  const int half = rope >> 1;
+  const int units = copy_units + (half >> 3);
+  const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (gid >= n_rows * units) return;
+  const int64_t row = gid / units;
+  const int u = static_cast<int>(gid - row * units);
+  const uint16_t* src = in + row * d;
+  uint16_t* dst = out + row * d;
+  if (u < copy_units) {
+    *reinterpret_cast<uint4*>(dst + u * 8) = __ldg(reinterpret_cast<const uint4*>(src + u * 8));
+    return;
+  }
+  const int i0 = (u - copy_units) * 8;
+  const uint4 a = __ldg(reinterpret_cast<const uint4*>(src + (d - rope) + i0));
+  const uint4 b = __ldg(reinterpret_cast<const uint4*>(src + (d - half) + i0));
+  const int p = __ldg(pos + row / rows_per_pos);
+  if (p < 0 || p >= n_pos) {
+    atomicOr(status, DEV_ERR_BAD_INDEX);
+    *reinterpret_cast<uint4*>(dst + (d - rope) + i0) = a;
+    *reinterpret_cast<uint4*>(dst + (d - half) + i0) = b;
+    return;
+  }
+  const float4* t = reinterpret_cast<const float4*>(cs + (static_cast<int64_t>(p) * half + i0) * 2);
+  float c[8], s[8];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float4 v = __ldg(t + q);
+    c[2 * q] = v.x;
+    s[2 * q] = v.y;
+    c[2 * q + 1] = v.z;
+    s[2 * q + 1] = v.w;
+  }
+  const uint32_t av[4] = {a.x, a.y, a.z, a.w};
+  const uint32_t bv[4] = {b.x, b.y, b.z, b.w};
+  uint32_t ya[4], yb[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float x1l = bf_lo(av[q]), x1h = bf_hi(av[q]);
+    const float x2l = bf_lo(bv[q]), x2h = bf_hi(bv[q]);
+    const float cl = c[2 * q], sl = s[2 * q], ch = c[2 * q + 1], sh = s[2 * q + 1];
+    ya[q] = pack_bf2(x1l * cl - x2l * sl, x1h * ch - x2h * sh);
+    yb[q] = pack_bf2(x2l * cl + x1l * sl, x2h * ch + x1h * sh);
+  }
+  *reinterpret_cast<uint4*>(dst + (d - rope) + i0) = make_uint4(ya[0], ya[1], ya[2], ya[3]);
+  *reinterpret_cast<uint4*>(dst + (d - half) + i0) = make_uint4(yb[0], yb[1], yb[2], yb[3]);
+}
+
+// Scalar path for any even rope: one thread per element of the first d - r/2 dims.
+__global__ void __launch_bounds__(256) rope_rows_scalar(const uint16_t* __restrict__ in, uint16_t* __restrict__ out,
+                                                        const int32_t* __restrict__ pos, int64_t n_rows,
+                                                        int rows_per_pos, int d, int rope,
+                                                        const float* __restrict__ cs, int n_pos, uint32_t* status) {
+  const int half = rope >> 1;
+  const int per_row = d - half;
+  const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (gid >= n_rows * per_row) return;
+  const int64_t row = gid / per_row;
+  const int e = static_cast<int>(gid - row * per_row);
+  const __nv_bfloat16* src = reinterpret_cast<const __nv_bfloat16*>(in) + row * d;
+  __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(out) + row * d;
+  if (e < d - rope) {
+    dst[e] = src[e];
+    return;
+  }
+  const int i = e - (d - rope);
+  const float x1 = __bfloat162float(src[d - rope + i]);
+  const float x2 = __bfloat162float(src[d - half + i]);
+  const int p = pos[row / rows_per_pos];
+  if (p < 0 || p >= n_pos) {
+    atomicOr(status, DEV_ERR_BAD_INDEX);
+    dst[d - rope + i] = src[d - rope + i];
+    dst[d - half + i] = src[d - half + i];
+    return;
+  }
+  const float c = cs[(static_cast<int64_t>(p) * half + i) * 2];
+  const float s = cs[(static_cast<int64_t>(p) * half + i) * 2 + 1];
+  dst[d - rope + i] = __float2bfloat16_rn(x1 * c - x2 * s);
+  dst[d - half + i] = __float2bfloat16_rn(x2 * c + x1 * s);
+}
+
+__global__ void __launch_bounds__(256) ranges_kernel(const int32_t* __restrict__ ks, const int32_t* __restrict__ ke,
+                                                     int n_q, int group, int n_kv, int max_len, int2* row_range,
+                                                     int2* group_range, uint32_t* status) {
+  const int g = blockIdx.x * blockDim.x + threadIdx.x;
+  const int n_groups = (n_q + group - 1) / group;
+  if (g >= n_groups) return;
+  int lo = 0x7FFFFFFF, hi = 0;
+  for (int t = g * group; t < min(n_q, g * group + group); ++t) {
+    const int a = ks[t], b = ke[t];
+    int2 r = make_int2(0, 0);
+    if (a < 0 || b < a || b > n_kv || b - a > max_len) {
+      atomicOr(status, DEV_ERR_RANGE);
+    } else if (b > a) {
+      r = make_int2(a, b);
+      lo = min(lo, a);
+      hi = max(hi, b);
+    }
+    row_range[t] = r;
+  }
+  group_range[g] = lo < hi ? make_int2(lo, hi) : make_int2(0, 0);
+}
+
+}  // namespace
+
+cudaError_t launch_rope_rows(const void* in, void* out, const int32_t* pos, int64_t n_rows, int rows_per_pos, int d,
+                             int rope, const float* cs, int n_pos, uint32_t* status, cudaStream_t st) {
+  if (n_rows <= 0) return cudaSuccess;
+  const int half = rope / 2;
+  if ((d - rope) % 8 == 0 && half % 8 == 0) {
+    const int64_t total = n_rows * ((d - rope) / 8 + half / 8);
+    const int64_t blocks = (total + 255) / 256;
+    rope_rows_vec<<<static_cast<unsigned>(blocks), 256, 0, st>>>(static_cast<const uint16_t*>(in),
+                                                                 static_cast<uint16_t*>(out), pos, n_rows,
+                                                                 rows_per_pos, d, rope, cs, n_pos, status);
+  } else {
+    const int64_t total = n_rows * (d - half);
+    const int64_t blocks = (total + 255) / 256;
+    rope_rows_scalar<<<static_cast<unsigned>(blocks), 256, 0, st>>>(static_cast<const uint16_t*>(in),
+                                                                    static_cast<uint16_t*>(out), pos, n_rows,
+                                                                    rows_per_pos, d, rope, cs, n_pos, status);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ranges(const int32_t* ks, const int32_t* ke, int n_q, int group, int n_kv, int max_len,
+                          int2* row_range, int2* group_range, uint32_t* status, cudaStream_t st) {
+  const int n_groups = (n_q + group - 1) / group;
+  if (n_groups <= 0) return cudaSuccess;
+  ranges_kernel<<<(n_groups + 255) / 256, 256, 0, st>>>(ks, ke, n_q, group, n_kv, max_len, row_range, group_range,
+                                                        status);
+  return cudaGetLastError();
+}
+
+}  // namespace dsa

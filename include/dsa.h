@@ -1,0 +1,239 @@
+/*
+ * dsa.h -- C ABI of libdsa: the DeepSeek Sparse Attention lightning indexer with a fused
+ * causal top-k, GLM-5.2 cross-layer IndexShare, and MLA-absorbed sparse attention, for
+ * one NVIDIA GB300 GPU (sm_103a).
+ *
+ * What the operations compute is defined on three public pages:
+ *   [MT] "add glm5.2 indexshare" (MaxText pull request #4832), Description and Code Review;
+ *   [MB] "GLM-5/5.1/5.2 DSA + LoRA enablement" (Megatron-Bridge pull request #15), the
+ *        commits on the indexer RoPE half swap, on capping top-k at the sequence length,
+ *        on cross-layer top-k sharing and on the per-query key ranges (cu_seqlens
+ *        starts/ends) of the indexer;
+ *   [EX] "GLM-5.2 IndexShare" (explainer), sections 1-2, "Layer execution pattern",
+ *        "Public config evidence", "What is actually shared?".
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Device pointers point to GPU global memory owned by the caller.  The library never
+ *    allocates device memory: every call that needs scratch space takes a workspace
+ *    (`ws`, `ws_bytes`) whose size the matching *_workspace_size query returns.  A
+ *    workspace must be 256-byte aligned and must not be used by two calls that can run
+ *    at the same time.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls only enqueue
+ *    work and return; results are ready when the stream reaches them.
+ *  - Arrays are dense and row-major ("[a][b]" = b fastest).  bf16 tensors must be
+ *    16-byte aligned (they are read by the Tensor Memory Accelerator or by 16-byte
+ *    vector loads).
+ *  - Every function returns a dsa_status and never throws or aborts.  Argument and shape
+ *    errors are detected on the host before anything is enqueued; the reason is then
+ *    available from dsa_last_error() on the calling thread.
+ *  - Faults found on the device (an index outside its range, a pipeline wait that ran
+ *    past its 2 s bound) are recorded in the first word of the workspace and read back
+ *    with dsa_workspace_status().  No kernel traps.
+ */
+#ifndef DSA_H_
+#define DSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum dsa_status {
+  DSA_OK = 0,
+  DSA_ERR_ARG = 1,         /* a NULL or misaligned pointer, or a value out of range        */
+  DSA_ERR_SHAPE = 2,       /* sizes that are inconsistent with each other                  */
+  DSA_ERR_NO_DONOR = 3,    /* a shared layer precedes every full layer                     */
+  DSA_ERR_UNSUPPORTED = 4, /* a valid size this build has no kernel for, or no sm_10x GPU  */
+  DSA_ERR_CUDA = 5,        /* a CUDA runtime call failed (message in dsa_last_error)       */
+  DSA_ERR_WORKSPACE = 6,   /* ws_bytes smaller than the *_workspace_size query             */
+  DSA_ERR_TIMEOUT = 7,     /* a device pipeline wait ran past its bound                    */
+  DSA_ERR_DEVICE = 8       /* the device counted out-of-range indices or a buffer overflow */
+} dsa_status;
+
+/* Human-readable name of a status code (static storage). */
+const char* dsa_status_string(dsa_status s);
+
+/* Message describing the last error returned on the calling thread ("" if none). */
+const char* dsa_last_error(void);
+
+/* ------------------------------------------------------------------ layer schedule -- */
+
+/* Values of an indexer_types array.  [EX] "Public config evidence": the released config
+ * lists one of "full" / "shared" per layer; [MT] Description: full layers run the
+ * lightning indexer, shared layers reuse the donor full layer's top-k indices. */
+#define DSA_LAYER_SHARED 0u
+#define DSA_LAYER_FULL 1u
+
+/* Donor of every layer: donors[l] = l for a full layer, else the nearest preceding full
+ * layer ([EX] "Layer execution pattern"; [MT] Code Review: shared layers 5, 6, 7 reuse
+ * layer 4).  indexer_types and donors are host arrays of n_layers entries.
+ * Errors: DSA_ERR_ARG (NULL, n_layers < 1, a value other than 0/1), DSA_ERR_NO_DONOR
+ * (a shared layer before the first full layer -- [MB] build-time stage assert). */
+dsa_status dsa_donor_table(int32_t n_layers, const uint8_t* indexer_types, int32_t* donors);
+
+/* ------------------------------------------------------------------ index RoPE ------- */
+
+/* Fill the host table rope_cs[p][i] = {cos(p * f_i), sin(p * f_i)} (float32, evaluated in
+ * float64) with f_i = theta^(-2i/rope_dim), for p in [0, n_pos), i in [0, rope_dim/2).
+ * The indexer rotates the LAST rope_dim dims of each index head with this table, pairing
+ * dim (d - r + i) with dim (d - r/2 + i) ([MB] RoPE half-swap commit: rotary dims sit in
+ * the last qk_pos_emb_head_dim of each index head).  host_out holds n_pos * rope_dim
+ * floats, caller-owned.  Errors: DSA_ERR_ARG (NULL, odd or negative rope_dim, n_pos < 1,
+ * theta <= 0). */
+dsa_status dsa_rope_table(double theta, int32_t rope_dim, int32_t n_pos, float* host_out);
+
+/* ------------------------------------------------------------------ indexer + top-k -- */
+
+/* Flags of dsa_indexer_desc. */
+#define DSA_IDX_ROPE_Q (1u << 0)           /* rotate q_idx before scoring                  */
+#define DSA_IDX_ROPE_K (1u << 1)           /* rotate k_idx before scoring (clear when the  */
+                                           /*  caller keeps an already-rotated key cache)  */
+#define DSA_IDX_INDEPENDENT_ROWS (1u << 2) /* rows do not share key ranges (batched decode:*/
+                                           /*  each row is its own sequence)               */
+
+typedef struct dsa_indexer_desc {
+  int32_t n_q;       /* query rows                                                       */
+  int32_t n_kv;      /* key rows in k_idx                                                */
+  int32_t n_heads;   /* index heads H_I: 4, 8, 16, 32 or 64                              */
+  int32_t head_dim;  /* index head dim d_I: 64 or 128                                    */
+  int32_t rope_dim;  /* RoPE dims r at the end of each head: even, 0 <= r <= d_I         */
+  int32_t topk;      /* index_topk k: 1 .. 2048                                          */
+  int32_t max_len;   /* an upper bound on every ke_t - ks_t (0 < max_len <= n_kv)        */
+  uint32_t flags;    /* DSA_IDX_*                                                        */
+} dsa_indexer_desc;
+
+/* Workspace bytes dsa_indexer_topk needs for this descriptor on the current device. */
+dsa_status dsa_indexer_workspace_size(const dsa_indexer_desc* desc, size_t* bytes);
+
+/* Lightning indexer with a fused streaming causal top-k ([EX] section 1: score the prefix
+ * tokens of every query and keep the top-k positions; spec formula):
+ *
+ *   s[t, j] = sum_h w[t, h] * max(0, rope(q_idx[t, h]) . rope(k_idx[j]))   j in [ks_t, ke_t)
+ *
+ * and idx_out[t] = the offsets j - ks_t of the min(topk, ke_t - ks_t) largest s[t, .]
+ * (ties to the lower j), sorted ascending, then -1 up to width topk ([MB] commit capping
+ * top-k at the sequence length and padding with -1).  One key head is shared by all index
+ * heads ([MB] one wk / k_norm per index head dim; weights_proj is a per-head scalar).
+ * The T x L score matrix is never written to memory: candidates above a running
+ * per-row threshold are kept in the workspace and cut back to k as they accumulate.
+ *
+ *   q_idx  bf16  [n_q][n_heads][head_dim]     k_idx bf16 [n_kv][head_dim]
+ *   w      f32   [n_q][n_heads]               q_pos int32 [n_q], k_pos int32 [n_kv]
+ *   ks, ke int32 [n_q]  key row range of row t: 0 <= ks_t <= ke_t <= n_kv,
+ *                       ke_t - ks_t <= max_len
+ *   rope_cs f32  [rope_n_pos][rope_dim/2][2]  table from dsa_rope_table (device copy);
+ *                may be NULL when neither ROPE flag is set or rope_dim == 0.  Positions
+ *                must lie in [0, rope_n_pos).
+ *   idx_out   int32 [n_q][topk]   (output)
+ *   score_out f32   [n_q][topk]   (optional output, NULL to skip): s of each selected key,
+ *                                  -inf on padding.
+ * q_pos / k_pos may be NULL when the matching ROPE flag is clear.
+ * Errors: DSA_ERR_ARG, DSA_ERR_UNSUPPORTED (n_heads / head_dim / topk outside the lists
+ * above), DSA_ERR_WORKSPACE, DSA_ERR_CUDA.  Device-side: a position outside the table,
+ * or a key range outside [0, n_kv) or longer than max_len, sets DSA_ERR_DEVICE in the
+ * workspace status. */
+dsa_status dsa_indexer_topk(const dsa_indexer_desc* desc, const void* q_idx, const void* k_idx, const float* w,
+                            const int32_t* q_pos, const int32_t* k_pos, const int32_t* ks, const int32_t* ke,
+                            const float* rope_cs, int32_t rope_n_pos, int32_t* idx_out, float* score_out, void* ws,
+                            size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------ sparse attention - */
+
+typedef struct dsa_attn_desc {
+  int32_t n_q;          /* query rows                                                    */
+  int32_t n_kv;         /* latent rows in kv                                             */
+  int32_t n_heads;      /* attention heads H: 1 .. 128                                   */
+  int32_t d_qk;         /* 576 = 512 latent + 64 rope ([MB] qk_rope_head_dim commit)     */
+  int32_t d_v;          /* 512: V is the first d_v dims of each latent row               */
+  int32_t topk;         /* width of each idx row                                         */
+  float softmax_scale;  /* tau, e.g. 1/sqrt(576)                                         */
+  uint32_t flags;       /* reserved, 0                                                   */
+} dsa_attn_desc;
+
+dsa_status dsa_sparse_attn_workspace_size(const dsa_attn_desc* desc, size_t* bytes);
+
+/* MLA-absorbed sparse attention over the selected latent rows ([EX] section 1: the main
+ * attention runs only on the selected positions; "What is actually shared?": every layer
+ * computes its own attention):
+ *
+ *   o[t, h]   = sum_{j in I_t} softmax_j(tau * q[t, h] . kv[ks_t + j]) * kv[ks_t + j, :d_v]
+ *   lse[t, h] = log sum_{j in I_t} exp(tau * q[t, h] . kv[ks_t + j])
+ *
+ * with I_t the entries of idx[t] that are >= 0.  All heads of a token read the same rows.
+ *   q   bf16 [n_q][n_heads][d_qk]     kv  bf16 [n_kv][d_qk]
+ *   idx int32 [n_q][topk]  offsets relative to ks_t, -1 = unused slot
+ *   ks  int32 [n_q]
+ *   out bf16 [n_q][n_heads][d_v]      (output)
+ *   lse f32  [n_q][n_heads]           (optional output, NULL to skip)
+ * A row with no valid index gives o = 0 and lse = -inf.  An index with ks_t + j outside
+ * [0, n_kv) is skipped and counted (DSA_ERR_DEVICE in the workspace status).
+ * Errors: DSA_ERR_ARG, DSA_ERR_UNSUPPORTED (d_qk != 576 or d_v != 512, n_heads > 128),
+ * DSA_ERR_WORKSPACE, DSA_ERR_CUDA. */
+dsa_status dsa_sparse_attn(const dsa_attn_desc* desc, const void* q, const void* kv, const int32_t* idx,
+                           const int32_t* ks, void* out, float* lse, void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------ index cache ------ */
+
+/* Host object mapping every layer to the device buffer holding its donor's indices
+ * ([EX] "Implementation checklist": cache the top-k of full layers, shared layers read
+ * the preceding full layer's; [MB] anchors publish top-k, skip layers reuse it).
+ * idx_buffers has n_layers entries; entry l must be a device buffer of n_q * topk int32
+ * for every full layer l and is ignored (may be NULL) for shared layers.  The cache
+ * stores the pointers, not the memory: the caller keeps the buffers alive.
+ * Errors: DSA_ERR_ARG, DSA_ERR_NO_DONOR. */
+typedef struct dsa_index_cache dsa_index_cache;
+
+dsa_status dsa_index_cache_create(int32_t n_layers, const uint8_t* indexer_types, int32_t n_q, int32_t topk,
+                                  int32_t* const* idx_buffers, dsa_index_cache** cache_out);
+/* Donor layer of `layer`.  Errors: DSA_ERR_ARG (NULL, layer out of range). */
+dsa_status dsa_index_cache_donor(const dsa_index_cache* cache, int32_t layer, int32_t* donor);
+/* Device buffer holding the indices `layer` attends with (its donor's), NULL on error. */
+int32_t* dsa_index_cache_indices(const dsa_index_cache* cache, int32_t layer);
+void dsa_index_cache_destroy(dsa_index_cache* cache);
+
+/* ------------------------------------------------------------------ layer loop ------- */
+
+/* Per-layer tensors.  q_idx, k_idx and w are read on full layers only (NULL allowed on
+ * shared layers); q, kv, out (and lse, optional) on every layer. */
+typedef struct dsa_layer_io {
+  const void* q_idx;
+  const void* k_idx;
+  const float* w;
+  const void* q;
+  const void* kv;
+  void* out;
+  float* lse;
+} dsa_layer_io;
+
+dsa_status dsa_layers_workspace_size(const dsa_indexer_desc* idx_desc, const dsa_attn_desc* attn_desc, size_t* bytes);
+
+/* The IndexShare layer loop ([EX] section 2 and "Layer execution pattern"; [MT] Key
+ * Changes: full layers compute, shared layers pass the cached state through).  For each
+ * layer l in order: if indexer_types[l] is full, run dsa_indexer_topk into the cache
+ * buffer of l; then run dsa_sparse_attn of layer l with the buffer of donor(l).  Shared
+ * layers launch no indexer work and read their donor's buffer unchanged.  indexer_types
+ * must equal the array the cache was created with.  Everything is enqueued on `stream`
+ * with no host synchronisation.  Errors: those of the two calls, DSA_ERR_SHAPE when the
+ * descriptors disagree (n_q, topk, n_kv) or do not match the cache. */
+dsa_status indexshare_layers_forward(const dsa_indexer_desc* idx_desc, const dsa_attn_desc* attn_desc,
+                                     int32_t n_layers, const uint8_t* indexer_types, const dsa_layer_io* layer_io,
+                                     const int32_t* ks, const int32_t* ke, const int32_t* q_pos,
+                                     const int32_t* k_pos, const float* rope_cs, int32_t rope_n_pos,
+                                     dsa_index_cache* cache, void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------ device status ---- */
+
+/* Synchronise `stream`, read the device status word of workspace `ws`, and map it:
+ * DSA_OK, DSA_ERR_TIMEOUT (a pipeline wait hit its bound) or DSA_ERR_DEVICE (bad index,
+ * range or overflow).  The raw bits are stored in *device_bits when it is not NULL.
+ * The word is cleared at the start of every call that takes the workspace. */
+dsa_status dsa_workspace_status(const void* ws, void* stream, uint32_t* device_bits);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_H_ */

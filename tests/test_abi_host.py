@@ -1,0 +1,168 @@
+"""Host-side checks of the C ABI (no GPU needed): exports, schedule, RoPE table, argument errors.
+
+Every call here either runs pure host code or must be rejected before anything is
+enqueued on a device, so none of them launches a kernel.
+"""
+import ctypes as C
+import math
+import os
+import re
+
+import numpy as np
+import pytest
+
+import dsa_indexer_cross_gb300 as D
+from dsa_indexer_cross_gb300 import _lib
+from oracle import dsa_oracle as O
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from dsa_indexer_cross_gb300.build import build
+    build()
+
+
+def declared_functions():
+    with open(os.path.join(ROOT, "include", "dsa.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dsa_[a-z_0-9]+|indexshare_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_function():
+    names = declared_functions()
+    assert len(names) >= 15
+    lib = C.CDLL(_lib.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/dsa.h but not exported"
+    assert set(names) == set(_lib.EXPORTED)
+
+
+def test_status_strings():
+    L = D.lib()
+    for code, name in _lib.STATUS_NAMES.items():
+        assert L.dsa_status_string(code).decode() == name
+
+
+def test_donor_table_matches_oracle_and_rejects_leading_shared():
+    types = ["full" if l % 4 == 0 else "shared" for l in range(78)]
+    assert D.dsa_donor_table(types) == O.donor_table(types)
+    rel = ["full", "full", "full", "shared", "shared", "shared", "full", "shared", "shared", "shared"]
+    assert D.dsa_donor_table(rel) == O.donor_table(rel)
+    with pytest.raises(D.DsaError) as e:
+        D.dsa_donor_table(["shared", "full"])
+    assert e.value.name == "DSA_ERR_NO_DONOR"
+    with pytest.raises(D.DsaError) as e:
+        D.dsa_donor_table([1, 7])
+    assert e.value.name == "DSA_ERR_ARG"
+
+
+def test_rope_table_matches_float64_cos_sin():
+    theta, r, n = 8e6, 64, 1 << 20
+    tab = D.dsa_rope_table(theta, r, n).numpy()
+    f = O.rope_inv_freq(r, theta)
+    for p in (0, 1, 7, 4095, 1044480, n - 1):
+        ang = p * f
+        np.testing.assert_array_equal(tab[p, :, 0], np.cos(ang).astype(np.float32))
+        np.testing.assert_array_equal(tab[p, :, 1], np.sin(ang).astype(np.float32))
+
+
+def test_index_cache_maps_layers_to_donor_buffers():
+    L = D.lib()
+    types = (C.c_uint8 * 8)(1, 1, 1, 0, 0, 0, 1, 0)
+    bufs = (C.c_void_p * 8)(0x1000, 0x2000, 0x3000, None, None, None, 0x7000, None)
+    h = C.c_void_p()
+    assert L.dsa_index_cache_create(8, types, 16, 4, bufs, C.byref(h)) == 0
+    want = [0x1000, 0x2000, 0x3000, 0x3000, 0x3000, 0x3000, 0x7000, 0x7000]
+    assert [L.dsa_index_cache_indices(h, l) for l in range(8)] == want
+    d = C.c_int32()
+    assert L.dsa_index_cache_donor(h, 5, C.byref(d)) == 0 and d.value == 2
+    assert L.dsa_index_cache_donor(h, 8, C.byref(d)) == 1
+    assert L.dsa_index_cache_indices(h, -1) is None
+    L.dsa_index_cache_destroy(h)
+    # a full layer without a buffer, and a schedule with no donor, are rejected
+    bufs[6] = None
+    assert L.dsa_index_cache_create(8, types, 16, 4, bufs, C.byref(h)) == 1
+    types2 = (C.c_uint8 * 2)(0, 1)
+    assert L.dsa_index_cache_create(2, types2, 16, 4, bufs, C.byref(h)) == 3
+
+
+def _idesc(**kw):
+    base = dict(n_q=8, n_kv=64, n_heads=32, head_dim=128, rope_dim=64, topk=16, max_len=64,
+                flags=D.DSA_IDX_ROPE_Q | D.DSA_IDX_ROPE_K)
+    base.update(kw)
+    return _lib.IndexerDesc(*base.values())
+
+
+@pytest.mark.parametrize("kw,name", [
+    (dict(head_dim=96), "DSA_ERR_UNSUPPORTED"),
+    (dict(n_heads=48), "DSA_ERR_UNSUPPORTED"),
+    (dict(rope_dim=3), "DSA_ERR_ARG"),
+    (dict(rope_dim=130), "DSA_ERR_ARG"),
+    (dict(topk=0), "DSA_ERR_UNSUPPORTED"),
+    (dict(topk=4096), "DSA_ERR_UNSUPPORTED"),
+    (dict(max_len=65), "DSA_ERR_ARG"),
+    (dict(n_q=-1), "DSA_ERR_ARG"),
+    (dict(flags=1 << 9), "DSA_ERR_ARG"),
+])
+def test_indexer_descriptor_errors(kw, name):
+    with pytest.raises(D.DsaError) as e:
+        D.dsa_indexer_workspace_size(_idesc(**kw))
+    assert e.value.name == name
+
+
+def test_indexer_null_pointers_rejected_before_launch():
+    L = D.lib()
+    desc = _idesc()
+    st = L.dsa_indexer_topk(C.byref(desc), None, None, None, None, None, None, None, None, 0, None, None, None, 0, None)
+    assert st == 1 and "non-NULL" in L.dsa_last_error().decode()
+    # misaligned bf16 pointer
+    st = L.dsa_indexer_topk(C.byref(desc), 0x1001, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, 0x7000, 0x8000, 16,
+                            0x9000, None, 0x10000, 1 << 30, None)
+    assert st == 1 and "aligned" in L.dsa_last_error().decode()
+
+
+def test_workspace_size_grows_with_rows_and_is_256_aligned():
+    a = D.dsa_indexer_workspace_size(_idesc(n_q=64))
+    b = D.dsa_indexer_workspace_size(_idesc(n_q=128))
+    assert b > a and a % 256 == 0 and b % 256 == 0
+    no_rope = D.dsa_indexer_workspace_size(_idesc(n_q=64, flags=0))
+    assert no_rope < a
+
+
+@pytest.mark.parametrize("kw,name", [
+    (dict(d_qk=192), "DSA_ERR_UNSUPPORTED"),
+    (dict(n_heads=0), "DSA_ERR_UNSUPPORTED"),
+    (dict(n_heads=256), "DSA_ERR_UNSUPPORTED"),
+    (dict(softmax_scale=0.0), "DSA_ERR_ARG"),
+    (dict(softmax_scale=float("nan")), "DSA_ERR_ARG"),
+    (dict(topk=0), "DSA_ERR_ARG"),
+])
+def test_attention_descriptor_errors(kw, name):
+    base = dict(n_q=4, n_kv=16, n_heads=16, d_qk=576, d_v=512, topk=8, softmax_scale=1 / 24.0, flags=0)
+    base.update(kw)
+    with pytest.raises(D.DsaError) as e:
+        D.dsa_sparse_attn_workspace_size(_lib.AttnDesc(*base.values()))
+    assert e.value.name == name
+
+
+def test_layer_loop_rejects_mismatched_schedule_before_launch():
+    L = D.lib()
+    types = (C.c_uint8 * 4)(1, 0, 0, 0)
+    bufs = (C.c_void_p * 4)(0x1000, None, None, None)
+    h = C.c_void_p()
+    assert L.dsa_index_cache_create(4, types, 8, 16, bufs, C.byref(h)) == 0
+    idesc = _idesc()
+    adesc = _lib.AttnDesc(8, 64, 16, 576, 512, 16, 1 / 24.0, 0)
+    io = (_lib.LayerIO * 4)()
+    other = (C.c_uint8 * 4)(1, 0, 1, 0)
+    st = L.indexshare_layers_forward(C.byref(idesc), C.byref(adesc), 4, other, io, None, None, None, None, None, 0, h,
+                                     0x100000, 1 << 30, None)
+    assert st == 2 and "indexer_types" in L.dsa_last_error().decode()
+    adesc_bad = _lib.AttnDesc(8, 64, 16, 576, 512, 32, 1 / 24.0, 0)
+    st = L.indexshare_layers_forward(C.byref(idesc), C.byref(adesc_bad), 4, types, io, None, None, None, None, None, 0,
+                                     h, 0x100000, 1 << 30, None)
+    assert st == 2
+    L.dsa_index_cache_destroy(h)

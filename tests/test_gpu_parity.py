@@ -1,0 +1,168 @@
+"""GPU parity: the C-ABI path (libdsa.so) against the float64 oracle on the same bytes.
+
+Top-k: the tie rule of tests/parity.py.  Attention: max-abs <= 1e-2 against the oracle fed
+the GPU's own indices, on unit-scale inputs (N(0,1) q / kv) and on the workloads'
+N(0,1)/sqrt(576) inputs (relative to the output's scale there).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import dsa_indexer_cross_gb300 as D
+from dsa_indexer_cross_gb300 import synth
+from gpu_cases import DEV, attn_errors, oracle_attn, oracle_scores, run_attn, run_indexer
+from parity import check_topk
+
+pytestmark = pytest.mark.gpu
+
+ATOL_OUT = 1e-2
+ATOL_LSE = 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from dsa_indexer_cross_gb300.build import build
+    build()
+    assert torch.cuda.is_available()
+
+
+def _check_indexer(w, geo, L, rows):
+    idx, sc, bits = run_indexer(w, geo, L, want_scores=True)
+    assert bits == 0, f"device status bits {bits:#x}"
+    score_rows = oracle_scores(w, geo, L, rows)
+    idx_np = idx.cpu().numpy()
+    bad = check_topk(idx_np, score_rows, w.topk, rows)
+    assert not bad, f"{len(bad)} rows violate the top-k rule, first: {bad[:3]}"
+    # reported scores of the selected keys agree with the oracle's
+    sc_np = sc.cpu().numpy()
+    for n, t in enumerate(rows):
+        sel = idx_np[t][idx_np[t] >= 0]
+        ref = score_rows[n][sel]
+        got = sc_np[t][: sel.size]
+        np.testing.assert_allclose(got, ref, rtol=2e-3, atol=2e-3 * (np.abs(ref).max() + 1e-30))
+        assert np.all(np.isneginf(sc_np[t][sel.size:]))
+    return idx
+
+
+def test_indexer_tiny_every_row():
+    w = synth.WORKLOADS["tiny"]
+    geo = synth.geometry(w)
+    L = synth.layer_inputs(w, geo, 0, device=DEV)
+    _check_indexer(w, geo, L, list(range(w.n_q)))
+
+
+def test_indexer_prefill_4k_sampled_rows():
+    w = synth.WORKLOADS["prefill_4k"]
+    geo = synth.geometry(w)
+    L = synth.layer_inputs(w, geo, 0, device=DEV, with_attn=False)
+    _check_indexer(w, geo, L, synth.sample_rows(w.n_q, 192, w.topk))
+
+
+@pytest.mark.parametrize("H_I,d,r,topk", [(16, 128, 64, 100), (64, 128, 64, 300), (8, 64, 16, 1), (32, 64, 0, 2048)])
+def test_indexer_ragged_ranges(H_I, d, r, topk):
+    # rows not a multiple of the group, empty rows, rows shorter than k, ragged key tail
+    rng = np.random.default_rng(H_I + topk)
+    n_q, n_kv = 77, 2600
+    ks = rng.integers(0, 600, n_q).astype(np.int32)
+    ln = rng.integers(0, 2000, n_q)
+    ln[[0, 5, 40]] = 0
+    ln[7] = 2000
+    ke = np.minimum(ks + ln, n_kv).astype(np.int32)
+    geo = synth.Geometry(n_kv, rng.integers(0, 5000, n_q).astype(np.int32), rng.integers(0, 5000, n_kv).astype(np.int32),
+                         ks, ke)
+    w = synth.Workload("ragged", "prefill", n_q, ("full",), H_I, d, r, 1e4, topk, 4)
+    L = synth.layer_inputs(w, geo, 0, device=DEV, with_attn=False)
+    _check_indexer(w, geo, L, list(range(n_q)))
+
+
+def test_indexer_independent_rows_decode_shape():
+    # batched decode: each row is its own sequence in a packed, already-rotated key cache
+    w = synth.Workload("decode_small", "decode", 6, ("full",), 64, 128, 64, 8e6, 256, 8, n_seqs=6, len_lo=1,
+                       len_hi=3000, rope_k=False)
+    geo = synth.geometry(w, seed=5)
+    L = synth.layer_inputs(w, geo, 0, device=DEV, with_attn=False)
+    _check_indexer(w, geo, L, list(range(w.n_q)))
+
+
+def _attn_case(w, geo, idx, rows, attn_scale, layer=1):
+    L = synth.layer_inputs(w, geo, layer, device=DEV, attn_scale=attn_scale)
+    out, lse, bits = run_attn(w, geo, L, idx)
+    assert bits == 0, f"device status bits {bits:#x}"
+    o_ref, lse_ref = oracle_attn(w, geo, L, idx.cpu().numpy(), rows)
+    e_o, e_l = attn_errors(out, lse, o_ref, lse_ref, rows)
+    return e_o, e_l, float(np.abs(o_ref).max())
+
+
+@pytest.mark.parametrize("name", ["tiny", "prefill_4k"])
+def test_attention_unit_scale_and_config_scale(name):
+    w = synth.WORKLOADS[name]
+    geo = synth.geometry(w)
+    Li = synth.layer_inputs(w, geo, 0, device=DEV, with_attn=False)
+    idx, _, bits = run_indexer(w, geo, Li)
+    assert bits == 0
+    rows = list(range(w.n_q)) if w.n_q <= 256 else synth.sample_rows(w.n_q, 96, w.topk)
+    e_o, e_l, _ = _attn_case(w, geo, idx, rows, "unit")
+    assert e_o <= ATOL_OUT and e_l <= ATOL_LSE, (e_o, e_l)
+    e_o, e_l, scale = _attn_case(w, geo, idx, rows, "config")
+    assert e_o <= ATOL_OUT * scale and e_l <= ATOL_LSE, (e_o, e_l, scale)
+
+
+@pytest.mark.parametrize("H", [1, 4, 16, 40, 64, 128])
+def test_attention_head_blocks_and_bad_indices(H):
+    rng = np.random.default_rng(H)
+    n_q, n_kv, topk = 9, 700, 200
+    ks = rng.integers(0, 100, n_q).astype(np.int32)
+    idx = rng.integers(0, 600, (n_q, topk)).astype(np.int32)
+    idx[rng.random((n_q, topk)) < 0.2] = -1          # scattered unused slots
+    idx[2, :] = -1                                   # a row with nothing selected
+    idx[3, 150:] = -1                                # a ragged row
+    idx[4, 7] = 650                                  # ks + 650 >= n_kv for ks >= 50 -> skipped, counted
+    geo = synth.Geometry(n_kv, np.zeros(n_q, np.int32), np.zeros(n_kv, np.int32), ks, ks)
+    w = synth.Workload("heads", "prefill", n_q, ("full", "shared"), 4, 64, 0, 1e4, topk, H)
+    L = synth.layer_inputs(w, geo, 1, device=DEV, attn_scale="unit")
+    out, lse, bits = run_attn(w, geo, L, torch.from_numpy(idx).to(DEV))
+    bad_expected = int(ks[4]) + 650 >= n_kv
+    assert (bits != 0) == bad_expected
+    idx_ref = idx.copy()
+    if bad_expected:
+        idx_ref[4, 7] = -1
+    o_ref, lse_ref = oracle_attn(w, geo, L, idx_ref, range(n_q))
+    e_o, e_l = attn_errors(out, lse, o_ref, lse_ref, range(n_q))
+    assert e_o <= ATOL_OUT and e_l <= ATOL_LSE, (e_o, e_l)
+    assert torch.all(out[2] == 0) and torch.all(torch.isneginf(lse[2]))
+
+
+@pytest.mark.parametrize("name", ["tiny", "prefill_4k"])
+def test_layers_forward_against_oracle(name):
+    w = synth.WORKLOADS[name]
+    geo = synth.geometry(w)
+    q_pos, k_pos, ks, ke = (torch.from_numpy(a).to(DEV) for a in (geo.q_pos, geo.k_pos, geo.ks, geo.ke))
+    layers = []
+    for l in range(len(w.layers)):
+        L = synth.layer_inputs(w, geo, l, device=DEV, attn_scale="unit")
+        L["out"] = torch.empty((w.n_q, w.n_heads, 512), dtype=torch.bfloat16, device=DEV)
+        L["lse"] = torch.empty((w.n_q, w.n_heads), dtype=torch.float32, device=DEV)
+        layers.append(L)
+    cache = D.IndexCache(w.layers, w.n_q, w.topk)
+    idesc = D.indexer_desc(w.n_q, geo.n_kv, w.n_heads_idx, w.head_dim_idx, w.rope_dim, w.topk, geo.max_len,
+                           D.DSA_IDX_ROPE_Q | D.DSA_IDX_ROPE_K)
+    adesc = D.attn_desc(w.n_q, geo.n_kv, w.n_heads, w.topk, w.softmax_scale)
+    rope = D.dsa_rope_table(w.theta, w.rope_dim, geo.max_pos).to(DEV)
+    ws = D.indexshare_layers_forward(idesc, adesc, w.layers, layers, ks, ke, q_pos, k_pos, rope, cache)
+    assert D.dsa_workspace_status(ws) == 0
+    donors = D.dsa_donor_table(w.layers)
+    rows = list(range(w.n_q)) if w.n_q <= 256 else synth.sample_rows(w.n_q, 48, w.topk)
+    for l, t in enumerate(w.layers):
+        assert cache.donor(l) == donors[l]
+        assert cache.indices_ptr(l) == cache.buffers[donors[l]].data_ptr()
+        if t == "full":
+            score_rows = oracle_scores(w, geo, layers[l], rows)
+            bad = check_topk(cache.buffers[l].cpu().numpy(), score_rows, w.topk, rows)
+            assert not bad, (l, bad[:3])
+        idx_np = cache.buffers[donors[l]].cpu().numpy()
+        o_ref, lse_ref = oracle_attn(w, geo, layers[l], idx_np, rows)
+        e_o, e_l = attn_errors(layers[l]["out"], layers[l]["lse"], o_ref, lse_ref, rows)
+        assert e_o <= ATOL_OUT and e_l <= ATOL_LSE, (l, e_o, e_l)
+    cache.close()
