@@ -43,6 +43,8 @@ def parse():
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--only", choices=["attn", "indexer"], default=None,
+                    help="run just one kernel call of the workload (for profiler captures); prints nothing")
     return ap.parse_args()
 
 
@@ -257,6 +259,21 @@ def run_native(args):
     def step():
         D.indexshare_layers_forward(idesc, adesc, w.layers, layers, ks, ke, q_pos, k_pos, rope, cache, ws=ws,
                                     stream=stream)
+
+    if args.only is not None:
+        # one indexer pass to produce real indices, then the requested kernel once
+        L0 = layers[0]
+        idx0 = cache.buffers[0]
+        iws = torch.empty(D.dsa_indexer_workspace_size(idesc), dtype=torch.uint8, device=dev)
+        D.dsa_indexer_topk(idesc, L0["q_idx"], L0["k_idx"], L0["w"], q_pos, k_pos, ks, ke, rope, idx0, None, ws=iws,
+                           stream=stream)
+        if args.only == "attn":
+            D.dsa_sparse_attn(adesc, L0["q"], L0["kv"], idx0, ks, L0["out"], L0["lse"], stream=stream)
+        else:
+            D.dsa_indexer_topk(idesc, L0["q_idx"], L0["k_idx"], L0["w"], q_pos, k_pos, ks, ke, rope, idx0, None,
+                               ws=iws, stream=stream)
+        torch.cuda.synchronize()
+        return 0
 
     for _ in range(args.warmup):
         step()

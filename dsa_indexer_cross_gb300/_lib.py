@@ -258,8 +258,14 @@ def indexshare_layers_forward(idesc: IndexerDesc, adesc: AttnDesc, indexer_types
     return ws
 
 
-def dsa_workspace_status(ws: torch.Tensor, stream=None) -> int:
-    """Synchronise and read the device status bits of a workspace; raises on a device fault."""
+def dsa_workspace_status(ws: torch.Tensor, stream=None, raise_on_fault: bool = True) -> int:
+    """Synchronise and read the device status bits of a workspace.
+
+    Raises DsaError on a device fault unless raise_on_fault is False, in which case the raw
+    bits are returned (0 = clean).  A CUDA error always raises.
+    """
     bits = C.c_uint32(0)
-    _check(lib().dsa_workspace_status(_ptr(ws), _stream(stream), C.byref(bits)))
+    st = lib().dsa_workspace_status(_ptr(ws), _stream(stream), C.byref(bits))
+    if st not in (0, 7, 8) or (st != 0 and raise_on_fault):
+        _check(st)
     return bits.value

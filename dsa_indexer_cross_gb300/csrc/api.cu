@@ -133,7 +133,7 @@ IndexerLayout indexer_layout(const dsa_indexer_desc* d, int sms) {
   p.n_heads = d->n_heads;
   p.head_dim = d->head_dim;
   p.topk = d->topk;
-  p.group = indep ? (d->n_heads >= 32 ? 1 : 32 / d->n_heads) : 256 / d->n_heads;
+  p.group = indep ? (d->n_heads >= 64 ? 1 : 64 / d->n_heads) : 256 / d->n_heads;
   p.n_groups = (d->n_q + p.group - 1) / p.group;
   const long long max_len = d->max_len > 0 ? d->max_len : 1;
   long long chunk;
@@ -144,6 +144,7 @@ IndexerLayout indexer_layout(const dsa_indexer_desc* d, int sms) {
     if (chunk < 4096) chunk = 4096;
   }
   if (chunk > 262144) chunk = 262144;
+  if (chunk < (max_len + 63) / 64) chunk = (max_len + 63) / 64;     // the final select reads <= 64 chunks
   chunk = (chunk + 127) / 128 * 128;
   p.chunk = static_cast<int>(chunk);
   p.n_chunks = static_cast<int>((max_len + chunk - 1) / chunk);
@@ -253,7 +254,9 @@ dsa_status check_attn_desc(const dsa_attn_desc* d) {
   return DSA_OK;
 }
 
-size_t attn_ws_bytes(const dsa_attn_desc* d) { return kAlign + align_up(static_cast<size_t>(d->n_q) * 4); }
+size_t attn_ws_bytes(const dsa_attn_desc* d) {
+  return kAlign + align_up(sparse_attn_ws_bytes(d->n_q, d->n_heads, d->n_kv, d->topk));
+}
 
 // status: device status header (first two words: bits, bad-index count); row_nt: n_q int32.
 dsa_status run_attn(const dsa_attn_desc* d, const void* q, const void* kv, const int32_t* idx, const int32_t* ks,
@@ -272,8 +275,13 @@ dsa_status run_attn(const dsa_attn_desc* d, const void* q, const void* kv, const
   cudaError_t e;
   if (clear_status && (e = cudaMemsetAsync(ws, 0, kAlign, st)) != cudaSuccess) return cuda_fail(e, "clear status");
   uint32_t* status = status_override ? status_override : reinterpret_cast<uint32_t*>(base);
-  e = launch_sparse_attn(d->n_q, d->n_kv, d->n_heads, d->topk, d->softmax_scale, q, kv, idx, ks, out, lse, status,
-                         reinterpret_cast<int32_t*>(base + kAlign), st);
+  CUtensorMap tkv;
+  std::memset(&tkv, 0, sizeof(tkv));
+  if (sparse_attn_dense_heads(d->n_heads, d->n_kv, d->topk) && d->n_kv > 0) {
+    if ((s = tmap_bf16(&tkv, kv, 576, d->n_kv, 64)) != DSA_OK) return s;
+  }
+  e = launch_sparse_attn(tkv, d->n_q, d->n_kv, d->n_heads, d->topk, d->softmax_scale, q, kv, idx, ks, out, lse, status,
+                         base + kAlign, st);
   if (e != cudaSuccess) return cuda_fail(e, "sparse attention kernel");
   return DSA_OK;
 }
@@ -281,6 +289,8 @@ dsa_status run_attn(const dsa_attn_desc* d, const void* q, const void* kv, const
 }  // namespace
 
 int device_sm_count() { return dev_info().sms; }
+
+
 
 }  // namespace dsa
 

@@ -26,6 +26,8 @@
 // K tiles go through a STAGES-deep ring, S^T is double-buffered in TMEM.
 #include <cuda_bf16.h>
 
+#include <cstddef>
+
 #include "kernels.h"
 #include "ptx.cuh"
 #include "topk.cuh"
@@ -44,16 +46,18 @@ struct Cfg {
   static constexpr int KB = DI / 64;                     // 128-byte K blocks per row
   static constexpr int Q_BYTES = N * DI * 2;
   static constexpr int K_STAGE_BYTES = kKeyTile * DI * 2;
-  static constexpr int SMEM_BUDGET = 232448 - 4096;      // dynamic budget after static smem
+  static constexpr int SMEM_BUDGET = 232448 - 6144;      // dynamic budget after static smem
   static constexpr int STAGES_FIT = (SMEM_BUDGET - 1024 - Q_BYTES) / K_STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT > 6 ? 6 : STAGES_FIT;
   static constexpr int DYN_SMEM = 1024 + Q_BYTES + STAGES * K_STAGE_BYTES;
   static constexpr uint32_t TMEM_COLS = (2 * N <= 32) ? 32 : (2 * N <= 64) ? 64 : (2 * N <= 128) ? 128 : (2 * N <= 256) ? 256 : 512;
-  static_assert(N % 32 == 0 && N >= 32 && N <= 256, "MMA N (epilogue reads 32 columns at a time)");
+  static_assert(N % 64 == 0 && N >= 64 && N <= 256, "MMA N (epilogue reads 64 columns at a time)");
   static_assert(STAGES >= 2, "shared memory");
 };
 
 struct Shared {
+  alignas(16) float w_s[256];   // read as float4 by the epilogue: keep 16-byte aligned
+  alignas(8) int2 rr[64];
   uint64_t k_full[8], k_empty[8];
   uint64_t q_full, q_empty;
   uint64_t t_full[2], t_empty[2];
@@ -62,12 +66,16 @@ struct Shared {
   uint32_t hist[256];
   int bc[4];
   int warp_off[4];
-  float w_s[256];
   uint32_t tau[64];
-  int cnt[64];
-  int2 rr[64];
+  int cnt[2][64];        // candidates held per query; [tile parity] so a tile reads one copy and writes the other
+  int qcnt[64][4];       // this tile's appends per (query, TMEM lane quarter)
   int epi_abort;
 };
+static_assert(offsetof(Shared, w_s) % 16 == 0, "float4 access");
+
+__device__ __forceinline__ void st_global_u32(uint32_t* p, uint32_t v) {
+  asm volatile("{\n .reg .u64 ga;\n cvta.to.global.u64 ga, %0;\n st.global.u32 [ga], %1;\n}\n" ::"l"(p), "r"(v) : "memory");
+}
 
 struct UnitInfo {
   int group, chunk, kbeg, kend, n_tiles;
@@ -86,30 +94,32 @@ __device__ __forceinline__ UnitInfo unit_info(int u, int n_groups, int chunk_len
   return ui;
 }
 
-// Cut the candidate buffer of one (row, chunk) back to its top-K.  Called by the 128
-// epilogue threads together.  Returns the new threshold key.
+// Cut the candidate buffer of one (row, chunk) back to its top-K, keeping the survivors in
+// their original (key index) order.  Called by the 128 epilogue threads together; thread i
+// owns the contiguous entries [i*P, i*P + P).  Returns the new threshold key.
 __device__ uint32_t compact_buffer(uint32_t* keys, int32_t* idxs, int n, int K, int tid, Shared& sh) {
+  const int P = (n + kEpiThreads - 1) / kEpiThreads;     // <= kMaxPer
+  const int e0 = tid * P;
   uint32_t rk[kMaxPer];
   int32_t ri[kMaxPer];
 #pragma unroll
   for (int i = 0; i < kMaxPer; ++i) {
-    const int e = tid + i * kEpiThreads;
-    rk[i] = e < n ? keys[e] : 0u;
-    ri[i] = e < n ? idxs[e] : 0;
+    const int e = e0 + i;
+    const bool in = i < P && e < n;
+    rk[i] = in ? keys[e] : 0u;
+    ri[i] = in ? idxs[e] : 0;
   }
   auto sync = [] { named_bar_sync(1, kEpiThreads); };
   auto fe = [&](auto&& f) {
 #pragma unroll
     for (int i = 0; i < kMaxPer; ++i)
-      if (tid + i * kEpiThreads < n) f(rk[i], ri[i]);
+      if (i < P && e0 + i < n) f(rk[i], ri[i]);
   };
   uint32_t v, cut;
   radix_threshold<kEpiThreads>(sync, fe, tid, K, sh.hist, sh.bc, v, cut);
   int keep = 0;
-#pragma unroll
-  for (int i = 0; i < kMaxPer; ++i)
-    if (tid + i * kEpiThreads < n && topk_keep(rk[i], ri[i], v, cut)) ++keep;
-  // block exclusive scan of `keep` over the 128 threads
+  fe([&](uint32_t key, int32_t idx) { keep += topk_keep(key, idx, v, cut) ? 1 : 0; });
+  // block exclusive scan of `keep` over the 128 threads (thread order = entry order)
   const int lane = tid & 31, wq = tid >> 5;
   int x = keep;
 #pragma unroll
@@ -119,17 +129,15 @@ __device__ uint32_t compact_buffer(uint32_t* keys, int32_t* idxs, int n, int K, 
   }
   if (lane == 31) sh.warp_off[wq] = x;
   sync();
-  int base = 0;
-  for (int wv = 0; wv < wq; ++wv) base += sh.warp_off[wv];
-  int pos = base + x - keep;
-#pragma unroll
-  for (int i = 0; i < kMaxPer; ++i) {
-    if (tid + i * kEpiThreads < n && topk_keep(rk[i], ri[i], v, cut)) {
-      keys[pos] = rk[i];
-      idxs[pos] = ri[i];
+  int pos = x - keep;
+  for (int wv = 0; wv < wq; ++wv) pos += sh.warp_off[wv];
+  fe([&](uint32_t key, int32_t idx) {
+    if (topk_keep(key, idx, v, cut)) {
+      keys[pos] = key;
+      idxs[pos] = idx;
       ++pos;
     }
-  }
+  });
   __threadfence_block();
   sync();
   return v;
@@ -151,6 +159,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sK = smem + C::Q_BYTES;
   const int warp = threadIdx.x >> 5;
   const int n_units = n_groups * n_chunks;
+  // k-th unit of this CTA, in "snake" order: forward on even rounds, backward on odd ones,
+  // so a CTA that drew a long unit in one round draws a short one in the next.
+  auto snake_unit = [&](int k) {
+    const int g = static_cast<int>(gridDim.x), b = static_cast<int>(blockIdx.x);
+    return k * g + ((k & 1) ? (g - 1 - b) : b);
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -184,7 +198,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmap_k);
       uint32_t kstage = 0, q_uses = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+      for (int k = 0; k * static_cast<int>(gridDim.x) < n_units && ok; ++k) {
+        const int u = snake_unit(k);
+        if (u >= n_units) continue;
         const UnitInfo ui = unit_info(u, n_groups, chunk_len, group_range);
         if (ui.n_tiles == 0) continue;
         if (q_uses > 0) ok = mbar_wait(&sh.q_empty, (q_uses - 1) & 1, &sh.abort_flag, status);
@@ -211,7 +227,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc = idesc_bf16_f32(128, N, 0, 0);
       uint32_t kstage = 0, q_uses = 0, tile = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+      for (int k = 0; k * static_cast<int>(gridDim.x) < n_units && ok; ++k) {
+        const int u = snake_unit(k);
+        if (u >= n_units) continue;
         const UnitInfo ui = unit_info(u, n_groups, chunk_len, group_range);
         if (ui.n_tiles == 0) continue;
         ok = mbar_wait(&sh.q_full, q_uses & 1, &sh.abort_flag, status);
@@ -251,7 +269,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // second one, so all four epilogue warps leave the loops at the same point.
     uint32_t tile = 0;
     bool stop = false;
-    for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
+    for (int k = 0; k * static_cast<int>(gridDim.x) < n_units && !stop; ++k) {
+      const int u = snake_unit(k);
+      if (u >= n_units) continue;
       const UnitInfo ui = unit_info(u, n_groups, chunk_len, group_range);
       const int t0 = ui.group * G;
       // per-unit state
@@ -263,58 +283,87 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t = t0 + tid;
         sh.rr[tid] = t < n_q ? row_range[t] : make_int2(0, 0);
         sh.tau[tid] = 0u;
-        sh.cnt[tid] = 0;
+        sh.cnt[tile & 1][tid] = 0;
       }
       named_bar_sync(1, kEpiThreads);
       for (int i = 0; i < ui.n_tiles; ++i, ++tile) {
         const int buf = tile & 1;
         bool ok = mbar_wait(&sh.t_full[buf], (tile >> 1) & 1, &sh.abort_flag, status);
         ok = __all_sync(0xffffffffu, ok);
+        uint32_t msk[G];
+        uint32_t key[G];
         if (ok) {
           tc_fence_after();
-          float acc[G];
+          // Head sum with NP independent partial sums per query (breaks the dependent FMA
+          // chain), TMEM read 64 columns per wait.
+          constexpr int NP = HI >= 16 ? 4 : 1;
+          float part[G][NP];
 #pragma unroll
-          for (int g = 0; g < G; ++g) acc[g] = 0.f;
+          for (int g = 0; g < G; ++g)
 #pragma unroll
-          for (int c0 = 0; c0 < N; c0 += 32) {
-            uint32_t v[32];
-            tmem_ld32(tmem + t_lane + buf * N + c0, v);
+            for (int p = 0; p < NP; ++p) part[g][p] = 0.f;
+#pragma unroll
+          for (int c0 = 0; c0 < N; c0 += 64) {
+            uint32_t v[64];
+            tmem_ld32(tmem + t_lane + buf * N + c0, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+            tmem_ld32(tmem + t_lane + buf * N + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
             tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 32; j += 4) {
+            for (int j = 0; j < 64; j += 4) {
               const float4 wv = *reinterpret_cast<const float4*>(&sh.w_s[c0 + j]);
-              acc[(c0 + j) / HI] = fmaf(wv.x, fmaxf(__uint_as_float(v[j]), 0.f), acc[(c0 + j) / HI]);
-              acc[(c0 + j + 1) / HI] = fmaf(wv.y, fmaxf(__uint_as_float(v[j + 1]), 0.f), acc[(c0 + j + 1) / HI]);
-              acc[(c0 + j + 2) / HI] = fmaf(wv.z, fmaxf(__uint_as_float(v[j + 2]), 0.f), acc[(c0 + j + 2) / HI]);
-              acc[(c0 + j + 3) / HI] = fmaf(wv.w, fmaxf(__uint_as_float(v[j + 3]), 0.f), acc[(c0 + j + 3) / HI]);
+              const float wj[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int col = c0 + j + e;
+                float& a = part[col / HI][NP == 1 ? 0 : (col % NP)];
+                a = fmaf(wj[e], fmaxf(__uint_as_float(v[j + e]), 0.f), a);
+              }
             }
+          }
+          float acc[G];
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            if constexpr (NP == 4) acc[g] = (part[g][0] + part[g][1]) + (part[g][2] + part[g][3]);
+            else acc[g] = part[g][0];
           }
           tc_fence_before();
           mbar_arrive(&sh.t_empty[buf]);
-          // append candidates that beat the running threshold
+          // append candidates that beat the running threshold, in key order: per query the
+          // four lane quarters publish their counts, then each writes after the lower ones
           const int j = ui.kbeg + i * kKeyTile + row;
 #pragma unroll
           for (int g = 0; g < G; ++g) {
             const int2 rr = sh.rr[g];
-            const uint32_t key = float_key(acc[g]);
-            const bool pass = j >= rr.x && j < rr.y && j < ui.kend && key > sh.tau[g];
-            const uint32_t m = __ballot_sync(0xffffffffu, pass);
-            if (m) {
-              int base = 0;
-              if (lane == 0) base = atomicAdd(&sh.cnt[g], __popc(m));
-              base = __shfl_sync(0xffffffffu, base, 0);
-              if (pass) {
-                const int pos = base + __popc(m & ((1u << lane) - 1u));
-                if (pos < cap) {
-                  const size_t off = (static_cast<size_t>(t0 + g) * n_chunks + ui.chunk) * cap + pos;
-                  cand_key[off] = key;
-                  cand_idx[off] = j;
-                }
-              }
-            }
+            key[g] = float_key(acc[g]);
+            msk[g] = __ballot_sync(0xffffffffu, j >= rr.x && j < rr.y && j < ui.kend && key[g] > sh.tau[g]);
+            if (lane == 0) sh.qcnt[g][quarter] = __popc(msk[g]);
           }
         } else if (lane == 0) {
           sh.epi_abort = 1;
+        }
+        named_bar_sync(1, kEpiThreads);
+        const int cur = tile & 1, nxt = cur ^ 1;
+        if (ok) {
+          const int j = ui.kbeg + i * kKeyTile + row;
+          // every query's write offset first (shared loads only), then the global stores
+          int pos[G];
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            int p0 = sh.cnt[cur][g] + __popc(msk[g] & ((1u << lane) - 1u));
+            for (int q = 0; q < quarter; ++q) p0 += sh.qcnt[g][q];
+            pos[g] = p0;
+          }
+          int tot = 0;
+          if (tid < G) tot = (sh.qcnt[tid][0] + sh.qcnt[tid][1]) + (sh.qcnt[tid][2] + sh.qcnt[tid][3]);
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            if (((msk[g] >> lane) & 1u) && pos[g] < cap) {
+              const size_t off = (static_cast<size_t>(t0 + g) * n_chunks + ui.chunk) * cap + pos[g];
+              st_global_u32(cand_key + off, key[g]);
+              st_global_u32(reinterpret_cast<uint32_t*>(cand_idx) + off, static_cast<uint32_t>(j));
+            }
+          }
+          if (tid < G) sh.cnt[nxt][tid] = sh.cnt[cur][tid] + tot;
         }
         named_bar_sync(1, kEpiThreads);
         stop = sh.epi_abort != 0;
@@ -322,14 +371,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           // cut back buffers that could overflow on the next tile
 #pragma unroll 1
           for (int g = 0; g < G; ++g) {
-            const int n = sh.cnt[g];
+            const int n = sh.cnt[nxt][g];
             if (n > cap - kKeyTile) {
               const size_t off = (static_cast<size_t>(t0 + g) * n_chunks + ui.chunk) * cap;
               __threadfence_block();
               const uint32_t v = compact_buffer(cand_key + off, cand_idx + off, n, topk, tid, sh);
               if (tid == 0) {
                 sh.tau[g] = v;
-                sh.cnt[g] = topk;
+                sh.cnt[nxt][g] = topk;
               }
               named_bar_sync(1, kEpiThreads);
             }
@@ -340,7 +389,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (stop) break;
       if (tid < G && t0 + tid < n_q)
-        cand_cnt[static_cast<size_t>(t0 + tid) * n_chunks + ui.chunk] = static_cast<uint32_t>(min(sh.cnt[tid], cap));
+        cand_cnt[static_cast<size_t>(t0 + tid) * n_chunks + ui.chunk] =
+            static_cast<uint32_t>(min(sh.cnt[tile & 1][tid], cap));
       named_bar_sync(1, kEpiThreads);
     }
   }
@@ -383,15 +433,15 @@ cudaError_t launch_indexer(const IndexerPlan& p, const CUtensorMap& tq, const CU
   DSA_IDX_CASE(16, 128, 16)
   DSA_IDX_CASE(32, 128, 8)
   DSA_IDX_CASE(64, 128, 4)
-  DSA_IDX_CASE(4, 64, 8)
-  DSA_IDX_CASE(8, 64, 4)
-  DSA_IDX_CASE(16, 64, 2)
-  DSA_IDX_CASE(32, 64, 1)
+  DSA_IDX_CASE(4, 64, 16)
+  DSA_IDX_CASE(8, 64, 8)
+  DSA_IDX_CASE(16, 64, 4)
+  DSA_IDX_CASE(32, 64, 2)
   DSA_IDX_CASE(64, 64, 1)
-  DSA_IDX_CASE(4, 128, 8)
-  DSA_IDX_CASE(8, 128, 4)
-  DSA_IDX_CASE(16, 128, 2)
-  DSA_IDX_CASE(32, 128, 1)
+  DSA_IDX_CASE(4, 128, 16)
+  DSA_IDX_CASE(8, 128, 8)
+  DSA_IDX_CASE(16, 128, 4)
+  DSA_IDX_CASE(32, 128, 2)
   DSA_IDX_CASE(64, 128, 1)
 #undef DSA_IDX_CASE
   return cudaErrorInvalidValue;

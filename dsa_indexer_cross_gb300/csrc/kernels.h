@@ -47,10 +47,15 @@ cudaError_t launch_select(int n_q, int n_chunks, int cap, int topk, const int2* 
                           uint32_t* status, cudaStream_t st);
 
 // ---------------------------------------------------------------------------- sparse attention
-// row_nt: n_q int32 of workspace (tiles of 64 index slots to visit per row).
-cudaError_t launch_sparse_attn(int n_q, int n_kv, int n_heads, int topk, float scale, const void* q, const void* kv,
-                               const int32_t* idx, const int32_t* ks, void* out, float* lse, uint32_t* status,
-                               int32_t* row_nt, cudaStream_t st);
+// Heads of the block-dense walk for this shape, or 0 for the per-token gather walk.
+int sparse_attn_dense_heads(int n_heads, int n_kv, int topk);
+// Scratch bytes launch_sparse_attn needs (per-row tile counts or per-block key ranges).
+size_t sparse_attn_ws_bytes(int n_q, int n_heads, int n_kv, int topk);
+// tmap_kv: kv as [n_kv x 576] bf16, 128-byte swizzled boxes of {64, 64} (read by the
+// block-dense walk only).
+cudaError_t launch_sparse_attn(const CUtensorMap& tmap_kv, int n_q, int n_kv, int n_heads, int topk, float scale,
+                               const void* q, const void* kv, const int32_t* idx, const int32_t* ks, void* out,
+                               float* lse, uint32_t* status, void* scratch, cudaStream_t st);
 
 int device_sm_count();
 

@@ -1,10 +1,13 @@
 // Final exact top-k of every query row from the indexer's per-chunk candidate buffers.
 //
 // Row t keeps k_t = min(topk, ke_t - ks_t) keys: the largest scores, ties to the lower key
-// index.  They are written as offsets j - ks_t in ascending order, then -1 up to width
-// topk ("GLM-5/5.1/5.2 DSA + LoRA enablement", commit capping top-k at the sequence length
-// and padding back with -1).  Candidates are (order-preserving score key, absolute key
-// index) pairs; every chunk buffer holds a superset of that chunk's top-k.
+// index.  They are written as offsets j - ks_t in ascending order, then -1 up to width topk
+// ("GLM-5/5.1/5.2 DSA + LoRA enablement", commit capping top-k at the sequence length and
+// padding back with -1).  Candidates are (order-preserving score key, absolute key index)
+// pairs; every chunk buffer holds a superset of that chunk's top-k and is already sorted by
+// key index (the indexer appends in key order and cuts back stably), and chunks cover
+// increasing key ranges, so the concatenated list is sorted and a stable compaction of the
+// selected entries is the sorted output.
 #include "kernels.h"
 #include "ptx.cuh"
 #include "topk.cuh"
@@ -13,8 +16,10 @@ namespace dsa {
 namespace {
 
 constexpr int kSelThreads = 256;
-constexpr int kMaxTopk = 2048;
+constexpr int kSelPer = 16;    // entries per thread kept in registers (rows up to 4096 candidates)
+constexpr int kMaxChunks = 64;
 
+template <bool kRegs>
 __global__ void __launch_bounds__(kSelThreads) select_kernel(int n_chunks, int cap, int topk,
                                                              const int2* __restrict__ row_range,
                                                              const uint32_t* __restrict__ cand_key,
@@ -24,82 +29,96 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(int n_chunks, int c
                                                              uint32_t* status) {
   __shared__ uint32_t hist[256];
   __shared__ int bc[4];
-  __shared__ int sel_n;
-  __shared__ int32_t sel_idx[kMaxTopk];
-  __shared__ uint32_t sel_key[kMaxTopk];
+  __shared__ int start[kMaxChunks + 1];
+  __shared__ int warp_tot[kSelThreads / 32];
   const int t = blockIdx.x;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int2 r = row_range[t];
-  int kt = min(topk, r.y - r.x);
   const size_t base = static_cast<size_t>(t) * n_chunks * cap;
   const uint32_t* cnt_row = cand_cnt + static_cast<size_t>(t) * n_chunks;
-  int total = 0;
-  for (int c = 0; c < n_chunks; ++c) total += min(static_cast<int>(cnt_row[c]), cap);
+  if (tid == 0) {
+    int s = 0;
+    for (int c = 0; c < n_chunks; ++c) {
+      start[c] = s;
+      s += min(static_cast<int>(cnt_row[c]), cap);
+    }
+    start[n_chunks] = s;
+  }
+  __syncthreads();
+  const int total = start[n_chunks];
+  int kt = min(topk, r.y - r.x);
   if (total < kt) {
     if (tid == 0) atomicOr(status, DEV_ERR_OVERFLOW);
     kt = total;
   }
+  int32_t* out = idx_out + static_cast<size_t>(t) * topk;
+  float* so = score_out ? score_out + static_cast<size_t>(t) * topk : nullptr;
+  // this thread owns the contiguous list positions [p0, p1)
+  const int per = (total + kSelThreads - 1) / kSelThreads;
+  const int p0 = min(total, tid * per), p1 = min(total, p0 + per);
+  auto at = [&](int pos) -> size_t {     // list position -> element offset in the buffers
+    int c = 0;
+    while (pos >= start[c + 1]) ++c;
+    return base + static_cast<size_t>(c) * cap + (pos - start[c]);
+  };
+  uint32_t rk[kRegs ? kSelPer : 1];
+  int32_t ri[kRegs ? kSelPer : 1];
+  if constexpr (kRegs) {
+#pragma unroll
+    for (int i = 0; i < kSelPer; ++i) {
+      if (p0 + i < p1) {
+        const size_t o = at(p0 + i);
+        rk[i] = __ldg(cand_key + o);
+        ri[i] = __ldg(cand_idx + o);
+      }
+    }
+  }
   auto fe = [&](auto&& f) {
-    for (int c = 0; c < n_chunks; ++c) {
-      const int n = min(static_cast<int>(cnt_row[c]), cap);
-      const uint32_t* kp = cand_key + base + static_cast<size_t>(c) * cap;
-      const int32_t* ip = cand_idx + base + static_cast<size_t>(c) * cap;
-      for (int e = tid; e < n; e += kSelThreads) f(__ldg(kp + e), __ldg(ip + e));
+    if constexpr (kRegs) {
+#pragma unroll
+      for (int i = 0; i < kSelPer; ++i)
+        if (p0 + i < p1) f(rk[i], ri[i]);
+    } else {
+      for (int p = p0; p < p1; ++p) {
+        const size_t o = at(p);
+        f(__ldg(cand_key + o), __ldg(cand_idx + o));
+      }
     }
   };
   uint32_t v = 0, cut = 0x7FFFFFFFu;
   const bool take_all = total <= kt;
-  if (kt > 0 && !take_all) {
-    radix_threshold<kSelThreads>([] { __syncthreads(); }, fe, tid, kt, hist, bc, v, cut);
+  if (kt > 0 && !take_all) radix_threshold<kSelThreads>([] { __syncthreads(); }, fe, tid, kt, hist, bc, v, cut);
+  // stable compaction of the kept entries in list (= key index) order
+  int keep = 0;
+  fe([&](uint32_t key, int32_t idx) { keep += (take_all || topk_keep(key, idx, v, cut)) ? 1 : 0; });
+  int x = keep;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
   }
-  if (tid == 0) sel_n = 0;
+  if (lane == 31) warp_tot[wid] = x;
   __syncthreads();
-  if (kt > 0) {
-    fe([&](uint32_t key, int32_t idx) {
-      if (take_all || topk_keep(key, idx, v, cut)) {
-        const int p = atomicAdd(&sel_n, 1);
-        if (p < kMaxTopk) {
-          sel_idx[p] = idx;
-          sel_key[p] = key;
-        }
+  int pos = x - keep;
+  for (int w = 0; w < wid; ++w) pos += warp_tot[w];
+  fe([&](uint32_t key, int32_t idx) {
+    if (take_all || topk_keep(key, idx, v, cut)) {
+      if (pos < topk) {
+        out[pos] = idx - r.x;
+        if (so) so[pos] = key_float(key);
       }
-    });
-  }
-  __syncthreads();
-  const int n = min(sel_n, kMaxTopk);
-  if (tid == 0 && n != kt) atomicOr(status, DEV_ERR_OVERFLOW);
-  int P = 1;
-  while (P < n) P <<= 1;
-  for (int i = n + tid; i < P; i += kSelThreads) {
-    sel_idx[i] = 0x7FFFFFFF;
-    sel_key[i] = 0;
-  }
-  __syncthreads();
-  // bitonic sort by key index, ascending
-  for (int k = 2; k <= P; k <<= 1) {
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int i = tid; i < P; i += kSelThreads) {
-        const int ixj = i ^ j;
-        if (ixj > i) {
-          const bool asc = (i & k) == 0;
-          const int32_t a = sel_idx[i], b = sel_idx[ixj];
-          if ((a > b) == asc) {
-            sel_idx[i] = b;
-            sel_idx[ixj] = a;
-            const uint32_t ka = sel_key[i];
-            sel_key[i] = sel_key[ixj];
-            sel_key[ixj] = ka;
-          }
-        }
-      }
-      __syncthreads();
+      ++pos;
     }
-  }
-  int32_t* out = idx_out + static_cast<size_t>(t) * topk;
-  for (int i = tid; i < topk; i += kSelThreads) out[i] = i < n ? sel_idx[i] - r.x : -1;
-  if (score_out) {
-    float* so = score_out + static_cast<size_t>(t) * topk;
-    for (int i = tid; i < topk; i += kSelThreads) so[i] = i < n ? key_float(sel_key[i]) : -__int_as_float(0x7f800000);
+  });
+  const int n_sel = [&] {
+    int s = 0;
+    for (int w = 0; w < kSelThreads / 32; ++w) s += warp_tot[w];
+    return s;
+  }();
+  if (tid == 0 && n_sel != kt) atomicOr(status, DEV_ERR_OVERFLOW);
+  for (int i = n_sel + tid; i < topk; i += kSelThreads) {
+    out[i] = -1;
+    if (so) so[i] = -__int_as_float(0x7f800000);
   }
 }
 
@@ -109,9 +128,13 @@ cudaError_t launch_select(int n_q, int n_chunks, int cap, int topk, const int2* 
                           const int32_t* cand_idx, const uint32_t* cand_cnt, int32_t* idx_out, float* score_out,
                           uint32_t* status, cudaStream_t st) {
   if (n_q <= 0) return cudaSuccess;
-  if (topk > kMaxTopk) return cudaErrorInvalidValue;
-  select_kernel<<<n_q, kSelThreads, 0, st>>>(n_chunks, cap, topk, row_range, cand_key, cand_idx, cand_cnt, idx_out,
-                                            score_out, status);
+  if (n_chunks > kMaxChunks) return cudaErrorInvalidValue;
+  if (static_cast<long long>(n_chunks) * cap <= static_cast<long long>(kSelThreads) * kSelPer)
+    select_kernel<true><<<n_q, kSelThreads, 0, st>>>(n_chunks, cap, topk, row_range, cand_key, cand_idx, cand_cnt,
+                                                    idx_out, score_out, status);
+  else
+    select_kernel<false><<<n_q, kSelThreads, 0, st>>>(n_chunks, cap, topk, row_range, cand_key, cand_idx, cand_cnt,
+                                                     idx_out, score_out, status);
   return cudaGetLastError();
 }
 

@@ -1,4 +1,4 @@
-// MLA-absorbed sparse attention over gathered latent rows, on tcgen05.
+// MLA-absorbed sparse attention over the selected latent rows, on tcgen05.
 //
 //   o[t, h] = sum_{j in I_t} softmax_j(tau * q[t, h] . kv[ks_t + j]) * kv[ks_t + j, :512]
 //
@@ -7,23 +7,36 @@
 // and the 512-d value follow "GLM-5/5.1/5.2 DSA + LoRA enablement", qk_rope_head_dim
 // commit.)  All heads of a token read the same selected rows.
 //
-// Formulation.  A CTA owns (token t, block of HB heads) and walks the token's index row in
-// tiles of 64 selected rows.  Because HB (16 or 32) is too small for the M side of the
-// tensor core, both products run transposed, with the gathered rows on M:
-//     S^T[r, h]  = Rows[r, :576] . Q[h, :576]            M = 64 rows,   N = HB, K = 576
-//     O^T[d, h] += Rows[:, d]^T  . P^T[r, h]             M = 128 dims,  N = HB, K = 64
-// The gathered tile is stored once in shared memory in the 128-byte-swizzled layout and
-// read as a K-major operand by the first product and as an MN-major operand by the
-// second, so each row is fetched from memory exactly once.  S^T is double-buffered in
-// TMEM; O^T (512 x HB fp32) stays in TMEM for the whole token.
+// Formulation.  A CTA owns a work item of HB "columns" (query, head pairs) and walks rows
+// of the latent cache in tiles of 64.  HB (16..64) is too small for the M side of the tensor
+// core, so both products run transposed, with the latent rows on M:
+//     S^T[r, c]  = Rows[r, :576] . Q[c, :576]            M = 64 rows,   N = HB, K = 576
+//     O^T[d, c] += Rows[:, d]^T  . P^T[r, c]             M = 128 dims,  N = HB, K = 64
+// The tile is stored once in shared memory in the 128-byte-swizzled layout and read as a
+// K-major operand by the first product and as an MN-major operand by the second, so each
+// row is brought on chip once per item.  S^T is double-buffered in TMEM; O^T (512 x HB
+// fp32) stays in TMEM for the whole item.
 //
-// Online softmax (base 2): per head the running max m and sum l live in registers of the
-// softmax warps; a tile whose max exceeds the max in use by more than 8 (a factor 256)
-// triggers a rescale of O^T in TMEM, otherwise the old max is kept (exact either way).
+// Two ways to walk the rows (template parameter HD):
+//   HD == 0  "gather": item = (token, block of HB heads); the tile holds the token's next
+//            64 selected rows, fetched with cp.async (zero-filled for -1 / out-of-range).
+//   HD  > 0  "block-dense": item = HB / HD consecutive tokens with all HD heads; the tile is
+//            64 CONSECUTIVE latent rows of the block's key range, fetched by TMA, and a
+//            per-(token, row) selection bitmask built from the index rows masks S^T.  Used
+//            when the selections are dense (short prefixes, k close to the prefix length):
+//            every row is then fetched once per block instead of once per token.
+// Both compute exactly the same sums; only unselected (masked) entries are skipped.
 //
-// Warp roles (288 threads): warps 0-3 gather rows with cp.async (zero-fill for unused or
-// out-of-range slots); warps 4-7 run the softmax and the epilogue; warp 8 owns TMEM and
-// issues the MMAs from one thread.  The CTA is persistent over (token, head block) items.
+// Online softmax (base 2): the per-column max in use lives in shared memory and changes only
+// when a score exceeds it by more than 8 (a factor 256); one barrier-reduction per tile
+// detects that, and only then are the tile's column maxima exchanged and O^T and the running
+// sums rescaled (exact either way).  Each thread keeps running sums of its own rows and the
+// column sums are reduced once per item.
+//
+// Warp roles (256 threads): warps 0-2 load Q and the rows (cp.async gathers, or one thread
+// issuing TMA tile loads in block-dense mode); warps 3-6 run the softmax, build the mask
+// (block-dense) and the epilogue; warp 7 owns TMEM and issues the MMAs from one thread.
+// Persistent CTAs.
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -32,60 +45,143 @@
 namespace dsa {
 namespace {
 
-constexpr int kRows = 64;          // selected rows per tile
+constexpr int kRows = 64;          // latent rows per tile
 constexpr int kDqk = 576;
 constexpr int kDv = 512;
 constexpr int kChunks = kDqk / 8;  // 16-byte chunks per latent row
 constexpr int kStages = 2;
-constexpr int kProd = 128;
-constexpr int kSoft = 128;
-constexpr int kThreads = kProd + kSoft + 32;
+constexpr int kProd = 96;                      // warps 0-2
+constexpr int kSoft = 128;                     // warps 3-6, one per TMEM lane quarter
+constexpr int kThreads = kProd + kSoft + 32;   // + warp 7 (MMA); 8 warps = 2 per SM sub-partition
 constexpr int kTileBytes = kRows * kDqk * 2;   // 72 KB
+constexpr int kDenseCols = 48;                 // columns of a block-dense item
+constexpr int kMaskBytes = 6144;               // selection bitmask budget (block-dense)
 
-template <int HB>
+template <int HB, int HD>
 struct ACfg {
+  static constexpr bool DENSE = HD > 0;
+  static constexpr int B = DENSE ? HB / HD : 1;                        // tokens per item
+  static constexpr int MAXR = DENSE ? (kMaskBytes * 8 / B) / 64 * 64 : 0;  // longest key range
   static constexpr int Q_BYTES = HB * kDqk * 2;
   static constexpr int P_BYTES = HB * kRows * 2;
-  static constexpr int DYN_SMEM = 1024 + kStages * kTileBytes + Q_BYTES + P_BYTES;
-  static constexpr uint32_t TMEM_COLS = 6 * HB <= 128 ? 128 : 256;
+  static constexpr int M_BYTES = DENSE ? kMaskBytes : 0;
+  static constexpr int DYN_SMEM = 1024 + kStages * kTileBytes + Q_BYTES + P_BYTES + M_BYTES;
+  static constexpr uint32_t TMEM_COLS = 6 * HB <= 128 ? 128 : 6 * HB <= 256 ? 256 : 512;
   static constexpr int O_COL = 0;
   static constexpr int S_COL = 4 * HB;
+  static_assert(HB % 16 == 0 && HB <= 64, "columns");
+  static_assert(!DENSE || HB % HD == 0, "whole tokens per dense item");
 };
 
+// Per-column softmax state lives in shared memory (uniform across the softmax threads).
 struct AShared {
   uint64_t full[kStages], empty[kStages];
-  uint64_t q_empty, s_full[2], s_empty[2], p_full, o_done, o_free;
+  uint64_t q_full, q_empty, s_full[2], s_empty[2], p_full, o_done, o_free;
   uint32_t tmem_base, abort_flag, soft_abort;
-  float red[4][32];
+  uint32_t prod_ok;
+  alignas(16) float red[4][64];
+  alignas(16) float m_used[64];
+  alignas(16) float l_run[64];
+  alignas(16) float alpha[64];
 };
+static_assert(ACfg<64, 0>::DYN_SMEM + sizeof(AShared) <= 232448, "HB=64 must fit in shared memory");
+static_assert(ACfg<48, 16>::DYN_SMEM + sizeof(AShared) <= 232448, "block-dense must fit in shared memory");
+
+// 16 consecutive floats of shared memory into registers (four 16-byte loads issued together).
+__device__ __forceinline__ void load_row16(float (&r)[16], const float* p) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float4 v = *reinterpret_cast<const float4*>(p + 4 * i);
+    r[4 * i] = v.x;
+    r[4 * i + 1] = v.y;
+    r[4 * i + 2] = v.z;
+    r[4 * i + 3] = v.w;
+  }
+}
+// Stores through explicit state spaces (the compiler then knows they cannot alias the
+// shared-memory loads around them).
+__device__ __forceinline__ void st_shared_u16(void* p, uint16_t v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(smem_u32(p)), "h"(v) : "memory");
+}
+__device__ __forceinline__ void st_global_u16(uint16_t* p, uint16_t v) {
+  asm volatile("{\n .reg .u64 ga;\n cvta.to.global.u64 ga, %0;\n st.global.u16 [ga], %1;\n}\n" ::"l"(p), "h"(v) : "memory");
+}
+
+// Named barrier over n threads that also returns the OR of a predicate across them.
+__device__ __forceinline__ bool bar_red_or(uint32_t id, uint32_t n, bool p) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %1, 0;\n bar.red.or.pred po, %2, %3, pi;\n selp.u32 %0, 1, 0, po;\n}\n"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(p)), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
 
 __device__ __forceinline__ uint32_t sw128(int row, int chunk) {
   return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
-template <int HB>
+// Work item description shared by all roles.
+struct Item {
+  int t0;        // gather: the token; block-dense: first token of the block
+  int hb;        // gather: head block; block-dense: 0
+  int nt;        // tiles of 64 rows
+  int lo;        // block-dense: first latent row of the block's range
+};
+
+template <int HB, int HD>
+__device__ __forceinline__ Item item_info(int item, int n_hb, const int32_t* row_nt, const int2* block_range) {
+  Item it{};
+  if constexpr (HD == 0) {
+    it.t0 = item / n_hb;
+    it.hb = item - it.t0 * n_hb;
+    it.nt = __ldg(row_nt + it.t0);
+    it.lo = 0;
+  } else {
+    it.t0 = item * (HB / HD);
+    it.hb = 0;
+    const int2 r = block_range[item];
+    it.lo = r.x;
+    it.nt = r.y > r.x ? (r.y - r.x + kRows - 1) / kRows : 0;
+  }
+  return it;
+}
+
+template <int HB, int HD>
 __global__ void __launch_bounds__(kThreads, 1)
-    sparse_attn_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ kv, const int32_t* __restrict__ idx,
-                       const int32_t* __restrict__ ks, const int32_t* __restrict__ row_nt, uint16_t* __restrict__ out,
-                       float* __restrict__ lse, int n_q, int n_kv, int H, int topk, float scale_log2,
-                       uint32_t* status, uint32_t* bad_count) {
-  using C = ACfg<HB>;
+    sparse_attn_kernel(const __grid_constant__ CUtensorMap tmap_kv, const uint16_t* __restrict__ q,
+                       const uint16_t* __restrict__ kv, const int32_t* __restrict__ idx,
+                       const int32_t* __restrict__ ks, const int32_t* __restrict__ row_nt,
+                       const int2* __restrict__ block_range, uint16_t* __restrict__ out, float* __restrict__ lse,
+                       int n_q, int n_kv, int H, int topk, float scale_log2, uint32_t* status, uint32_t* bad_count) {
+  using C = ACfg<HB, HD>;
+  constexpr bool DENSE = C::DENSE;
+  constexpr int B = C::B;
   extern __shared__ uint8_t smem_raw[];
   __shared__ AShared sh;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sT = smem;                                   // kStages tiles
   uint8_t* sQ = smem + kStages * kTileBytes;            // HB x 576, 9 blocks of HB x 128 B
   uint8_t* sP = sQ + C::Q_BYTES;                        // P^T: HB x 64, K-major
+  uint32_t* sMask = reinterpret_cast<uint32_t*>(sP + C::P_BYTES);   // block-dense: B x MAXR bits
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int n_hb = (H + HB - 1) / HB;
-  const int n_items = n_q * n_hb;
+  const int n_hb = DENSE ? 1 : (H + HB - 1) / HB;
+  const int n_items = DENSE ? (n_q + B - 1) / B : n_q * n_hb;
+  // k-th item of this CTA in "snake" order (forward on even rounds, backward on odd ones):
+  // causal items grow with their index, so alternating directions balances the CTAs.
+  auto snake_item = [&](int k) {
+    const int gdim = static_cast<int>(gridDim.x), b = static_cast<int>(blockIdx.x);
+    return k * gdim + ((k & 1) ? (gdim - 1 - b) : b);
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&sh.full[s], kProd);
+      mbar_init(&sh.full[s], DENSE ? 1 : kProd);
       mbar_init(&sh.empty[s], 1);
     }
+    mbar_init(&sh.q_full, kProd);
     mbar_init(&sh.q_empty, 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sh.s_full[b], 1);
@@ -99,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
     fence_proxy_async_smem();
   }
-  if (warp == 8) {
+  if (warp == 7) {
     tmem_alloc(&sh.tmem_base, C::TMEM_COLS);
     tmem_relinquish();
   }
@@ -108,53 +204,103 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = sh.tmem_base;
 
-  if (warp < 4) {
-    // ---------------------------------------------------------------- gather producers
+  if (warp < 3) {
+    // ---------------------------------------------------------------- Q (+ gathered rows)
+    // Thread 0 does every wait and publishes the outcome in sh.prod_ok between two named
+    // barriers (id 2), so the four producer warps always stop at the same point.
     const int tid = threadIdx.x;
     uint32_t g = 0, it = 0;
     bool ok = true;
-    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-      const int t = item / n_hb, hb = item - t * n_hb;
-      const int nt = __ldg(row_nt + t);
-      if (nt == 0) continue;
-      if (it > 0) ok = mbar_wait(&sh.q_empty, (it - 1) & 1, &sh.abort_flag, status);
+    auto sync_ok = [&](bool mine) -> bool {
+      if (tid == 0) sh.prod_ok = mine ? 1u : 0u;
+      named_bar_sync(2, kProd);
+      const bool r = sh.prod_ok != 0;
+      named_bar_sync(2, kProd);
+      return r;
+    };
+    for (int k = 0; k * static_cast<int>(gridDim.x) < n_items && ok; ++k) {
+      const int item = snake_item(k);
+      if (item >= n_items) continue;
+      const Item I = item_info<HB, HD>(item, n_hb, row_nt, block_range);
+      if (I.nt == 0) continue;
+      bool w_ok = true;
+      if (tid == 0 && it > 0) w_ok = mbar_wait(&sh.q_empty, (it - 1) & 1, &sh.abort_flag, status);
+      ok = sync_ok(w_ok);
       if (!ok) break;
-      // Q block: HB heads x 72 chunks
       for (int c = tid; c < HB * kChunks; c += kProd) {
         const int h = c / kChunks, ch = c - h * kChunks;
-        const int head = hb * HB + h;
-        const bool v = head < H;
-        const uint16_t* src = q + (static_cast<size_t>(t) * H + (v ? head : 0)) * kDqk + ch * 8;
+        size_t qrow;
+        bool v;
+        if constexpr (DENSE) {
+          v = I.t0 + h / HD < n_q;
+          qrow = static_cast<size_t>(I.t0) * H + h;       // (token, head) rows are contiguous
+        } else {
+          const int head = I.hb * HB + h;
+          v = head < H;
+          qrow = static_cast<size_t>(I.t0) * H + head;
+        }
+        const uint16_t* src = q + (v ? qrow : 0) * kDqk + ch * 8;
         cp_async_16_zfill(smem_u32(sQ + (ch >> 3) * (HB * 128) + sw128(h, ch & 7)), src, v);
       }
-      const int kst = __ldg(ks + t);
-      const int32_t* irow = idx + static_cast<size_t>(t) * topk;
-      for (int i = 0; i < nt; ++i, ++g) {
-        const int s = g % kStages;
-        if (g >= kStages) {
-          ok = mbar_wait(&sh.empty[s], ((g / kStages) - 1) & 1, &sh.abort_flag, status);
-          if (!ok) break;
-        }
-        uint8_t* dst = sT + s * kTileBytes;
-        for (int c = tid; c < kRows * kChunks; c += kProd) {
-          const int r = c / kChunks, ch = c - r * kChunks;
-          const int slot = i * kRows + r;
-          const int j = slot < topk ? __ldg(irow + slot) : -1;
-          const long long row = static_cast<long long>(kst) + j;
-          const bool v = j >= 0 && row < n_kv && row >= 0;
-          if (ch == 0 && j >= 0 && !v) {
-            atomicOr(status, DEV_ERR_BAD_INDEX);
-            atomicAdd(bad_count, 1u);
+      cp_async_mbar_arrive(&sh.q_full);
+      if constexpr (DENSE) {
+        // one thread streams the block's consecutive latent rows with TMA
+        if (tid == 0) {
+          for (int i = 0; i < I.nt; ++i, ++g) {
+            const int s = g % kStages;
+            if (g >= kStages) {
+              ok = mbar_wait(&sh.empty[s], ((g / kStages) - 1) & 1, &sh.abort_flag, status);
+              if (!ok) break;
+            }
+            mbar_arrive_expect_tx(&sh.full[s], kTileBytes);
+            uint8_t* dst = sT + s * kTileBytes;
+            for (int b = 0; b < kDqk / 64; ++b)
+              tma_load_2d(dst + b * (kRows * 128), &tmap_kv, &sh.full[s], b * 64, I.lo + i * kRows);
           }
-          const uint16_t* src = kv + (v ? row : 0) * kDqk + ch * 8;
-          cp_async_16_zfill(smem_u32(dst + (ch >> 3) * (kRows * 128) + sw128(r, ch & 7)), src, v);
         }
-        cp_async_mbar_arrive(&sh.full[s]);
+        ok = sync_ok(ok);
+      } else {
+        const int t = I.t0;
+        const long long kst = __ldg(ks + t);
+        const int32_t* irow = idx + static_cast<size_t>(t) * topk;
+        for (int i = 0; i < I.nt; ++i, ++g) {
+          const int s = g % kStages;
+          w_ok = true;
+          if (tid == 0 && g >= kStages) w_ok = mbar_wait(&sh.empty[s], ((g / kStages) - 1) & 1, &sh.abort_flag, status);
+          ok = sync_ok(w_ok);
+          if (!ok) break;
+          // resolve every chunk's row first (independent loads), then issue the copies
+          constexpr int kPer = kRows * kChunks / kProd;   // 36 chunks per thread
+          int rows[kPer];
+#pragma unroll
+          for (int k = 0; k < kPer; ++k) {
+            const int c = tid + k * kProd;
+            const int r = c / kChunks;
+            const int slot = i * kRows + r;
+            const int j = slot < topk ? __ldg(irow + slot) : -1;
+            const long long row = kst + j;
+            const bool v = j >= 0 && row >= 0 && row < n_kv;
+            if (j >= 0 && !v && c - r * kChunks == 0) {
+              atomicOr(status, DEV_ERR_BAD_INDEX);
+              atomicAdd(bad_count, 1u);
+            }
+            rows[k] = v ? static_cast<int>(row) : -1;
+          }
+          uint8_t* dst = sT + s * kTileBytes;
+#pragma unroll
+          for (int k = 0; k < kPer; ++k) {
+            const int c = tid + k * kProd;
+            const int r = c / kChunks, ch = c - r * kChunks;
+            const uint16_t* src = kv + static_cast<size_t>(rows[k] >= 0 ? rows[k] : 0) * kDqk + ch * 8;
+            cp_async_16_zfill(smem_u32(dst + (ch >> 3) * (kRows * 128) + sw128(r, ch & 7)), src, rows[k] >= 0);
+          }
+          cp_async_mbar_arrive(&sh.full[s]);
+        }
       }
       ++it;
     }
     cp_async_wait<0>();
-  } else if (warp < 8) {
+  } else if (warp < 7) {
     // ---------------------------------------------------------------- softmax + epilogue
     const int tid = threadIdx.x - kProd;   // 0..127
     const int qd = warp & 3;               // TMEM lane quarter
@@ -166,64 +312,114 @@ __global__ void __launch_bounds__(kThreads, 1)
     // barrier, so the four softmax warps always leave the loops at the same point.
     uint32_t g = 0, it = 0;
     bool stop = false;
-    for (int item = blockIdx.x; item < n_items && !stop; item += gridDim.x) {
-      const int t = item / n_hb, hb = item - t * n_hb;
-      const int nt = __ldg(row_nt + t);
-      if (nt == 0) {
+    for (int k = 0; k * static_cast<int>(gridDim.x) < n_items && !stop; ++k) {
+      const int item = snake_item(k);
+      if (item >= n_items) continue;
+      const Item I = item_info<HB, HD>(item, n_hb, row_nt, block_range);
+      // column c -> (token, head)
+      auto col_token = [&](int c) { return DENSE ? I.t0 + c / (DENSE ? HD : 1) : I.t0; };
+      auto col_head = [&](int c) { return DENSE ? c % (DENSE ? HD : 1) : I.hb * HB + c; };
+      auto col_ok = [&](int c) { return col_token(c) < n_q && col_head(c) < H; };
+      if (I.nt == 0) {
         for (int e = tid; e < HB * kDv; e += kSoft) {
-          const int h = e / kDv, head = hb * HB + h;
-          if (head < H) out[(static_cast<size_t>(t) * H + head) * kDv + (e - h * kDv)] = 0;
+          const int c = e / kDv;
+          if (col_ok(c))
+            out[(static_cast<size_t>(col_token(c)) * H + col_head(c)) * kDv + (e - c * kDv)] = 0;
         }
-        if (lse && tid < HB && hb * HB + tid < H) lse[static_cast<size_t>(t) * H + hb * HB + tid] = -INFINITY;
+        if (lse && tid < HB && col_ok(tid))
+          lse[static_cast<size_t>(col_token(tid)) * H + col_head(tid)] = -INFINITY;
         continue;
       }
-      const int kst = __ldg(ks + t);
-      const int32_t* irow = idx + static_cast<size_t>(t) * topk;
-      float m_used[HB], l_run[HB];
+      // Column max in shared memory (read by all softmax threads); the running sum of this
+      // thread's rows stays in registers and is reduced across rows once per item.
+      if (tid < HB) sh.m_used[tid] = -INFINITY;
+      float lp[HB];
 #pragma unroll
-      for (int h = 0; h < HB; ++h) {
-        m_used[h] = -INFINITY;
-        l_run[h] = 0.f;
+      for (int c = 0; c < HB; ++c) lp[c] = 0.f;
+      const int32_t* irow = idx + static_cast<size_t>(I.t0) * topk;
+      if constexpr (DENSE) {
+        // selection bitmask over the block's key range [lo, lo + nt*64); bits that fall in
+        // the same word are OR-ed across the warp before one shared atomic
+        const int words = I.nt * (kRows / 32);
+        for (int e = tid; e < B * words; e += kSoft) sMask[(e / words) * (C::MAXR / 32) + (e % words)] = 0u;
+        named_bar_sync(1, kSoft);
+        constexpr int kU = 8;     // index loads in flight per thread
+        for (int base = 0; base < B * topk; base += kSoft * kU) {
+          int jv[kU];
+          long long kv0[kU];
+#pragma unroll
+          for (int u = 0; u < kU; ++u) {
+            const int e = base + u * kSoft + tid;
+            const int t = I.t0 + (e < B * topk ? e / topk : 0);
+            const bool in = e < B * topk && t < n_q;
+            jv[u] = in ? __ldg(irow + e) : -1;
+            kv0[u] = in ? static_cast<long long>(__ldg(ks + t)) : 0;
+          }
+#pragma unroll
+          for (int u = 0; u < kU; ++u) {
+            const int e = base + u * kSoft + tid;
+            int word = -1;
+            uint32_t bit = 0u;
+            if (jv[u] >= 0) {
+              const long long row = kv0[u] + jv[u];
+              if (row < 0 || row >= n_kv) {
+                atomicOr(status, DEV_ERR_BAD_INDEX);
+                atomicAdd(bad_count, 1u);
+              } else {
+                const int o = static_cast<int>(row - I.lo);
+                word = (e / topk) * (C::MAXR / 32) + (o >> 5);
+                bit = 1u << (o & 31);
+              }
+            }
+            const uint32_t peers = __match_any_sync(0xffffffffu, word);
+            const uint32_t bits = __reduce_or_sync(peers, bit);
+            if (word >= 0 && lane == __ffs(peers) - 1) atomicOr(&sMask[word], bits);
+          }
+        }
       }
-      for (int i = 0; i < nt; ++i, ++g) {
+      named_bar_sync(1, kSoft);
+      const long long kst = DENSE ? 0 : __ldg(ks + I.t0);
+      for (int i = 0; i < I.nt; ++i, ++g) {
         const int sb = g & 1;
+        int row_j = -1;
+        if constexpr (!DENSE) {
+          const int slot = i * kRows + r;
+          row_j = (row_lane && slot < topk) ? __ldg(irow + slot) : -1;
+        }
         bool ok = mbar_wait(&sh.s_full[sb], (g >> 1) & 1, &sh.abort_flag, status);
         ok = __all_sync(0xffffffffu, ok);
         float sc[HB];
-        bool valid = false;
+        bool need = false;
         if (ok) {
           tc_fence_after();
-          uint32_t raw[HB];
-          if constexpr (HB == 16) {
+#pragma unroll
+          for (int hh = 0; hh < HB / 16; ++hh) {
             uint32_t v16[16];
-            tmem_ld16(tmem + t_lane + C::S_COL + sb * HB, v16);
+            tmem_ld16(tmem + t_lane + C::S_COL + sb * HB + hh * 16, v16);
             tmem_ld_wait();
 #pragma unroll
-            for (int h = 0; h < 16; ++h) raw[h] = v16[h];
-          } else {
-            uint32_t v32[32];
-            tmem_ld32(tmem + t_lane + C::S_COL + sb * HB, v32);
-            tmem_ld_wait();
-#pragma unroll
-            for (int h = 0; h < 32; ++h) raw[h] = v32[h];
+            for (int h = 0; h < 16; ++h) sc[hh * 16 + h] = __uint_as_float(v16[h]);
           }
           tc_fence_before();
           mbar_arrive(&sh.s_empty[sb]);
-          const int slot = i * kRows + r;
-          const int j = (row_lane && slot < topk) ? __ldg(irow + slot) : -1;
-          const long long row = static_cast<long long>(kst) + j;
-          valid = row_lane && j >= 0 && row >= 0 && row < n_kv;
+          bool vb[B];
+          if constexpr (DENSE) {
+            const int o = i * kRows + r;
 #pragma unroll
-          for (int h = 0; h < HB; ++h) sc[h] = valid ? __uint_as_float(raw[h]) * scale_log2 : -INFINITY;
-          // tile max per head over the 64 rows
+            for (int b = 0; b < B; ++b)
+              vb[b] = row_lane && ((sMask[b * (C::MAXR / 32) + (o >> 5)] >> (o & 31)) & 1u);
+          } else {
+            vb[0] = row_lane && row_j >= 0 && kst + row_j < n_kv && kst + row_j >= 0;
+          }
 #pragma unroll
-          for (int h = 0; h < HB; ++h) {
-            float x = sc[h];
-            x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 8));
-            x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 4));
-            x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 2));
-            x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 1));
-            if (lane == 0) sh.red[qd][h] = x;
+          for (int c0 = 0; c0 < HB; c0 += 16) {
+            float mr[16];
+            load_row16(mr, &sh.m_used[c0]);
+#pragma unroll
+            for (int c = c0; c < c0 + 16; ++c) {
+              sc[c] = vb[DENSE ? c / (DENSE ? HD : 1) : 0] ? sc[c] * scale_log2 : -INFINITY;
+              need |= sc[c] > mr[c - c0] + 8.f;   // only a max that grew by > 2^8 forces a rescale
+            }
           }
           // the previous tile's PV must be done before P is overwritten or O^T rescaled
           if (g > 0) {
@@ -231,25 +427,49 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = __all_sync(0xffffffffu, ok);
           }
         }
+        // One barrier-reduction per tile decides whether the slow path runs.  The abort
+        // flag is written before it and read only inside the slow path, between two more
+        // barriers, so every softmax warp takes the same branch.
         if (!ok && lane == 0) sh.soft_abort = 1;
-        named_bar_sync(1, kSoft);
-        stop = sh.soft_abort != 0;
-        float alpha[HB];
-        float ps[HB];
-        if (!stop) {
-          tc_fence_after();
-          bool rescale = false;
+        if (bar_red_or(1, kSoft, need || !ok)) {
+          if (ok) {
 #pragma unroll
-          for (int h = 0; h < HB; ++h) {
-            const float m = fmaxf(fmaxf(sh.red[0][h], sh.red[1][h]), fmaxf(sh.red[2][h], sh.red[3][h]));
-            alpha[h] = 1.f;
-            if (m > m_used[h] + 8.f) {
-              alpha[h] = exp2f(m_used[h] - m);   // 0 when m_used = -inf
-              m_used[h] = m;
-              rescale = true;
+            for (int c = 0; c < HB; ++c) {
+              float x = sc[c];
+              x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 8));
+              x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 4));
+              x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 2));
+              x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 1));
+              if (lane == 0) sh.red[qd][c] = x;
             }
           }
-          if (rescale && i > 0) {
+          named_bar_sync(1, kSoft);
+          stop = sh.soft_abort != 0;
+          if (!stop && tid < HB) {
+            const int c = tid;
+            const float m = fmaxf(fmaxf(sh.red[0][c], sh.red[1][c]), fmaxf(sh.red[2][c], sh.red[3][c]));
+            float a = 1.f;
+            if (m > sh.m_used[c] + 8.f) {
+              a = exp2f(sh.m_used[c] - m);         // 0 when the old max is -inf
+              sh.m_used[c] = m;
+            }
+            sh.alpha[c] = a;
+          }
+          named_bar_sync(1, kSoft);
+          if (stop) break;
+          tc_fence_after();
+          bool any = false;
+#pragma unroll
+          for (int c0 = 0; c0 < HB; c0 += 16) {
+            float ar[16];
+            load_row16(ar, &sh.alpha[c0]);
+#pragma unroll
+            for (int c = c0; c < c0 + 16; ++c) {
+              lp[c] *= ar[c - c0];
+              any |= ar[c - c0] != 1.f;
+            }
+          }
+          if (any && i > 0) {
 #pragma unroll
             for (int b = 0; b < 4; ++b) {
 #pragma unroll
@@ -257,89 +477,88 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t o[16];
                 tmem_ld16(tmem + t_lane + C::O_COL + b * HB + hh * 16, o);
                 tmem_ld_wait();
+                float ar[16];
+                load_row16(ar, &sh.alpha[hh * 16]);
 #pragma unroll
-                for (int h = 0; h < 16; ++h) o[h] = __float_as_uint(__uint_as_float(o[h]) * alpha[hh * 16 + h]);
+                for (int h = 0; h < 16; ++h) o[h] = __float_as_uint(__uint_as_float(o[h]) * ar[h]);
                 tmem_st16(tmem + t_lane + C::O_COL + b * HB + hh * 16, o);
               }
             }
             tmem_st_wait();
           }
-          // P = exp2(s - m) in bf16, written as the K-major B operand of the second product
+        }
+        // P = exp2(s - m) in bf16, written as the K-major B operand of the second product; the
+        // running sums add the same rounded values the tensor core multiplies.
 #pragma unroll
-          for (int h = 0; h < HB; ++h) {
-            const float p = valid ? exp2f(sc[h] - m_used[h]) : 0.f;
+        for (int c0 = 0; c0 < HB; c0 += 16) {
+          float mr[16];
+          load_row16(mr, &sh.m_used[c0]);
+#pragma unroll
+          for (int c = c0; c < c0 + 16; ++c) {
+            const float p = sc[c] == -INFINITY ? 0.f : exp2f(sc[c] - mr[c - c0]);
             const __nv_bfloat16 pb = __float2bfloat16_rn(p);
-            ps[h] = __bfloat162float(pb);
             if (row_lane) {
-              const uint32_t off = (h >> 3) * 1024 + (h & 7) * 128 + ((((r >> 3) ^ (h & 7)) & 7) << 4) + (r & 7) * 2;
-              *reinterpret_cast<__nv_bfloat16*>(sP + off) = pb;
+              const uint32_t off = (c >> 3) * 1024 + (c & 7) * 128 + ((((r >> 3) ^ (c & 7)) & 7) << 4) + (r & 7) * 2;
+              st_shared_u16(sP + off, *reinterpret_cast<const uint16_t*>(&pb));
+              lp[c] += __bfloat162float(pb);
             }
           }
-          fence_proxy_async_smem();
-          tc_fence_before();
-          mbar_arrive(&sh.p_full);
         }
-        named_bar_sync(1, kSoft);      // everyone has read red[] (max) and soft_abort
-        if (stop) break;
-        // row sums per head
-#pragma unroll
-        for (int h = 0; h < HB; ++h) {
-          float x = ps[h];
-          x += __shfl_xor_sync(0xffffffffu, x, 8);
-          x += __shfl_xor_sync(0xffffffffu, x, 4);
-          x += __shfl_xor_sync(0xffffffffu, x, 2);
-          x += __shfl_xor_sync(0xffffffffu, x, 1);
-          if (lane == 0) sh.red[qd][h] = x;
-        }
-        named_bar_sync(1, kSoft);
-#pragma unroll
-        for (int h = 0; h < HB; ++h)
-          l_run[h] = l_run[h] * alpha[h] + ((sh.red[0][h] + sh.red[1][h]) + (sh.red[2][h] + sh.red[3][h]));
-        named_bar_sync(1, kSoft);      // red[] free for the next tile
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&sh.p_full);
       }
       if (stop) break;
-      // epilogue: O^T / l -> out
+      // item end: column sums over the 64 rows, then O^T / l -> out
+#pragma unroll
+      for (int c = 0; c < HB; ++c) {
+        float x = lp[c];
+        x += __shfl_xor_sync(0xffffffffu, x, 8);
+        x += __shfl_xor_sync(0xffffffffu, x, 4);
+        x += __shfl_xor_sync(0xffffffffu, x, 2);
+        x += __shfl_xor_sync(0xffffffffu, x, 1);
+        if (lane == 0) sh.red[qd][c] = x;
+      }
       bool ok = mbar_wait(&sh.o_done, (g - 1) & 1, &sh.abort_flag, status);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok && lane == 0) sh.soft_abort = 1;
       named_bar_sync(1, kSoft);
       stop = sh.soft_abort != 0;
+      if (tid < HB) sh.l_run[tid] = (sh.red[0][tid] + sh.red[1][tid]) + (sh.red[2][tid] + sh.red[3][tid]);
       named_bar_sync(1, kSoft);
       if (stop) break;
       tc_fence_after();
-      float inv[HB];
 #pragma unroll
-      for (int h = 0; h < HB; ++h) inv[h] = l_run[h] > 0.f ? 1.f / l_run[h] : 0.f;
+      for (int hh = 0; hh < HB / 16; ++hh) {
+        float inv[16];
+        load_row16(inv, &sh.l_run[hh * 16]);
 #pragma unroll
-      for (int b = 0; b < 4; ++b) {
+        for (int h = 0; h < 16; ++h) inv[h] = inv[h] > 0.f ? 1.f / inv[h] : 0.f;
 #pragma unroll
-        for (int hh = 0; hh < HB / 16; ++hh) {
+        for (int b = 0; b < 4; ++b) {
           uint32_t o[16];
           tmem_ld16(tmem + t_lane + C::O_COL + b * HB + hh * 16, o);
           tmem_ld_wait();
           const int d = b * 128 + qd * 32 + lane;
 #pragma unroll
           for (int h = 0; h < 16; ++h) {
-            const int head = hb * HB + hh * 16 + h;
-            if (head < H) {
-              const __nv_bfloat16 ob = __float2bfloat16_rn(__uint_as_float(o[h]) * inv[hh * 16 + h]);
-              out[(static_cast<size_t>(t) * H + head) * kDv + d] = *reinterpret_cast<const uint16_t*>(&ob);
+            const int c = hh * 16 + h;
+            if (col_ok(c)) {
+              const __nv_bfloat16 ob = __float2bfloat16_rn(__uint_as_float(o[h]) * inv[h]);
+              st_global_u16(out + (static_cast<size_t>(col_token(c)) * H + col_head(c)) * kDv + d,
+                            *reinterpret_cast<const uint16_t*>(&ob));
             }
           }
         }
       }
-      if (lse && tid < HB && hb * HB + tid < H) {
-        float mv = 0.f, lv = 0.f;
-#pragma unroll
-        for (int h = 0; h < HB; ++h)
-          if (h == tid) {
-            mv = m_used[h];
-            lv = l_run[h];
-          }
-        lse[static_cast<size_t>(t) * H + hb * HB + tid] = lv > 0.f ? (mv + log2f(lv)) * 0.69314718055994531f : -INFINITY;
+      if (lse && tid < HB && col_ok(tid)) {
+        const float lv = sh.l_run[tid];
+        lse[static_cast<size_t>(col_token(tid)) * H + col_head(tid)] =
+            lv > 0.f ? (sh.m_used[tid] + log2f(lv)) * 0.69314718055994531f : -INFINITY;
       }
       tc_fence_before();
       mbar_arrive(&sh.o_free);
+      named_bar_sync(1, kSoft);                                 // per-column state and mask may be reset now
       ++it;
     }
   } else {
@@ -365,13 +584,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_commit(&sh.s_full[sb]);
         return true;
       };
-      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-        const int t = item / n_hb;
-        const int nt = __ldg(row_nt + t);
-        if (nt == 0) continue;
-        ok = issue_qk(g);
-        for (int i = 0; i < nt && ok; ++i, ++g) {
-          if (i + 1 < nt) ok = issue_qk(g + 1);
+      for (int k = 0; k * static_cast<int>(gridDim.x) < n_items && ok; ++k) {
+        const int item = snake_item(k);
+        if (item >= n_items) continue;
+        const Item I = item_info<HB, HD>(item, n_hb, row_nt, block_range);
+        if (I.nt == 0) continue;
+        ok = mbar_wait(&sh.q_full, it & 1, &sh.abort_flag, status);
+        if (ok) ok = issue_qk(g);
+        for (int i = 0; i < I.nt && ok; ++i, ++g) {
+          if (i + 1 < I.nt) ok = issue_qk(g + 1);
           else umma_commit(&sh.q_empty);
           if (!ok) break;
           ok = mbar_wait(&sh.p_full, g & 1, &sh.abort_flag, status);
@@ -396,7 +617,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 8) tmem_dealloc(tmem, C::TMEM_COLS);
+  if (warp == 7) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
 // row_nt[t] = number of 64-slot tiles up to the last slot holding an index >= 0.
@@ -414,33 +635,101 @@ __global__ void __launch_bounds__(256) row_tiles_kernel(const int32_t* __restric
   if (lane == 0) row_nt[t] = (last + kRows) / kRows;
 }
 
-template <int HB>
-cudaError_t launch_hb(int n_q, int n_kv, int H, int topk, float scale, const void* q, const void* kv,
-                      const int32_t* idx, const int32_t* ks, const int32_t* row_nt, void* out, float* lse,
-                      uint32_t* status, cudaStream_t st) {
-  using C = ACfg<HB>;
-  auto kern = sparse_attn_kernel<HB>;
+// block_range[b] = [min, max + 1) of the in-range latent rows selected by tokens
+// [b*B, b*B + B); (0, 0) when none.  One warp per block.
+__global__ void __launch_bounds__(256) block_range_kernel(const int32_t* __restrict__ idx,
+                                                          const int32_t* __restrict__ ks, int n_q, int n_kv,
+                                                          int topk, int B, int2* __restrict__ block_range) {
+  const int blk = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const int n_blk = (n_q + B - 1) / B;
+  if (blk >= n_blk) return;
+  int lo = 0x7FFFFFFF, hi = -1;
+  for (int b = 0; b < B; ++b) {
+    const int t = blk * B + b;
+    if (t >= n_q) break;
+    const long long kst = __ldg(ks + t);
+    const int32_t* irow = idx + static_cast<size_t>(t) * topk;
+    for (int s = lane; s < topk; s += 32) {
+      const int j = __ldg(irow + s);
+      const long long row = kst + j;
+      if (j >= 0 && row >= 0 && row < n_kv) {
+        lo = min(lo, static_cast<int>(row));
+        hi = max(hi, static_cast<int>(row));
+      }
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, off));
+    hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, off));
+  }
+  if (lane == 0) block_range[blk] = hi >= lo ? make_int2(lo, hi + 1) : make_int2(0, 0);
+}
+
+template <int HB, int HD>
+cudaError_t launch_cfg(const CUtensorMap& tmap, int n_q, int n_kv, int H, int topk, float scale, const void* q,
+                       const void* kv, const int32_t* idx, const int32_t* ks, const int32_t* row_nt,
+                       const int2* block_range, void* out, float* lse, uint32_t* status, cudaStream_t st) {
+  using C = ACfg<HB, HD>;
+  auto kern = sparse_attn_kernel<HB, HD>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::DYN_SMEM);
   if (e != cudaSuccess) return e;
-  const int n_items = n_q * ((H + HB - 1) / HB);
+  const int n_items = C::DENSE ? (n_q + C::B - 1) / C::B : n_q * ((H + HB - 1) / HB);
   const int grid = n_items < device_sm_count() ? n_items : device_sm_count();
-  kern<<<grid, kThreads, C::DYN_SMEM, st>>>(static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(kv), idx, ks,
-                                            row_nt, static_cast<uint16_t*>(out), lse, n_q, n_kv, H, topk,
-                                            scale * 1.4426950408889634f, status, status + 1);
+  kern<<<grid, kThreads, C::DYN_SMEM, st>>>(tmap, static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(kv),
+                                            idx, ks, row_nt, block_range, static_cast<uint16_t*>(out), lse, n_q, n_kv,
+                                            H, topk, scale * 1.4426950408889634f, status, status + 1);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_sparse_attn(int n_q, int n_kv, int n_heads, int topk, float scale, const void* q, const void* kv,
-                               const int32_t* idx, const int32_t* ks, void* out, float* lse, uint32_t* status,
-                               int32_t* row_nt, cudaStream_t st) {
+int sparse_attn_dense_heads(int n_heads, int n_kv, int topk) {
+  // block-dense walk pays off when each row of the block's key range is selected by
+  // several of the block's tokens; it needs the whole range to fit the selection mask.
+  if (n_heads != 1 && n_heads != 2 && n_heads != 4 && n_heads != 8 && n_heads != 16) return 0;
+  const int B = kDenseCols / n_heads;
+  const int maxr = (kMaskBytes * 8 / B) / 64 * 64;
+  if (n_kv > maxr) return 0;
+  if (2LL * B * topk < n_kv) return 0;
+  return n_heads;
+}
+
+size_t sparse_attn_ws_bytes(int n_q, int n_heads, int n_kv, int topk) {
+  const int hd = sparse_attn_dense_heads(n_heads, n_kv, topk);
+  if (hd) return static_cast<size_t>((n_q + kDenseCols / hd - 1) / (kDenseCols / hd)) * sizeof(int2);
+  return static_cast<size_t>(n_q) * sizeof(int32_t);
+}
+
+cudaError_t launch_sparse_attn(const CUtensorMap& tmap_kv, int n_q, int n_kv, int n_heads, int topk, float scale,
+                               const void* q, const void* kv, const int32_t* idx, const int32_t* ks, void* out,
+                               float* lse, uint32_t* status, void* scratch, cudaStream_t st) {
   if (n_q <= 0) return cudaSuccess;
+  const int hd = sparse_attn_dense_heads(n_heads, n_kv, topk);
+  cudaError_t e;
+  if (hd) {
+    const int B = kDenseCols / hd;
+    const int n_blk = (n_q + B - 1) / B;
+    int2* br = static_cast<int2*>(scratch);
+    block_range_kernel<<<(n_blk + 7) / 8, 256, 0, st>>>(idx, ks, n_q, n_kv, topk, B, br);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    switch (hd) {
+      case 1: return launch_cfg<48, 1>(tmap_kv, n_q, n_kv, n_heads, topk, scale, q, kv, idx, ks, nullptr, br, out, lse, status, st);
+      case 2: return launch_cfg<48, 2>(tmap_kv, n_q, n_kv, n_heads, topk, scale, q, kv, idx, ks, nullptr, br, out, lse, status, st);
+      case 4: return launch_cfg<48, 4>(tmap_kv, n_q, n_kv, n_heads, topk, scale, q, kv, idx, ks, nullptr, br, out, lse, status, st);
+      case 8: return launch_cfg<48, 8>(tmap_kv, n_q, n_kv, n_heads, topk, scale, q, kv, idx, ks, nullptr, br, out, lse, status, st);
+      default: return launch_cfg<48, 16>(tmap_kv, n_q, n_kv, n_heads, topk, scale, q, kv, idx, ks, nullptr, br, out, lse, status, st);
+    }
+  }
+  int32_t* row_nt = static_cast<int32_t*>(scratch);
   row_tiles_kernel<<<(n_q + 7) / 8, 256, 0, st>>>(idx, n_q, topk, row_nt);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  if (n_heads <= 16) return launch_hb<16>(n_q, n_kv, n_heads, topk, scale, q, kv, idx, ks, row_nt, out, lse, status, st);
-  return launch_hb<32>(n_q, n_kv, n_heads, topk, scale, q, kv, idx, ks, row_nt, out, lse, status, st);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (n_heads <= 16)
+    return launch_cfg<16, 0>(tmap_kv, n_q, n_kv, n_heads, topk, scale, q, kv, idx, ks, row_nt, nullptr, out, lse, status, st);
+  if (n_heads <= 32)
+    return launch_cfg<32, 0>(tmap_kv, n_q, n_kv, n_heads, topk, scale, q, kv, idx, ks, row_nt, nullptr, out, lse, status, st);
+  return launch_cfg<64, 0>(tmap_kv, n_q, n_kv, n_heads, topk, scale, q, kv, idx, ks, row_nt, nullptr, out, lse, status, st);
 }
 
 }  // namespace dsa

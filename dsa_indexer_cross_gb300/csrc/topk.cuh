@@ -48,6 +48,14 @@ __device__ __forceinline__ void find_bin(const uint32_t* hist, int need, int* bc
   }
 }
 
+// Histogram increment aggregated over the lanes of a warp that hit the same bin (scores
+// cluster in few high-order bins, so plain shared atomics would serialise).
+__device__ __forceinline__ void hist_add(uint32_t* hist, uint32_t bin) {
+  const uint32_t act = __activemask();
+  const uint32_t peers = __match_any_sync(act, bin);
+  if ((threadIdx.x & 31u) == static_cast<uint32_t>(__ffs(peers) - 1)) atomicAdd(&hist[bin], __popc(peers));
+}
+
 // `sync()` synchronises the NT cooperating threads; `tid` is this thread's rank in
 // [0, NT) with rank 0..31 forming one warp.  `fe(f)` calls f(key, idx) for every entry
 // this thread owns.  hist: 256 words of shared memory; bc: 4 ints of shared memory.
@@ -61,7 +69,7 @@ __device__ void radix_threshold(const Sync& sync, const ForEach& fe, int tid, in
     for (int i = tid; i < 256; i += NT) hist[i] = 0;
     sync();
     fe([&](uint32_t key, int32_t) {
-      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+      if ((key & mask) == prefix) hist_add(hist, (key >> shift) & 255u);
     });
     sync();
     if (tid < 32) find_bin<true>(hist, need, bc);
@@ -85,7 +93,7 @@ __device__ void radix_threshold(const Sync& sync, const ForEach& fe, int tid, in
     sync();
     fe([&](uint32_t key, int32_t idx) {
       const uint32_t u = static_cast<uint32_t>(idx);
-      if (key == prefix && (u & m2) == p2) atomicAdd(&hist[(u >> shift) & 255u], 1u);
+      if (key == prefix && (u & m2) == p2) hist_add(hist, (u >> shift) & 255u);
     });
     sync();
     if (tid < 32) find_bin<false>(hist, need, bc);

@@ -162,7 +162,9 @@ dsa_status dsa_sparse_attn_workspace_size(const dsa_attn_desc* desc, size_t* byt
  *   o[t, h]   = sum_{j in I_t} softmax_j(tau * q[t, h] . kv[ks_t + j]) * kv[ks_t + j, :d_v]
  *   lse[t, h] = log sum_{j in I_t} exp(tau * q[t, h] . kv[ks_t + j])
  *
- * with I_t the entries of idx[t] that are >= 0.  All heads of a token read the same rows.
+ * with I_t the entries of idx[t] that are >= 0, which must be distinct (as the indexer's
+ * rows are); repeated offsets in one row are not supported.  All heads of a token read the
+ * same rows.
  *   q   bf16 [n_q][n_heads][d_qk]     kv  bf16 [n_kv][d_qk]
  *   idx int32 [n_q][topk]  offsets relative to ks_t, -1 = unused slot
  *   ks  int32 [n_q]

@@ -27,6 +27,8 @@ def check_topk_row(gpu_row: np.ndarray, scores: np.ndarray, k: int, oracle_row: 
         return "-1 padding not confined to the tail"
     if np.unique(valid).size != valid.size:
         return "duplicate offsets"
+    if np.any(np.diff(valid) <= 0):
+        return "offsets not in ascending order"
     if valid.size and (valid.min() < 0 or valid.max() >= L):
         return f"offset outside [0, {L})"
     if kt == L:

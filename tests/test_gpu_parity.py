@@ -18,7 +18,11 @@ from parity import check_topk
 pytestmark = pytest.mark.gpu
 
 ATOL_OUT = 1e-2
-ATOL_LSE = 1e-3
+# The softmax weights enter the second product as bf16 (relative rounding <= 2^-9) and the
+# denominator sums those same rounded weights, so the log-sum-exp the kernel reports is
+# log(sum of rounded weights): within log(1 + 2^-9) ~ 2e-3 of the exact value, plus fp32
+# accumulation error.  4e-3 leaves a factor 2.
+ATOL_LSE = 4e-3
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -41,7 +45,8 @@ def _check_indexer(w, geo, L, rows):
         sel = idx_np[t][idx_np[t] >= 0]
         ref = score_rows[n][sel]
         got = sc_np[t][: sel.size]
-        np.testing.assert_allclose(got, ref, rtol=2e-3, atol=2e-3 * (np.abs(ref).max() + 1e-30))
+        if sel.size:
+            np.testing.assert_allclose(got, ref, rtol=2e-3, atol=2e-3 * (np.abs(ref).max() + 1e-30))
         assert np.all(np.isneginf(sc_np[t][sel.size:]))
     return idx
 
@@ -114,7 +119,7 @@ def test_attention_head_blocks_and_bad_indices(H):
     rng = np.random.default_rng(H)
     n_q, n_kv, topk = 9, 700, 200
     ks = rng.integers(0, 100, n_q).astype(np.int32)
-    idx = rng.integers(0, 600, (n_q, topk)).astype(np.int32)
+    idx = np.stack([rng.permutation(600)[:topk] for _ in range(n_q)]).astype(np.int32)   # distinct offsets
     idx[rng.random((n_q, topk)) < 0.2] = -1          # scattered unused slots
     idx[2, :] = -1                                   # a row with nothing selected
     idx[3, 150:] = -1                                # a ragged row
@@ -166,3 +171,23 @@ def test_layers_forward_against_oracle(name):
         e_o, e_l = attn_errors(layers[l]["out"], layers[l]["lse"], o_ref, lse_ref, rows)
         assert e_o <= ATOL_OUT and e_l <= ATOL_LSE, (l, e_o, e_l)
     cache.close()
+
+
+@pytest.mark.parametrize("H", [4, 16])
+def test_attention_gather_walk_for_small_heads(H):
+    # a long key range with a short index row takes the per-token gather walk
+    rng = np.random.default_rng(100 + H)
+    n_q, n_kv, topk = 37, 5000, 128
+    ks = rng.integers(0, 1000, n_q).astype(np.int32)
+    idx = np.stack([rng.permutation(3900)[:topk] for _ in range(n_q)]).astype(np.int32)
+    idx[rng.random((n_q, topk)) < 0.1] = -1
+    idx[5, :] = -1
+    geo = synth.Geometry(n_kv, np.zeros(n_q, np.int32), np.zeros(n_kv, np.int32), ks, ks)
+    w = synth.Workload("gather", "prefill", n_q, ("full", "shared"), 4, 64, 0, 1e4, topk, H)
+    L = synth.layer_inputs(w, geo, 1, device=DEV, attn_scale="unit")
+    out, lse, bits = run_attn(w, geo, L, torch.from_numpy(idx).to(DEV))
+    assert bits == 0
+    o_ref, lse_ref = oracle_attn(w, geo, L, idx, range(n_q))
+    e_o, e_l = attn_errors(out, lse, o_ref, lse_ref, range(n_q))
+    assert e_o <= ATOL_OUT and e_l <= ATOL_LSE, (e_o, e_l)
+    assert torch.all(out[5] == 0) and torch.all(torch.isneginf(lse[5]))

@@ -7,6 +7,7 @@ from parity import check_topk_row
 def test_exact_set_required_when_gap_is_clear():
     s = np.array([5.0, 4.0, 3.0, 1.0, 0.5])
     assert check_topk_row(np.array([0, 1, 2]), s, 3) is None
+    assert check_topk_row(np.array([1, 0, 2]), s, 3) is not None      # rows are sorted ascending
     assert check_topk_row(np.array([0, 1, 3]), s, 3) is not None
 
 
