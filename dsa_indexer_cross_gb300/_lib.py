@@ -27,7 +27,8 @@ STATUS_NAMES = {0: "DSA_OK", 1: "DSA_ERR_ARG", 2: "DSA_ERR_SHAPE", 3: "DSA_ERR_N
 EXPORTED = ("dsa_status_string", "dsa_last_error", "dsa_donor_table", "dsa_rope_table", "dsa_indexer_workspace_size",
             "dsa_indexer_topk", "dsa_sparse_attn_workspace_size", "dsa_sparse_attn", "dsa_index_cache_create",
             "dsa_index_cache_donor", "dsa_index_cache_indices", "dsa_index_cache_destroy",
-            "dsa_layers_workspace_size", "indexshare_layers_forward", "dsa_workspace_status")
+            "dsa_layers_workspace_size", "indexshare_layers_forward", "dsa_workspace_status",
+            "dsa_indexer_topk_static")
 
 
 class DsaError(RuntimeError):
@@ -94,6 +95,8 @@ def lib() -> C.CDLL:
                                                 vp, vp, vp, i32, vp, vp, sz, vp]
         L.dsa_workspace_status.restype = st
         L.dsa_workspace_status.argtypes = [vp, vp, P(u32)]
+        L.dsa_indexer_topk_static.restype = st
+        L.dsa_indexer_topk_static.argtypes = [P(IndexerDesc), vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp]
         _lib = L
     return _lib
 
@@ -170,6 +173,15 @@ def dsa_indexer_topk(desc: IndexerDesc, q_idx, k_idx, w, q_pos, k_pos, ks, ke, r
                                   _ptr(ks), _ptr(ke), _ptr(rope_cs), n_pos, _ptr(idx_out), _ptr(score_out),
                                   _ptr(ws), ws.numel(), _stream(stream)))
     return ws
+
+
+def dsa_indexer_topk_static(desc: IndexerDesc, q_idx, k_idx, w, q_pos, k_pos, ks, ke, rope_cs, idx_out,
+                            score_out=None, stream=None) -> None:
+    """dsa_indexer_topk with the library's static device scratch instead of a workspace."""
+    n_pos = rope_cs.shape[0] if rope_cs is not None else 0
+    _check(lib().dsa_indexer_topk_static(C.byref(desc), _ptr(q_idx), _ptr(k_idx), _ptr(w), _ptr(q_pos), _ptr(k_pos),
+                                         _ptr(ks), _ptr(ke), _ptr(rope_cs), n_pos, _ptr(idx_out), _ptr(score_out),
+                                         _stream(stream)))
 
 
 # ------------------------------------------------------------------------------ attention

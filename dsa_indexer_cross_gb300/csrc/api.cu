@@ -290,7 +290,23 @@ dsa_status run_attn(const dsa_attn_desc* d, const void* q, const void* kv, const
 
 int device_sm_count() { return dev_info().sms; }
 
+dsa_status indexer_workspace_bytes(const dsa_indexer_desc* d, size_t* bytes) {
+  dsa_status s = check_indexer_desc(d);
+  if (s != DSA_OK) return s;
+  const DevInfo di = dev_info();
+  *bytes = indexer_layout(d, di.sms > 0 ? di.sms : 148).total;
+  return DSA_OK;
+}
 
+dsa_status indexer_run(const dsa_indexer_desc* d, const void* q_idx, const void* k_idx, const float* w,
+                       const int32_t* q_pos, const int32_t* k_pos, const int32_t* ks, const int32_t* ke,
+                       const float* rope_cs, int32_t rope_n_pos, int32_t* idx_out, float* score_out, void* ws,
+                       size_t ws_bytes, cudaStream_t st) {
+  return run_indexer(d, q_idx, k_idx, w, q_pos, k_pos, ks, ke, rope_cs, rope_n_pos, idx_out, score_out, ws, ws_bytes,
+                     st, true);
+}
+
+dsa_status set_error(dsa_status s, const char* msg) { return fail(s, "%s", msg); }
 
 }  // namespace dsa
 

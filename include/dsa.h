@@ -140,6 +140,26 @@ dsa_status dsa_indexer_topk(const dsa_indexer_desc* desc, const void* q_idx, con
                             const float* rope_cs, int32_t rope_n_pos, int32_t* idx_out, float* score_out, void* ws,
                             size_t ws_bytes, void* stream);
 
+/* Indexer + top-k for callers that cannot allocate device memory.  The pages have no
+ * counterpart to this entry point; it exists for callers that cannot hand the library a
+ * workspace -- for example a plugin that a host framework calls with only its input and
+ * output buffers (the framework owns the device allocator), or a latency-critical loop in
+ * which a cudaMalloc and its implicit synchronisation are not acceptable.
+ * Same arguments, results and errors as dsa_indexer_topk, minus ws / ws_bytes.  Scratch
+ * comes from one file-scope device array of DSA_STATIC_SCRATCH_BYTES held on every GPU
+ * that uses this call until the process exits; no allocation routine is called.  The first
+ * call on a device (with that device current) looks up the array's address once; make that
+ * call before any stream capture.  Problems that need more scratch than the array holds are
+ * rejected with DSA_ERR_WORKSPACE.  All calls on a device share the array: calls whose work
+ * overlaps on the GPU race and must be serialised by the caller.  The status word that
+ * dsa_workspace_status reads is not exposed for this variant; device-side faults are still
+ * recorded in the array and cleared at the start of the next call. */
+#define DSA_STATIC_SCRATCH_BYTES (32u << 20)
+dsa_status dsa_indexer_topk_static(const dsa_indexer_desc* desc, const void* q_idx, const void* k_idx, const float* w,
+                                   const int32_t* q_pos, const int32_t* k_pos, const int32_t* ks, const int32_t* ke,
+                                   const float* rope_cs, int32_t rope_n_pos, int32_t* idx_out, float* score_out,
+                                   void* stream);
+
 /* ------------------------------------------------------------------ sparse attention - */
 
 typedef struct dsa_attn_desc {
