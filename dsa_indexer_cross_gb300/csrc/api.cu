@@ -148,7 +148,7 @@ IndexerLayout indexer_layout(const dsa_indexer_desc* d, int sms) {
   chunk = (chunk + 127) / 128 * 128;
   p.chunk = static_cast<int>(chunk);
   p.n_chunks = static_cast<int>((max_len + chunk - 1) / chunk);
-  const int cap0 = d->topk * 2 > d->topk + 128 ? d->topk * 2 : d->topk + 128;
+  const int cap0 = 2 * d->topk + 128;   // rows of up to 2k keys never need a cut-back
   p.cap = (cap0 + 127) / 128 * 128;
   const long long units = static_cast<long long>(p.n_groups) * p.n_chunks;
   p.grid = static_cast<int>(units < sms ? units : sms);
@@ -218,7 +218,9 @@ dsa_status run_indexer(const dsa_indexer_desc* d, const void* q_idx, const void*
   const IndexerPlan& p = L.plan;
   int2* rr = reinterpret_cast<int2*>(base + L.off_rr);
   int2* gr = reinterpret_cast<int2*>(base + L.off_gr);
-  e = launch_ranges(ks, ke, d->n_q, p.group, d->n_kv, d->max_len, rr, gr, status, st);
+  // rows whose whole range fits in k keep every key; without requested scores they need no scoring
+  const int trivial_len = score_out ? 0 : d->topk;
+  e = launch_ranges(ks, ke, d->n_q, p.group, d->n_kv, d->max_len, trivial_len, rr, gr, status, st);
   if (e != cudaSuccess) return cuda_fail(e, "key ranges");
   uint32_t* cnt = reinterpret_cast<uint32_t*>(base + L.off_cnt);
   uint32_t* ck = reinterpret_cast<uint32_t*>(base + L.off_key);
@@ -235,7 +237,7 @@ dsa_status run_indexer(const dsa_indexer_desc* d, const void* q_idx, const void*
     if ((e = cudaMemsetAsync(cnt, 0, static_cast<size_t>(d->n_q) * p.n_chunks * 4, st)) != cudaSuccess)
       return cuda_fail(e, "clear counts");
   }
-  e = launch_select(d->n_q, p.n_chunks, p.cap, d->topk, rr, ck, ci, cnt, idx_out, score_out, status, st);
+  e = launch_select(d->n_q, p.n_chunks, p.cap, d->topk, trivial_len, rr, ck, ci, cnt, idx_out, score_out, status, st);
   if (e != cudaSuccess) return cuda_fail(e, "top-k select");
   return DSA_OK;
 }

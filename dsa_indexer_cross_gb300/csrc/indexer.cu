@@ -38,7 +38,7 @@ namespace {
 constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
 constexpr int kKeyTile = 128;
-constexpr int kMaxPer = 32;  // cap / kEpiThreads <= 32  (cap <= 4096)
+constexpr int kMaxPer = 33;  // ceil(cap / kEpiThreads) with cap = 2k + 128 <= 4224
 
 template <int HI, int DI, int G>
 struct Cfg {
@@ -68,10 +68,21 @@ struct Shared {
   int warp_off[4];
   uint32_t tau[64];
   int cnt[2][64];        // candidates held per query; [tile parity] so a tile reads one copy and writes the other
-  int qcnt[64][4];       // this tile's appends per (query, TMEM lane quarter)
+  alignas(16) int qcnt[4][64];   // this tile's appends per (TMEM lane quarter, query)
   int epi_abort;
 };
 static_assert(offsetof(Shared, w_s) % 16 == 0, "float4 access");
+
+// Named barrier over n threads that also returns the OR of a predicate across them.
+__device__ __forceinline__ bool bar_red_or(uint32_t id, uint32_t n, bool p) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %1, 0;\n bar.red.or.pred po, %2, %3, pi;\n selp.u32 %0, 1, 0, po;\n}\n"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(p)), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
 
 __device__ __forceinline__ void st_global_u32(uint32_t* p, uint32_t v) {
   asm volatile("{\n .reg .u64 ga;\n cvta.to.global.u64 ga, %0;\n st.global.u32 [ga], %1;\n}\n" ::"l"(p), "r"(v) : "memory");
@@ -336,39 +347,50 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int2 rr = sh.rr[g];
             key[g] = float_key(acc[g]);
             msk[g] = __ballot_sync(0xffffffffu, j >= rr.x && j < rr.y && j < ui.kend && key[g] > sh.tau[g]);
-            if (lane == 0) sh.qcnt[g][quarter] = __popc(msk[g]);
           }
-        } else if (lane == 0) {
-          sh.epi_abort = 1;
+          if (lane == 0) {
+#pragma unroll
+            for (int g = 0; g < G; ++g) sh.qcnt[quarter][g] = __popc(msk[g]);
+          }
         }
-        named_bar_sync(1, kEpiThreads);
+        named_bar_sync(1, kEpiThreads);                       // X: per-quarter counts published
         const int cur = tile & 1, nxt = cur ^ 1;
+        bool need = false;
         if (ok) {
           const int j = ui.kbeg + i * kKeyTile + row;
           // every query's write offset first (shared loads only), then the global stores
           int pos[G];
 #pragma unroll
-          for (int g = 0; g < G; ++g) {
-            int p0 = sh.cnt[cur][g] + __popc(msk[g] & ((1u << lane) - 1u));
-            for (int q = 0; q < quarter; ++q) p0 += sh.qcnt[g][q];
-            pos[g] = p0;
+          for (int g = 0; g < G; ++g) pos[g] = sh.cnt[cur][g] + __popc(msk[g] & ((1u << lane) - 1u));
+          for (int q = 0; q < quarter; ++q) {
+#pragma unroll
+            for (int g = 0; g < G; ++g) pos[g] += sh.qcnt[q][g];
           }
           int tot = 0;
-          if (tid < G) tot = (sh.qcnt[tid][0] + sh.qcnt[tid][1]) + (sh.qcnt[tid][2] + sh.qcnt[tid][3]);
+          if (tid < G) tot = (sh.qcnt[0][tid] + sh.qcnt[1][tid]) + (sh.qcnt[2][tid] + sh.qcnt[3][tid]);
+          const size_t rowbase = (static_cast<size_t>(t0) * n_chunks + ui.chunk) * cap;
 #pragma unroll
           for (int g = 0; g < G; ++g) {
             if (((msk[g] >> lane) & 1u) && pos[g] < cap) {
-              const size_t off = (static_cast<size_t>(t0 + g) * n_chunks + ui.chunk) * cap + pos[g];
+              const size_t off = rowbase + static_cast<size_t>(g) * n_chunks * cap + pos[g];
               st_global_u32(cand_key + off, key[g]);
               st_global_u32(reinterpret_cast<uint32_t*>(cand_idx) + off, static_cast<uint32_t>(j));
             }
           }
-          if (tid < G) sh.cnt[nxt][tid] = sh.cnt[cur][tid] + tot;
+          if (tid < G) {
+            const int n = sh.cnt[cur][tid] + tot;
+            sh.cnt[nxt][tid] = n;
+            need = n > cap - kKeyTile;                      // could overflow on the next tile
+          }
         }
-        named_bar_sync(1, kEpiThreads);
-        stop = sh.epi_abort != 0;
-        if (!stop) {
-          // cut back buffers that could overflow on the next tile
+        // Y: one barrier-reduction decides whether anything beyond the appends is needed (a
+        // cut-back or an abort).  The abort flag is written before it and read only in the
+        // slow path, between it and one more barrier, so all epilogue warps branch alike.
+        if (!ok && lane == 0) sh.epi_abort = 1;
+        if (bar_red_or(1, kEpiThreads, need || !ok)) {
+          stop = sh.epi_abort != 0;
+          named_bar_sync(1, kEpiThreads);
+          if (stop) break;
 #pragma unroll 1
           for (int g = 0; g < G; ++g) {
             const int n = sh.cnt[nxt][g];
@@ -384,8 +406,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        named_bar_sync(1, kEpiThreads);
-        if (stop) break;
       }
       if (stop) break;
       if (tid < G && t0 + tid < n_q)

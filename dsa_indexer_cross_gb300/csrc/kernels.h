@@ -30,9 +30,11 @@ struct IndexerPlan {
   int topk;
 };
 
-// Fills row_range[t] = (ks, ke) when valid, else (0, 0) and flags; group_range[g] = union.
+// Fills row_range[t] = (ks, ke) when valid, else (0, 0) and flags; group_range[g] = union of
+// the ranges of the group's rows longer than trivial_len (shorter rows keep every key and are
+// not scored).
 cudaError_t launch_ranges(const int32_t* ks, const int32_t* ke, int n_q, int group, int n_kv, int max_len,
-                          int2* row_range, int2* group_range, uint32_t* status, cudaStream_t st);
+                          int trivial_len, int2* row_range, int2* group_range, uint32_t* status, cudaStream_t st);
 
 // Scores + streaming top-k candidates.  tmap_q covers rotated q as [(n_q*H_I) x d_I] bf16,
 // tmap_k covers rotated k as [n_kv x d_I] bf16, both 128-byte swizzled, boxes {64, N} and
@@ -42,7 +44,9 @@ cudaError_t launch_indexer(const IndexerPlan& p, const CUtensorMap& tmap_q, cons
                            int32_t* cand_idx, uint32_t* cand_cnt, uint32_t* status, cudaStream_t st);
 
 // Exact top-k of every row from its candidates; writes offsets (ascending) and -1 padding.
-cudaError_t launch_select(int n_q, int n_chunks, int cap, int topk, const int2* row_range, const uint32_t* cand_key,
+// Rows of at most trivial_len keys are written as 0..L-1 without reading candidates.
+cudaError_t launch_select(int n_q, int n_chunks, int cap, int topk, int trivial_len, const int2* row_range,
+                          const uint32_t* cand_key,
                           const int32_t* cand_idx, const uint32_t* cand_cnt, int32_t* idx_out, float* score_out,
                           uint32_t* status, cudaStream_t st);
 

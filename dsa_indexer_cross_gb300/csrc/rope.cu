@@ -108,8 +108,8 @@ __global__ void __launch_bounds__(256) rope_rows_scalar(const uint16_t* __restri
 }
 
 __global__ void __launch_bounds__(256) ranges_kernel(const int32_t* __restrict__ ks, const int32_t* __restrict__ ke,
-                                                     int n_q, int group, int n_kv, int max_len, int2* row_range,
-                                                     int2* group_range, uint32_t* status) {
+                                                     int n_q, int group, int n_kv, int max_len, int trivial_len,
+                                                     int2* row_range, int2* group_range, uint32_t* status) {
   const int g = blockIdx.x * blockDim.x + threadIdx.x;
   const int n_groups = (n_q + group - 1) / group;
   if (g >= n_groups) return;
@@ -121,8 +121,10 @@ __global__ void __launch_bounds__(256) ranges_kernel(const int32_t* __restrict__
       atomicOr(status, DEV_ERR_RANGE);
     } else if (b > a) {
       r = make_int2(a, b);
-      lo = min(lo, a);
-      hi = max(hi, b);
+      if (b - a > trivial_len) {
+        lo = min(lo, a);
+        hi = max(hi, b);
+      }
     }
     row_range[t] = r;
   }
@@ -152,11 +154,11 @@ cudaError_t launch_rope_rows(const void* in, void* out, const int32_t* pos, int6
 }
 
 cudaError_t launch_ranges(const int32_t* ks, const int32_t* ke, int n_q, int group, int n_kv, int max_len,
-                          int2* row_range, int2* group_range, uint32_t* status, cudaStream_t st) {
+                          int trivial_len, int2* row_range, int2* group_range, uint32_t* status, cudaStream_t st) {
   const int n_groups = (n_q + group - 1) / group;
   if (n_groups <= 0) return cudaSuccess;
-  ranges_kernel<<<(n_groups + 255) / 256, 256, 0, st>>>(ks, ke, n_q, group, n_kv, max_len, row_range, group_range,
-                                                        status);
+  ranges_kernel<<<(n_groups + 255) / 256, 256, 0, st>>>(ks, ke, n_q, group, n_kv, max_len, trivial_len, row_range,
+                                                        group_range, status);
   return cudaGetLastError();
 }
 

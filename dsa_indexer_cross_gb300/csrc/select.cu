@@ -16,11 +16,11 @@ namespace dsa {
 namespace {
 
 constexpr int kSelThreads = 256;
-constexpr int kSelPer = 16;    // entries per thread kept in registers (rows up to 4096 candidates)
+constexpr int kSelPer = 17;    // entries per thread kept in registers (rows up to 4352 candidates)
 constexpr int kMaxChunks = 64;
 
 template <bool kRegs>
-__global__ void __launch_bounds__(kSelThreads) select_kernel(int n_chunks, int cap, int topk,
+__global__ void __launch_bounds__(kSelThreads) select_kernel(int n_chunks, int cap, int topk, int trivial_len,
                                                              const int2* __restrict__ row_range,
                                                              const uint32_t* __restrict__ cand_key,
                                                              const int32_t* __restrict__ cand_idx,
@@ -34,6 +34,18 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(int n_chunks, int c
   const int t = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int2 r = row_range[t];
+  if (r.y - r.x <= trivial_len) {
+    // the whole range is selected: offsets 0 .. L-1 in order, no candidates read.  The host
+    // passes trivial_len = 0 whenever scores are requested, so only empty rows get here then.
+    int32_t* out = idx_out + static_cast<size_t>(t) * topk;
+    float* so = score_out ? score_out + static_cast<size_t>(t) * topk : nullptr;
+    const int L = r.y - r.x;
+    for (int i = tid; i < topk; i += kSelThreads) {
+      out[i] = i < L ? i : -1;
+      if (so) so[i] = -__int_as_float(0x7f800000);
+    }
+    return;
+  }
   const size_t base = static_cast<size_t>(t) * n_chunks * cap;
   const uint32_t* cnt_row = cand_cnt + static_cast<size_t>(t) * n_chunks;
   if (tid == 0) {
@@ -124,16 +136,17 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(int n_chunks, int c
 
 }  // namespace
 
-cudaError_t launch_select(int n_q, int n_chunks, int cap, int topk, const int2* row_range, const uint32_t* cand_key,
+cudaError_t launch_select(int n_q, int n_chunks, int cap, int topk, int trivial_len, const int2* row_range,
+                          const uint32_t* cand_key,
                           const int32_t* cand_idx, const uint32_t* cand_cnt, int32_t* idx_out, float* score_out,
                           uint32_t* status, cudaStream_t st) {
   if (n_q <= 0) return cudaSuccess;
   if (n_chunks > kMaxChunks) return cudaErrorInvalidValue;
   if (static_cast<long long>(n_chunks) * cap <= static_cast<long long>(kSelThreads) * kSelPer)
-    select_kernel<true><<<n_q, kSelThreads, 0, st>>>(n_chunks, cap, topk, row_range, cand_key, cand_idx, cand_cnt,
+    select_kernel<true><<<n_q, kSelThreads, 0, st>>>(n_chunks, cap, topk, trivial_len, row_range, cand_key, cand_idx, cand_cnt,
                                                     idx_out, score_out, status);
   else
-    select_kernel<false><<<n_q, kSelThreads, 0, st>>>(n_chunks, cap, topk, row_range, cand_key, cand_idx, cand_cnt,
+    select_kernel<false><<<n_q, kSelThreads, 0, st>>>(n_chunks, cap, topk, trivial_len, row_range, cand_key, cand_idx, cand_cnt,
                                                      idx_out, score_out, status);
   return cudaGetLastError();
 }
