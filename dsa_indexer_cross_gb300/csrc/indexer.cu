@@ -275,9 +275,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = threadIdx.x & 31;
     const int row = quarter * 32 + lane;       // key within the tile
     const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
-    // A failed (timed-out) wait is published through sh.epi_abort, written only before
-    // the first named barrier of a tile and read only between that barrier and the
-    // second one, so all four epilogue warps leave the loops at the same point.
+    // A failed (timed-out) wait reaches every epilogue warp through the per-tile
+    // barrier-reduction (fast tiles) or through sh.epi_abort, written only before the
+    // barrier-reduction and read only after it (slow tiles), so all four epilogue warps
+    // leave the loops at the same point.
     uint32_t tile = 0;
     bool stop = false;
     for (int k = 0; k * static_cast<int>(gridDim.x) < n_units && !stop; ++k) {
@@ -299,10 +300,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       named_bar_sync(1, kEpiThreads);
       for (int i = 0; i < ui.n_tiles; ++i, ++tile) {
         const int buf = tile & 1;
+        const int tile0 = ui.kbeg + i * kKeyTile;
+        // Fast tile: no query's buffer has been cut back yet and none can fill up through
+        // this tile (uniform across the CTA).  tau is then still below every key, so every
+        // in-range key is appended and its slot is its offset in the range: no ballots, no
+        // counts exchanged.  Counts only grow with i, so once a tile is slow the rest are.
+        bool fast = true;
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const int2 rr = sh.rr[g];
+          const int a = max(rr.x, ui.kbeg), b = min(rr.y, ui.kend);
+          fast = fast && min(b, tile0 + kKeyTile) - a <= cap - kKeyTile;
+        }
         bool ok = mbar_wait(&sh.t_full[buf], (tile >> 1) & 1, &sh.abort_flag, status);
         ok = __all_sync(0xffffffffu, ok);
         uint32_t msk[G];
         uint32_t key[G];
+        float acc[G];
         if (ok) {
           tc_fence_after();
           // Head sum with NP independent partial sums per query (breaks the dependent FMA
@@ -331,7 +345,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
           }
-          float acc[G];
 #pragma unroll
           for (int g = 0; g < G; ++g) {
             if constexpr (NP == 4) acc[g] = (part[g][0] + part[g][1]) + (part[g][2] + part[g][3]);
@@ -339,9 +352,39 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_before();
           mbar_arrive(&sh.t_empty[buf]);
+          if (fast) {
+            // every in-range key is appended: key j of query g goes to slot j - a_g
+            const int j = tile0 + row;
+            const size_t rowbase = (static_cast<size_t>(t0) * n_chunks + ui.chunk) * cap;
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+              const int2 rr = sh.rr[g];
+              const int a = max(rr.x, ui.kbeg), b = min(rr.y, ui.kend);
+              if (j >= a && j < b) {
+                const size_t off = rowbase + static_cast<size_t>(g) * n_chunks * cap + (j - a);
+                st_global_u32(cand_key + off, float_key(acc[g]));
+                st_global_u32(reinterpret_cast<uint32_t*>(cand_idx) + off, static_cast<uint32_t>(j));
+              }
+            }
+            if (tid < G) {
+              const int2 rr = sh.rr[tid];
+              const int a = max(rr.x, ui.kbeg), b = min(rr.y, ui.kend);
+              sh.cnt[(tile & 1) ^ 1][tid] = max(0, min(b, tile0 + kKeyTile) - a);
+            }
+          }
+        }
+        if (fast) {
+          // one barrier-reduction per tile carries a timed-out wait to every epilogue warp
+          if (bar_red_or(1, kEpiThreads, !ok)) {
+            stop = true;
+            break;
+          }
+          continue;
+        }
+        if (ok) {
           // append candidates that beat the running threshold, in key order: per query the
           // four lane quarters publish their counts, then each writes after the lower ones
-          const int j = ui.kbeg + i * kKeyTile + row;
+          const int j = tile0 + row;
 #pragma unroll
           for (int g = 0; g < G; ++g) {
             const int2 rr = sh.rr[g];
@@ -357,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int cur = tile & 1, nxt = cur ^ 1;
         bool need = false;
         if (ok) {
-          const int j = ui.kbeg + i * kKeyTile + row;
+          const int j = tile0 + row;
           // every query's write offset first (shared loads only), then the global stores
           int pos[G];
 #pragma unroll
