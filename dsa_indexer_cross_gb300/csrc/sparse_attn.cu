@@ -12,10 +12,14 @@
 // core, so both products run transposed, with the latent rows on M:
 //     S^T[r, c]  = Rows[r, :576] . Q[c, :576]            M = 64 rows,   N = HB, K = 576
 //     O^T[d, c] += Rows[:, d]^T  . P^T[r, c]             M = 128 dims,  N = HB, K = 64
-// The tile is stored once in shared memory in the 128-byte-swizzled layout and read as a
-// K-major operand by the first product and as an MN-major operand by the second, so each
-// row is brought on chip once per item.  S^T is double-buffered in TMEM; O^T (512 x HB
-// fp32) stays in TMEM for the whole item.
+// A tile is stored once in shared memory as nine 64-dim blocks in the 128-byte-swizzled
+// layout, read as a K-major operand by the first product and as an MN-major operand by the
+// second, so each row is brought on chip once per item.  Every block has its own full/empty
+// barrier pair: a block is refilled for tile g + 2 as soon as the last product of tile g
+// that reads it has finished, so loads overlap the tail of the previous tile.  P^T of tile g
+// (bf16, MN-major) is written into that tile's rope block, which the first product no longer
+// needs once S^T is complete.  S^T is double-buffered in TMEM; O^T (512 x HB fp32) stays in
+// TMEM for the whole item.
 //
 // Two ways to walk the rows (template parameter HD):
 //   HD == 0  "gather": item = (token, block of HB heads); the tile holds the token's next
@@ -30,11 +34,12 @@
 // Online softmax (base 2): the per-column max in use lives in shared memory and changes only
 // when a score exceeds it by more than 8 (a factor 256); one barrier-reduction per tile
 // detects that, and only then are the tile's column maxima exchanged and O^T and the running
-// sums rescaled (exact either way).  Each thread keeps running sums of its own rows and the
-// column sums are reduced once per item.
+// sums rescaled (exact either way).  A softmax warp reads its 16 rows of S^T with the 16x256b
+// TMEM shape, so each thread holds two rows and HB/4 columns; running sums stay in registers
+// and are reduced once per item.
 //
 // Warp roles (256 threads): warps 0-2 load Q and the rows (cp.async gathers, or one thread
-// issuing TMA tile loads in block-dense mode); warps 3-6 run the softmax, build the mask
+// issuing TMA block loads in block-dense mode); warps 3-6 run the softmax, build the mask
 // (block-dense) and the epilogue; warp 7 owns TMEM and issues the MMAs from one thread.
 // Persistent CTAs.
 #include <cuda_bf16.h>
@@ -49,13 +54,14 @@ constexpr int kRows = 64;          // latent rows per tile
 constexpr int kDqk = 576;
 constexpr int kDv = 512;
 constexpr int kChunks = kDqk / 8;  // 16-byte chunks per latent row
-constexpr int kStages = 2;
+constexpr int kKB = kDqk / 64;     // 64-dim blocks per tile (the last one holds the rope dims)
+constexpr int kBlkBytes = kRows * 128;         // one block: 64 rows x 128 B
+constexpr int kSlots = 2 * kKB;                // two tiles in flight
 constexpr int kProd = 96;                      // warps 0-2
 constexpr int kSoft = 128;                     // warps 3-6, one per TMEM lane quarter
 constexpr int kThreads = kProd + kSoft + 32;   // + warp 7 (MMA); 8 warps = 2 per SM sub-partition
-constexpr int kTileBytes = kRows * kDqk * 2;   // 72 KB
-constexpr int kDenseCols = 48;                 // columns of a block-dense item
-constexpr int kMaskBytes = 6144;               // selection bitmask budget (block-dense)
+constexpr int kDenseCols = 64;                 // columns of a block-dense item
+constexpr int kMaskBytes = 4096;               // selection bitmask budget (block-dense)
 
 template <int HB, int HD>
 struct ACfg {
@@ -63,19 +69,20 @@ struct ACfg {
   static constexpr int B = DENSE ? HB / HD : 1;                        // tokens per item
   static constexpr int MAXR = DENSE ? (kMaskBytes * 8 / B) / 64 * 64 : 0;  // longest key range
   static constexpr int Q_BYTES = HB * kDqk * 2;
-  static constexpr int P_BYTES = HB * kRows * 2;
   static constexpr int M_BYTES = DENSE ? kMaskBytes : 0;
-  static constexpr int DYN_SMEM = 1024 + kStages * kTileBytes + Q_BYTES + P_BYTES + M_BYTES;
+  static constexpr int DYN_SMEM = 1024 + kSlots * kBlkBytes + Q_BYTES + M_BYTES;
   static constexpr uint32_t TMEM_COLS = 6 * HB <= 128 ? 128 : 6 * HB <= 256 ? 256 : 512;
   static constexpr int O_COL = 0;
   static constexpr int S_COL = 4 * HB;
+  static constexpr int NR = HB / 8;                                    // 16x256b repetitions
   static_assert(HB % 16 == 0 && HB <= 64, "columns");
   static_assert(!DENSE || HB % HD == 0, "whole tokens per dense item");
+  static_assert(HB * kRows * 2 <= kBlkBytes, "P^T must fit in the rope block");
 };
 
 // Per-column softmax state lives in shared memory (uniform across the softmax threads).
 struct AShared {
-  uint64_t full[kStages], empty[kStages];
+  uint64_t full[kSlots], empty[kSlots];
   uint64_t q_full, q_empty, s_full[2], s_empty[2], p_full, o_done, o_free;
   uint32_t tmem_base, abort_flag, soft_abort;
   uint32_t prod_ok;
@@ -85,7 +92,9 @@ struct AShared {
   alignas(16) float alpha[64];
 };
 static_assert(ACfg<64, 0>::DYN_SMEM + sizeof(AShared) <= 232448, "HB=64 must fit in shared memory");
-static_assert(ACfg<48, 16>::DYN_SMEM + sizeof(AShared) <= 232448, "block-dense must fit in shared memory");
+static_assert(ACfg<64, 16>::DYN_SMEM + sizeof(AShared) <= 232448, "block-dense must fit in shared memory");
+
+__device__ __forceinline__ int slot_of(uint32_t g, int kb) { return static_cast<int>(g & 1u) * kKB + kb; }
 
 // 16 consecutive floats of shared memory into registers (four 16-byte loads issued together).
 __device__ __forceinline__ void load_row16(float (&r)[16], const float* p) {
@@ -100,8 +109,8 @@ __device__ __forceinline__ void load_row16(float (&r)[16], const float* p) {
 }
 // Stores through explicit state spaces (the compiler then knows they cannot alias the
 // shared-memory loads around them).
-__device__ __forceinline__ void st_shared_u16(void* p, uint16_t v) {
-  asm volatile("st.shared.u16 [%0], %1;" ::"r"(smem_u32(p)), "h"(v) : "memory");
+__device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 __device__ __forceinline__ void st_global_u16(uint16_t* p, uint16_t v) {
   asm volatile("{\n .reg .u64 ga;\n cvta.to.global.u64 ga, %0;\n st.global.u16 [ga], %1;\n}\n" ::"l"(p), "h"(v) : "memory");
@@ -158,13 +167,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   using C = ACfg<HB, HD>;
   constexpr bool DENSE = C::DENSE;
   constexpr int B = C::B;
+  constexpr int NR = C::NR;
   extern __shared__ uint8_t smem_raw[];
   __shared__ AShared sh;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sT = smem;                                   // kStages tiles
-  uint8_t* sQ = smem + kStages * kTileBytes;            // HB x 576, 9 blocks of HB x 128 B
-  uint8_t* sP = sQ + C::Q_BYTES;                        // P^T: HB x 64, K-major
-  uint32_t* sMask = reinterpret_cast<uint32_t*>(sP + C::P_BYTES);   // block-dense: B x MAXR bits
+  uint8_t* sT = smem;                                   // kSlots blocks of 64 rows x 128 B
+  uint8_t* sQ = smem + kSlots * kBlkBytes;              // HB x 576, 9 blocks of HB x 128 B
+  uint32_t* sMask = reinterpret_cast<uint32_t*>(sQ + C::Q_BYTES);   // block-dense: B x MAXR bits
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int n_hb = DENSE ? 1 : (H + HB - 1) / HB;
@@ -177,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kSlots; ++s) {
       mbar_init(&sh.full[s], DENSE ? 1 : kProd);
       mbar_init(&sh.empty[s], 1);
     }
@@ -207,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < 3) {
     // ---------------------------------------------------------------- Q (+ gathered rows)
     // Thread 0 does every wait and publishes the outcome in sh.prod_ok between two named
-    // barriers (id 2), so the four producer warps always stop at the same point.
+    // barriers (id 2), so the three producer warps always stop at the same point.
     const int tid = threadIdx.x;
     uint32_t g = 0, it = 0;
     bool ok = true;
@@ -244,18 +253,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       cp_async_mbar_arrive(&sh.q_full);
       if constexpr (DENSE) {
-        // one thread streams the block's consecutive latent rows with TMA
+        // one thread streams the block's consecutive latent rows with TMA, one 64-dim block
+        // at a time as soon as its slot is released
         if (tid == 0) {
-          for (int i = 0; i < I.nt; ++i, ++g) {
-            const int s = g % kStages;
-            if (g >= kStages) {
-              ok = mbar_wait(&sh.empty[s], ((g / kStages) - 1) & 1, &sh.abort_flag, status);
-              if (!ok) break;
+          for (int i = 0; i < I.nt && ok; ++i, ++g) {
+            for (int kb = 0; kb < kKB; ++kb) {
+              const int s = slot_of(g, kb);
+              if (g >= 2) {
+                ok = mbar_wait(&sh.empty[s], ((g >> 1) - 1) & 1, &sh.abort_flag, status);
+                if (!ok) break;
+              }
+              mbar_arrive_expect_tx(&sh.full[s], kBlkBytes);
+              tma_load_2d(sT + s * kBlkBytes, &tmap_kv, &sh.full[s], kb * 64, I.lo + i * kRows);
             }
-            mbar_arrive_expect_tx(&sh.full[s], kTileBytes);
-            uint8_t* dst = sT + s * kTileBytes;
-            for (int b = 0; b < kDqk / 64; ++b)
-              tma_load_2d(dst + b * (kRows * 128), &tmap_kv, &sh.full[s], b * 64, I.lo + i * kRows);
           }
         }
         ok = sync_ok(ok);
@@ -264,13 +274,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const long long kst = __ldg(ks + t);
         const int32_t* irow = idx + static_cast<size_t>(t) * topk;
         for (int i = 0; i < I.nt; ++i, ++g) {
-          const int s = g % kStages;
           w_ok = true;
-          if (tid == 0 && g >= kStages) w_ok = mbar_wait(&sh.empty[s], ((g / kStages) - 1) & 1, &sh.abort_flag, status);
+          if (tid == 0 && g >= 2) {
+            for (int kb = 0; kb < kKB && w_ok; ++kb)
+              w_ok = mbar_wait(&sh.empty[slot_of(g, kb)], ((g >> 1) - 1) & 1, &sh.abort_flag, status);
+          }
           ok = sync_ok(w_ok);
           if (!ok) break;
           // resolve every chunk's row first (independent loads), then issue the copies
-          constexpr int kPer = kRows * kChunks / kProd;   // 36 chunks per thread
+          constexpr int kPer = kRows * kChunks / kProd;   // 48 chunks per thread
           int rows[kPer];
 #pragma unroll
           for (int k = 0; k < kPer; ++k) {
@@ -286,15 +298,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             rows[k] = v ? static_cast<int>(row) : -1;
           }
-          uint8_t* dst = sT + s * kTileBytes;
+          uint8_t* dst = sT + (g & 1u) * (kKB * kBlkBytes);
 #pragma unroll
           for (int k = 0; k < kPer; ++k) {
             const int c = tid + k * kProd;
             const int r = c / kChunks, ch = c - r * kChunks;
             const uint16_t* src = kv + static_cast<size_t>(rows[k] >= 0 ? rows[k] : 0) * kDqk + ch * 8;
-            cp_async_16_zfill(smem_u32(dst + (ch >> 3) * (kRows * 128) + sw128(r, ch & 7)), src, rows[k] >= 0);
+            cp_async_16_zfill(smem_u32(dst + (ch >> 3) * kBlkBytes + sw128(r, ch & 7)), src, rows[k] >= 0);
           }
-          cp_async_mbar_arrive(&sh.full[s]);
+          for (int kb = 0; kb < kKB; ++kb) cp_async_mbar_arrive(&sh.full[slot_of(g, kb)]);
         }
       }
       ++it;
@@ -304,8 +316,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------------- softmax + epilogue
     const int tid = threadIdx.x - kProd;   // 0..127
     const int qd = warp & 3;               // TMEM lane quarter
-    const int r = qd * 16 + lane;          // S^T row owned (lanes 0..15 of the quarter)
-    const bool row_lane = lane < 16;
+    const int r0 = qd * 16 + (lane >> 2);  // S^T rows held: r0 and r0 + 8
+    const int cq = 2 * (lane & 3);         // column pair within each group of 8 columns
     const uint32_t t_lane = static_cast<uint32_t>(qd * 32) << 16;
     // A failed (timed-out) wait is published through sh.soft_abort, written only before a
     // named barrier and read right after it; the next write can only happen after a later
@@ -330,12 +342,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           lse[static_cast<size_t>(col_token(tid)) * H + col_head(tid)] = -INFINITY;
         continue;
       }
-      // Column max in shared memory (read by all softmax threads); the running sum of this
-      // thread's rows stays in registers and is reduced across rows once per item.
+      // Column max in shared memory (read by all softmax threads); the running sums of this
+      // thread's two rows stay in registers and are reduced across rows once per item.
       if (tid < HB) sh.m_used[tid] = -INFINITY;
-      float lp[HB];
+      float lp[2 * NR];
 #pragma unroll
-      for (int c = 0; c < HB; ++c) lp[c] = 0.f;
+      for (int c = 0; c < 2 * NR; ++c) lp[c] = 0.f;
       const int32_t* irow = idx + static_cast<size_t>(I.t0) * topk;
       if constexpr (DENSE) {
         // selection bitmask over the block's key range [lo, lo + nt*64); bits that fall in
@@ -381,50 +393,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       const long long kst = DENSE ? 0 : __ldg(ks + I.t0);
       for (int i = 0; i < I.nt; ++i, ++g) {
         const int sb = g & 1;
-        int row_j = -1;
+        bool rv0 = false, rv1 = false;   // gather: rows r0 / r0 + 8 hold a valid selection
         if constexpr (!DENSE) {
-          const int slot = i * kRows + r;
-          row_j = (row_lane && slot < topk) ? __ldg(irow + slot) : -1;
+          const int s0 = i * kRows + r0, s1 = s0 + 8;
+          const int j0 = s0 < topk ? __ldg(irow + s0) : -1;
+          const int j1 = s1 < topk ? __ldg(irow + s1) : -1;
+          rv0 = j0 >= 0 && kst + j0 >= 0 && kst + j0 < n_kv;
+          rv1 = j1 >= 0 && kst + j1 >= 0 && kst + j1 < n_kv;
         }
         bool ok = mbar_wait(&sh.s_full[sb], (g >> 1) & 1, &sh.abort_flag, status);
         ok = __all_sync(0xffffffffu, ok);
-        float sc[HB];
+        float sc[4 * NR];   // [4k + j]: j = 0,1 row r0 columns 8k+cq, +1;  j = 2,3 row r0 + 8
         bool need = false;
         if (ok) {
           tc_fence_after();
-#pragma unroll
-          for (int hh = 0; hh < HB / 16; ++hh) {
-            uint32_t v16[16];
-            tmem_ld16(tmem + t_lane + C::S_COL + sb * HB + hh * 16, v16);
-            tmem_ld_wait();
-#pragma unroll
-            for (int h = 0; h < 16; ++h) sc[hh * 16 + h] = __uint_as_float(v16[h]);
-          }
+          uint32_t v[4 * NR];
+          tmem_ld_16x256b<NR>(tmem + t_lane + C::S_COL + sb * HB, v);
+          tmem_ld_wait();
           tc_fence_before();
           mbar_arrive(&sh.s_empty[sb]);
-          bool vb[B];
-          if constexpr (DENSE) {
-            const int o = i * kRows + r;
 #pragma unroll
-            for (int b = 0; b < B; ++b)
-              vb[b] = row_lane && ((sMask[b * (C::MAXR / 32) + (o >> 5)] >> (o & 31)) & 1u);
-          } else {
-            vb[0] = row_lane && row_j >= 0 && kst + row_j < n_kv && kst + row_j >= 0;
-          }
+          for (int kk = 0; kk < NR; ++kk) {
+            const float2 mu = *reinterpret_cast<const float2*>(&sh.m_used[8 * kk + cq]);
 #pragma unroll
-          for (int c0 = 0; c0 < HB; c0 += 16) {
-            float mr[16];
-            load_row16(mr, &sh.m_used[c0]);
-#pragma unroll
-            for (int c = c0; c < c0 + 16; ++c) {
-              sc[c] = vb[DENSE ? c / (DENSE ? HD : 1) : 0] ? sc[c] * scale_log2 : -INFINITY;
-              need |= sc[c] > mr[c - c0] + 8.f;   // only a max that grew by > 2^8 forces a rescale
+            for (int j = 0; j < 4; ++j) {
+              const int c = 8 * kk + cq + (j & 1);
+              bool valid;
+              if constexpr (DENSE) {
+                const int r = r0 + ((j & 2) ? 8 : 0);
+                const uint2 mw = *reinterpret_cast<const uint2*>(
+                    &sMask[(c / (DENSE ? HD : 1)) * (C::MAXR / 32) + i * (kRows / 32)]);
+                valid = (((r < 32 ? mw.x : mw.y) >> (r & 31)) & 1u) != 0u;
+              } else {
+                valid = (j & 2) ? rv1 : rv0;
+              }
+              const float x = valid ? __uint_as_float(v[4 * kk + j]) * scale_log2 : -INFINITY;
+              sc[4 * kk + j] = x;
+              need |= x > ((j & 1) ? mu.y : mu.x) + 8.f;   // only a max that grew by > 2^8 forces a rescale
             }
-          }
-          // the previous tile's PV must be done before P is overwritten or O^T rescaled
-          if (g > 0) {
-            ok = mbar_wait(&sh.o_done, (g - 1) & 1, &sh.abort_flag, status);
-            ok = __all_sync(0xffffffffu, ok);
           }
         }
         // One barrier-reduction per tile decides whether the slow path runs.  The abort
@@ -434,13 +440,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (bar_red_or(1, kSoft, need || !ok)) {
           if (ok) {
 #pragma unroll
-            for (int c = 0; c < HB; ++c) {
-              float x = sc[c];
-              x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 8));
-              x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 4));
-              x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 2));
-              x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 1));
-              if (lane == 0) sh.red[qd][c] = x;
+            for (int kk = 0; kk < NR; ++kk) {
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                float x = fmaxf(sc[4 * kk + e], sc[4 * kk + 2 + e]);
+                x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 4));
+                x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 8));
+                x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 16));
+                if (lane < 4) sh.red[qd][8 * kk + cq + e] = x;
+              }
+            }
+            // O^T may only be rescaled once the previous tile's PV has finished
+            if (i > 0) {
+              ok = mbar_wait(&sh.o_done, (g - 1) & 1, &sh.abort_flag, status);
+              ok = __all_sync(0xffffffffu, ok);
+              if (!ok && lane == 0) sh.soft_abort = 1;
             }
           }
           named_bar_sync(1, kSoft);
@@ -460,14 +474,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           bool any = false;
 #pragma unroll
+          for (int kk = 0; kk < NR; ++kk) {
+            const float2 a = *reinterpret_cast<const float2*>(&sh.alpha[8 * kk + cq]);
+            lp[2 * kk] *= a.x;
+            lp[2 * kk + 1] *= a.y;
+          }
+#pragma unroll
           for (int c0 = 0; c0 < HB; c0 += 16) {
             float ar[16];
             load_row16(ar, &sh.alpha[c0]);
 #pragma unroll
-            for (int c = c0; c < c0 + 16; ++c) {
-              lp[c] *= ar[c - c0];
-              any |= ar[c - c0] != 1.f;
-            }
+            for (int c = 0; c < 16; ++c) any |= ar[c] != 1.f;
           }
           if (any && i > 0) {
 #pragma unroll
@@ -487,23 +504,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st_wait();
           }
         }
-        // P = exp2(s - m) in bf16, written as the K-major B operand of the second product; the
-        // running sums add the same rounded values the tensor core multiplies.
+        // P = exp2(s - m) in bf16, written MN-major (row-by-row, 64 columns per 128 B) into
+        // this tile's rope block as the B operand of the second product; the running sums
+        // add the same rounded values the tensor core multiplies.
+        const uint32_t p_base = smem_u32(sT + slot_of(g, kKB - 1) * kBlkBytes);
 #pragma unroll
-        for (int c0 = 0; c0 < HB; c0 += 16) {
-          float mr[16];
-          load_row16(mr, &sh.m_used[c0]);
+        for (int kk = 0; kk < NR; ++kk) {
+          const float2 mu = *reinterpret_cast<const float2*>(&sh.m_used[8 * kk + cq]);
 #pragma unroll
-          for (int c = c0; c < c0 + 16; ++c) {
-            const float p = sc[c] == -INFINITY ? 0.f : exp2f(sc[c] - mr[c - c0]);
-            const __nv_bfloat16 pb = __float2bfloat16_rn(p);
-            if (row_lane) {
-              const uint32_t off = (c >> 3) * 1024 + (c & 7) * 128 + ((((r >> 3) ^ (c & 7)) & 7) << 4) + (r & 7) * 2;
-              st_shared_u16(sP + off, *reinterpret_cast<const uint16_t*>(&pb));
-              lp[c] += __bfloat162float(pb);
-            }
+          for (int h = 0; h < 2; ++h) {
+            const int r = r0 + 8 * h;
+            const float x0 = sc[4 * kk + 2 * h], x1 = sc[4 * kk + 2 * h + 1];
+            const float p0 = x0 == -INFINITY ? 0.f : exp2f(x0 - mu.x);
+            const float p1 = x1 == -INFINITY ? 0.f : exp2f(x1 - mu.y);
+            const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+            st_shared_u32(p_base + r * 128 + ((kk ^ (r & 7)) << 4) + cq * 2, *reinterpret_cast<const uint32_t*>(&pb));
+            lp[2 * kk] += __low2float(pb);
+            lp[2 * kk + 1] += __high2float(pb);
           }
         }
+        // Wait for the previous tile's PV before publishing P: PV(g) queues behind it anyway,
+        // and waiting on every phase keeps the parity waits on o_done exact (the MMA stream
+        // runs in order, so PV(g - 2) is complete once S^T(g) is).  A timeout here raises the
+        // CTA abort flag, and the next wait of this loop turns it into a uniform stop.
+        if (i > 0) (void)mbar_wait(&sh.o_done, (g - 1) & 1, &sh.abort_flag, status);
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(&sh.p_full);
@@ -511,13 +535,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (stop) break;
       // item end: column sums over the 64 rows, then O^T / l -> out
 #pragma unroll
-      for (int c = 0; c < HB; ++c) {
-        float x = lp[c];
-        x += __shfl_xor_sync(0xffffffffu, x, 8);
-        x += __shfl_xor_sync(0xffffffffu, x, 4);
-        x += __shfl_xor_sync(0xffffffffu, x, 2);
-        x += __shfl_xor_sync(0xffffffffu, x, 1);
-        if (lane == 0) sh.red[qd][c] = x;
+      for (int kk = 0; kk < NR; ++kk) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          float x = lp[2 * kk + e];
+          x += __shfl_xor_sync(0xffffffffu, x, 4);
+          x += __shfl_xor_sync(0xffffffffu, x, 8);
+          x += __shfl_xor_sync(0xffffffffu, x, 16);
+          if (lane < 4) sh.red[qd][8 * kk + cq + e] = x;
+        }
       }
       bool ok = mbar_wait(&sh.o_done, (g - 1) & 1, &sh.abort_flag, status);
       ok = __all_sync(0xffffffffu, ok);
@@ -528,6 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       named_bar_sync(1, kSoft);
       if (stop) break;
       tc_fence_after();
+      const int lane_d = lane;   // O^T rows: thread = dimension within the quarter
 #pragma unroll
       for (int hh = 0; hh < HB / 16; ++hh) {
         float inv[16];
@@ -539,7 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t o[16];
           tmem_ld16(tmem + t_lane + C::O_COL + b * HB + hh * 16, o);
           tmem_ld_wait();
-          const int d = b * 128 + qd * 32 + lane;
+          const int d = b * 128 + qd * 32 + lane_d;
 #pragma unroll
           for (int h = 0; h < 16; ++h) {
             const int c = hh * 16 + h;
@@ -565,21 +592,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t id_qk = idesc_bf16_f32(64, HB, 0, 0);
-      constexpr uint32_t id_pv = idesc_bf16_f32(128, HB, 1, 0);
-      const uint32_t sq = smem_u32(sQ), sp = smem_u32(sP), st0 = smem_u32(sT);
+      constexpr uint32_t id_pv = idesc_bf16_f32(128, HB, 1, 1);
+      const uint32_t sq = smem_u32(sQ), st0 = smem_u32(sT);
       uint32_t g = 0, it = 0;
       bool ok = true;
+      // S^T(gq): one 64-dim block at a time, each as soon as it has landed
       auto issue_qk = [&](uint32_t gq) -> bool {
-        const int s = gq % kStages, sb = gq & 1;
-        if (!mbar_wait(&sh.full[s], (gq / kStages) & 1, &sh.abort_flag, status)) return false;
+        const int sb = gq & 1;
         if (gq >= 2 && !mbar_wait(&sh.s_empty[sb], ((gq >> 1) - 1) & 1, &sh.abort_flag, status)) return false;
-        tc_fence_after();
-        const uint32_t a0 = st0 + s * kTileBytes;
-#pragma unroll 4
-        for (int k = 0; k < kDqk / 16; ++k) {
-          const int kb = k >> 2, sub = k & 3;
-          umma_bf16(tmem + C::S_COL + sb * HB, sdesc_sw128(a0 + kb * (kRows * 128) + sub * 32, 16, 1024),
-                    sdesc_sw128(sq + kb * (HB * 128) + sub * 32, 16, 1024), id_qk, k > 0 ? 1u : 0u);
+        for (int kb = 0; kb < kKB; ++kb) {
+          const int s = slot_of(gq, kb);
+          if (!mbar_wait(&sh.full[s], (gq >> 1) & 1, &sh.abort_flag, status)) return false;
+          tc_fence_after();
+          const uint32_t a0 = st0 + s * kBlkBytes;
+#pragma unroll
+          for (int sub = 0; sub < 4; ++sub)
+            umma_bf16(tmem + C::S_COL + sb * HB, sdesc_sw128(a0 + sub * 32, 16, 1024),
+                      sdesc_sw128(sq + kb * (HB * 128) + sub * 32, 16, 1024), id_qk, (kb | sub) ? 1u : 0u);
         }
         umma_commit(&sh.s_full[sb]);
         return true;
@@ -599,16 +628,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (ok && i == 0 && it > 0) ok = mbar_wait(&sh.o_free, (it - 1) & 1, &sh.abort_flag, status);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t a0 = st0 + (g % kStages) * kTileBytes;
+          const uint32_t pb = st0 + slot_of(g, kKB - 1) * kBlkBytes;
 #pragma unroll
           for (int b = 0; b < 4; ++b) {
+            const uint32_t a0 = st0 + slot_of(g, 2 * b) * kBlkBytes;
 #pragma unroll
-            for (int k = 0; k < kRows / 16; ++k) {
-              umma_bf16(tmem + C::O_COL + b * HB, sdesc_sw128(a0 + (2 * b) * (kRows * 128) + k * 2048, kRows * 128, 1024),
-                        sdesc_sw128(sp + k * 32, 16, 1024), id_pv, (i > 0 || k > 0) ? 1u : 0u);
+            for (int kq = 0; kq < kRows / 16; ++kq) {
+              umma_bf16(tmem + C::O_COL + b * HB, sdesc_sw128(a0 + kq * 2048, kBlkBytes, 1024),
+                        sdesc_sw128(pb + kq * 2048, kBlkBytes, 1024), id_pv, (i > 0 || kq > 0) ? 1u : 0u);
             }
+            // the two value blocks of this O^T block may be refilled once these finish
+            umma_commit(&sh.empty[slot_of(g, 2 * b)]);
+            umma_commit(&sh.empty[slot_of(g, 2 * b + 1)]);
           }
-          umma_commit(&sh.empty[g % kStages]);
+          umma_commit(&sh.empty[slot_of(g, kKB - 1)]);    // rope block, which also held P^T
           umma_commit(&sh.o_done);
         }
         ++it;
@@ -715,11 +748,11 @@ cudaError_t launch_sparse_attn(const CUtensorMap& tmap_kv, int n_q, int n_kv, in
     block_range_kernel<<<(n_blk + 7) / 8, 256, 0, st>>>(idx, ks, n_q, n_kv, topk, B, br);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     switch (hd) {
-      case 1: return launch_cfg<48, 1>(tmap_kv, n_q, n_kv, n_heads, topk, scale, q, kv, idx, ks, nullptr, br, out, lse, status, st);
-      case 2: return launch_cfg<48, 2>(tmap_kv, n_q, n_kv, n_heads, topk, scale, q, kv, idx, ks, nullptr, br, out, lse, status, st);
-      case 4: return launch_cfg<48, 4>(tmap_kv, n_q, n_kv, n_heads, topk, scale, q, kv, idx, ks, nullptr, br, out, lse, status, st);
-      case 8: return launch_cfg<48, 8>(tmap_kv, n_q, n_kv, n_heads, topk, scale, q, kv, idx, ks, nullptr, br, out, lse, status, st);
-      default: return launch_cfg<48, 16>(tmap_kv, n_q, n_kv, n_heads, topk, scale, q, kv, idx, ks, nullptr, br, out, lse, status, st);
+      case 1: return launch_cfg<kDenseCols, 1>(tmap_kv, n_q, n_kv, n_heads, topk, scale, q, kv, idx, ks, nullptr, br, out, lse, status, st);
+      case 2: return launch_cfg<kDenseCols, 2>(tmap_kv, n_q, n_kv, n_heads, topk, scale, q, kv, idx, ks, nullptr, br, out, lse, status, st);
+      case 4: return launch_cfg<kDenseCols, 4>(tmap_kv, n_q, n_kv, n_heads, topk, scale, q, kv, idx, ks, nullptr, br, out, lse, status, st);
+      case 8: return launch_cfg<kDenseCols, 8>(tmap_kv, n_q, n_kv, n_heads, topk, scale, q, kv, idx, ks, nullptr, br, out, lse, status, st);
+      default: return launch_cfg<kDenseCols, 16>(tmap_kv, n_q, n_kv, n_heads, topk, scale, q, kv, idx, ks, nullptr, br, out, lse, status, st);
     }
   }
   int32_t* row_nt = static_cast<int32_t*>(scratch);
