@@ -38,9 +38,11 @@
 // TMEM shape, so each thread holds two rows and HB/4 columns; running sums stay in registers
 // and are reduced once per item.
 //
-// Warp roles (256 threads): warps 0-2 load Q and the rows (cp.async gathers, or one thread
-// issuing TMA block loads in block-dense mode); warps 3-6 run the softmax, build the mask
-// (block-dense) and the epilogue; warp 7 owns TMEM and issues the MMAs from one thread.
+// Warp roles (256 threads): warps 0-1 load Q and the rows (cp.async gathers, or one thread
+// issuing TMA block loads in block-dense mode); warp 2 issues the S^T products; warps 3-6 run
+// the softmax, build the mask (block-dense) and the epilogue; warp 7 owns TMEM and issues the
+// PV products.  With the two products issued from separate warps, PV(g) goes out as soon as
+// P(g) exists instead of queueing behind S^T(g+1), whose blocks may still be in flight.
 // Persistent CTAs.
 #include <cuda_bf16.h>
 
@@ -57,9 +59,9 @@ constexpr int kChunks = kDqk / 8;  // 16-byte chunks per latent row
 constexpr int kKB = kDqk / 64;     // 64-dim blocks per tile (the last one holds the rope dims)
 constexpr int kBlkBytes = kRows * 128;         // one block: 64 rows x 128 B
 constexpr int kSlots = 2 * kKB;                // two tiles in flight
-constexpr int kProd = 96;                      // warps 0-2
+constexpr int kProd = 64;                      // warps 0-1
 constexpr int kSoft = 128;                     // warps 3-6, one per TMEM lane quarter
-constexpr int kThreads = kProd + kSoft + 32;   // + warp 7 (MMA); 8 warps = 2 per SM sub-partition
+constexpr int kThreads = kProd + 32 + kSoft + 32;   // + warp 2 (S^T MMAs), warp 7 (PV MMAs); 8 warps
 constexpr int kDenseCols = 64;                 // columns of a block-dense item
 constexpr int kMaskBytes = 4096;               // selection bitmask budget (block-dense)
 
@@ -114,6 +116,14 @@ __device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v) {
 }
 __device__ __forceinline__ void st_global_u16(uint16_t* p, uint16_t v) {
   asm volatile("{\n .reg .u64 ga;\n cvta.to.global.u64 ga, %0;\n st.global.u16 [ga], %1;\n}\n" ::"l"(p), "h"(v) : "memory");
+}
+
+// 2^x by the hardware approximation (ex2.approx.ftz.f32; relative error far below the bf16
+// rounding that P goes through next); exp2(-inf) = +0.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // Named barrier over n threads that also returns the OR of a predicate across them.
@@ -213,10 +223,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = sh.tmem_base;
 
-  if (warp < 3) {
+  if (warp < 2) {
     // ---------------------------------------------------------------- Q (+ gathered rows)
     // Thread 0 does every wait and publishes the outcome in sh.prod_ok between two named
-    // barriers (id 2), so the three producer warps always stop at the same point.
+    // barriers (id 2), so the two producer warps always stop at the same point.
     const int tid = threadIdx.x;
     uint32_t g = 0, it = 0;
     bool ok = true;
@@ -282,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = sync_ok(w_ok);
           if (!ok) break;
           // resolve every chunk's row first (independent loads), then issue the copies
-          constexpr int kPer = kRows * kChunks / kProd;   // 48 chunks per thread
+          constexpr int kPer = kRows * kChunks / kProd;   // 72 chunks per thread
           int rows[kPer];
 #pragma unroll
           for (int k = 0; k < kPer; ++k) {
@@ -312,9 +322,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++it;
     }
     cp_async_wait<0>();
-  } else if (warp < 7) {
+  } else if (warp >= 3 && warp < 7) {
     // ---------------------------------------------------------------- softmax + epilogue
-    const int tid = threadIdx.x - kProd;   // 0..127
+    const int tid = threadIdx.x - 96;      // 0..127
     const int qd = warp & 3;               // TMEM lane quarter
     const int r0 = qd * 16 + (lane >> 2);  // S^T rows held: r0 and r0 + 8
     const int cq = 2 * (lane & 3);         // column pair within each group of 8 columns
@@ -510,13 +520,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t p_base = smem_u32(sT + slot_of(g, kKB - 1) * kBlkBytes);
 #pragma unroll
         for (int kk = 0; kk < NR; ++kk) {
-          const float2 mu = *reinterpret_cast<const float2*>(&sh.m_used[8 * kk + cq]);
+          // a column whose max is still -inf has only masked (-inf) entries so far: subtract 0
+          // there so that exp2(-inf) = 0 instead of exp2(NaN)
+          float2 mu = *reinterpret_cast<const float2*>(&sh.m_used[8 * kk + cq]);
+          mu.x = mu.x == -INFINITY ? 0.f : mu.x;
+          mu.y = mu.y == -INFINITY ? 0.f : mu.y;
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const int r = r0 + 8 * h;
-            const float x0 = sc[4 * kk + 2 * h], x1 = sc[4 * kk + 2 * h + 1];
-            const float p0 = x0 == -INFINITY ? 0.f : exp2f(x0 - mu.x);
-            const float p1 = x1 == -INFINITY ? 0.f : exp2f(x1 - mu.y);
+            const float p0 = ex2_approx(sc[4 * kk + 2 * h] - mu.x);
+            const float p1 = ex2_approx(sc[4 * kk + 2 * h + 1] - mu.y);
             const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
             st_shared_u32(p_base + r * 128 + ((kk ^ (r & 7)) << 4) + cq * 2, *reinterpret_cast<const uint32_t*>(&pb));
             lp[2 * kk] += __low2float(pb);
@@ -524,9 +537,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         // Wait for the previous tile's PV before publishing P: PV(g) queues behind it anyway,
-        // and waiting on every phase keeps the parity waits on o_done exact (the MMA stream
-        // runs in order, so PV(g - 2) is complete once S^T(g) is).  A timeout here raises the
-        // CTA abort flag, and the next wait of this loop turns it into a uniform stop.
+        // and since PV(g) cannot start before P(g), waiting here on every tile (and at every
+        // item end) means all earlier o_done phases are complete whenever this loop waits, so
+        // its parity waits are exact.  A timeout here raises the CTA abort flag, and the next
+        // wait of this loop turns it into a uniform stop.
         if (i > 0) (void)mbar_wait(&sh.o_done, (g - 1) & 1, &sh.abort_flag, status);
         fence_proxy_async_smem();
         tc_fence_before();
@@ -589,63 +603,73 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++it;
     }
   } else {
-    // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t id_qk = idesc_bf16_f32(64, HB, 0, 0);
-      constexpr uint32_t id_pv = idesc_bf16_f32(128, HB, 1, 1);
-      const uint32_t sq = smem_u32(sQ), st0 = smem_u32(sT);
-      uint32_t g = 0, it = 0;
-      bool ok = true;
-      // S^T(gq): one 64-dim block at a time, each as soon as it has landed
-      auto issue_qk = [&](uint32_t gq) -> bool {
-        const int sb = gq & 1;
-        if (gq >= 2 && !mbar_wait(&sh.s_empty[sb], ((gq >> 1) - 1) & 1, &sh.abort_flag, status)) return false;
-        for (int kb = 0; kb < kKB; ++kb) {
-          const int s = slot_of(gq, kb);
-          if (!mbar_wait(&sh.full[s], (gq >> 1) & 1, &sh.abort_flag, status)) return false;
-          tc_fence_after();
-          const uint32_t a0 = st0 + s * kBlkBytes;
-#pragma unroll
-          for (int sub = 0; sub < 4; ++sub)
-            umma_bf16(tmem + C::S_COL + sb * HB, sdesc_sw128(a0 + sub * 32, 16, 1024),
-                      sdesc_sw128(sq + kb * (HB * 128) + sub * 32, 16, 1024), id_qk, (kb | sub) ? 1u : 0u);
-        }
-        umma_commit(&sh.s_full[sb]);
-        return true;
-      };
-      for (int k = 0; k * static_cast<int>(gridDim.x) < n_items && ok; ++k) {
-        const int item = snake_item(k);
-        if (item >= n_items) continue;
-        const Item I = item_info<HB, HD>(item, n_hb, row_nt, block_range);
-        if (I.nt == 0) continue;
-        ok = mbar_wait(&sh.q_full, it & 1, &sh.abort_flag, status);
-        if (ok) ok = issue_qk(g);
+    // ---------------------------------------------------------------- MMA issuers
+    // Warp 2 issues S^T, warp 7 issues PV.  Each whole warp runs its loop, so every
+    // descriptor is warp-uniform and built as a per-tile base plus compile-time offsets; one
+    // elected lane issues each instruction.  A commit tracks the MMAs of its own warp.
+    constexpr uint32_t id_qk = idesc_bf16_f32(64, HB, 0, 0);
+    constexpr uint32_t id_pv = idesc_bf16_f32(128, HB, 1, 1);
+    const uint32_t st0 = smem_u32(sT);
+    uint32_t g = 0, it = 0;
+    bool ok = true;
+    auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, &sh.abort_flag, status));
+    };
+    const bool qk_warp = warp == 2;
+    const uint64_t dq0 = sdesc_sw128(smem_u32(sQ), 16, 1024);       // Q: B operand of S^T, K-major
+    for (int k = 0; k * static_cast<int>(gridDim.x) < n_items && ok; ++k) {
+      const int item = snake_item(k);
+      if (item >= n_items) continue;
+      const Item I = item_info<HB, HD>(item, n_hb, row_nt, block_range);
+      if (I.nt == 0) continue;
+      if (qk_warp) {
+        // S^T(g) = tile . Q^T, one 64-dim block at a time as each lands
+        ok = wait(&sh.q_full, it & 1);
         for (int i = 0; i < I.nt && ok; ++i, ++g) {
-          if (i + 1 < I.nt) ok = issue_qk(g + 1);
-          else umma_commit(&sh.q_empty);
+          const int sb = g & 1;
+          if (g >= 2 && !(ok = wait(&sh.s_empty[sb], ((g >> 1) - 1) & 1))) break;
+          tc_fence_after();
+          const uint64_t da = sdesc_sw128(st0 + (g & 1u) * (kKB * kBlkBytes), 16, 1024);
+          const uint32_t d_s = tmem + C::S_COL + sb * HB;
+#pragma unroll
+          for (int kb = 0; kb < kKB; ++kb) {
+            if (!(ok = wait(&sh.full[slot_of(g, kb)], (g >> 1) & 1))) break;
+#pragma unroll
+            for (int sub = 0; sub < 4; ++sub)
+              umma_bf16_elect(d_s, da + static_cast<uint64_t>((kb * kBlkBytes + sub * 32) >> 4),
+                              dq0 + static_cast<uint64_t>((kb * HB * 128 + sub * 32) >> 4), id_qk, (kb | sub) ? 1u : 0u);
+          }
           if (!ok) break;
-          ok = mbar_wait(&sh.p_full, g & 1, &sh.abort_flag, status);
-          if (ok && i == 0 && it > 0) ok = mbar_wait(&sh.o_free, (it - 1) & 1, &sh.abort_flag, status);
+          umma_commit_elect(&sh.s_full[sb]);
+        }
+        if (ok) umma_commit_elect(&sh.q_empty);          // Q may be replaced once these finish
+      } else {
+        // O^T += V^T P^T: A = the tile's value blocks (MN-major, 64-dim blocks one slot
+        // apart), B = P^T in the rope block (MN-major)
+        for (int i = 0; i < I.nt && ok; ++i, ++g) {
+          ok = wait(&sh.p_full, g & 1);
+          if (ok && i == 0 && it > 0) ok = wait(&sh.o_free, (it - 1) & 1);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t pb = st0 + slot_of(g, kKB - 1) * kBlkBytes;
+          const uint32_t tb = st0 + (g & 1u) * (kKB * kBlkBytes);
+          const uint64_t dv = sdesc_sw128(tb, kBlkBytes, 1024);
+          const uint64_t dp = sdesc_sw128(tb + (kKB - 1) * kBlkBytes, kBlkBytes, 1024);
+          const uint32_t acc0 = i > 0 ? 1u : 0u;
 #pragma unroll
           for (int b = 0; b < 4; ++b) {
-            const uint32_t a0 = st0 + slot_of(g, 2 * b) * kBlkBytes;
 #pragma unroll
-            for (int kq = 0; kq < kRows / 16; ++kq) {
-              umma_bf16(tmem + C::O_COL + b * HB, sdesc_sw128(a0 + kq * 2048, kBlkBytes, 1024),
-                        sdesc_sw128(pb + kq * 2048, kBlkBytes, 1024), id_pv, (i > 0 || kq > 0) ? 1u : 0u);
-            }
+            for (int kq = 0; kq < kRows / 16; ++kq)
+              umma_bf16_elect(tmem + C::O_COL + b * HB, dv + static_cast<uint64_t>((2 * b * kBlkBytes + kq * 2048) >> 4),
+                              dp + static_cast<uint64_t>((kq * 2048) >> 4), id_pv, kq > 0 ? 1u : acc0);
             // the two value blocks of this O^T block may be refilled once these finish
-            umma_commit(&sh.empty[slot_of(g, 2 * b)]);
-            umma_commit(&sh.empty[slot_of(g, 2 * b + 1)]);
+            umma_commit_elect(&sh.empty[slot_of(g, 2 * b)]);
+            umma_commit_elect(&sh.empty[slot_of(g, 2 * b + 1)]);
           }
-          umma_commit(&sh.empty[slot_of(g, kKB - 1)]);    // rope block, which also held P^T
-          umma_commit(&sh.o_done);
+          umma_commit_elect(&sh.empty[slot_of(g, kKB - 1)]);    // rope block, which also held P^T
+          umma_commit_elect(&sh.o_done);
         }
-        ++it;
       }
+      ++it;
     }
   }
   tc_fence_before();
