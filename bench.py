@@ -145,11 +145,21 @@ def roofline_numbers(w, geo):
     pairs = L.sum()                                          # causal (query, key) pairs
     attn_gathered = rows * w.d_qk * 2 + w.n_q * w.n_heads * (w.d_qk + w.d_v) * 2 + w.n_q * w.topk * 4
     attn_flops = 2.0 * rows * w.n_heads * (w.d_qk + w.d_v)
-    idx_flops = 2.0 * pairs * w.n_heads_idx * w.head_dim_idx
+    idx_flops_causal = 2.0 * pairs * w.n_heads_idx * w.head_dim_idx
+    # rows whose prefix is no longer than k select all of it; only the others need scores
+    idx_flops = 2.0 * L[L > w.topk].sum() * w.n_heads_idx * w.head_dim_idx
     idx_bytes = (w.n_q * w.n_heads_idx * w.head_dim_idx * 2 + geo.n_kv * w.head_dim_idx * 2 + w.n_q * w.n_heads_idx * 4
                  + w.n_q * w.topk * 4)
+    attn_min_bytes = (w.n_q * w.n_heads * w.d_qk * 2 + geo.n_kv * w.d_qk * 2 + w.n_q * w.topk * 4
+                      + w.n_q * w.n_heads * (w.d_v * 2 + 4))
     return dict(attn_gathered=float(attn_gathered), attn_flops=attn_flops, idx_flops=idx_flops,
-                idx_bytes=float(idx_bytes), rows=int(rows), pairs=int(pairs))
+                idx_flops_causal=idx_flops_causal, idx_bytes=float(idx_bytes), attn_min_bytes=float(attn_min_bytes),
+                rows=int(rows), pairs=int(pairs))
+
+
+# DRAM bytes (read + write) of one sparse_attn_kernel launch on this workload from an ncu
+# capture of the current kernel (profiles/sparse_attn_prefill_4k.md); None when not measured.
+ATTN_TRAFFIC_BYTES = 147.05e6
 
 
 def peaks():
@@ -370,14 +380,22 @@ def run_native(args):
         "e2e": {"value": ws_n * w.n_q / (e2e_ms / 1e3), "unit": "query_tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": gpu_launches * args.steps,
-        "roofline": {"kernel": "sparse_attn_kernel", "bound": "hbm", "achieved": attn_gbs, "peak": hbm, "unit": "GB/s",
-                     "frac": attn_gbs / hbm, "traffic": None, "peak_kind": peak_kind,
-                     "algorithmic_bytes_per_launch": R["attn_gathered"], "ms_per_launch": attn_ms,
-                     "strict_tensor_tflops": attn_strict_tflops, "strict_tensor_frac": attn_strict_tflops / tc_sus},
-        "roofline_indexer": {"kernel": "indexer (rope + tcgen05 scores/top-k + select)", "bound": "tensor",
+        # The latent cache of one layer is L2-resident at this size, so the binding roofline of
+        # the attention is the tensor one: selected (query, head, row) triples x (576 + 512) x 2
+        # FLOPs.  The minimum HBM bytes (inputs once + outputs) and the bytes a per-token gather
+        # would move are given for context.
+        "roofline": {"kernel": "sparse_attn_kernel", "bound": "tensor", "achieved": attn_strict_tflops,
+                     "peak": tc_burst, "unit": "TFLOP/s", "frac": attn_strict_tflops / tc_burst,
+                     "traffic": ATTN_TRAFFIC_BYTES, "peak_kind": peak_kind + " (bf16 burst)",
+                     "algorithmic_flops_per_launch": R["attn_flops"], "ms_per_launch": attn_ms,
+                     "min_hbm_bytes_per_launch": R["attn_min_bytes"],
+                     "min_hbm_frac": R["attn_min_bytes"] / (attn_ms / 1e3) / 1e9 / hbm,
+                     "per_token_gather_bytes_per_launch": R["attn_gathered"], "per_token_gather_gbs": attn_gbs},
+        "roofline_indexer": {"kernel": "indexer call (rope + tcgen05 scores/top-k + select)", "bound": "tensor",
                              "achieved": idx_tflops, "peak": tc_burst, "unit": "TFLOP/s", "frac": idx_tflops / tc_burst,
-                             "algorithmic_flops_per_launch": R["idx_flops"], "ms_per_launch": idx_ms,
-                             "peak_kind": peak_kind},
+                             "algorithmic_flops_per_launch": R["idx_flops"],
+                             "causal_flops_per_launch": R["idx_flops_causal"], "ms_per_launch": idx_ms,
+                             "peak_kind": peak_kind + " (bf16 burst)"},
         "clocks": clk.summary(),
     }
     if rank == 0 and not args.no_cpu_baseline:
