@@ -322,12 +322,12 @@ def run_native(args):
             fn()
             b.record(stream)
         torch.cuda.synchronize()
-        return sum(a.elapsed_time(b) for a, b in e) / n
+        return statistics.median(a.elapsed_time(b) for a, b in e)
 
     attn_ms = time_call(lambda: D.dsa_sparse_attn(adesc, L0["q"], L0["kv"], idx_full, ks, L0["out"], L0["lse"],
-                                                  ws=attn_ws, stream=stream), 10)
+                                                  ws=attn_ws, stream=stream), 20)
     idx_ms = time_call(lambda: D.dsa_indexer_topk(idesc, L0["q_idx"], L0["k_idx"], L0["w"], q_pos, k_pos, ks, ke, rope,
-                                                  idx_full, None, ws=idx_ws, stream=stream), 10)
+                                                  idx_full, None, ws=idx_ws, stream=stream), 20)
 
     # ---------------- end to end through the C ABI from pinned host buffers
     in_keys = ("q_idx", "k_idx", "w", "q", "kv")
@@ -390,7 +390,10 @@ def run_native(args):
                      "algorithmic_flops_per_launch": R["attn_flops"], "ms_per_launch": attn_ms,
                      "min_hbm_bytes_per_launch": R["attn_min_bytes"],
                      "min_hbm_frac": R["attn_min_bytes"] / (attn_ms / 1e3) / 1e9 / hbm,
-                     "per_token_gather_bytes_per_launch": R["attn_gathered"], "per_token_gather_gbs": attn_gbs},
+                     "per_token_gather_bytes_per_launch": R["attn_gathered"], "per_token_gather_gbs": attn_gbs,
+                     # the gather framing of the roofline (each token reads its own rows from HBM);
+                     # above 1 means rows were reused from L2 / shared memory across tokens
+                     "per_token_gather_frac_of_hbm": attn_gbs / hbm},
         "roofline_indexer": {"kernel": "indexer call (rope + tcgen05 scores/top-k + select)", "bound": "tensor",
                              "achieved": idx_tflops, "peak": tc_burst, "unit": "TFLOP/s", "frac": idx_tflops / tc_burst,
                              "algorithmic_flops_per_launch": R["idx_flops"],

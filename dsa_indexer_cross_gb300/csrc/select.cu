@@ -16,8 +16,116 @@ namespace dsa {
 namespace {
 
 constexpr int kSelThreads = 256;
+constexpr int kBins = 2048;         // linear bins over the row's [min, max] key range
+constexpr int kBoundaryMax = 256;   // boundary-bin entries ranked directly; more -> radix passes
 constexpr int kSelPer = 17;    // entries per thread kept in registers (rows up to 4352 candidates)
 constexpr int kMaxChunks = 64;
+
+// Exact top-K threshold in one histogram pass for rows whose scores are spread out: 2048
+// bins linear in score over [min, max] locate the bin holding the K-th entry, and the entries
+// of that bin (normally a handful) are ranked directly by (key desc, index asc).  Returns
+// false, before touching (v, cut), when that bin holds more than kBoundaryMax entries (many
+// equal or nearly equal scores); the caller then runs the radix passes.  Same contract as
+// radix_threshold: exactly K entries satisfy key > v || (key == v && idx <= cut).
+struct LinearSmem {
+  uint32_t hist[kBins];
+  uint32_t bkey[kBoundaryMax];
+  int32_t bidx[kBoundaryMax];
+  uint32_t wmin[kSelThreads / 32], wmax[kSelThreads / 32];
+  int wsum[kSelThreads / 32];
+  int misc[8];
+};
+
+template <class ForEach>
+__device__ bool linear_threshold(const ForEach& fe, int tid, int K, LinearSmem& L, uint32_t& v, uint32_t& cut) {
+  const int lane = tid & 31, w = tid >> 5;
+  uint32_t mn = 0xFFFFFFFFu, mx = 0u;
+  fe([&](uint32_t key, int32_t) {
+    mn = min(mn, key);
+    mx = max(mx, key);
+  });
+  mn = __reduce_min_sync(0xffffffffu, mn);
+  mx = __reduce_max_sync(0xffffffffu, mx);
+  if (lane == 0) {
+    L.wmin[w] = mn;
+    L.wmax[w] = mx;
+  }
+  for (int i = tid; i < kBins; i += kSelThreads) L.hist[i] = 0u;
+  if (tid == 0) L.misc[3] = 0;
+  __syncthreads();
+  uint32_t kmin = L.wmin[0], kmax = L.wmax[0];
+#pragma unroll
+  for (int i = 1; i < kSelThreads / 32; ++i) {
+    kmin = min(kmin, L.wmin[i]);
+    kmax = max(kmax, L.wmax[i]);
+  }
+  // bins are linear in score value (keys are log-spaced); (f - fmin) * scale is monotone
+  // non-decreasing in f under round-to-nearest, so a higher bin never holds a smaller score
+  const float fmin = key_float(kmin), fmax = key_float(kmax);
+  const float span = fmax - fmin;
+  const float scale = span > 0.f && span < 3.0e38f ? static_cast<float>(kBins) / span : 0.f;
+  auto bin_of = [&](uint32_t key) {
+    const float y = (key_float(key) - fmin) * scale;
+    return y >= static_cast<float>(kBins - 1) ? kBins - 1 : (y > 0.f ? static_cast<int>(y) : 0);
+  };
+  fe([&](uint32_t key, int32_t) { atomicAdd(&L.hist[bin_of(key)], 1u); });
+  __syncthreads();
+  // thread tid owns the 8 bins [kBins - 8 tid - 8, kBins - 8 tid), visited from the top
+  constexpr int kPerT = kBins / kSelThreads;
+  int h[kPerT], sum = 0;
+#pragma unroll
+  for (int j = 0; j < kPerT; ++j) {
+    h[j] = static_cast<int>(L.hist[kBins - 1 - (tid * kPerT + j)]);
+    sum += h[j];
+  }
+  int x = sum;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
+  }
+  if (lane == 31) L.wsum[w] = x;
+  __syncthreads();
+  int c = x - sum;
+  for (int i = 0; i < w; ++i) c += L.wsum[i];
+  if (c < K && K <= c + sum) {
+#pragma unroll
+    for (int j = 0; j < kPerT; ++j) {
+      if (c < K && K <= c + h[j]) {
+        L.misc[0] = kBins - 1 - (tid * kPerT + j);
+        L.misc[1] = c;
+        L.misc[2] = h[j];
+      }
+      c += h[j];
+    }
+  }
+  __syncthreads();
+  const int b = L.misc[0], above = L.misc[1], hb = L.misc[2];
+  if (hb > kBoundaryMax) return false;
+  fe([&](uint32_t key, int32_t idx) {
+    if (bin_of(key) == b) {
+      const int slot = atomicAdd(&L.misc[3], 1);
+      L.bkey[slot] = key;
+      L.bidx[slot] = idx;
+    }
+  });
+  __syncthreads();
+  const int need = K - above;   // 1 <= need <= hb
+  for (int i = tid; i < hb; i += kSelThreads) {
+    const uint32_t ki = L.bkey[i];
+    const int32_t ii = L.bidx[i];
+    int rank = 0;
+    for (int j = 0; j < hb; ++j) rank += (L.bkey[j] > ki || (L.bkey[j] == ki && L.bidx[j] < ii)) ? 1 : 0;
+    if (rank == need - 1) {
+      L.misc[4] = static_cast<int>(ki);
+      L.misc[5] = ii;
+    }
+  }
+  __syncthreads();
+  v = static_cast<uint32_t>(L.misc[4]);
+  cut = static_cast<uint32_t>(L.misc[5]);
+  return true;
+}
 
 template <bool kRegs>
 __global__ void __launch_bounds__(kSelThreads) select_kernel(int n_chunks, int cap, int topk, int trivial_len,
@@ -31,6 +139,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(int n_chunks, int c
   __shared__ int bc[4];
   __shared__ int start[kMaxChunks + 1];
   __shared__ int warp_tot[kSelThreads / 32];
+  __shared__ LinearSmem lin;
   const int t = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int2 r = row_range[t];
@@ -99,7 +208,10 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(int n_chunks, int c
   };
   uint32_t v = 0, cut = 0x7FFFFFFFu;
   const bool take_all = total <= kt;
-  if (kt > 0 && !take_all) radix_threshold<kSelThreads>([] { __syncthreads(); }, fe, tid, kt, hist, bc, v, cut);
+  if (kt > 0 && !take_all && !linear_threshold(fe, tid, kt, lin, v, cut)) {
+    __syncthreads();
+    radix_threshold<kSelThreads>([] { __syncthreads(); }, fe, tid, kt, hist, bc, v, cut);
+  }
   // stable compaction of the kept entries in list (= key index) order
   int keep = 0;
   fe([&](uint32_t key, int32_t idx) { keep += (take_all || topk_keep(key, idx, v, cut)) ? 1 : 0; });

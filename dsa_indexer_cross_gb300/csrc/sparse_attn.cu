@@ -693,35 +693,58 @@ __global__ void __launch_bounds__(256) row_tiles_kernel(const int32_t* __restric
 }
 
 // block_range[b] = [min, max + 1) of the in-range latent rows selected by tokens
-// [b*B, b*B + B); (0, 0) when none.  One warp per block.
+// [b*B, b*B + B); (0, 0) when none.  One CTA per block, 16-byte loads of the index rows when
+// they are 16-byte aligned.
 __global__ void __launch_bounds__(256) block_range_kernel(const int32_t* __restrict__ idx,
                                                           const int32_t* __restrict__ ks, int n_q, int n_kv,
                                                           int topk, int B, int2* __restrict__ block_range) {
-  const int blk = blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  const int n_blk = (n_q + B - 1) / B;
-  if (blk >= n_blk) return;
+  __shared__ long long kst[64];
+  __shared__ int red_lo[8], red_hi[8];
+  const int blk = blockIdx.x;
+  const int t0 = blk * B;
+  const int nt = min(B, n_q - t0);
+  for (int i = threadIdx.x; i < nt; i += blockDim.x) kst[i] = __ldg(ks + t0 + i);
+  __syncthreads();
   int lo = 0x7FFFFFFF, hi = -1;
-  for (int b = 0; b < B; ++b) {
-    const int t = blk * B + b;
-    if (t >= n_q) break;
-    const long long kst = __ldg(ks + t);
-    const int32_t* irow = idx + static_cast<size_t>(t) * topk;
-    for (int s = lane; s < topk; s += 32) {
-      const int j = __ldg(irow + s);
-      const long long row = kst + j;
-      if (j >= 0 && row >= 0 && row < n_kv) {
-        lo = min(lo, static_cast<int>(row));
-        hi = max(hi, static_cast<int>(row));
-      }
+  auto take = [&](int j, int b) {
+    const long long row = kst[b] + j;
+    if (j >= 0 && row >= 0 && row < n_kv) {
+      lo = min(lo, static_cast<int>(row));
+      hi = max(hi, static_cast<int>(row));
     }
+  };
+  const int32_t* base = idx + static_cast<size_t>(t0) * topk;
+  const int total = nt * topk;
+  if ((topk & 3) == 0 && (reinterpret_cast<uintptr_t>(base) & 15) == 0) {
+    for (int e = threadIdx.x * 4; e < total; e += blockDim.x * 4) {
+      const int4 v = __ldg(reinterpret_cast<const int4*>(base + e));
+      const int b = e / topk;        // the four entries belong to one token (topk % 4 == 0)
+      take(v.x, b);
+      take(v.y, b);
+      take(v.z, b);
+      take(v.w, b);
+    }
+  } else {
+    for (int e = threadIdx.x; e < total; e += blockDim.x) take(__ldg(base + e), e / topk);
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
     lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, off));
     hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, off));
   }
-  if (lane == 0) block_range[blk] = hi >= lo ? make_int2(lo, hi + 1) : make_int2(0, 0);
+  const int w = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) {
+    red_lo[w] = lo;
+    red_hi[w] = hi;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int i = 1; i < static_cast<int>(blockDim.x >> 5); ++i) {
+      lo = min(lo, red_lo[i]);
+      hi = max(hi, red_hi[i]);
+    }
+    block_range[blk] = hi >= lo ? make_int2(lo, hi + 1) : make_int2(0, 0);
+  }
 }
 
 template <int HB, int HD>
@@ -769,7 +792,7 @@ cudaError_t launch_sparse_attn(const CUtensorMap& tmap_kv, int n_q, int n_kv, in
     const int B = kDenseCols / hd;
     const int n_blk = (n_q + B - 1) / B;
     int2* br = static_cast<int2*>(scratch);
-    block_range_kernel<<<(n_blk + 7) / 8, 256, 0, st>>>(idx, ks, n_q, n_kv, topk, B, br);
+    block_range_kernel<<<n_blk, 256, 0, st>>>(idx, ks, n_q, n_kv, topk, B, br);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     switch (hd) {
       case 1: return launch_cfg<kDenseCols, 1>(tmap_kv, n_q, n_kv, n_heads, topk, scale, q, kv, idx, ks, nullptr, br, out, lse, status, st);
