@@ -186,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&sh.q_empty, 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sh.t_full[b], 1);
-      mbar_init(&sh.t_empty[b], kEpiThreads);
+      mbar_init(&sh.t_empty[b], kEpiThreads / 32);   // one arrive per epilogue warp
     }
     sh.abort_flag = 0;
     sh.epi_abort = 0;
@@ -351,7 +351,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             else acc[g] = part[g][0];
           }
           tc_fence_before();
-          mbar_arrive(&sh.t_empty[buf]);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh.t_empty[buf]);
           if (fast) {
             // every in-range key is appended: key j of query g goes to slot j - a_g
             const int j = tile0 + row;

@@ -204,11 +204,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&sh.q_empty, 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sh.s_full[b], 1);
-      mbar_init(&sh.s_empty[b], kSoft);
+      mbar_init(&sh.s_empty[b], kSoft / 32);   // one arrive per softmax warp
     }
-    mbar_init(&sh.p_full, kSoft);
+    mbar_init(&sh.p_full, kSoft / 32);
     mbar_init(&sh.o_done, 1);
-    mbar_init(&sh.o_free, kSoft);
+    mbar_init(&sh.o_free, kSoft / 32);
     sh.abort_flag = 0;
     sh.soft_abort = 0;
     fence_mbar_init();
@@ -421,7 +421,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_16x256b<NR>(tmem + t_lane + C::S_COL + sb * HB, v);
           tmem_ld_wait();
           tc_fence_before();
-          mbar_arrive(&sh.s_empty[sb]);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh.s_empty[sb]);
 #pragma unroll
           for (int kk = 0; kk < NR; ++kk) {
             const float2 mu = *reinterpret_cast<const float2*>(&sh.m_used[8 * kk + cq]);
@@ -544,7 +545,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (i > 0) (void)mbar_wait(&sh.o_done, (g - 1) & 1, &sh.abort_flag, status);
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(&sh.p_full);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.p_full);
       }
       if (stop) break;
       // item end: column sums over the 64 rows, then O^T / l -> out
@@ -598,7 +600,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             lv > 0.f ? (sh.m_used[tid] + log2f(lv)) * 0.69314718055994531f : -INFINITY;
       }
       tc_fence_before();
-      mbar_arrive(&sh.o_free);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.o_free);
       named_bar_sync(1, kSoft);                                 // per-column state and mask may be reset now
       ++it;
     }
