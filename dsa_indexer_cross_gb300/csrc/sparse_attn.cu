@@ -109,13 +109,10 @@ __device__ __forceinline__ void load_row16(float (&r)[16], const float* p) {
     r[4 * i + 3] = v.w;
   }
 }
-// Stores through explicit state spaces (the compiler then knows they cannot alias the
-// shared-memory loads around them).
+// Store through the explicit shared state space (the compiler then knows it cannot alias the
+// shared-memory loads around it).
 __device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v) {
   asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-__device__ __forceinline__ void st_global_u16(uint16_t* p, uint16_t v) {
-  asm volatile("{\n .reg .u64 ga;\n cvta.to.global.u64 ga, %0;\n st.global.u16 [ga], %1;\n}\n" ::"l"(p), "h"(v) : "memory");
 }
 
 // 2^x by the hardware approximation (ex2.approx.ftz.f32; relative error far below the bf16
@@ -360,42 +357,89 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < 2 * NR; ++c) lp[c] = 0.f;
       const int32_t* irow = idx + static_cast<size_t>(I.t0) * topk;
       if constexpr (DENSE) {
-        // selection bitmask over the block's key range [lo, lo + nt*64); bits that fall in
-        // the same word are OR-ed across the warp before one shared atomic
+        // selection bitmask over the block's key range [lo, lo + nt*64)
         const int words = I.nt * (kRows / 32);
         for (int e = tid; e < B * words; e += kSoft) sMask[(e / words) * (C::MAXR / 32) + (e % words)] = 0u;
         named_bar_sync(1, kSoft);
-        constexpr int kU = 8;     // index loads in flight per thread
-        for (int base = 0; base < B * topk; base += kSoft * kU) {
-          int jv[kU];
-          long long kv0[kU];
-#pragma unroll
-          for (int u = 0; u < kU; ++u) {
-            const int e = base + u * kSoft + tid;
-            const int t = I.t0 + (e < B * topk ? e / topk : 0);
-            const bool in = e < B * topk && t < n_q;
-            jv[u] = in ? __ldg(irow + e) : -1;
-            kv0[u] = in ? static_cast<long long>(__ldg(ks + t)) : 0;
+        // One selection: (word, bit) of the mask, or word -1 for a -1 slot or a bad index.
+        const int n_tok = min(B, n_q - I.t0);
+        auto locate = [&](int b, int j, long long k0, int& word, uint32_t& bit) {
+          word = -1;
+          bit = 0u;
+          if (j < 0) return;
+          const long long row = k0 + j;
+          if (row < 0 || row >= n_kv) {
+            atomicOr(status, DEV_ERR_BAD_INDEX);
+            atomicAdd(bad_count, 1u);
+            return;
           }
+          const int o = static_cast<int>(row - I.lo);
+          word = b * (C::MAXR / 32) + (o >> 5);
+          bit = 1u << (o & 31);
+        };
+        // OR the bits of each run of adjacent lanes that hit the same word, then one shared
+        // atomic per run (scalar path).
+        auto warp_or = [&](int word, uint32_t bits) {
 #pragma unroll
-          for (int u = 0; u < kU; ++u) {
-            const int e = base + u * kSoft + tid;
-            int word = -1;
-            uint32_t bit = 0u;
-            if (jv[u] >= 0) {
-              const long long row = kv0[u] + jv[u];
-              if (row < 0 || row >= n_kv) {
-                atomicOr(status, DEV_ERR_BAD_INDEX);
-                atomicAdd(bad_count, 1u);
-              } else {
-                const int o = static_cast<int>(row - I.lo);
-                word = (e / topk) * (C::MAXR / 32) + (o >> 5);
-                bit = 1u << (o & 31);
-              }
+          for (int off = 1; off < 32; off <<= 1) {
+            const uint32_t y = __shfl_down_sync(0xffffffffu, bits, off);
+            const int wo = __shfl_down_sync(0xffffffffu, word, off);
+            if (lane + off < 32 && wo == word) bits |= y;
+          }
+          const int wp = __shfl_up_sync(0xffffffffu, word, 1);
+          if (word >= 0 && (lane == 0 || wp != word)) atomicOr(&sMask[word], bits);
+        };
+        const int E = n_tok * topk;   // index entries of the block's valid tokens
+        if ((topk & 3) == 0 && (reinterpret_cast<uintptr_t>(irow) & 15u) == 0) {
+          // 16-byte loads, all of a round issued before any is used: with 4 tokens x 2048
+          // slots the whole block is one round
+          constexpr int kV = 16;
+          for (int base = 0; base < E; base += kSoft * 4 * kV) {
+            int4 v[kV];
+            long long k0[kV];
+#pragma unroll
+            for (int m = 0; m < kV; ++m) {
+              const int e = base + (m * kSoft + tid) * 4;
+              const bool in = e < E;
+              v[m] = in ? __ldg(reinterpret_cast<const int4*>(irow + e)) : make_int4(-1, -1, -1, -1);
+              k0[m] = in ? static_cast<long long>(__ldg(ks + I.t0 + e / topk)) : 0;
             }
-            const uint32_t peers = __match_any_sync(0xffffffffu, word);
-            const uint32_t bits = __reduce_or_sync(peers, bit);
-            if (word >= 0 && lane == __ffs(peers) - 1) atomicOr(&sMask[word], bits);
+#pragma unroll
+            for (int m = 0; m < kV; ++m) {
+              const int e = base + (m * kSoft + tid) * 4;
+              const int b = e < E ? e / topk : 0;   // the four entries share a token (topk % 4 == 0)
+              // the thread's four entries usually fall in one or two words: OR locally, then
+              // plain shared atomics (no cross-lane chain, so the groups overlap)
+              const int jj[4] = {v[m].x, v[m].y, v[m].z, v[m].w};
+              int w0 = -1;
+              uint32_t bits0 = 0u;
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                int w;
+                uint32_t bt;
+                locate(b, jj[q], k0[m], w, bt);
+                if (w < 0) continue;
+                if (w0 < 0) w0 = w;
+                if (w == w0) {
+                  bits0 |= bt;
+                } else {
+                  atomicOr(&sMask[w0], bits0);
+                  w0 = w;
+                  bits0 = bt;
+                }
+              }
+              if (w0 >= 0) atomicOr(&sMask[w0], bits0);
+            }
+          }
+        } else {
+          for (int e = tid; e < ((E + kSoft - 1) / kSoft) * kSoft; e += kSoft) {
+            int w = -1;
+            uint32_t bt = 0u;
+            if (e < E) {
+              const int b = e / topk;
+              locate(b, __ldg(irow + e), __ldg(ks + I.t0 + b), w, bt);
+            }
+            warp_or(w, bt);
           }
         }
       }
@@ -570,26 +614,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       named_bar_sync(1, kSoft);
       if (stop) break;
       tc_fence_after();
-      const int lane_d = lane;   // O^T rows: thread = dimension within the quarter
+      // Column c is output row row0 + c in both walks (block-dense: HD == H, so the block's
+      // (token, head) rows are consecutive; gather: the head block of one token); this thread
+      // writes dimension b*128 + qd*32 + lane of every valid column.
+      {
+        const long long row0 = static_cast<long long>(I.t0) * H + (DENSE ? 0 : I.hb * HB);
+        const int n_cols = DENSE ? min(HB, (n_q - I.t0) * H) : min(HB, H - I.hb * HB);
+        uint16_t* obase = out + row0 * kDv + qd * 32 + lane;
 #pragma unroll
-      for (int hh = 0; hh < HB / 16; ++hh) {
-        float inv[16];
-        load_row16(inv, &sh.l_run[hh * 16]);
+        for (int hh = 0; hh < HB / 16; ++hh) {
+          float inv[16];
+          load_row16(inv, &sh.l_run[hh * 16]);
 #pragma unroll
-        for (int h = 0; h < 16; ++h) inv[h] = inv[h] > 0.f ? 1.f / inv[h] : 0.f;
+          for (int h = 0; h < 16; ++h) inv[h] = inv[h] > 0.f ? 1.f / inv[h] : 0.f;
+          uint32_t o[4][16];
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          uint32_t o[16];
-          tmem_ld16(tmem + t_lane + C::O_COL + b * HB + hh * 16, o);
+          for (int b = 0; b < 4; ++b) tmem_ld16(tmem + t_lane + C::O_COL + b * HB + hh * 16, o[b]);
           tmem_ld_wait();
-          const int d = b * 128 + qd * 32 + lane_d;
 #pragma unroll
           for (int h = 0; h < 16; ++h) {
             const int c = hh * 16 + h;
-            if (col_ok(c)) {
-              const __nv_bfloat16 ob = __float2bfloat16_rn(__uint_as_float(o[h]) * inv[h]);
-              st_global_u16(out + (static_cast<size_t>(col_token(c)) * H + col_head(c)) * kDv + d,
-                            *reinterpret_cast<const uint16_t*>(&ob));
+            if (c < n_cols) {
+              uint16_t* orow = obase + static_cast<long long>(c) * kDv;
+#pragma unroll
+              for (int b = 0; b < 4; ++b) {
+                const __nv_bfloat16 ob = __float2bfloat16_rn(__uint_as_float(o[b][h]) * inv[h]);
+                orow[b * 128] = *reinterpret_cast<const uint16_t*>(&ob);
+              }
             }
           }
         }
@@ -771,6 +822,8 @@ cudaError_t launch_cfg(const CUtensorMap& tmap, int n_q, int n_kv, int H, int to
 int sparse_attn_dense_heads(int n_heads, int n_kv, int topk) {
   // block-dense walk pays off when each row of the block's key range is selected by
   // several of the block's tokens; it needs the whole range to fit the selection mask.
+  // Returns n_heads: the walk takes all heads of a token (HD == H, which the kernel's output
+  // row mapping relies on).
   if (n_heads != 1 && n_heads != 2 && n_heads != 4 && n_heads != 8 && n_heads != 16) return 0;
   const int B = kDenseCols / n_heads;
   const int maxr = (kMaskBytes * 8 / B) / 64 * 64;
