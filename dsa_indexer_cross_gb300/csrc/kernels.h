@@ -53,7 +53,8 @@ cudaError_t launch_select(int n_q, int n_chunks, int cap, int topk, int trivial_
 // ---------------------------------------------------------------------------- sparse attention
 // Heads of the block-dense walk for this shape, or 0 for the per-token gather walk.
 int sparse_attn_dense_heads(int n_heads, int n_kv, int topk);
-// Scratch bytes launch_sparse_attn needs (per-row tile counts or per-block key ranges).
+// Scratch bytes launch_sparse_attn needs (per-row tile counts, or per-block key ranges and
+// selection bitmasks).
 size_t sparse_attn_ws_bytes(int n_q, int n_heads, int n_kv, int topk);
 // tmap_kv: kv as [n_kv x 576] bf16, 128-byte swizzled boxes of {64, 64} (read by the
 // block-dense walk only).

@@ -169,8 +169,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     sparse_attn_kernel(const __grid_constant__ CUtensorMap tmap_kv, const uint16_t* __restrict__ q,
                        const uint16_t* __restrict__ kv, const int32_t* __restrict__ idx,
                        const int32_t* __restrict__ ks, const int32_t* __restrict__ row_nt,
-                       const int2* __restrict__ block_range, uint16_t* __restrict__ out, float* __restrict__ lse,
-                       int n_q, int n_kv, int H, int topk, float scale_log2, uint32_t* status, uint32_t* bad_count) {
+                       const int2* __restrict__ block_range, const uint32_t* __restrict__ block_mask,
+                       uint16_t* __restrict__ out, float* __restrict__ lse, int n_q, int n_kv, int H, int topk,
+                       float scale_log2, uint32_t* status, uint32_t* bad_count) {
   using C = ACfg<HB, HD>;
   constexpr bool DENSE = C::DENSE;
   constexpr int B = C::B;
@@ -357,90 +358,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < 2 * NR; ++c) lp[c] = 0.f;
       const int32_t* irow = idx + static_cast<size_t>(I.t0) * topk;
       if constexpr (DENSE) {
-        // selection bitmask over the block's key range [lo, lo + nt*64)
-        const int words = I.nt * (kRows / 32);
-        for (int e = tid; e < B * words; e += kSoft) sMask[(e / words) * (C::MAXR / 32) + (e % words)] = 0u;
-        named_bar_sync(1, kSoft);
-        // One selection: (word, bit) of the mask, or word -1 for a -1 slot or a bad index.
-        const int n_tok = min(B, n_q - I.t0);
-        auto locate = [&](int b, int j, long long k0, int& word, uint32_t& bit) {
-          word = -1;
-          bit = 0u;
-          if (j < 0) return;
-          const long long row = k0 + j;
-          if (row < 0 || row >= n_kv) {
-            atomicOr(status, DEV_ERR_BAD_INDEX);
-            atomicAdd(bad_count, 1u);
-            return;
-          }
-          const int o = static_cast<int>(row - I.lo);
-          word = b * (C::MAXR / 32) + (o >> 5);
-          bit = 1u << (o & 31);
-        };
-        // OR the bits of each run of adjacent lanes that hit the same word, then one shared
-        // atomic per run (scalar path).
-        auto warp_or = [&](int word, uint32_t bits) {
+        // the item's selection bitmask over its key range, built by the pre-pass: one
+        // round of 16-byte loads into shared memory
+        constexpr int kVec = kMaskBytes / 16;
+        const int4* gm = reinterpret_cast<const int4*>(block_mask) + static_cast<size_t>(item) * kVec;
+        int4 mv[(kVec + kSoft - 1) / kSoft];
 #pragma unroll
-          for (int off = 1; off < 32; off <<= 1) {
-            const uint32_t y = __shfl_down_sync(0xffffffffu, bits, off);
-            const int wo = __shfl_down_sync(0xffffffffu, word, off);
-            if (lane + off < 32 && wo == word) bits |= y;
-          }
-          const int wp = __shfl_up_sync(0xffffffffu, word, 1);
-          if (word >= 0 && (lane == 0 || wp != word)) atomicOr(&sMask[word], bits);
-        };
-        const int E = n_tok * topk;   // index entries of the block's valid tokens
-        if ((topk & 3) == 0 && (reinterpret_cast<uintptr_t>(irow) & 15u) == 0) {
-          // 16-byte loads, all of a round issued before any is used: with 4 tokens x 2048
-          // slots the whole block is one round
-          constexpr int kV = 16;
-          for (int base = 0; base < E; base += kSoft * 4 * kV) {
-            int4 v[kV];
-            long long k0[kV];
+        for (int u = 0; u < (kVec + kSoft - 1) / kSoft; ++u) {
+          const int e = tid + u * kSoft;
+          if (e < kVec) mv[u] = __ldg(gm + e);
+        }
 #pragma unroll
-            for (int m = 0; m < kV; ++m) {
-              const int e = base + (m * kSoft + tid) * 4;
-              const bool in = e < E;
-              v[m] = in ? __ldg(reinterpret_cast<const int4*>(irow + e)) : make_int4(-1, -1, -1, -1);
-              k0[m] = in ? static_cast<long long>(__ldg(ks + I.t0 + e / topk)) : 0;
-            }
-#pragma unroll
-            for (int m = 0; m < kV; ++m) {
-              const int e = base + (m * kSoft + tid) * 4;
-              const int b = e < E ? e / topk : 0;   // the four entries share a token (topk % 4 == 0)
-              // the thread's four entries usually fall in one or two words: OR locally, then
-              // plain shared atomics (no cross-lane chain, so the groups overlap)
-              const int jj[4] = {v[m].x, v[m].y, v[m].z, v[m].w};
-              int w0 = -1;
-              uint32_t bits0 = 0u;
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                int w;
-                uint32_t bt;
-                locate(b, jj[q], k0[m], w, bt);
-                if (w < 0) continue;
-                if (w0 < 0) w0 = w;
-                if (w == w0) {
-                  bits0 |= bt;
-                } else {
-                  atomicOr(&sMask[w0], bits0);
-                  w0 = w;
-                  bits0 = bt;
-                }
-              }
-              if (w0 >= 0) atomicOr(&sMask[w0], bits0);
-            }
-          }
-        } else {
-          for (int e = tid; e < ((E + kSoft - 1) / kSoft) * kSoft; e += kSoft) {
-            int w = -1;
-            uint32_t bt = 0u;
-            if (e < E) {
-              const int b = e / topk;
-              locate(b, __ldg(irow + e), __ldg(ks + I.t0 + b), w, bt);
-            }
-            warp_or(w, bt);
-          }
+        for (int u = 0; u < (kVec + kSoft - 1) / kSoft; ++u) {
+          const int e = tid + u * kSoft;
+          if (e < kVec) reinterpret_cast<int4*>(sMask)[e] = mv[u];
         }
       }
       named_bar_sync(1, kSoft);
@@ -746,30 +677,47 @@ __global__ void __launch_bounds__(256) row_tiles_kernel(const int32_t* __restric
   if (lane == 0) row_nt[t] = (last + kRows) / kRows;
 }
 
-// block_range[b] = [min, max + 1) of the in-range latent rows selected by tokens
-// [b*B, b*B + B); (0, 0) when none.  One CTA per block, 16-byte loads of the index rows when
-// they are 16-byte aligned.
-__global__ void __launch_bounds__(256) block_range_kernel(const int32_t* __restrict__ idx,
-                                                          const int32_t* __restrict__ ks, int n_q, int n_kv,
-                                                          int topk, int B, int2* __restrict__ block_range) {
-  __shared__ long long kst[64];
+// Pre-pass of the block-dense walk, one CTA per block of B tokens:
+//   block_range[b] = [min, max + 1) of the in-range latent rows the block's tokens select
+//                    ((0, 0) when none);
+//   block_mask[b]  = for each token, bit o of its MAXR-bit row is set when row min + o is one of
+//                    its selections (the layout the attention kernel copies into shared memory).
+// Index slots outside [0, n_kv) are counted in the status words (they are skipped).
+template <int B, int MAXR>
+__global__ void __launch_bounds__(256) block_mask_kernel(const int32_t* __restrict__ idx,
+                                                         const int32_t* __restrict__ ks, int n_q, int n_kv,
+                                                         int topk, int2* __restrict__ block_range,
+                                                         uint32_t* __restrict__ block_mask, uint32_t* status,
+                                                         uint32_t* bad_count) {
+  constexpr int kRowWords = MAXR / 32;
+  constexpr int kWords = B * kRowWords;
+  __shared__ long long kst[B];
   __shared__ int red_lo[8], red_hi[8];
+  __shared__ alignas(16) uint32_t mask[kWords];
   const int blk = blockIdx.x;
   const int t0 = blk * B;
   const int nt = min(B, n_q - t0);
   for (int i = threadIdx.x; i < nt; i += blockDim.x) kst[i] = __ldg(ks + t0 + i);
+  for (int i = threadIdx.x; i < kWords; i += blockDim.x) mask[i] = 0u;
   __syncthreads();
+  const int32_t* base = idx + static_cast<size_t>(t0) * topk;
+  const int total = nt * topk;
+  const bool vec = (topk & 3) == 0 && (reinterpret_cast<uintptr_t>(base) & 15) == 0;
+  // pass 1: the range (and the bad-index count)
   int lo = 0x7FFFFFFF, hi = -1;
   auto take = [&](int j, int b) {
     const long long row = kst[b] + j;
-    if (j >= 0 && row >= 0 && row < n_kv) {
-      lo = min(lo, static_cast<int>(row));
-      hi = max(hi, static_cast<int>(row));
+    if (j >= 0) {
+      if (row >= 0 && row < n_kv) {
+        lo = min(lo, static_cast<int>(row));
+        hi = max(hi, static_cast<int>(row));
+      } else {
+        atomicOr(status, DEV_ERR_BAD_INDEX);
+        atomicAdd(bad_count, 1u);
+      }
     }
   };
-  const int32_t* base = idx + static_cast<size_t>(t0) * topk;
-  const int total = nt * topk;
-  if ((topk & 3) == 0 && (reinterpret_cast<uintptr_t>(base) & 15) == 0) {
+  if (vec) {
     for (int e = threadIdx.x * 4; e < total; e += blockDim.x * 4) {
       const int4 v = __ldg(reinterpret_cast<const int4*>(base + e));
       const int b = e / topk;        // the four entries belong to one token (topk % 4 == 0)
@@ -792,19 +740,45 @@ __global__ void __launch_bounds__(256) block_range_kernel(const int32_t* __restr
     red_hi[w] = hi;
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    for (int i = 1; i < static_cast<int>(blockDim.x >> 5); ++i) {
-      lo = min(lo, red_lo[i]);
-      hi = max(hi, red_hi[i]);
-    }
-    block_range[blk] = hi >= lo ? make_int2(lo, hi + 1) : make_int2(0, 0);
+  lo = red_lo[0];
+  hi = red_hi[0];
+  for (int i = 1; i < static_cast<int>(blockDim.x >> 5); ++i) {
+    lo = min(lo, red_lo[i]);
+    hi = max(hi, red_hi[i]);
   }
+  if (threadIdx.x == 0) block_range[blk] = hi >= lo ? make_int2(lo, hi + 1) : make_int2(0, 0);
+  // pass 2: the bits, relative to lo (hi - lo < n_kv <= MAXR)
+  auto mark = [&](int j, int b) {
+    const long long row = kst[b] + j;
+    if (j >= 0 && row >= 0 && row < n_kv) {
+      const int o = static_cast<int>(row) - lo;
+      atomicOr(&mask[b * kRowWords + (o >> 5)], 1u << (o & 31));
+    }
+  };
+  if (hi >= lo) {
+    if (vec) {
+      for (int e = threadIdx.x * 4; e < total; e += blockDim.x * 4) {
+        const int4 v = __ldg(reinterpret_cast<const int4*>(base + e));
+        const int b = e / topk;
+        mark(v.x, b);
+        mark(v.y, b);
+        mark(v.z, b);
+        mark(v.w, b);
+      }
+    } else {
+      for (int e = threadIdx.x; e < total; e += blockDim.x) mark(__ldg(base + e), e / topk);
+    }
+  }
+  __syncthreads();
+  uint4* dst = reinterpret_cast<uint4*>(block_mask + static_cast<size_t>(blk) * kWords);
+  for (int i = threadIdx.x; i < kWords / 4; i += blockDim.x) dst[i] = reinterpret_cast<const uint4*>(mask)[i];
 }
 
 template <int HB, int HD>
 cudaError_t launch_cfg(const CUtensorMap& tmap, int n_q, int n_kv, int H, int topk, float scale, const void* q,
                        const void* kv, const int32_t* idx, const int32_t* ks, const int32_t* row_nt,
-                       const int2* block_range, void* out, float* lse, uint32_t* status, cudaStream_t st) {
+                       const int2* block_range, const uint32_t* block_mask, void* out, float* lse, uint32_t* status,
+                       cudaStream_t st) {
   using C = ACfg<HB, HD>;
   auto kern = sparse_attn_kernel<HB, HD>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::DYN_SMEM);
@@ -812,7 +786,8 @@ cudaError_t launch_cfg(const CUtensorMap& tmap, int n_q, int n_kv, int H, int to
   const int n_items = C::DENSE ? (n_q + C::B - 1) / C::B : n_q * ((H + HB - 1) / HB);
   const int grid = n_items < device_sm_count() ? n_items : device_sm_count();
   kern<<<grid, kThreads, C::DYN_SMEM, st>>>(tmap, static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(kv),
-                                            idx, ks, row_nt, block_range, static_cast<uint16_t*>(out), lse, n_q, n_kv,
+                                            idx, ks, row_nt, block_range, block_mask, static_cast<uint16_t*>(out), lse,
+                                            n_q, n_kv,
                                             H, topk, scale * 1.4426950408889634f, status, status + 1);
   return cudaGetLastError();
 }
@@ -832,9 +807,36 @@ int sparse_attn_dense_heads(int n_heads, int n_kv, int topk) {
   return n_heads;
 }
 
+namespace {
+
+// Block-dense scratch: per token block its key range (int2), then (16-byte aligned) its
+// selection bitmask of kMaskBytes.
+size_t dense_mask_offset(int n_blk) { return (static_cast<size_t>(n_blk) * sizeof(int2) + 15) & ~size_t(15); }
+
+template <int HD>
+cudaError_t launch_dense(const CUtensorMap& tmap_kv, int n_q, int n_kv, int n_heads, int topk, float scale,
+                         const void* q, const void* kv, const int32_t* idx, const int32_t* ks, void* out, float* lse,
+                         uint32_t* status, void* scratch, cudaStream_t st) {
+  using C = ACfg<kDenseCols, HD>;
+  static_assert(C::B * (C::MAXR / 32) * 4 == kMaskBytes, "one bitmask per block fills the budget exactly");
+  const int n_blk = (n_q + C::B - 1) / C::B;
+  int2* br = static_cast<int2*>(scratch);
+  uint32_t* bm = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(scratch) + dense_mask_offset(n_blk));
+  block_mask_kernel<C::B, C::MAXR><<<n_blk, 256, 0, st>>>(idx, ks, n_q, n_kv, topk, br, bm, status, status + 1);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_cfg<kDenseCols, HD>(tmap_kv, n_q, n_kv, n_heads, topk, scale, q, kv, idx, ks, nullptr, br, bm, out,
+                                    lse, status, st);
+}
+
+}  // namespace
+
 size_t sparse_attn_ws_bytes(int n_q, int n_heads, int n_kv, int topk) {
   const int hd = sparse_attn_dense_heads(n_heads, n_kv, topk);
-  if (hd) return static_cast<size_t>((n_q + kDenseCols / hd - 1) / (kDenseCols / hd)) * sizeof(int2);
+  if (hd) {
+    const int n_blk = (n_q + kDenseCols / hd - 1) / (kDenseCols / hd);
+    return dense_mask_offset(n_blk) + static_cast<size_t>(n_blk) * kMaskBytes;
+  }
   return static_cast<size_t>(n_q) * sizeof(int32_t);
 }
 
@@ -843,29 +845,27 @@ cudaError_t launch_sparse_attn(const CUtensorMap& tmap_kv, int n_q, int n_kv, in
                                float* lse, uint32_t* status, void* scratch, cudaStream_t st) {
   if (n_q <= 0) return cudaSuccess;
   const int hd = sparse_attn_dense_heads(n_heads, n_kv, topk);
-  cudaError_t e;
   if (hd) {
-    const int B = kDenseCols / hd;
-    const int n_blk = (n_q + B - 1) / B;
-    int2* br = static_cast<int2*>(scratch);
-    block_range_kernel<<<n_blk, 256, 0, st>>>(idx, ks, n_q, n_kv, topk, B, br);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
     switch (hd) {
-      case 1: return launch_cfg<kDenseCols, 1>(tmap_kv, n_q, n_kv, n_heads, topk, scale, q, kv, idx, ks, nullptr, br, out, lse, status, st);
-      case 2: return launch_cfg<kDenseCols, 2>(tmap_kv, n_q, n_kv, n_heads, topk, scale, q, kv, idx, ks, nullptr, br, out, lse, status, st);
-      case 4: return launch_cfg<kDenseCols, 4>(tmap_kv, n_q, n_kv, n_heads, topk, scale, q, kv, idx, ks, nullptr, br, out, lse, status, st);
-      case 8: return launch_cfg<kDenseCols, 8>(tmap_kv, n_q, n_kv, n_heads, topk, scale, q, kv, idx, ks, nullptr, br, out, lse, status, st);
-      default: return launch_cfg<kDenseCols, 16>(tmap_kv, n_q, n_kv, n_heads, topk, scale, q, kv, idx, ks, nullptr, br, out, lse, status, st);
+      case 1: return launch_dense<1>(tmap_kv, n_q, n_kv, n_heads, topk, scale, q, kv, idx, ks, out, lse, status, scratch, st);
+      case 2: return launch_dense<2>(tmap_kv, n_q, n_kv, n_heads, topk, scale, q, kv, idx, ks, out, lse, status, scratch, st);
+      case 4: return launch_dense<4>(tmap_kv, n_q, n_kv, n_heads, topk, scale, q, kv, idx, ks, out, lse, status, scratch, st);
+      case 8: return launch_dense<8>(tmap_kv, n_q, n_kv, n_heads, topk, scale, q, kv, idx, ks, out, lse, status, scratch, st);
+      default: return launch_dense<16>(tmap_kv, n_q, n_kv, n_heads, topk, scale, q, kv, idx, ks, out, lse, status, scratch, st);
     }
   }
   int32_t* row_nt = static_cast<int32_t*>(scratch);
   row_tiles_kernel<<<(n_q + 7) / 8, 256, 0, st>>>(idx, n_q, topk, row_nt);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
   if (n_heads <= 16)
-    return launch_cfg<16, 0>(tmap_kv, n_q, n_kv, n_heads, topk, scale, q, kv, idx, ks, row_nt, nullptr, out, lse, status, st);
+    return launch_cfg<16, 0>(tmap_kv, n_q, n_kv, n_heads, topk, scale, q, kv, idx, ks, row_nt, nullptr, nullptr, out, lse,
+                             status, st);
   if (n_heads <= 32)
-    return launch_cfg<32, 0>(tmap_kv, n_q, n_kv, n_heads, topk, scale, q, kv, idx, ks, row_nt, nullptr, out, lse, status, st);
-  return launch_cfg<64, 0>(tmap_kv, n_q, n_kv, n_heads, topk, scale, q, kv, idx, ks, row_nt, nullptr, out, lse, status, st);
+    return launch_cfg<32, 0>(tmap_kv, n_q, n_kv, n_heads, topk, scale, q, kv, idx, ks, row_nt, nullptr, nullptr, out, lse,
+                             status, st);
+  return launch_cfg<64, 0>(tmap_kv, n_q, n_kv, n_heads, topk, scale, q, kv, idx, ks, row_nt, nullptr, nullptr, out, lse,
+                           status, st);
 }
 
 }  // namespace dsa
