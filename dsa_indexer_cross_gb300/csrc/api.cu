@@ -99,6 +99,24 @@ dsa_status tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t 
   return DSA_OK;
 }
 
+// Latent cache [rows][576] bf16 viewed as (64 dims, rows, 9 blocks of 64 dims): one box
+// {64, 64, 9} is a whole 64-row tile, landing in shared memory as nine 64-row x 128-byte
+// blocks (128-byte swizzle), the layout the attention kernel reads.  One copy per tile keeps
+// the TMA unit far busier than nine per-block copies.
+dsa_status tmap_kv_tiles(CUtensorMap* m, const void* base, uint64_t rows) {
+  auto fn = encode_fn();
+  if (!fn) return fail(DSA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[3] = {64, rows, 9};
+  cuuint64_t strides[2] = {576 * 2, 64 * 2};
+  cuuint32_t box[3] = {64, 64, 9};
+  cuuint32_t es[3] = {1, 1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(DSA_ERR_CUDA, "cuTensorMapEncodeTiled (latent tiles) failed (%d)", static_cast<int>(r));
+  return DSA_OK;
+}
+
 // ------------------------------------------------------------------ indexer plan
 bool supported_heads(int h) { return h == 4 || h == 8 || h == 16 || h == 32 || h == 64; }
 
@@ -280,7 +298,7 @@ dsa_status run_attn(const dsa_attn_desc* d, const void* q, const void* kv, const
   CUtensorMap tkv;
   std::memset(&tkv, 0, sizeof(tkv));
   if (sparse_attn_dense_heads(d->n_heads, d->n_kv, d->topk) && d->n_kv > 0) {
-    if ((s = tmap_bf16(&tkv, kv, 576, d->n_kv, 64)) != DSA_OK) return s;
+    if ((s = tmap_kv_tiles(&tkv, kv, d->n_kv)) != DSA_OK) return s;
   }
   e = launch_sparse_attn(tkv, d->n_q, d->n_kv, d->n_heads, d->topk, d->softmax_scale, q, kv, idx, ks, out, lse, status,
                          base + kAlign, st);

@@ -14,12 +14,12 @@
 //     O^T[d, c] += Rows[:, d]^T  . P^T[r, c]             M = 128 dims,  N = HB, K = 64
 // A tile is stored once in shared memory as nine 64-dim blocks in the 128-byte-swizzled
 // layout, read as a K-major operand by the first product and as an MN-major operand by the
-// second, so each row is brought on chip once per item.  Every block has its own full/empty
-// barrier pair: a block is refilled for tile g + 2 as soon as the last product of tile g
-// that reads it has finished, so loads overlap the tail of the previous tile.  P^T of tile g
-// (bf16, MN-major) is written into that tile's rope block, which the first product no longer
-// needs once S^T is complete.  S^T is double-buffered in TMEM; O^T (512 x HB fp32) stays in
-// TMEM for the whole item.
+// second, so each row is brought on chip once per item.  Two tiles are in flight, each slot set
+// with one full/empty barrier pair; block-dense tiles arrive as one 3-D TMA box (one copy of
+// 72 KB keeps the TMA unit much busier than nine 8 KB copies).  P^T of tile g (bf16, MN-major)
+// is written into that tile's rope block, which the first product no longer needs once S^T is
+// complete.  S^T is double-buffered in TMEM; O^T (512 x HB fp32) stays in TMEM for the whole
+// item.
 //
 // Two ways to walk the rows (template parameter HD):
 //   HD == 0  "gather": item = (token, block of HB heads); the tile holds the token's next
@@ -84,7 +84,7 @@ struct ACfg {
 
 // Per-column softmax state lives in shared memory (uniform across the softmax threads).
 struct AShared {
-  uint64_t full[kSlots], empty[kSlots];
+  uint64_t full[2], empty[2];   // per tile slot set (nine 64-dim blocks)
   uint64_t q_full, q_empty, s_full[2], s_empty[2], p_full, o_done, o_free;
   uint32_t tmem_base, abort_flag, soft_abort;
   uint32_t prod_ok;
@@ -194,7 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kSlots; ++s) {
+    for (int s = 0; s < 2; ++s) {
       mbar_init(&sh.full[s], DENSE ? 1 : kProd);
       mbar_init(&sh.empty[s], 1);
     }
@@ -261,19 +261,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       cp_async_mbar_arrive(&sh.q_full);
       if constexpr (DENSE) {
-        // one thread streams the block's consecutive latent rows with TMA, one 64-dim block
-        // at a time as soon as its slot is released
+        // one thread streams the block's consecutive latent rows with TMA, one whole 64-row
+        // tile (nine 64-dim blocks, one 3-D box) per copy as soon as its slot set is released
         if (tid == 0) {
           for (int i = 0; i < I.nt && ok; ++i, ++g) {
-            for (int kb = 0; kb < kKB; ++kb) {
-              const int s = slot_of(g, kb);
-              if (g >= 2) {
-                ok = mbar_wait(&sh.empty[s], ((g >> 1) - 1) & 1, &sh.abort_flag, status);
-                if (!ok) break;
-              }
-              mbar_arrive_expect_tx(&sh.full[s], kBlkBytes);
-              tma_load_2d(sT + s * kBlkBytes, &tmap_kv, &sh.full[s], kb * 64, I.lo + i * kRows);
+            const int s = g & 1;
+            if (g >= 2) {
+              ok = mbar_wait(&sh.empty[s], ((g >> 1) - 1) & 1, &sh.abort_flag, status);
+              if (!ok) break;
             }
+            mbar_arrive_expect_tx(&sh.full[s], kKB * kBlkBytes);
+            tma_load_3d(sT + slot_of(g, 0) * kBlkBytes, &tmap_kv, &sh.full[s], 0, I.lo + i * kRows, 0);
           }
         }
         ok = sync_ok(ok);
@@ -283,10 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int32_t* irow = idx + static_cast<size_t>(t) * topk;
         for (int i = 0; i < I.nt; ++i, ++g) {
           w_ok = true;
-          if (tid == 0 && g >= 2) {
-            for (int kb = 0; kb < kKB && w_ok; ++kb)
-              w_ok = mbar_wait(&sh.empty[slot_of(g, kb)], ((g >> 1) - 1) & 1, &sh.abort_flag, status);
-          }
+          if (tid == 0 && g >= 2) w_ok = mbar_wait(&sh.empty[g & 1], ((g >> 1) - 1) & 1, &sh.abort_flag, status);
           ok = sync_ok(w_ok);
           if (!ok) break;
           // resolve every chunk's row first (independent loads), then issue the copies
@@ -314,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint16_t* src = kv + static_cast<size_t>(rows[k] >= 0 ? rows[k] : 0) * kDqk + ch * 8;
             cp_async_16_zfill(smem_u32(dst + (ch >> 3) * kBlkBytes + sw128(r, ch & 7)), src, rows[k] >= 0);
           }
-          for (int kb = 0; kb < kKB; ++kb) cp_async_mbar_arrive(&sh.full[slot_of(g, kb)]);
+          cp_async_mbar_arrive(&sh.full[g & 1]);
         }
       }
       ++it;
@@ -613,18 +608,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < I.nt && ok; ++i, ++g) {
           const int sb = g & 1;
           if (g >= 2 && !(ok = wait(&sh.s_empty[sb], ((g >> 1) - 1) & 1))) break;
+          if (!(ok = wait(&sh.full[g & 1], (g >> 1) & 1))) break;
           tc_fence_after();
           const uint64_t da = sdesc_sw128(st0 + (g & 1u) * (kKB * kBlkBytes), 16, 1024);
           const uint32_t d_s = tmem + C::S_COL + sb * HB;
 #pragma unroll
           for (int kb = 0; kb < kKB; ++kb) {
-            if (!(ok = wait(&sh.full[slot_of(g, kb)], (g >> 1) & 1))) break;
 #pragma unroll
             for (int sub = 0; sub < 4; ++sub)
               umma_bf16_elect(d_s, da + static_cast<uint64_t>((kb * kBlkBytes + sub * 32) >> 4),
                               dq0 + static_cast<uint64_t>((kb * HB * 128 + sub * 32) >> 4), id_qk, (kb | sub) ? 1u : 0u);
           }
-          if (!ok) break;
           umma_commit_elect(&sh.s_full[sb]);
         }
         if (ok) umma_commit_elect(&sh.q_empty);          // Q may be replaced once these finish
@@ -646,11 +640,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kq = 0; kq < kRows / 16; ++kq)
               umma_bf16_elect(tmem + C::O_COL + b * HB, dv + static_cast<uint64_t>((2 * b * kBlkBytes + kq * 2048) >> 4),
                               dp + static_cast<uint64_t>((kq * 2048) >> 4), id_pv, kq > 0 ? 1u : acc0);
-            // the two value blocks of this O^T block may be refilled once these finish
-            umma_commit_elect(&sh.empty[slot_of(g, 2 * b)]);
-            umma_commit_elect(&sh.empty[slot_of(g, 2 * b + 1)]);
           }
-          umma_commit_elect(&sh.empty[slot_of(g, kKB - 1)]);    // rope block, which also held P^T
+          umma_commit_elect(&sh.empty[g & 1]);    // the tile (whose rope block also held P^T) may be refilled
           umma_commit_elect(&sh.o_done);
         }
       }
