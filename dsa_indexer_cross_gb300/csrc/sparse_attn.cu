@@ -85,7 +85,7 @@ struct ACfg {
 // Per-column softmax state lives in shared memory (uniform across the softmax threads).
 struct AShared {
   uint64_t full[2], empty[2];   // per tile slot set (nine 64-dim blocks)
-  uint64_t q_full, q_empty, s_full[2], s_empty[2], p_full, o_done, o_free;
+  uint64_t q_full, q_empty, s_full[2], s_empty[2], p_full, o_done[2], o_free;   // o_done[g & 1]: PV(g) complete
   uint32_t tmem_base, abort_flag, soft_abort;
   uint32_t prod_ok;
   alignas(16) float red[4][64];
@@ -205,7 +205,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sh.s_empty[b], kSoft / 32);   // one arrive per softmax warp
     }
     mbar_init(&sh.p_full, kSoft / 32);
-    mbar_init(&sh.o_done, 1);
+    mbar_init(&sh.o_done[0], 1);
+    mbar_init(&sh.o_done[1], 1);
     mbar_init(&sh.o_free, kSoft / 32);
     sh.abort_flag = 0;
     sh.soft_abort = 0;
@@ -433,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // O^T may only be rescaled once the previous tile's PV has finished
             if (i > 0) {
-              ok = mbar_wait(&sh.o_done, (g - 1) & 1, &sh.abort_flag, status);
+              ok = mbar_wait(&sh.o_done[(g - 1) & 1], ((g - 1) >> 1) & 1, &sh.abort_flag, status);
               ok = __all_sync(0xffffffffu, ok);
               if (!ok && lane == 0) sh.soft_abort = 1;
             }
@@ -507,12 +508,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             lp[2 * kk + 1] += __high2float(pb);
           }
         }
-        // Wait for the previous tile's PV before publishing P: PV(g) queues behind it anyway,
-        // and since PV(g) cannot start before P(g), waiting here on every tile (and at every
-        // item end) means all earlier o_done phases are complete whenever this loop waits, so
-        // its parity waits are exact.  A timeout here raises the CTA abort flag, and the next
-        // wait of this loop turns it into a uniform stop.
-        if (i > 0) (void)mbar_wait(&sh.o_done, (g - 1) & 1, &sh.abort_flag, status);
+        // P(g) goes out without waiting for PV(g - 1): PV(g) queues behind it in the tensor
+        // pipe anyway.  PV completions are signalled on o_done[g & 1]; S^T(g) complete implies
+        // tile g was loaded, hence PV(g - 2) and everything before it finished, so a wait for
+        // PV(g - 1) on o_done[(g - 1) & 1] at parity ((g - 1) >> 1) & 1 is exact.
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
@@ -531,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane < 4) sh.red[qd][8 * kk + cq + e] = x;
         }
       }
-      bool ok = mbar_wait(&sh.o_done, (g - 1) & 1, &sh.abort_flag, status);
+      bool ok = mbar_wait(&sh.o_done[(g - 1) & 1], ((g - 1) >> 1) & 1, &sh.abort_flag, status);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok && lane == 0) sh.soft_abort = 1;
       named_bar_sync(1, kSoft);
@@ -642,7 +641,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                               dp + static_cast<uint64_t>((kq * 2048) >> 4), id_pv, kq > 0 ? 1u : acc0);
           }
           umma_commit_elect(&sh.empty[g & 1]);    // the tile (whose rope block also held P^T) may be refilled
-          umma_commit_elect(&sh.o_done);
+          umma_commit_elect(&sh.o_done[g & 1]);
         }
       }
       ++it;
