@@ -159,7 +159,7 @@ def roofline_numbers(w, geo):
 
 # DRAM bytes (read + write) of one sparse_attn_kernel launch on this workload from an ncu
 # capture of the current kernel (profiles/sparse_attn_prefill_4k.md); None when not measured.
-ATTN_TRAFFIC_BYTES = 147.05e6
+ATTN_TRAFFIC_BYTES = 112.04e6
 
 
 def peaks():
