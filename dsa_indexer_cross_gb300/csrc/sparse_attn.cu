@@ -60,8 +60,8 @@ constexpr int kKB = kDqk / 64;     // 64-dim blocks per tile (the last one holds
 constexpr int kBlkBytes = kRows * 128;         // one block: 64 rows x 128 B
 constexpr int kSlots = 2 * kKB;                // two tiles in flight
 constexpr int kProd = 64;                      // warps 0-1
-constexpr int kSoft = 128;                     // warps 3-6, one per TMEM lane quarter
-constexpr int kThreads = kProd + 32 + kSoft + 32;   // + warp 2 (S^T MMAs), warp 7 (PV MMAs); 8 warps
+// Warps 0-1 load, warp 2 issues S^T, warps 3-6 (and, block-dense, 8-11) run the softmax,
+// warp 7 owns TMEM and issues PV.
 constexpr int kDenseCols = 64;                 // columns of a block-dense item
 constexpr int kMaskBytes = 4096;               // selection bitmask budget (block-dense)
 
@@ -76,7 +76,11 @@ struct ACfg {
   static constexpr uint32_t TMEM_COLS = 6 * HB <= 128 ? 128 : 6 * HB <= 256 ? 256 : 512;
   static constexpr int O_COL = 0;
   static constexpr int S_COL = 4 * HB;
-  static constexpr int NR = HB / 8;                                    // 16x256b repetitions
+  static constexpr int SW = DENSE ? 8 : 4;                             // softmax warps (2 or 1 per lane quarter)
+  static constexpr int SOFT = 32 * SW;
+  static constexpr int THREADS = kProd + 32 + SOFT + 32;
+  static constexpr int CW = HB / (SW / 4);                             // columns per softmax warp
+  static constexpr int NR = CW / 8;                                    // 16x256b repetitions per warp
   static_assert(HB % 16 == 0 && HB <= 64, "columns");
   static_assert(!DENSE || HB % HD == 0, "whole tokens per dense item");
   static_assert(HB * kRows * 2 <= kBlkBytes, "P^T must fit in the rope block");
@@ -165,7 +169,7 @@ __device__ __forceinline__ Item item_info(int item, int n_hb, const int32_t* row
 }
 
 template <int HB, int HD>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(ACfg<HB, HD>::THREADS, 1)
     sparse_attn_kernel(const __grid_constant__ CUtensorMap tmap_kv, const uint16_t* __restrict__ q,
                        const uint16_t* __restrict__ kv, const int32_t* __restrict__ idx,
                        const int32_t* __restrict__ ks, const int32_t* __restrict__ row_nt,
@@ -202,12 +206,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&sh.q_empty, 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sh.s_full[b], 1);
-      mbar_init(&sh.s_empty[b], kSoft / 32);   // one arrive per softmax warp
+      mbar_init(&sh.s_empty[b], C::SW);   // one arrive per softmax warp
     }
-    mbar_init(&sh.p_full, kSoft / 32);
+    mbar_init(&sh.p_full, C::SW);
     mbar_init(&sh.o_done[0], 1);
     mbar_init(&sh.o_done[1], 1);
-    mbar_init(&sh.o_free, kSoft / 32);
+    mbar_init(&sh.o_free, C::SW);
     sh.abort_flag = 0;
     sh.soft_abort = 0;
     fence_mbar_init();
@@ -316,16 +320,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++it;
     }
     cp_async_wait<0>();
-  } else if (warp >= 3 && warp < 7) {
+  } else if ((warp >= 3 && warp < 7) || warp >= 8) {
     // ---------------------------------------------------------------- softmax + epilogue
-    const int tid = threadIdx.x - 96;      // 0..127
+    constexpr int kSoft = C::SOFT;
+    const int tid = warp < 7 ? static_cast<int>(threadIdx.x) - 96 : 128 + static_cast<int>(threadIdx.x) - 256;
     const int qd = warp & 3;               // TMEM lane quarter
+    const int c_off = warp >= 8 ? C::CW : 0;   // this warp's columns: [c_off, c_off + CW)
     const int r0 = qd * 16 + (lane >> 2);  // S^T rows held: r0 and r0 + 8
     const int cq = 2 * (lane & 3);         // column pair within each group of 8 columns
     const uint32_t t_lane = static_cast<uint32_t>(qd * 32) << 16;
     // A failed (timed-out) wait is published through sh.soft_abort, written only before a
     // named barrier and read right after it; the next write can only happen after a later
-    // barrier, so the four softmax warps always leave the loops at the same point.
+    // barrier, so all softmax warps always leave the loops at the same point.
     uint32_t g = 0, it = 0;
     bool stop = false;
     for (int k = 0; k * static_cast<int>(gridDim.x) < n_items && !stop; ++k) {
@@ -389,17 +395,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) {
           tc_fence_after();
           uint32_t v[4 * NR];
-          tmem_ld_16x256b<NR>(tmem + t_lane + C::S_COL + sb * HB, v);
+          tmem_ld_16x256b<NR>(tmem + t_lane + C::S_COL + sb * HB + c_off, v);
           tmem_ld_wait();
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&sh.s_empty[sb]);
 #pragma unroll
           for (int kk = 0; kk < NR; ++kk) {
-            const float2 mu = *reinterpret_cast<const float2*>(&sh.m_used[8 * kk + cq]);
+            const float2 mu = *reinterpret_cast<const float2*>(&sh.m_used[c_off + 8 * kk + cq]);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-              const int c = 8 * kk + cq + (j & 1);
+              const int c = c_off + 8 * kk + cq + (j & 1);
               bool valid;
               if constexpr (DENSE) {
                 const int r = r0 + ((j & 2) ? 8 : 0);
@@ -429,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 4));
                 x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 8));
                 x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 16));
-                if (lane < 4) sh.red[qd][8 * kk + cq + e] = x;
+                if (lane < 4) sh.red[qd][c_off + 8 * kk + cq + e] = x;
               }
             }
             // O^T may only be rescaled once the previous tile's PV has finished
@@ -457,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           bool any = false;
 #pragma unroll
           for (int kk = 0; kk < NR; ++kk) {
-            const float2 a = *reinterpret_cast<const float2*>(&sh.alpha[8 * kk + cq]);
+            const float2 a = *reinterpret_cast<const float2*>(&sh.alpha[c_off + 8 * kk + cq]);
             lp[2 * kk] *= a.x;
             lp[2 * kk + 1] *= a.y;
           }
@@ -472,7 +478,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int b = 0; b < 4; ++b) {
 #pragma unroll
-              for (int hh = 0; hh < HB / 16; ++hh) {
+              for (int hw = 0; hw < C::CW / 16; ++hw) {
+                const int hh = c_off / 16 + hw;
                 uint32_t o[16];
                 tmem_ld16(tmem + t_lane + C::O_COL + b * HB + hh * 16, o);
                 tmem_ld_wait();
@@ -494,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < NR; ++kk) {
           // a column whose max is still -inf has only masked (-inf) entries so far: subtract 0
           // there so that exp2(-inf) = 0 instead of exp2(NaN)
-          float2 mu = *reinterpret_cast<const float2*>(&sh.m_used[8 * kk + cq]);
+          float2 mu = *reinterpret_cast<const float2*>(&sh.m_used[c_off + 8 * kk + cq]);
           mu.x = mu.x == -INFINITY ? 0.f : mu.x;
           mu.y = mu.y == -INFINITY ? 0.f : mu.y;
 #pragma unroll
@@ -503,7 +510,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float p0 = ex2_approx(sc[4 * kk + 2 * h] - mu.x);
             const float p1 = ex2_approx(sc[4 * kk + 2 * h + 1] - mu.y);
             const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
-            st_shared_u32(p_base + r * 128 + ((kk ^ (r & 7)) << 4) + cq * 2, *reinterpret_cast<const uint32_t*>(&pb));
+            const int chunk = c_off / 8 + kk;   // 8-column (16-byte) chunk of the 64-column row
+            st_shared_u32(p_base + r * 128 + ((chunk ^ (r & 7)) << 4) + cq * 2, *reinterpret_cast<const uint32_t*>(&pb));
             lp[2 * kk] += __low2float(pb);
             lp[2 * kk + 1] += __high2float(pb);
           }
@@ -527,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           x += __shfl_xor_sync(0xffffffffu, x, 4);
           x += __shfl_xor_sync(0xffffffffu, x, 8);
           x += __shfl_xor_sync(0xffffffffu, x, 16);
-          if (lane < 4) sh.red[qd][8 * kk + cq + e] = x;
+          if (lane < 4) sh.red[qd][c_off + 8 * kk + cq + e] = x;
         }
       }
       bool ok = mbar_wait(&sh.o_done[(g - 1) & 1], ((g - 1) >> 1) & 1, &sh.abort_flag, status);
@@ -541,13 +549,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       // Column c is output row row0 + c in both walks (block-dense: HD == H, so the block's
       // (token, head) rows are consecutive; gather: the head block of one token); this thread
-      // writes dimension b*128 + qd*32 + lane of every valid column.
+      // writes dimension b*128 + qd*32 + lane of every valid column of its column range.
       {
         const long long row0 = static_cast<long long>(I.t0) * H + (DENSE ? 0 : I.hb * HB);
         const int n_cols = DENSE ? min(HB, (n_q - I.t0) * H) : min(HB, H - I.hb * HB);
         uint16_t* obase = out + row0 * kDv + qd * 32 + lane;
 #pragma unroll
-        for (int hh = 0; hh < HB / 16; ++hh) {
+        for (int hw = 0; hw < C::CW / 16; ++hw) {
+          const int hh = c_off / 16 + hw;
           float inv[16];
           load_row16(inv, &sh.l_run[hh * 16]);
 #pragma unroll
@@ -775,7 +784,7 @@ cudaError_t launch_cfg(const CUtensorMap& tmap, int n_q, int n_kv, int H, int to
   if (e != cudaSuccess) return e;
   const int n_items = C::DENSE ? (n_q + C::B - 1) / C::B : n_q * ((H + HB - 1) / HB);
   const int grid = n_items < device_sm_count() ? n_items : device_sm_count();
-  kern<<<grid, kThreads, C::DYN_SMEM, st>>>(tmap, static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(kv),
+  kern<<<grid, C::THREADS, C::DYN_SMEM, st>>>(tmap, static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(kv),
                                             idx, ks, row_nt, block_range, block_mask, static_cast<uint16_t*>(out), lse,
                                             n_q, n_kv,
                                             H, topk, scale * 1.4426950408889634f, status, status + 1);
