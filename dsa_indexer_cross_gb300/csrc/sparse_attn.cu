@@ -611,12 +611,14 @@ __global__ void __launch_bounds__(ACfg<HB, HD>::THREADS, 1)
       const Item I = item_info<HB, HD>(item, n_hb, row_nt, block_range);
       if (I.nt == 0) continue;
       if (qk_warp) {
-        // S^T(g) = tile . Q^T, one 64-dim block at a time as each lands
+        // S^T(g) = tile . Q^T once the whole tile has landed
         ok = wait(&sh.q_full, it & 1);
+        fence_proxy_async_smem();   // Q was written by cp.async (generic proxy); the MMA reads it
         for (int i = 0; i < I.nt && ok; ++i, ++g) {
           const int sb = g & 1;
           if (g >= 2 && !(ok = wait(&sh.s_empty[sb], ((g >> 1) - 1) & 1))) break;
           if (!(ok = wait(&sh.full[g & 1], (g >> 1) & 1))) break;
+          if constexpr (!DENSE) fence_proxy_async_smem();   // gathered rows came through cp.async
           tc_fence_after();
           const uint64_t da = sdesc_sw128(st0 + (g & 1u) * (kKB * kBlkBytes), 16, 1024);
           const uint32_t d_s = tmem + C::S_COL + sb * HB;
