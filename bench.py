@@ -329,6 +329,20 @@ def run_native(args):
     idx_ms = time_call(lambda: D.dsa_indexer_topk(idesc, L0["q_idx"], L0["k_idx"], L0["w"], q_pos, k_pos, ks, ke, rope,
                                                   idx_full, None, ws=idx_ws, stream=stream), 20)
 
+    # ---------------- per-phase split of the indexer call (CUDA events between its launches,
+    # recorded only in this separate loop); median over 20 calls, L2 flushed before each
+    D.dsa_profile_enable(True)
+    phases = []
+    try:
+        for _ in range(20):
+            flush.zero_()
+            D.dsa_indexer_topk(idesc, L0["q_idx"], L0["k_idx"], L0["w"], q_pos, k_pos, ks, ke, rope, idx_full, None,
+                               ws=idx_ws, stream=stream)
+            phases.append(D.dsa_profile_indexer_last())
+    finally:
+        D.dsa_profile_enable(False)
+    phase_ms = [statistics.median(p[i] for p in phases) for i in range(4)]
+
     # ---------------- end to end through the C ABI from pinned host buffers
     in_keys = ("q_idx", "k_idx", "w", "q", "kv")
     host_in = [{k: v.cpu().pin_memory() for k, v in L.items() if k in in_keys} for L in layers]
@@ -365,6 +379,7 @@ def run_native(args):
     attn_gbs = R["attn_gathered"] / (attn_ms / 1e3) / 1e9
     attn_strict_tflops = R["attn_flops"] / (attn_ms / 1e3) / 1e12
     idx_tflops = R["idx_flops"] / (idx_ms / 1e3) / 1e12
+    score_tflops = R["idx_flops"] / (phase_ms[2] / 1e3) / 1e12
     gpu_launches = sum((3 if t == "full" else 0) + 2 for t in w.layers) + 2 * sum(t == "full" for t in w.layers)
 
     line = {
@@ -399,6 +414,13 @@ def run_native(args):
                              "algorithmic_flops_per_launch": R["idx_flops"],
                              "causal_flops_per_launch": R["idx_flops_causal"], "ms_per_launch": idx_ms,
                              "peak_kind": peak_kind + " (bf16 burst)"},
+        # the tensor-core score kernel of that call on its own (events between the call's launches)
+        "roofline_indexer_kernel": {"kernel": "indexer_kernel (tcgen05 scores + streaming top-k)", "bound": "tensor",
+                                    "achieved": score_tflops, "peak": tc_burst, "unit": "TFLOP/s",
+                                    "frac": score_tflops / tc_burst, "algorithmic_flops_per_launch": R["idx_flops"],
+                                    "ms_per_launch": phase_ms[2], "peak_kind": peak_kind + " (bf16 burst)",
+                                    "call_phase_ms": {"rope": phase_ms[0], "ranges": phase_ms[1],
+                                                      "scores_topk": phase_ms[2], "select": phase_ms[3]}},
         "clocks": clk.summary(),
     }
     if rank == 0 and not args.no_cpu_baseline:

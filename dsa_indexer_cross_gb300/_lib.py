@@ -28,7 +28,7 @@ EXPORTED = ("dsa_status_string", "dsa_last_error", "dsa_donor_table", "dsa_rope_
             "dsa_indexer_topk", "dsa_sparse_attn_workspace_size", "dsa_sparse_attn", "dsa_index_cache_create",
             "dsa_index_cache_donor", "dsa_index_cache_indices", "dsa_index_cache_destroy",
             "dsa_layers_workspace_size", "indexshare_layers_forward", "dsa_workspace_status",
-            "dsa_indexer_topk_static")
+            "dsa_indexer_topk_static", "dsa_profile_enable", "dsa_profile_indexer_last")
 
 
 class DsaError(RuntimeError):
@@ -95,6 +95,10 @@ def lib() -> C.CDLL:
                                                 vp, vp, vp, i32, vp, vp, sz, vp]
         L.dsa_workspace_status.restype = st
         L.dsa_workspace_status.argtypes = [vp, vp, P(u32)]
+        L.dsa_profile_enable.restype = st
+        L.dsa_profile_enable.argtypes = [i32]
+        L.dsa_profile_indexer_last.restype = st
+        L.dsa_profile_indexer_last.argtypes = [P(C.c_float), i32]
         L.dsa_indexer_topk_static.restype = st
         L.dsa_indexer_topk_static.argtypes = [P(IndexerDesc), vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp]
         _lib = L
@@ -281,3 +285,16 @@ def dsa_workspace_status(ws: torch.Tensor, stream=None, raise_on_fault: bool = T
     if st not in (0, 7, 8) or (st != 0 and raise_on_fault):
         _check(st)
     return bits.value
+
+
+def dsa_profile_enable(on: bool) -> None:
+    """Turn per-phase event recording of indexer calls on or off (process-wide)."""
+    _check(lib().dsa_profile_enable(1 if on else 0))
+
+
+def dsa_profile_indexer_last() -> list:
+    """Device milliseconds of the last profiled indexer call on the current device:
+    [RoPE, key-range plan, scores + streaming top-k, final select]."""
+    ms = (C.c_float * 4)()
+    _check(lib().dsa_profile_indexer_last(ms, 4))
+    return [float(x) for x in ms]

@@ -5,6 +5,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <new>
 #include <string>
@@ -68,6 +69,37 @@ dsa_status check_device() {
   if (d.major != 10 || d.minor != 3)
     return fail(DSA_ERR_UNSUPPORTED, "libdsa is built for sm_103a; the current device is sm_%d%d", d.major, d.minor);
   return DSA_OK;
+}
+
+// ------------------------------------------------------------------ phase profiling
+// Five events per device bracket the four phases of an indexer call while profiling is on.
+std::atomic<int> g_profile{0};
+struct PhaseEvents {
+  cudaEvent_t ev[5];
+  bool created = false;
+  bool recorded = false;
+};
+PhaseEvents g_phase[64];
+std::mutex g_phase_mu;
+
+// The current device's events, created on first use; nullptr when profiling is off or the
+// events cannot be created.
+PhaseEvents* phase_events() {
+  if (!g_profile.load(std::memory_order_relaxed)) return nullptr;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(g_phase_mu);
+  PhaseEvents& p = g_phase[dev];
+  if (!p.created) {
+    for (int i = 0; i < 5; ++i) {
+      if (cudaEventCreate(&p.ev[i]) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+      }
+    }
+    p.created = true;
+  }
+  return &p;
 }
 
 // ------------------------------------------------------------------ tensor maps
@@ -221,6 +253,8 @@ dsa_status run_indexer(const dsa_indexer_desc* d, const void* q_idx, const void*
   if (clear_status && (e = cudaMemsetAsync(ws, 0, kAlign, st)) != cudaSuccess) return cuda_fail(e, "clear status");
   const void* qr = q_idx;
   const void* kr = k_idx;
+  PhaseEvents* pe = phase_events();
+  if (pe) (void)cudaEventRecord(pe->ev[0], st);
   if (rq) {
     e = launch_rope_rows(q_idx, base + L.off_q, q_pos, static_cast<int64_t>(d->n_q) * d->n_heads, d->n_heads,
                          d->head_dim, d->rope_dim, rope_cs, rope_n_pos, status, st);
@@ -236,10 +270,12 @@ dsa_status run_indexer(const dsa_indexer_desc* d, const void* q_idx, const void*
   const IndexerPlan& p = L.plan;
   int2* rr = reinterpret_cast<int2*>(base + L.off_rr);
   int2* gr = reinterpret_cast<int2*>(base + L.off_gr);
+  if (pe) (void)cudaEventRecord(pe->ev[1], st);
   // rows whose whole range fits in k keep every key; without requested scores they need no scoring
   const int trivial_len = score_out ? 0 : d->topk;
   e = launch_ranges(ks, ke, d->n_q, p.group, d->n_kv, d->max_len, trivial_len, rr, gr, status, st);
   if (e != cudaSuccess) return cuda_fail(e, "key ranges");
+  if (pe) (void)cudaEventRecord(pe->ev[2], st);
   uint32_t* cnt = reinterpret_cast<uint32_t*>(base + L.off_cnt);
   uint32_t* ck = reinterpret_cast<uint32_t*>(base + L.off_key);
   int32_t* ci = reinterpret_cast<int32_t*>(base + L.off_idx);
@@ -255,8 +291,13 @@ dsa_status run_indexer(const dsa_indexer_desc* d, const void* q_idx, const void*
     if ((e = cudaMemsetAsync(cnt, 0, static_cast<size_t>(d->n_q) * p.n_chunks * 4, st)) != cudaSuccess)
       return cuda_fail(e, "clear counts");
   }
+  if (pe) (void)cudaEventRecord(pe->ev[3], st);
   e = launch_select(d->n_q, p.n_chunks, p.cap, d->topk, trivial_len, rr, ck, ci, cnt, idx_out, score_out, status, st);
   if (e != cudaSuccess) return cuda_fail(e, "top-k select");
+  if (pe) {
+    (void)cudaEventRecord(pe->ev[4], st);
+    pe->recorded = true;
+  }
   return DSA_OK;
 }
 
@@ -527,6 +568,32 @@ dsa_status dsa_workspace_status(const void* ws, void* stream, uint32_t* device_b
   if (device_bits) *device_bits = h.status;
   if (h.status & DEV_ERR_TIMEOUT) return fail(DSA_ERR_TIMEOUT, "a device pipeline wait ran past its bound");
   if (h.status) return fail(DSA_ERR_DEVICE, "device status 0x%x (%u bad indices)", h.status, h.bad_count);
+  return DSA_OK;
+}
+
+dsa_status dsa_profile_enable(int32_t on) {
+  g_profile.store(on ? 1 : 0, std::memory_order_relaxed);
+  return DSA_OK;
+}
+
+dsa_status dsa_profile_indexer_last(float* ms, int32_t n) {
+  if (!ms || n < 1) return fail(DSA_ERR_ARG, "ms must be non-NULL and n >= 1");
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(DSA_ERR_UNSUPPORTED, "device %d out of range", dev);
+  PhaseEvents* p = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_phase_mu);
+    if (g_phase[dev].created && g_phase[dev].recorded) p = &g_phase[dev];
+  }
+  if (!p) return fail(DSA_ERR_UNSUPPORTED, "no profiled indexer call on device %d", dev);
+  if ((e = cudaEventSynchronize(p->ev[4])) != cudaSuccess) return cuda_fail(e, "profile events");
+  for (int i = 0; i < 4 && i < n; ++i) {
+    float t = 0.f;
+    if ((e = cudaEventElapsedTime(&t, p->ev[i], p->ev[i + 1])) != cudaSuccess) return cuda_fail(e, "profile events");
+    ms[i] = t;
+  }
   return DSA_OK;
 }
 

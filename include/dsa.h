@@ -254,6 +254,23 @@ dsa_status indexshare_layers_forward(const dsa_indexer_desc* idx_desc, const dsa
  * The word is cleared at the start of every call that takes the workspace. */
 dsa_status dsa_workspace_status(const void* ws, void* stream, uint32_t* device_bits);
 
+/* ------------------------------------------------------------------ profiling ------- */
+
+/* Process-wide switch (off by default).  While on, every indexer call (dsa_indexer_topk,
+ * its static-scratch variant and the full layers of indexshare_layers_forward) records CUDA
+ * events on its stream between its phases, so that dsa_profile_indexer_last can report
+ * device time per phase.  The events add no work to the kernels.  Not meant for calls that
+ * run concurrently from several host threads.  The pages have no counterpart: this exists to
+ * measure the score kernel on its own.  Errors: none (DSA_OK). */
+dsa_status dsa_profile_enable(int32_t on);
+
+/* Device time, in milliseconds, of each phase of the last profiled indexer call made on the
+ * current device: ms[0] = RoPE of the index q and k, ms[1] = key-range plan, ms[2] = scores
+ * with the streaming top-k (the tensor-core kernel), ms[3] = final top-k select.  Writes the
+ * first min(n, 4) values; waits for that call to finish.  Errors: DSA_ERR_ARG (ms NULL or
+ * n < 1), DSA_ERR_UNSUPPORTED (no profiled call yet on this device), DSA_ERR_CUDA. */
+dsa_status dsa_profile_indexer_last(float* ms, int32_t n);
+
 #ifdef __cplusplus
 }
 #endif

@@ -166,3 +166,13 @@ def test_layer_loop_rejects_mismatched_schedule_before_launch():
                                      h, 0x100000, 1 << 30, None)
     assert st == 2
     L.dsa_index_cache_destroy(h)
+
+
+def test_profiling_switch_and_argument_errors():
+    # the switch needs no device; reading needs a non-NULL buffer of at least one value
+    L = _lib.lib()
+    assert L.dsa_profile_enable(1) == 0
+    assert L.dsa_profile_indexer_last(None, 4) == 1          # DSA_ERR_ARG
+    buf = (C.c_float * 4)()
+    assert L.dsa_profile_indexer_last(buf, 0) == 1
+    assert L.dsa_profile_enable(0) == 0
