@@ -157,9 +157,9 @@ def roofline_numbers(w, geo):
                 rows=int(rows), pairs=int(pairs))
 
 
-# DRAM bytes (read + write) of one sparse_attn_kernel launch on this workload from an ncu
-# capture of the current kernel (profiles/sparse_attn_prefill_4k.md); None when not measured.
-ATTN_TRAFFIC_BYTES = 112.04e6
+# DRAM bytes (read + write) of one sparse_attn_kernel launch, per workload, from an ncu capture
+# of the current kernel (profiles/sparse_attn_<workload>.md); workloads not listed report None.
+ATTN_TRAFFIC_BYTES = {"prefill_4k": 112.04e6}
 
 
 def peaks():
@@ -387,7 +387,7 @@ def run_native(args):
         "value": value, "unit": "query_tokens/s", "n_gpus": ws_n, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16 (fp32 accumulate)", "data": "synthetic (seeded Gaussian, bf16)",
-        "config": {"workload": f"{w.name}: T={w.n_q} prefill, {len(w.layers)} layers "
+        "config": {"workload": f"{w.name}: {w.n_q} queries ({w.kind}, {geo.n_kv} keys), {len(w.layers)} layers "
                                f"{''.join(t[0].upper() for t in w.layers)}, H_I={w.n_heads_idx}x{w.head_dim_idx} "
                                f"(rope {w.rope_dim}, theta {w.theta:g}), topk={w.topk}, H={w.n_heads} 576/512",
                    "l2": "flushed between timed steps (512 MiB write outside the events)",
@@ -401,7 +401,7 @@ def run_native(args):
         # would move are given for context.
         "roofline": {"kernel": "sparse_attn_kernel", "bound": "tensor", "achieved": attn_strict_tflops,
                      "peak": tc_burst, "unit": "TFLOP/s", "frac": attn_strict_tflops / tc_burst,
-                     "traffic": ATTN_TRAFFIC_BYTES, "peak_kind": peak_kind + " (bf16 burst)",
+                     "traffic": ATTN_TRAFFIC_BYTES.get(w.name), "peak_kind": peak_kind + " (bf16 burst)",
                      "algorithmic_flops_per_launch": R["attn_flops"], "ms_per_launch": attn_ms,
                      "min_hbm_bytes_per_launch": R["attn_min_bytes"],
                      "min_hbm_frac": R["attn_min_bytes"] / (attn_ms / 1e3) / 1e9 / hbm,

@@ -336,12 +336,25 @@ dsa_status run_attn(const dsa_attn_desc* d, const void* q, const void* kv, const
   cudaError_t e;
   if (clear_status && (e = cudaMemsetAsync(ws, 0, kAlign, st)) != cudaSuccess) return cuda_fail(e, "clear status");
   uint32_t* status = status_override ? status_override : reinterpret_cast<uint32_t*>(base);
-  CUtensorMap tkv;
+  // every operand of the kernel arrives by TMA: q as (token, head) rows, kv as whole 64-row
+  // tiles (block-dense walk) or as single rows for four-row gathers (gather walk)
+  CUtensorMap tkv, tq;
   std::memset(&tkv, 0, sizeof(tkv));
-  if (sparse_attn_dense_heads(d->n_heads, d->n_kv, d->topk) && d->n_kv > 0) {
-    if ((s = tmap_kv_tiles(&tkv, kv, d->n_kv)) != DSA_OK) return s;
+  std::memset(&tq, 0, sizeof(tq));
+  if (sparse_attn_dense_heads(d->n_heads, d->n_kv, d->topk)) {
+    if (d->n_kv > 0) s = tmap_kv_tiles(&tkv, kv, d->n_kv);   // an empty cache gives every block an empty range
+  } else if (d->n_kv > 0) {
+    s = tmap_bf16(&tkv, kv, 576, d->n_kv, 1);
+  } else {
+    // an empty cache has no row for the map; every slot is then masked, and the gathers that
+    // still run read the first row of q instead (any 576-wide row in bounds will do)
+    s = tmap_bf16(&tkv, q, 576, 1, 1);
   }
-  e = launch_sparse_attn(tkv, d->n_q, d->n_kv, d->n_heads, d->topk, d->softmax_scale, q, kv, idx, ks, out, lse, status,
+  if (s != DSA_OK) return s;
+  if ((s = tmap_bf16(&tq, q, 576, static_cast<uint64_t>(d->n_q) * d->n_heads,
+                     static_cast<uint32_t>(sparse_attn_q_box_rows(d->n_heads, d->n_kv, d->topk)))) != DSA_OK)
+    return s;
+  e = launch_sparse_attn(tkv, tq, d->n_q, d->n_kv, d->n_heads, d->topk, d->softmax_scale, idx, ks, out, lse, status,
                          base + kAlign, st);
   if (e != cudaSuccess) return cuda_fail(e, "sparse attention kernel");
   return DSA_OK;

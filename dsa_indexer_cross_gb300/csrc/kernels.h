@@ -56,11 +56,17 @@ int sparse_attn_dense_heads(int n_heads, int n_kv, int topk);
 // Scratch bytes launch_sparse_attn needs (per-row tile counts, or per-block key ranges and
 // selection bitmasks).
 size_t sparse_attn_ws_bytes(int n_q, int n_heads, int n_kv, int topk);
-// tmap_kv: kv [n_kv x 576] bf16 viewed as (64 dims, n_kv rows, 9 dim blocks) with 128-byte
-// swizzled boxes of {64, 64, 9} = one 64-row tile (read by the block-dense walk only).
-cudaError_t launch_sparse_attn(const CUtensorMap& tmap_kv, int n_q, int n_kv, int n_heads, int topk, float scale,
-                               const void* q, const void* kv, const int32_t* idx, const int32_t* ks, void* out,
-                               float* lse, uint32_t* status, void* scratch, cudaStream_t st);
+// Rows of q (consecutive (token, head) rows) that one work item of the chosen walk reads:
+// the box height of tmap_q.
+int sparse_attn_q_box_rows(int n_heads, int n_kv, int topk);
+// tmap_kv: block-dense walk -- kv [n_kv x 576] bf16 viewed as (64 dims, n_kv rows, 9 dim
+// blocks) with 128-byte swizzled boxes of {64, 64, 9} = one 64-row tile; gather walk -- kv as
+// a 2-D [n_kv][576] tensor with 128-byte swizzled boxes of {64, 1} (four-row gathers).
+// tmap_q: q as a 2-D [n_q * n_heads][576] tensor, 128-byte swizzled boxes of
+// {64, sparse_attn_q_box_rows(...)}.
+cudaError_t launch_sparse_attn(const CUtensorMap& tmap_kv, const CUtensorMap& tmap_q, int n_q, int n_kv, int n_heads,
+                               int topk, float scale, const int32_t* idx, const int32_t* ks, void* out, float* lse,
+                               uint32_t* status, void* scratch, cudaStream_t st);
 
 int device_sm_count();
 

@@ -38,10 +38,10 @@
 // TMEM shape, so each thread holds two rows and HB/4 columns; running sums stay in registers
 // and are reduced once per item.
 //
-// Warp roles (256 threads): warps 0-1 load Q and the rows (cp.async gathers, or one thread
-// issuing TMA block loads in block-dense mode); warp 2 issues the S^T products; warps 3-6 run
-// the softmax, build the mask (block-dense) and the epilogue; warp 7 owns TMEM and issues the
-// PV products.  With the two products issued from separate warps, PV(g) goes out as soon as
+// Warp roles (256 threads): warps 0-1 load Q and the rows, all through the Tensor Memory
+// Accelerator (Q as nine 64-dim boxes; the rows as four-row gathers, or one 3-D box per tile in
+// block-dense mode); warp 2 issues the S^T products; warps 3-6 run the softmax and the
+// epilogue; warp 7 owns TMEM and issues the PV products.  With the two products issued from separate warps, PV(g) goes out as soon as
 // P(g) exists instead of queueing behind S^T(g+1), whose blocks may still be in flight.
 // Persistent CTAs.
 #include <cuda_bf16.h>
@@ -55,7 +55,6 @@ namespace {
 constexpr int kRows = 64;          // latent rows per tile
 constexpr int kDqk = 576;
 constexpr int kDv = 512;
-constexpr int kChunks = kDqk / 8;  // 16-byte chunks per latent row
 constexpr int kKB = kDqk / 64;     // 64-dim blocks per tile (the last one holds the rope dims)
 constexpr int kBlkBytes = kRows * 128;         // one block: 64 rows x 128 B
 constexpr int kSlots = 2 * kKB;                // two tiles in flight
@@ -170,8 +169,8 @@ __device__ __forceinline__ Item item_info(int item, int n_hb, const int32_t* row
 
 template <int HB, int HD>
 __global__ void __launch_bounds__(ACfg<HB, HD>::THREADS, 1)
-    sparse_attn_kernel(const __grid_constant__ CUtensorMap tmap_kv, const uint16_t* __restrict__ q,
-                       const uint16_t* __restrict__ kv, const int32_t* __restrict__ idx,
+    sparse_attn_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_constant__ CUtensorMap tmap_q,
+                       const int32_t* __restrict__ idx,
                        const int32_t* __restrict__ ks, const int32_t* __restrict__ row_nt,
                        const int2* __restrict__ block_range, const uint32_t* __restrict__ block_mask,
                        uint16_t* __restrict__ out, float* __restrict__ lse, int n_q, int n_kv, int H, int topk,
@@ -199,10 +198,10 @@ __global__ void __launch_bounds__(ACfg<HB, HD>::THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&sh.full[s], DENSE ? 1 : kProd);
+      mbar_init(&sh.full[s], 1);
       mbar_init(&sh.empty[s], 1);
     }
-    mbar_init(&sh.q_full, kProd);
+    mbar_init(&sh.q_full, 1);
     mbar_init(&sh.q_empty, 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sh.s_full[b], 1);
@@ -227,9 +226,10 @@ __global__ void __launch_bounds__(ACfg<HB, HD>::THREADS, 1)
   const uint32_t tmem = sh.tmem_base;
 
   if (warp < 2) {
-    // ---------------------------------------------------------------- Q (+ gathered rows)
-    // Thread 0 does every wait and publishes the outcome in sh.prod_ok between two named
-    // barriers (id 2), so the two producer warps always stop at the same point.
+    // ---------------------------------------------------------------- Q and the rows (TMA)
+    // Thread 0 does every wait and arms every barrier, then publishes the outcome in
+    // sh.prod_ok between two named barriers (id 2), so the two producer warps always stop at
+    // the same point and no copy is issued before its barrier expects the bytes.
     const int tid = threadIdx.x;
     uint32_t g = 0, it = 0;
     bool ok = true;
@@ -246,28 +246,22 @@ __global__ void __launch_bounds__(ACfg<HB, HD>::THREADS, 1)
       const Item I = item_info<HB, HD>(item, n_hb, row_nt, block_range);
       if (I.nt == 0) continue;
       bool w_ok = true;
-      if (tid == 0 && it > 0) w_ok = mbar_wait(&sh.q_empty, (it - 1) & 1, &sh.abort_flag, status);
+      if (tid == 0) {
+        if (it > 0) w_ok = mbar_wait(&sh.q_empty, (it - 1) & 1, &sh.abort_flag, status);
+        if (w_ok) {
+          // the item's HB consecutive (token, head) rows of q, as nine boxes of HB x 64 dims;
+          // rows past the end of q read as zeros, and columns past the last head are never stored
+          const int qrow = I.t0 * H + (DENSE ? 0 : I.hb * HB);
+          mbar_arrive_expect_tx(&sh.q_full, C::Q_BYTES);
+#pragma unroll 1
+          for (int kb = 0; kb < kKB; ++kb) tma_load_2d(sQ + kb * (HB * 128), &tmap_q, &sh.q_full, kb * 64, qrow);
+        }
+      }
       ok = sync_ok(w_ok);
       if (!ok) break;
-      for (int c = tid; c < HB * kChunks; c += kProd) {
-        const int h = c / kChunks, ch = c - h * kChunks;
-        size_t qrow;
-        bool v;
-        if constexpr (DENSE) {
-          v = I.t0 + h / HD < n_q;
-          qrow = static_cast<size_t>(I.t0) * H + h;       // (token, head) rows are contiguous
-        } else {
-          const int head = I.hb * HB + h;
-          v = head < H;
-          qrow = static_cast<size_t>(I.t0) * H + head;
-        }
-        const uint16_t* src = q + (v ? qrow : 0) * kDqk + ch * 8;
-        cp_async_16_zfill(smem_u32(sQ + (ch >> 3) * (HB * 128) + sw128(h, ch & 7)), src, v);
-      }
-      cp_async_mbar_arrive(&sh.q_full);
       if constexpr (DENSE) {
-        // one thread streams the block's consecutive latent rows with TMA, one whole 64-row
-        // tile (nine 64-dim blocks, one 3-D box) per copy as soon as its slot set is released
+        // one thread streams the block's consecutive latent rows, one whole 64-row tile (nine
+        // 64-dim blocks, one 3-D box) per copy as soon as its slot set is released
         if (tid == 0) {
           for (int i = 0; i < I.nt && ok; ++i, ++g) {
             const int s = g & 1;
@@ -281,45 +275,44 @@ __global__ void __launch_bounds__(ACfg<HB, HD>::THREADS, 1)
         }
         ok = sync_ok(ok);
       } else {
+        // A tile is 16 groups of four selected rows x 9 blocks of 64 dims = 144 four-row
+        // gathers of 512 bytes.  Thread tid handles row group tid % 16 for blocks tid / 16,
+        // tid / 16 + 4 and tid / 16 + 8.  The row indices are read before the slot set is
+        // released.  A slot without a selection (-1) gathers row 0 and is masked by the softmax.
         const int t = I.t0;
         const long long kst = __ldg(ks + t);
         const int32_t* irow = idx + static_cast<size_t>(t) * topk;
+        const int grp = tid & 15;
+        const int b0 = tid >> 4;
         for (int i = 0; i < I.nt; ++i, ++g) {
-          w_ok = true;
-          if (tid == 0 && g >= 2) w_ok = mbar_wait(&sh.empty[g & 1], ((g >> 1) - 1) & 1, &sh.abort_flag, status);
-          ok = sync_ok(w_ok);
-          if (!ok) break;
-          // resolve every chunk's row first (independent loads), then issue the copies
-          constexpr int kPer = kRows * kChunks / kProd;   // 72 chunks per thread
-          int rows[kPer];
+          int rows[4];
 #pragma unroll
-          for (int k = 0; k < kPer; ++k) {
-            const int c = tid + k * kProd;
-            const int r = c / kChunks;
-            const int slot = i * kRows + r;
+          for (int u = 0; u < 4; ++u) {
+            const int slot = i * kRows + 4 * grp + u;
             const int j = slot < topk ? __ldg(irow + slot) : -1;
             const long long row = kst + j;
             const bool v = j >= 0 && row >= 0 && row < n_kv;
-            if (j >= 0 && !v && c - r * kChunks == 0) {
+            if (j >= 0 && !v && b0 == 0) {
               atomicOr(status, DEV_ERR_BAD_INDEX);
               atomicAdd(bad_count, 1u);
             }
-            rows[k] = v ? static_cast<int>(row) : -1;
+            rows[u] = v ? static_cast<int>(row) : 0;
           }
-          uint8_t* dst = sT + (g & 1u) * (kKB * kBlkBytes);
+          w_ok = true;
+          if (tid == 0) {
+            if (g >= 2) w_ok = mbar_wait(&sh.empty[g & 1], ((g >> 1) - 1) & 1, &sh.abort_flag, status);
+            if (w_ok) mbar_arrive_expect_tx(&sh.full[g & 1], kKB * kBlkBytes);
+          }
+          ok = sync_ok(w_ok);
+          if (!ok) break;
+          uint8_t* dst = sT + slot_of(g, 0) * kBlkBytes + grp * (4 * 128);
 #pragma unroll
-          for (int k = 0; k < kPer; ++k) {
-            const int c = tid + k * kProd;
-            const int r = c / kChunks, ch = c - r * kChunks;
-            const uint16_t* src = kv + static_cast<size_t>(rows[k] >= 0 ? rows[k] : 0) * kDqk + ch * 8;
-            cp_async_16_zfill(smem_u32(dst + (ch >> 3) * kBlkBytes + sw128(r, ch & 7)), src, rows[k] >= 0);
-          }
-          cp_async_mbar_arrive(&sh.full[g & 1]);
+          for (int b = b0; b < kKB; b += 4)
+            tma_gather4(dst + b * kBlkBytes, &tmap_kv, &sh.full[g & 1], b * 64, rows[0], rows[1], rows[2], rows[3]);
         }
       }
       ++it;
     }
-    cp_async_wait<0>();
   } else if ((warp >= 3 && warp < 7) || warp >= 8) {
     // ---------------------------------------------------------------- softmax + epilogue
     constexpr int kSoft = C::SOFT;
@@ -613,12 +606,10 @@ __global__ void __launch_bounds__(ACfg<HB, HD>::THREADS, 1)
       if (qk_warp) {
         // S^T(g) = tile . Q^T once the whole tile has landed
         ok = wait(&sh.q_full, it & 1);
-        fence_proxy_async_smem();   // Q was written by cp.async (generic proxy); the MMA reads it
         for (int i = 0; i < I.nt && ok; ++i, ++g) {
           const int sb = g & 1;
           if (g >= 2 && !(ok = wait(&sh.s_empty[sb], ((g >> 1) - 1) & 1))) break;
           if (!(ok = wait(&sh.full[g & 1], (g >> 1) & 1))) break;
-          if constexpr (!DENSE) fence_proxy_async_smem();   // gathered rows came through cp.async
           tc_fence_after();
           const uint64_t da = sdesc_sw128(st0 + (g & 1u) * (kKB * kBlkBytes), 16, 1024);
           const uint32_t d_s = tmem + C::S_COL + sb * HB;
@@ -776,8 +767,8 @@ __global__ void __launch_bounds__(256) block_mask_kernel(const int32_t* __restri
 }
 
 template <int HB, int HD>
-cudaError_t launch_cfg(const CUtensorMap& tmap, int n_q, int n_kv, int H, int topk, float scale, const void* q,
-                       const void* kv, const int32_t* idx, const int32_t* ks, const int32_t* row_nt,
+cudaError_t launch_cfg(const CUtensorMap& tmap, const CUtensorMap& tmap_q, int n_q, int n_kv, int H, int topk,
+                       float scale, const int32_t* idx, const int32_t* ks, const int32_t* row_nt,
                        const int2* block_range, const uint32_t* block_mask, void* out, float* lse, uint32_t* status,
                        cudaStream_t st) {
   using C = ACfg<HB, HD>;
@@ -786,10 +777,9 @@ cudaError_t launch_cfg(const CUtensorMap& tmap, int n_q, int n_kv, int H, int to
   if (e != cudaSuccess) return e;
   const int n_items = C::DENSE ? (n_q + C::B - 1) / C::B : n_q * ((H + HB - 1) / HB);
   const int grid = n_items < device_sm_count() ? n_items : device_sm_count();
-  kern<<<grid, C::THREADS, C::DYN_SMEM, st>>>(tmap, static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(kv),
-                                            idx, ks, row_nt, block_range, block_mask, static_cast<uint16_t*>(out), lse,
-                                            n_q, n_kv,
-                                            H, topk, scale * 1.4426950408889634f, status, status + 1);
+  kern<<<grid, C::THREADS, C::DYN_SMEM, st>>>(tmap, tmap_q, idx, ks, row_nt, block_range, block_mask,
+                                            static_cast<uint16_t*>(out), lse, n_q, n_kv, H, topk,
+                                            scale * 1.4426950408889634f, status, status + 1);
   return cudaGetLastError();
 }
 
@@ -815,8 +805,8 @@ namespace {
 size_t dense_mask_offset(int n_blk) { return (static_cast<size_t>(n_blk) * sizeof(int2) + 15) & ~size_t(15); }
 
 template <int HD>
-cudaError_t launch_dense(const CUtensorMap& tmap_kv, int n_q, int n_kv, int n_heads, int topk, float scale,
-                         const void* q, const void* kv, const int32_t* idx, const int32_t* ks, void* out, float* lse,
+cudaError_t launch_dense(const CUtensorMap& tmap_kv, const CUtensorMap& tmap_q, int n_q, int n_kv, int n_heads,
+                         int topk, float scale, const int32_t* idx, const int32_t* ks, void* out, float* lse,
                          uint32_t* status, void* scratch, cudaStream_t st) {
   using C = ACfg<kDenseCols, HD>;
   static_assert(C::B * (C::MAXR / 32) * 4 == kMaskBytes, "one bitmask per block fills the budget exactly");
@@ -826,7 +816,7 @@ cudaError_t launch_dense(const CUtensorMap& tmap_kv, int n_q, int n_kv, int n_he
   block_mask_kernel<C::B, C::MAXR><<<n_blk, 256, 0, st>>>(idx, ks, n_q, n_kv, topk, br, bm, status, status + 1);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  return launch_cfg<kDenseCols, HD>(tmap_kv, n_q, n_kv, n_heads, topk, scale, q, kv, idx, ks, nullptr, br, bm, out,
+  return launch_cfg<kDenseCols, HD>(tmap_kv, tmap_q, n_q, n_kv, n_heads, topk, scale, idx, ks, nullptr, br, bm, out,
                                     lse, status, st);
 }
 
@@ -841,32 +831,37 @@ size_t sparse_attn_ws_bytes(int n_q, int n_heads, int n_kv, int topk) {
   return static_cast<size_t>(n_q) * sizeof(int32_t);
 }
 
-cudaError_t launch_sparse_attn(const CUtensorMap& tmap_kv, int n_q, int n_kv, int n_heads, int topk, float scale,
-                               const void* q, const void* kv, const int32_t* idx, const int32_t* ks, void* out,
-                               float* lse, uint32_t* status, void* scratch, cudaStream_t st) {
+int sparse_attn_q_box_rows(int n_heads, int n_kv, int topk) {
+  if (sparse_attn_dense_heads(n_heads, n_kv, topk)) return kDenseCols;
+  return n_heads <= 16 ? 16 : n_heads <= 32 ? 32 : 64;
+}
+
+cudaError_t launch_sparse_attn(const CUtensorMap& tmap_kv, const CUtensorMap& tmap_q, int n_q, int n_kv, int n_heads,
+                               int topk, float scale, const int32_t* idx, const int32_t* ks, void* out, float* lse,
+                               uint32_t* status, void* scratch, cudaStream_t st) {
   if (n_q <= 0) return cudaSuccess;
   const int hd = sparse_attn_dense_heads(n_heads, n_kv, topk);
   if (hd) {
     switch (hd) {
-      case 1: return launch_dense<1>(tmap_kv, n_q, n_kv, n_heads, topk, scale, q, kv, idx, ks, out, lse, status, scratch, st);
-      case 2: return launch_dense<2>(tmap_kv, n_q, n_kv, n_heads, topk, scale, q, kv, idx, ks, out, lse, status, scratch, st);
-      case 4: return launch_dense<4>(tmap_kv, n_q, n_kv, n_heads, topk, scale, q, kv, idx, ks, out, lse, status, scratch, st);
-      case 8: return launch_dense<8>(tmap_kv, n_q, n_kv, n_heads, topk, scale, q, kv, idx, ks, out, lse, status, scratch, st);
-      default: return launch_dense<16>(tmap_kv, n_q, n_kv, n_heads, topk, scale, q, kv, idx, ks, out, lse, status, scratch, st);
+      case 1: return launch_dense<1>(tmap_kv, tmap_q, n_q, n_kv, n_heads, topk, scale, idx, ks, out, lse, status, scratch, st);
+      case 2: return launch_dense<2>(tmap_kv, tmap_q, n_q, n_kv, n_heads, topk, scale, idx, ks, out, lse, status, scratch, st);
+      case 4: return launch_dense<4>(tmap_kv, tmap_q, n_q, n_kv, n_heads, topk, scale, idx, ks, out, lse, status, scratch, st);
+      case 8: return launch_dense<8>(tmap_kv, tmap_q, n_q, n_kv, n_heads, topk, scale, idx, ks, out, lse, status, scratch, st);
+      default: return launch_dense<16>(tmap_kv, tmap_q, n_q, n_kv, n_heads, topk, scale, idx, ks, out, lse, status, scratch, st);
     }
   }
   int32_t* row_nt = static_cast<int32_t*>(scratch);
   row_tiles_kernel<<<(n_q + 7) / 8, 256, 0, st>>>(idx, n_q, topk, row_nt);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (n_heads <= 16)
-    return launch_cfg<16, 0>(tmap_kv, n_q, n_kv, n_heads, topk, scale, q, kv, idx, ks, row_nt, nullptr, nullptr, out, lse,
-                             status, st);
-  if (n_heads <= 32)
-    return launch_cfg<32, 0>(tmap_kv, n_q, n_kv, n_heads, topk, scale, q, kv, idx, ks, row_nt, nullptr, nullptr, out, lse,
-                             status, st);
-  return launch_cfg<64, 0>(tmap_kv, n_q, n_kv, n_heads, topk, scale, q, kv, idx, ks, row_nt, nullptr, nullptr, out, lse,
-                           status, st);
+  switch (sparse_attn_q_box_rows(n_heads, n_kv, topk)) {
+    case 16: return launch_cfg<16, 0>(tmap_kv, tmap_q, n_q, n_kv, n_heads, topk, scale, idx, ks, row_nt, nullptr, nullptr,
+                                      out, lse, status, st);
+    case 32: return launch_cfg<32, 0>(tmap_kv, tmap_q, n_q, n_kv, n_heads, topk, scale, idx, ks, row_nt, nullptr, nullptr,
+                                      out, lse, status, st);
+    default: return launch_cfg<64, 0>(tmap_kv, tmap_q, n_q, n_kv, n_heads, topk, scale, idx, ks, row_nt, nullptr, nullptr,
+                                      out, lse, status, st);
+  }
 }
 
 }  // namespace dsa
