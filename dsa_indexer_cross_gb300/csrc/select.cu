@@ -138,7 +138,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(int n_chunks, int c
   __shared__ uint32_t hist[256];
   __shared__ int bc[4];
   __shared__ int start[kMaxChunks + 1];
-  __shared__ int warp_tot[kSelThreads / 32];
+  __shared__ int warp_tot[2][kSelThreads / 32];
   __shared__ LinearSmem lin;
   const int t = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -174,75 +174,159 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(int n_chunks, int c
   }
   int32_t* out = idx_out + static_cast<size_t>(t) * topk;
   float* so = score_out ? score_out + static_cast<size_t>(t) * topk : nullptr;
-  // this thread owns the contiguous list positions [p0, p1)
-  const int per = (total + kSelThreads - 1) / kSelThreads;
-  const int p0 = min(total, tid * per), p1 = min(total, p0 + per);
-  auto at = [&](int pos) -> size_t {     // list position -> element offset in the buffers
-    int c = 0;
-    while (pos >= start[c + 1]) ++c;
-    return base + static_cast<size_t>(c) * cap + (pos - start[c]);
+  auto finish = [&](int n_sel) {
+    if (tid == 0 && n_sel != kt) atomicOr(status, DEV_ERR_OVERFLOW);
+    for (int i = n_sel + tid; i < topk; i += kSelThreads) {
+      out[i] = -1;
+      if (so) so[i] = -__int_as_float(0x7f800000);
+    }
   };
-  uint32_t rk[kRegs ? kSelPer : 1];
-  int32_t ri[kRegs ? kSelPer : 1];
+  const bool take_all = total <= kt;
+  uint32_t v = 0, cut = 0x7FFFFFFFu;
   if constexpr (kRegs) {
+    // Up to kSelPer entries per thread, held in registers: thread tid owns the contiguous list
+    // positions [p0, p1), so a block scan of per-thread counts gives the stable order.
+    const int per = (total + kSelThreads - 1) / kSelThreads;
+    const int p0 = min(total, tid * per), p1 = min(total, p0 + per);
+    uint32_t rk[kSelPer];
+    int32_t ri[kSelPer];
 #pragma unroll
     for (int i = 0; i < kSelPer; ++i) {
       if (p0 + i < p1) {
-        const size_t o = at(p0 + i);
+        int c = 0;
+        while (p0 + i >= start[c + 1]) ++c;
+        const size_t o = base + static_cast<size_t>(c) * cap + (p0 + i - start[c]);
         rk[i] = __ldg(cand_key + o);
         ri[i] = __ldg(cand_idx + o);
       }
     }
-  }
-  auto fe = [&](auto&& f) {
-    if constexpr (kRegs) {
+    auto fe = [&](auto&& f) {
 #pragma unroll
       for (int i = 0; i < kSelPer; ++i)
         if (p0 + i < p1) f(rk[i], ri[i]);
-    } else {
-      for (int p = p0; p < p1; ++p) {
-        const size_t o = at(p);
-        f(__ldg(cand_key + o), __ldg(cand_idx + o));
-      }
+    };
+    if (kt > 0 && !take_all && !linear_threshold(fe, tid, kt, lin, v, cut)) {
+      __syncthreads();
+      radix_threshold<kSelThreads>([] { __syncthreads(); }, fe, tid, kt, hist, bc, v, cut);
     }
-  };
-  uint32_t v = 0, cut = 0x7FFFFFFFu;
-  const bool take_all = total <= kt;
-  if (kt > 0 && !take_all && !linear_threshold(fe, tid, kt, lin, v, cut)) {
-    __syncthreads();
-    radix_threshold<kSelThreads>([] { __syncthreads(); }, fe, tid, kt, hist, bc, v, cut);
-  }
-  // stable compaction of the kept entries in list (= key index) order
-  int keep = 0;
-  fe([&](uint32_t key, int32_t idx) { keep += (take_all || topk_keep(key, idx, v, cut)) ? 1 : 0; });
-  int x = keep;
+    int keep = 0;
+    fe([&](uint32_t key, int32_t idx) { keep += (take_all || topk_keep(key, idx, v, cut)) ? 1 : 0; });
+    int x = keep;
 #pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, off);
-    if (lane >= off) x += y;
-  }
-  if (lane == 31) warp_tot[wid] = x;
-  __syncthreads();
-  int pos = x - keep;
-  for (int w = 0; w < wid; ++w) pos += warp_tot[w];
-  fe([&](uint32_t key, int32_t idx) {
-    if (take_all || topk_keep(key, idx, v, cut)) {
-      if (pos < topk) {
-        out[pos] = idx - r.x;
-        if (so) so[pos] = key_float(key);
-      }
-      ++pos;
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, off);
+      if (lane >= off) x += y;
     }
-  });
-  const int n_sel = [&] {
-    int s = 0;
-    for (int w = 0; w < kSelThreads / 32; ++w) s += warp_tot[w];
-    return s;
-  }();
-  if (tid == 0 && n_sel != kt) atomicOr(status, DEV_ERR_OVERFLOW);
-  for (int i = n_sel + tid; i < topk; i += kSelThreads) {
-    out[i] = -1;
-    if (so) so[i] = -__int_as_float(0x7f800000);
+    if (lane == 31) warp_tot[0][wid] = x;
+    __syncthreads();
+    int pos = x - keep;
+    for (int w = 0; w < wid; ++w) pos += warp_tot[0][w];
+    fe([&](uint32_t key, int32_t idx) {
+      if (take_all || topk_keep(key, idx, v, cut)) {
+        if (pos < topk) {
+          out[pos] = idx - r.x;
+          if (so) so[pos] = key_float(key);
+        }
+        ++pos;
+      }
+    });
+    int n_sel = 0;
+    for (int w = 0; w < kSelThreads / 32; ++w) n_sel += warp_tot[0][w];
+    finish(n_sel);
+  } else {
+    // Larger rows stay in the buffers (L2).  The threshold passes only need every entry
+    // once, in any order: thread tid reads positions tid, tid + 256, ... chunk by chunk, with
+    // four loads in flight.
+    auto fe = [&](auto&& f) {
+      for (int c = 0; c < n_chunks; ++c) {
+        const int n = start[c + 1] - start[c];
+        const uint32_t* kp = cand_key + base + static_cast<size_t>(c) * cap;
+        const int32_t* ip = cand_idx + base + static_cast<size_t>(c) * cap;
+        for (int e0 = tid; e0 < n; e0 += 4 * kSelThreads) {
+          uint32_t kk[4];
+          int32_t ii[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int e = e0 + u * kSelThreads;
+            if (e < n) {
+              kk[u] = __ldg(kp + e);
+              ii[u] = __ldg(ip + e);
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            if (e0 + u * kSelThreads < n) f(kk[u], ii[u]);
+        }
+      }
+    };
+    if (kt > 0 && !take_all && !linear_threshold(fe, tid, kt, lin, v, cut)) {
+      __syncthreads();
+      radix_threshold<kSelThreads>([] { __syncthreads(); }, fe, tid, kt, hist, bc, v, cut);
+    }
+    // Stable compaction in list order, in rounds of 1024 entries of one chunk: thread tid
+    // takes the four consecutive entries 4 tid .. 4 tid + 3 of the round (one 16-byte load
+    // each of keys and indices when all four exist), and a block scan of the per-thread
+    // counts places them.  The warp totals alternate between two arrays, so one barrier
+    // per round suffices.
+    int written = 0, round = 0;
+    for (int c = 0; c < n_chunks; ++c) {
+      const int n = start[c + 1] - start[c];
+      const uint32_t* kp = cand_key + base + static_cast<size_t>(c) * cap;
+      const int32_t* ip = cand_idx + base + static_cast<size_t>(c) * cap;
+      for (int r0 = 0; r0 < n; r0 += 4 * kSelThreads, ++round) {
+        const int e = r0 + 4 * tid;
+        uint32_t kk[4] = {0u, 0u, 0u, 0u};
+        int32_t ii[4] = {0, 0, 0, 0};
+        if (e + 3 < n) {
+          const uint4 k4 = __ldg(reinterpret_cast<const uint4*>(kp + e));
+          const int4 i4 = __ldg(reinterpret_cast<const int4*>(ip + e));
+          kk[0] = k4.x; kk[1] = k4.y; kk[2] = k4.z; kk[3] = k4.w;
+          ii[0] = i4.x; ii[1] = i4.y; ii[2] = i4.z; ii[3] = i4.w;
+        } else {
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            if (e + u < n) {
+              kk[u] = __ldg(kp + e + u);
+              ii[u] = __ldg(ip + e + u);
+            }
+        }
+        bool kf[4];
+        int keep = 0;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          kf[u] = e + u < n && (take_all || topk_keep(kk[u], ii[u], v, cut));
+          keep += kf[u] ? 1 : 0;
+        }
+        int x = keep;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, x, off);
+          if (lane >= off) x += y;
+        }
+        const int par = round & 1;
+        if (lane == 31) warp_tot[par][wid] = x;
+        __syncthreads();
+        int pos = written + x - keep, tot = 0;
+#pragma unroll
+        for (int w = 0; w < kSelThreads / 32; ++w) {
+          const int t = warp_tot[par][w];
+          pos += w < wid ? t : 0;
+          tot += t;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          if (kf[u]) {
+            if (pos < topk) {
+              out[pos] = ii[u] - r.x;
+              if (so) so[pos] = key_float(kk[u]);
+            }
+            ++pos;
+          }
+        }
+        written += tot;
+      }
+    }
+    finish(written);
   }
 }
 

@@ -81,6 +81,7 @@ struct ACfg {
   static constexpr int CW = HB / (SW / 4);                             // columns per softmax warp
   static constexpr int NR = CW / 8;                                    // 16x256b repetitions per warp
   static_assert(HB % 16 == 0 && HB <= 64, "columns");
+  static_assert(CW % 16 == 0, "the epilogue reads 16-column groups");
   static_assert(!DENSE || HB % HD == 0, "whole tokens per dense item");
   static_assert(HB * kRows * 2 <= kBlkBytes, "P^T must fit in the rope block");
 };
