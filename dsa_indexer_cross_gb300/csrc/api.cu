@@ -336,8 +336,8 @@ dsa_status run_attn(const dsa_attn_desc* d, const void* q, const void* kv, const
   cudaError_t e;
   if (clear_status && (e = cudaMemsetAsync(ws, 0, kAlign, st)) != cudaSuccess) return cuda_fail(e, "clear status");
   uint32_t* status = status_override ? status_override : reinterpret_cast<uint32_t*>(base);
-  // every operand of the kernel arrives by TMA: q as (token, head) rows, kv as whole 64-row
-  // tiles (block-dense walk) or as single rows for four-row gathers (gather walk)
+  // tensor maps: q as (token, head) rows; kv as whole 64-row tiles (block-dense walk) or as
+  // single rows for four-row gathers (gather walk)
   CUtensorMap tkv, tq;
   std::memset(&tkv, 0, sizeof(tkv));
   std::memset(&tq, 0, sizeof(tq));
@@ -354,7 +354,7 @@ dsa_status run_attn(const dsa_attn_desc* d, const void* q, const void* kv, const
   if ((s = tmap_bf16(&tq, q, 576, static_cast<uint64_t>(d->n_q) * d->n_heads,
                      static_cast<uint32_t>(sparse_attn_q_box_rows(d->n_heads, d->n_kv, d->topk)))) != DSA_OK)
     return s;
-  e = launch_sparse_attn(tkv, tq, d->n_q, d->n_kv, d->n_heads, d->topk, d->softmax_scale, idx, ks, out, lse, status,
+  e = launch_sparse_attn(tkv, tq, d->n_q, d->n_kv, d->n_heads, d->topk, d->softmax_scale, kv, idx, ks, out, lse, status,
                          base + kAlign, st);
   if (e != cudaSuccess) return cuda_fail(e, "sparse attention kernel");
   return DSA_OK;

@@ -65,8 +65,8 @@ int sparse_attn_q_box_rows(int n_heads, int n_kv, int topk);
 // tmap_q: q as a 2-D [n_q * n_heads][576] tensor, 128-byte swizzled boxes of
 // {64, sparse_attn_q_box_rows(...)}.
 cudaError_t launch_sparse_attn(const CUtensorMap& tmap_kv, const CUtensorMap& tmap_q, int n_q, int n_kv, int n_heads,
-                               int topk, float scale, const int32_t* idx, const int32_t* ks, void* out, float* lse,
-                               uint32_t* status, void* scratch, cudaStream_t st);
+                               int topk, float scale, const void* kv, const int32_t* idx, const int32_t* ks, void* out,
+                               float* lse, uint32_t* status, void* scratch, cudaStream_t st);
 
 int device_sm_count();
 

@@ -38,9 +38,9 @@
 // TMEM shape, so each thread holds two rows and HB/4 columns; running sums stay in registers
 // and are reduced once per item.
 //
-// Warp roles (256 threads): warps 0-1 load Q and the rows, all through the Tensor Memory
-// Accelerator (Q as nine 64-dim boxes; the rows as four-row gathers, or one 3-D box per tile in
-// block-dense mode); warp 2 issues the S^T products; warps 3-6 run the softmax and the
+// Warp roles (256 threads): warps 0-1 load Q and the rows (Q as nine 64-dim TMA boxes; the
+// rows as one 3-D TMA box per tile in block-dense mode, or as four-row TMA gathers plus
+// cp.async for the last blocks in the gather walk); warp 2 issues the S^T products; warps 3-6 run the softmax and the
 // epilogue; warp 7 owns TMEM and issues the PV products.  With the two products issued from separate warps, PV(g) goes out as soon as
 // P(g) exists instead of queueing behind S^T(g+1), whose blocks may still be in flight.
 // Persistent CTAs.
@@ -59,6 +59,10 @@ constexpr int kKB = kDqk / 64;     // 64-dim blocks per tile (the last one holds
 constexpr int kBlkBytes = kRows * 128;         // one block: 64 rows x 128 B
 constexpr int kSlots = 2 * kKB;                // two tiles in flight
 constexpr int kProd = 64;                      // warps 0-1
+// Gather walk: the last kCpBlocks 64-dim blocks of every tile come through cp.async (the
+// load/store unit) while the other blocks come through four-row TMA gathers, so both copy
+// paths of the SM work on a tile at once (the TMA unit alone takes ~37 cycles per gather).
+constexpr int kCpBlocks = 2;
 // Warps 0-1 load, warp 2 issues S^T, warps 3-6 (and, block-dense, 8-11) run the softmax,
 // warp 7 owns TMEM and issues PV.
 constexpr int kDenseCols = 64;                 // columns of a block-dense item
@@ -171,7 +175,7 @@ __device__ __forceinline__ Item item_info(int item, int n_hb, const int32_t* row
 template <int HB, int HD>
 __global__ void __launch_bounds__(ACfg<HB, HD>::THREADS, 1)
     sparse_attn_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_constant__ CUtensorMap tmap_q,
-                       const int32_t* __restrict__ idx,
+                       const uint16_t* __restrict__ kv, const int32_t* __restrict__ idx,
                        const int32_t* __restrict__ ks, const int32_t* __restrict__ row_nt,
                        const int2* __restrict__ block_range, const uint32_t* __restrict__ block_mask,
                        uint16_t* __restrict__ out, float* __restrict__ lse, int n_q, int n_kv, int H, int topk,
@@ -199,7 +203,7 @@ __global__ void __launch_bounds__(ACfg<HB, HD>::THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&sh.full[s], 1);
+      mbar_init(&sh.full[s], DENSE || kCpBlocks == 0 ? 1 : 1 + kProd);   // + the cp.async arrivals
       mbar_init(&sh.empty[s], 1);
     }
     mbar_init(&sh.q_full, 1);
@@ -276,40 +280,62 @@ __global__ void __launch_bounds__(ACfg<HB, HD>::THREADS, 1)
         }
         ok = sync_ok(ok);
       } else {
-        // A tile is 16 groups of four selected rows x 9 blocks of 64 dims = 144 four-row
-        // gathers of 512 bytes.  Thread tid handles row group tid % 16 for blocks tid / 16,
-        // tid / 16 + 4 and tid / 16 + 8.  The row indices are read before the slot set is
-        // released.  A slot without a selection (-1) gathers row 0 and is masked by the softmax.
+        // A tile is 64 selected rows x 9 blocks of 64 dims.  Blocks [0, kTmaBlocks) come as
+        // 16 groups of four rows per block through four-row TMA gathers: thread tid handles row
+        // group tid % 16 for blocks tid / 16, tid / 16 + 4, ...  The other blocks come through
+        // cp.async: thread tid copies 16-byte chunk tid % 8 of rows tid / 8 + 8 m (m < 8), so a
+        // warp reads four whole 128-byte row segments per instruction.  Row indices are read
+        // before the slot set is released.  A slot without a selection (-1) reads row 0 (TMA)
+        // or zeros (cp.async) and is masked by the softmax.
+        constexpr int kTmaBlocks = kKB - kCpBlocks;
         const int t = I.t0;
         const long long kst = __ldg(ks + t);
         const int32_t* irow = idx + static_cast<size_t>(t) * topk;
         const int grp = tid & 15;
         const int b0 = tid >> 4;
+        auto row_of = [&](int slot, bool count_bad) -> int {
+          const int j = slot < topk ? __ldg(irow + slot) : -1;
+          const long long row = kst + j;
+          const bool v = j >= 0 && row >= 0 && row < n_kv;
+          if (count_bad && j >= 0 && !v) {
+            atomicOr(status, DEV_ERR_BAD_INDEX);
+            atomicAdd(bad_count, 1u);
+          }
+          return v ? static_cast<int>(row) : -1;
+        };
         for (int i = 0; i < I.nt; ++i, ++g) {
           int rows[4];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int slot = i * kRows + 4 * grp + u;
-            const int j = slot < topk ? __ldg(irow + slot) : -1;
-            const long long row = kst + j;
-            const bool v = j >= 0 && row >= 0 && row < n_kv;
-            if (j >= 0 && !v && b0 == 0) {
-              atomicOr(status, DEV_ERR_BAD_INDEX);
-              atomicAdd(bad_count, 1u);
-            }
-            rows[u] = v ? static_cast<int>(row) : 0;
+          for (int u = 0; u < 4; ++u) rows[u] = row_of(i * kRows + 4 * grp + u, b0 == 0);
+          int crow[kCpBlocks > 0 ? 8 : 1];
+          if constexpr (kCpBlocks > 0) {
+#pragma unroll
+            for (int m = 0; m < 8; ++m) crow[m] = row_of(i * kRows + (tid >> 3) + 8 * m, false);
           }
           w_ok = true;
           if (tid == 0) {
             if (g >= 2) w_ok = mbar_wait(&sh.empty[g & 1], ((g >> 1) - 1) & 1, &sh.abort_flag, status);
-            if (w_ok) mbar_arrive_expect_tx(&sh.full[g & 1], kKB * kBlkBytes);
+            if (w_ok) mbar_arrive_expect_tx(&sh.full[g & 1], kTmaBlocks * kBlkBytes);
           }
           ok = sync_ok(w_ok);
           if (!ok) break;
-          uint8_t* dst = sT + slot_of(g, 0) * kBlkBytes + grp * (4 * 128);
+          uint8_t* tile = sT + slot_of(g, 0) * kBlkBytes;
 #pragma unroll
-          for (int b = b0; b < kKB; b += 4)
-            tma_gather4(dst + b * kBlkBytes, &tmap_kv, &sh.full[g & 1], b * 64, rows[0], rows[1], rows[2], rows[3]);
+          for (int b = b0; b < kTmaBlocks; b += 4)
+            tma_gather4(tile + b * kBlkBytes + grp * (4 * 128), &tmap_kv, &sh.full[g & 1], b * 64, max(rows[0], 0),
+                        max(rows[1], 0), max(rows[2], 0), max(rows[3], 0));
+          if constexpr (kCpBlocks > 0) {
+            const int ch = tid & 7;
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+              const int r = (tid >> 3) + 8 * m;
+              const uint16_t* src = kv + static_cast<size_t>(crow[m] >= 0 ? crow[m] : 0) * kDqk + ch * 8;
+#pragma unroll
+              for (int b = kTmaBlocks; b < kKB; ++b)
+                cp_async_16_zfill(smem_u32(tile + b * kBlkBytes + sw128(r, ch)), src + b * 64, crow[m] >= 0);
+            }
+            cp_async_mbar_arrive(&sh.full[g & 1]);
+          }
         }
       }
       ++it;
@@ -611,6 +637,7 @@ __global__ void __launch_bounds__(ACfg<HB, HD>::THREADS, 1)
           const int sb = g & 1;
           if (g >= 2 && !(ok = wait(&sh.s_empty[sb], ((g >> 1) - 1) & 1))) break;
           if (!(ok = wait(&sh.full[g & 1], (g >> 1) & 1))) break;
+          if constexpr (!DENSE && kCpBlocks > 0) fence_proxy_async_smem();   // cp.async-written blocks
           tc_fence_after();
           const uint64_t da = sdesc_sw128(st0 + (g & 1u) * (kKB * kBlkBytes), 16, 1024);
           const uint32_t d_s = tmem + C::S_COL + sb * HB;
@@ -629,6 +656,7 @@ __global__ void __launch_bounds__(ACfg<HB, HD>::THREADS, 1)
         // apart), B = P^T in the rope block (MN-major)
         for (int i = 0; i < I.nt && ok; ++i, ++g) {
           ok = wait(&sh.p_full, g & 1);
+          if constexpr (!DENSE && kCpBlocks > 0) fence_proxy_async_smem();   // V blocks written by cp.async
           if (ok && i == 0 && it > 0) ok = wait(&sh.o_free, (it - 1) & 1);
           if (!ok) break;
           tc_fence_after();
@@ -769,7 +797,7 @@ __global__ void __launch_bounds__(256) block_mask_kernel(const int32_t* __restri
 
 template <int HB, int HD>
 cudaError_t launch_cfg(const CUtensorMap& tmap, const CUtensorMap& tmap_q, int n_q, int n_kv, int H, int topk,
-                       float scale, const int32_t* idx, const int32_t* ks, const int32_t* row_nt,
+                       float scale, const void* kv, const int32_t* idx, const int32_t* ks, const int32_t* row_nt,
                        const int2* block_range, const uint32_t* block_mask, void* out, float* lse, uint32_t* status,
                        cudaStream_t st) {
   using C = ACfg<HB, HD>;
@@ -778,7 +806,8 @@ cudaError_t launch_cfg(const CUtensorMap& tmap, const CUtensorMap& tmap_q, int n
   if (e != cudaSuccess) return e;
   const int n_items = C::DENSE ? (n_q + C::B - 1) / C::B : n_q * ((H + HB - 1) / HB);
   const int grid = n_items < device_sm_count() ? n_items : device_sm_count();
-  kern<<<grid, C::THREADS, C::DYN_SMEM, st>>>(tmap, tmap_q, idx, ks, row_nt, block_range, block_mask,
+  kern<<<grid, C::THREADS, C::DYN_SMEM, st>>>(tmap, tmap_q, static_cast<const uint16_t*>(kv), idx, ks, row_nt,
+                                            block_range, block_mask,
                                             static_cast<uint16_t*>(out), lse, n_q, n_kv, H, topk,
                                             scale * 1.4426950408889634f, status, status + 1);
   return cudaGetLastError();
@@ -817,7 +846,7 @@ cudaError_t launch_dense(const CUtensorMap& tmap_kv, const CUtensorMap& tmap_q, 
   block_mask_kernel<C::B, C::MAXR><<<n_blk, 256, 0, st>>>(idx, ks, n_q, n_kv, topk, br, bm, status, status + 1);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  return launch_cfg<kDenseCols, HD>(tmap_kv, tmap_q, n_q, n_kv, n_heads, topk, scale, idx, ks, nullptr, br, bm, out,
+  return launch_cfg<kDenseCols, HD>(tmap_kv, tmap_q, n_q, n_kv, n_heads, topk, scale, nullptr, idx, ks, nullptr, br, bm, out,
                                     lse, status, st);
 }
 
@@ -838,7 +867,7 @@ int sparse_attn_q_box_rows(int n_heads, int n_kv, int topk) {
 }
 
 cudaError_t launch_sparse_attn(const CUtensorMap& tmap_kv, const CUtensorMap& tmap_q, int n_q, int n_kv, int n_heads,
-                               int topk, float scale, const int32_t* idx, const int32_t* ks, void* out, float* lse,
+                               int topk, float scale, const void* kv, const int32_t* idx, const int32_t* ks, void* out, float* lse,
                                uint32_t* status, void* scratch, cudaStream_t st) {
   if (n_q <= 0) return cudaSuccess;
   const int hd = sparse_attn_dense_heads(n_heads, n_kv, topk);
@@ -856,11 +885,11 @@ cudaError_t launch_sparse_attn(const CUtensorMap& tmap_kv, const CUtensorMap& tm
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   switch (sparse_attn_q_box_rows(n_heads, n_kv, topk)) {
-    case 16: return launch_cfg<16, 0>(tmap_kv, tmap_q, n_q, n_kv, n_heads, topk, scale, idx, ks, row_nt, nullptr, nullptr,
+    case 16: return launch_cfg<16, 0>(tmap_kv, tmap_q, n_q, n_kv, n_heads, topk, scale, kv, idx, ks, row_nt, nullptr, nullptr,
                                       out, lse, status, st);
-    case 32: return launch_cfg<32, 0>(tmap_kv, tmap_q, n_q, n_kv, n_heads, topk, scale, idx, ks, row_nt, nullptr, nullptr,
+    case 32: return launch_cfg<32, 0>(tmap_kv, tmap_q, n_q, n_kv, n_heads, topk, scale, kv, idx, ks, row_nt, nullptr, nullptr,
                                       out, lse, status, st);
-    default: return launch_cfg<64, 0>(tmap_kv, tmap_q, n_q, n_kv, n_heads, topk, scale, idx, ks, row_nt, nullptr, nullptr,
+    default: return launch_cfg<64, 0>(tmap_kv, tmap_q, n_q, n_kv, n_heads, topk, scale, kv, idx, ks, row_nt, nullptr, nullptr,
                                       out, lse, status, st);
   }
 }
