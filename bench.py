@@ -127,10 +127,10 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------------- workload
-def build_inputs(w, geo, device):
+def build_inputs(w, geo, device, n_layers=None):
     from dsa_indexer_cross_gb300 import synth
     layers = []
-    for l in range(len(w.layers)):
+    for l in range(len(w.layers) if n_layers is None else n_layers):
         L = synth.layer_inputs(w, geo, l, device=device)
         L["out"] = torch.empty((w.n_q, w.n_heads, w.d_v), dtype=torch.bfloat16, device=device)
         L["lse"] = torch.empty((w.n_q, w.n_heads), dtype=torch.float32, device=device)
@@ -159,7 +159,7 @@ def roofline_numbers(w, geo):
 
 # DRAM bytes (read + write) of one sparse_attn_kernel launch, per workload, from an ncu capture
 # of the current kernel (profiles/sparse_attn_<workload>.md); workloads not listed report None.
-ATTN_TRAFFIC_BYTES = {"prefill_4k": 112.04e6}
+ATTN_TRAFFIC_BYTES = {"prefill_4k": 112.24e6, "chunk_1m": 8.775e9}
 
 
 def peaks():
@@ -254,7 +254,8 @@ def run_native(args):
     geo = synth.geometry(w)
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
     q_pos, k_pos, ks, ke = t(geo.q_pos), t(geo.k_pos), t(geo.ks), t(geo.ke)
-    layers = build_inputs(w, geo, dev)
+    # a profiler capture (--only) needs the first layer alone
+    layers = build_inputs(w, geo, dev, n_layers=1 if args.only is not None else None)
     cache = D.IndexCache(w.layers, w.n_q, w.topk, device=dev)
     flags = D.DSA_IDX_ROPE_Q | (D.DSA_IDX_ROPE_K if w.rope_k else 0)
     if w.kind == "decode":
@@ -376,9 +377,11 @@ def run_native(args):
 
     hbm, tc_burst, tc_sus, peak_kind = peaks()
     R = roofline_numbers(w, geo)
+    hbm_bound_attn = geo.n_kv * w.d_qk * 2 > (64 << 20)   # one layer's latent cache well beyond L2
     attn_gbs = R["attn_gathered"] / (attn_ms / 1e3) / 1e9
     attn_strict_tflops = R["attn_flops"] / (attn_ms / 1e3) / 1e12
     idx_tflops = R["idx_flops"] / (idx_ms / 1e3) / 1e12
+    idx_gbs = R["idx_bytes"] / (idx_ms / 1e3) / 1e9
     score_tflops = R["idx_flops"] / (phase_ms[2] / 1e3) / 1e12
     gpu_launches = sum((3 if t == "full" else 0) + 2 for t in w.layers) + 2 * sum(t == "full" for t in w.layers)
 
@@ -395,25 +398,35 @@ def run_native(args):
         "e2e": {"value": ws_n * w.n_q / (e2e_ms / 1e3), "unit": "query_tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": gpu_launches * args.steps,
-        # The latent cache of one layer is L2-resident at this size, so the binding roofline of
-        # the attention is the tensor one: selected (query, head, row) triples x (576 + 512) x 2
-        # FLOPs.  The minimum HBM bytes (inputs once + outputs) and the bytes a per-token gather
-        # would move are given for context.
-        "roofline": {"kernel": "sparse_attn_kernel", "bound": "tensor", "achieved": attn_strict_tflops,
-                     "peak": tc_burst, "unit": "TFLOP/s", "frac": attn_strict_tflops / tc_burst,
-                     "traffic": ATTN_TRAFFIC_BYTES.get(w.name), "peak_kind": peak_kind + " (bf16 burst)",
-                     "algorithmic_flops_per_launch": R["attn_flops"], "ms_per_launch": attn_ms,
-                     "min_hbm_bytes_per_launch": R["attn_min_bytes"],
-                     "min_hbm_frac": R["attn_min_bytes"] / (attn_ms / 1e3) / 1e9 / hbm,
-                     "per_token_gather_bytes_per_launch": R["attn_gathered"], "per_token_gather_gbs": attn_gbs,
-                     # the gather framing of the roofline (each token reads its own rows from HBM);
-                     # above 1 means rows were reused from L2 / shared memory across tokens
-                     "per_token_gather_frac_of_hbm": attn_gbs / hbm},
-        "roofline_indexer": {"kernel": "indexer call (rope + tcgen05 scores/top-k + select)", "bound": "tensor",
-                             "achieved": idx_tflops, "peak": tc_burst, "unit": "TFLOP/s", "frac": idx_tflops / tc_burst,
-                             "algorithmic_flops_per_launch": R["idx_flops"],
-                             "causal_flops_per_launch": R["idx_flops_causal"], "ms_per_launch": idx_ms,
-                             "peak_kind": peak_kind + " (bf16 burst)"},
+        # While one layer's latent cache is L2-resident (prefill_4k, long_32k) the binding
+        # roofline of the attention is the tensor one: selected (query, head, row) triples x
+        # (576 + 512) x 2 FLOPs.  A cache far larger than L2 (chunk_1m, decode_64) makes it the
+        # HBM one: every token gathers its own rows (the per-token gather bytes).  Both framings
+        # and the minimum HBM bytes (inputs once + outputs) are given either way.
+        "roofline": dict(({"bound": "hbm", "achieved": attn_gbs, "peak": hbm, "unit": "GB/s",
+                           "frac": attn_gbs / hbm, "peak_kind": peak_kind + " (HBM copy)"}
+                          if hbm_bound_attn else
+                          {"bound": "tensor", "achieved": attn_strict_tflops, "peak": tc_burst, "unit": "TFLOP/s",
+                           "frac": attn_strict_tflops / tc_burst, "peak_kind": peak_kind + " (bf16 burst)"}),
+                     kernel="sparse_attn_kernel", traffic=ATTN_TRAFFIC_BYTES.get(w.name),
+                     tensor_tflops=attn_strict_tflops, tensor_frac=attn_strict_tflops / tc_burst,
+                     algorithmic_flops_per_launch=R["attn_flops"], ms_per_launch=attn_ms,
+                     **{
+                        "min_hbm_bytes_per_launch": R["attn_min_bytes"],
+                        "min_hbm_frac": R["attn_min_bytes"] / (attn_ms / 1e3) / 1e9 / hbm,
+                        "per_token_gather_bytes_per_launch": R["attn_gathered"], "per_token_gather_gbs": attn_gbs,
+                        # the gather framing of the roofline (each token reads its own rows from HBM);
+                        # above 1 means rows were reused from L2 / shared memory across tokens
+                        "per_token_gather_frac_of_hbm": attn_gbs / hbm}),
+        # decode scores 64 flop per byte of index keys: bound by HBM, not by the tensor cores
+        "roofline_indexer": dict(({"bound": "hbm", "achieved": idx_gbs, "peak": hbm, "unit": "GB/s",
+                                   "frac": idx_gbs / hbm, "peak_kind": peak_kind + " (HBM copy)"}
+                                  if w.kind == "decode" else
+                                  {"bound": "tensor", "achieved": idx_tflops, "peak": tc_burst, "unit": "TFLOP/s",
+                                   "frac": idx_tflops / tc_burst, "peak_kind": peak_kind + " (bf16 burst)"}),
+                                 kernel="indexer call (rope + tcgen05 scores/top-k + select)",
+                                 algorithmic_flops_per_launch=R["idx_flops"], algorithmic_bytes_per_launch=R["idx_bytes"],
+                                 causal_flops_per_launch=R["idx_flops_causal"], ms_per_launch=idx_ms),
         # the tensor-core score kernel of that call on its own (events between the call's launches)
         "roofline_indexer_kernel": {"kernel": "indexer_kernel (tcgen05 scores + streaming top-k)", "bound": "tensor",
                                     "achieved": score_tflops, "peak": tc_burst, "unit": "TFLOP/s",
