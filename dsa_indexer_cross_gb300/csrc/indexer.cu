@@ -336,12 +336,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int j = 0; j < 64; j += 4) {
               const float4 wv = *reinterpret_cast<const float4*>(&sh.w_s[c0 + j]);
-              const float wj[4] = {wv.x, wv.y, wv.z, wv.w};
+              const float r0 = fmaxf(__uint_as_float(v[j]), 0.f), r1 = fmaxf(__uint_as_float(v[j + 1]), 0.f);
+              const float r2 = fmaxf(__uint_as_float(v[j + 2]), 0.f), r3 = fmaxf(__uint_as_float(v[j + 3]), 0.f);
+              const int g = (c0 + j) / HI;
+              if constexpr (NP == 4) {
+                // columns c0+j .. c0+j+3 feed partial sums 0..3 of query g: two packed FMAs
+                fma2(part[g][0], part[g][1], wv.x, wv.y, r0, r1);
+                fma2(part[g][2], part[g][3], wv.z, wv.w, r2, r3);
+              } else {
+                const float wj[4] = {wv.x, wv.y, wv.z, wv.w}, rj[4] = {r0, r1, r2, r3};
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int col = c0 + j + e;
-                float& a = part[col / HI][NP == 1 ? 0 : (col % NP)];
-                a = fmaf(wj[e], fmaxf(__uint_as_float(v[j + e]), 0.f), a);
+                for (int e = 0; e < 4; ++e) {
+                  float& acc_e = part[(c0 + j + e) / HI][0];
+                  acc_e = fmaf(wj[e], rj[e], acc_e);
+                }
               }
             }
           }
