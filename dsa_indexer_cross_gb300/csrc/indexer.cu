@@ -39,6 +39,7 @@ constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
 constexpr int kKeyTile = 128;
 constexpr int kMaxPer = 33;  // ceil(cap / kEpiThreads) with cap = 2k + 128 <= 4224
+constexpr int kCutBins = 2048;   // value-linear bins of a cut-back
 
 template <int HI, int DI, int G>
 struct Cfg {
@@ -46,7 +47,7 @@ struct Cfg {
   static constexpr int KB = DI / 64;                     // 128-byte K blocks per row
   static constexpr int Q_BYTES = N * DI * 2;
   static constexpr int K_STAGE_BYTES = kKeyTile * DI * 2;
-  static constexpr int SMEM_BUDGET = 232448 - 6144;      // dynamic budget after static smem
+  static constexpr int SMEM_BUDGET = 232448 - 14336;     // dynamic budget after static smem
   static constexpr int STAGES_FIT = (SMEM_BUDGET - 1024 - Q_BYTES) / K_STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT > 6 ? 6 : STAGES_FIT;
   static constexpr int DYN_SMEM = 1024 + Q_BYTES + STAGES * K_STAGE_BYTES;
@@ -63,15 +64,17 @@ struct Shared {
   uint64_t t_full[2], t_empty[2];
   uint32_t tmem_base;
   uint32_t abort_flag;
-  uint32_t hist[256];
+  uint32_t hist[kCutBins];   // cut-back histogram (the radix fallback uses the first 256 bins)
   int bc[4];
   int warp_off[4];
+  uint32_t wmin[4], wmax[4];
   uint32_t tau[64];
   int cnt[2][64];        // candidates held per query; [tile parity] so a tile reads one copy and writes the other
   alignas(16) int qcnt[4][64];   // this tile's appends per (TMEM lane quarter, query)
   int epi_abort;
 };
 static_assert(offsetof(Shared, w_s) % 16 == 0, "float4 access");
+static_assert(sizeof(Shared) <= 14336, "static shared memory within the budget the stage count assumes");
 
 // Named barrier over n threads that also returns the OR of a predicate across them.
 __device__ __forceinline__ bool bar_red_or(uint32_t id, uint32_t n, bool p) {
@@ -84,8 +87,12 @@ __device__ __forceinline__ bool bar_red_or(uint32_t id, uint32_t n, bool p) {
   return r != 0;
 }
 
+// Candidate store through the global state space.  No "memory" clobber: the compiler may keep
+// shared-memory state in registers across it (a generic store could alias shared memory).
+// The store stays in program order with the other volatile asm statements (barriers, fences)
+// that publish it.
 __device__ __forceinline__ void st_global_u32(uint32_t* p, uint32_t v) {
-  asm volatile("{\n .reg .u64 ga;\n cvta.to.global.u64 ga, %0;\n st.global.u32 [ga], %1;\n}\n" ::"l"(p), "r"(v) : "memory");
+  asm volatile("{\n .reg .u64 ga;\n cvta.to.global.u64 ga, %0;\n st.global.u32 [ga], %1;\n}\n" ::"l"(p), "r"(v));
 }
 
 struct UnitInfo {
@@ -105,18 +112,33 @@ __device__ __forceinline__ UnitInfo unit_info(int u, int n_groups, int chunk_len
   return ui;
 }
 
-// Cut the candidate buffer of one (row, chunk) back to its top-K, keeping the survivors in
-// their original (key index) order.  Called by the 128 epilogue threads together; thread i
-// owns the contiguous entries [i*P, i*P + P).  Returns the new threshold key.
-__device__ uint32_t compact_buffer(uint32_t* keys, int32_t* idxs, int n, int K, int tid, Shared& sh) {
-  const int P = (n + kEpiThreads - 1) / kEpiThreads;     // <= kMaxPer
-  const int e0 = tid * P;
+// Cut the candidate buffer of one (row, chunk) back to a superset of its top-K, keeping the
+// survivors in their original (key index) order.  Called by the 128 epilogue threads together.
+//
+// The buffer only has to keep every entry that can still be in the final top-K, so the cut
+// need not be exact: one histogram of 2048 bins linear in score over the buffer's [min, max]
+// finds the bin b holding the K-th largest score, and every entry in bins >= b is kept (at
+// least K entries; bins are monotone in score, so everything dropped scores below everything
+// kept).  The new threshold is the smallest kept key: a later key at or below it has at least
+// K earlier keys at or above it and loses to them (ties go to the lower key index).  When the
+// boundary bin is crowded (many equal or nearly equal scores) so that the cut would free less
+// than half the headroom, the exact radix select (threshold (v, cut), exactly K kept) runs
+// instead.  Returns {threshold key, entries kept}.
+struct CutResult {
+  uint32_t tau;
+  int kept;
+};
+__device__ CutResult compact_buffer(uint32_t* keys, int32_t* idxs, int n, int K, int tid, Shared& sh) {
+  // Entry tid + 128 i is held by thread tid in slot i (coalesced loads and stores); round i
+  // is the 128 entries [128 i, 128 i + 128), so list order = (round, thread) order.
+  const int lane = tid & 31, wq = tid >> 5;
+  const int rounds = (n + kEpiThreads - 1) / kEpiThreads;   // <= kMaxPer
   uint32_t rk[kMaxPer];
   int32_t ri[kMaxPer];
 #pragma unroll
   for (int i = 0; i < kMaxPer; ++i) {
-    const int e = e0 + i;
-    const bool in = i < P && e < n;
+    const int e = tid + i * kEpiThreads;
+    const bool in = e < n;
     rk[i] = in ? keys[e] : 0u;
     ri[i] = in ? idxs[e] : 0;
   }
@@ -124,34 +146,130 @@ __device__ uint32_t compact_buffer(uint32_t* keys, int32_t* idxs, int n, int K, 
   auto fe = [&](auto&& f) {
 #pragma unroll
     for (int i = 0; i < kMaxPer; ++i)
-      if (i < P && e0 + i < n) f(rk[i], ri[i]);
+      if (tid + i * kEpiThreads < n) f(rk[i], ri[i]);
   };
-  uint32_t v, cut;
-  radix_threshold<kEpiThreads>(sync, fe, tid, K, sh.hist, sh.bc, v, cut);
-  int keep = 0;
-  fe([&](uint32_t key, int32_t idx) { keep += topk_keep(key, idx, v, cut) ? 1 : 0; });
-  // block exclusive scan of `keep` over the 128 threads (thread order = entry order)
-  const int lane = tid & 31, wq = tid >> 5;
-  int x = keep;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, off);
-    if (lane >= off) x += y;
-  }
-  if (lane == 31) sh.warp_off[wq] = x;
-  sync();
-  int pos = x - keep;
-  for (int wv = 0; wv < wq; ++wv) pos += sh.warp_off[wv];
-  fe([&](uint32_t key, int32_t idx) {
-    if (topk_keep(key, idx, v, cut)) {
-      keys[pos] = key;
-      idxs[pos] = idx;
-      ++pos;
-    }
+  // ---- coarse cut: key range, then one histogram pass
+  uint32_t mn = 0xFFFFFFFFu, mx = 0u;
+  fe([&](uint32_t key, int32_t) {
+    mn = min(mn, key);
+    mx = max(mx, key);
   });
+  mn = __reduce_min_sync(0xffffffffu, mn);
+  mx = __reduce_max_sync(0xffffffffu, mx);
+  if (lane == 0) {
+    sh.wmin[wq] = mn;
+    sh.wmax[wq] = mx;
+  }
+  for (int i = tid; i < kCutBins; i += kEpiThreads) sh.hist[i] = 0u;
+  sync();
+  const uint32_t kmin = min(min(sh.wmin[0], sh.wmin[1]), min(sh.wmin[2], sh.wmin[3]));
+  const uint32_t kmax = max(max(sh.wmax[0], sh.wmax[1]), max(sh.wmax[2], sh.wmax[3]));
+  const float fmin = key_float(kmin), fmax = key_float(kmax);
+  const float span = fmax - fmin;
+  const float scale = span > 0.f && span < 3.0e38f ? static_cast<float>(kCutBins) / span : 0.f;
+  auto bin_of = [&](uint32_t key) {
+    const float y = (key_float(key) - fmin) * scale;
+    return y >= static_cast<float>(kCutBins - 1) ? kCutBins - 1 : (y > 0.f ? static_cast<int>(y) : 0);
+  };
+  fe([&](uint32_t key, int32_t) { atomicAdd(&sh.hist[bin_of(key)], 1u); });
+  sync();
+  // thread tid owns the 16 bins [kCutBins - 16 tid - 16, kCutBins - 16 tid), visited from the top
+  constexpr int kPerT = kCutBins / kEpiThreads;
+  {
+    int h[kPerT], sum = 0;
+#pragma unroll
+    for (int j = 0; j < kPerT; ++j) {
+      h[j] = static_cast<int>(sh.hist[kCutBins - 1 - (tid * kPerT + j)]);
+      sum += h[j];
+    }
+    int x = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, off);
+      if (lane >= off) x += y;
+    }
+    if (lane == 31) sh.warp_off[wq] = x;
+    sync();
+    int c = x - sum;
+    for (int w = 0; w < wq; ++w) c += sh.warp_off[w];
+    if (c < K && K <= c + sum) {
+#pragma unroll
+      for (int j = 0; j < kPerT; ++j) {
+        if (c < K && K <= c + h[j]) {
+          sh.bc[0] = kCutBins - 1 - (tid * kPerT + j);
+          sh.bc[1] = c + h[j];   // entries in bins >= the boundary bin
+        }
+        c += h[j];
+      }
+    }
+    sync();
+  }
+  const int bb = sh.bc[0], kept_coarse = sh.bc[1];
+  const int cap_free = n - kKeyTile;   // the cut is only worth it if it frees half the headroom
+  const bool coarse = kept_coarse <= K + (cap_free - K) / 2;
+  uint32_t v = 0, cut = 0x7FFFFFFFu;
+  if (!coarse) {
+    sync();
+    radix_threshold<kEpiThreads>(sync, fe, tid, K, sh.hist, sh.bc, v, cut);
+  }
+  // ---- stable compaction: per round, a ballot per warp; warp counts of every round go to
+  // shared memory (sh.hist is free now), one warp turns them into exclusive offsets in
+  // (round, warp) order, and every kept entry lands at its offset + its rank in the ballot
+  uint32_t kb[kMaxPer];
+  uint32_t kmin_kept = 0xFFFFFFFFu;
+  uint32_t* rc = sh.hist;   // [kMaxPer][4] counts, then offsets
+#pragma unroll
+  for (int i = 0; i < kMaxPer; ++i) {
+    const bool in = tid + i * kEpiThreads < n;
+    const bool k = in && (coarse ? bin_of(rk[i]) >= bb : topk_keep(rk[i], ri[i], v, cut));
+    kb[i] = __ballot_sync(0xffffffffu, k);
+    if (k) kmin_kept = min(kmin_kept, rk[i]);
+    if (lane == 0 && i < rounds) rc[i * 4 + wq] = __popc(kb[i]);
+  }
+  kmin_kept = __reduce_min_sync(0xffffffffu, kmin_kept);
+  if (lane == 0) sh.wmin[wq] = kmin_kept;
+  sync();
+  if (wq == 0) {
+    // exclusive scan of rounds * 4 counts in order (at most 132), 32 lanes x 5 entries
+    constexpr int kPer = (kMaxPer * 4 + 31) / 32;
+    const int m = rounds * 4;
+    uint32_t c[kPer], sum = 0;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int e = lane * kPer + j;
+      c[j] = e < m ? rc[e] : 0u;
+      sum += c[j];
+    }
+    uint32_t x = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, x, off);
+      if (lane >= off) x += y;
+    }
+    uint32_t run = x - sum;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int e = lane * kPer + j;
+      if (e < m) rc[e] = run;
+      run += c[j];
+    }
+    if (lane == 31) sh.bc[2] = static_cast<int>(x);   // total kept
+  }
+  sync();
+  const int kept = sh.bc[2];
+  const uint32_t tau = coarse ? min(min(sh.wmin[0], sh.wmin[1]), min(sh.wmin[2], sh.wmin[3])) : v;
+  const uint32_t below = (1u << lane) - 1u;
+#pragma unroll
+  for (int i = 0; i < kMaxPer; ++i) {
+    if (i < rounds && ((kb[i] >> lane) & 1u)) {
+      const int pos = static_cast<int>(rc[i * 4 + wq] + __popc(kb[i] & below));
+      keys[pos] = rk[i];
+      idxs[pos] = ri[i];
+    }
+  }
   __threadfence_block();
   sync();
-  return v;
+  return CutResult{tau, kept};
 }
 
 template <int HI, int DI, int G>
@@ -449,10 +567,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (n > cap - kKeyTile) {
               const size_t off = (static_cast<size_t>(t0 + g) * n_chunks + ui.chunk) * cap;
               __threadfence_block();
-              const uint32_t v = compact_buffer(cand_key + off, cand_idx + off, n, topk, tid, sh);
+              const CutResult cr = compact_buffer(cand_key + off, cand_idx + off, n, topk, tid, sh);
               if (tid == 0) {
-                sh.tau[g] = v;
-                sh.cnt[nxt][g] = topk;
+                sh.tau[g] = cr.tau;
+                sh.cnt[nxt][g] = cr.kept;
               }
               named_bar_sync(1, kEpiThreads);
             }
