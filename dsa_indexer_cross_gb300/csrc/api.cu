@@ -280,12 +280,18 @@ dsa_status run_indexer(const dsa_indexer_desc* d, const void* q_idx, const void*
   uint32_t* ck = reinterpret_cast<uint32_t*>(base + L.off_key);
   int32_t* ci = reinterpret_cast<int32_t*>(base + L.off_idx);
   if (d->n_kv > 0) {
-    CUtensorMap tq, tk;
-    if ((s = tmap_bf16(&tq, qr, d->head_dim, static_cast<uint64_t>(d->n_q) * d->n_heads,
-                       static_cast<uint32_t>(p.group * d->n_heads))) != DSA_OK)
-      return s;
+    // the rotated copies hold only the 64-dim blocks with rotary dims; the blocks before
+    // them are read from the inputs (same shape and box)
+    CUtensorMap tq, tk, tqi, tki;
+    const uint64_t q_rows = static_cast<uint64_t>(d->n_q) * d->n_heads;
+    const uint32_t q_box = static_cast<uint32_t>(p.group * d->n_heads);
+    if ((s = tmap_bf16(&tq, qr, d->head_dim, q_rows, q_box)) != DSA_OK) return s;
+    if ((s = tmap_bf16(&tqi, q_idx, d->head_dim, q_rows, q_box)) != DSA_OK) return s;
     if ((s = tmap_bf16(&tk, kr, d->head_dim, d->n_kv, 128)) != DSA_OK) return s;
-    e = launch_indexer(p, tq, tk, w, d->n_q, rr, gr, ck, ci, cnt, status, st);
+    if ((s = tmap_bf16(&tki, k_idx, d->head_dim, d->n_kv, 128)) != DSA_OK) return s;
+    const int q_split = rq ? rope_split_blocks(d->head_dim, d->rope_dim) : 0;
+    const int k_split = rk ? rope_split_blocks(d->head_dim, d->rope_dim) : 0;
+    e = launch_indexer(p, tq, tk, tqi, tki, q_split, k_split, w, d->n_q, rr, gr, ck, ci, cnt, status, st);
     if (e != cudaSuccess) return cuda_fail(e, "indexer kernel");
   } else {
     if ((e = cudaMemsetAsync(cnt, 0, static_cast<size_t>(d->n_q) * p.n_chunks * 4, st)) != cudaSuccess)

@@ -275,6 +275,8 @@ __device__ CutResult compact_buffer(uint32_t* keys, int32_t* idxs, int n, int K,
 template <int HI, int DI, int G>
 __global__ void __launch_bounds__(kThreads, 1)
     indexer_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                   const __grid_constant__ CUtensorMap tmap_q_in, const __grid_constant__ CUtensorMap tmap_k_in,
+                   int q_split, int k_split,
                    const float* __restrict__ w, int n_q, const int2* __restrict__ row_range,
                    const int2* __restrict__ group_range, int n_groups, int n_chunks, int chunk_len, int cap, int topk,
                    uint32_t* __restrict__ cand_key, int32_t* __restrict__ cand_idx, uint32_t* __restrict__ cand_cnt,
@@ -325,6 +327,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (elect_lane0()) {
       tma_prefetch_desc(&tmap_q);
       tma_prefetch_desc(&tmap_k);
+      tma_prefetch_desc(&tmap_q_in);
+      tma_prefetch_desc(&tmap_k_in);
       uint32_t kstage = 0, q_uses = 0;
       bool ok = true;
       for (int k = 0; k * static_cast<int>(gridDim.x) < n_units && ok; ++k) {
@@ -335,7 +339,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (q_uses > 0) ok = mbar_wait(&sh.q_empty, (q_uses - 1) & 1, &sh.abort_flag, status);
         if (!ok) break;
         mbar_arrive_expect_tx(&sh.q_full, C::Q_BYTES);
-        for (int b = 0; b < KB; ++b) tma_load_2d(sQ + b * N * 128, &tmap_q, &sh.q_full, b * 64, ui.group * N);
+        // 64-dim blocks without rotary dims come from the unrotated input
+        for (int b = 0; b < KB; ++b)
+          tma_load_2d(sQ + b * N * 128, b < q_split ? &tmap_q_in : &tmap_q, &sh.q_full, b * 64, ui.group * N);
         ++q_uses;
         for (int i = 0; i < ui.n_tiles; ++i, ++kstage) {
           const int s = kstage % STAGES;
@@ -346,7 +352,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(&sh.k_full[s], C::K_STAGE_BYTES);
           uint8_t* dst = sK + s * C::K_STAGE_BYTES;
           for (int b = 0; b < KB; ++b)
-            tma_load_2d(dst + b * kKeyTile * 128, &tmap_k, &sh.k_full[s], b * 64, ui.kbeg + i * kKeyTile);
+            tma_load_2d(dst + b * kKeyTile * 128, b < k_split ? &tmap_k_in : &tmap_k, &sh.k_full[s], b * 64,
+                        ui.kbeg + i * kKeyTile);
         }
       }
     }
@@ -591,14 +598,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int HI, int DI, int G>
-cudaError_t launch_t(const IndexerPlan& p, const CUtensorMap& tq, const CUtensorMap& tk, const float* w, int n_q,
+cudaError_t launch_t(const IndexerPlan& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tqi,
+                     const CUtensorMap& tki, int q_split, int k_split, const float* w, int n_q,
                      const int2* row_range, const int2* group_range, uint32_t* ck, int32_t* ci, uint32_t* cc,
                      uint32_t* status, cudaStream_t st) {
   using C = Cfg<HI, DI, G>;
   auto kern = indexer_kernel<HI, DI, G>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::DYN_SMEM);
   if (e != cudaSuccess) return e;
-  kern<<<p.grid, kThreads, C::DYN_SMEM, st>>>(tq, tk, w, n_q, row_range, group_range, p.n_groups, p.n_chunks,
+  kern<<<p.grid, kThreads, C::DYN_SMEM, st>>>(tq, tk, tqi, tki, q_split, k_split, w, n_q, row_range, group_range,
+                                             p.n_groups, p.n_chunks,
                                              p.chunk, p.cap, p.topk, ck, ci, cc, status);
   return cudaGetLastError();
 }
@@ -606,13 +615,15 @@ cudaError_t launch_t(const IndexerPlan& p, const CUtensorMap& tq, const CUtensor
 }  // namespace
 
 
-cudaError_t launch_indexer(const IndexerPlan& p, const CUtensorMap& tq, const CUtensorMap& tk, const float* w, int n_q,
+cudaError_t launch_indexer(const IndexerPlan& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tqi,
+                           const CUtensorMap& tki, int q_split, int k_split, const float* w, int n_q,
                            const int2* row_range, const int2* group_range, uint32_t* ck, int32_t* ci, uint32_t* cc,
                            uint32_t* status, cudaStream_t st) {
   if (p.n_groups * p.n_chunks == 0) return cudaSuccess;
 #define DSA_IDX_CASE(HI_, DI_, G_)                                                                      \
   if (p.n_heads == HI_ && p.head_dim == DI_ && p.group == G_)                                           \
-    return launch_t<HI_, DI_, G_>(p, tq, tk, w, n_q, row_range, group_range, ck, ci, cc, status, st);
+    return launch_t<HI_, DI_, G_>(p, tq, tk, tqi, tki, q_split, k_split, w, n_q, row_range, group_range, ck, ci, cc, \
+                                  status, st);
   DSA_IDX_CASE(4, 64, 64)
   DSA_IDX_CASE(8, 64, 32)
   DSA_IDX_CASE(16, 64, 16)

@@ -17,7 +17,9 @@ struct WsHeader {
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
 // ---------------------------------------------------------------------------- RoPE pre-pass
-// out[row] = in[row] with its last `rope` dims rotated at position pos[row / rows_per_pos].
+// out[row] = in[row] with its last `rope` dims rotated at position pos[row / rows_per_pos];
+// only dims from the first 64-dim block holding rotary dims on are written
+// (rope_split_blocks gives how many leading blocks are left to the unrotated input).
 cudaError_t launch_rope_rows(const void* in, void* out, const int32_t* pos, int64_t n_rows, int rows_per_pos, int d,
                              int rope, const float* cs, int n_pos, uint32_t* status, cudaStream_t st);
 
@@ -39,7 +41,12 @@ cudaError_t launch_ranges(const int32_t* ks, const int32_t* ke, int n_q, int gro
 // Scores + streaming top-k candidates.  tmap_q covers rotated q as [(n_q*H_I) x d_I] bf16,
 // tmap_k covers rotated k as [n_kv x d_I] bf16, both 128-byte swizzled, boxes {64, N} and
 // {64, 128}.
-cudaError_t launch_indexer(const IndexerPlan& p, const CUtensorMap& tmap_q, const CUtensorMap& tmap_k, const float* w,
+inline int rope_split_blocks(int d, int rope) { return rope > 0 ? (d - rope) / 64 : 0; }
+// tmap_q / tmap_k: rotated copies; tmap_q_in / tmap_k_in: the unrotated inputs, read for the
+// 64-dim blocks below q_split / k_split.
+cudaError_t launch_indexer(const IndexerPlan& p, const CUtensorMap& tmap_q, const CUtensorMap& tmap_k,
+                           const CUtensorMap& tmap_q_in, const CUtensorMap& tmap_k_in, int q_split, int k_split,
+                           const float* w,
                            int n_q, const int2* row_range, const int2* group_range, uint32_t* cand_key,
                            int32_t* cand_idx, uint32_t* cand_cnt, uint32_t* status, cudaStream_t st);
 

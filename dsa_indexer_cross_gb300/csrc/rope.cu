@@ -21,12 +21,15 @@ __device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
 }
 
 // Vector path: (d - rope) % 8 == 0 and (rope / 2) % 8 == 0.  One thread per unit of 8
-// copied elements or of 8 rotated pairs.
+// copied elements or of 8 rotated pairs.  Only dims [d0, d) are written, d0 = the start of
+// the first 64-dim block holding rotary dims: the score kernel reads the blocks before it
+// straight from the unrotated input.
 __global__ void __launch_bounds__(256) rope_rows_vec(const uint16_t* __restrict__ in, uint16_t* __restrict__ out,
                                                      const int32_t* __restrict__ pos, int64_t n_rows,
                                                      int rows_per_pos, int d, int rope, const float* __restrict__ cs,
                                                      int n_pos, uint32_t* status) {
-  const int copy_units = (d - rope) >> 3;
+  const int d0 = (d - rope) / 64 * 64;
+  const int copy_units = (d - rope - d0) >> 3;
   const int half = rope >> 1;
   const int units = copy_units + (half >> 3);
   const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -36,7 +39,7 @@ __global__ void __launch_bounds__(256) rope_rows_vec(const uint16_t* __restrict_
   const uint16_t* src = in + row * d;
   uint16_t* dst = out + row * d;
   if (u < copy_units) {
-    *reinterpret_cast<uint4*>(dst + u * 8) = __ldg(reinterpret_cast<const uint4*>(src + u * 8));
+    *reinterpret_cast<uint4*>(dst + d0 + u * 8) = __ldg(reinterpret_cast<const uint4*>(src + d0 + u * 8));
     return;
   }
   const int i0 = (u - copy_units) * 8;
@@ -74,17 +77,18 @@ __global__ void __launch_bounds__(256) rope_rows_vec(const uint16_t* __restrict_
   *reinterpret_cast<uint4*>(dst + (d - half) + i0) = make_uint4(yb[0], yb[1], yb[2], yb[3]);
 }
 
-// Scalar path for any even rope: one thread per element of the first d - r/2 dims.
+// Scalar path for any even rope: one thread per element of dims [d0, d - r/2) (d0 as above).
 __global__ void __launch_bounds__(256) rope_rows_scalar(const uint16_t* __restrict__ in, uint16_t* __restrict__ out,
                                                         const int32_t* __restrict__ pos, int64_t n_rows,
                                                         int rows_per_pos, int d, int rope,
                                                         const float* __restrict__ cs, int n_pos, uint32_t* status) {
   const int half = rope >> 1;
-  const int per_row = d - half;
+  const int d0 = (d - rope) / 64 * 64;
+  const int per_row = d - half - d0;
   const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (gid >= n_rows * per_row) return;
   const int64_t row = gid / per_row;
-  const int e = static_cast<int>(gid - row * per_row);
+  const int e = d0 + static_cast<int>(gid - row * per_row);
   const __nv_bfloat16* src = reinterpret_cast<const __nv_bfloat16*>(in) + row * d;
   __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(out) + row * d;
   if (e < d - rope) {
@@ -107,28 +111,39 @@ __global__ void __launch_bounds__(256) rope_rows_scalar(const uint16_t* __restri
   dst[d - half + i] = __float2bfloat16_rn(x2 * c + x1 * s);
 }
 
+// One thread per row; blocks of 256 rows hold whole groups (group divides 256), and each
+// group's union of non-trivial ranges is gathered with shared-memory atomics.
 __global__ void __launch_bounds__(256) ranges_kernel(const int32_t* __restrict__ ks, const int32_t* __restrict__ ke,
                                                      int n_q, int group, int n_kv, int max_len, int trivial_len,
                                                      int2* row_range, int2* group_range, uint32_t* status) {
-  const int g = blockIdx.x * blockDim.x + threadIdx.x;
-  const int n_groups = (n_q + group - 1) / group;
-  if (g >= n_groups) return;
-  int lo = 0x7FFFFFFF, hi = 0;
-  for (int t = g * group; t < min(n_q, g * group + group); ++t) {
-    const int a = ks[t], b = ke[t];
+  __shared__ int s_lo[256], s_hi[256];
+  const int per_block = 256 / group;
+  if (static_cast<int>(threadIdx.x) < per_block) {
+    s_lo[threadIdx.x] = 0x7FFFFFFF;
+    s_hi[threadIdx.x] = 0;
+  }
+  __syncthreads();
+  const int t = blockIdx.x * 256 + threadIdx.x;
+  if (t < n_q) {
+    const int a = __ldg(ks + t), b = __ldg(ke + t);
     int2 r = make_int2(0, 0);
     if (a < 0 || b < a || b > n_kv || b - a > max_len) {
       atomicOr(status, DEV_ERR_RANGE);
     } else if (b > a) {
       r = make_int2(a, b);
       if (b - a > trivial_len) {
-        lo = min(lo, a);
-        hi = max(hi, b);
+        atomicMin(&s_lo[threadIdx.x / group], a);
+        atomicMax(&s_hi[threadIdx.x / group], b);
       }
     }
     row_range[t] = r;
   }
-  group_range[g] = lo < hi ? make_int2(lo, hi) : make_int2(0, 0);
+  __syncthreads();
+  const int g = blockIdx.x * per_block + static_cast<int>(threadIdx.x);
+  if (static_cast<int>(threadIdx.x) < per_block && g * group < n_q) {
+    const int lo = s_lo[threadIdx.x], hi = s_hi[threadIdx.x];
+    group_range[g] = lo < hi ? make_int2(lo, hi) : make_int2(0, 0);
+  }
 }
 
 }  // namespace
@@ -155,10 +170,10 @@ cudaError_t launch_rope_rows(const void* in, void* out, const int32_t* pos, int6
 
 cudaError_t launch_ranges(const int32_t* ks, const int32_t* ke, int n_q, int group, int n_kv, int max_len,
                           int trivial_len, int2* row_range, int2* group_range, uint32_t* status, cudaStream_t st) {
-  const int n_groups = (n_q + group - 1) / group;
-  if (n_groups <= 0) return cudaSuccess;
-  ranges_kernel<<<(n_groups + 255) / 256, 256, 0, st>>>(ks, ke, n_q, group, n_kv, max_len, trivial_len, row_range,
-                                                        group_range, status);
+  if (n_q <= 0) return cudaSuccess;
+  if (group < 1 || 256 % group != 0) return cudaErrorInvalidValue;
+  ranges_kernel<<<(n_q + 255) / 256, 256, 0, st>>>(ks, ke, n_q, group, n_kv, max_len, trivial_len, row_range,
+                                                   group_range, status);
   return cudaGetLastError();
 }
 
