@@ -35,10 +35,8 @@
 namespace dsa {
 namespace {
 
-constexpr int kThreads = 192;
-constexpr int kEpiThreads = 128;
 constexpr int kKeyTile = 128;
-constexpr int kMaxPer = 33;  // ceil(cap / kEpiThreads) with cap = 2k + 128 <= 4224
+constexpr int kMaxCap = 4224;    // cap = 2k + 128 with k <= 2048
 constexpr int kCutBins = 2048;   // value-linear bins of a cut-back
 
 template <int HI, int DI, int G>
@@ -52,7 +50,16 @@ struct Cfg {
   static constexpr int STAGES = STAGES_FIT > 6 ? 6 : STAGES_FIT;
   static constexpr int DYN_SMEM = 1024 + Q_BYTES + STAGES * K_STAGE_BYTES;
   static constexpr uint32_t TMEM_COLS = (2 * N <= 32) ? 32 : (2 * N <= 64) ? 64 : (2 * N <= 128) ? 128 : (2 * N <= 256) ? 256 : 512;
-  static_assert(N % 64 == 0 && N >= 64 && N <= 256, "MMA N (epilogue reads 64 columns at a time)");
+  // Epilogue: one warp per TMEM lane quarter per half; with several queries per group the
+  // queries (and their TMEM columns) are split between two halves, so two warps share every
+  // lane quarter and hide each other's latencies.
+  static constexpr int HALVES = G >= 2 && N >= 128 ? 2 : 1;
+  static constexpr int EPI = 128 * HALVES;               // epilogue threads
+  static constexpr int THREADS = 64 + EPI;
+  static constexpr int GH = G / HALVES;                  // queries per half
+  static constexpr int NH = N / HALVES;                  // TMEM columns per half
+  static_assert(N % 64 == 0 && N >= 64 && N <= 256, "MMA N");
+  static_assert(NH % 64 == 0, "epilogue reads 64 columns at a time");
   static_assert(STAGES >= 2, "shared memory");
 };
 
@@ -66,8 +73,8 @@ struct Shared {
   uint32_t abort_flag;
   uint32_t hist[kCutBins];   // cut-back histogram (the radix fallback uses the first 256 bins)
   int bc[4];
-  int warp_off[4];
-  uint32_t wmin[4], wmax[4];
+  int warp_off[8];
+  uint32_t wmin[8], wmax[8];
   uint32_t tau[64];
   int cnt[2][64];        // candidates held per query; [tile parity] so a tile reads one copy and writes the other
   alignas(16) int qcnt[4][64];   // this tile's appends per (TMEM lane quarter, query)
@@ -113,7 +120,7 @@ __device__ __forceinline__ UnitInfo unit_info(int u, int n_groups, int chunk_len
 }
 
 // Cut the candidate buffer of one (row, chunk) back to a superset of its top-K, keeping the
-// survivors in their original (key index) order.  Called by the 128 epilogue threads together.
+// survivors in their original (key index) order.  Called by the NT epilogue threads together.
 //
 // The buffer only has to keep every entry that can still be in the final top-K, so the cut
 // need not be exact: one histogram of 2048 bins linear in score over the buffer's [min, max]
@@ -128,25 +135,28 @@ struct CutResult {
   uint32_t tau;
   int kept;
 };
+template <int NT>
 __device__ CutResult compact_buffer(uint32_t* keys, int32_t* idxs, int n, int K, int tid, Shared& sh) {
-  // Entry tid + 128 i is held by thread tid in slot i (coalesced loads and stores); round i
-  // is the 128 entries [128 i, 128 i + 128), so list order = (round, thread) order.
+  // Entry tid + NT i is held by thread tid in slot i (coalesced loads and stores); round i
+  // is the NT entries [NT i, NT i + NT), so list order = (round, thread) order.
+  constexpr int kMaxPer = (kMaxCap + NT - 1) / NT;
+  constexpr int NW = NT / 32;
   const int lane = tid & 31, wq = tid >> 5;
-  const int rounds = (n + kEpiThreads - 1) / kEpiThreads;   // <= kMaxPer
+  const int rounds = (n + NT - 1) / NT;   // <= kMaxPer
   uint32_t rk[kMaxPer];
   int32_t ri[kMaxPer];
 #pragma unroll
   for (int i = 0; i < kMaxPer; ++i) {
-    const int e = tid + i * kEpiThreads;
+    const int e = tid + i * NT;
     const bool in = e < n;
     rk[i] = in ? keys[e] : 0u;
     ri[i] = in ? idxs[e] : 0;
   }
-  auto sync = [] { named_bar_sync(1, kEpiThreads); };
+  auto sync = [] { named_bar_sync(1, NT); };
   auto fe = [&](auto&& f) {
 #pragma unroll
     for (int i = 0; i < kMaxPer; ++i)
-      if (tid + i * kEpiThreads < n) f(rk[i], ri[i]);
+      if (tid + i * NT < n) f(rk[i], ri[i]);
   };
   // ---- coarse cut: key range, then one histogram pass
   uint32_t mn = 0xFFFFFFFFu, mx = 0u;
@@ -160,10 +170,14 @@ __device__ CutResult compact_buffer(uint32_t* keys, int32_t* idxs, int n, int K,
     sh.wmin[wq] = mn;
     sh.wmax[wq] = mx;
   }
-  for (int i = tid; i < kCutBins; i += kEpiThreads) sh.hist[i] = 0u;
+  for (int i = tid; i < kCutBins; i += NT) sh.hist[i] = 0u;
   sync();
-  const uint32_t kmin = min(min(sh.wmin[0], sh.wmin[1]), min(sh.wmin[2], sh.wmin[3]));
-  const uint32_t kmax = max(max(sh.wmax[0], sh.wmax[1]), max(sh.wmax[2], sh.wmax[3]));
+  uint32_t kmin = sh.wmin[0], kmax = sh.wmax[0];
+#pragma unroll
+  for (int w = 1; w < NW; ++w) {
+    kmin = min(kmin, sh.wmin[w]);
+    kmax = max(kmax, sh.wmax[w]);
+  }
   const float fmin = key_float(kmin), fmax = key_float(kmax);
   const float span = fmax - fmin;
   const float scale = span > 0.f && span < 3.0e38f ? static_cast<float>(kCutBins) / span : 0.f;
@@ -173,8 +187,9 @@ __device__ CutResult compact_buffer(uint32_t* keys, int32_t* idxs, int n, int K,
   };
   fe([&](uint32_t key, int32_t) { atomicAdd(&sh.hist[bin_of(key)], 1u); });
   sync();
-  // thread tid owns the 16 bins [kCutBins - 16 tid - 16, kCutBins - 16 tid), visited from the top
-  constexpr int kPerT = kCutBins / kEpiThreads;
+  // thread tid owns the kPerT bins [kCutBins - kPerT (tid + 1), kCutBins - kPerT tid), visited
+  // from the top
+  constexpr int kPerT = kCutBins / NT;
   {
     int h[kPerT], sum = 0;
 #pragma unroll
@@ -210,29 +225,29 @@ __device__ CutResult compact_buffer(uint32_t* keys, int32_t* idxs, int n, int K,
   uint32_t v = 0, cut = 0x7FFFFFFFu;
   if (!coarse) {
     sync();
-    radix_threshold<kEpiThreads>(sync, fe, tid, K, sh.hist, sh.bc, v, cut);
+    radix_threshold<NT>(sync, fe, tid, K, sh.hist, sh.bc, v, cut);
   }
   // ---- stable compaction: per round, a ballot per warp; warp counts of every round go to
   // shared memory (sh.hist is free now), one warp turns them into exclusive offsets in
   // (round, warp) order, and every kept entry lands at its offset + its rank in the ballot
   uint32_t kb[kMaxPer];
   uint32_t kmin_kept = 0xFFFFFFFFu;
-  uint32_t* rc = sh.hist;   // [kMaxPer][4] counts, then offsets
+  uint32_t* rc = sh.hist;   // [kMaxPer][NW] counts, then offsets
 #pragma unroll
   for (int i = 0; i < kMaxPer; ++i) {
-    const bool in = tid + i * kEpiThreads < n;
+    const bool in = tid + i * NT < n;
     const bool k = in && (coarse ? bin_of(rk[i]) >= bb : topk_keep(rk[i], ri[i], v, cut));
     kb[i] = __ballot_sync(0xffffffffu, k);
     if (k) kmin_kept = min(kmin_kept, rk[i]);
-    if (lane == 0 && i < rounds) rc[i * 4 + wq] = __popc(kb[i]);
+    if (lane == 0 && i < rounds) rc[i * NW + wq] = __popc(kb[i]);
   }
   kmin_kept = __reduce_min_sync(0xffffffffu, kmin_kept);
   if (lane == 0) sh.wmin[wq] = kmin_kept;
   sync();
   if (wq == 0) {
-    // exclusive scan of rounds * 4 counts in order (at most 132), 32 lanes x 5 entries
-    constexpr int kPer = (kMaxPer * 4 + 31) / 32;
-    const int m = rounds * 4;
+    // exclusive scan of rounds * NW counts in order, 32 lanes x kPer entries
+    constexpr int kPer = (kMaxPer * NW + 31) / 32;
+    const int m = rounds * NW;
     uint32_t c[kPer], sum = 0;
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
@@ -257,12 +272,17 @@ __device__ CutResult compact_buffer(uint32_t* keys, int32_t* idxs, int n, int K,
   }
   sync();
   const int kept = sh.bc[2];
-  const uint32_t tau = coarse ? min(min(sh.wmin[0], sh.wmin[1]), min(sh.wmin[2], sh.wmin[3])) : v;
+  uint32_t tau = v;
+  if (coarse) {
+    tau = sh.wmin[0];
+#pragma unroll
+    for (int w = 1; w < NW; ++w) tau = min(tau, sh.wmin[w]);
+  }
   const uint32_t below = (1u << lane) - 1u;
 #pragma unroll
   for (int i = 0; i < kMaxPer; ++i) {
     if (i < rounds && ((kb[i] >> lane) & 1u)) {
-      const int pos = static_cast<int>(rc[i * 4 + wq] + __popc(kb[i] & below));
+      const int pos = static_cast<int>(rc[i * NW + wq] + __popc(kb[i] & below));
       keys[pos] = rk[i];
       idxs[pos] = ri[i];
     }
@@ -273,7 +293,7 @@ __device__ CutResult compact_buffer(uint32_t* keys, int32_t* idxs, int n, int K,
 }
 
 template <int HI, int DI, int G>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<HI, DI, G>::THREADS, 1)
     indexer_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                    const __grid_constant__ CUtensorMap tmap_q_in, const __grid_constant__ CUtensorMap tmap_k_in,
                    int q_split, int k_split,
@@ -306,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&sh.q_empty, 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sh.t_full[b], 1);
-      mbar_init(&sh.t_empty[b], kEpiThreads / 32);   // one arrive per epilogue warp
+      mbar_init(&sh.t_empty[b], C::EPI / 32);   // one arrive per epilogue warp
     }
     sh.abort_flag = 0;
     sh.epi_abort = 0;
@@ -395,15 +415,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------------ epilogue
-    const int tid = threadIdx.x - 64;          // 0..127
+    constexpr int EPI = C::EPI, GH = C::GH, NH = C::NH;
+    const int tid = threadIdx.x - 64;          // 0 .. EPI - 1
     const int quarter = warp & 3;              // TMEM lane quarter this warp may access
+    const int half = tid / 128;                // queries [half * GH, half * GH + GH)
+    const int g0 = half * GH;
     const int lane = threadIdx.x & 31;
     const int row = quarter * 32 + lane;       // key within the tile
     const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
     // A failed (timed-out) wait reaches every epilogue warp through the per-tile
     // barrier-reduction (fast tiles) or through sh.epi_abort, written only before the
-    // barrier-reduction and read only after it (slow tiles), so all four epilogue warps
-    // leave the loops at the same point.
+    // barrier-reduction and read only after it (slow tiles), so all epilogue warps leave the
+    // loops at the same point.
     uint32_t tile = 0;
     bool stop = false;
     for (int k = 0; k * static_cast<int>(gridDim.x) < n_units && !stop; ++k) {
@@ -412,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const UnitInfo ui = unit_info(u, n_groups, chunk_len, group_range);
       const int t0 = ui.group * G;
       // per-unit state
-      for (int i = tid; i < N; i += kEpiThreads) {
+      for (int i = tid; i < N; i += EPI) {
         const int t = t0 + i / HI;
         sh.w_s[i] = t < n_q ? __ldg(w + static_cast<size_t>(t) * HI + (i % HI)) : 0.f;
       }
@@ -422,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         sh.tau[tid] = 0u;
         sh.cnt[tile & 1][tid] = 0;
       }
-      named_bar_sync(1, kEpiThreads);
+      named_bar_sync(1, EPI);
       for (int i = 0; i < ui.n_tiles; ++i, ++tile) {
         const int buf = tile & 1;
         const int tile0 = ui.kbeg + i * kKeyTile;
@@ -439,35 +462,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         bool ok = mbar_wait(&sh.t_full[buf], (tile >> 1) & 1, &sh.abort_flag, status);
         ok = __all_sync(0xffffffffu, ok);
-        uint32_t msk[G];
-        uint32_t key[G];
-        float acc[G];
+        uint32_t msk[GH];
+        uint32_t key[GH];
+        float acc[GH];
         if (ok) {
           tc_fence_after();
-          // Head sum with NP independent partial sums per query (breaks the dependent FMA
-          // chain), TMEM read 64 columns per wait.
+          // Head sum of this half's queries with NP independent partial sums per query
+          // (breaks the dependent FMA chain), TMEM read 64 columns per wait.
           constexpr int NP = HI >= 16 ? 4 : 1;
-          float part[G][NP];
+          float part[GH][NP];
 #pragma unroll
-          for (int g = 0; g < G; ++g)
+          for (int g = 0; g < GH; ++g)
 #pragma unroll
             for (int p = 0; p < NP; ++p) part[g][p] = 0.f;
 #pragma unroll
-          for (int c0 = 0; c0 < N; c0 += 64) {
+          for (int c0 = 0; c0 < NH; c0 += 64) {
+            const int cc = half * NH + c0;   // TMEM column of this chunk
             uint32_t v[64];
-            tmem_ld32(tmem + t_lane + buf * N + c0, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-            tmem_ld32(tmem + t_lane + buf * N + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+            tmem_ld32(tmem + t_lane + buf * N + cc, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+            tmem_ld32(tmem + t_lane + buf * N + cc + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
             tmem_ld_wait();
 #pragma unroll
             for (int j = 0; j < 64; j += 4) {
-              const float4 wv = *reinterpret_cast<const float4*>(&sh.w_s[c0 + j]);
+              const float4 wv = *reinterpret_cast<const float4*>(&sh.w_s[cc + j]);
               const float r0 = fmaxf(__uint_as_float(v[j]), 0.f), r1 = fmaxf(__uint_as_float(v[j + 1]), 0.f);
               const float r2 = fmaxf(__uint_as_float(v[j + 2]), 0.f), r3 = fmaxf(__uint_as_float(v[j + 3]), 0.f);
-              const int g = (c0 + j) / HI;
+              const int gl = (c0 + j) / HI;   // query within the half
               if constexpr (NP == 4) {
-                // columns c0+j .. c0+j+3 feed partial sums 0..3 of query g: two packed FMAs
-                fma2(part[g][0], part[g][1], wv.x, wv.y, r0, r1);
-                fma2(part[g][2], part[g][3], wv.z, wv.w, r2, r3);
+                // columns cc+j .. cc+j+3 feed partial sums 0..3 of query gl: two packed FMAs
+                fma2(part[gl][0], part[gl][1], wv.x, wv.y, r0, r1);
+                fma2(part[gl][2], part[gl][3], wv.z, wv.w, r2, r3);
               } else {
                 const float wj[4] = {wv.x, wv.y, wv.z, wv.w}, rj[4] = {r0, r1, r2, r3};
 #pragma unroll
@@ -479,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
 #pragma unroll
-          for (int g = 0; g < G; ++g) {
+          for (int g = 0; g < GH; ++g) {
             if constexpr (NP == 4) acc[g] = (part[g][0] + part[g][1]) + (part[g][2] + part[g][3]);
             else acc[g] = part[g][0];
           }
@@ -491,12 +515,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int j = tile0 + row;
             const size_t rowbase = (static_cast<size_t>(t0) * n_chunks + ui.chunk) * cap;
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
+            for (int gl = 0; gl < GH; ++gl) {
+              const int g = g0 + gl;
               const int2 rr = sh.rr[g];
               const int a = max(rr.x, ui.kbeg), b = min(rr.y, ui.kend);
               if (j >= a && j < b) {
                 const size_t off = rowbase + static_cast<size_t>(g) * n_chunks * cap + (j - a);
-                st_global_u32(cand_key + off, float_key(acc[g]));
+                st_global_u32(cand_key + off, float_key(acc[gl]));
                 st_global_u32(reinterpret_cast<uint32_t*>(cand_idx) + off, static_cast<uint32_t>(j));
               }
             }
@@ -509,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (fast) {
           // one barrier-reduction per tile carries a timed-out wait to every epilogue warp
-          if (bar_red_or(1, kEpiThreads, !ok)) {
+          if (bar_red_or(1, EPI, !ok)) {
             stop = true;
             break;
           }
@@ -520,37 +545,38 @@ __global__ void __launch_bounds__(kThreads, 1)
           // four lane quarters publish their counts, then each writes after the lower ones
           const int j = tile0 + row;
 #pragma unroll
-          for (int g = 0; g < G; ++g) {
+          for (int gl = 0; gl < GH; ++gl) {
+            const int g = g0 + gl;
             const int2 rr = sh.rr[g];
-            key[g] = float_key(acc[g]);
-            msk[g] = __ballot_sync(0xffffffffu, j >= rr.x && j < rr.y && j < ui.kend && key[g] > sh.tau[g]);
+            key[gl] = float_key(acc[gl]);
+            msk[gl] = __ballot_sync(0xffffffffu, j >= rr.x && j < rr.y && j < ui.kend && key[gl] > sh.tau[g]);
           }
           if (lane == 0) {
 #pragma unroll
-            for (int g = 0; g < G; ++g) sh.qcnt[quarter][g] = __popc(msk[g]);
+            for (int gl = 0; gl < GH; ++gl) sh.qcnt[quarter][g0 + gl] = __popc(msk[gl]);
           }
         }
-        named_bar_sync(1, kEpiThreads);                       // X: per-quarter counts published
+        named_bar_sync(1, EPI);                               // X: per-quarter counts published
         const int cur = tile & 1, nxt = cur ^ 1;
         bool need = false;
         if (ok) {
           const int j = tile0 + row;
           // every query's write offset first (shared loads only), then the global stores
-          int pos[G];
+          int pos[GH];
 #pragma unroll
-          for (int g = 0; g < G; ++g) pos[g] = sh.cnt[cur][g] + __popc(msk[g] & ((1u << lane) - 1u));
+          for (int gl = 0; gl < GH; ++gl) pos[gl] = sh.cnt[cur][g0 + gl] + __popc(msk[gl] & ((1u << lane) - 1u));
           for (int q = 0; q < quarter; ++q) {
 #pragma unroll
-            for (int g = 0; g < G; ++g) pos[g] += sh.qcnt[q][g];
+            for (int gl = 0; gl < GH; ++gl) pos[gl] += sh.qcnt[q][g0 + gl];
           }
           int tot = 0;
           if (tid < G) tot = (sh.qcnt[0][tid] + sh.qcnt[1][tid]) + (sh.qcnt[2][tid] + sh.qcnt[3][tid]);
           const size_t rowbase = (static_cast<size_t>(t0) * n_chunks + ui.chunk) * cap;
 #pragma unroll
-          for (int g = 0; g < G; ++g) {
-            if (((msk[g] >> lane) & 1u) && pos[g] < cap) {
-              const size_t off = rowbase + static_cast<size_t>(g) * n_chunks * cap + pos[g];
-              st_global_u32(cand_key + off, key[g]);
+          for (int gl = 0; gl < GH; ++gl) {
+            if (((msk[gl] >> lane) & 1u) && pos[gl] < cap) {
+              const size_t off = rowbase + static_cast<size_t>(g0 + gl) * n_chunks * cap + pos[gl];
+              st_global_u32(cand_key + off, key[gl]);
               st_global_u32(reinterpret_cast<uint32_t*>(cand_idx) + off, static_cast<uint32_t>(j));
             }
           }
@@ -564,9 +590,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // cut-back or an abort).  The abort flag is written before it and read only in the
         // slow path, between it and one more barrier, so all epilogue warps branch alike.
         if (!ok && lane == 0) sh.epi_abort = 1;
-        if (bar_red_or(1, kEpiThreads, need || !ok)) {
+        if (bar_red_or(1, EPI, need || !ok)) {
           stop = sh.epi_abort != 0;
-          named_bar_sync(1, kEpiThreads);
+          named_bar_sync(1, EPI);
           if (stop) break;
 #pragma unroll 1
           for (int g = 0; g < G; ++g) {
@@ -574,12 +600,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (n > cap - kKeyTile) {
               const size_t off = (static_cast<size_t>(t0 + g) * n_chunks + ui.chunk) * cap;
               __threadfence_block();
-              const CutResult cr = compact_buffer(cand_key + off, cand_idx + off, n, topk, tid, sh);
+              const CutResult cr = compact_buffer<EPI>(cand_key + off, cand_idx + off, n, topk, tid, sh);
               if (tid == 0) {
                 sh.tau[g] = cr.tau;
                 sh.cnt[nxt][g] = cr.kept;
               }
-              named_bar_sync(1, kEpiThreads);
+              named_bar_sync(1, EPI);
             }
           }
         }
@@ -588,7 +614,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (tid < G && t0 + tid < n_q)
         cand_cnt[static_cast<size_t>(t0 + tid) * n_chunks + ui.chunk] =
             static_cast<uint32_t>(min(sh.cnt[tile & 1][tid], cap));
-      named_bar_sync(1, kEpiThreads);
+      named_bar_sync(1, EPI);
     }
   }
 
@@ -606,7 +632,7 @@ cudaError_t launch_t(const IndexerPlan& p, const CUtensorMap& tq, const CUtensor
   auto kern = indexer_kernel<HI, DI, G>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::DYN_SMEM);
   if (e != cudaSuccess) return e;
-  kern<<<p.grid, kThreads, C::DYN_SMEM, st>>>(tq, tk, tqi, tki, q_split, k_split, w, n_q, row_range, group_range,
+  kern<<<p.grid, C::THREADS, C::DYN_SMEM, st>>>(tq, tk, tqi, tki, q_split, k_split, w, n_q, row_range, group_range,
                                              p.n_groups, p.n_chunks,
                                              p.chunk, p.cap, p.topk, ck, ci, cc, status);
   return cudaGetLastError();
