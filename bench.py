@@ -159,7 +159,7 @@ def roofline_numbers(w, geo):
 
 # DRAM bytes (read + write) of one sparse_attn_kernel launch, per workload, from an ncu capture
 # of the current kernel (profiles/sparse_attn_<workload>.md); workloads not listed report None.
-ATTN_TRAFFIC_BYTES = {"prefill_4k": 112.24e6, "chunk_1m": 8.775e9}
+ATTN_TRAFFIC_BYTES = {"prefill_4k": 112.24e6, "chunk_1m": 8.671e9}
 
 
 def peaks():

@@ -62,7 +62,7 @@ constexpr int kProd = 64;                      // warps 0-1
 // Gather walk: the last kCpBlocks 64-dim blocks of every tile come through cp.async (the
 // load/store unit) while the other blocks come through four-row TMA gathers, so both copy
 // paths of the SM work on a tile at once (the TMA unit alone takes ~37 cycles per gather).
-constexpr int kCpBlocks = 2;
+constexpr int kCpBlocks = 3;
 // Warps 0-1 load, warp 2 issues S^T, warps 3-6 (and, block-dense, 8-11) run the softmax,
 // warp 7 owns TMEM and issues PV.
 constexpr int kDenseCols = 64;                 // columns of a block-dense item
