@@ -43,6 +43,9 @@ def parse():
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--mtp-steps", type=int, default=0,
+                    help="decode workloads: also time multi-step MTP drafting with IndexShare (indexer at step 0, "
+                         "later steps reuse its indices) and report it under 'mtp'")
     ap.add_argument("--only", choices=["attn", "indexer"], default=None,
                     help="run just one kernel call of the workload (for profiler captures); prints nothing")
     return ap.parse_args()
@@ -238,6 +241,55 @@ def run_reference(args):
             "e2e": {"value": value, "unit": "query_tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
     return 0
+
+
+# --------------------------------------------------------------------------- MTP drafting
+def time_mtp(D, synth, w, steps: int, dev, stream, flush, reps: int = 10):
+    """Time one draft cycle of `steps` MTP steps (dsa_mtp_indexshare_step: the indexer at step 0,
+    attention only at the later steps), one query per sequence per step.  Median over reps,
+    L2 flushed before each cycle."""
+    geos = synth.mtp_geometry(w, steps)
+    g0 = geos[0]
+    L0 = synth.layer_inputs(w.replace(layers=("full",)), g0, 0, device=dev)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    ks, k_pos = t(g0.ks), t(g0.k_pos)
+    kes, qps = [t(g.ke) for g in geos], [t(g.q_pos) for g in geos]
+    rope = D.dsa_rope_table(w.theta, w.rope_dim, max(g.max_pos for g in geos)).to(dev)
+    flags = D.DSA_IDX_ROPE_Q | (D.DSA_IDX_ROPE_K if w.rope_k else 0) | D.DSA_IDX_INDEPENDENT_ROWS
+    idesc = D.indexer_desc(w.n_q, g0.n_kv, w.n_heads_idx, w.head_dim_idx, w.rope_dim, w.topk, g0.max_len, flags)
+    adesc = D.attn_desc(w.n_q, g0.n_kv, w.n_heads, w.topk, w.softmax_scale)
+    ws = torch.empty(D.dsa_layers_workspace_size(idesc, adesc), dtype=torch.uint8, device=dev)
+    mtp_idx = torch.empty((w.n_q, w.topk), dtype=torch.int32, device=dev)
+    layer = dict(L0)
+    layer["out"] = torch.empty((w.n_q, w.n_heads, w.d_v), dtype=torch.bfloat16, device=dev)
+    layer["lse"] = torch.empty((w.n_q, w.n_heads), dtype=torch.float32, device=dev)
+
+    def cycle(ev=None):
+        for s in range(steps):
+            if ev is not None:
+                ev[s].record(stream)
+            D.dsa_mtp_indexshare_step(idesc, adesc, s, layer, ks, kes[s], qps[s], k_pos, rope, mtp_idx, ws=ws,
+                                      stream=stream)
+        if ev is not None:
+            ev[steps].record(stream)
+
+    cycle()
+    torch.cuda.synchronize()
+    per_step = [[] for _ in range(steps)]
+    for _ in range(reps):
+        flush.zero_()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+        cycle(ev)
+        torch.cuda.synchronize()
+        for s in range(steps):
+            per_step[s].append(ev[s].elapsed_time(ev[s + 1]))
+    if D.dsa_workspace_status(ws) != 0:
+        raise RuntimeError("device status set during the MTP cycles")
+    step_ms = [statistics.median(x) for x in per_step]
+    cyc = sum(step_ms)
+    return {"steps": steps, "step_ms": step_ms, "cycle_ms": cyc,
+            "draft_tokens_per_s": steps * w.n_q / (cyc / 1e3),
+            "note": "indexer at step 0 only; later steps attend with step 0's indices"}
 
 
 # --------------------------------------------------------------------------- native arm
@@ -436,6 +488,8 @@ def run_native(args):
                                                       "scores_topk": phase_ms[2], "select": phase_ms[3]}},
         "clocks": clk.summary(),
     }
+    if args.mtp_steps > 0 and w.kind == "decode":
+        line["mtp"] = time_mtp(D, synth, w, args.mtp_steps, dev, stream, flush)
     if rank == 0 and not args.no_cpu_baseline:
         hl = host_layers(layers)
         rate, n_rows, spent = time_oracle(w, geo, hl, args.cpu_seconds)

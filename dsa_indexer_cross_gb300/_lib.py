@@ -28,7 +28,7 @@ EXPORTED = ("dsa_status_string", "dsa_last_error", "dsa_donor_table", "dsa_rope_
             "dsa_indexer_topk", "dsa_sparse_attn_workspace_size", "dsa_sparse_attn", "dsa_index_cache_create",
             "dsa_index_cache_donor", "dsa_index_cache_indices", "dsa_index_cache_destroy",
             "dsa_layers_workspace_size", "indexshare_layers_forward", "dsa_workspace_status",
-            "dsa_indexer_topk_static", "dsa_profile_enable", "dsa_profile_indexer_last")
+            "dsa_indexer_topk_static", "dsa_profile_enable", "dsa_profile_indexer_last", "dsa_mtp_indexshare_step")
 
 
 class DsaError(RuntimeError):
@@ -101,6 +101,9 @@ def lib() -> C.CDLL:
         L.dsa_profile_indexer_last.argtypes = [P(C.c_float), i32]
         L.dsa_indexer_topk_static.restype = st
         L.dsa_indexer_topk_static.argtypes = [P(IndexerDesc), vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp]
+        L.dsa_mtp_indexshare_step.restype = st
+        L.dsa_mtp_indexshare_step.argtypes = [P(IndexerDesc), P(AttnDesc), i32, P(LayerIO), vp, vp, vp, vp, vp, i32,
+                                              vp, vp, sz, vp]
         _lib = L
     return _lib
 
@@ -271,6 +274,23 @@ def indexshare_layers_forward(idesc: IndexerDesc, adesc: AttnDesc, indexer_types
     _check(lib().indexshare_layers_forward(C.byref(idesc), C.byref(adesc), len(types), _u8(types), io, _ptr(ks),
                                            _ptr(ke), _ptr(q_pos), _ptr(k_pos), _ptr(rope_cs), n_pos, cache.handle,
                                            _ptr(ws), ws.numel(), _stream(stream)))
+    return ws
+
+
+def dsa_mtp_indexshare_step(idesc: IndexerDesc, adesc: AttnDesc, step: int, layer: dict, ks, ke, q_pos, k_pos,
+                            rope_cs, mtp_idx, ws=None, stream=None):
+    """One MTP draft step: step 0 runs the indexer into mtp_idx and attends with it; later
+    steps attend with mtp_idx unchanged.  layer: 'q', 'kv', 'out' (+ 'lse') and, at step 0,
+    'q_idx', 'k_idx', 'w'."""
+    L = layer
+    io = LayerIO(_ptr(L.get("q_idx")), _ptr(L.get("k_idx")), _ptr(L.get("w")), _ptr(L["q"]), _ptr(L["kv"]),
+                 _ptr(L["out"]), _ptr(L.get("lse")))
+    if ws is None:
+        ws = torch.empty(dsa_layers_workspace_size(idesc, adesc), dtype=torch.uint8, device=L["q"].device)
+    n_pos = rope_cs.shape[0] if rope_cs is not None else 0
+    _check(lib().dsa_mtp_indexshare_step(C.byref(idesc), C.byref(adesc), int(step), C.byref(io), _ptr(ks), _ptr(ke),
+                                         _ptr(q_pos), _ptr(k_pos), _ptr(rope_cs), n_pos, _ptr(mtp_idx), _ptr(ws),
+                                         ws.numel(), _stream(stream)))
     return ws
 
 

@@ -578,6 +578,38 @@ dsa_status indexshare_layers_forward(const dsa_indexer_desc* idx_desc, const dsa
   return DSA_OK;
 }
 
+dsa_status dsa_mtp_indexshare_step(const dsa_indexer_desc* idx_desc, const dsa_attn_desc* attn_desc, int32_t step,
+                                   const dsa_layer_io* io, const int32_t* ks, const int32_t* ke,
+                                   const int32_t* q_pos, const int32_t* k_pos, const float* rope_cs,
+                                   int32_t rope_n_pos, int32_t* mtp_idx, void* ws, size_t ws_bytes, void* stream) {
+  dsa_status s = check_indexer_desc(idx_desc);
+  if (s != DSA_OK) return s;
+  if ((s = check_attn_desc(attn_desc)) != DSA_OK) return s;
+  if (step < 0) return fail(DSA_ERR_ARG, "MTP step %d must be >= 0", step);
+  if (!io || !mtp_idx || !ws) return fail(DSA_ERR_ARG, "layer_io, mtp_idx and ws must be non-NULL");
+  if (idx_desc->n_q != attn_desc->n_q || idx_desc->topk != attn_desc->topk)
+    return fail(DSA_ERR_SHAPE, "indexer and attention descriptors disagree on n_q or topk");
+  if (!io->q || !io->kv || !io->out) return fail(DSA_ERR_ARG, "q, kv and out must be non-NULL");
+  if (step == 0 && (!io->q_idx || !io->k_idx || !io->w))
+    return fail(DSA_ERR_ARG, "MTP step 0 runs the indexer: q_idx, k_idx and w must be non-NULL");
+  size_t need = 0;
+  if ((s = dsa_layers_workspace_size(idx_desc, attn_desc, &need)) != DSA_OK) return s;
+  if (ws_bytes < need) return fail(DSA_ERR_WORKSPACE, "MTP workspace too small: %zu < %zu bytes", ws_bytes, need);
+  if ((s = check_device()) != DSA_OK) return s;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  size_t idx_ws = 0;
+  dsa_indexer_workspace_size(idx_desc, &idx_ws);
+  cudaError_t e;
+  if ((e = cudaMemsetAsync(ws, 0, kAlign, st)) != cudaSuccess) return cuda_fail(e, "clear status");
+  if (step == 0) {
+    s = run_indexer(idx_desc, io->q_idx, io->k_idx, io->w, q_pos, k_pos, ks, ke, rope_cs, rope_n_pos, mtp_idx,
+                    nullptr, ws, idx_ws, st, false);
+    if (s != DSA_OK) return s;
+  }
+  return run_attn(attn_desc, io->q, io->kv, mtp_idx, ks, io->out, io->lse, static_cast<uint8_t*>(ws) + idx_ws,
+                  ws_bytes - idx_ws, st, false, static_cast<uint32_t*>(ws));
+}
+
 dsa_status dsa_workspace_status(const void* ws, void* stream, uint32_t* device_bits) {
   if (!ws) return fail(DSA_ERR_ARG, "workspace is NULL");
   WsHeader h{};

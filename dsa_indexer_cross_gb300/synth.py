@@ -119,6 +119,20 @@ def geometry(w: Workload, seed: int = 1234) -> Geometry:
     raise ValueError(w.kind)
 
 
+def mtp_geometry(w: Workload, steps: int, seed: int = 1234) -> list:
+    """Batched decode with multi-step MTP drafting: sequence b holds lens[b] cached rows plus
+    room for the steps' draft rows; at step s its query sits at position lens[b] - 1 + s and
+    sees keys [off_b, off_b + lens[b] + s).  Returns one Geometry per step (same key cache)."""
+    rng = np.random.default_rng(seed)
+    lens = rng.integers(w.len_lo, w.len_hi + 1, size=w.n_seqs).astype(np.int64)
+    span = lens + steps - 1
+    off = np.concatenate([[0], np.cumsum(span)[:-1]])
+    n_kv = int(span.sum())
+    k_pos = (np.arange(n_kv) - np.repeat(off, span)).astype(np.int32)
+    return [Geometry(n_kv, (lens - 1 + s).astype(np.int32), k_pos, off.astype(np.int32),
+                     (off + lens + s).astype(np.int32)) for s in range(steps)]
+
+
 def _gen(device, seed: int) -> torch.Generator:
     g = torch.Generator(device=device)
     g.manual_seed(seed)

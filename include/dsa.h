@@ -246,6 +246,30 @@ dsa_status indexshare_layers_forward(const dsa_indexer_desc* idx_desc, const dsa
                                      const int32_t* k_pos, const float* rope_cs, int32_t rope_n_pos,
                                      dsa_index_cache* cache, void* ws, size_t ws_bytes, void* stream);
 
+/* ------------------------------------------------------------------ MTP drafting ---- */
+
+/* One step of multi-step MTP drafting with IndexShare ([EX] "MTP path: IndexShare +
+ * KVShare": for multi-step MTP the indexer runs at the first step and the following steps
+ * reuse its top-k indices; "Public config evidence": index_share_for_mtp_iteration).
+ *   step == 0: dsa_indexer_topk of this step's query rows into mtp_idx, then
+ *              dsa_sparse_attn with mtp_idx;
+ *   step  > 0: no indexer work; dsa_sparse_attn of this step's q over its kv with the
+ *              indices left in mtp_idx by step 0, read unchanged.
+ * Row t of every step is the draft token of the same sequence t.  The indices are offsets
+ * from ks[t], so every step must pass the same ks; a later step's range [ks_t, ke_t) may be
+ * longer than step 0's (the drafts' own latent rows appended), and the step-0 selection,
+ * all inside step 0's range, stays causal for it.  io: q_idx, k_idx and w are read at step 0
+ * only (NULL allowed after); q, kv, out (and lse, optional) at every step.  mtp_idx:
+ * caller-owned device buffer of n_q * topk int32, written at step 0 and only read after.
+ * idx_desc is used at step 0 only; attn_desc describes this step (its n_kv may grow with the
+ * step).  Workspace: dsa_layers_workspace_size(idx_desc, attn_desc) bytes.  Errors: those
+ * of the two calls, DSA_ERR_ARG (step < 0, NULL io / mtp_idx / ws, missing tensors),
+ * DSA_ERR_SHAPE (the descriptors disagree on n_q or topk). */
+dsa_status dsa_mtp_indexshare_step(const dsa_indexer_desc* idx_desc, const dsa_attn_desc* attn_desc, int32_t step,
+                                   const dsa_layer_io* io, const int32_t* ks, const int32_t* ke,
+                                   const int32_t* q_pos, const int32_t* k_pos, const float* rope_cs,
+                                   int32_t rope_n_pos, int32_t* mtp_idx, void* ws, size_t ws_bytes, void* stream);
+
 /* ------------------------------------------------------------------ device status ---- */
 
 /* Synchronise `stream`, read the device status word of workspace `ws`, and map it:

@@ -280,3 +280,26 @@ def layers_forward(indexer_types: Sequence[str], layers: Sequence[dict],
         o_l.append(o)
         lse_l.append(lse)
     return idx_l, o_l, lse_l
+
+
+def mtp_indexshare_steps(steps: Sequence[dict], q_pos_steps: Sequence, k_pos, ks, ke_steps: Sequence,
+                         rope_dim: int, theta: float, topk: int, scale: float, d_v: int = 512,
+                         rope_q: bool = True, rope_k: bool = True, rows: Sequence[int] | None = None):
+    """Multi-step MTP drafting with IndexShare.
+
+    "GLM-5.2 IndexShare" (explainer), section "MTP path: IndexShare + KVShare": for multi-step
+    MTP the indexer is placed at the first step and the following steps reuse its top-k
+    indices.  steps[s] holds 'q' and 'kv' (every step) and, at step 0, 'q_idx', 'k_idx', 'w';
+    q_pos_steps[s] / ke_steps[s] are the query positions and key-range ends of step s (the
+    range start ks is common, the indices being offsets from it).  Returns (idx of step 0,
+    o per step, lse per step).
+    """
+    s0 = steps[0]
+    idx = indexer_topk(s0["q_idx"], s0["k_idx"], s0["w"], q_pos_steps[0], k_pos, ks, ke_steps[0],
+                       rope_dim, theta, topk, rope_q, rope_k, rows=rows)
+    o_l, lse_l = [], []
+    for st in steps:
+        o, lse = sparse_attn(st["q"], st["kv"], idx, ks, scale, d_v, rows=rows)
+        o_l.append(o)
+        lse_l.append(lse)
+    return idx, o_l, lse_l

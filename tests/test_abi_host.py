@@ -176,3 +176,26 @@ def test_profiling_switch_and_argument_errors():
     buf = (C.c_float * 4)()
     assert L.dsa_profile_indexer_last(buf, 0) == 1
     assert L.dsa_profile_enable(0) == 0
+
+
+def test_mtp_step_argument_errors_before_launch():
+    # step < 0, NULL mtp_idx, missing step-0 indexer inputs and disagreeing descriptors are
+    # all rejected on the host (fake non-NULL pointers are never dereferenced)
+    L = _lib.lib()
+    idesc = D.indexer_desc(8, 64, 4, 64, 16, 32, 64, D.DSA_IDX_ROPE_Q | D.DSA_IDX_ROPE_K)
+    adesc = D.attn_desc(8, 64, 4, 32, 1 / 24.0)
+    fake = 0x100000
+    io = _lib.LayerIO(fake, fake, fake, fake, fake, fake, None)
+    args = (None, None, None, None, None, 0)
+    assert L.dsa_mtp_indexshare_step(C.byref(idesc), C.byref(adesc), -1, C.byref(io), *args, fake, fake, 1 << 30,
+                                     None) == 1
+    assert "step" in L.dsa_last_error().decode()
+    assert L.dsa_mtp_indexshare_step(C.byref(idesc), C.byref(adesc), 0, C.byref(io), *args, None, fake, 1 << 30,
+                                     None) == 1
+    io0 = _lib.LayerIO(None, fake, fake, fake, fake, fake, None)
+    assert L.dsa_mtp_indexshare_step(C.byref(idesc), C.byref(adesc), 0, C.byref(io0), *args, fake, fake, 1 << 30,
+                                     None) == 1
+    assert "q_idx" in L.dsa_last_error().decode()
+    adesc_bad = D.attn_desc(8, 64, 4, 16, 1 / 24.0)
+    assert L.dsa_mtp_indexshare_step(C.byref(idesc), C.byref(adesc_bad), 1, C.byref(io), *args, fake, fake, 1 << 30,
+                                     None) == 2

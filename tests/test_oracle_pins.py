@@ -282,3 +282,39 @@ def test_layers_forward_reuses_donor_indices_and_runs_own_attention():
     # each layer's output is its own attention over the shared index set
     o1, _ = O.sparse_attn(layers[1]["q"], layers[1]["kv"], idx[0], np.zeros(T, int), 1 / 24.0)
     np.testing.assert_array_equal(o[1], o1)
+
+
+# ---------------------------------------------------------------------------- MTP IndexShare
+
+def test_mtp_steps_attend_with_the_first_step_selection_brute_force():
+    # "MTP path: IndexShare + KVShare": the indexer runs at the first MTP step and the later
+    # steps reuse its top-k.  Brute force: dense step-0 scores, full argsort mask, and dense
+    # masked attention of every step's q over that same mask (the later steps' longer ranges
+    # must not enter).
+    rng = np.random.default_rng(21)
+    lens, steps, H_I, d, r, k, H = np.array([6, 11, 17, 23]), 3, 2, 16, 8, 5, 2
+    span = lens + steps - 1
+    off = np.concatenate([[0], np.cumsum(span)[:-1]])
+    n_kv = int(span.sum())
+    k_pos = np.arange(n_kv) - np.repeat(off, span)
+    ks = off
+    ke_steps = [off + lens + s for s in range(steps)]
+    q_pos_steps = [lens - 1 + s for s in range(steps)]
+    B = lens.size
+    kv = rng.standard_normal((n_kv, 24))
+    st = [{"q": rng.standard_normal((B, H, 24)), "kv": kv} for _ in range(steps)]
+    st[0].update(q_idx=O.round_to_bf16(rng.standard_normal((B, H_I, d)) / 4),
+                 k_idx=O.round_to_bf16(rng.standard_normal((n_kv, d)) / 4), w=rng.standard_normal((B, H_I)))
+    idx, o, lse = O.mtp_indexshare_steps(st, q_pos_steps, k_pos, ks, ke_steps, r, 1e4, k, 0.3, d_v=16)
+    q_rot = O.apply_index_rope(st[0]["q_idx"], q_pos_steps[0][:, None], r, 1e4)
+    k_rot = O.apply_index_rope(st[0]["k_idx"], k_pos, r, 1e4)
+    S = brute.dense_scores(q_rot, k_rot, st[0]["w"], ks, ke_steps[0])
+    mask = brute.topk_mask(S, ks, ke_steps[0], k)
+    for b in range(B):
+        assert set((idx[b][idx[b] >= 0] + ks[b]).tolist()) == set(np.nonzero(mask[b])[0].tolist())
+        assert idx[b].max() < lens[b]                      # inside step 0's causal range
+    for s in range(steps):
+        ob, lseb = brute.dense_masked_attn(st[s]["q"], kv, mask, 0.3, d_v=16)
+        np.testing.assert_allclose(o[s], ob, rtol=1e-11, atol=1e-12)
+        np.testing.assert_allclose(lse[s], lseb, rtol=1e-12)
+    assert not np.allclose(o[1], o[0])                     # each step runs its own attention
