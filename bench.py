@@ -46,6 +46,9 @@ def parse():
     ap.add_argument("--mtp-steps", type=int, default=0,
                     help="decode workloads: also time multi-step MTP drafting with IndexShare (indexer at step 0, "
                          "later steps reuse its indices) and report it under 'mtp'")
+    ap.add_argument("--paged", action="store_true",
+                    help="decode workloads: also time the paged-cache indexer and attention (128-row pages, "
+                         "shuffled) against the contiguous calls on the same data, under 'paged'")
     ap.add_argument("--only", choices=["attn", "indexer"], default=None,
                     help="run just one kernel call of the workload (for profiler captures); prints nothing")
     return ap.parse_args()
@@ -292,6 +295,70 @@ def time_mtp(D, synth, w, steps: int, dev, stream, flush, reps: int = 10):
             "note": "indexer at step 0 only; later steps attend with step 0's indices"}
 
 
+# --------------------------------------------------------------------------- paged caches
+def time_paged(D, synth, w, geo, L0, idx_full, attn_ms_contig, idx_ms_contig, dev, stream, flush, reps: int = 20,
+               seed: int = 3):
+    """The same decode layer with its index-key and latent caches in shuffled 128-row pages behind a
+    block table: median time of dsa_indexer_topk_paged and dsa_sparse_attn_paged (L2 flushed
+    before each call), beside the contiguous calls' times."""
+    P = D.DSA_PAGE_ROWS
+    lens = (geo.ke - geo.ks).astype(np.int64)
+    n_pp = (lens + P - 1) // P
+    n_pages = int(n_pp.sum())
+    perm = np.random.default_rng(seed).permutation(n_pages)
+    bt = np.full((lens.size, int(n_pp.max())), -1, dtype=np.int32)
+    phys = np.zeros(int(lens.sum()), dtype=np.int64)
+    k = 0
+    for t, L in enumerate(lens):
+        bt[t, :n_pp[t]] = perm[k:k + n_pp[t]]
+        k += n_pp[t]
+        j = np.arange(L)
+        phys[geo.ks[t] + j] = bt[t, j // P].astype(np.int64) * P + j % P
+    phys_t = torch.from_numpy(phys).to(dev)
+    k_cache = torch.zeros((n_pages * P, w.head_dim_idx), dtype=torch.bfloat16, device=dev)
+    kv_cache = torch.zeros((n_pages * P, w.d_qk), dtype=torch.bfloat16, device=dev)
+    k_cache[phys_t] = L0["k_idx"]
+    kv_cache[phys_t] = L0["kv"]
+    bt_d = torch.from_numpy(bt).to(dev)
+    sl_d = torch.from_numpy(lens.astype(np.int32)).to(dev)
+    pages = D.paged_cache(bt_d, sl_d, n_pages)
+    rope = D.dsa_rope_table(w.theta, w.rope_dim, geo.max_pos).to(dev)
+    q_pos = torch.from_numpy(geo.q_pos).to(dev)
+    flags = D.DSA_IDX_ROPE_Q | D.DSA_IDX_INDEPENDENT_ROWS
+    idesc = D.indexer_desc(w.n_q, n_pages * P, w.n_heads_idx, w.head_dim_idx, w.rope_dim, w.topk, geo.max_len, flags)
+    adesc = D.attn_desc(w.n_q, n_pages * P, w.n_heads, w.topk, w.softmax_scale)
+    idx = torch.empty((w.n_q, w.topk), dtype=torch.int32, device=dev)
+    out = torch.empty((w.n_q, w.n_heads, w.d_v), dtype=torch.bfloat16, device=dev)
+    iws = torch.empty(D.dsa_indexer_workspace_size(idesc), dtype=torch.uint8, device=dev)
+    aws = torch.empty(D.dsa_sparse_attn_workspace_size(adesc), dtype=torch.uint8, device=dev)
+
+    def timed(fn):
+        fn()
+        ms = []
+        for _ in range(reps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ms.append(a.elapsed_time(b))
+        return statistics.median(ms)
+
+    i_ms = timed(lambda: D.dsa_indexer_topk_paged(idesc, L0["q_idx"], k_cache, L0["w"], q_pos, pages, rope, idx, None,
+                                                  ws=iws, stream=stream))
+    if D.dsa_workspace_status(iws) != 0:
+        raise RuntimeError("device status set by the paged indexer")
+    same = bool(torch.equal(idx, idx_full))
+    a_ms = timed(lambda: D.dsa_sparse_attn_paged(adesc, L0["q"], kv_cache, idx, pages, out, None, ws=aws,
+                                                 stream=stream))
+    if D.dsa_workspace_status(aws) != 0:
+        raise RuntimeError("device status set by the paged attention")
+    return {"page_rows": P, "n_pages": n_pages, "indexer_ms": i_ms, "attn_ms": a_ms,
+            "contiguous_indexer_ms": idx_ms_contig, "contiguous_attn_ms": attn_ms_contig,
+            "indices_equal_contiguous": same}
+
+
 # --------------------------------------------------------------------------- native arm
 def run_native(args):
     ws_n, rank, local = dist_env()
@@ -488,6 +555,8 @@ def run_native(args):
                                                       "scores_topk": phase_ms[2], "select": phase_ms[3]}},
         "clocks": clk.summary(),
     }
+    if args.paged and w.kind == "decode":
+        line["paged"] = time_paged(D, synth, w, geo, layers[0], idx_full, attn_ms, idx_ms, dev, stream, flush)
     if args.mtp_steps > 0 and w.kind == "decode":
         line["mtp"] = time_mtp(D, synth, w, args.mtp_steps, dev, stream, flush)
     if rank == 0 and not args.no_cpu_baseline:

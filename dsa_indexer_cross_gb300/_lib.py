@@ -28,7 +28,8 @@ EXPORTED = ("dsa_status_string", "dsa_last_error", "dsa_donor_table", "dsa_rope_
             "dsa_indexer_topk", "dsa_sparse_attn_workspace_size", "dsa_sparse_attn", "dsa_index_cache_create",
             "dsa_index_cache_donor", "dsa_index_cache_indices", "dsa_index_cache_destroy",
             "dsa_layers_workspace_size", "indexshare_layers_forward", "dsa_workspace_status",
-            "dsa_indexer_topk_static", "dsa_profile_enable", "dsa_profile_indexer_last", "dsa_mtp_indexshare_step")
+            "dsa_indexer_topk_static", "dsa_profile_enable", "dsa_profile_indexer_last", "dsa_mtp_indexshare_step",
+            "dsa_indexer_topk_paged", "dsa_sparse_attn_paged")
 
 
 class DsaError(RuntimeError):
@@ -101,6 +102,10 @@ def lib() -> C.CDLL:
         L.dsa_profile_indexer_last.argtypes = [P(C.c_float), i32]
         L.dsa_indexer_topk_static.restype = st
         L.dsa_indexer_topk_static.argtypes = [P(IndexerDesc), vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp]
+        L.dsa_indexer_topk_paged.restype = st
+        L.dsa_indexer_topk_paged.argtypes = [P(IndexerDesc), vp, vp, vp, vp, P(PagedCache), vp, i32, vp, vp, vp, sz, vp]
+        L.dsa_sparse_attn_paged.restype = st
+        L.dsa_sparse_attn_paged.argtypes = [P(AttnDesc), vp, vp, vp, P(PagedCache), vp, vp, vp, sz, vp]
         L.dsa_mtp_indexshare_step.restype = st
         L.dsa_mtp_indexshare_step.argtypes = [P(IndexerDesc), P(AttnDesc), i32, P(LayerIO), vp, vp, vp, vp, vp, i32,
                                               vp, vp, sz, vp]
@@ -274,6 +279,40 @@ def indexshare_layers_forward(idesc: IndexerDesc, adesc: AttnDesc, indexer_types
     _check(lib().indexshare_layers_forward(C.byref(idesc), C.byref(adesc), len(types), _u8(types), io, _ptr(ks),
                                            _ptr(ke), _ptr(q_pos), _ptr(k_pos), _ptr(rope_cs), n_pos, cache.handle,
                                            _ptr(ws), ws.numel(), _stream(stream)))
+    return ws
+
+
+DSA_PAGE_ROWS = 128
+
+
+class PagedCache(C.Structure):
+    """dsa_paged_cache: row t's logical key j sits at cache row
+    block_table[t, j // page_rows] * page_rows + j % page_rows, valid for j < seq_len[t]."""
+    _fields_ = [("block_table", C.c_void_p), ("seq_len", C.c_void_p), ("max_pages", C.c_int32),
+                ("n_pages", C.c_int32), ("page_rows", C.c_int32)]
+
+
+def paged_cache(block_table: torch.Tensor, seq_len: torch.Tensor, n_pages: int) -> PagedCache:
+    """block_table: int32 [n_q, max_pages] device tensor; seq_len: int32 [n_q] (kept alive by the caller)."""
+    return PagedCache(_ptr(block_table), _ptr(seq_len), block_table.shape[1], n_pages, DSA_PAGE_ROWS)
+
+
+def dsa_indexer_topk_paged(desc: IndexerDesc, q_idx, k_cache, w, q_pos, pages: PagedCache, rope_cs, idx_out,
+                           score_out=None, ws=None, stream=None):
+    if ws is None:
+        ws = torch.empty(dsa_indexer_workspace_size(desc), dtype=torch.uint8, device=q_idx.device)
+    n_pos = rope_cs.shape[0] if rope_cs is not None else 0
+    _check(lib().dsa_indexer_topk_paged(C.byref(desc), _ptr(q_idx), _ptr(k_cache), _ptr(w), _ptr(q_pos),
+                                        C.byref(pages), _ptr(rope_cs), n_pos, _ptr(idx_out), _ptr(score_out),
+                                        _ptr(ws), ws.numel(), _stream(stream)))
+    return ws
+
+
+def dsa_sparse_attn_paged(desc: AttnDesc, q, kv_cache, idx, pages: PagedCache, out, lse=None, ws=None, stream=None):
+    if ws is None:
+        ws = torch.empty(dsa_sparse_attn_workspace_size(desc), dtype=torch.uint8, device=q.device)
+    _check(lib().dsa_sparse_attn_paged(C.byref(desc), _ptr(q), _ptr(kv_cache), _ptr(idx), C.byref(pages), _ptr(out),
+                                       _ptr(lse), _ptr(ws), ws.numel(), _stream(stream)))
     return ws
 
 

@@ -4,6 +4,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <algorithm>
 #include <cstring>
 #include <atomic>
 #include <mutex>
@@ -226,16 +227,18 @@ IndexerLayout indexer_layout(const dsa_indexer_desc* d, int sms) {
   return L;
 }
 
+// pg (paged key cache): ks is NULL (every range starts at logical key 0), ke = seq_len, and
+// k_idx is the page array itself.
 dsa_status run_indexer(const dsa_indexer_desc* d, const void* q_idx, const void* k_idx, const float* w,
                        const int32_t* q_pos, const int32_t* k_pos, const int32_t* ks, const int32_t* ke,
                        const float* rope_cs, int32_t rope_n_pos, int32_t* idx_out, float* score_out, void* ws,
-                       size_t ws_bytes, cudaStream_t st, bool clear_status) {
+                       size_t ws_bytes, cudaStream_t st, bool clear_status, const PagedRows* pg = nullptr) {
   dsa_status s = check_indexer_desc(d);
   if (s != DSA_OK) return s;
   if (d->n_q == 0) return DSA_OK;
   const bool rq = (d->flags & DSA_IDX_ROPE_Q) && d->rope_dim > 0;
   const bool rk = (d->flags & DSA_IDX_ROPE_K) && d->rope_dim > 0;
-  if (!q_idx || !k_idx || !w || !ks || !ke || !idx_out || !ws)
+  if (!q_idx || !k_idx || !w || (!ks && !pg) || !ke || !idx_out || !ws)
     return fail(DSA_ERR_ARG, "q_idx, k_idx, w, ks, ke, idx_out and ws must be non-NULL");
   if ((rq && !q_pos) || (rk && !k_pos) || ((rq || rk) && (!rope_cs || rope_n_pos < 1)))
     return fail(DSA_ERR_ARG, "RoPE requested but q_pos/k_pos/rope_cs/rope_n_pos missing");
@@ -273,7 +276,11 @@ dsa_status run_indexer(const dsa_indexer_desc* d, const void* q_idx, const void*
   if (pe) (void)cudaEventRecord(pe->ev[1], st);
   // rows whose whole range fits in k keep every key; without requested scores they need no scoring
   const int trivial_len = score_out ? 0 : d->topk;
-  e = launch_ranges(ks, ke, d->n_q, p.group, d->n_kv, d->max_len, trivial_len, rr, gr, status, st);
+  // paged: logical keys run up to max_pages pages, whatever the physical page count
+  const int range_limit = pg ? static_cast<int>(std::min<long long>(static_cast<long long>(pg->max_pages) * kPageRows,
+                                                                   0x7FFFFFFF))
+                             : d->n_kv;
+  e = launch_ranges(ks, ke, d->n_q, p.group, range_limit, d->max_len, trivial_len, rr, gr, status, st);
   if (e != cudaSuccess) return cuda_fail(e, "key ranges");
   if (pe) (void)cudaEventRecord(pe->ev[2], st);
   uint32_t* cnt = reinterpret_cast<uint32_t*>(base + L.off_cnt);
@@ -291,7 +298,8 @@ dsa_status run_indexer(const dsa_indexer_desc* d, const void* q_idx, const void*
     if ((s = tmap_bf16(&tki, k_idx, d->head_dim, d->n_kv, 128)) != DSA_OK) return s;
     const int q_split = rq ? rope_split_blocks(d->head_dim, d->rope_dim) : 0;
     const int k_split = rk ? rope_split_blocks(d->head_dim, d->rope_dim) : 0;
-    e = launch_indexer(p, tq, tk, tqi, tki, q_split, k_split, w, d->n_q, rr, gr, ck, ci, cnt, status, st);
+    e = launch_indexer(p, tq, tk, tqi, tki, q_split, k_split, pg ? *pg : PagedRows{}, w, d->n_q, rr, gr, ck, ci, cnt,
+                       status, st);
     if (e != cudaSuccess) return cuda_fail(e, "indexer kernel");
   } else {
     if ((e = cudaMemsetAsync(cnt, 0, static_cast<size_t>(d->n_q) * p.n_chunks * 4, st)) != cudaSuccess)
@@ -326,13 +334,15 @@ size_t attn_ws_bytes(const dsa_attn_desc* d) {
 }
 
 // status: device status header (first two words: bits, bad-index count); row_nt: n_q int32.
+// pg (paged latent cache): ks is unused, offsets map through the block table.
 dsa_status run_attn(const dsa_attn_desc* d, const void* q, const void* kv, const int32_t* idx, const int32_t* ks,
                     void* out, float* lse, void* ws, size_t ws_bytes, cudaStream_t st, bool clear_status,
-                    uint32_t* status_override = nullptr) {
+                    uint32_t* status_override = nullptr, const PagedRows* pg = nullptr) {
   dsa_status s = check_attn_desc(d);
   if (s != DSA_OK) return s;
   if (d->n_q == 0) return DSA_OK;
-  if (!q || !kv || !idx || !ks || !out || !ws) return fail(DSA_ERR_ARG, "q, kv, idx, ks, out and ws must be non-NULL");
+  if (!q || !kv || !idx || (!ks && !pg) || !out || !ws)
+    return fail(DSA_ERR_ARG, "q, kv, idx, ks, out and ws must be non-NULL");
   if (!aligned16(q) || !aligned16(kv) || !aligned16(out)) return fail(DSA_ERR_ARG, "q, kv and out must be 16-byte aligned");
   if (reinterpret_cast<uintptr_t>(ws) % kAlign) return fail(DSA_ERR_ARG, "workspace must be 256-byte aligned");
   if ((s = check_device()) != DSA_OK) return s;
@@ -347,7 +357,7 @@ dsa_status run_attn(const dsa_attn_desc* d, const void* q, const void* kv, const
   CUtensorMap tkv, tq;
   std::memset(&tkv, 0, sizeof(tkv));
   std::memset(&tq, 0, sizeof(tq));
-  if (sparse_attn_dense_heads(d->n_heads, d->n_kv, d->topk)) {
+  if (!pg && sparse_attn_dense_heads(d->n_heads, d->n_kv, d->topk)) {
     if (d->n_kv > 0) s = tmap_kv_tiles(&tkv, kv, d->n_kv);   // an empty cache gives every block an empty range
   } else if (d->n_kv > 0) {
     s = tmap_bf16(&tkv, kv, 576, d->n_kv, 1);
@@ -358,9 +368,10 @@ dsa_status run_attn(const dsa_attn_desc* d, const void* q, const void* kv, const
   }
   if (s != DSA_OK) return s;
   if ((s = tmap_bf16(&tq, q, 576, static_cast<uint64_t>(d->n_q) * d->n_heads,
-                     static_cast<uint32_t>(sparse_attn_q_box_rows(d->n_heads, d->n_kv, d->topk)))) != DSA_OK)
+                     static_cast<uint32_t>(sparse_attn_q_box_rows(d->n_heads, d->n_kv, d->topk, pg != nullptr)))) != DSA_OK)
     return s;
-  e = launch_sparse_attn(tkv, tq, d->n_q, d->n_kv, d->n_heads, d->topk, d->softmax_scale, kv, idx, ks, out, lse, status,
+  e = launch_sparse_attn(tkv, tq, d->n_q, d->n_kv, d->n_heads, d->topk, d->softmax_scale, kv, idx, ks,
+                         pg ? *pg : PagedRows{}, out, lse, status,
                          base + kAlign, st);
   if (e != cudaSuccess) return cuda_fail(e, "sparse attention kernel");
   return DSA_OK;
@@ -608,6 +619,52 @@ dsa_status dsa_mtp_indexshare_step(const dsa_indexer_desc* idx_desc, const dsa_a
   }
   return run_attn(attn_desc, io->q, io->kv, mtp_idx, ks, io->out, io->lse, static_cast<uint8_t*>(ws) + idx_ws,
                   ws_bytes - idx_ws, st, false, static_cast<uint32_t*>(ws));
+}
+
+namespace {
+dsa_status check_pages(const dsa_paged_cache* pc, int32_t n_kv, PagedRows* pg) {
+  if (!pc || !pc->block_table || !pc->seq_len) return fail(DSA_ERR_ARG, "paged cache: block_table and seq_len must be non-NULL");
+  if (pc->page_rows != kPageRows)
+    return fail(DSA_ERR_UNSUPPORTED, "page_rows %d: this build supports %d-row pages", pc->page_rows, kPageRows);
+  if (pc->max_pages < 1 || pc->n_pages < 1) return fail(DSA_ERR_ARG, "max_pages and n_pages must be >= 1");
+  if (static_cast<long long>(pc->n_pages) * kPageRows != n_kv)
+    return fail(DSA_ERR_SHAPE, "n_kv %d must equal n_pages * page_rows = %lld", n_kv,
+                static_cast<long long>(pc->n_pages) * kPageRows);
+  pg->block_table = pc->block_table;
+  pg->seq_len = pc->seq_len;
+  pg->max_pages = pc->max_pages;
+  pg->n_pages = pc->n_pages;
+  return DSA_OK;
+}
+}  // namespace
+
+dsa_status dsa_indexer_topk_paged(const dsa_indexer_desc* desc, const void* q_idx, const void* k_cache, const float* w,
+                                  const int32_t* q_pos, const dsa_paged_cache* pages, const float* rope_cs,
+                                  int32_t rope_n_pos, int32_t* idx_out, float* score_out, void* ws, size_t ws_bytes,
+                                  void* stream) {
+  dsa_status s = check_indexer_desc(desc);
+  if (s != DSA_OK) return s;
+  PagedRows pg;
+  if ((s = check_pages(pages, desc->n_kv, &pg)) != DSA_OK) return s;
+  if (!(desc->flags & DSA_IDX_INDEPENDENT_ROWS) || (desc->flags & DSA_IDX_ROPE_K))
+    return fail(DSA_ERR_ARG, "a paged key cache needs DSA_IDX_INDEPENDENT_ROWS and a pre-rotated cache (no DSA_IDX_ROPE_K)");
+  if (desc->n_heads != 64)
+    return fail(DSA_ERR_UNSUPPORTED, "paged key cache: %d index heads (one row per key stream needs 64)", desc->n_heads);
+  if (static_cast<long long>(desc->max_len) > static_cast<long long>(pages->max_pages) * kPageRows)
+    return fail(DSA_ERR_ARG, "max_len %d exceeds max_pages * page_rows", desc->max_len);
+  return run_indexer(desc, q_idx, k_cache, w, q_pos, nullptr, nullptr, pages->seq_len, rope_cs, rope_n_pos, idx_out,
+                     score_out, ws, ws_bytes, static_cast<cudaStream_t>(stream), true, &pg);
+}
+
+dsa_status dsa_sparse_attn_paged(const dsa_attn_desc* desc, const void* q, const void* kv_cache, const int32_t* idx,
+                                 const dsa_paged_cache* pages, void* out, float* lse, void* ws, size_t ws_bytes,
+                                 void* stream) {
+  dsa_status s = check_attn_desc(desc);
+  if (s != DSA_OK) return s;
+  PagedRows pg;
+  if ((s = check_pages(pages, desc->n_kv, &pg)) != DSA_OK) return s;
+  return run_attn(desc, q, kv_cache, idx, nullptr, out, lse, ws, ws_bytes, static_cast<cudaStream_t>(stream), true,
+                  nullptr, &pg);
 }
 
 dsa_status dsa_workspace_status(const void* ws, void* stream, uint32_t* device_bits) {

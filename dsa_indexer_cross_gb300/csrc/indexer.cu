@@ -296,7 +296,7 @@ template <int HI, int DI, int G>
 __global__ void __launch_bounds__(Cfg<HI, DI, G>::THREADS, 1)
     indexer_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                    const __grid_constant__ CUtensorMap tmap_q_in, const __grid_constant__ CUtensorMap tmap_k_in,
-                   int q_split, int k_split,
+                   int q_split, int k_split, const PagedRows pg,
                    const float* __restrict__ w, int n_q, const int2* __restrict__ row_range,
                    const int2* __restrict__ group_range, int n_groups, int n_chunks, int chunk_len, int cap, int topk,
                    uint32_t* __restrict__ cand_key, int32_t* __restrict__ cand_idx, uint32_t* __restrict__ cand_cnt,
@@ -371,9 +371,22 @@ __global__ void __launch_bounds__(Cfg<HI, DI, G>::THREADS, 1)
           }
           mbar_arrive_expect_tx(&sh.k_full[s], C::K_STAGE_BYTES);
           uint8_t* dst = sK + s * C::K_STAGE_BYTES;
+          // cache row of the tile's first key: contiguous, or its page (one 128-key tile per
+          // page; a group is one row in paged mode).  A page outside the cache is flagged and
+          // row 0 read instead (the tile's scores are then meaningless, the status says so).
+          int krow = ui.kbeg + i * kKeyTile;
+          if (pg.block_table) {
+            const int lp = krow >> kPageShift;
+            const int page = lp < pg.max_pages ? __ldg(pg.block_table + static_cast<size_t>(ui.group) * pg.max_pages + lp) : -1;
+            if (page < 0 || page >= pg.n_pages) {
+              atomicOr(status, DEV_ERR_BAD_INDEX);
+              krow = 0;
+            } else {
+              krow = page << kPageShift;
+            }
+          }
           for (int b = 0; b < KB; ++b)
-            tma_load_2d(dst + b * kKeyTile * 128, b < k_split ? &tmap_k_in : &tmap_k, &sh.k_full[s], b * 64,
-                        ui.kbeg + i * kKeyTile);
+            tma_load_2d(dst + b * kKeyTile * 128, b < k_split ? &tmap_k_in : &tmap_k, &sh.k_full[s], b * 64, krow);
         }
       }
     }
@@ -625,14 +638,14 @@ __global__ void __launch_bounds__(Cfg<HI, DI, G>::THREADS, 1)
 
 template <int HI, int DI, int G>
 cudaError_t launch_t(const IndexerPlan& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tqi,
-                     const CUtensorMap& tki, int q_split, int k_split, const float* w, int n_q,
+                     const CUtensorMap& tki, int q_split, int k_split, const PagedRows& pg, const float* w, int n_q,
                      const int2* row_range, const int2* group_range, uint32_t* ck, int32_t* ci, uint32_t* cc,
                      uint32_t* status, cudaStream_t st) {
   using C = Cfg<HI, DI, G>;
   auto kern = indexer_kernel<HI, DI, G>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::DYN_SMEM);
   if (e != cudaSuccess) return e;
-  kern<<<p.grid, C::THREADS, C::DYN_SMEM, st>>>(tq, tk, tqi, tki, q_split, k_split, w, n_q, row_range, group_range,
+  kern<<<p.grid, C::THREADS, C::DYN_SMEM, st>>>(tq, tk, tqi, tki, q_split, k_split, pg, w, n_q, row_range, group_range,
                                              p.n_groups, p.n_chunks,
                                              p.chunk, p.cap, p.topk, ck, ci, cc, status);
   return cudaGetLastError();
@@ -642,13 +655,14 @@ cudaError_t launch_t(const IndexerPlan& p, const CUtensorMap& tq, const CUtensor
 
 
 cudaError_t launch_indexer(const IndexerPlan& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tqi,
-                           const CUtensorMap& tki, int q_split, int k_split, const float* w, int n_q,
+                           const CUtensorMap& tki, int q_split, int k_split, const PagedRows& pg, const float* w, int n_q,
                            const int2* row_range, const int2* group_range, uint32_t* ck, int32_t* ci, uint32_t* cc,
                            uint32_t* status, cudaStream_t st) {
   if (p.n_groups * p.n_chunks == 0) return cudaSuccess;
+  if (pg.block_table && (p.group != 1 || p.chunk % kPageRows != 0)) return cudaErrorInvalidValue;
 #define DSA_IDX_CASE(HI_, DI_, G_)                                                                      \
   if (p.n_heads == HI_ && p.head_dim == DI_ && p.group == G_)                                           \
-    return launch_t<HI_, DI_, G_>(p, tq, tk, tqi, tki, q_split, k_split, w, n_q, row_range, group_range, ck, ci, cc, \
+    return launch_t<HI_, DI_, G_>(p, tq, tk, tqi, tki, q_split, k_split, pg, w, n_q, row_range, group_range, ck, ci, cc, \
                                   status, st);
   DSA_IDX_CASE(4, 64, 64)
   DSA_IDX_CASE(8, 64, 32)

@@ -16,6 +16,18 @@ struct WsHeader {
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
+// Paged latent / index-key caches: pages of kPageRows rows; row t's logical key j lives at
+// cache row block_table[t * max_pages + j / kPageRows] * kPageRows + j % kPageRows and is
+// valid for j < seq_len[t].  block_table == nullptr means a contiguous cache (rows ks[t] + j).
+constexpr int kPageShift = 7;
+constexpr int kPageRows = 1 << kPageShift;
+struct PagedRows {
+  const int32_t* block_table = nullptr;
+  const int32_t* seq_len = nullptr;
+  int max_pages = 0;
+  int n_pages = 0;
+};
+
 // ---------------------------------------------------------------------------- RoPE pre-pass
 // out[row] = in[row] with its last `rope` dims rotated at position pos[row / rows_per_pos];
 // only dims from the first 64-dim block holding rotary dims on are written
@@ -32,7 +44,8 @@ struct IndexerPlan {
   int topk;
 };
 
-// Fills row_range[t] = (ks, ke) when valid, else (0, 0) and flags; group_range[g] = union of
+// Fills row_range[t] = (ks, ke) when valid (ks == nullptr: every range starts at 0), else
+// (0, 0) and flags; group_range[g] = union of
 // the ranges of the group's rows longer than trivial_len (shorter rows keep every key and are
 // not scored).
 cudaError_t launch_ranges(const int32_t* ks, const int32_t* ke, int n_q, int group, int n_kv, int max_len,
@@ -46,7 +59,7 @@ inline int rope_split_blocks(int d, int rope) { return rope > 0 ? (d - rope) / 6
 // 64-dim blocks below q_split / k_split.
 cudaError_t launch_indexer(const IndexerPlan& p, const CUtensorMap& tmap_q, const CUtensorMap& tmap_k,
                            const CUtensorMap& tmap_q_in, const CUtensorMap& tmap_k_in, int q_split, int k_split,
-                           const float* w,
+                           const PagedRows& pg, const float* w,
                            int n_q, const int2* row_range, const int2* group_range, uint32_t* cand_key,
                            int32_t* cand_idx, uint32_t* cand_cnt, uint32_t* status, cudaStream_t st);
 
@@ -64,16 +77,17 @@ int sparse_attn_dense_heads(int n_heads, int n_kv, int topk);
 // selection bitmasks).
 size_t sparse_attn_ws_bytes(int n_q, int n_heads, int n_kv, int topk);
 // Rows of q (consecutive (token, head) rows) that one work item of the chosen walk reads:
-// the box height of tmap_q.
-int sparse_attn_q_box_rows(int n_heads, int n_kv, int topk);
+// the box height of tmap_q (a paged cache always takes the gather walk).
+int sparse_attn_q_box_rows(int n_heads, int n_kv, int topk, bool paged);
 // tmap_kv: block-dense walk -- kv [n_kv x 576] bf16 viewed as (64 dims, n_kv rows, 9 dim
 // blocks) with 128-byte swizzled boxes of {64, 64, 9} = one 64-row tile; gather walk -- kv as
 // a 2-D [n_kv][576] tensor with 128-byte swizzled boxes of {64, 1} (four-row gathers).
 // tmap_q: q as a 2-D [n_q * n_heads][576] tensor, 128-byte swizzled boxes of
 // {64, sparse_attn_q_box_rows(...)}.
 cudaError_t launch_sparse_attn(const CUtensorMap& tmap_kv, const CUtensorMap& tmap_q, int n_q, int n_kv, int n_heads,
-                               int topk, float scale, const void* kv, const int32_t* idx, const int32_t* ks, void* out,
-                               float* lse, uint32_t* status, void* scratch, cudaStream_t st);
+                               int topk, float scale, const void* kv, const int32_t* idx, const int32_t* ks,
+                               const PagedRows& pg, void* out, float* lse, uint32_t* status, void* scratch,
+                               cudaStream_t st);
 
 int device_sm_count();
 

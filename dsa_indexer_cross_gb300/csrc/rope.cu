@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(256) ranges_kernel(const int32_t* __restrict__
   __syncthreads();
   const int t = blockIdx.x * 256 + threadIdx.x;
   if (t < n_q) {
-    const int a = __ldg(ks + t), b = __ldg(ke + t);
+    const int a = ks ? __ldg(ks + t) : 0, b = __ldg(ke + t);
     int2 r = make_int2(0, 0);
     if (a < 0 || b < a || b > n_kv || b - a > max_len) {
       atomicOr(status, DEV_ERR_RANGE);

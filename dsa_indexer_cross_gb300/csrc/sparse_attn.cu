@@ -172,11 +172,47 @@ __device__ __forceinline__ Item item_info(int item, int n_hb, const int32_t* row
   return it;
 }
 
-template <int HB, int HD>
+// Where one token's selection offsets live: rows kst + j of a contiguous cache, or (PAGED)
+// through the token's block-table row, offsets valid below lim.  Built once per work item so
+// the per-slot mapping touches no further per-token state; the cache kind is a template
+// parameter, so the contiguous kernel carries no trace of paging.
+struct TokenRows {
+  long long kst;
+  const int32_t* bt;
+  int lim;
+};
+template <bool PAGED>
+__device__ __forceinline__ TokenRows token_rows(const PagedRows& pg, const int32_t* ks, int t) {
+  TokenRows r{};
+  if constexpr (PAGED) {
+    r.bt = pg.block_table + static_cast<size_t>(t) * pg.max_pages;
+    r.lim = min(__ldg(pg.seq_len + t), pg.max_pages << kPageShift);
+  } else {
+    r.kst = __ldg(ks + t);
+  }
+  return r;
+}
+// Latent row of selection offset j: -1 for an empty slot (j < 0), -2 for an offset or page
+// outside the cache.
+template <bool PAGED>
+__device__ __forceinline__ long long latent_row(const TokenRows& tr, const PagedRows& pg, int n_kv, int j) {
+  if (j < 0) return -1;
+  if constexpr (PAGED) {
+    if (j >= tr.lim) return -2;
+    const int page = __ldg(tr.bt + (j >> kPageShift));
+    if (page < 0 || page >= pg.n_pages) return -2;
+    return (static_cast<long long>(page) << kPageShift) + (j & (kPageRows - 1));
+  } else {
+    const long long row = tr.kst + j;
+    return row >= 0 && row < n_kv ? row : -2;
+  }
+}
+
+template <int HB, int HD, bool PAGED>
 __global__ void __launch_bounds__(ACfg<HB, HD>::THREADS, 1)
     sparse_attn_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_constant__ CUtensorMap tmap_q,
                        const uint16_t* __restrict__ kv, const int32_t* __restrict__ idx,
-                       const int32_t* __restrict__ ks, const int32_t* __restrict__ row_nt,
+                       const int32_t* __restrict__ ks, const PagedRows pg, const int32_t* __restrict__ row_nt,
                        const int2* __restrict__ block_range, const uint32_t* __restrict__ block_mask,
                        uint16_t* __restrict__ out, float* __restrict__ lse, int n_q, int n_kv, int H, int topk,
                        float scale_log2, uint32_t* status, uint32_t* bad_count) {
@@ -289,15 +325,24 @@ __global__ void __launch_bounds__(ACfg<HB, HD>::THREADS, 1)
         // or zeros (cp.async) and is masked by the softmax.
         constexpr int kTmaBlocks = kKB - kCpBlocks;
         const int t = I.t0;
-        const long long kst = __ldg(ks + t);
         const int32_t* irow = idx + static_cast<size_t>(t) * topk;
+        const TokenRows trow = token_rows<PAGED>(pg, ks, t);
         const int grp = tid & 15;
         const int b0 = tid >> 4;
         auto row_of = [&](int slot, bool count_bad) -> int {
           const int j = slot < topk ? __ldg(irow + slot) : -1;
-          const long long row = kst + j;
-          const bool v = j >= 0 && row >= 0 && row < n_kv;
-          if (count_bad && j >= 0 && !v) {
+          long long row;
+          bool v, bad;
+          if constexpr (PAGED) {
+            row = latent_row<true>(trow, pg, n_kv, j);
+            v = row >= 0;
+            bad = row == -2;
+          } else {
+            row = trow.kst + j;
+            v = j >= 0 && row >= 0 && row < n_kv;
+            bad = j >= 0 && !v;
+          }
+          if (count_bad && bad) {
             atomicOr(status, DEV_ERR_BAD_INDEX);
             atomicAdd(bad_count, 1u);
           }
@@ -397,7 +442,8 @@ __global__ void __launch_bounds__(ACfg<HB, HD>::THREADS, 1)
         }
       }
       named_bar_sync(1, kSoft);
-      const long long kst = DENSE ? 0 : __ldg(ks + I.t0);
+      TokenRows trow{};
+      if constexpr (!DENSE) trow = token_rows<PAGED>(pg, ks, I.t0);
       for (int i = 0; i < I.nt; ++i, ++g) {
         const int sb = g & 1;
         bool rv0 = false, rv1 = false;   // gather: rows r0 / r0 + 8 hold a valid selection
@@ -405,8 +451,14 @@ __global__ void __launch_bounds__(ACfg<HB, HD>::THREADS, 1)
           const int s0 = i * kRows + r0, s1 = s0 + 8;
           const int j0 = s0 < topk ? __ldg(irow + s0) : -1;
           const int j1 = s1 < topk ? __ldg(irow + s1) : -1;
-          rv0 = j0 >= 0 && kst + j0 >= 0 && kst + j0 < n_kv;
-          rv1 = j1 >= 0 && kst + j1 >= 0 && kst + j1 < n_kv;
+          if constexpr (PAGED) {
+            rv0 = latent_row<true>(trow, pg, n_kv, j0) >= 0;
+            rv1 = latent_row<true>(trow, pg, n_kv, j1) >= 0;
+          } else {
+            const long long kst = trow.kst;
+            rv0 = j0 >= 0 && kst + j0 >= 0 && kst + j0 < n_kv;
+            rv1 = j1 >= 0 && kst + j1 >= 0 && kst + j1 < n_kv;
+          }
         }
         bool ok = mbar_wait(&sh.s_full[sb], (g >> 1) & 1, &sh.abort_flag, status);
         ok = __all_sync(0xffffffffu, ok);
@@ -795,18 +847,19 @@ __global__ void __launch_bounds__(256) block_mask_kernel(const int32_t* __restri
   for (int i = threadIdx.x; i < kWords / 4; i += blockDim.x) dst[i] = reinterpret_cast<const uint4*>(mask)[i];
 }
 
-template <int HB, int HD>
+template <int HB, int HD, bool PAGED = false>
 cudaError_t launch_cfg(const CUtensorMap& tmap, const CUtensorMap& tmap_q, int n_q, int n_kv, int H, int topk,
-                       float scale, const void* kv, const int32_t* idx, const int32_t* ks, const int32_t* row_nt,
+                       float scale, const void* kv, const int32_t* idx, const int32_t* ks, const PagedRows& pg,
+                       const int32_t* row_nt,
                        const int2* block_range, const uint32_t* block_mask, void* out, float* lse, uint32_t* status,
                        cudaStream_t st) {
   using C = ACfg<HB, HD>;
-  auto kern = sparse_attn_kernel<HB, HD>;
+  auto kern = sparse_attn_kernel<HB, HD, PAGED>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::DYN_SMEM);
   if (e != cudaSuccess) return e;
   const int n_items = C::DENSE ? (n_q + C::B - 1) / C::B : n_q * ((H + HB - 1) / HB);
   const int grid = n_items < device_sm_count() ? n_items : device_sm_count();
-  kern<<<grid, C::THREADS, C::DYN_SMEM, st>>>(tmap, tmap_q, static_cast<const uint16_t*>(kv), idx, ks, row_nt,
+  kern<<<grid, C::THREADS, C::DYN_SMEM, st>>>(tmap, tmap_q, static_cast<const uint16_t*>(kv), idx, ks, pg, row_nt,
                                             block_range, block_mask,
                                             static_cast<uint16_t*>(out), lse, n_q, n_kv, H, topk,
                                             scale * 1.4426950408889634f, status, status + 1);
@@ -846,10 +899,26 @@ cudaError_t launch_dense(const CUtensorMap& tmap_kv, const CUtensorMap& tmap_q, 
   block_mask_kernel<C::B, C::MAXR><<<n_blk, 256, 0, st>>>(idx, ks, n_q, n_kv, topk, br, bm, status, status + 1);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  return launch_cfg<kDenseCols, HD>(tmap_kv, tmap_q, n_q, n_kv, n_heads, topk, scale, nullptr, idx, ks, nullptr, br, bm, out,
+  return launch_cfg<kDenseCols, HD>(tmap_kv, tmap_q, n_q, n_kv, n_heads, topk, scale, nullptr, idx, ks, PagedRows{},
+                                    nullptr, br, bm, out,
                                     lse, status, st);
 }
 
+}  // namespace
+
+namespace {
+// Gather walk, contiguous or paged cache (separate instantiations).
+template <int HB>
+cudaError_t launch_gather(const CUtensorMap& tmap_kv, const CUtensorMap& tmap_q, int n_q, int n_kv, int n_heads,
+                          int topk, float scale, const void* kv, const int32_t* idx, const int32_t* ks,
+                          const PagedRows& pg, const int32_t* row_nt, void* out, float* lse, uint32_t* status,
+                          cudaStream_t st) {
+  if (pg.block_table)
+    return launch_cfg<HB, 0, true>(tmap_kv, tmap_q, n_q, n_kv, n_heads, topk, scale, kv, idx, ks, pg, row_nt, nullptr,
+                                   nullptr, out, lse, status, st);
+  return launch_cfg<HB, 0, false>(tmap_kv, tmap_q, n_q, n_kv, n_heads, topk, scale, kv, idx, ks, pg, row_nt, nullptr,
+                                  nullptr, out, lse, status, st);
+}
 }  // namespace
 
 size_t sparse_attn_ws_bytes(int n_q, int n_heads, int n_kv, int topk) {
@@ -861,16 +930,17 @@ size_t sparse_attn_ws_bytes(int n_q, int n_heads, int n_kv, int topk) {
   return static_cast<size_t>(n_q) * sizeof(int32_t);
 }
 
-int sparse_attn_q_box_rows(int n_heads, int n_kv, int topk) {
-  if (sparse_attn_dense_heads(n_heads, n_kv, topk)) return kDenseCols;
+int sparse_attn_q_box_rows(int n_heads, int n_kv, int topk, bool paged) {
+  if (!paged && sparse_attn_dense_heads(n_heads, n_kv, topk)) return kDenseCols;
   return n_heads <= 16 ? 16 : n_heads <= 32 ? 32 : 64;
 }
 
 cudaError_t launch_sparse_attn(const CUtensorMap& tmap_kv, const CUtensorMap& tmap_q, int n_q, int n_kv, int n_heads,
-                               int topk, float scale, const void* kv, const int32_t* idx, const int32_t* ks, void* out, float* lse,
-                               uint32_t* status, void* scratch, cudaStream_t st) {
+                               int topk, float scale, const void* kv, const int32_t* idx, const int32_t* ks,
+                               const PagedRows& pg, void* out, float* lse, uint32_t* status, void* scratch,
+                               cudaStream_t st) {
   if (n_q <= 0) return cudaSuccess;
-  const int hd = sparse_attn_dense_heads(n_heads, n_kv, topk);
+  const int hd = pg.block_table ? 0 : sparse_attn_dense_heads(n_heads, n_kv, topk);   // paged: gather walk
   if (hd) {
     switch (hd) {
       case 1: return launch_dense<1>(tmap_kv, tmap_q, n_q, n_kv, n_heads, topk, scale, idx, ks, out, lse, status, scratch, st);
@@ -884,13 +954,13 @@ cudaError_t launch_sparse_attn(const CUtensorMap& tmap_kv, const CUtensorMap& tm
   row_tiles_kernel<<<(n_q + 7) / 8, 256, 0, st>>>(idx, n_q, topk, row_nt);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  switch (sparse_attn_q_box_rows(n_heads, n_kv, topk)) {
-    case 16: return launch_cfg<16, 0>(tmap_kv, tmap_q, n_q, n_kv, n_heads, topk, scale, kv, idx, ks, row_nt, nullptr, nullptr,
-                                      out, lse, status, st);
-    case 32: return launch_cfg<32, 0>(tmap_kv, tmap_q, n_q, n_kv, n_heads, topk, scale, kv, idx, ks, row_nt, nullptr, nullptr,
-                                      out, lse, status, st);
-    default: return launch_cfg<64, 0>(tmap_kv, tmap_q, n_q, n_kv, n_heads, topk, scale, kv, idx, ks, row_nt, nullptr, nullptr,
-                                      out, lse, status, st);
+  switch (sparse_attn_q_box_rows(n_heads, n_kv, topk, pg.block_table != nullptr)) {
+    case 16: return launch_gather<16>(tmap_kv, tmap_q, n_q, n_kv, n_heads, topk, scale, kv, idx, ks, pg, row_nt, out,
+                                      lse, status, st);
+    case 32: return launch_gather<32>(tmap_kv, tmap_q, n_q, n_kv, n_heads, topk, scale, kv, idx, ks, pg, row_nt, out,
+                                      lse, status, st);
+    default: return launch_gather<64>(tmap_kv, tmap_q, n_q, n_kv, n_heads, topk, scale, kv, idx, ks, pg, row_nt, out,
+                                      lse, status, st);
   }
 }
 

@@ -246,6 +246,46 @@ dsa_status indexshare_layers_forward(const dsa_indexer_desc* idx_desc, const dsa
                                      const int32_t* k_pos, const float* rope_cs, int32_t rope_n_pos,
                                      dsa_index_cache* cache, void* ws, size_t ws_bytes, void* stream);
 
+/* ------------------------------------------------------------------ paged caches ---- */
+
+/* Paged decode caches (a serving layout; the pages describe per-query key ranges only -- the
+ * Megatron-Bridge commits' per-query starts/ends -- so the paging is this library's own):
+ * the index-key cache [n_pages * page_rows][d_I] bf16 (stored already rotated) and the
+ * latent cache [n_pages * page_rows][576] bf16 hold pages of page_rows rows; query row t's
+ * logical key j (j < seq_len[t]) sits at cache row
+ *   block_table[t * max_pages + j / page_rows] * page_rows + j % page_rows.
+ * All arrays are device memory owned by the caller.  page_rows must be DSA_PAGE_ROWS (one
+ * 128-key indexer tile per page, so every tile is one TMA box). */
+#define DSA_PAGE_ROWS 128
+typedef struct dsa_paged_cache {
+  const int32_t* block_table; /* [n_q][max_pages] int32 physical page ids                    */
+  const int32_t* seq_len;     /* [n_q] int32: keys of row t are logical positions [0, seq_len) */
+  int32_t max_pages;          /* columns of block_table                                       */
+  int32_t n_pages;            /* pages in the cache arrays: desc->n_kv == n_pages * page_rows */
+  int32_t page_rows;          /* DSA_PAGE_ROWS                                                */
+} dsa_paged_cache;
+
+/* dsa_indexer_topk over a paged, pre-rotated index-key cache: row t scores its logical keys
+ * [0, seq_len[t]) and idx_out holds logical positions (offsets from 0), same selection and
+ * order rules as dsa_indexer_topk.  Requires DSA_IDX_INDEPENDENT_ROWS, no DSA_IDX_ROPE_K,
+ * n_heads == 64 (one row per key stream) and max_len <= max_pages * page_rows; the workspace
+ * is dsa_indexer_workspace_size(desc).  A block-table entry outside [0, n_pages) is counted in
+ * the workspace status.  Errors: those of dsa_indexer_topk, DSA_ERR_SHAPE (n_kv !=
+ * n_pages * page_rows), DSA_ERR_UNSUPPORTED (page_rows, n_heads). */
+dsa_status dsa_indexer_topk_paged(const dsa_indexer_desc* desc, const void* q_idx, const void* k_cache, const float* w,
+                                  const int32_t* q_pos, const dsa_paged_cache* pages, const float* rope_cs,
+                                  int32_t rope_n_pos, int32_t* idx_out, float* score_out, void* ws, size_t ws_bytes,
+                                  void* stream);
+
+/* dsa_sparse_attn over a paged latent cache: idx[t] holds logical positions of row t (as
+ * dsa_indexer_topk_paged writes them); an entry >= seq_len[t] or on a page outside the cache
+ * is skipped and counted.  Always the per-token gather walk.  Workspace:
+ * dsa_sparse_attn_workspace_size(desc).  Errors: those of dsa_sparse_attn, DSA_ERR_SHAPE,
+ * DSA_ERR_UNSUPPORTED (page_rows). */
+dsa_status dsa_sparse_attn_paged(const dsa_attn_desc* desc, const void* q, const void* kv_cache, const int32_t* idx,
+                                 const dsa_paged_cache* pages, void* out, float* lse, void* ws, size_t ws_bytes,
+                                 void* stream);
+
 /* ------------------------------------------------------------------ MTP drafting ---- */
 
 /* One step of multi-step MTP drafting with IndexShare ([EX] "MTP path: IndexShare +

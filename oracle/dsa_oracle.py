@@ -303,3 +303,24 @@ def mtp_indexshare_steps(steps: Sequence[dict], q_pos_steps: Sequence, k_pos, ks
         o_l.append(o)
         lse_l.append(lse)
     return idx, o_l, lse_l
+
+
+def unpage_rows(cache: np.ndarray, block_table: np.ndarray, seq_len: np.ndarray, page_rows: int):
+    """Gather each row's logical keys out of a paged cache into one packed array.
+
+    Layout of the paged decode caches: query row t's logical key j (j < seq_len[t]) is cache
+    row block_table[t, j // page_rows] * page_rows + j % page_rows.  Returns (packed, ks, ke)
+    with row t's keys at packed[ks[t]:ke[t]] in logical order, so the contiguous-cache
+    functions above apply unchanged and their offsets are logical positions.
+    """
+    parts, ks, ke, off = [], [], [], 0
+    for t in range(len(seq_len)):
+        L = int(seq_len[t])
+        j = np.arange(L)
+        rows = block_table[t, j // page_rows].astype(np.int64) * page_rows + j % page_rows
+        parts.append(cache[rows])
+        ks.append(off)
+        ke.append(off + L)
+        off += L
+    packed = np.concatenate(parts, axis=0) if parts else cache[:0]
+    return packed, np.asarray(ks, np.int64), np.asarray(ke, np.int64)

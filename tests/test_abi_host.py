@@ -199,3 +199,29 @@ def test_mtp_step_argument_errors_before_launch():
     adesc_bad = D.attn_desc(8, 64, 4, 16, 1 / 24.0)
     assert L.dsa_mtp_indexshare_step(C.byref(idesc), C.byref(adesc_bad), 1, C.byref(io), *args, fake, fake, 1 << 30,
                                      None) == 2
+
+
+def test_paged_calls_reject_bad_layouts_before_launch():
+    L = _lib.lib()
+    fake = 0x100000
+    flags = D.DSA_IDX_ROPE_Q | D.DSA_IDX_INDEPENDENT_ROWS
+    idesc = D.indexer_desc(4, 8 * 128, 64, 128, 64, 32, 1024, flags)
+    pages = _lib.PagedCache(fake, fake, 8, 8, 128)
+    args = (fake, fake, fake, fake)
+    ok_rest = (fake, 16, fake, None, fake, 1 << 30, None)
+    bad = _lib.PagedCache(fake, fake, 8, 8, 64)                    # page_rows other than 128
+    assert L.dsa_indexer_topk_paged(C.byref(idesc), *args, C.byref(bad), *ok_rest) == 4
+    short = _lib.PagedCache(fake, fake, 8, 7, 128)                 # n_kv != n_pages * page_rows
+    assert L.dsa_indexer_topk_paged(C.byref(idesc), *args, C.byref(short), *ok_rest) == 2
+    roped = D.indexer_desc(4, 8 * 128, 64, 128, 64, 32, 1024, flags | D.DSA_IDX_ROPE_K)
+    assert L.dsa_indexer_topk_paged(C.byref(roped), *args, C.byref(pages), *ok_rest) == 1
+    h32 = D.indexer_desc(4, 8 * 128, 32, 128, 64, 32, 1024, flags)
+    assert L.dsa_indexer_topk_paged(C.byref(h32), *args, C.byref(pages), *ok_rest) == 4
+    long_ = D.indexer_desc(4, 8 * 128, 64, 128, 64, 32, 1025, flags)   # max_len beyond max_pages pages
+    assert L.dsa_indexer_topk_paged(C.byref(long_), *args, C.byref(pages), *ok_rest) == 1
+    nobt = _lib.PagedCache(None, fake, 8, 8, 128)
+    assert L.dsa_indexer_topk_paged(C.byref(idesc), *args, C.byref(nobt), *ok_rest) == 1
+    adesc = D.attn_desc(4, 8 * 128, 16, 32, 1 / 24.0)
+    assert L.dsa_sparse_attn_paged(C.byref(adesc), fake, fake, fake, C.byref(short), fake, None, fake, 1 << 30,
+                                   None) == 2
+    assert L.dsa_sparse_attn_paged(C.byref(adesc), fake, fake, fake, None, fake, None, fake, 1 << 30, None) == 1

@@ -318,3 +318,33 @@ def test_mtp_steps_attend_with_the_first_step_selection_brute_force():
         np.testing.assert_allclose(o[s], ob, rtol=1e-11, atol=1e-12)
         np.testing.assert_allclose(lse[s], lseb, rtol=1e-12)
     assert not np.allclose(o[1], o[0])                     # each step runs its own attention
+
+
+# ---------------------------------------------------------------------------- paged caches
+
+def test_unpage_rows_hand_example_and_round_trip():
+    # 2 rows, pages of 2 rows; row 0 = keys 0..2 on pages (3, 1), row 1 = keys 0..3 on (0, 2)
+    cache = np.arange(8 * 3, dtype=np.float64).reshape(8, 3)      # cache row r = [3r, 3r+1, 3r+2]
+    bt = np.array([[3, 1], [0, 2]])
+    packed, ks, ke = O.unpage_rows(cache, bt, np.array([3, 4]), 2)
+    assert ks.tolist() == [0, 3] and ke.tolist() == [3, 7]
+    np.testing.assert_array_equal(packed[:, 0] / 3, [6, 7, 2, 0, 1, 4, 5])
+    # scattering a packed cache into shuffled pages and gathering it back is the identity
+    rng = np.random.default_rng(5)
+    lens = np.array([5, 1, 9, 4])
+    P = 4
+    n_pages_row = (lens + P - 1) // P
+    perm = rng.permutation(int(n_pages_row.sum()) + 3)
+    bt = np.full((lens.size, int(n_pages_row.max())), -1)
+    src = rng.standard_normal((int(lens.sum()), 5))
+    paged = np.zeros((perm.size * P, 5))
+    k, off = 0, 0
+    for t, L in enumerate(lens):
+        for p in range(n_pages_row[t]):
+            bt[t, p] = perm[k]
+            n = min(P, L - p * P)
+            paged[perm[k] * P: perm[k] * P + n] = src[off + p * P: off + p * P + n]
+            k += 1
+        off += L
+    back, ks, ke = O.unpage_rows(paged, bt, lens, P)
+    np.testing.assert_array_equal(back, src)
