@@ -46,6 +46,9 @@ def parse():
     ap.add_argument("--mtp-steps", type=int, default=0,
                     help="decode workloads: also time multi-step MTP drafting with IndexShare (indexer at step 0, "
                          "later steps reuse its indices) and report it under 'mtp'")
+    ap.add_argument("--proj", action="store_true",
+                    help="also time the indexer's input projections (wq_b, wk + k_norm, weights_proj) for the "
+                         "workload's query rows, hidden width 6144 and query latent 2048, under 'proj'")
     ap.add_argument("--paged", action="store_true",
                     help="decode workloads: also time the paged-cache indexer and attention (128-row pages, "
                          "shuffled) against the contiguous calls on the same data, under 'paged'")
@@ -293,6 +296,46 @@ def time_mtp(D, synth, w, steps: int, dev, stream, flush, reps: int = 10):
     return {"steps": steps, "step_ms": step_ms, "cycle_ms": cyc,
             "draft_tokens_per_s": steps * w.n_q / (cyc / 1e3),
             "note": "indexer at step 0 only; later steps attend with step 0's indices"}
+
+
+# --------------------------------------------------------------------------- projections
+def time_proj(D, w, dev, stream, flush, tc_peak, d_hidden: int = 6144, d_q: int = 2048, reps: int = 20):
+    """Median time of dsa_indexer_projections for the workload's query rows (synthetic weights),
+    against the bf16 peak on its FLOPs: 2 T (H_I d_I d_q + d_I d_h + H_I d_h)."""
+    g = torch.Generator(device=dev)
+    g.manual_seed(77)
+    T, H, d = w.n_q, w.n_heads_idx, w.head_dim_idx
+    rn = lambda *s: torch.randn(s, generator=g, device=dev, dtype=torch.float32)
+    x = (rn(T, d_hidden) * 0.5).to(torch.bfloat16)
+    ql = (rn(T, d_q) * 0.5).to(torch.bfloat16)
+    wq = (rn(H * d, d_q) / math.sqrt(d_q)).to(torch.bfloat16)
+    wk = (rn(d, d_hidden) / math.sqrt(d_hidden)).to(torch.bfloat16)
+    wp = (rn(H, d_hidden) / math.sqrt(d_hidden)).to(torch.bfloat16)
+    gamma, beta = torch.ones(d, device=dev), torch.zeros(d, device=dev)
+    q_idx = torch.empty((T, H, d), dtype=torch.bfloat16, device=dev)
+    k_idx = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
+    wo = torch.empty((T, H), dtype=torch.float32, device=dev)
+    ws = torch.zeros(256, dtype=torch.uint8, device=dev)
+    desc = D.ProjDesc(T, d_hidden, d_q, H, d, 1e-6)
+    call = lambda: D.dsa_indexer_projections(desc, x, ql, wq, wk, gamma, beta, wp, q_idx, k_idx, wo, ws=ws,
+                                             stream=stream)
+    call()
+    ms = []
+    for _ in range(reps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        call()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms.append(a.elapsed_time(b))
+    if D.dsa_workspace_status(ws) != 0:
+        raise RuntimeError("device status set by the projections")
+    m = statistics.median(ms)
+    flops = 2.0 * T * (H * d * d_q + d * d_hidden + H * d_hidden)
+    return {"d_hidden": d_hidden, "d_q": d_q, "ms": m, "tflops": flops / (m / 1e3) / 1e12,
+            "frac_of_bf16_peak": flops / (m / 1e3) / 1e12 / tc_peak,
+            "note": "synthetic weights; widths assumed (the pages give none)"}
 
 
 # --------------------------------------------------------------------------- paged caches
@@ -555,6 +598,8 @@ def run_native(args):
                                                       "scores_topk": phase_ms[2], "select": phase_ms[3]}},
         "clocks": clk.summary(),
     }
+    if args.proj:
+        line["proj"] = time_proj(D, w, dev, stream, flush, tc_burst)
     if args.paged and w.kind == "decode":
         line["paged"] = time_paged(D, synth, w, geo, layers[0], idx_full, attn_ms, idx_ms, dev, stream, flush)
     if args.mtp_steps > 0 and w.kind == "decode":

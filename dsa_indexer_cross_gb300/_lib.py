@@ -29,7 +29,7 @@ EXPORTED = ("dsa_status_string", "dsa_last_error", "dsa_donor_table", "dsa_rope_
             "dsa_index_cache_donor", "dsa_index_cache_indices", "dsa_index_cache_destroy",
             "dsa_layers_workspace_size", "indexshare_layers_forward", "dsa_workspace_status",
             "dsa_indexer_topk_static", "dsa_profile_enable", "dsa_profile_indexer_last", "dsa_mtp_indexshare_step",
-            "dsa_indexer_topk_paged", "dsa_sparse_attn_paged")
+            "dsa_indexer_topk_paged", "dsa_sparse_attn_paged", "dsa_indexer_projections")
 
 
 class DsaError(RuntimeError):
@@ -102,6 +102,8 @@ def lib() -> C.CDLL:
         L.dsa_profile_indexer_last.argtypes = [P(C.c_float), i32]
         L.dsa_indexer_topk_static.restype = st
         L.dsa_indexer_topk_static.argtypes = [P(IndexerDesc), vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp]
+        L.dsa_indexer_projections.restype = st
+        L.dsa_indexer_projections.argtypes = [P(ProjDesc), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.dsa_indexer_topk_paged.restype = st
         L.dsa_indexer_topk_paged.argtypes = [P(IndexerDesc), vp, vp, vp, vp, P(PagedCache), vp, i32, vp, vp, vp, sz, vp]
         L.dsa_sparse_attn_paged.restype = st
@@ -279,6 +281,22 @@ def indexshare_layers_forward(idesc: IndexerDesc, adesc: AttnDesc, indexer_types
     _check(lib().indexshare_layers_forward(C.byref(idesc), C.byref(adesc), len(types), _u8(types), io, _ptr(ks),
                                            _ptr(ke), _ptr(q_pos), _ptr(k_pos), _ptr(rope_cs), n_pos, cache.handle,
                                            _ptr(ws), ws.numel(), _stream(stream)))
+    return ws
+
+
+class ProjDesc(C.Structure):
+    _fields_ = [("n_tokens", C.c_int32), ("d_hidden", C.c_int32), ("d_q", C.c_int32), ("n_heads", C.c_int32),
+                ("head_dim", C.c_int32), ("ln_eps", C.c_float)]
+
+
+def dsa_indexer_projections(desc: "ProjDesc", x, q_latent, wq_b, wk, k_norm_w, k_norm_b, weights_proj, q_idx, k_idx,
+                            w, ws=None, stream=None):
+    """q_idx = q_latent wq_b^T, k_idx = LayerNorm(x wk^T) (k_norm weight / bias), w = x weights_proj^T."""
+    if ws is None:
+        ws = torch.zeros(256, dtype=torch.uint8, device=x.device)
+    _check(lib().dsa_indexer_projections(C.byref(desc), _ptr(x), _ptr(q_latent), _ptr(wq_b), _ptr(wk), _ptr(k_norm_w),
+                                         _ptr(k_norm_b), _ptr(weights_proj), _ptr(q_idx), _ptr(k_idx), _ptr(w),
+                                         _ptr(ws), ws.numel(), _stream(stream)))
     return ws
 
 

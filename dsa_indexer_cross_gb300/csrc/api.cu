@@ -667,6 +667,54 @@ dsa_status dsa_sparse_attn_paged(const dsa_attn_desc* desc, const void* q, const
                   nullptr, &pg);
 }
 
+dsa_status dsa_indexer_projections(const dsa_proj_desc* d, const void* x, const void* q_latent, const void* wq_b,
+                                   const void* wk, const float* k_norm_w, const float* k_norm_b,
+                                   const void* weights_proj, void* q_idx, void* k_idx, float* w, void* ws,
+                                   size_t ws_bytes, void* stream) {
+  if (!d) return fail(DSA_ERR_ARG, "projection descriptor is NULL");
+  if (d->n_tokens < 0) return fail(DSA_ERR_ARG, "n_tokens must be >= 0");
+  if (d->d_hidden <= 0 || d->d_hidden % 64 || d->d_q <= 0 || d->d_q % 64)
+    return fail(DSA_ERR_UNSUPPORTED, "d_hidden %d / d_q %d must be positive multiples of 64", d->d_hidden, d->d_q);
+  if (!supported_heads(d->n_heads)) return fail(DSA_ERR_UNSUPPORTED, "index n_heads %d", d->n_heads);
+  if (d->head_dim != 64 && d->head_dim != 128) return fail(DSA_ERR_UNSUPPORTED, "index head_dim %d", d->head_dim);
+  if (!(d->ln_eps >= 0.f) || !std::isfinite(d->ln_eps)) return fail(DSA_ERR_ARG, "ln_eps must be finite and >= 0");
+  if (!x || !q_latent || !wq_b || !wk || !k_norm_w || !k_norm_b || !weights_proj || !q_idx || !k_idx || !w || !ws)
+    return fail(DSA_ERR_ARG, "every tensor and ws must be non-NULL");
+  if (!aligned16(x) || !aligned16(q_latent) || !aligned16(wq_b) || !aligned16(wk) || !aligned16(weights_proj) ||
+      !aligned16(q_idx) || !aligned16(k_idx))
+    return fail(DSA_ERR_ARG, "bf16 tensors must be 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(ws) % kAlign) return fail(DSA_ERR_ARG, "workspace must be 256-byte aligned");
+  if (ws_bytes < kAlign) return fail(DSA_ERR_WORKSPACE, "projection workspace too small: %zu < %zu bytes", ws_bytes, kAlign);
+  if (d->n_tokens == 0) return DSA_OK;
+  dsa_status s;
+  if ((s = check_device()) != DSA_OK) return s;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if ((e = cudaMemsetAsync(ws, 0, kAlign, st)) != cudaSuccess) return cuda_fail(e, "clear status");
+  const int nq = d->n_heads * d->head_dim;
+  const int nw_tile = std::max(32, (d->n_heads + 31) / 32 * 32);
+  const uint64_t T = static_cast<uint64_t>(d->n_tokens);
+  CUtensorMap ta[3], tb[3];
+  if ((s = tmap_bf16(&ta[0], q_latent, d->d_q, T, 128)) != DSA_OK) return s;
+  if ((s = tmap_bf16(&tb[0], wq_b, d->d_q, nq, 256)) != DSA_OK) return s;
+  if ((s = tmap_bf16(&ta[1], x, d->d_hidden, T, 128)) != DSA_OK) return s;
+  if ((s = tmap_bf16(&tb[1], wk, d->d_hidden, d->head_dim, d->head_dim)) != DSA_OK) return s;
+  if ((s = tmap_bf16(&ta[2], x, d->d_hidden, T, 128)) != DSA_OK) return s;
+  if ((s = tmap_bf16(&tb[2], weights_proj, d->d_hidden, d->n_heads, nw_tile)) != DSA_OK) return s;
+  ProjJobs J{};
+  J.n_jobs = 3;
+  J.job[0] = ProjJob{nq, d->d_q, 256, kProjEpiBf16, q_idx, nullptr, nullptr, 0.f};
+  J.job[1] = ProjJob{d->head_dim, d->d_hidden, d->head_dim, kProjEpiLayerNorm, k_idx, k_norm_w, k_norm_b, d->ln_eps};
+  J.job[2] = ProjJob{d->n_heads, d->d_hidden, nw_tile, kProjEpiF32, w, nullptr, nullptr, 0.f};
+  const int m_tiles = (d->n_tokens + 127) / 128;
+  J.first_unit[0] = 0;
+  for (int j = 0; j < 3; ++j)
+    J.first_unit[j + 1] = J.first_unit[j] + m_tiles * ((J.job[j].n_total + J.job[j].n_tile - 1) / J.job[j].n_tile);
+  e = launch_projections(ta, tb, J, d->n_tokens, static_cast<uint32_t*>(ws), st);
+  if (e != cudaSuccess) return cuda_fail(e, "projection kernel");
+  return DSA_OK;
+}
+
 dsa_status dsa_workspace_status(const void* ws, void* stream, uint32_t* device_bits) {
   if (!ws) return fail(DSA_ERR_ARG, "workspace is NULL");
   WsHeader h{};

@@ -89,6 +89,27 @@ cudaError_t launch_sparse_attn(const CUtensorMap& tmap_kv, const CUtensorMap& tm
                                const PagedRows& pg, void* out, float* lse, uint32_t* status, void* scratch,
                                cudaStream_t st);
 
+// ---------------------------------------------------------------------------- indexer projections
+// One output matrix Y[T][n_total] = A[T][k] . W[n_total][k]^T of the projection kernel, in N tiles
+// of n_tile outputs (32..256, multiple of 32; the LayerNorm epilogue needs n_tile == n_total).
+enum { kProjEpiBf16 = 0, kProjEpiLayerNorm = 1, kProjEpiF32 = 2 };
+struct ProjJob {
+  int n_total, k, n_tile, epi;
+  void* out;             // bf16 (kProjEpiBf16, kProjEpiLayerNorm) or fp32 [T][n_total]
+  const float* gamma;    // LayerNorm weight / bias [n_total]
+  const float* beta;
+  float eps;
+};
+struct ProjJobs {
+  ProjJob job[3];
+  int n_jobs;
+  int first_unit[4];     // first unit of each job; first_unit[n_jobs] = total units
+};
+// ta[j] / tb[j]: the activations [T][k] and the weights [n_total][k] of job j, bf16, 128-byte
+// swizzled boxes of {64, 128} and {64, n_tile}.
+cudaError_t launch_projections(const CUtensorMap* ta, const CUtensorMap* tb, const ProjJobs& J, int n_tokens,
+                               uint32_t* status, cudaStream_t st);
+
 int device_sm_count();
 
 }  // namespace dsa

@@ -246,6 +246,37 @@ dsa_status indexshare_layers_forward(const dsa_indexer_desc* idx_desc, const dsa
                                      const int32_t* k_pos, const float* rope_cs, int32_t rope_n_pos,
                                      dsa_index_cache* cache, void* ws, size_t ws_bytes, void* stream);
 
+/* ------------------------------------------------------------------ projections ----- */
+
+/* The indexer's input projections of one full layer ("GLM-5/5.1/5.2 DSA + LoRA enablement",
+ * indexer RoPE half-swap commit: wq_b, wk, k_norm -- a LayerNorm with weight and bias applied
+ * to the key before RoPE -- and weights_proj, one scalar per index head):
+ *   q_idx[t] = q_latent[t] . wq_b^T                               [n_heads * head_dim] bf16
+ *   k_idx[t] = LayerNorm_eps(x[t] . wk^T) * k_norm_w + k_norm_b   [head_dim]           bf16
+ *   w[t]     = x[t] . weights_proj^T                              [n_heads]            fp32
+ * (no further scaling: fold any into weights_proj).  The outputs feed dsa_indexer_topk
+ * (which applies the RoPE).  All three run in one tensor-core kernel (fp32 accumulation, the
+ * LayerNorm in fp32 on the accumulator, outputs rounded once).
+ * Layouts, row-major device arrays: x [n_tokens][d_hidden], q_latent [n_tokens][d_q] bf16;
+ * wq_b [n_heads * head_dim][d_q], wk [head_dim][d_hidden], weights_proj [n_heads][d_hidden]
+ * bf16; k_norm_w, k_norm_b [head_dim] fp32.  d_hidden and d_q multiples of 64; n_heads in
+ * {4, 8, 16, 32, 64}, head_dim in {64, 128} (the indexer's lists); ws: at least 256 bytes,
+ * 256-byte aligned (its first word is the status read by dsa_workspace_status).
+ * Errors: DSA_ERR_ARG, DSA_ERR_UNSUPPORTED, DSA_ERR_WORKSPACE, DSA_ERR_CUDA. */
+typedef struct dsa_proj_desc {
+  int32_t n_tokens;
+  int32_t d_hidden;  /* width of x (K of wk and weights_proj)        */
+  int32_t d_q;       /* width of the query latent (K of wq_b)       */
+  int32_t n_heads;   /* index heads H_I                              */
+  int32_t head_dim;  /* d_I                                          */
+  float ln_eps;      /* k_norm epsilon                               */
+} dsa_proj_desc;
+
+dsa_status dsa_indexer_projections(const dsa_proj_desc* desc, const void* x, const void* q_latent, const void* wq_b,
+                                   const void* wk, const float* k_norm_w, const float* k_norm_b,
+                                   const void* weights_proj, void* q_idx, void* k_idx, float* w, void* ws,
+                                   size_t ws_bytes, void* stream);
+
 /* ------------------------------------------------------------------ paged caches ---- */
 
 /* Paged decode caches (a serving layout; the pages describe per-query key ranges only -- the

@@ -324,3 +324,26 @@ def unpage_rows(cache: np.ndarray, block_table: np.ndarray, seq_len: np.ndarray,
         off += L
     packed = np.concatenate(parts, axis=0) if parts else cache[:0]
     return packed, np.asarray(ks, np.int64), np.asarray(ke, np.int64)
+
+
+def indexer_projections(x: np.ndarray, q_latent: np.ndarray, wq_b: np.ndarray, wk: np.ndarray,
+                        k_norm_w: np.ndarray, k_norm_b: np.ndarray, w_proj: np.ndarray,
+                        n_heads: int, head_dim: int, eps: float):
+    """The indexer's input projections of one full layer.
+
+    "GLM-5/5.1/5.2 DSA + LoRA enablement" (Megatron-Bridge pull request), indexer RoPE
+    half-swap commit: wq_b gives the index queries, wk the shared index key, k_norm (a
+    LayerNorm with weight and bias) is applied to the key before RoPE, weights_proj gives one
+    scalar per index head.  Read here as q_idx = q_latent wq_b^T, k_idx = LayerNorm(x wk^T)
+    (biased variance, epsilon inside the square root) * k_norm_w + k_norm_b, w = x
+    weights_proj^T, with q_idx and k_idx rounded to bf16 once (what the indexer consumes).
+    Returns (q_idx [T, H, d], k_idx [T, d], w [T, H]) as float64.
+    """
+    T = x.shape[0]
+    q = round_to_bf16(np.asarray(q_latent, np.float64) @ np.asarray(wq_b, np.float64).T).reshape(T, n_heads, head_dim)
+    y = np.asarray(x, np.float64) @ np.asarray(wk, np.float64).T
+    mu = y.mean(axis=1, keepdims=True)
+    var = ((y - mu) ** 2).mean(axis=1, keepdims=True)
+    k = round_to_bf16((y - mu) / np.sqrt(var + eps) * np.asarray(k_norm_w, np.float64) + np.asarray(k_norm_b, np.float64))
+    w = np.asarray(x, np.float64) @ np.asarray(w_proj, np.float64).T
+    return q, k, w

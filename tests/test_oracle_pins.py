@@ -348,3 +348,31 @@ def test_unpage_rows_hand_example_and_round_trip():
         off += L
     back, ks, ke = O.unpage_rows(paged, bt, lens, P)
     np.testing.assert_array_equal(back, src)
+
+
+# ---------------------------------------------------------------------------- projections
+
+def test_projections_layer_norm_matches_torch_and_closed_forms():
+    rng = np.random.default_rng(31)
+    T, D, Dq, H, d, eps = 5, 64, 64, 2, 8, 1e-6
+    x = rng.standard_normal((T, D))
+    ql = rng.standard_normal((T, Dq))
+    wk = rng.standard_normal((d, D))
+    g, b = rng.standard_normal(d), rng.standard_normal(d)
+    # one-hot weights select input columns: q_idx[t, h, i] = q_latent[t, sel[h * d + i]]
+    sel = rng.integers(0, Dq, size=H * d)
+    wq = np.zeros((H * d, Dq))
+    wq[np.arange(H * d), sel] = 1.0
+    wp = np.zeros((H, D))
+    wp[0, 3], wp[1, 7] = 1.0, -2.0
+    q, k, w = O.indexer_projections(x, ql, wq, wk, g, b, wp, H, d, eps)
+    np.testing.assert_array_equal(q.reshape(T, H * d), O.round_to_bf16(ql[:, sel]))
+    np.testing.assert_array_equal(w, np.stack([x[:, 3], -2.0 * x[:, 7]], axis=1))
+    ref = torch.nn.functional.layer_norm(torch.from_numpy(x @ wk.T), (d,), torch.from_numpy(g), torch.from_numpy(b),
+                                         eps=eps).numpy()
+    np.testing.assert_array_equal(k, O.round_to_bf16(ref))
+    # a row whose projected key is constant normalises to the bias
+    x2 = np.zeros((1, D))
+    wk2 = np.ones((d, D))
+    _, k2, _ = O.indexer_projections(x2 + 1.0, ql[:1], wq, wk2, g, b, wp, H, d, eps)
+    np.testing.assert_allclose(k2[0], O.round_to_bf16(b), rtol=0, atol=0)
