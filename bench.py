@@ -506,24 +506,20 @@ def run_native(args):
         D.dsa_profile_enable(False)
     phase_ms = [statistics.median(p[i] for p in phases) for i in range(4)]
 
-    # ---------------- end to end through the C ABI from pinned host buffers
+    # ---------------- end to end through the C ABI from pinned host buffers: every layer's
+    # inputs are uploaded and every layer's output downloaded inside the timed region, with
+    # the library's host pipeline overlapping the transfers of one layer with the kernels of
+    # another
+    from dsa_indexer_cross_gb300.pipeline import HostLayerPipeline
     in_keys = ("q_idx", "k_idx", "w", "q", "kv")
     host_in = [{k: v.cpu().pin_memory() for k, v in L.items() if k in in_keys} for L in layers]
     host_out = [torch.empty(L["out"].shape, dtype=L["out"].dtype).pin_memory() for L in layers]
     h2d = sum(v.numel() * v.element_size() for H in host_in for v in H.values())
     d2h = sum(v.numel() * v.element_size() for v in host_out)
-    dev_in = [{k: torch.empty_like(v, device=dev) for k, v in H.items()} for H in host_in]
-    for l, L in enumerate(dev_in):
-        L["out"], L["lse"] = layers[l]["out"], layers[l]["lse"]
+    pipe = HostLayerPipeline(idesc, adesc, w.layers, host_in, dev)
 
     def e2e_step():
-        for H, Dd in zip(host_in, dev_in):
-            for k, v in H.items():
-                Dd[k].copy_(v, non_blocking=True)
-        D.indexshare_layers_forward(idesc, adesc, w.layers, dev_in, ks, ke, q_pos, k_pos, rope, cache, ws=ws,
-                                    stream=stream)
-        for L, Ho in zip(dev_in, host_out):
-            Ho.copy_(L["out"], non_blocking=True)
+        pipe.forward(host_in, host_out, ks, ke, q_pos, k_pos, rope, stream=stream)
 
     e2e_step()
     torch.cuda.synchronize()
@@ -534,6 +530,8 @@ def run_native(args):
         b.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in e2e_ev) / len(e2e_ev), dev)
+    if D.dsa_workspace_status(pipe.iws) != 0 or D.dsa_workspace_status(pipe.aws) != 0:
+        raise RuntimeError("device status set during the end-to-end steps")
     if D.dsa_workspace_status(ws) != 0:
         raise RuntimeError("device status set during the timed region")
 
