@@ -692,25 +692,26 @@ dsa_status dsa_indexer_projections(const dsa_proj_desc* d, const void* x, const 
   cudaError_t e;
   if ((e = cudaMemsetAsync(ws, 0, kAlign, st)) != cudaSuccess) return cuda_fail(e, "clear status");
   const int nq = d->n_heads * d->head_dim;
-  const int nw_tile = std::max(32, (d->n_heads + 31) / 32 * 32);
+  const int nw_box = std::max(32, (d->n_heads + 31) / 32 * 32);   // head-weight rows in the key tile
   const uint64_t T = static_cast<uint64_t>(d->n_tokens);
-  CUtensorMap ta[3], tb[3];
-  if ((s = tmap_bf16(&ta[0], q_latent, d->d_q, T, 128)) != DSA_OK) return s;
-  if ((s = tmap_bf16(&tb[0], wq_b, d->d_q, nq, 256)) != DSA_OK) return s;
-  if ((s = tmap_bf16(&ta[1], x, d->d_hidden, T, 128)) != DSA_OK) return s;
-  if ((s = tmap_bf16(&tb[1], wk, d->d_hidden, d->head_dim, d->head_dim)) != DSA_OK) return s;
-  if ((s = tmap_bf16(&ta[2], x, d->d_hidden, T, 128)) != DSA_OK) return s;
-  if ((s = tmap_bf16(&tb[2], weights_proj, d->d_hidden, d->n_heads, nw_tile)) != DSA_OK) return s;
+  // the key + head-weight units (d_hidden / 64 K blocks each) go first, the shorter query
+  // units after them, so the last round of the persistent grid is made of short units
+  CUtensorMap ta[2], tb[2], tb2;
+  if ((s = tmap_bf16(&ta[0], x, d->d_hidden, T, 128)) != DSA_OK) return s;
+  if ((s = tmap_bf16(&tb[0], wk, d->d_hidden, d->head_dim, d->head_dim)) != DSA_OK) return s;
+  if ((s = tmap_bf16(&tb2, weights_proj, d->d_hidden, d->n_heads, nw_box)) != DSA_OK) return s;
+  if ((s = tmap_bf16(&ta[1], q_latent, d->d_q, T, 128)) != DSA_OK) return s;
+  if ((s = tmap_bf16(&tb[1], wq_b, d->d_q, nq, 256)) != DSA_OK) return s;
   ProjJobs J{};
-  J.n_jobs = 3;
-  J.job[0] = ProjJob{nq, d->d_q, 256, kProjEpiBf16, q_idx, nullptr, nullptr, 0.f};
-  J.job[1] = ProjJob{d->head_dim, d->d_hidden, d->head_dim, kProjEpiLayerNorm, k_idx, k_norm_w, k_norm_b, d->ln_eps};
-  J.job[2] = ProjJob{d->n_heads, d->d_hidden, nw_tile, kProjEpiF32, w, nullptr, nullptr, 0.f};
+  J.n_jobs = 2;
+  J.job[0] = ProjJob{d->head_dim, d->d_hidden, d->head_dim + nw_box, kProjEpiLayerNormF32, k_idx, k_norm_w, k_norm_b,
+                     d->ln_eps, w, d->n_heads};
+  J.job[1] = ProjJob{nq, d->d_q, 256, kProjEpiBf16, q_idx, nullptr, nullptr, 0.f, nullptr, 0};
   const int m_tiles = (d->n_tokens + 127) / 128;
   J.first_unit[0] = 0;
-  for (int j = 0; j < 3; ++j)
-    J.first_unit[j + 1] = J.first_unit[j] + m_tiles * ((J.job[j].n_total + J.job[j].n_tile - 1) / J.job[j].n_tile);
-  e = launch_projections(ta, tb, J, d->n_tokens, static_cast<uint32_t*>(ws), st);
+  J.first_unit[1] = m_tiles;
+  J.first_unit[2] = m_tiles + m_tiles * (nq / 256);
+  e = launch_projections(ta, tb, tb2, J, d->n_tokens, static_cast<uint32_t*>(ws), st);
   if (e != cudaSuccess) return cuda_fail(e, "projection kernel");
   return DSA_OK;
 }

@@ -90,25 +90,31 @@ cudaError_t launch_sparse_attn(const CUtensorMap& tmap_kv, const CUtensorMap& tm
                                cudaStream_t st);
 
 // ---------------------------------------------------------------------------- indexer projections
-// One output matrix Y[T][n_total] = A[T][k] . W[n_total][k]^T of the projection kernel, in N tiles
-// of n_tile outputs (32..256, multiple of 32; the LayerNorm epilogue needs n_tile == n_total).
-enum { kProjEpiBf16 = 0, kProjEpiLayerNorm = 1, kProjEpiF32 = 2 };
+// One GEMM job of the projection kernel, Y = A[T][k] . W^T in N tiles of n_tile weight rows.
+//   kProjEpiBf16:        W = one matrix [n_total][k], output bf16 [T][n_total], n_tile <= 256;
+//   kProjEpiLayerNormF32: W = two matrices stacked in one tile -- n_total rows (LayerNorm'd,
+//                        output bf16 [T][n_total]) then n2 rows (output fp32 out2 [T][n2]) --
+//                        so both share one pass over the activations; n_tile = n_total + the
+//                        second matrix's box height.
+enum { kProjEpiBf16 = 0, kProjEpiLayerNormF32 = 1 };
 struct ProjJob {
   int n_total, k, n_tile, epi;
-  void* out;             // bf16 (kProjEpiBf16, kProjEpiLayerNorm) or fp32 [T][n_total]
+  void* out;
   const float* gamma;    // LayerNorm weight / bias [n_total]
   const float* beta;
   float eps;
+  float* out2;           // fp32 tail outputs [T][n2]
+  int n2;
 };
 struct ProjJobs {
-  ProjJob job[3];
+  ProjJob job[2];
   int n_jobs;
-  int first_unit[4];     // first unit of each job; first_unit[n_jobs] = total units
+  int first_unit[3];     // first unit of each job; first_unit[n_jobs] = total units
 };
-// ta[j] / tb[j]: the activations [T][k] and the weights [n_total][k] of job j, bf16, 128-byte
-// swizzled boxes of {64, 128} and {64, n_tile}.
-cudaError_t launch_projections(const CUtensorMap* ta, const CUtensorMap* tb, const ProjJobs& J, int n_tokens,
-                               uint32_t* status, cudaStream_t st);
+// ta[j]: the activations of job j ([T][k] bf16, boxes {64, 128}); tb[j]: its weights ([rows][k],
+// boxes {64, rows of the tile}); tb2: the second weight matrix of the LayerNorm job.
+cudaError_t launch_projections(const CUtensorMap* ta, const CUtensorMap* tb, const CUtensorMap& tb2,
+                               const ProjJobs& J, int n_tokens, uint32_t* status, cudaStream_t st);
 
 int device_sm_count();
 

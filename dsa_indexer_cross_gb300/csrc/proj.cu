@@ -7,12 +7,14 @@
 //   q_idx[t] = q_latent[t] . wq_b^T          -> [H_I * d_I] bf16
 //   k_idx[t] = LayerNorm(x[t] . wk^T)        -> [d_I] bf16 (affine k_norm weight / bias)
 //   w[t]     = x[t] . weights_proj^T         -> [H_I] fp32
-// Every output is a GEMM over the token rows with its own epilogue, so one persistent kernel
-// walks the units (output matrix, 128-token tile, N tile) of all three: TMA streams 64-wide K
-// blocks of the activations and of the weight rows into a four-stage ring, one thread issues
-// tcgen05.mma (M = 128 tokens, N <= 256 outputs, K = 16) into a double-buffered TMEM
-// accumulator, and four epilogue warps (thread = token row = TMEM lane) convert and store; the
-// LayerNorm unit holds a whole key row (N = d_I) so the normalisation happens in registers.
+// Every output is a GEMM over the token rows, so one persistent kernel walks the units (job,
+// 128-token tile, N tile) of two jobs: the query projection, and the key and head-weight
+// projections together (wk's rows and weights_proj's rows stacked in one weight tile, so both
+// read the activations once).  TMA streams 64-wide K blocks of the activations and of the
+// weight rows into a four-stage ring, one thread issues tcgen05.mma (M = 128 tokens, N <= 256,
+// K = 16) into a double-buffered TMEM accumulator, and four epilogue warps (thread = token row
+// = TMEM lane) convert and store; a key row is whole in one tile (N >= d_I), so the LayerNorm
+// happens in registers.
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -56,8 +58,7 @@ __device__ __forceinline__ PUnit punit(const ProjJobs& J, int u, int m_tiles) {
 __global__ void __launch_bounds__(kPThreads, 1)
     proj_kernel(const __grid_constant__ CUtensorMap ta0, const __grid_constant__ CUtensorMap tb0,
                 const __grid_constant__ CUtensorMap ta1, const __grid_constant__ CUtensorMap tb1,
-                const __grid_constant__ CUtensorMap ta2, const __grid_constant__ CUtensorMap tb2, const ProjJobs J,
-                int n_tokens, uint32_t* status) {
+                const __grid_constant__ CUtensorMap tb_2, const ProjJobs J, int n_tokens, uint32_t* status) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ ProjShared sh;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -65,8 +66,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
   const int m_tiles = (n_tokens + kPM - 1) / kPM;
   const int n_units = J.first_unit[J.n_jobs];
   auto maps = [&](int job, const CUtensorMap*& a, const CUtensorMap*& b) {
-    a = job == 0 ? &ta0 : job == 1 ? &ta1 : &ta2;
-    b = job == 0 ? &tb0 : job == 1 ? &tb1 : &tb2;
+    a = job == 0 ? &ta0 : &ta1;
+    b = job == 0 ? &tb0 : &tb1;
   };
 
   if (threadIdx.x == 0) {
@@ -109,7 +110,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
           uint8_t* a = smem + s * kPStageBytes;
           mbar_arrive_expect_tx(&sh.full[s], bytes);
           tma_load_2d(a, ma, &sh.full[s], kb * 64, p.m0);                 // rows past n_tokens read zeros
-          tma_load_2d(a + kPABytes, mb, &sh.full[s], kb * 64, p.n0);      // rows past n_total read zeros
+          tma_load_2d(a + kPABytes, mb, &sh.full[s], kb * 64, p.n0);      // rows past the matrix read zeros
+          if (jb.epi == kProjEpiLayerNormF32)                             // the stacked second matrix
+            tma_load_2d(a + kPABytes + jb.n_total * 128, &tb_2, &sh.full[s], kb * 64, 0);
         }
       }
     }
@@ -156,19 +159,19 @@ __global__ void __launch_bounds__(kPThreads, 1)
       const int token = p.m0 + quarter * 32 + lane;
       const bool live = token < n_tokens;
       const uint32_t tcol = tmem + t_lane + buf * kPMaxN;
-      if (jb.epi == kProjEpiLayerNorm) {
+      if (jb.epi == kProjEpiLayerNormF32) {
         // mean, then the centred sum of squares, then the normalised, scaled, shifted row
         float sum = 0.f;
-        for (int c0 = 0; c0 < jb.n_tile; c0 += 32) {
+        for (int c0 = 0; c0 < jb.n_total; c0 += 32) {
           uint32_t v[32];
           tmem_ld32(tcol + c0, v);
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 32; ++i) sum += __uint_as_float(v[i]);
         }
-        const float mean = sum / static_cast<float>(jb.n_tile);
+        const float mean = sum / static_cast<float>(jb.n_total);
         float ss = 0.f;
-        for (int c0 = 0; c0 < jb.n_tile; c0 += 32) {
+        for (int c0 = 0; c0 < jb.n_total; c0 += 32) {
           uint32_t v[32];
           tmem_ld32(tcol + c0, v);
           tmem_ld_wait();
@@ -178,8 +181,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
             ss = fmaf(d, d, ss);
           }
         }
-        const float rstd = rsqrtf(ss / static_cast<float>(jb.n_tile) + jb.eps);
-        for (int c0 = 0; c0 < jb.n_tile; c0 += 32) {
+        const float rstd = rsqrtf(ss / static_cast<float>(jb.n_total) + jb.eps);
+        for (int c0 = 0; c0 < jb.n_total; c0 += 32) {
           uint32_t v[32];
           tmem_ld32(tcol + c0, v);
           tmem_ld_wait();
@@ -198,6 +201,16 @@ __global__ void __launch_bounds__(kPThreads, 1)
             for (int q = 0; q < 4; ++q) dst[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
           }
         }
+        // the stacked head-weight columns: fp32, possibly fewer than 32 (H_I < 32)
+        for (int c0 = jb.n_total; c0 < jb.n_total + jb.n2; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld32(tcol + c0, v);
+          tmem_ld_wait();
+          if (!live) continue;
+          float* dst = jb.out2 + static_cast<size_t>(token) * jb.n2 + (c0 - jb.n_total);
+          const int n = min(32, jb.n_total + jb.n2 - c0);
+          for (int i = 0; i < n; ++i) dst[i] = __uint_as_float(v[i]);
+        }
       } else {
         for (int c0 = 0; c0 < jb.n_tile; c0 += 32) {
           uint32_t v[32];
@@ -205,20 +218,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
           tmem_ld_wait();
           const int col = p.n0 + c0;
           if (!live || col >= jb.n_total) continue;
-          if (jb.epi == kProjEpiBf16) {
-            uint32_t o[16];
+          uint32_t o[16];
 #pragma unroll
-            for (int i = 0; i < 32; i += 2) o[i / 2] = pack_bf16x2(__uint_as_float(v[i]), __uint_as_float(v[i + 1]));
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(jb.out) +
-                                                  static_cast<size_t>(token) * jb.n_total + col);
+          for (int i = 0; i < 32; i += 2) o[i / 2] = pack_bf16x2(__uint_as_float(v[i]), __uint_as_float(v[i + 1]));
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(jb.out) +
+                                                static_cast<size_t>(token) * jb.n_total + col);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) dst[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
-          } else {
-            // fp32 columns, possibly fewer than 32 left in a narrow matrix (H_I < 32)
-            float* dst = static_cast<float*>(jb.out) + static_cast<size_t>(token) * jb.n_total + col;
-            const int n = min(32, jb.n_total - col);
-            for (int i = 0; i < n; ++i) dst[i] = __uint_as_float(v[i]);
-          }
+          for (int q = 0; q < 4; ++q) dst[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
         }
       }
       tc_fence_before();
@@ -234,20 +240,21 @@ __global__ void __launch_bounds__(kPThreads, 1)
 
 }  // namespace
 
-cudaError_t launch_projections(const CUtensorMap* ta, const CUtensorMap* tb, const ProjJobs& J, int n_tokens,
-                               uint32_t* status, cudaStream_t st) {
+cudaError_t launch_projections(const CUtensorMap* ta, const CUtensorMap* tb, const CUtensorMap& tb2,
+                               const ProjJobs& J, int n_tokens, uint32_t* status, cudaStream_t st) {
   if (n_tokens <= 0 || J.first_unit[J.n_jobs] <= 0) return cudaSuccess;
+  if (J.n_jobs != 2) return cudaErrorInvalidValue;
   for (int j = 0; j < J.n_jobs; ++j) {
     const ProjJob& jb = J.job[j];
     if (jb.k <= 0 || jb.k % 64 || jb.n_tile < 32 || jb.n_tile > kPMaxN || jb.n_tile % 32 ||
-        (jb.epi == kProjEpiLayerNorm && jb.n_tile != jb.n_total))
+        (jb.epi == kProjEpiLayerNormF32 && (jb.n_total % 32 || jb.n_tile < jb.n_total + jb.n2)))
       return cudaErrorInvalidValue;
   }
   cudaError_t e = cudaFuncSetAttribute(proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPDynSmem);
   if (e != cudaSuccess) return e;
   const int units = J.first_unit[J.n_jobs];
   const int grid = units < device_sm_count() ? units : device_sm_count();
-  proj_kernel<<<grid, kPThreads, kPDynSmem, st>>>(ta[0], tb[0], ta[1], tb[1], ta[2], tb[2], J, n_tokens, status);
+  proj_kernel<<<grid, kPThreads, kPDynSmem, st>>>(ta[0], tb[0], ta[1], tb[1], tb2, J, n_tokens, status);
   return cudaGetLastError();
 }
 
