@@ -109,7 +109,7 @@ typedef struct dsa_indexer_desc {
 dsa_status dsa_indexer_workspace_size(const dsa_indexer_desc* desc, size_t* bytes);
 
 /* Lightning indexer with a fused streaming causal top-k ([EX] section 1: score the prefix
- * tokens of every query and keep the top-k positions; spec formula):
+ * tokens of every query and keep the top-k positions; the score of the problem statement):
  *
  *   s[t, j] = sum_h w[t, h] * max(0, rope(q_idx[t, h]) . rope(k_idx[j]))   j in [ks_t, ke_t)
  *
