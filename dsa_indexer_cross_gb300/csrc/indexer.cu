@@ -17,13 +17,16 @@
 // Streaming top-k.  Per (row, chunk) the kernel keeps a candidate buffer of `cap` entries
 // (order-preserving score key, key index) in the workspace and a running threshold tau in
 // shared memory.  A score is appended only when it beats tau.  When a buffer could
-// overflow on the next tile the 128 epilogue threads cut it back to exactly its top-k by
-// (score desc, index asc) and raise tau to the k-th key.  Keys of a unit are visited in
-// increasing index order, so "beats tau" is a strict comparison.
+// overflow on the next tile the epilogue threads cut it back to a superset of its top-k (one
+// binned pass, exact radix select when the boundary bin is crowded) and raise tau to the
+// smallest kept key.  Keys of a unit are visited in increasing index order, so "beats tau" is
+// a strict comparison.
 //
-// Warp roles (192 threads): warp 0 = TMA producer, warp 1 = MMA issuer (owns TMEM),
-// warps 2..5 = epilogue (TMEM lane quarters 2, 3, 0, 1).  Q is single-buffered per unit,
-// K tiles go through a STAGES-deep ring, S^T is double-buffered in TMEM.
+// Warp roles: warp 0 = TMA producer, warp 1 = MMA issuer (owns TMEM), then the epilogue:
+// warps 2..5 (TMEM lane quarters 2, 3, 0, 1), and with several queries per group warps 6..9
+// as a second half that takes the other half of the queries (192 or 320 threads).  Q is
+// single-buffered per unit, K tiles go through a STAGES-deep ring, S^T is double-buffered in
+// TMEM.
 #include <cuda_bf16.h>
 
 #include <cstddef>

@@ -23,7 +23,9 @@
 //
 // Two ways to walk the rows (template parameter HD):
 //   HD == 0  "gather": item = (token, block of HB heads); the tile holds the token's next
-//            64 selected rows, fetched with cp.async (zero-filled for -1 / out-of-range).
+//            64 selected rows, fetched as four-row TMA gathers plus cp.async for the last
+//            blocks (an empty slot reads row 0 or zeros and is masked); a paged cache maps
+//            each offset through the token's block table (template parameter PAGED).
 //   HD  > 0  "block-dense": item = HB / HD consecutive tokens with all HD heads; the tile is
 //            64 CONSECUTIVE latent rows of the block's key range, fetched by TMA, and a
 //            per-(token, row) selection bitmask built from the index rows masks S^T.  Used
