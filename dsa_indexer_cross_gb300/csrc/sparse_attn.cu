@@ -40,12 +40,13 @@
 // TMEM shape, so each thread holds two rows and HB/4 columns; running sums stay in registers
 // and are reduced once per item.
 //
-// Warp roles (256 threads): warps 0-1 load Q and the rows (Q as nine 64-dim TMA boxes; the
-// rows as one 3-D TMA box per tile in block-dense mode, or as four-row TMA gathers plus
-// cp.async for the last blocks in the gather walk); warp 2 issues the S^T products; warps 3-6 run the softmax and the
-// epilogue; warp 7 owns TMEM and issues the PV products.  With the two products issued from separate warps, PV(g) goes out as soon as
-// P(g) exists instead of queueing behind S^T(g+1), whose blocks may still be in flight.
-// Persistent CTAs.
+// Warp roles: warps 0-1 load Q and the rows (Q as nine 64-dim TMA boxes; the rows as one
+// 3-D TMA box per tile in block-dense mode, or as four-row TMA gathers plus cp.async for the
+// last blocks in the gather walk); warp 2 issues the S^T products; warps 3-6 (and 8-11 in
+// the block-dense walk) run the softmax and the epilogue; warp 7 owns TMEM and issues the PV
+// products (256 threads, 384 block-dense).  With the two products issued from separate
+// warps, PV(g) goes out as soon as P(g) exists instead of queueing behind S^T(g+1), whose
+// blocks may still be in flight.  Persistent CTAs.
 #include <cuda_bf16.h>
 
 #include "kernels.h"
