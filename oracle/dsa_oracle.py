@@ -347,3 +347,42 @@ def indexer_projections(x: np.ndarray, q_latent: np.ndarray, wq_b: np.ndarray, w
     k = round_to_bf16((y - mu) / np.sqrt(var + eps) * np.asarray(k_norm_w, np.float64) + np.asarray(k_norm_b, np.float64))
     w = np.asarray(x, np.float64) @ np.asarray(w_proj, np.float64).T
     return q, k, w
+
+
+def sparse_attn_backward(q: np.ndarray, kv: np.ndarray, idx: np.ndarray, ks: np.ndarray, scale: float,
+                         d_o: np.ndarray, d_lse: np.ndarray | None = None, d_v: int = 512):
+    """Gradients of the sparse attention above with respect to q and the latent rows.
+
+    Differentiates exactly what sparse_attn computes (no page prints a backward; the training
+    pages only name the backward kernels): for token t, head h and selected rows j,
+        s_j = scale q . kv_j,  p_j = exp(s_j - lse),  o = sum_j p_j kv_j[:d_v],
+    given the upstream d_o (and d_lse, optional):
+        dp_j = d_o . kv_j[:d_v],  D = sum_j p_j dp_j,  ds_j = p_j (dp_j - D + d_lse),
+        dq += scale sum_j ds_j kv_j,
+        dkv_j += scale ds_j q  (+ p_j d_o on the first d_v dims),
+    summed over every (token, head) that selects row j.  Returns (dq [T, H, D], dkv [n_kv, D]).
+    """
+    q = np.asarray(q, np.float64)
+    kv = np.asarray(kv, np.float64)
+    T, H, Dq = q.shape
+    dq = np.zeros_like(q)
+    dkv = np.zeros_like(kv)
+    for t in range(T):
+        sel = idx[t][idx[t] >= 0]
+        if sel.size == 0:
+            continue
+        rows = int(ks[t]) + sel
+        K = kv[rows]                                    # [n, D]
+        s = scale * (q[t] @ K.T)                        # [H, n]
+        m = s.max(axis=1, keepdims=True)
+        p = np.exp(s - m)
+        p /= p.sum(axis=1, keepdims=True)               # = exp(s - lse)
+        dp = np.asarray(d_o[t], np.float64) @ K[:, :d_v].T   # [H, n]
+        D = (p * dp).sum(axis=1, keepdims=True)
+        g = 0.0 if d_lse is None else np.asarray(d_lse[t], np.float64)[:, None]
+        ds = p * (dp - D + g)
+        dq[t] = scale * ds @ K
+        contrib = scale * ds.T @ q[t]                   # [n, D]
+        contrib[:, :d_v] += p.T @ np.asarray(d_o[t], np.float64)
+        np.add.at(dkv, rows, contrib)
+    return dq, dkv

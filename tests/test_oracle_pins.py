@@ -376,3 +376,47 @@ def test_projections_layer_norm_matches_torch_and_closed_forms():
     wk2 = np.ones((d, D))
     _, k2, _ = O.indexer_projections(x2 + 1.0, ql[:1], wq, wk2, g, b, wp, H, d, eps)
     np.testing.assert_allclose(k2[0], O.round_to_bf16(b), rtol=0, atol=0)
+
+
+# ---------------------------------------------------------------------------- attention backward
+
+def test_sparse_attn_backward_matches_finite_differences():
+    # central differences of L = sum d_o . o + sum d_lse . lse through the forward oracle; rows
+    # shared by several tokens (the scatter of dkv) and -1 padding included
+    rng = np.random.default_rng(41)
+    T, H, D, dv, n_kv, k = 4, 2, 12, 8, 9, 5
+    q = rng.standard_normal((T, H, D))
+    kv = rng.standard_normal((n_kv, D))
+    ks = np.array([0, 1, 2, 0])
+    idx = np.full((T, k), -1)
+    for t in range(T):
+        L = int(rng.integers(2, k + 1))
+        idx[t, :L] = np.sort(rng.choice(n_kv - ks[t], size=L, replace=False))
+    d_o = rng.standard_normal((T, H, dv))
+    d_lse = rng.standard_normal((T, H))
+    scale = 0.4
+
+    def loss(q_, kv_):
+        o, lse = O.sparse_attn(q_, kv_, idx, ks, scale, d_v=dv)
+        return float((d_o * o).sum() + (d_lse * lse).sum())
+
+    dq, dkv = O.sparse_attn_backward(q, kv, idx, ks, scale, d_o, d_lse, d_v=dv)
+    h = 1e-6
+    fq = np.zeros_like(q)
+    for i in np.ndindex(q.shape):
+        qp, qm = q.copy(), q.copy()
+        qp[i] += h
+        qm[i] -= h
+        fq[i] = (loss(qp, kv) - loss(qm, kv)) / (2 * h)
+    fk = np.zeros_like(kv)
+    for i in np.ndindex(kv.shape):
+        kp, km = kv.copy(), kv.copy()
+        kp[i] += h
+        km[i] -= h
+        fk[i] = (loss(q, kp) - loss(q, km)) / (2 * h)
+    np.testing.assert_allclose(dq, fq, rtol=1e-6, atol=1e-7)
+    np.testing.assert_allclose(dkv, fk, rtol=1e-6, atol=1e-7)
+    # a row no token selects gets no gradient
+    unused = sorted(set(range(n_kv)) - {int(ks[t]) + int(j) for t in range(T) for j in idx[t] if j >= 0})
+    for r in unused:
+        assert not dkv[r].any()
