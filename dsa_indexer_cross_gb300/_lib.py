@@ -29,7 +29,7 @@ EXPORTED = ("dsa_status_string", "dsa_last_error", "dsa_donor_table", "dsa_rope_
             "dsa_index_cache_donor", "dsa_index_cache_indices", "dsa_index_cache_destroy",
             "dsa_layers_workspace_size", "indexshare_layers_forward", "dsa_workspace_status",
             "dsa_indexer_topk_static", "dsa_profile_enable", "dsa_profile_indexer_last", "dsa_mtp_indexshare_step",
-            "dsa_indexer_topk_paged", "dsa_sparse_attn_paged", "dsa_indexer_projections")
+            "dsa_indexer_topk_paged", "dsa_sparse_attn_paged", "dsa_indexer_projections", "dsa_sparse_attn_backward")
 
 
 class DsaError(RuntimeError):
@@ -102,6 +102,8 @@ def lib() -> C.CDLL:
         L.dsa_profile_indexer_last.argtypes = [P(C.c_float), i32]
         L.dsa_indexer_topk_static.restype = st
         L.dsa_indexer_topk_static.argtypes = [P(IndexerDesc), vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp]
+        L.dsa_sparse_attn_backward.restype = st
+        L.dsa_sparse_attn_backward.argtypes = [P(AttnDesc), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.dsa_indexer_projections.restype = st
         L.dsa_indexer_projections.argtypes = [P(ProjDesc), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.dsa_indexer_topk_paged.restype = st
@@ -281,6 +283,15 @@ def indexshare_layers_forward(idesc: IndexerDesc, adesc: AttnDesc, indexer_types
     _check(lib().indexshare_layers_forward(C.byref(idesc), C.byref(adesc), len(types), _u8(types), io, _ptr(ks),
                                            _ptr(ke), _ptr(q_pos), _ptr(k_pos), _ptr(rope_cs), n_pos, cache.handle,
                                            _ptr(ws), ws.numel(), _stream(stream)))
+    return ws
+
+
+def dsa_sparse_attn_backward(desc: AttnDesc, q, kv, idx, ks, out, lse, d_out, dq, dkv, ws=None, stream=None):
+    """dq (written) and dkv (zeroed, then accumulated), fp32, for the upstream gradient d_out."""
+    if ws is None:
+        ws = torch.zeros(256, dtype=torch.uint8, device=q.device)
+    _check(lib().dsa_sparse_attn_backward(C.byref(desc), _ptr(q), _ptr(kv), _ptr(idx), _ptr(ks), _ptr(out), _ptr(lse),
+                                          _ptr(d_out), _ptr(dq), _ptr(dkv), _ptr(ws), ws.numel(), _stream(stream)))
     return ws
 
 

@@ -716,6 +716,29 @@ dsa_status dsa_indexer_projections(const dsa_proj_desc* d, const void* x, const 
   return DSA_OK;
 }
 
+dsa_status dsa_sparse_attn_backward(const dsa_attn_desc* desc, const void* q, const void* kv, const int32_t* idx,
+                                    const int32_t* ks, const void* out, const float* lse, const void* d_out,
+                                    float* dq, float* dkv, void* ws, size_t ws_bytes, void* stream) {
+  dsa_status s = check_attn_desc(desc);
+  if (s != DSA_OK) return s;
+  if (!q || !kv || !idx || !ks || !out || !lse || !d_out || !dq || !dkv || !ws)
+    return fail(DSA_ERR_ARG, "every tensor and ws must be non-NULL");
+  if (reinterpret_cast<uintptr_t>(ws) % kAlign) return fail(DSA_ERR_ARG, "workspace must be 256-byte aligned");
+  if (ws_bytes < kAlign) return fail(DSA_ERR_WORKSPACE, "backward workspace too small: %zu < %zu bytes", ws_bytes, kAlign);
+  if ((s = check_device()) != DSA_OK) return s;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if ((e = cudaMemsetAsync(ws, 0, kAlign, st)) != cudaSuccess) return cuda_fail(e, "clear status");
+  if (desc->n_kv > 0 &&
+      (e = cudaMemsetAsync(dkv, 0, static_cast<size_t>(desc->n_kv) * 576 * sizeof(float), st)) != cudaSuccess)
+    return cuda_fail(e, "clear dkv");
+  if (desc->n_q == 0) return DSA_OK;
+  e = launch_sparse_attn_bwd(desc->n_q, desc->n_kv, desc->n_heads, desc->topk, desc->softmax_scale, q, kv, idx, ks, out,
+                             lse, d_out, dq, dkv, static_cast<uint32_t*>(ws), st);
+  if (e != cudaSuccess) return cuda_fail(e, "sparse attention backward");
+  return DSA_OK;
+}
+
 dsa_status dsa_workspace_status(const void* ws, void* stream, uint32_t* device_bits) {
   if (!ws) return fail(DSA_ERR_ARG, "workspace is NULL");
   WsHeader h{};

@@ -116,6 +116,14 @@ struct ProjJobs {
 cudaError_t launch_projections(const CUtensorMap* ta, const CUtensorMap* tb, const CUtensorMap& tb2,
                                const ProjJobs& J, int n_tokens, uint32_t* status, cudaStream_t st);
 
+// ---------------------------------------------------------------------------- attention backward
+// dq [n_q][H][576] fp32 (written), dkv [n_kv][576] fp32 (accumulated: zero it first), given the
+// forward's out (bf16) and lse (fp32) and the upstream gradient dout [n_q][H][512] bf16.
+cudaError_t launch_sparse_attn_bwd(int n_q, int n_kv, int n_heads, int topk, float scale, const void* q,
+                                   const void* kv, const int32_t* idx, const int32_t* ks, const void* out,
+                                   const float* lse, const void* dout, float* dq, float* dkv, uint32_t* status,
+                                   cudaStream_t st);
+
 int device_sm_count();
 
 }  // namespace dsa

@@ -277,6 +277,22 @@ dsa_status dsa_indexer_projections(const dsa_proj_desc* desc, const void* x, con
                                    const void* weights_proj, void* q_idx, void* k_idx, float* w, void* ws,
                                    size_t ws_bytes, void* stream);
 
+/* ------------------------------------------------------------------ training ------- */
+
+/* Gradients of dsa_sparse_attn (the training pages name the backward kernels only; this is the
+ * exact gradient of the forward above).  With p_j = exp(tau q . kv_j - lse) and D = d_out . out:
+ *   dq[t, h]  = tau sum_j p_j (d_out . kv_j[:512] - D) kv_j
+ *   dkv[row] += tau p_j (d_out . kv_j[:512] - D) q[t, h] + p_j d_out[t, h] (first 512 dims)
+ * summed over every (t, h) selecting the row.  Inputs as in dsa_sparse_attn plus the forward's
+ * out [n_q][n_heads][512] bf16 and lse [n_q][n_heads] fp32, and d_out [n_q][n_heads][512]
+ * bf16.  Outputs fp32: dq [n_q][n_heads][576] (written) and dkv [n_kv][576] (zeroed here, then
+ * accumulated).  A first version on the CUDA cores (dkv by atomic adds), far slower than the
+ * forward.  ws: at least 256 bytes, 256-byte aligned (status word).  Errors: DSA_ERR_ARG,
+ * DSA_ERR_UNSUPPORTED (d_qk != 576 or d_v != 512), DSA_ERR_WORKSPACE, DSA_ERR_CUDA. */
+dsa_status dsa_sparse_attn_backward(const dsa_attn_desc* desc, const void* q, const void* kv, const int32_t* idx,
+                                    const int32_t* ks, const void* out, const float* lse, const void* d_out,
+                                    float* dq, float* dkv, void* ws, size_t ws_bytes, void* stream);
+
 /* ------------------------------------------------------------------ paged caches ---- */
 
 /* Paged decode caches (a serving layout; the pages describe per-query key ranges only -- the
