@@ -723,6 +723,8 @@ dsa_status dsa_sparse_attn_backward(const dsa_attn_desc* desc, const void* q, co
   if (s != DSA_OK) return s;
   if (!q || !kv || !idx || !ks || !out || !lse || !d_out || !dq || !dkv || !ws)
     return fail(DSA_ERR_ARG, "every tensor and ws must be non-NULL");
+  if (!aligned16(q) || !aligned16(kv) || !aligned16(out) || !aligned16(d_out) || !aligned16(dq) || !aligned16(dkv))
+    return fail(DSA_ERR_ARG, "q, kv, out, d_out, dq and dkv must be 16-byte aligned");
   if (reinterpret_cast<uintptr_t>(ws) % kAlign) return fail(DSA_ERR_ARG, "workspace must be 256-byte aligned");
   if (ws_bytes < kAlign) return fail(DSA_ERR_WORKSPACE, "backward workspace too small: %zu < %zu bytes", ws_bytes, kAlign);
   if ((s = check_device()) != DSA_OK) return s;
