@@ -225,3 +225,22 @@ def test_paged_calls_reject_bad_layouts_before_launch():
     assert L.dsa_sparse_attn_paged(C.byref(adesc), fake, fake, fake, C.byref(short), fake, None, fake, 1 << 30,
                                    None) == 2
     assert L.dsa_sparse_attn_paged(C.byref(adesc), fake, fake, fake, None, fake, None, fake, 1 << 30, None) == 1
+
+
+def test_attention_backward_argument_errors_before_launch():
+    # NULL tensors, misaligned tensors, a misaligned or short status workspace and a bad
+    # descriptor are rejected on the host (fake pointers are never dereferenced)
+    L = _lib.lib()
+    adesc = D.attn_desc(4, 256, 16, 32, 1 / 24.0)
+    fake = 0x100000
+    t = [fake] * 9                                  # q kv idx ks out lse d_out dq dkv
+    ok = L.dsa_sparse_attn_backward
+    assert ok(C.byref(adesc), *t[:8], None, fake, 256, None) == 1
+    for i in (0, 1, 4, 6, 7, 8):                    # the bf16 / fp32 tensors read or written in 16-byte pieces
+        bad = list(t)
+        bad[i] = fake + 8
+        assert ok(C.byref(adesc), *bad, fake, 256, None) == 1
+        assert "aligned" in L.dsa_last_error().decode()
+    assert ok(C.byref(adesc), *t, fake + 16, 256, None) == 1
+    assert ok(C.byref(adesc), *t, fake, 128, None) == 6
+    assert ok(C.byref(D.attn_desc(4, 256, 16, 32, 1 / 24.0, d_qk=192)), *t, fake, 256, None) == 4
