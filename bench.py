@@ -49,6 +49,9 @@ def parse():
     ap.add_argument("--proj", action="store_true",
                     help="also time the indexer's input projections (wq_b, wk + k_norm, weights_proj) for the "
                          "workload's query rows, hidden width 6144 and query latent 2048, under 'proj'")
+    ap.add_argument("--bwd", action="store_true",
+                    help="also time the sparse-attention backward (dq, dkv) of the first layer for a seeded "
+                         "upstream gradient, under 'bwd'")
     ap.add_argument("--paged", action="store_true",
                     help="decode workloads: also time the paged-cache indexer and attention (128-row pages, "
                          "shuffled) against the contiguous calls on the same data, under 'paged'")
@@ -338,6 +341,39 @@ def time_proj(D, w, dev, stream, flush, tc_peak, d_hidden: int = 6144, d_q: int 
             "note": "synthetic weights; widths assumed (the pages give none)"}
 
 
+# --------------------------------------------------------------------------- backward
+def time_bwd(D, w, adesc, L0, idx, ks, attn_ms, flops_fwd, dev, stream, flush, tc_peak, reps: int = 5):
+    """Median time of dsa_sparse_attn_backward on one layer (the forward's own out and lse, a
+    seeded d_out), L2 flushed before each call.  FLOPs: 2.5x the forward's (S and dP recomputed,
+    then dQ, dS^T Q and P^T dO)."""
+    g = torch.Generator(device=dev)
+    g.manual_seed(5)
+    d_out = torch.randn(L0["out"].shape, generator=g, device=dev).to(torch.bfloat16)
+    dq = torch.empty((w.n_q, w.n_heads, w.d_qk), dtype=torch.float32, device=dev)
+    dkv = torch.empty((adesc.n_kv, w.d_qk), dtype=torch.float32, device=dev)
+    ws = torch.zeros(256, dtype=torch.uint8, device=dev)
+    D.dsa_sparse_attn(adesc, L0["q"], L0["kv"], idx, ks, L0["out"], L0["lse"], stream=stream)
+    call = lambda: D.dsa_sparse_attn_backward(adesc, L0["q"], L0["kv"], idx, ks, L0["out"], L0["lse"], d_out, dq, dkv,
+                                              ws=ws, stream=stream)
+    call()
+    ms = []
+    for _ in range(reps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        call()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms.append(a.elapsed_time(b))
+    if D.dsa_workspace_status(ws) != 0:
+        raise RuntimeError("device status set by the backward")
+    m = statistics.median(ms)
+    flops = 2.5 * flops_fwd
+    return {"ms": m, "forward_ms": attn_ms, "flops": flops, "tflops": flops / (m / 1e3) / 1e12,
+            "frac_of_bf16_peak": flops / (m / 1e3) / 1e12 / tc_peak,
+            "kernel": "sparse_attn_bwd_kernel (bf16 warp-level MMAs, dkv by float2 atomics)"}
+
+
 # --------------------------------------------------------------------------- paged caches
 def time_paged(D, synth, w, geo, L0, idx_full, attn_ms_contig, idx_ms_contig, dev, stream, flush, reps: int = 20,
                seed: int = 3):
@@ -598,6 +634,9 @@ def run_native(args):
     }
     if args.proj:
         line["proj"] = time_proj(D, w, dev, stream, flush, tc_burst)
+    if args.bwd:
+        line["bwd"] = time_bwd(D, w, adesc, layers[0], idx_full, ks, attn_ms, R["attn_flops"], dev, stream, flush,
+                               tc_burst)
     if args.paged and w.kind == "decode":
         line["paged"] = time_paged(D, synth, w, geo, layers[0], idx_full, attn_ms, idx_ms, dev, stream, flush)
     if args.mtp_steps > 0 and w.kind == "decode":
