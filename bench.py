@@ -371,7 +371,7 @@ def time_bwd(D, w, adesc, L0, idx, ks, attn_ms, flops_fwd, dev, stream, flush, t
     flops = 2.5 * flops_fwd
     return {"ms": m, "forward_ms": attn_ms, "flops": flops, "tflops": flops / (m / 1e3) / 1e12,
             "frac_of_bf16_peak": flops / (m / 1e3) / 1e12 / tc_peak,
-            "kernel": "sparse_attn_bwd_kernel (bf16 warp-level MMAs, dkv by float2 atomics)"}
+            "kernel": "sparse_attn_bwd_kernel (bf16 warp-level MMAs, dkv by 16-byte atomics)"}
 
 
 # --------------------------------------------------------------------------- paged caches

@@ -15,7 +15,7 @@
 //   A  S = Q KV^T and dP = dO V^T (HB heads x 64 rows; K = 576 and 512), then P and
 //      dS' = tau dS in registers, stored to shared memory in bf16;
 //   B  dQ += dS' KV (HB x 576, K = 64 rows), held in registers across chunks;
-//   C  dKV = dS'^T Q + P^T dO (64 rows x 576, K = HB heads), added to HBM with float2 atomics
+//   C  dKV = dS'^T Q + P^T dO (64 rows x 576, K = HB heads), added to HBM with 16-byte atomics
 //      (a row is selected by many tokens).
 // Shared-memory rows are padded by 16 bytes so the eight row addresses of every ldmatrix fall
 // in distinct bank groups.  No wait in this kernel spins: its only synchronisation is
@@ -264,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_bwd_kernel(
       }
     }
 
-    // ---- C: dKV for chunk rows 16 mc.. x dims 288 nc.., scattered with float2 atomics
+    // ---- C: dKV for chunk rows 16 mc.. x dims 288 nc.., scattered with 16-byte atomics
     {
       const int mc = warp & 3, nc = warp >> 2;
       const int i4 = lane >> 3;
@@ -298,11 +298,18 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_bwd_kernel(
             mma16816(o[1], ap[kk], bb[2], bb[3]);
           }
         }
+        // lanes tig and tig ^ 1 swap halves so that each holds four consecutive dims of one
+        // row (even tig: row ra, dims 2 tig..+3; odd: row ra + 8, dims 2 tig - 2..+3), then one
+        // 16-byte atomic add each
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-          const int d = d0 + j * 8 + 2 * tig;
-          if (row_a >= 0) atomicAdd(reinterpret_cast<float2*>(dkv + row_a * kDq + d), make_float2(o[j][0], o[j][1]));
-          if (row_b >= 0) atomicAdd(reinterpret_cast<float2*>(dkv + row_b * kDq + d), make_float2(o[j][2], o[j][3]));
+          const bool odd = tig & 1;
+          const float y0 = __shfl_xor_sync(0xffffffffu, odd ? o[j][0] : o[j][2], 1);
+          const float y1 = __shfl_xor_sync(0xffffffffu, odd ? o[j][1] : o[j][3], 1);
+          const int d = d0 + j * 8 + 2 * (tig & 2);
+          const long long row = odd ? row_b : row_a;
+          const float4 v = odd ? make_float4(y0, y1, o[j][2], o[j][3]) : make_float4(o[j][0], o[j][1], y0, y1);
+          if (row >= 0) atomicAdd(reinterpret_cast<float4*>(dkv + row * kDq + d), v);
         }
       }
     }

@@ -286,7 +286,7 @@ dsa_status dsa_indexer_projections(const dsa_proj_desc* desc, const void* x, con
  * summed over every (t, h) selecting the row.  Inputs as in dsa_sparse_attn plus the forward's
  * out [n_q][n_heads][512] bf16 and lse [n_q][n_heads] fp32, and d_out [n_q][n_heads][512]
  * bf16.  Outputs fp32: dq [n_q][n_heads][576] (written) and dkv [n_kv][576] (zeroed here, then
- * accumulated; rows shared by several tokens receive float2 atomic adds, so the order of the
+ * accumulated; rows shared by several tokens receive atomic adds, so the order of the
  * additions, and the last bits of dkv, vary from run to run).  All tensors 16-byte aligned.
  * Out-of-range indices are counted in the status word and skipped.
  * ws: at least 256 bytes, 256-byte aligned (status word).  Errors: DSA_ERR_ARG,
