@@ -320,7 +320,7 @@ dsa_status check_attn_desc(const dsa_attn_desc* d) {
   if (!d) return fail(DSA_ERR_ARG, "attention descriptor is NULL");
   if (d->n_q < 0 || d->n_kv < 0) return fail(DSA_ERR_ARG, "n_q and n_kv must be >= 0");
   if (d->d_qk != 576 || d->d_v != 512)
-    return fail(DSA_ERR_UNSUPPORTED, "d_qk/d_v %d/%d: this build supports 576/512", d->d_qk, d->d_v);
+    return fail(DSA_ERR_UNSUPPORTED, "d_qk/d_v %d/%d: this library supports 576/512", d->d_qk, d->d_v);
   if (d->n_heads < 1 || d->n_heads > 128) return fail(DSA_ERR_UNSUPPORTED, "n_heads %d outside 1..128", d->n_heads);
   if (d->topk < 1) return fail(DSA_ERR_ARG, "topk must be >= 1");
   if (!(d->softmax_scale > 0.f) || !std::isfinite(d->softmax_scale))
@@ -625,7 +625,7 @@ namespace {
 dsa_status check_pages(const dsa_paged_cache* pc, int32_t n_kv, PagedRows* pg) {
   if (!pc || !pc->block_table || !pc->seq_len) return fail(DSA_ERR_ARG, "paged cache: block_table and seq_len must be non-NULL");
   if (pc->page_rows != kPageRows)
-    return fail(DSA_ERR_UNSUPPORTED, "page_rows %d: this build supports %d-row pages", pc->page_rows, kPageRows);
+    return fail(DSA_ERR_UNSUPPORTED, "page_rows %d: this library supports %d-row pages", pc->page_rows, kPageRows);
   if (pc->max_pages < 1 || pc->n_pages < 1) return fail(DSA_ERR_ARG, "max_pages and n_pages must be >= 1");
   if (static_cast<long long>(pc->n_pages) * kPageRows != n_kv)
     return fail(DSA_ERR_SHAPE, "n_kv %d must equal n_pages * page_rows = %lld", n_kv,

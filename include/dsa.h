@@ -46,7 +46,7 @@ typedef enum dsa_status {
   DSA_ERR_ARG = 1,         /* a NULL or misaligned pointer, or a value out of range        */
   DSA_ERR_SHAPE = 2,       /* sizes that are inconsistent with each other                  */
   DSA_ERR_NO_DONOR = 3,    /* a shared layer precedes every full layer                     */
-  DSA_ERR_UNSUPPORTED = 4, /* a valid size this build has no kernel for, or no sm_10x GPU  */
+  DSA_ERR_UNSUPPORTED = 4, /* a valid size this library has no kernel for, or no sm_10x GPU */
   DSA_ERR_CUDA = 5,        /* a CUDA runtime call failed (message in dsa_last_error)       */
   DSA_ERR_WORKSPACE = 6,   /* ws_bytes smaller than the *_workspace_size query             */
   DSA_ERR_TIMEOUT = 7,     /* a device pipeline wait ran past its bound                    */
