@@ -420,3 +420,48 @@ def test_sparse_attn_backward_matches_finite_differences():
     unused = sorted(set(range(n_kv)) - {int(ks[t]) + int(j) for t in range(T) for j in idx[t] if j >= 0})
     for r in unused:
         assert not dkv[r].any()
+
+
+def test_sparse_attn_backward_single_row_closed_form():
+    # one selected row: p = 1 and D = dp, so ds = d_lse exactly; with no d_lse dq vanishes and
+    # the row's value dims receive d_o summed over heads
+    rng = np.random.default_rng(43)
+    T, H, D, dv, n_kv = 3, 4, 10, 6, 7
+    q = rng.standard_normal((T, H, D))
+    kv = rng.standard_normal((n_kv, D))
+    ks = np.array([0, 2, 1])
+    idx = np.array([[3, -1, -1], [0, -1, -1], [5, -1, -1]])
+    d_o = rng.standard_normal((T, H, dv))
+    d_lse = rng.standard_normal((T, H))
+    scale = 0.7
+    dq, dkv = O.sparse_attn_backward(q, kv, idx, ks, scale, d_o, d_v=dv)
+    np.testing.assert_allclose(dq, 0.0, atol=1e-12)
+    want = np.zeros_like(kv)
+    for t in range(T):
+        want[ks[t] + idx[t, 0], :dv] += d_o[t].sum(axis=0)
+    np.testing.assert_allclose(dkv, want, atol=1e-12)
+    dq, dkv = O.sparse_attn_backward(q, kv, idx, ks, scale, d_o, d_lse, d_v=dv)
+    for t in range(T):
+        r = ks[t] + idx[t, 0]
+        np.testing.assert_allclose(dq[t], scale * d_lse[t][:, None] * kv[r][None, :], atol=1e-12)
+        want[r] += scale * d_lse[t] @ q[t]
+    np.testing.assert_allclose(dkv, want, atol=1e-12)
+
+
+def test_sparse_attn_backward_identical_rows_closed_form():
+    # n selected rows with equal contents: p = 1/n and dp_j = D for every j, so ds = 0: dq
+    # vanishes and each row receives d_o / n (summed over heads) on its value dims only
+    rng = np.random.default_rng(44)
+    H, D, dv, n = 3, 10, 6, 4
+    q = rng.standard_normal((1, H, D))
+    row = rng.standard_normal(D)
+    kv = np.tile(row, (n + 2, 1))
+    idx = np.array([[0, 2, 3, 5]])
+    d_o = rng.standard_normal((1, H, dv))
+    dq, dkv = O.sparse_attn_backward(q, kv, idx, np.array([0]), 0.5, d_o, d_v=dv)
+    np.testing.assert_allclose(dq, 0.0, atol=1e-12)
+    for r in range(n + 2):
+        want = np.zeros(D)
+        if r in (0, 2, 3, 5):
+            want[:dv] = d_o[0].sum(axis=0) / n
+        np.testing.assert_allclose(dkv[r], want, atol=1e-12)
