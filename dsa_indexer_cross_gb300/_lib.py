@@ -123,11 +123,24 @@ def _check(status: int) -> None:
 
 
 def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    """Device address of a contiguous CUDA tensor (every tensor argument of libdsa's GPU calls is
+    device memory; a host tensor is refused here rather than handed to a kernel)."""
     if t is None:
         return None
+    if not t.is_cuda:
+        raise ValueError("tensors passed to libdsa must be CUDA tensors (device memory)")
     if not t.is_contiguous():
         raise ValueError("tensors passed to libdsa must be contiguous")
     return t.data_ptr()
+
+
+def _want(t: torch.Tensor, dtype, numel: int, name: str) -> None:
+    """Refuse a tensor of the wrong type or too few elements before its address reaches a kernel
+    (the C ABI takes bare pointers and cannot check either)."""
+    if t.dtype != dtype:
+        raise ValueError(f"{name}: expected {dtype}, got {t.dtype}")
+    if t.numel() < numel:
+        raise ValueError(f"{name}: needs at least {numel} elements, has {t.numel()}")
 
 
 def _stream(stream) -> Optional[int]:
@@ -288,6 +301,13 @@ def indexshare_layers_forward(idesc: IndexerDesc, adesc: AttnDesc, indexer_types
 
 def dsa_sparse_attn_backward(desc: AttnDesc, q, kv, idx, ks, out, lse, d_out, dq, dkv, ws=None, stream=None):
     """dq (written) and dkv (zeroed, then accumulated), fp32, for the upstream gradient d_out."""
+    n_q, n_kv, H, k = desc.n_q, desc.n_kv, desc.n_heads, desc.topk
+    bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
+    for t, dt, n, name in ((q, bf, n_q * H * desc.d_qk, "q"), (kv, bf, n_kv * desc.d_qk, "kv"), (idx, i32, n_q * k, "idx"),
+                           (ks, i32, n_q, "ks"), (out, bf, n_q * H * desc.d_v, "out"), (lse, f32, n_q * H, "lse"),
+                           (d_out, bf, n_q * H * desc.d_v, "d_out"), (dq, f32, n_q * H * desc.d_qk, "dq"),
+                           (dkv, f32, n_kv * desc.d_qk, "dkv")):
+        _want(t, dt, n, name)
     if ws is None:
         ws = torch.zeros(256, dtype=torch.uint8, device=q.device)
     _check(lib().dsa_sparse_attn_backward(C.byref(desc), _ptr(q), _ptr(kv), _ptr(idx), _ptr(ks), _ptr(out), _ptr(lse),

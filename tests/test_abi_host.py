@@ -244,3 +244,25 @@ def test_attention_backward_argument_errors_before_launch():
     assert ok(C.byref(adesc), *t, fake + 16, 256, None) == 1
     assert ok(C.byref(adesc), *t, fake, 128, None) == 6
     assert ok(C.byref(D.attn_desc(4, 256, 16, 32, 1 / 24.0, d_qk=192)), *t, fake, 256, None) == 4
+
+
+def test_binding_refuses_host_tensors_and_wrong_dtypes_before_the_call():
+    # the ctypes binding hands bare addresses to the library, so it refuses what a kernel would
+    # misread: host tensors (every tensor argument is device memory), and for the backward
+    # tensors of the wrong type or size (a bf16 dkv would be written past its end as fp32)
+    import torch
+    adesc = D.attn_desc(2, 8, 4, 4, 1 / 24.0)
+    bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
+    args = dict(q=torch.zeros((2, 4, 576), dtype=bf), kv=torch.zeros((8, 576), dtype=bf),
+                idx=torch.zeros((2, 4), dtype=i32), ks=torch.zeros(2, dtype=i32),
+                out=torch.zeros((2, 4, 512), dtype=bf), lse=torch.zeros((2, 4), dtype=f32),
+                d_out=torch.zeros((2, 4, 512), dtype=bf), dq=torch.zeros((2, 4, 576), dtype=f32),
+                dkv=torch.zeros((8, 576), dtype=f32))
+    with pytest.raises(ValueError, match="CUDA"):
+        D.dsa_sparse_attn(adesc, args["q"], args["kv"], args["idx"], args["ks"], args["out"], args["lse"])
+    with pytest.raises(ValueError, match="CUDA"):
+        D.dsa_sparse_attn_backward(adesc, **args)
+    with pytest.raises(ValueError, match="dkv: expected torch.float32"):
+        D.dsa_sparse_attn_backward(adesc, **dict(args, dkv=torch.zeros((8, 576), dtype=bf)))
+    with pytest.raises(ValueError, match="idx: needs at least 8"):
+        D.dsa_sparse_attn_backward(adesc, **dict(args, idx=torch.zeros((2, 3), dtype=i32)))
