@@ -266,3 +266,14 @@ def test_binding_refuses_host_tensors_and_wrong_dtypes_before_the_call():
         D.dsa_sparse_attn_backward(adesc, **dict(args, dkv=torch.zeros((8, 576), dtype=bf)))
     with pytest.raises(ValueError, match="idx: needs at least 8"):
         D.dsa_sparse_attn_backward(adesc, **dict(args, idx=torch.zeros((2, 3), dtype=i32)))
+
+
+def test_empty_batch_is_a_no_op_before_any_device_work():
+    # n_q = 0 is valid: the forward calls return DSA_OK without touching a pointer or a device
+    L = _lib.lib()
+    idesc = D.indexer_desc(0, 128, 16, 64, 32, 8, 128, D.DSA_IDX_ROPE_Q | D.DSA_IDX_ROPE_K)
+    assert L.dsa_indexer_topk(C.byref(idesc), *([None] * 8), 0, None, None, None, 0, None) == 0
+    adesc = D.attn_desc(0, 128, 16, 8, 1 / 24.0)
+    assert L.dsa_sparse_attn(C.byref(adesc), *([None] * 7), 0, None) == 0
+    # a negative count is an argument error
+    assert L.dsa_sparse_attn(C.byref(D.attn_desc(-1, 128, 16, 8, 1 / 24.0)), *([None] * 7), 0, None) == 1
