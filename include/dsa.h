@@ -279,8 +279,10 @@ dsa_status dsa_indexer_projections(const dsa_proj_desc* desc, const void* x, con
 
 /* ------------------------------------------------------------------ training ------- */
 
-/* Gradients of dsa_sparse_attn (the training pages name the backward kernels only; this is the
- * exact gradient of the forward above).  With p_j = exp(tau q . kv_j - lse) and D = d_out . out:
+/* Gradients of dsa_sparse_attn.  [MB]'s commit that vendors the fused sparse-MLA and
+ * lightning-indexer kernels for training names a backward for each but defines neither; this
+ * is the exact gradient of the forward above.  With p_j = exp(tau q . kv_j - lse) and
+ * D = d_out . out:
  *   dq[t, h]  = tau sum_j p_j (d_out . kv_j[:512] - D) kv_j
  *   dkv[row] += tau p_j (d_out . kv_j[:512] - D) q[t, h] + p_j d_out[t, h] (first 512 dims)
  * summed over every (t, h) selecting the row.  Inputs as in dsa_sparse_attn plus the forward's
