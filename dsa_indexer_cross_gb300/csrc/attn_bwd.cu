@@ -6,7 +6,9 @@
 //   dp_j = d_o . kv_j[:512],   ds_j = p_j (dp_j - D),
 //   dq   = tau sum_j ds_j kv_j,
 //   dkv_j += tau ds_j q + p_j d_o (first 512 dims), summed over every (token, head) selecting j.
-// The training pages only name the backward kernels; this is the exact gradient of the forward.
+// "GLM-5/5.1/5.2 DSA + LoRA enablement" (Megatron-Bridge pull request #15), in the commit that
+// vendors the fused sparse-MLA and lightning-indexer kernels for training, names a backward for
+// each but defines neither; this is the exact gradient of the forward.
 //
 // One CTA per (token, block of HB = 16 or 32 heads; 16 when the layer has at most 16), eight
 // warps, bf16 tensor-core MMAs (m16n8k16, fp32 accumulate) fed from shared memory by ldmatrix.

@@ -353,8 +353,9 @@ def sparse_attn_backward(q: np.ndarray, kv: np.ndarray, idx: np.ndarray, ks: np.
                          d_o: np.ndarray, d_lse: np.ndarray | None = None, d_v: int = 512):
     """Gradients of the sparse attention above with respect to q and the latent rows.
 
-    Differentiates exactly what sparse_attn computes (no page prints a backward; the training
-    pages only name the backward kernels): for token t, head h and selected rows j,
+    Differentiates exactly what sparse_attn computes.  No page defines a backward: "GLM-5/5.1/5.2
+    DSA + LoRA enablement" (Megatron-Bridge pull request #15), in the commit that vendors the
+    fused training kernels, only names one.  For token t, head h and selected rows j,
         s_j = scale q . kv_j,  p_j = exp(s_j - lse),  o = sum_j p_j kv_j[:d_v],
     given the upstream d_o (and d_lse, optional):
         dp_j = d_o . kv_j[:d_v],  D = sum_j p_j dp_j,  ds_j = p_j (dp_j - D + d_lse),
