@@ -193,8 +193,20 @@ def dsa_indexer_workspace_size(desc: IndexerDesc) -> int:
     return n.value
 
 
+def _indexer_args(desc: IndexerDesc, q_idx, k_idx, w, q_pos, k_pos, ks, ke, rope_cs, idx_out, score_out) -> None:
+    n_q, n_kv, H, d, k = desc.n_q, desc.n_kv, desc.n_heads, desc.head_dim, desc.topk
+    bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
+    for t, dt, n, name in ((q_idx, bf, n_q * H * d, "q_idx"), (k_idx, bf, n_kv * d, "k_idx"), (w, f32, n_q * H, "w"),
+                           (q_pos, i32, n_q, "q_pos"), (k_pos, i32, n_kv, "k_pos"), (ks, i32, n_q, "ks"),
+                           (ke, i32, n_q, "ke"), (rope_cs, f32, 0, "rope_cs"), (idx_out, i32, n_q * k, "idx_out"),
+                           (score_out, f32, n_q * k, "score_out")):
+        if t is not None:
+            _want(t, dt, n, name)
+
+
 def dsa_indexer_topk(desc: IndexerDesc, q_idx, k_idx, w, q_pos, k_pos, ks, ke, rope_cs, idx_out, score_out=None,
                      ws=None, stream=None) -> torch.Tensor:
+    _indexer_args(desc, q_idx, k_idx, w, q_pos, k_pos, ks, ke, rope_cs, idx_out, score_out)
     if ws is None:
         ws = torch.empty(dsa_indexer_workspace_size(desc), dtype=torch.uint8, device=idx_out.device)
     n_pos = rope_cs.shape[0] if rope_cs is not None else 0
@@ -226,6 +238,12 @@ def dsa_sparse_attn_workspace_size(desc: AttnDesc) -> int:
 
 
 def dsa_sparse_attn(desc: AttnDesc, q, kv, idx, ks, out, lse=None, ws=None, stream=None) -> torch.Tensor:
+    n_q, n_kv, H, k = desc.n_q, desc.n_kv, desc.n_heads, desc.topk
+    bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
+    for t, dt, n, name in ((q, bf, n_q * H * desc.d_qk, "q"), (kv, bf, n_kv * desc.d_qk, "kv"), (idx, i32, n_q * k, "idx"),
+                           (ks, i32, n_q, "ks"), (out, bf, n_q * H * desc.d_v, "out"), (lse, f32, n_q * H, "lse")):
+        if t is not None:
+            _want(t, dt, n, name)
     if ws is None:
         ws = torch.empty(dsa_sparse_attn_workspace_size(desc), dtype=torch.uint8, device=out.device)
     _check(lib().dsa_sparse_attn(C.byref(desc), _ptr(q), _ptr(kv), _ptr(idx), _ptr(ks), _ptr(out), _ptr(lse),

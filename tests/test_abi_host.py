@@ -277,3 +277,28 @@ def test_empty_batch_is_a_no_op_before_any_device_work():
     assert L.dsa_sparse_attn(C.byref(adesc), *([None] * 7), 0, None) == 0
     # a negative count is an argument error
     assert L.dsa_sparse_attn(C.byref(D.attn_desc(-1, 128, 16, 8, 1 / 24.0)), *([None] * 7), 0, None) == 1
+
+
+def test_forward_wrappers_check_types_and_sizes_before_the_call():
+    import torch
+    bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
+    adesc = D.attn_desc(2, 8, 4, 4, 1 / 24.0)
+    q, kv = torch.zeros((2, 4, 576), dtype=bf), torch.zeros((8, 576), dtype=bf)
+    idx, ks = torch.zeros((2, 4), dtype=i32), torch.zeros(2, dtype=i32)
+    out, lse = torch.zeros((2, 4, 512), dtype=bf), torch.zeros((2, 4), dtype=f32)
+    with pytest.raises(ValueError, match="q: expected torch.bfloat16"):
+        D.dsa_sparse_attn(adesc, q.float(), kv, idx, ks, out, lse)
+    with pytest.raises(ValueError, match="ks: expected torch.int32"):
+        D.dsa_sparse_attn(adesc, q, kv, idx, ks.long(), out, lse)
+    with pytest.raises(ValueError, match="out: needs at least 4096"):
+        D.dsa_sparse_attn(adesc, q, kv, idx, ks, out[:1], lse)
+    idesc = D.indexer_desc(2, 8, 16, 64, 32, 4, 8, D.DSA_IDX_ROPE_Q | D.DSA_IDX_ROPE_K)
+    args = [torch.zeros((2, 16, 64), dtype=bf), torch.zeros((8, 64), dtype=bf), torch.zeros((2, 16), dtype=f32),
+            torch.zeros(2, dtype=i32), torch.zeros(8, dtype=i32), ks, ks, torch.zeros((8, 16, 2), dtype=f32),
+            torch.zeros((2, 4), dtype=i32)]
+    with pytest.raises(ValueError, match="w: expected torch.float32"):
+        D.dsa_indexer_topk(idesc, *args[:2], args[2].to(bf), *args[3:])
+    with pytest.raises(ValueError, match="idx_out: needs at least 8"):
+        D.dsa_indexer_topk(idesc, *args[:8], torch.zeros((2, 3), dtype=i32))
+    with pytest.raises(ValueError, match="CUDA"):                         # well-formed, but host memory
+        D.dsa_indexer_topk(idesc, *args)
