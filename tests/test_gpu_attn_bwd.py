@@ -27,7 +27,11 @@ def _built():
     assert torch.cuda.is_available()
 
 
-@pytest.mark.parametrize("n_q,n_kv,H,topk", [(48, 200, 16, 64), (30, 120, 40, 48), (17, 90, 4, 40)])
+# the kernel walks each token's k slots in chunks of 64 rows, double-buffered: k > 64 covers the
+# buffer alternation and dQ accumulated across chunks, k = 136 a ragged last chunk, and the gap
+# rows an all-empty chunk between two selected ones
+@pytest.mark.parametrize("n_q,n_kv,H,topk", [(48, 200, 16, 64), (30, 120, 40, 48), (17, 90, 4, 40),
+                                             (20, 700, 16, 200), (12, 500, 40, 136)])
 def test_backward_matches_oracle(n_q, n_kv, H, topk):
     rng = np.random.default_rng(n_q + H)
     ks = rng.integers(0, n_kv // 3, size=n_q).astype(np.int32)
@@ -35,6 +39,12 @@ def test_backward_matches_oracle(n_q, n_kv, H, topk):
     for t in range(n_q):
         L = int(rng.integers(1, min(topk, n_kv - ks[t]) + 1))
         idx[t, :L] = np.sort(rng.choice(n_kv - ks[t], size=L, replace=False))
+    if topk > 128:
+        tail = min(20, topk - 128)
+        for t in (1, 4):   # slots 64..127 empty, selections before and after them
+            idx[t] = -1
+            sel = np.sort(rng.choice(n_kv - ks[t], size=20 + tail, replace=False))
+            idx[t, :20], idx[t, 128:128 + tail] = sel[:20], sel[20:]
     g = torch.Generator(device=DEV)
     g.manual_seed(n_q * 3 + H)
     q = torch.randn((n_q, H, 576), generator=g, device=DEV).to(torch.bfloat16)
