@@ -111,9 +111,7 @@ __device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, u
 }
 
 // ------------------------------------------------------------------------------- cp.async
-__device__ __forceinline__ void cp_async_16(uint32_t dst_smem, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst_smem), "l"(src) : "memory");
-}
+// 16 bytes global -> shared; an invalid source reads nothing and lands zeros
 __device__ __forceinline__ void cp_async_16_zfill(uint32_t dst_smem, const void* src, bool valid) {
   const uint32_t n = valid ? 16u : 0u;
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst_smem), "l"(src), "r"(n) : "memory");
