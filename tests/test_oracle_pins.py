@@ -465,3 +465,15 @@ def test_sparse_attn_backward_identical_rows_closed_form():
         if r in (0, 2, 3, 5):
             want[:dv] = d_o[0].sum(axis=0) / n
         np.testing.assert_allclose(dkv[r], want, atol=1e-12)
+
+
+def test_rope_inverse_frequencies_closed_form():
+    # theta^(-2i/r): pair 0 turns once per position, consecutive pairs differ by theta^(-2/r),
+    # and the last pair sits at theta^(-(r-2)/r); a rotary width must be even
+    for r, theta in ((64, 8e6), (32, 1e4), (2, 5.0)):
+        f = O.rope_inv_freq(r, theta)
+        assert f.shape == (r // 2,) and f[0] == 1.0
+        np.testing.assert_allclose(f[1:] / f[:-1], theta ** (-2.0 / r), rtol=1e-14)
+        np.testing.assert_allclose(f[-1], theta ** (-(r - 2) / r), rtol=1e-14)
+    with pytest.raises(ValueError):
+        O.rope_inv_freq(63, 1e4)
