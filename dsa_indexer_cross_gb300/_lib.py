@@ -29,7 +29,11 @@ EXPORTED = ("dsa_status_string", "dsa_last_error", "dsa_donor_table", "dsa_rope_
             "dsa_index_cache_donor", "dsa_index_cache_indices", "dsa_index_cache_destroy",
             "dsa_layers_workspace_size", "indexshare_layers_forward", "dsa_workspace_status",
             "dsa_indexer_topk_static", "dsa_profile_enable", "dsa_profile_indexer_last", "dsa_mtp_indexshare_step",
-            "dsa_indexer_topk_paged", "dsa_sparse_attn_paged", "dsa_indexer_projections", "dsa_sparse_attn_backward")
+            "dsa_indexer_topk_paged", "dsa_sparse_attn_paged", "dsa_indexer_projections", "dsa_sparse_attn_backward",
+            "dsa_indexer_static_status", "dsa_profile_read")
+
+PROFILE_KINDS = {0: "rope", 1: "ranges", 2: "indexer", 3: "select", 4: "attn_prep", 5: "attn", 6: "attn_bwd",
+                 7: "proj", 8: "indexer_bwd"}
 
 
 class DsaError(RuntimeError):
@@ -47,6 +51,10 @@ class IndexerDesc(C.Structure):
 class AttnDesc(C.Structure):
     _fields_ = [("n_q", C.c_int32), ("n_kv", C.c_int32), ("n_heads", C.c_int32), ("d_qk", C.c_int32),
                 ("d_v", C.c_int32), ("topk", C.c_int32), ("softmax_scale", C.c_float), ("flags", C.c_uint32)]
+
+
+class ProfileRecord(C.Structure):
+    _fields_ = [("kind", C.c_int32), ("ms", C.c_float)]
 
 
 class LayerIO(C.Structure):
@@ -102,6 +110,10 @@ def lib() -> C.CDLL:
         L.dsa_profile_indexer_last.argtypes = [P(C.c_float), i32]
         L.dsa_indexer_topk_static.restype = st
         L.dsa_indexer_topk_static.argtypes = [P(IndexerDesc), vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp]
+        L.dsa_indexer_static_status.restype = st
+        L.dsa_indexer_static_status.argtypes = [vp, P(u32)]
+        L.dsa_profile_read.restype = st
+        L.dsa_profile_read.argtypes = [P(ProfileRecord), i32, P(i32)]
         L.dsa_sparse_attn_backward.restype = st
         L.dsa_sparse_attn_backward.argtypes = [P(AttnDesc), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.dsa_indexer_projections.restype = st
@@ -219,6 +231,7 @@ def dsa_indexer_topk(desc: IndexerDesc, q_idx, k_idx, w, q_pos, k_pos, ks, ke, r
 def dsa_indexer_topk_static(desc: IndexerDesc, q_idx, k_idx, w, q_pos, k_pos, ks, ke, rope_cs, idx_out,
                             score_out=None, stream=None) -> None:
     """dsa_indexer_topk with the library's static device scratch instead of a workspace."""
+    _indexer_args(desc, q_idx, k_idx, w, q_pos, k_pos, ks, ke, rope_cs, idx_out, score_out)
     n_pos = rope_cs.shape[0] if rope_cs is not None else 0
     _check(lib().dsa_indexer_topk_static(C.byref(desc), _ptr(q_idx), _ptr(k_idx), _ptr(w), _ptr(q_pos), _ptr(k_pos),
                                          _ptr(ks), _ptr(ke), _ptr(rope_cs), n_pos, _ptr(idx_out), _ptr(score_out),
@@ -341,6 +354,13 @@ class ProjDesc(C.Structure):
 def dsa_indexer_projections(desc: "ProjDesc", x, q_latent, wq_b, wk, k_norm_w, k_norm_b, weights_proj, q_idx, k_idx,
                             w, ws=None, stream=None):
     """q_idx = q_latent wq_b^T, k_idx = LayerNorm(x wk^T) (k_norm weight / bias), w = x weights_proj^T."""
+    T, dh, dq, H, d = desc.n_tokens, desc.d_hidden, desc.d_q, desc.n_heads, desc.head_dim
+    bf, f32 = torch.bfloat16, torch.float32
+    for t, dt, n, name in ((x, bf, T * dh, "x"), (q_latent, bf, T * dq, "q_latent"), (wq_b, bf, H * d * dq, "wq_b"),
+                           (wk, bf, d * dh, "wk"), (k_norm_w, f32, d, "k_norm_w"), (k_norm_b, f32, d, "k_norm_b"),
+                           (weights_proj, bf, H * dh, "weights_proj"), (q_idx, bf, T * H * d, "q_idx"),
+                           (k_idx, bf, T * d, "k_idx"), (w, f32, T * H, "w")):
+        _want(t, dt, n, name)
     if ws is None:
         ws = torch.zeros(256, dtype=torch.uint8, device=x.device)
     _check(lib().dsa_indexer_projections(C.byref(desc), _ptr(x), _ptr(q_latent), _ptr(wq_b), _ptr(wk), _ptr(k_norm_w),
@@ -364,8 +384,21 @@ def paged_cache(block_table: torch.Tensor, seq_len: torch.Tensor, n_pages: int) 
     return PagedCache(_ptr(block_table), _ptr(seq_len), block_table.shape[1], n_pages, DSA_PAGE_ROWS)
 
 
+def _paged_args(pages: PagedCache) -> None:
+    if not pages.block_table or not pages.seq_len:
+        raise ValueError("paged cache: block_table and seq_len must be set")
+
+
 def dsa_indexer_topk_paged(desc: IndexerDesc, q_idx, k_cache, w, q_pos, pages: PagedCache, rope_cs, idx_out,
                            score_out=None, ws=None, stream=None):
+    n_q, H, d, k = desc.n_q, desc.n_heads, desc.head_dim, desc.topk
+    bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
+    for t, dt, n, name in ((q_idx, bf, n_q * H * d, "q_idx"), (k_cache, bf, desc.n_kv * d, "k_cache"),
+                           (w, f32, n_q * H, "w"), (q_pos, i32, n_q, "q_pos"), (rope_cs, f32, 0, "rope_cs"),
+                           (idx_out, i32, n_q * k, "idx_out"), (score_out, f32, n_q * k, "score_out")):
+        if t is not None:
+            _want(t, dt, n, name)
+    _paged_args(pages)
     if ws is None:
         ws = torch.empty(dsa_indexer_workspace_size(desc), dtype=torch.uint8, device=q_idx.device)
     n_pos = rope_cs.shape[0] if rope_cs is not None else 0
@@ -376,6 +409,13 @@ def dsa_indexer_topk_paged(desc: IndexerDesc, q_idx, k_cache, w, q_pos, pages: P
 
 
 def dsa_sparse_attn_paged(desc: AttnDesc, q, kv_cache, idx, pages: PagedCache, out, lse=None, ws=None, stream=None):
+    n_q, H, k = desc.n_q, desc.n_heads, desc.topk
+    bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
+    for t, dt, n, name in ((q, bf, n_q * H * desc.d_qk, "q"), (kv_cache, bf, desc.n_kv * desc.d_qk, "kv_cache"),
+                           (idx, i32, n_q * k, "idx"), (out, bf, n_q * H * desc.d_v, "out"), (lse, f32, n_q * H, "lse")):
+        if t is not None:
+            _want(t, dt, n, name)
+    _paged_args(pages)
     if ws is None:
         ws = torch.empty(dsa_sparse_attn_workspace_size(desc), dtype=torch.uint8, device=q.device)
     _check(lib().dsa_sparse_attn_paged(C.byref(desc), _ptr(q), _ptr(kv_cache), _ptr(idx), C.byref(pages), _ptr(out),
@@ -389,6 +429,17 @@ def dsa_mtp_indexshare_step(idesc: IndexerDesc, adesc: AttnDesc, step: int, laye
     steps attend with mtp_idx unchanged.  layer: 'q', 'kv', 'out' (+ 'lse') and, at step 0,
     'q_idx', 'k_idx', 'w'."""
     L = layer
+    n_q, H, k = adesc.n_q, adesc.n_heads, adesc.topk
+    bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
+    for key, dt, n in (("q", bf, n_q * H * adesc.d_qk), ("kv", bf, adesc.n_kv * adesc.d_qk),
+                       ("out", bf, n_q * H * adesc.d_v), ("lse", f32, n_q * H)):
+        if L.get(key) is not None:
+            _want(L[key], dt, n, key)
+    _want(mtp_idx, i32, n_q * k, "mtp_idx")
+    for t, dt, n, name in ((ks, i32, n_q, "ks"), (ke, i32, n_q, "ke"), (q_pos, i32, n_q, "q_pos")):
+        _want(t, dt, n, name)
+    if step == 0:
+        _indexer_args(idesc, L.get("q_idx"), L.get("k_idx"), L.get("w"), None, k_pos, None, None, rope_cs, None, None)
     io = LayerIO(_ptr(L.get("q_idx")), _ptr(L.get("k_idx")), _ptr(L.get("w")), _ptr(L["q"]), _ptr(L["kv"]),
                  _ptr(L["out"]), _ptr(L.get("lse")))
     if ws is None:
@@ -424,3 +475,22 @@ def dsa_profile_indexer_last() -> list:
     ms = (C.c_float * 4)()
     _check(lib().dsa_profile_indexer_last(ms, 4))
     return [float(x) for x in ms]
+
+
+def dsa_indexer_static_status(stream=None, raise_on_fault: bool = True) -> int:
+    """Status bits of the last dsa_indexer_topk_static call on the current device (synchronises
+    the stream).  Raises DsaError on a device fault unless raise_on_fault is False."""
+    bits = C.c_uint32(0)
+    st = lib().dsa_indexer_static_status(_stream(stream), C.byref(bits))
+    if st not in (0, 7, 8) or (st != 0 and raise_on_fault):
+        _check(st)
+    return bits.value
+
+
+def dsa_profile_read(cap: int = 8192) -> list:
+    """[(kind name, device ms)] of every launch logged on the current device since profiling was
+    switched on, in launch order (waits for them to finish)."""
+    buf = (ProfileRecord * cap)()
+    n = C.c_int32(0)
+    _check(lib().dsa_profile_read(buf, cap, C.byref(n)))
+    return [(PROFILE_KINDS.get(buf[i].kind, str(buf[i].kind)), float(buf[i].ms)) for i in range(min(n.value, cap))]

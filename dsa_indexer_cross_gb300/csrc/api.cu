@@ -103,6 +103,27 @@ PhaseEvents* phase_events() {
   return &p;
 }
 
+// ------------------------------------------------------------------ launch log
+// Per device: a fixed ring of event pairs, created on first use and kept; records are
+// appended while profiling is on and read back (after their events complete) by
+// dsa_profile_read.  A full log drops further records and says so.
+constexpr int kLogCap = 8192;
+struct LaunchLog {
+  cudaEvent_t ev[kLogCap][2];
+  int kind[kLogCap];
+  int n_created = 0;   // event pairs created so far
+  int n = 0;           // records in the log
+  bool dropped = false;
+};
+LaunchLog* g_log[64] = {};
+std::mutex g_log_mu;
+
+LaunchLog* launch_log(int dev) {
+  if (dev < 0 || dev >= 64) return nullptr;
+  if (!g_log[dev]) g_log[dev] = new (std::nothrow) LaunchLog;
+  return g_log[dev];
+}
+
 // ------------------------------------------------------------------ tensor maps
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -259,14 +280,18 @@ dsa_status run_indexer(const dsa_indexer_desc* d, const void* q_idx, const void*
   PhaseEvents* pe = phase_events();
   if (pe) (void)cudaEventRecord(pe->ev[0], st);
   if (rq) {
+    const int ps = prof_begin(kProfRope, st);
     e = launch_rope_rows(q_idx, base + L.off_q, q_pos, static_cast<int64_t>(d->n_q) * d->n_heads, d->n_heads,
                          d->head_dim, d->rope_dim, rope_cs, rope_n_pos, status, st);
+    prof_end(ps, st);
     if (e != cudaSuccess) return cuda_fail(e, "index q RoPE");
     qr = base + L.off_q;
   }
   if (rk && d->n_kv > 0) {
+    const int ps = prof_begin(kProfRope, st);
     e = launch_rope_rows(k_idx, base + L.off_k, k_pos, d->n_kv, 1, d->head_dim, d->rope_dim, rope_cs, rope_n_pos,
                          status, st);
+    prof_end(ps, st);
     if (e != cudaSuccess) return cuda_fail(e, "index k RoPE");
     kr = base + L.off_k;
   }
@@ -280,7 +305,9 @@ dsa_status run_indexer(const dsa_indexer_desc* d, const void* q_idx, const void*
   const int range_limit = pg ? static_cast<int>(std::min<long long>(static_cast<long long>(pg->max_pages) * kPageRows,
                                                                    0x7FFFFFFF))
                              : d->n_kv;
+  int ps = prof_begin(kProfRanges, st);
   e = launch_ranges(ks, ke, d->n_q, p.group, range_limit, d->max_len, trivial_len, rr, gr, status, st);
+  prof_end(ps, st);
   if (e != cudaSuccess) return cuda_fail(e, "key ranges");
   if (pe) (void)cudaEventRecord(pe->ev[2], st);
   uint32_t* cnt = reinterpret_cast<uint32_t*>(base + L.off_cnt);
@@ -298,15 +325,19 @@ dsa_status run_indexer(const dsa_indexer_desc* d, const void* q_idx, const void*
     if ((s = tmap_bf16(&tki, k_idx, d->head_dim, d->n_kv, 128)) != DSA_OK) return s;
     const int q_split = rq ? rope_split_blocks(d->head_dim, d->rope_dim) : 0;
     const int k_split = rk ? rope_split_blocks(d->head_dim, d->rope_dim) : 0;
+    ps = prof_begin(kProfIndexer, st);
     e = launch_indexer(p, tq, tk, tqi, tki, q_split, k_split, pg ? *pg : PagedRows{}, w, d->n_q, rr, gr, ck, ci, cnt,
                        status, st);
+    prof_end(ps, st);
     if (e != cudaSuccess) return cuda_fail(e, "indexer kernel");
   } else {
     if ((e = cudaMemsetAsync(cnt, 0, static_cast<size_t>(d->n_q) * p.n_chunks * 4, st)) != cudaSuccess)
       return cuda_fail(e, "clear counts");
   }
   if (pe) (void)cudaEventRecord(pe->ev[3], st);
+  ps = prof_begin(kProfSelect, st);
   e = launch_select(d->n_q, p.n_chunks, p.cap, d->topk, trivial_len, rr, ck, ci, cnt, idx_out, score_out, status, st);
+  prof_end(ps, st);
   if (e != cudaSuccess) return cuda_fail(e, "top-k select");
   if (pe) {
     (void)cudaEventRecord(pe->ev[4], st);
@@ -380,6 +411,42 @@ dsa_status run_attn(const dsa_attn_desc* d, const void* q, const void* kv, const
 }  // namespace
 
 int device_sm_count() { return dev_info().sms; }
+
+int prof_begin(int kind, cudaStream_t st) {
+  if (!g_profile.load(std::memory_order_relaxed)) return -1;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  std::lock_guard<std::mutex> lock(g_log_mu);
+  LaunchLog* L = launch_log(dev);
+  if (!L) return -1;
+  if (L->n >= kLogCap) {
+    L->dropped = true;
+    return -1;
+  }
+  const int i = L->n;
+  if (i >= L->n_created) {
+    if (cudaEventCreate(&L->ev[i][0]) != cudaSuccess) return ((void)cudaGetLastError(), -1);
+    if (cudaEventCreate(&L->ev[i][1]) != cudaSuccess) {
+      cudaEventDestroy(L->ev[i][0]);
+      return ((void)cudaGetLastError(), -1);
+    }
+    L->n_created = i + 1;
+  }
+  if (cudaEventRecord(L->ev[i][0], st) != cudaSuccess) return ((void)cudaGetLastError(), -1);
+  L->kind[i] = kind;
+  L->n = i + 1;
+  return i;
+}
+
+void prof_end(int slot, cudaStream_t st) {
+  if (slot < 0) return;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return;
+  std::lock_guard<std::mutex> lock(g_log_mu);
+  LaunchLog* L = launch_log(dev);
+  if (!L || slot >= L->n) return;
+  if (cudaEventRecord(L->ev[slot][1], st) != cudaSuccess) (void)cudaGetLastError();
+}
 
 dsa_status indexer_workspace_bytes(const dsa_indexer_desc* d, size_t* bytes) {
   dsa_status s = check_indexer_desc(d);
@@ -711,7 +778,9 @@ dsa_status dsa_indexer_projections(const dsa_proj_desc* d, const void* x, const 
   J.first_unit[0] = 0;
   J.first_unit[1] = m_tiles;
   J.first_unit[2] = m_tiles + m_tiles * (nq / 256);
+  const int ps = prof_begin(kProfProj, st);
   e = launch_projections(ta, tb, tb2, J, d->n_tokens, static_cast<uint32_t*>(ws), st);
+  prof_end(ps, st);
   if (e != cudaSuccess) return cuda_fail(e, "projection kernel");
   return DSA_OK;
 }
@@ -735,8 +804,10 @@ dsa_status dsa_sparse_attn_backward(const dsa_attn_desc* desc, const void* q, co
       (e = cudaMemsetAsync(dkv, 0, static_cast<size_t>(desc->n_kv) * 576 * sizeof(float), st)) != cudaSuccess)
     return cuda_fail(e, "clear dkv");
   if (desc->n_q == 0) return DSA_OK;
+  const int ps = prof_begin(kProfAttnBwd, st);
   e = launch_sparse_attn_bwd(desc->n_q, desc->n_kv, desc->n_heads, desc->topk, desc->softmax_scale, q, kv, idx, ks, out,
                              lse, d_out, dq, dkv, static_cast<uint32_t*>(ws), st);
+  prof_end(ps, st);
   if (e != cudaSuccess) return cuda_fail(e, "sparse attention backward");
   return DSA_OK;
 }
@@ -754,7 +825,36 @@ dsa_status dsa_workspace_status(const void* ws, void* stream, uint32_t* device_b
 }
 
 dsa_status dsa_profile_enable(int32_t on) {
+  if (on) {
+    // a new measurement starts with an empty launch log on every device
+    std::lock_guard<std::mutex> lock(g_log_mu);
+    for (LaunchLog* L : g_log)
+      if (L) {
+        L->n = 0;
+        L->dropped = false;
+      }
+  }
   g_profile.store(on ? 1 : 0, std::memory_order_relaxed);
+  return DSA_OK;
+}
+
+dsa_status dsa_profile_read(dsa_profile_record* out, int32_t cap, int32_t* n) {
+  if (!n || cap < 0 || (cap > 0 && !out)) return fail(DSA_ERR_ARG, "n must be non-NULL and out must hold cap records");
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  std::lock_guard<std::mutex> lock(g_log_mu);
+  LaunchLog* L = (dev >= 0 && dev < 64) ? g_log[dev] : nullptr;
+  const int have = L ? L->n : 0;
+  *n = have;
+  for (int i = 0; i < have && i < cap; ++i) {
+    if ((e = cudaEventSynchronize(L->ev[i][1])) != cudaSuccess) return cuda_fail(e, "launch log events");
+    float t = 0.f;
+    if ((e = cudaEventElapsedTime(&t, L->ev[i][0], L->ev[i][1])) != cudaSuccess) return cuda_fail(e, "launch log events");
+    out[i].kind = L->kind[i];
+    out[i].ms = t;
+  }
+  if (L && L->dropped) return fail(DSA_ERR_WORKSPACE, "launch log full: records after the first %d were dropped", kLogCap);
   return DSA_OK;
 }
 

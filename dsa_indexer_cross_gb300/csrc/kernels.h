@@ -126,4 +126,16 @@ cudaError_t launch_sparse_attn_bwd(int n_q, int n_kv, int n_heads, int topk, flo
 
 int device_sm_count();
 
+// ---------------------------------------------------------------------------- launch log
+// While profiling is switched on (dsa_profile_enable), every kernel launch of the library is
+// bracketed by a pair of CUDA events on its stream, tagged with the kernel's kind, so that a
+// caller can read each launch's device time afterwards (dsa_profile_read).  Off, both calls
+// do nothing.  prof_begin returns the record's slot (-1 when nothing is recorded).
+enum ProfKind : int {
+  kProfRope = 0, kProfRanges = 1, kProfIndexer = 2, kProfSelect = 3, kProfAttnPrep = 4, kProfAttn = 5,
+  kProfAttnBwd = 6, kProfProj = 7, kProfIndexerBwd = 8
+};
+int prof_begin(int kind, cudaStream_t st);
+void prof_end(int slot, cudaStream_t st);
+
 }  // namespace dsa

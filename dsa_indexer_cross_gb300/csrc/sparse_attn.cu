@@ -862,10 +862,12 @@ cudaError_t launch_cfg(const CUtensorMap& tmap, const CUtensorMap& tmap_q, int n
   if (e != cudaSuccess) return e;
   const int n_items = C::DENSE ? (n_q + C::B - 1) / C::B : n_q * ((H + HB - 1) / HB);
   const int grid = n_items < device_sm_count() ? n_items : device_sm_count();
+  const int ps = prof_begin(kProfAttn, st);
   kern<<<grid, C::THREADS, C::DYN_SMEM, st>>>(tmap, tmap_q, static_cast<const uint16_t*>(kv), idx, ks, pg, row_nt,
                                             block_range, block_mask,
                                             static_cast<uint16_t*>(out), lse, n_q, n_kv, H, topk,
                                             scale * 1.4426950408889634f, status, status + 1);
+  prof_end(ps, st);
   return cudaGetLastError();
 }
 
@@ -899,7 +901,9 @@ cudaError_t launch_dense(const CUtensorMap& tmap_kv, const CUtensorMap& tmap_q, 
   const int n_blk = (n_q + C::B - 1) / C::B;
   int2* br = static_cast<int2*>(scratch);
   uint32_t* bm = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(scratch) + dense_mask_offset(n_blk));
+  const int ps = prof_begin(kProfAttnPrep, st);
   block_mask_kernel<C::B, C::MAXR><<<n_blk, 256, 0, st>>>(idx, ks, n_q, n_kv, topk, br, bm, status, status + 1);
+  prof_end(ps, st);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_cfg<kDenseCols, HD>(tmap_kv, tmap_q, n_q, n_kv, n_heads, topk, scale, nullptr, idx, ks, PagedRows{},
@@ -954,7 +958,9 @@ cudaError_t launch_sparse_attn(const CUtensorMap& tmap_kv, const CUtensorMap& tm
     }
   }
   int32_t* row_nt = static_cast<int32_t*>(scratch);
+  const int ps = prof_begin(kProfAttnPrep, st);
   row_tiles_kernel<<<(n_q + 7) / 8, 256, 0, st>>>(idx, n_q, topk, row_nt);
+  prof_end(ps, st);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   switch (sparse_attn_q_box_rows(n_heads, n_kv, topk, pg.block_table != nullptr)) {

@@ -11,11 +11,16 @@
 //
 // Set-up: the first call on a device (with that device current) looks up the array's
 // device address once with cudaGetSymbolAddress and caches it; make that first call before
-// any stream capture.  Every call on a device shares the array and it keeps the previous
-// call's contents: the status word is cleared at the start of each call and every other
-// scratch word is written before it is read.  Calls whose work overlaps on the GPU (other
-// streams, other host threads) race on the array and must be serialised by the caller.
+// any stream capture.  The cached address belongs to the device's primary context, so the
+// entry point must not be used again after that context is reset.  Every call on a device
+// shares the array and it keeps the previous call's contents: the status word is cleared at
+// the start of each call and every other scratch word is written before it is read.  Calls
+// whose work overlaps on the GPU (other streams, other host threads) race on the array and
+// must be serialised by the caller.  dsa_indexer_static_status reads the status word of the
+// last call (a device-to-host copy of the array's first 256 bytes; nothing is allocated).
 #include <mutex>
+
+#include "../../include/dsa.h"
 
 #include "api_internal.h"
 #include "kernels.h"
@@ -65,4 +70,16 @@ extern "C" dsa_status dsa_indexer_topk_static(const dsa_indexer_desc* desc, cons
   if ((s = dsa::scratch_address(&ws)) != DSA_OK) return s;
   return dsa::indexer_run(desc, q_idx, k_idx, w, q_pos, k_pos, ks, ke, rope_cs, rope_n_pos, idx_out, score_out, ws,
                           DSA_STATIC_SCRATCH_BYTES, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" dsa_status dsa_indexer_static_status(void* stream, uint32_t* device_bits) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return dsa::set_error(DSA_ERR_CUDA, "cudaGetDevice failed");
+  void* ws = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(dsa::g_mu);
+    if (dev >= 0 && dev < dsa::kMaxDevices) ws = dsa::g_addr[dev];
+  }
+  if (!ws) return dsa::set_error(DSA_ERR_UNSUPPORTED, "no dsa_indexer_topk_static call has been made on this device");
+  return dsa_workspace_status(ws, stream, device_bits);
 }

@@ -151,14 +151,25 @@ dsa_status dsa_indexer_topk(const dsa_indexer_desc* desc, const void* q_idx, con
  * call on a device (with that device current) looks up the array's address once; make that
  * call before any stream capture.  Problems that need more scratch than the array holds are
  * rejected with DSA_ERR_WORKSPACE.  All calls on a device share the array: calls whose work
- * overlaps on the GPU race and must be serialised by the caller.  The status word that
- * dsa_workspace_status reads is not exposed for this variant; device-side faults are still
- * recorded in the array and cleared at the start of the next call. */
+ * overlaps on the GPU race and must be serialised by the caller.  Device-side faults (bad
+ * positions or key ranges, a timed-out pipeline wait) are recorded in the array's status
+ * word, which dsa_indexer_static_status reads; the next call clears it.  The cached address
+ * belongs to the device's primary context: after cudaDeviceReset (or anything else that
+ * destroys and re-creates that context) this entry point must not be called again in the
+ * same process. */
 #define DSA_STATIC_SCRATCH_BYTES (32u << 20)
 dsa_status dsa_indexer_topk_static(const dsa_indexer_desc* desc, const void* q_idx, const void* k_idx, const float* w,
                                    const int32_t* q_pos, const int32_t* k_pos, const int32_t* ks, const int32_t* ke,
                                    const float* rope_cs, int32_t rope_n_pos, int32_t* idx_out, float* score_out,
                                    void* stream);
+
+/* Status of the last dsa_indexer_topk_static call on the current device, the counterpart of
+ * dsa_workspace_status for that variant: synchronises `stream` (pass the stream of that
+ * call), reads the status word of the static array and maps it the same way (DSA_OK,
+ * DSA_ERR_TIMEOUT, DSA_ERR_DEVICE); the raw bits go to *device_bits when it is not NULL.
+ * Allocates nothing.  Errors: DSA_ERR_UNSUPPORTED (no static call made on this device yet),
+ * DSA_ERR_CUDA. */
+dsa_status dsa_indexer_static_status(void* stream, uint32_t* device_bits);
 
 /* ------------------------------------------------------------------ sparse attention - */
 
@@ -385,6 +396,30 @@ dsa_status dsa_profile_enable(int32_t on);
  * first min(n, 4) values; waits for that call to finish.  Errors: DSA_ERR_ARG (ms NULL or
  * n < 1), DSA_ERR_UNSUPPORTED (no profiled call yet on this device), DSA_ERR_CUDA. */
 dsa_status dsa_profile_indexer_last(float* ms, int32_t n);
+
+/* Launch log.  While profiling is on, every kernel launch of the library (in every call,
+ * any stream) is also bracketed by two CUDA events on its stream and logged with its kind;
+ * dsa_profile_enable(1) empties the log of every device.  dsa_profile_read waits for the
+ * logged launches of the current device to finish and copies up to `cap` records, in launch
+ * order, into out; *n receives the number logged.  The log holds 8192 records per device;
+ * later launches are not logged and dsa_profile_read then returns DSA_ERR_WORKSPACE (the
+ * records it copied are valid).  Errors: DSA_ERR_ARG, DSA_ERR_WORKSPACE, DSA_ERR_CUDA. */
+enum {
+  DSA_PROF_ROPE = 0,          /* index q or k RoPE pre-pass                                 */
+  DSA_PROF_RANGES = 1,        /* key-range plan                                             */
+  DSA_PROF_INDEXER = 2,       /* tcgen05 scores + streaming top-k                           */
+  DSA_PROF_SELECT = 3,        /* final top-k select                                         */
+  DSA_PROF_ATTN_PREP = 4,     /* attention pre-pass (tile counts or block masks)            */
+  DSA_PROF_ATTN = 5,          /* sparse attention kernel                                    */
+  DSA_PROF_ATTN_BWD = 6,      /* sparse attention backward                                  */
+  DSA_PROF_PROJ = 7,          /* indexer projections                                        */
+  DSA_PROF_INDEXER_BWD = 8    /* indexer backward                                           */
+};
+typedef struct dsa_profile_record {
+  int32_t kind;   /* DSA_PROF_*                        */
+  float ms;       /* device time of the launch, in ms  */
+} dsa_profile_record;
+dsa_status dsa_profile_read(dsa_profile_record* out, int32_t cap, int32_t* n);
 
 #ifdef __cplusplus
 }

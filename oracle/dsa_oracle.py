@@ -16,7 +16,7 @@ public pages:
   2 "What IndexShare changes", "Layer execution pattern", "Public config evidence",
   "What is actually shared?", "Implementation checklist").
 
-Readings taken where the pages are silent (each also listed in the design notes):
+Readings taken where the pages are silent:
 
 * index RoPE rotates the LAST ``r`` dims of each index head (Megatron convention), with
   rotate-half pairing (i, i + r/2) inside those dims, inv_freq_i = theta^(-2i/r) and

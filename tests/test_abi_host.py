@@ -302,3 +302,58 @@ def test_forward_wrappers_check_types_and_sizes_before_the_call():
         D.dsa_indexer_topk(idesc, *args[:8], torch.zeros((2, 3), dtype=i32))
     with pytest.raises(ValueError, match="CUDA"):                         # well-formed, but host memory
         D.dsa_indexer_topk(idesc, *args)
+
+
+def test_static_paged_projection_and_mtp_wrappers_check_types_and_sizes():
+    # every wrapper that hands tensors to the library checks type and size first, so a
+    # mistyped or short tensor never reaches a kernel as a bare pointer
+    import torch
+    bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
+    idesc = D.indexer_desc(2, 8, 16, 64, 32, 4, 8, D.DSA_IDX_ROPE_Q | D.DSA_IDX_ROPE_K)
+    ks = torch.zeros(2, dtype=i32)
+    args = [torch.zeros((2, 16, 64), dtype=bf), torch.zeros((8, 64), dtype=bf), torch.zeros((2, 16), dtype=f32),
+            torch.zeros(2, dtype=i32), torch.zeros(8, dtype=i32), ks, ks, torch.zeros((8, 16, 2), dtype=f32),
+            torch.zeros((2, 4), dtype=i32)]
+    with pytest.raises(ValueError, match="q_idx: expected torch.bfloat16"):
+        D.dsa_indexer_topk_static(idesc, args[0].float(), *args[1:])
+    with pytest.raises(ValueError, match="idx_out: needs at least 8"):
+        D.dsa_indexer_topk_static(idesc, *args[:8], torch.zeros((2, 3), dtype=i32))
+    # paged: 64 index heads, one 128-row page per row
+    pdesc = D.indexer_desc(2, 256, 64, 128, 64, 4, 128, D.DSA_IDX_ROPE_Q | D.DSA_IDX_INDEPENDENT_ROWS)
+    pages = D.PagedCache(8, 8, 1, 2, D.DSA_PAGE_ROWS)    # fake non-NULL addresses: never reached
+    q_idx, k_cache = torch.zeros((2, 64, 128), dtype=bf), torch.zeros((256, 128), dtype=bf)
+    w, q_pos, idx = torch.zeros((2, 64), dtype=f32), torch.zeros(2, dtype=i32), torch.zeros((2, 4), dtype=i32)
+    rope = torch.zeros((8, 32, 2), dtype=f32)
+    with pytest.raises(ValueError, match="k_cache: needs at least 32768"):
+        D.dsa_indexer_topk_paged(pdesc, q_idx, k_cache[:10], w, q_pos, pages, rope, idx)
+    with pytest.raises(ValueError, match="w: expected torch.float32"):
+        D.dsa_indexer_topk_paged(pdesc, q_idx, k_cache, w.to(bf), q_pos, pages, rope, idx)
+    adesc = D.attn_desc(2, 256, 4, 4, 1 / 24.0)
+    q, kvc = torch.zeros((2, 4, 576), dtype=bf), torch.zeros((256, 576), dtype=bf)
+    out = torch.zeros((2, 4, 512), dtype=bf)
+    with pytest.raises(ValueError, match="idx: expected torch.int32"):
+        D.dsa_sparse_attn_paged(adesc, q, kvc, idx.long(), pages, out)
+    with pytest.raises(ValueError, match="kv_cache: needs at least"):
+        D.dsa_sparse_attn_paged(adesc, q, kvc[:3], idx, pages, out)
+    # projections
+    pd = D.ProjDesc(4, 128, 64, 16, 64, 1e-6)
+    t = dict(x=torch.zeros((4, 128), dtype=bf), q_latent=torch.zeros((4, 64), dtype=bf),
+             wq_b=torch.zeros((1024, 64), dtype=bf), wk=torch.zeros((64, 128), dtype=bf),
+             k_norm_w=torch.ones(64), k_norm_b=torch.zeros(64), weights_proj=torch.zeros((16, 128), dtype=bf),
+             q_idx=torch.zeros((4, 16, 64), dtype=bf), k_idx=torch.zeros((4, 64), dtype=bf),
+             w=torch.zeros((4, 16), dtype=f32))
+    with pytest.raises(ValueError, match="wk: needs at least 8192"):
+        D.dsa_indexer_projections(pd, **dict(t, wk=t["wk"][:3]))
+    with pytest.raises(ValueError, match="k_norm_w: expected torch.float32"):
+        D.dsa_indexer_projections(pd, **dict(t, k_norm_w=torch.ones(64, dtype=bf)))
+    # MTP step
+    layer = dict(q=q, kv=kvc, out=out, q_idx=torch.zeros((2, 16, 64), dtype=bf), k_idx=torch.zeros((256, 64), dtype=bf),
+                 w=torch.zeros((2, 16), dtype=f32))
+    mdesc = D.indexer_desc(2, 256, 16, 64, 32, 4, 256, D.DSA_IDX_ROPE_Q | D.DSA_IDX_ROPE_K)
+    kpos = torch.zeros(256, dtype=i32)
+    with pytest.raises(ValueError, match="mtp_idx: needs at least 8"):
+        D.dsa_mtp_indexshare_step(mdesc, adesc, 0, layer, ks, ks, ks, kpos, rope, torch.zeros(3, dtype=i32))
+    with pytest.raises(ValueError, match="q: expected torch.bfloat16"):
+        D.dsa_mtp_indexshare_step(mdesc, adesc, 1, dict(layer, q=q.float()), ks, ks, ks, kpos, rope, idx)
+    with pytest.raises(ValueError, match="w: expected torch.float32"):
+        D.dsa_mtp_indexshare_step(mdesc, adesc, 0, dict(layer, w=layer["w"].to(bf)), ks, ks, ks, kpos, rope, idx)

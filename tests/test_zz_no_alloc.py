@@ -67,6 +67,27 @@ def test_static_scratch_rejects_problems_beyond_its_size():
                           D.DSA_IDX_ROPE_Q | D.DSA_IDX_ROPE_K)
     assert D.dsa_indexer_workspace_size(desc) > (32 << 20)
     z = torch.zeros(16, dtype=torch.int32, device="cuda")
+    p = z.data_ptr()
+    lib = D.lib()
+    st = lib.dsa_indexer_topk_static(C.byref(desc), p, p, p, p, p, p, p, p, 1, p, None,
+                                     torch.cuda.current_stream().cuda_stream)
+    assert _lib.STATUS_NAMES[st] == "DSA_ERR_WORKSPACE"
+
+
+def test_static_scratch_reports_device_faults_through_its_status_query():
+    """A key range outside [0, n_kv) is flagged on the device; the static variant's status
+    query reports it, and the next clean call clears it."""
+    w = synth.WORKLOADS["tiny"]
+    geo = synth.geometry(w)
+    desc, L, q_pos, k_pos, ks, ke, rope = _inputs(w, geo)
+    idx = torch.empty((w.n_q, w.topk), dtype=torch.int32, device="cuda")
+    bad_ke = ke.clone()
+    bad_ke[5] = geo.n_kv + 10
+    D.dsa_indexer_topk_static(desc, L["q_idx"], L["k_idx"], L["w"], q_pos, k_pos, ks, bad_ke, rope, idx)
+    bits = D.dsa_indexer_static_status(raise_on_fault=False)
+    assert bits != 0
     with pytest.raises(D.DsaError) as e:
-        _lib.dsa_indexer_topk_static(desc, z, z, z, z, z, z, z, z.float(), z)
-    assert e.value.name == "DSA_ERR_WORKSPACE"
+        D.dsa_indexer_static_status()
+    assert e.value.name == "DSA_ERR_DEVICE"
+    D.dsa_indexer_topk_static(desc, L["q_idx"], L["k_idx"], L["w"], q_pos, k_pos, ks, ke, rope, idx)
+    assert D.dsa_indexer_static_status() == 0
