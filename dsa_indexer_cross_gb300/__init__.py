@@ -9,7 +9,7 @@ from ._lib import (AttnDesc, DsaError, IndexCache, IndexerDesc, LayerIO, PagedCa
                    DSA_IDX_ROPE_Q, DSA_LAYER_FULL, DSA_LAYER_SHARED, attn_desc, dsa_donor_table,
                    dsa_indexer_topk, dsa_indexer_topk_static, dsa_indexer_workspace_size, dsa_layers_workspace_size, dsa_mtp_indexshare_step,
                    dsa_profile_enable,
-                   dsa_profile_indexer_last, dsa_profile_read, dsa_indexer_static_status, dsa_rope_table,
+                   dsa_profile_indexer_last, dsa_profile_read, dsa_indexer_static_status, dsa_debug_pipeline, dsa_rope_table,
                    dsa_sparse_attn, dsa_sparse_attn_workspace_size, dsa_workspace_status, indexer_desc,
                    indexshare_layers_forward, lib)
 
@@ -17,5 +17,5 @@ __all__ = ["AttnDesc", "DsaError", "IndexCache", "IndexerDesc", "LayerIO", "Page
            "dsa_indexer_topk_paged", "dsa_sparse_attn_paged", "paged_cache", "ProjDesc", "dsa_indexer_projections", "dsa_sparse_attn_backward", "DSA_IDX_INDEPENDENT_ROWS", "DSA_IDX_ROPE_K",
            "DSA_IDX_ROPE_Q", "DSA_LAYER_FULL", "DSA_LAYER_SHARED", "attn_desc", "dsa_donor_table", "dsa_indexer_topk", "dsa_indexer_topk_static",
            "dsa_indexer_workspace_size", "dsa_layers_workspace_size", "dsa_mtp_indexshare_step", "dsa_profile_enable",
-           "dsa_profile_indexer_last", "dsa_profile_read", "dsa_indexer_static_status", "dsa_rope_table", "dsa_sparse_attn",
+           "dsa_profile_indexer_last", "dsa_profile_read", "dsa_indexer_static_status", "dsa_debug_pipeline", "dsa_rope_table", "dsa_sparse_attn",
            "dsa_sparse_attn_workspace_size", "dsa_workspace_status", "indexer_desc", "indexshare_layers_forward", "lib"]

@@ -30,7 +30,7 @@ EXPORTED = ("dsa_status_string", "dsa_last_error", "dsa_donor_table", "dsa_rope_
             "dsa_layers_workspace_size", "indexshare_layers_forward", "dsa_workspace_status",
             "dsa_indexer_topk_static", "dsa_profile_enable", "dsa_profile_indexer_last", "dsa_mtp_indexshare_step",
             "dsa_indexer_topk_paged", "dsa_sparse_attn_paged", "dsa_indexer_projections", "dsa_sparse_attn_backward",
-            "dsa_indexer_static_status", "dsa_profile_read")
+            "dsa_indexer_static_status", "dsa_profile_read", "dsa_debug_pipeline")
 
 PROFILE_KINDS = {0: "rope", 1: "ranges", 2: "indexer", 3: "select", 4: "attn_prep", 5: "attn", 6: "attn_bwd",
                  7: "proj", 8: "indexer_bwd"}
@@ -112,6 +112,8 @@ def lib() -> C.CDLL:
         L.dsa_indexer_topk_static.argtypes = [P(IndexerDesc), vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp]
         L.dsa_indexer_static_status.restype = st
         L.dsa_indexer_static_status.argtypes = [vp, P(u32)]
+        L.dsa_debug_pipeline.restype = st
+        L.dsa_debug_pipeline.argtypes = [i32, C.c_uint64]
         L.dsa_profile_read.restype = st
         L.dsa_profile_read.argtypes = [P(ProfileRecord), i32, P(i32)]
         L.dsa_sparse_attn_backward.restype = st
@@ -494,3 +496,9 @@ def dsa_profile_read(cap: int = 8192) -> list:
     n = C.c_int32(0)
     _check(lib().dsa_profile_read(buf, cap, C.byref(n)))
     return [(PROFILE_KINDS.get(buf[i].kind, str(buf[i].kind)), float(buf[i].ms)) for i in range(min(n.value, cap))]
+
+
+def dsa_debug_pipeline(stop_after_tiles: int = -1, wait_ns: int = 0) -> None:
+    """Test hook: bound every pipeline wait at wait_ns (0: the default 2 s) and make the TMA
+    producers stop after stop_after_tiles tiles (-1: never).  Process-wide."""
+    _check(lib().dsa_debug_pipeline(int(stop_after_tiles), int(wait_ns)))

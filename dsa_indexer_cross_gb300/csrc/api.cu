@@ -103,6 +103,10 @@ PhaseEvents* phase_events() {
   return &p;
 }
 
+// ------------------------------------------------------------------ pipeline test hook
+std::atomic<unsigned long long> g_wait_ns{2000000000ull};
+std::atomic<int> g_stop_after{-1};
+
 // ------------------------------------------------------------------ launch log
 // Per device: a fixed ring of event pairs, created on first use and kept; records are
 // appended while profiling is on and read back (after their events complete) by
@@ -208,18 +212,22 @@ IndexerLayout indexer_layout(const dsa_indexer_desc* d, int sms) {
   p.group = indep ? (d->n_heads >= 64 ? 1 : 64 / d->n_heads) : 256 / d->n_heads;
   p.n_groups = (d->n_q + p.group - 1) / p.group;
   const long long max_len = d->max_len > 0 ? d->max_len : 1;
+  // keys one group's union of row ranges can span: a row's own range for prefill-like rows
+  // (the rows of a group share their prefix), G separate ranges for independent rows
+  long long span = max_len;
+  if (indep && p.group > 1) span = std::min<long long>(static_cast<long long>(p.group) * max_len, std::max(d->n_kv, 1));
   long long chunk;
   if (p.n_groups >= 4LL * sms) {
-    chunk = max_len;
+    chunk = span;
   } else {
-    chunk = (max_len * p.n_groups + 4LL * sms - 1) / (4LL * sms);
+    chunk = (span * p.n_groups + 4LL * sms - 1) / (4LL * sms);
     if (chunk < 4096) chunk = 4096;
   }
   if (chunk > 262144) chunk = 262144;
-  if (chunk < (max_len + 63) / 64) chunk = (max_len + 63) / 64;     // the final select reads <= 64 chunks
+  if (chunk < (span + 63) / 64) chunk = (span + 63) / 64;     // the final select reads <= 64 chunks
   chunk = (chunk + 127) / 128 * 128;
   p.chunk = static_cast<int>(chunk);
-  p.n_chunks = static_cast<int>((max_len + chunk - 1) / chunk);
+  p.n_chunks = static_cast<int>((span + chunk - 1) / chunk);
   const int cap0 = 2 * d->topk + 128;   // rows of up to 2k keys never need a cut-back
   p.cap = (cap0 + 127) / 128 * 128;
   const long long units = static_cast<long long>(p.n_groups) * p.n_chunks;
@@ -306,7 +314,8 @@ dsa_status run_indexer(const dsa_indexer_desc* d, const void* q_idx, const void*
                                                                    0x7FFFFFFF))
                              : d->n_kv;
   int ps = prof_begin(kProfRanges, st);
-  e = launch_ranges(ks, ke, d->n_q, p.group, range_limit, d->max_len, trivial_len, rr, gr, status, st);
+  e = launch_ranges(ks, ke, d->n_q, p.group, range_limit, d->max_len, trivial_len,
+                    static_cast<long long>(p.n_chunks) * p.chunk, rr, gr, status, st);
   prof_end(ps, st);
   if (e != cudaSuccess) return cuda_fail(e, "key ranges");
   if (pe) (void)cudaEventRecord(pe->ev[2], st);
@@ -326,8 +335,8 @@ dsa_status run_indexer(const dsa_indexer_desc* d, const void* q_idx, const void*
     const int q_split = rq ? rope_split_blocks(d->head_dim, d->rope_dim) : 0;
     const int k_split = rk ? rope_split_blocks(d->head_dim, d->rope_dim) : 0;
     ps = prof_begin(kProfIndexer, st);
-    e = launch_indexer(p, tq, tk, tqi, tki, q_split, k_split, pg ? *pg : PagedRows{}, w, d->n_q, rr, gr, ck, ci, cnt,
-                       status, st);
+    e = launch_indexer(p, tq, tk, tqi, tki, q_split, k_split, pg ? *pg : PagedRows{}, w, d->n_q, rr, gr, trivial_len,
+                       ck, ci, cnt, idx_out, score_out, status, pipeline_debug(), st);
     prof_end(ps, st);
     if (e != cudaSuccess) return cuda_fail(e, "indexer kernel");
   } else {
@@ -336,7 +345,10 @@ dsa_status run_indexer(const dsa_indexer_desc* d, const void* q_idx, const void*
   }
   if (pe) (void)cudaEventRecord(pe->ev[3], st);
   ps = prof_begin(kProfSelect, st);
-  e = launch_select(d->n_q, p.n_chunks, p.cap, d->topk, trivial_len, rr, ck, ci, cnt, idx_out, score_out, status, st);
+  // one key chunk per row: the indexer kernel already wrote every scored row
+  const bool only_trivial = d->n_kv > 0 && p.n_chunks == 1;
+  e = launch_select(d->n_q, p.n_chunks, p.cap, d->topk, trivial_len, only_trivial, rr, ck, ci, cnt, idx_out, score_out,
+                    status, st);
   prof_end(ps, st);
   if (e != cudaSuccess) return cuda_fail(e, "top-k select");
   if (pe) {
@@ -411,6 +423,13 @@ dsa_status run_attn(const dsa_attn_desc* d, const void* q, const void* kv, const
 }  // namespace
 
 int device_sm_count() { return dev_info().sms; }
+
+PipelineDebug pipeline_debug() {
+  PipelineDebug d;
+  d.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
+  d.stop_after_tiles = g_stop_after.load(std::memory_order_relaxed);
+  return d;
+}
 
 int prof_begin(int kind, cudaStream_t st) {
   if (!g_profile.load(std::memory_order_relaxed)) return -1;
@@ -821,6 +840,13 @@ dsa_status dsa_workspace_status(const void* ws, void* stream, uint32_t* device_b
   if (device_bits) *device_bits = h.status;
   if (h.status & DEV_ERR_TIMEOUT) return fail(DSA_ERR_TIMEOUT, "a device pipeline wait ran past its bound");
   if (h.status) return fail(DSA_ERR_DEVICE, "device status 0x%x (%u bad indices)", h.status, h.bad_count);
+  return DSA_OK;
+}
+
+dsa_status dsa_debug_pipeline(int32_t stop_after_tiles, uint64_t wait_ns) {
+  if (stop_after_tiles < -1) return fail(DSA_ERR_ARG, "stop_after_tiles must be >= -1");
+  g_stop_after.store(stop_after_tiles, std::memory_order_relaxed);
+  g_wait_ns.store(wait_ns == 0 ? 2000000000ull : static_cast<unsigned long long>(wait_ns), std::memory_order_relaxed);
   return DSA_OK;
 }
 

@@ -10,23 +10,27 @@
 // range).  The MMA puts 128 KEYS in M and the G*H_I (query, head) pairs of the group in
 // N (<= 256), so one key tile is one tcgen05.mma chain of d_I/16 instructions:
 //     S^T[key, (g, h)] = K_tile[key, :] . Q_group[(g, h), :]
-// A thread of the epilogue owns one key (one TMEM lane) and reduces the heads of every
-// query in registers, so the head sum and the ReLU/weight epilogue never leave the SM and
-// the score matrix is never written anywhere.
+// into one of two TMEM accumulators.
 //
-// Streaming top-k.  Per (row, chunk) the kernel keeps a candidate buffer of `cap` entries
-// (order-preserving score key, key index) in the workspace and a running threshold tau in
-// shared memory.  A score is appended only when it beats tau.  When a buffer could
-// overflow on the next tile the epilogue threads cut it back to a superset of its top-k (one
-// binned pass, exact radix select when the boundary bin is crowded) and raise tau to the
-// smallest kept key.  Keys of a unit are visited in increasing index order, so "beats tau" is
-// a strict comparison.
-//
-// Warp roles: warp 0 = TMA producer, warp 1 = MMA issuer (owns TMEM), then the epilogue:
-// warps 2..5 (TMEM lane quarters 2, 3, 0, 1), and with several queries per group warps 6..9
-// as a second half that takes the other half of the queries (192 or 320 threads).  Q is
-// single-buffered per unit, K tiles go through a STAGES-deep ring, S^T is double-buffered in
-// TMEM.
+// Warp roles (no role waits on a CTA-wide barrier inside the tile loop):
+//   warp 0            TMA producer: Q of the unit once, K tiles through a STAGES-deep ring;
+//   warp 1            MMA issuer (owns TMEM);
+//   head-sum warps    NE = 4 or 8: a warp owns one TMEM lane quarter (32 keys) and half or
+//                     all of the group's queries; it reduces the heads of each query in
+//                     registers (ReLU * w with packed fp32 FMAs) and writes one fp32 score per
+//                     (query, key) into a shared-memory score ring of RING tiles;
+//   top-k warps       NT <= 8: a warp owns queries g = warp, warp + NT, ...; per tile it reads
+//                     its queries' 128 scores from the ring and appends those that beat the
+//                     query's running threshold tau to the query's candidate buffer (order-
+//                     preserving score key + key index, in key order, in the workspace).  When
+//                     a buffer could overflow on the next tile the warp cuts it back alone to a
+//                     superset of its top-k (one 512-bin pass linear in score; the exact radix
+//                     select when the boundary bin is crowded) and raises tau to the smallest
+//                     kept key.  When the unit covers the whole row (one key chunk per row),
+//                     the warp also makes the row's exact final selection and writes the
+//                     indices (ascending offsets, -1 padded) itself.
+// The score matrix is never written anywhere.  Keys of a unit are visited in increasing
+// index order, so "beats tau" is a strict comparison (ties go to the lower index).
 #include <cuda_bf16.h>
 
 #include <cstddef>
@@ -39,8 +43,9 @@ namespace dsa {
 namespace {
 
 constexpr int kKeyTile = 128;
-constexpr int kMaxCap = 4224;    // cap = 2k + 128 with k <= 2048
-constexpr int kCutBins = 2048;   // value-linear bins of a cut-back
+constexpr int kBins = 512;        // value-linear bins of a warp's cut-back / final select
+constexpr int kBoundary = 128;    // boundary-bin entries ranked directly by a warp
+constexpr int kLoadsInFlight = 16;
 
 template <int HI, int DI, int G>
 struct Cfg {
@@ -48,62 +53,52 @@ struct Cfg {
   static constexpr int KB = DI / 64;                     // 128-byte K blocks per row
   static constexpr int Q_BYTES = N * DI * 2;
   static constexpr int K_STAGE_BYTES = kKeyTile * DI * 2;
-  static constexpr int SMEM_BUDGET = 232448 - 14336;     // dynamic budget after static smem
-  static constexpr int STAGES_FIT = (SMEM_BUDGET - 1024 - Q_BYTES) / K_STAGE_BYTES;
-  static constexpr int STAGES = STAGES_FIT > 6 ? 6 : STAGES_FIT;
-  static constexpr int DYN_SMEM = 1024 + Q_BYTES + STAGES * K_STAGE_BYTES;
-  static constexpr uint32_t TMEM_COLS = (2 * N <= 32) ? 32 : (2 * N <= 64) ? 64 : (2 * N <= 128) ? 128 : (2 * N <= 256) ? 256 : 512;
-  // Epilogue: one warp per TMEM lane quarter per half; with several queries per group the
-  // queries (and their TMEM columns) are split between two halves, so two warps share every
-  // lane quarter and hide each other's latencies.
+  // head-sum warps: one per TMEM lane quarter per half; with several queries per group the
+  // queries (and their TMEM columns) are split between two halves
   static constexpr int HALVES = G >= 2 && N >= 128 ? 2 : 1;
-  static constexpr int EPI = 128 * HALVES;               // epilogue threads
-  static constexpr int THREADS = 64 + EPI;
+  static constexpr int NE = 4 * HALVES;
   static constexpr int GH = G / HALVES;                  // queries per half
   static constexpr int NH = N / HALVES;                  // TMEM columns per half
+  static constexpr int NT = G < 8 ? G : 8;               // top-k warps
+  static constexpr int QPT = (G + NT - 1) / NT;          // queries per top-k warp
+  static constexpr int THREADS = 32 * (2 + NE + NT);
+  static constexpr int RING_SLOT = G * kKeyTile * 4;     // one tile's scores of the group
+  static constexpr int SMEM_MAX = 232448;                // dynamic + static per CTA
+  static constexpr int STATIC_EST = 2048 + NT * (kBins * 4 + kBoundary * 8 + 16) + NE * NH * 4;
+  static constexpr int AVAIL = SMEM_MAX - STATIC_EST - 1024 - Q_BYTES;
+  // K stages first (up to 4), then as many ring slots as fit (2 .. 16)
+  static constexpr int STAGES_FIT = (AVAIL - 2 * RING_SLOT) / K_STAGE_BYTES;
+  static constexpr int STAGES = STAGES_FIT > 4 ? 4 : STAGES_FIT;
+  static constexpr int RING_FIT = (AVAIL - STAGES * K_STAGE_BYTES) / RING_SLOT;
+  static constexpr int RING = RING_FIT > 16 ? 16 : RING_FIT;
+  static constexpr int DYN_SMEM = 1024 + Q_BYTES + STAGES * K_STAGE_BYTES + RING * RING_SLOT;
+  static constexpr uint32_t TMEM_COLS = (2 * N <= 32) ? 32 : (2 * N <= 64) ? 64 : (2 * N <= 128) ? 128 : (2 * N <= 256) ? 256 : 512;
   static_assert(N % 64 == 0 && N >= 64 && N <= 256, "MMA N");
-  static_assert(NH % 64 == 0, "epilogue reads 64 columns at a time");
-  static_assert(STAGES >= 2, "shared memory");
+  static_assert(NH % 64 == 0 || NH == 64, "head-sum reads 64 columns at a time");
+  static_assert(GH * HI == NH, "a half holds whole queries");
+  static_assert(STAGES >= 2 && RING >= 2, "shared memory");
 };
 
+// Per top-k warp scratch: histogram bins, then the boundary bin's entries.
+struct WarpScratch {
+  uint32_t hist[kBins];
+  uint32_t bkey[kBoundary];
+  int32_t bidx[kBoundary];
+  int bc[4];
+};
+
+template <int NT, int NE, int NH>
 struct Shared {
-  alignas(16) float w_s[256];   // read as float4 by the epilogue: keep 16-byte aligned
-  alignas(8) int2 rr[64];
-  uint64_t k_full[8], k_empty[8];
+  uint64_t k_full[4], k_empty[4];
   uint64_t q_full, q_empty;
   uint64_t t_full[2], t_empty[2];
+  uint64_t r_full[16], r_empty[16];
+  uint64_t mma_done;
   uint32_t tmem_base;
   uint32_t abort_flag;
-  uint32_t hist[kCutBins];   // cut-back histogram (the radix fallback uses the first 256 bins)
-  int bc[4];
-  int warp_off[8];
-  uint32_t wmin[8], wmax[8];
-  uint32_t tau[64];
-  int cnt[2][64];        // candidates held per query; [tile parity] so a tile reads one copy and writes the other
-  alignas(16) int qcnt[4][64];   // this tile's appends per (TMEM lane quarter, query)
-  int epi_abort;
+  alignas(16) float w_s[NE][NH];   // head weights of the unit, one private copy per head-sum warp
+  WarpScratch ws[NT];
 };
-static_assert(offsetof(Shared, w_s) % 16 == 0, "float4 access");
-static_assert(sizeof(Shared) <= 14336, "static shared memory within the budget the stage count assumes");
-
-// Named barrier over n threads that also returns the OR of a predicate across them.
-__device__ __forceinline__ bool bar_red_or(uint32_t id, uint32_t n, bool p) {
-  uint32_t r;
-  asm volatile(
-      "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %1, 0;\n bar.red.or.pred po, %2, %3, pi;\n selp.u32 %0, 1, 0, po;\n}\n"
-      : "=r"(r)
-      : "r"(static_cast<uint32_t>(p)), "r"(id), "r"(n)
-      : "memory");
-  return r != 0;
-}
-
-// Candidate store through the global state space.  No "memory" clobber: the compiler may keep
-// shared-memory state in registers across it (a generic store could alias shared memory).
-// The store stays in program order with the other volatile asm statements (barriers, fences)
-// that publish it.
-__device__ __forceinline__ void st_global_u32(uint32_t* p, uint32_t v) {
-  asm volatile("{\n .reg .u64 ga;\n cvta.to.global.u64 ga, %0;\n st.global.u32 [ga], %1;\n}\n" ::"l"(p), "r"(v));
-}
 
 struct UnitInfo {
   int group, chunk, kbeg, kend, n_tiles;
@@ -122,197 +117,283 @@ __device__ __forceinline__ UnitInfo unit_info(int u, int n_groups, int chunk_len
   return ui;
 }
 
-// Cut the candidate buffer of one (row, chunk) back to a superset of its top-K, keeping the
-// survivors in their original (key index) order.  Called by the NT epilogue threads together.
-//
-// The buffer only has to keep every entry that can still be in the final top-K, so the cut
-// need not be exact: one histogram of 2048 bins linear in score over the buffer's [min, max]
-// finds the bin b holding the K-th largest score, and every entry in bins >= b is kept (at
-// least K entries; bins are monotone in score, so everything dropped scores below everything
-// kept).  The new threshold is the smallest kept key: a later key at or below it has at least
-// K earlier keys at or above it and loses to them (ties go to the lower key index).  When the
-// boundary bin is crowded (many equal or nearly equal scores) so that the cut would free less
-// than half the headroom, the exact radix select (threshold (v, cut), exactly K kept) runs
-// instead.  Returns {threshold key, entries kept}.
-struct CutResult {
-  uint32_t tau;
-  int kept;
-};
-template <int NT>
-__device__ CutResult compact_buffer(uint32_t* keys, int32_t* idxs, int n, int K, int tid, Shared& sh) {
-  // Entry tid + NT i is held by thread tid in slot i (coalesced loads and stores); round i
-  // is the NT entries [NT i, NT i + NT), so list order = (round, thread) order.
-  constexpr int kMaxPer = (kMaxCap + NT - 1) / NT;
-  constexpr int NW = NT / 32;
-  const int lane = tid & 31, wq = tid >> 5;
-  const int rounds = (n + NT - 1) / NT;   // <= kMaxPer
-  uint32_t rk[kMaxPer];
-  int32_t ri[kMaxPer];
-#pragma unroll
-  for (int i = 0; i < kMaxPer; ++i) {
-    const int e = tid + i * NT;
-    const bool in = e < n;
-    rk[i] = in ? keys[e] : 0u;
-    ri[i] = in ? idxs[e] : 0;
+// Warp-uniform bounded wait (every lane polls; the result is agreed across the warp).
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                          uint32_t* status, unsigned long long limit_ns) {
+  const bool ok = mbar_wait_for(bar, parity, abort_flag, status, limit_ns);
+  return __all_sync(0xffffffffu, ok);
+}
+
+
+// ------------------------------------------------------------------ warp-level top-k helpers
+// A top-k warp works on one candidate buffer at a time (keys[], idxs[] of n entries in the
+// workspace, sorted by key index).  Entry e is held by lane e % 32; passes over a buffer keep
+// kLoadsInFlight loads per lane in flight.
+
+// Histogram increment aggregated over the lanes that hit the same bin (bin -1: none).
+__device__ __forceinline__ void warp_hist_add(uint32_t* hist, int bin) {
+  const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+  if (bin >= 0 && static_cast<int>(threadIdx.x & 31u) == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
+}
+
+// Bin of a key under a value-linear map of [fmin, fmax] onto kBins bins; monotone
+// non-decreasing in the key, so a higher bin never holds a smaller score.
+struct BinMap {
+  float fmin, scale;
+  __device__ __forceinline__ BinMap(uint32_t kmin, uint32_t kmax) {
+    fmin = key_float(kmin);
+    const float span = key_float(kmax) - fmin;
+    scale = span > 0.f && span < 3.0e38f ? static_cast<float>(kBins) / span : 0.f;
   }
-  auto sync = [] { named_bar_sync(1, NT); };
-  auto fe = [&](auto&& f) {
-#pragma unroll
-    for (int i = 0; i < kMaxPer; ++i)
-      if (tid + i * NT < n) f(rk[i], ri[i]);
-  };
-  // ---- coarse cut: key range, then one histogram pass
-  uint32_t mn = 0xFFFFFFFFu, mx = 0u;
-  fe([&](uint32_t key, int32_t) {
-    mn = min(mn, key);
-    mx = max(mx, key);
-  });
-  mn = __reduce_min_sync(0xffffffffu, mn);
-  mx = __reduce_max_sync(0xffffffffu, mx);
-  if (lane == 0) {
-    sh.wmin[wq] = mn;
-    sh.wmax[wq] = mx;
-  }
-  for (int i = tid; i < kCutBins; i += NT) sh.hist[i] = 0u;
-  sync();
-  uint32_t kmin = sh.wmin[0], kmax = sh.wmax[0];
-#pragma unroll
-  for (int w = 1; w < NW; ++w) {
-    kmin = min(kmin, sh.wmin[w]);
-    kmax = max(kmax, sh.wmax[w]);
-  }
-  const float fmin = key_float(kmin), fmax = key_float(kmax);
-  const float span = fmax - fmin;
-  const float scale = span > 0.f && span < 3.0e38f ? static_cast<float>(kCutBins) / span : 0.f;
-  auto bin_of = [&](uint32_t key) {
+  __device__ __forceinline__ int operator()(uint32_t key) const {
     const float y = (key_float(key) - fmin) * scale;
-    return y >= static_cast<float>(kCutBins - 1) ? kCutBins - 1 : (y > 0.f ? static_cast<int>(y) : 0);
-  };
-  fe([&](uint32_t key, int32_t) { atomicAdd(&sh.hist[bin_of(key)], 1u); });
-  sync();
-  // thread tid owns the kPerT bins [kCutBins - kPerT (tid + 1), kCutBins - kPerT tid), visited
-  // from the top
-  constexpr int kPerT = kCutBins / NT;
-  {
-    int h[kPerT], sum = 0;
+    return y >= static_cast<float>(kBins - 1) ? kBins - 1 : (y > 0.f ? static_cast<int>(y) : 0);
+  }
+};
+
+// The bin b holding the need-th largest entry (bins visited from the top): returns b, the
+// entries in bins above b and the entries in b.  Lane l owns bins [16 l, 16 l + 16).
+struct Boundary {
+  int b, above, hb;
+};
+__device__ __forceinline__ Boundary warp_boundary(const uint32_t* hist, int need) {
+  const int lane = threadIdx.x & 31;
+  constexpr int kPer = kBins / 32;
+  int h[kPer], s = 0;
 #pragma unroll
-    for (int j = 0; j < kPerT; ++j) {
-      h[j] = static_cast<int>(sh.hist[kCutBins - 1 - (tid * kPerT + j)]);
-      sum += h[j];
+  for (int j = 0; j < kPer; ++j) {
+    h[j] = static_cast<int>(hist[lane * kPer + j]);
+    s += h[j];
+  }
+  int x = s;   // inclusive suffix sum over lanes >= this one
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_down_sync(0xffffffffu, x, off);
+    if (lane + off < 32) x += y;
+  }
+  int c = x - s;
+  int fb = -1, fa = 0, fh = 0;
+#pragma unroll
+  for (int j = kPer - 1; j >= 0; --j) {
+    if (c < need && need <= c + h[j]) {
+      fb = lane * kPer + j;
+      fa = c;
+      fh = h[j];
     }
-    int x = sum;
+    c += h[j];
+  }
+  const uint32_t m = __ballot_sync(0xffffffffu, fb >= 0);
+  const int src = m ? __ffs(m) - 1 : 0;
+  Boundary r;
+  r.b = __shfl_sync(0xffffffffu, fb, src);
+  r.above = __shfl_sync(0xffffffffu, fa, src);
+  r.hb = __shfl_sync(0xffffffffu, fh, src);
+  return r;
+}
+
+// Calls f(valid, key, idx) for every entry of the buffer, all lanes together (f may use warp
+// collectives); with kWithIdx false, idx is not loaded (0).
+template <bool kWithIdx, class F>
+__device__ __forceinline__ void warp_for_each(const uint32_t* keys, const int32_t* idxs, int n, F&& f) {
+  const int lane = threadIdx.x & 31;
+  for (int e0 = 0; e0 < n; e0 += 32 * kLoadsInFlight) {
+    uint32_t k[kLoadsInFlight];
+    int32_t ix[kLoadsInFlight];
 #pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, x, off);
-      if (lane >= off) x += y;
+    for (int u = 0; u < kLoadsInFlight; ++u) {
+      const int e = e0 + u * 32 + lane;
+      k[u] = e < n ? keys[e] : 0u;
+      ix[u] = (kWithIdx && e < n) ? idxs[e] : 0;
     }
-    if (lane == 31) sh.warp_off[wq] = x;
-    sync();
-    int c = x - sum;
-    for (int w = 0; w < wq; ++w) c += sh.warp_off[w];
-    if (c < K && K <= c + sum) {
 #pragma unroll
-      for (int j = 0; j < kPerT; ++j) {
-        if (c < K && K <= c + h[j]) {
-          sh.bc[0] = kCutBins - 1 - (tid * kPerT + j);
-          sh.bc[1] = c + h[j];   // entries in bins >= the boundary bin
-        }
-        c += h[j];
+    for (int u = 0; u < kLoadsInFlight; ++u) f(e0 + u * 32 + lane < n, k[u], ix[u]);
+  }
+}
+
+// Exact threshold (v, cut): exactly K entries satisfy key > v || (key == v && idx <= cut),
+// the top-K by key with ties to the lower index.  One histogram pass finds the boundary bin;
+// its entries (normally a handful) are gathered and ranked directly; a crowded boundary bin
+// (many equal or nearly equal scores) falls back to radix passes over the whole buffer.
+__device__ void warp_exact_threshold(const uint32_t* keys, const int32_t* idxs, int n, int K, uint32_t kmin,
+                                     uint32_t kmax, WarpScratch& ws, int* bc, uint32_t& v, uint32_t& cut) {
+  const int lane = threadIdx.x & 31;
+  const BinMap bin(kmin, kmax);
+  for (int i = lane; i < kBins; i += 32) ws.hist[i] = 0u;
+  __syncwarp();
+  warp_for_each<false>(keys, idxs, n, [&](bool ok, uint32_t key, int32_t) { warp_hist_add(ws.hist, ok ? bin(key) : -1); });
+  __syncwarp();
+  const Boundary bd = warp_boundary(ws.hist, K);
+  if (bd.hb <= kBoundary) {
+    int got = 0;
+    warp_for_each<true>(keys, idxs, n, [&](bool ok, uint32_t key, int32_t idx) {
+      const bool in = ok && bin(key) == bd.b;
+      const uint32_t m = __ballot_sync(0xffffffffu, in);
+      if (in) {
+        const int p = got + __popc(m & ((1u << lane) - 1u));
+        ws.bkey[p] = key;
+        ws.bidx[p] = idx;
+      }
+      got += __popc(m);
+    });
+    __syncwarp();
+    const int need = K - bd.above;   // 1 <= need <= hb
+    uint32_t fv = 0, fc = 0;
+    bool found = false;
+    for (int i = lane; i < bd.hb; i += 32) {
+      const uint32_t ki = ws.bkey[i];
+      const int32_t ii = ws.bidx[i];
+      int rank = 0;
+      for (int j = 0; j < bd.hb; ++j) rank += (ws.bkey[j] > ki || (ws.bkey[j] == ki && ws.bidx[j] < ii)) ? 1 : 0;
+      if (rank == need - 1) {
+        fv = ki;
+        fc = static_cast<uint32_t>(ii);
+        found = true;
       }
     }
-    sync();
+    const uint32_t m = __ballot_sync(0xffffffffu, found);
+    const int src = m ? __ffs(m) - 1 : 0;
+    v = __shfl_sync(0xffffffffu, fv, src);
+    cut = __shfl_sync(0xffffffffu, fc, src);
+    __syncwarp();
+    return;
   }
-  const int bb = sh.bc[0], kept_coarse = sh.bc[1];
-  const int cap_free = n - kKeyTile;   // the cut is only worth it if it frees half the headroom
-  const bool coarse = kept_coarse <= K + (cap_free - K) / 2;
-  uint32_t v = 0, cut = 0x7FFFFFFFu;
-  if (!coarse) {
-    sync();
-    radix_threshold<NT>(sync, fe, tid, K, sh.hist, sh.bc, v, cut);
-  }
-  // ---- stable compaction: per round, a ballot per warp; warp counts of every round go to
-  // shared memory (sh.hist is free now), one warp turns them into exclusive offsets in
-  // (round, warp) order, and every kept entry lands at its offset + its rank in the ballot
-  uint32_t kb[kMaxPer];
-  uint32_t kmin_kept = 0xFFFFFFFFu;
-  uint32_t* rc = sh.hist;   // [kMaxPer][NW] counts, then offsets
-#pragma unroll
-  for (int i = 0; i < kMaxPer; ++i) {
-    const bool in = tid + i * NT < n;
-    const bool k = in && (coarse ? bin_of(rk[i]) >= bb : topk_keep(rk[i], ri[i], v, cut));
-    kb[i] = __ballot_sync(0xffffffffu, k);
-    if (k) kmin_kept = min(kmin_kept, rk[i]);
-    if (lane == 0 && i < rounds) rc[i * NW + wq] = __popc(kb[i]);
-  }
-  kmin_kept = __reduce_min_sync(0xffffffffu, kmin_kept);
-  if (lane == 0) sh.wmin[wq] = kmin_kept;
-  sync();
-  if (wq == 0) {
-    // exclusive scan of rounds * NW counts in order, 32 lanes x kPer entries
-    constexpr int kPer = (kMaxPer * NW + 31) / 32;
-    const int m = rounds * NW;
-    uint32_t c[kPer], sum = 0;
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-      const int e = lane * kPer + j;
-      c[j] = e < m ? rc[e] : 0u;
-      sum += c[j];
-    }
-    uint32_t x = sum;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const uint32_t y = __shfl_up_sync(0xffffffffu, x, off);
-      if (lane >= off) x += y;
-    }
-    uint32_t run = x - sum;
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-      const int e = lane * kPer + j;
-      if (e < m) rc[e] = run;
-      run += c[j];
-    }
-    if (lane == 31) sh.bc[2] = static_cast<int>(x);   // total kept
-  }
-  sync();
-  const int kept = sh.bc[2];
-  uint32_t tau = v;
-  if (coarse) {
-    tau = sh.wmin[0];
-#pragma unroll
-    for (int w = 1; w < NW; ++w) tau = min(tau, sh.wmin[w]);
-  }
-  const uint32_t below = (1u << lane) - 1u;
-#pragma unroll
-  for (int i = 0; i < kMaxPer; ++i) {
-    if (i < rounds && ((kb[i] >> lane) & 1u)) {
-      const int pos = static_cast<int>(rc[i * NW + wq] + __popc(kb[i] & below));
-      keys[pos] = rk[i];
-      idxs[pos] = ri[i];
-    }
-  }
-  __threadfence_block();
-  sync();
-  return CutResult{tau, kept};
+  __syncwarp();
+  auto fe = [&](auto&& f) {
+    warp_for_each<true>(keys, idxs, n, [&](bool ok, uint32_t key, int32_t idx) {
+      if (ok) f(key, idx);
+    });
+  };
+  radix_threshold<32>([] { __syncwarp(); }, fe, lane, K, ws.hist, bc, v, cut);
 }
+
+// Stable in-place compaction of the buffer to the entries `keep` selects; returns the count
+// and the smallest / largest kept key (warp-uniform).
+template <class Keep>
+__device__ __forceinline__ int warp_compact(uint32_t* keys, int32_t* idxs, int n, const Keep& keep, uint32_t& kmin,
+                                            uint32_t& kmax) {
+  const int lane = threadIdx.x & 31;
+  int written = 0;
+  uint32_t mn = 0xFFFFFFFFu, mx = 0u;
+  for (int e0 = 0; e0 < n; e0 += 32 * kLoadsInFlight) {
+    uint32_t k[kLoadsInFlight];
+    int32_t ix[kLoadsInFlight];
+#pragma unroll
+    for (int u = 0; u < kLoadsInFlight; ++u) {
+      const int e = e0 + u * 32 + lane;
+      k[u] = e < n ? keys[e] : 0u;
+      ix[u] = e < n ? idxs[e] : 0;
+    }
+    __syncwarp();   // every lane's loads of this batch before any store into it
+#pragma unroll
+    for (int u = 0; u < kLoadsInFlight; ++u) {
+      const bool kp = e0 + u * 32 + lane < n && keep(k[u], ix[u]);
+      const uint32_t m = __ballot_sync(0xffffffffu, kp);
+      if (kp) {
+        const int p = written + __popc(m & ((1u << lane) - 1u));
+        keys[p] = k[u];
+        idxs[p] = ix[u];
+        mn = min(mn, k[u]);
+        mx = max(mx, k[u]);
+      }
+      written += __popc(m);
+    }
+  }
+  __syncwarp();
+  kmin = __reduce_min_sync(0xffffffffu, mn);
+  kmax = __reduce_max_sync(0xffffffffu, mx);
+  return written;
+}
+
+// Cut a candidate buffer back to a superset of its top-K.  Coarse when it frees enough room:
+// every entry in the boundary bin or above is kept (>= K entries, everything dropped scores
+// below everything kept).  Otherwise exact: exactly K kept.  Either way the new threshold is
+// the smallest kept key: a later key at or below it has at least K earlier keys at or above
+// it and loses to them (ties go to the lower index).
+__device__ int warp_cut_back(uint32_t* keys, int32_t* idxs, int n, int K, int cap, uint32_t& kmin, uint32_t& kmax,
+                             WarpScratch& ws, int* bc) {
+  const int lane = threadIdx.x & 31;
+  const BinMap bin(kmin, kmax);
+  for (int i = lane; i < kBins; i += 32) ws.hist[i] = 0u;
+  __syncwarp();
+  warp_for_each<false>(keys, idxs, n, [&](bool ok, uint32_t key, int32_t) { warp_hist_add(ws.hist, ok ? bin(key) : -1); });
+  __syncwarp();
+  const Boundary bd = warp_boundary(ws.hist, K);
+  const int kept = bd.above + bd.hb;
+  __syncwarp();
+  if (kept <= K + (cap - K) / 2 && kept + kKeyTile <= cap)
+    return warp_compact(keys, idxs, n, [&](uint32_t key, int32_t) { return bin(key) >= bd.b; }, kmin, kmax);
+  uint32_t v = 0, cut = 0;
+  warp_exact_threshold(keys, idxs, n, K, kmin, kmax, ws, bc, v, cut);
+  return warp_compact(keys, idxs, n, [&](uint32_t key, int32_t idx) { return topk_keep(key, idx, v, cut); }, kmin,
+                      kmax);
+}
+
+// Final exact selection of one row from its single candidate buffer: the min(topk, L)
+// largest, ties to the lower index, written as ascending offsets from ks (the buffer is in
+// key order) and -1 padding to width topk; scores too when requested.
+__device__ void warp_final_select(const uint32_t* keys, const int32_t* idxs, int n, int Kt, int ks, int topk,
+                                  uint32_t kmin, uint32_t kmax, int32_t* out, float* score_out, WarpScratch& ws,
+                                  int* bc, uint32_t* status) {
+  const int lane = threadIdx.x & 31;
+  uint32_t v = 0, cut = 0x7FFFFFFFu;
+  const bool all = n <= Kt;
+  if (!all) warp_exact_threshold(keys, idxs, n, Kt, kmin, kmax, ws, bc, v, cut);
+  int written = 0;
+  warp_for_each<true>(keys, idxs, n, [&](bool ok, uint32_t key, int32_t idx) {
+    const bool kp = ok && (all || topk_keep(key, idx, v, cut));
+    const uint32_t m = __ballot_sync(0xffffffffu, kp);
+    if (kp) {
+      const int p = written + __popc(m & ((1u << lane) - 1u));
+      if (p < topk) {
+        out[p] = idx - ks;
+        if (score_out) score_out[p] = key_float(key);
+      }
+    }
+    written += __popc(m);
+  });
+  if (written != min(Kt, n) || n < Kt) {
+    if (lane == 0) atomicOr(status, DEV_ERR_OVERFLOW);
+  }
+  for (int p = written + lane; p < topk; p += 32) {
+    out[p] = -1;
+    if (score_out) score_out[p] = -__int_as_float(0x7f800000);
+  }
+}
+
+// ------------------------------------------------------------------ the kernel
+struct IndexerArgs {
+  const float* w;
+  int n_q;
+  const int2* row_range;
+  const int2* group_range;
+  int n_groups, n_chunks, chunk_len, cap, topk, trivial_len;
+  uint32_t* cand_key;
+  int32_t* cand_idx;
+  uint32_t* cand_cnt;
+  int32_t* idx_out;       // final indices, written here when every row is one key chunk
+  float* score_out;
+  uint32_t* status;
+  unsigned long long wait_ns;   // bound of every pipeline wait
+  int stop_after;               // test hook: the producer stops after this many key tiles (< 0: never)
+};
 
 template <int HI, int DI, int G>
 __global__ void __launch_bounds__(Cfg<HI, DI, G>::THREADS, 1)
     indexer_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                    const __grid_constant__ CUtensorMap tmap_q_in, const __grid_constant__ CUtensorMap tmap_k_in,
-                   int q_split, int k_split, const PagedRows pg,
-                   const float* __restrict__ w, int n_q, const int2* __restrict__ row_range,
-                   const int2* __restrict__ group_range, int n_groups, int n_chunks, int chunk_len, int cap, int topk,
-                   uint32_t* __restrict__ cand_key, int32_t* __restrict__ cand_idx, uint32_t* __restrict__ cand_cnt,
-                   uint32_t* status) {
+                   int q_split, int k_split, const PagedRows pg, const IndexerArgs A) {
   using C = Cfg<HI, DI, G>;
-  constexpr int N = C::N, KB = C::KB, STAGES = C::STAGES;
+  constexpr int N = C::N, KB = C::KB, STAGES = C::STAGES, RING = C::RING, NE = C::NE, NT = C::NT, NH = C::NH;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ Shared sh;
+  __shared__ Shared<NT, NE, NH> sh;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
   uint8_t* sK = smem + C::Q_BYTES;
+  float* ring = reinterpret_cast<float*>(sK + STAGES * C::K_STAGE_BYTES);   // [RING][G][128]
   const int warp = threadIdx.x >> 5;
-  const int n_units = n_groups * n_chunks;
+  const int lane = threadIdx.x & 31;
+  const int n_units = A.n_groups * A.n_chunks;
+  uint32_t* status = A.status;
   // k-th unit of this CTA, in "snake" order: forward on even rounds, backward on odd ones,
   // so a CTA that drew a long unit in one round draws a short one in the next.
   auto snake_unit = [&](int k) {
@@ -329,10 +410,14 @@ __global__ void __launch_bounds__(Cfg<HI, DI, G>::THREADS, 1)
     mbar_init(&sh.q_empty, 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sh.t_full[b], 1);
-      mbar_init(&sh.t_empty[b], C::EPI / 32);   // one arrive per epilogue warp
+      mbar_init(&sh.t_empty[b], NE);     // one arrive per head-sum warp
     }
+    for (int r = 0; r < RING; ++r) {
+      mbar_init(&sh.r_full[r], NE);
+      mbar_init(&sh.r_empty[r], NT);
+    }
+    mbar_init(&sh.mma_done, 1);
     sh.abort_flag = 0;
-    sh.epi_abort = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
   }
@@ -344,10 +429,11 @@ __global__ void __launch_bounds__(Cfg<HI, DI, G>::THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sh.tmem_base;
+  const unsigned long long wait_ns = A.wait_ns;
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
-    if (elect_lane0()) {
+    if (lane == 0) {
       tma_prefetch_desc(&tmap_q);
       tma_prefetch_desc(&tmap_k);
       tma_prefetch_desc(&tmap_q_in);
@@ -357,9 +443,9 @@ __global__ void __launch_bounds__(Cfg<HI, DI, G>::THREADS, 1)
       for (int k = 0; k * static_cast<int>(gridDim.x) < n_units && ok; ++k) {
         const int u = snake_unit(k);
         if (u >= n_units) continue;
-        const UnitInfo ui = unit_info(u, n_groups, chunk_len, group_range);
+        const UnitInfo ui = unit_info(u, A.n_groups, A.chunk_len, A.group_range);
         if (ui.n_tiles == 0) continue;
-        if (q_uses > 0) ok = mbar_wait(&sh.q_empty, (q_uses - 1) & 1, &sh.abort_flag, status);
+        if (q_uses > 0) ok = mbar_wait_for(&sh.q_empty, (q_uses - 1) & 1, &sh.abort_flag, status, wait_ns);
         if (!ok) break;
         mbar_arrive_expect_tx(&sh.q_full, C::Q_BYTES);
         // 64-dim blocks without rotary dims come from the unrotated input
@@ -367,9 +453,13 @@ __global__ void __launch_bounds__(Cfg<HI, DI, G>::THREADS, 1)
           tma_load_2d(sQ + b * N * 128, b < q_split ? &tmap_q_in : &tmap_q, &sh.q_full, b * 64, ui.group * N);
         ++q_uses;
         for (int i = 0; i < ui.n_tiles; ++i, ++kstage) {
+          if (A.stop_after >= 0 && kstage >= static_cast<uint32_t>(A.stop_after)) {
+            ok = false;   // test hook: stop feeding the pipeline; its waits then run out
+            break;
+          }
           const int s = kstage % STAGES;
           if (kstage >= STAGES) {
-            ok = mbar_wait(&sh.k_empty[s], ((kstage / STAGES) - 1) & 1, &sh.abort_flag, status);
+            ok = mbar_wait_for(&sh.k_empty[s], ((kstage / STAGES) - 1) & 1, &sh.abort_flag, status, wait_ns);
             if (!ok) break;
           }
           mbar_arrive_expect_tx(&sh.k_full[s], C::K_STAGE_BYTES);
@@ -392,26 +482,30 @@ __global__ void __launch_bounds__(Cfg<HI, DI, G>::THREADS, 1)
             tma_load_2d(dst + b * kKeyTile * 128, b < k_split ? &tmap_k_in : &tmap_k, &sh.k_full[s], b * 64, krow);
         }
       }
+      // let copies still in flight land before the CTA can exit (bounded; normally all done)
+      if (q_uses > 0) mbar_drain(&sh.q_full, (q_uses - 1) & 1, 200000000ull);
+      for (uint32_t j = kstage > STAGES ? kstage - STAGES : 0; j < kstage; ++j)
+        mbar_drain(&sh.k_full[j % STAGES], (j / STAGES) & 1, 200000000ull);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
-    if (elect_lane0()) {
+    if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(128, N, 0, 0);
       uint32_t kstage = 0, q_uses = 0, tile = 0;
       bool ok = true;
       for (int k = 0; k * static_cast<int>(gridDim.x) < n_units && ok; ++k) {
         const int u = snake_unit(k);
         if (u >= n_units) continue;
-        const UnitInfo ui = unit_info(u, n_groups, chunk_len, group_range);
+        const UnitInfo ui = unit_info(u, A.n_groups, A.chunk_len, A.group_range);
         if (ui.n_tiles == 0) continue;
-        ok = mbar_wait(&sh.q_full, q_uses & 1, &sh.abort_flag, status);
+        ok = mbar_wait_for(&sh.q_full, q_uses & 1, &sh.abort_flag, status, wait_ns);
         if (!ok) break;
         ++q_uses;
         for (int i = 0; i < ui.n_tiles; ++i, ++kstage, ++tile) {
           const int s = kstage % STAGES;
           const int buf = tile & 1;
-          ok = mbar_wait(&sh.k_full[s], (kstage / STAGES) & 1, &sh.abort_flag, status);
-          if (ok && tile >= 2) ok = mbar_wait(&sh.t_empty[buf], ((tile >> 1) - 1) & 1, &sh.abort_flag, status);
+          ok = mbar_wait_for(&sh.k_full[s], (kstage / STAGES) & 1, &sh.abort_flag, status, wait_ns);
+          if (ok && tile >= 2) ok = mbar_wait_for(&sh.t_empty[buf], ((tile >> 1) - 1) & 1, &sh.abort_flag, status, wait_ns);
           if (!ok) break;
           tc_fence_after();
           const uint32_t a0 = smem_u32(sK + s * C::K_STAGE_BYTES);
@@ -428,209 +522,197 @@ __global__ void __launch_bounds__(Cfg<HI, DI, G>::THREADS, 1)
         }
         if (ok) umma_commit(&sh.q_empty);
       }
+      // every MMA issued has completed before TMEM is released
+      umma_commit(&sh.mma_done);
+      mbar_drain(&sh.mma_done, 0, 200000000ull);
     }
-  } else {
-    // ------------------------------------------------------------------ epilogue
-    constexpr int EPI = C::EPI, GH = C::GH, NH = C::NH;
-    const int tid = threadIdx.x - 64;          // 0 .. EPI - 1
+  } else if (warp < 2 + NE) {
+    // ------------------------------------------------------------------ head-sum warps
+    const int hw = warp - 2;
     const int quarter = warp & 3;              // TMEM lane quarter this warp may access
-    const int half = tid / 128;                // queries [half * GH, half * GH + GH)
-    const int g0 = half * GH;
-    const int lane = threadIdx.x & 31;
+    const int half = hw >> 2;                  // queries [half * GH, half * GH + GH)
+    const int g0 = half * C::GH;
     const int row = quarter * 32 + lane;       // key within the tile
     const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
-    // A failed (timed-out) wait reaches every epilogue warp through the per-tile
-    // barrier-reduction (fast tiles) or through sh.epi_abort, written only before the
-    // barrier-reduction and read only after it (slow tiles), so all epilogue warps leave the
-    // loops at the same point.
+    float* w_s = sh.w_s[hw];
     uint32_t tile = 0;
-    bool stop = false;
-    for (int k = 0; k * static_cast<int>(gridDim.x) < n_units && !stop; ++k) {
+    bool ok = true;
+    for (int k = 0; k * static_cast<int>(gridDim.x) < n_units && ok; ++k) {
       const int u = snake_unit(k);
       if (u >= n_units) continue;
-      const UnitInfo ui = unit_info(u, n_groups, chunk_len, group_range);
-      const int t0 = ui.group * G;
-      // per-unit state
-      for (int i = tid; i < N; i += EPI) {
+      const UnitInfo ui = unit_info(u, A.n_groups, A.chunk_len, A.group_range);
+      if (ui.n_tiles == 0) continue;
+      // this warp's private copy of the head weights of its queries
+      const int t0 = ui.group * G + g0;
+      for (int i = lane; i < NH; i += 32) {
         const int t = t0 + i / HI;
-        sh.w_s[i] = t < n_q ? __ldg(w + static_cast<size_t>(t) * HI + (i % HI)) : 0.f;
+        w_s[i] = t < A.n_q ? __ldg(A.w + static_cast<size_t>(t) * HI + (i % HI)) : 0.f;
       }
-      if (tid < G) {
-        const int t = t0 + tid;
-        sh.rr[tid] = t < n_q ? row_range[t] : make_int2(0, 0);
-        sh.tau[tid] = 0u;
-        sh.cnt[tile & 1][tid] = 0;
-      }
-      named_bar_sync(1, EPI);
+      __syncwarp();
       for (int i = 0; i < ui.n_tiles; ++i, ++tile) {
         const int buf = tile & 1;
+        const int slot = tile % RING;
+        ok = warp_wait(&sh.t_full[buf], (tile >> 1) & 1, &sh.abort_flag, status, wait_ns);
+        if (ok && tile >= RING) ok = warp_wait(&sh.r_empty[slot], ((tile / RING) - 1) & 1, &sh.abort_flag, status, wait_ns);
+        if (!ok) break;
+        tc_fence_after();
+        // head sum of this half's queries with NP independent partial sums per query (breaks
+        // the dependent FMA chain); TMEM read 64 columns per wait
+        constexpr int NP = HI >= 16 ? 4 : 1;
+        constexpr int GH = C::GH;
+        float part[GH][NP];
+#pragma unroll
+        for (int g = 0; g < GH; ++g)
+#pragma unroll
+          for (int p = 0; p < NP; ++p) part[g][p] = 0.f;
+#pragma unroll
+        for (int c0 = 0; c0 < NH; c0 += 64) {
+          const int cc = half * NH + c0;   // TMEM column of this chunk
+          uint32_t v[64];
+          tmem_ld32(tmem + t_lane + buf * N + cc, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+          tmem_ld32(tmem + t_lane + buf * N + cc + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 64; j += 4) {
+            const float4 wv = *reinterpret_cast<const float4*>(&w_s[c0 + j]);
+            const float r0 = fmaxf(__uint_as_float(v[j]), 0.f), r1 = fmaxf(__uint_as_float(v[j + 1]), 0.f);
+            const float r2 = fmaxf(__uint_as_float(v[j + 2]), 0.f), r3 = fmaxf(__uint_as_float(v[j + 3]), 0.f);
+            const int gl = (c0 + j) / HI;   // query within the half
+            if constexpr (NP == 4) {
+              fma2(part[gl][0], part[gl][1], wv.x, wv.y, r0, r1);
+              fma2(part[gl][2], part[gl][3], wv.z, wv.w, r2, r3);
+            } else {
+              const float wj[4] = {wv.x, wv.y, wv.z, wv.w}, rj[4] = {r0, r1, r2, r3};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                float& acc_e = part[(c0 + j + e) / HI][0];
+                acc_e = fmaf(wj[e], rj[e], acc_e);
+              }
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.t_empty[buf]);
+        float* rs = ring + static_cast<size_t>(slot) * G * kKeyTile;
+#pragma unroll
+        for (int g = 0; g < GH; ++g) {
+          float acc;
+          if constexpr (NP == 4) acc = (part[g][0] + part[g][1]) + (part[g][2] + part[g][3]);
+          else acc = part[g][0];
+          rs[(g0 + g) * kKeyTile + row] = acc;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.r_full[slot]);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------------ top-k warps
+    const int tw = warp - 2 - NE;               // queries tw, tw + NT, ...
+    constexpr int QPT = C::QPT;
+    WarpScratch& ws = sh.ws[tw];
+    const uint32_t below = (1u << lane) - 1u;
+    const int cap = A.cap, topk = A.topk;
+    const bool final_here = A.n_chunks == 1;
+    uint32_t tile = 0;
+    bool ok = true;
+    for (int k = 0; k * static_cast<int>(gridDim.x) < n_units && ok; ++k) {
+      const int u = snake_unit(k);
+      if (u >= n_units) continue;
+      const UnitInfo ui = unit_info(u, A.n_groups, A.chunk_len, A.group_range);
+      if (ui.n_tiles == 0) continue;
+      // per owned query: key range within this unit, count, threshold, key extremes
+      int qa[QPT], qb[QPT], cnt[QPT];
+      uint32_t tau[QPT], lmin[QPT], lmax[QPT];
+      bool live[QPT];
+#pragma unroll
+      for (int qi = 0; qi < QPT; ++qi) {
+        const int g = tw + qi * NT;
+        const int t = ui.group * G + g;
+        int2 rr = make_int2(0, 0);
+        if (g < G && t < A.n_q) rr = A.row_range[t];
+        live[qi] = g < G && t < A.n_q && rr.y - rr.x > A.trivial_len;
+        qa[qi] = max(rr.x, ui.kbeg);
+        qb[qi] = live[qi] ? min(rr.y, ui.kend) : qa[qi];
+        cnt[qi] = 0;
+        tau[qi] = 0u;
+        lmin[qi] = 0xFFFFFFFFu;
+        lmax[qi] = 0u;
+      }
+      for (int i = 0; i < ui.n_tiles; ++i, ++tile) {
+        const int slot = tile % RING;
+        ok = warp_wait(&sh.r_full[slot], (tile / RING) & 1, &sh.abort_flag, status, wait_ns);
+        if (!ok) break;
+        const float* rs = ring + static_cast<size_t>(slot) * G * kKeyTile;
         const int tile0 = ui.kbeg + i * kKeyTile;
-        // Fast tile: no query's buffer has been cut back yet and none can fill up through
-        // this tile (uniform across the CTA).  tau is then still below every key, so every
-        // in-range key is appended and its slot is its offset in the range: no ballots, no
-        // counts exchanged.  Counts only grow with i, so once a tile is slow the rest are.
-        bool fast = true;
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const int2 rr = sh.rr[g];
-          const int a = max(rr.x, ui.kbeg), b = min(rr.y, ui.kend);
-          fast = fast && min(b, tile0 + kKeyTile) - a <= cap - kKeyTile;
-        }
-        bool ok = mbar_wait(&sh.t_full[buf], (tile >> 1) & 1, &sh.abort_flag, status);
-        ok = __all_sync(0xffffffffu, ok);
-        uint32_t msk[GH];
-        uint32_t key[GH];
-        float acc[GH];
-        if (ok) {
-          tc_fence_after();
-          // Head sum of this half's queries with NP independent partial sums per query
-          // (breaks the dependent FMA chain), TMEM read 64 columns per wait.
-          constexpr int NP = HI >= 16 ? 4 : 1;
-          float part[GH][NP];
+        for (int qi = 0; qi < QPT; ++qi) {
+          const int g = tw + qi * NT;
+          if (g >= G) continue;
+          if (tile0 >= qb[qi] || tile0 + kKeyTile <= qa[qi]) continue;   // warp-uniform
+          const size_t off = (static_cast<size_t>(ui.group * G + g) * A.n_chunks + ui.chunk) * cap;
+          uint32_t* ck = A.cand_key + off;
+          int32_t* ci = A.cand_idx + off;
 #pragma unroll
-          for (int g = 0; g < GH; ++g)
-#pragma unroll
-            for (int p = 0; p < NP; ++p) part[g][p] = 0.f;
-#pragma unroll
-          for (int c0 = 0; c0 < NH; c0 += 64) {
-            const int cc = half * NH + c0;   // TMEM column of this chunk
-            uint32_t v[64];
-            tmem_ld32(tmem + t_lane + buf * N + cc, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-            tmem_ld32(tmem + t_lane + buf * N + cc + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-            tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 64; j += 4) {
-              const float4 wv = *reinterpret_cast<const float4*>(&sh.w_s[cc + j]);
-              const float r0 = fmaxf(__uint_as_float(v[j]), 0.f), r1 = fmaxf(__uint_as_float(v[j + 1]), 0.f);
-              const float r2 = fmaxf(__uint_as_float(v[j + 2]), 0.f), r3 = fmaxf(__uint_as_float(v[j + 3]), 0.f);
-              const int gl = (c0 + j) / HI;   // query within the half
-              if constexpr (NP == 4) {
-                // columns cc+j .. cc+j+3 feed partial sums 0..3 of query gl: two packed FMAs
-                fma2(part[gl][0], part[gl][1], wv.x, wv.y, r0, r1);
-                fma2(part[gl][2], part[gl][3], wv.z, wv.w, r2, r3);
-              } else {
-                const float wj[4] = {wv.x, wv.y, wv.z, wv.w}, rj[4] = {r0, r1, r2, r3};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  float& acc_e = part[(c0 + j + e) / HI][0];
-                  acc_e = fmaf(wj[e], rj[e], acc_e);
-                }
+          for (int r = 0; r < 4; ++r) {
+            const int j = tile0 + r * 32 + lane;
+            const uint32_t key = float_key(rs[g * kKeyTile + r * 32 + lane]);
+            const bool pass = j >= qa[qi] && j < qb[qi] && key > tau[qi];
+            const uint32_t m = __ballot_sync(0xffffffffu, pass);
+            if (pass) {
+              const int p = cnt[qi] + __popc(m & below);
+              if (p < cap) {
+                ck[p] = key;
+                ci[p] = j;
               }
+              lmin[qi] = min(lmin[qi], key);
+              lmax[qi] = max(lmax[qi], key);
             }
-          }
-#pragma unroll
-          for (int g = 0; g < GH; ++g) {
-            if constexpr (NP == 4) acc[g] = (part[g][0] + part[g][1]) + (part[g][2] + part[g][3]);
-            else acc[g] = part[g][0];
-          }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sh.t_empty[buf]);
-          if (fast) {
-            // every in-range key is appended: key j of query g goes to slot j - a_g
-            const int j = tile0 + row;
-            const size_t rowbase = (static_cast<size_t>(t0) * n_chunks + ui.chunk) * cap;
-#pragma unroll
-            for (int gl = 0; gl < GH; ++gl) {
-              const int g = g0 + gl;
-              const int2 rr = sh.rr[g];
-              const int a = max(rr.x, ui.kbeg), b = min(rr.y, ui.kend);
-              if (j >= a && j < b) {
-                const size_t off = rowbase + static_cast<size_t>(g) * n_chunks * cap + (j - a);
-                st_global_u32(cand_key + off, float_key(acc[gl]));
-                st_global_u32(reinterpret_cast<uint32_t*>(cand_idx) + off, static_cast<uint32_t>(j));
-              }
-            }
-            if (tid < G) {
-              const int2 rr = sh.rr[tid];
-              const int a = max(rr.x, ui.kbeg), b = min(rr.y, ui.kend);
-              sh.cnt[(tile & 1) ^ 1][tid] = max(0, min(b, tile0 + kKeyTile) - a);
-            }
+            cnt[qi] += __popc(m);
           }
         }
-        if (fast) {
-          // one barrier-reduction per tile carries a timed-out wait to every epilogue warp
-          if (bar_red_or(1, EPI, !ok)) {
-            stop = true;
-            break;
-          }
-          continue;
-        }
-        if (ok) {
-          // append candidates that beat the running threshold, in key order: per query the
-          // four lane quarters publish their counts, then each writes after the lower ones
-          const int j = tile0 + row;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.r_empty[slot]);
+        // cut back any buffer that could overflow on the next tile
 #pragma unroll
-          for (int gl = 0; gl < GH; ++gl) {
-            const int g = g0 + gl;
-            const int2 rr = sh.rr[g];
-            key[gl] = float_key(acc[gl]);
-            msk[gl] = __ballot_sync(0xffffffffu, j >= rr.x && j < rr.y && j < ui.kend && key[gl] > sh.tau[g]);
+        for (int qi = 0; qi < QPT; ++qi) {
+          const int g = tw + qi * NT;
+          if (g >= G || cnt[qi] <= cap - kKeyTile) continue;
+          const size_t off = (static_cast<size_t>(ui.group * G + g) * A.n_chunks + ui.chunk) * cap;
+          if (cnt[qi] > cap) {
+            if (lane == 0) atomicOr(status, DEV_ERR_OVERFLOW);
+            cnt[qi] = cap;
           }
-          if (lane == 0) {
-#pragma unroll
-            for (int gl = 0; gl < GH; ++gl) sh.qcnt[quarter][g0 + gl] = __popc(msk[gl]);
-          }
-        }
-        named_bar_sync(1, EPI);                               // X: per-quarter counts published
-        const int cur = tile & 1, nxt = cur ^ 1;
-        bool need = false;
-        if (ok) {
-          const int j = tile0 + row;
-          // every query's write offset first (shared loads only), then the global stores
-          int pos[GH];
-#pragma unroll
-          for (int gl = 0; gl < GH; ++gl) pos[gl] = sh.cnt[cur][g0 + gl] + __popc(msk[gl] & ((1u << lane) - 1u));
-          for (int q = 0; q < quarter; ++q) {
-#pragma unroll
-            for (int gl = 0; gl < GH; ++gl) pos[gl] += sh.qcnt[q][g0 + gl];
-          }
-          int tot = 0;
-          if (tid < G) tot = (sh.qcnt[0][tid] + sh.qcnt[1][tid]) + (sh.qcnt[2][tid] + sh.qcnt[3][tid]);
-          const size_t rowbase = (static_cast<size_t>(t0) * n_chunks + ui.chunk) * cap;
-#pragma unroll
-          for (int gl = 0; gl < GH; ++gl) {
-            if (((msk[gl] >> lane) & 1u) && pos[gl] < cap) {
-              const size_t off = rowbase + static_cast<size_t>(g0 + gl) * n_chunks * cap + pos[gl];
-              st_global_u32(cand_key + off, key[gl]);
-              st_global_u32(reinterpret_cast<uint32_t*>(cand_idx) + off, static_cast<uint32_t>(j));
-            }
-          }
-          if (tid < G) {
-            const int n = sh.cnt[cur][tid] + tot;
-            sh.cnt[nxt][tid] = n;
-            need = n > cap - kKeyTile;                      // could overflow on the next tile
-          }
-        }
-        // Y: one barrier-reduction decides whether anything beyond the appends is needed (a
-        // cut-back or an abort).  The abort flag is written before it and read only in the
-        // slow path, between it and one more barrier, so all epilogue warps branch alike.
-        if (!ok && lane == 0) sh.epi_abort = 1;
-        if (bar_red_or(1, EPI, need || !ok)) {
-          stop = sh.epi_abort != 0;
-          named_bar_sync(1, EPI);
-          if (stop) break;
-#pragma unroll 1
-          for (int g = 0; g < G; ++g) {
-            const int n = sh.cnt[nxt][g];
-            if (n > cap - kKeyTile) {
-              const size_t off = (static_cast<size_t>(t0 + g) * n_chunks + ui.chunk) * cap;
-              __threadfence_block();
-              const CutResult cr = compact_buffer<EPI>(cand_key + off, cand_idx + off, n, topk, tid, sh);
-              if (tid == 0) {
-                sh.tau[g] = cr.tau;
-                sh.cnt[nxt][g] = cr.kept;
-              }
-              named_bar_sync(1, EPI);
-            }
-          }
+          __syncwarp();   // this warp's appends are visible to all its lanes
+          uint32_t kmin = __reduce_min_sync(0xffffffffu, lmin[qi]), kmax = __reduce_max_sync(0xffffffffu, lmax[qi]);
+          cnt[qi] = warp_cut_back(A.cand_key + off, A.cand_idx + off, cnt[qi], topk, cap, kmin, kmax, ws, ws.bc);
+          tau[qi] = kmin;
+          lmin[qi] = kmin;
+          lmax[qi] = kmax;
         }
       }
-      if (stop) break;
-      if (tid < G && t0 + tid < n_q)
-        cand_cnt[static_cast<size_t>(t0 + tid) * n_chunks + ui.chunk] =
-            static_cast<uint32_t>(min(sh.cnt[tile & 1][tid], cap));
-      named_bar_sync(1, EPI);
+      if (!ok) break;
+      // the unit is done: final selection of rows finished here, else the chunk's count
+#pragma unroll 1
+      for (int qi = 0; qi < QPT; ++qi) {
+        const int g = tw + qi * NT;
+        const int t = ui.group * G + g;
+        if (g >= G || t >= A.n_q) continue;
+        const size_t off = (static_cast<size_t>(t) * A.n_chunks + ui.chunk) * cap;
+        const int n = min(cnt[qi], cap);
+        __syncwarp();
+        if (!final_here) {
+          if (lane == 0) A.cand_cnt[static_cast<size_t>(t) * A.n_chunks + ui.chunk] = static_cast<uint32_t>(n);
+          continue;
+        }
+        if (!live[qi]) continue;   // trivial and empty rows are written by the select pass
+        const int2 rr = A.row_range[t];
+        const int Kt = min(topk, rr.y - rr.x);
+        const uint32_t kmin = __reduce_min_sync(0xffffffffu, lmin[qi]), kmax = __reduce_max_sync(0xffffffffu, lmax[qi]);
+        warp_final_select(A.cand_key + off, A.cand_idx + off, n, Kt, rr.x, topk, kmin, kmax,
+                          A.idx_out + static_cast<size_t>(t) * topk,
+                          A.score_out ? A.score_out + static_cast<size_t>(t) * topk : nullptr, ws, ws.bc, status);
+      }
     }
   }
 
@@ -641,16 +723,20 @@ __global__ void __launch_bounds__(Cfg<HI, DI, G>::THREADS, 1)
 
 template <int HI, int DI, int G>
 cudaError_t launch_t(const IndexerPlan& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tqi,
-                     const CUtensorMap& tki, int q_split, int k_split, const PagedRows& pg, const float* w, int n_q,
-                     const int2* row_range, const int2* group_range, uint32_t* ck, int32_t* ci, uint32_t* cc,
-                     uint32_t* status, cudaStream_t st) {
+                     const CUtensorMap& tki, int q_split, int k_split, const PagedRows& pg, const IndexerArgs& A,
+                     cudaStream_t st) {
   using C = Cfg<HI, DI, G>;
   auto kern = indexer_kernel<HI, DI, G>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::DYN_SMEM);
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  kern<<<p.grid, C::THREADS, C::DYN_SMEM, st>>>(tq, tk, tqi, tki, q_split, k_split, pg, w, n_q, row_range, group_range,
-                                             p.n_groups, p.n_chunks,
-                                             p.chunk, p.cap, p.topk, ck, ci, cc, status);
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::DYN_SMEM);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  kern<<<p.grid, C::THREADS, C::DYN_SMEM, st>>>(tq, tk, tqi, tki, q_split, k_split, pg, A);
   return cudaGetLastError();
 }
 
@@ -659,14 +745,33 @@ cudaError_t launch_t(const IndexerPlan& p, const CUtensorMap& tq, const CUtensor
 
 cudaError_t launch_indexer(const IndexerPlan& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tqi,
                            const CUtensorMap& tki, int q_split, int k_split, const PagedRows& pg, const float* w, int n_q,
-                           const int2* row_range, const int2* group_range, uint32_t* ck, int32_t* ci, uint32_t* cc,
-                           uint32_t* status, cudaStream_t st) {
+                           const int2* row_range, const int2* group_range, int trivial_len, uint32_t* ck, int32_t* ci,
+                           uint32_t* cc, int32_t* idx_out, float* score_out, uint32_t* status,
+                           const PipelineDebug& dbg, cudaStream_t st) {
   if (p.n_groups * p.n_chunks == 0) return cudaSuccess;
   if (pg.block_table && (p.group != 1 || p.chunk % kPageRows != 0)) return cudaErrorInvalidValue;
+  IndexerArgs A;
+  A.w = w;
+  A.n_q = n_q;
+  A.row_range = row_range;
+  A.group_range = group_range;
+  A.n_groups = p.n_groups;
+  A.n_chunks = p.n_chunks;
+  A.chunk_len = p.chunk;
+  A.cap = p.cap;
+  A.topk = p.topk;
+  A.trivial_len = trivial_len;
+  A.cand_key = ck;
+  A.cand_idx = ci;
+  A.cand_cnt = cc;
+  A.idx_out = idx_out;
+  A.score_out = score_out;
+  A.status = status;
+  A.wait_ns = dbg.wait_ns;
+  A.stop_after = dbg.stop_after_tiles;
 #define DSA_IDX_CASE(HI_, DI_, G_)                                                                      \
   if (p.n_heads == HI_ && p.head_dim == DI_ && p.group == G_)                                           \
-    return launch_t<HI_, DI_, G_>(p, tq, tk, tqi, tki, q_split, k_split, pg, w, n_q, row_range, group_range, ck, ci, cc, \
-                                  status, st);
+    return launch_t<HI_, DI_, G_>(p, tq, tk, tqi, tki, q_split, k_split, pg, A, st);
   DSA_IDX_CASE(4, 64, 64)
   DSA_IDX_CASE(8, 64, 32)
   DSA_IDX_CASE(16, 64, 16)

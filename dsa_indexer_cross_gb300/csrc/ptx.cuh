@@ -62,19 +62,32 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 
 // Bounded wait.  `abort_flag` is a CTA-shared word: once any waiter in the CTA has timed out
 // every other waiter gives up at once instead of serving its own full timeout.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag,
-                                          uint32_t* dev_status) {
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                              uint32_t* dev_status, unsigned long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       *abort_flag = 1u;
       if (dev_status) atomicOr(dev_status, DEV_ERR_TIMEOUT);
       return false;
     }
   }
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                          uint32_t* dev_status) {
+  return mbar_wait_for(bar, parity, abort_flag, dev_status, kWaitLimitNs);
+}
+// Bounded wait that ignores the abort flag: used at exit to let copies already in flight land
+// before the CTA's shared memory is released.  Returns false (and records nothing) when the
+// limit passes.
+__device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity, unsigned long long limit_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  return true;
 }
 
 // ------------------------------------------------------------------------------- TMA

@@ -115,7 +115,8 @@ __global__ void __launch_bounds__(256) rope_rows_scalar(const uint16_t* __restri
 // group's union of non-trivial ranges is gathered with shared-memory atomics.
 __global__ void __launch_bounds__(256) ranges_kernel(const int32_t* __restrict__ ks, const int32_t* __restrict__ ke,
                                                      int n_q, int group, int n_kv, int max_len, int trivial_len,
-                                                     int2* row_range, int2* group_range, uint32_t* status) {
+                                                     long long span_limit, int2* row_range, int2* group_range,
+                                                     uint32_t* status) {
   __shared__ int s_lo[256], s_hi[256];
   const int per_block = 256 / group;
   if (static_cast<int>(threadIdx.x) < per_block) {
@@ -141,7 +142,12 @@ __global__ void __launch_bounds__(256) ranges_kernel(const int32_t* __restrict__
   __syncthreads();
   const int g = blockIdx.x * per_block + static_cast<int>(threadIdx.x);
   if (static_cast<int>(threadIdx.x) < per_block && g * group < n_q) {
-    const int lo = s_lo[threadIdx.x], hi = s_hi[threadIdx.x];
+    const int lo = s_lo[threadIdx.x];
+    int hi = s_hi[threadIdx.x];
+    if (lo < hi && static_cast<long long>(hi) - lo > span_limit) {
+      atomicOr(status, DEV_ERR_RANGE);   // rows of one group further apart than the plan covers
+      hi = static_cast<int>(lo + span_limit);
+    }
     group_range[g] = lo < hi ? make_int2(lo, hi) : make_int2(0, 0);
   }
 }
@@ -169,10 +175,11 @@ cudaError_t launch_rope_rows(const void* in, void* out, const int32_t* pos, int6
 }
 
 cudaError_t launch_ranges(const int32_t* ks, const int32_t* ke, int n_q, int group, int n_kv, int max_len,
-                          int trivial_len, int2* row_range, int2* group_range, uint32_t* status, cudaStream_t st) {
+                          int trivial_len, long long span_limit, int2* row_range, int2* group_range,
+                          uint32_t* status, cudaStream_t st) {
   if (n_q <= 0) return cudaSuccess;
   if (group < 1 || 256 % group != 0) return cudaErrorInvalidValue;
-  ranges_kernel<<<(n_q + 255) / 256, 256, 0, st>>>(ks, ke, n_q, group, n_kv, max_len, trivial_len, row_range,
+  ranges_kernel<<<(n_q + 255) / 256, 256, 0, st>>>(ks, ke, n_q, group, n_kv, max_len, trivial_len, span_limit, row_range,
                                                    group_range, status);
   return cudaGetLastError();
 }

@@ -129,6 +129,7 @@ __device__ bool linear_threshold(const ForEach& fe, int tid, int K, LinearSmem& 
 
 template <bool kRegs>
 __global__ void __launch_bounds__(kSelThreads) select_kernel(int n_chunks, int cap, int topk, int trivial_len,
+                                                             bool only_trivial,
                                                              const int2* __restrict__ row_range,
                                                              const uint32_t* __restrict__ cand_key,
                                                              const int32_t* __restrict__ cand_idx,
@@ -143,6 +144,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(int n_chunks, int c
   const int t = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int2 r = row_range[t];
+  if (only_trivial && r.y - r.x > trivial_len) return;   // written by the indexer kernel
   if (r.y - r.x <= trivial_len) {
     // the whole range is selected: offsets 0 .. L-1 in order, no candidates read.  The host
     // passes trivial_len = 0 whenever scores are requested, so only empty rows get here then.
@@ -332,17 +334,18 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(int n_chunks, int c
 
 }  // namespace
 
-cudaError_t launch_select(int n_q, int n_chunks, int cap, int topk, int trivial_len, const int2* row_range,
+cudaError_t launch_select(int n_q, int n_chunks, int cap, int topk, int trivial_len, bool only_trivial,
+                          const int2* row_range,
                           const uint32_t* cand_key,
                           const int32_t* cand_idx, const uint32_t* cand_cnt, int32_t* idx_out, float* score_out,
                           uint32_t* status, cudaStream_t st) {
   if (n_q <= 0) return cudaSuccess;
   if (n_chunks > kMaxChunks) return cudaErrorInvalidValue;
   if (static_cast<long long>(n_chunks) * cap <= static_cast<long long>(kSelThreads) * kSelPer)
-    select_kernel<true><<<n_q, kSelThreads, 0, st>>>(n_chunks, cap, topk, trivial_len, row_range, cand_key, cand_idx, cand_cnt,
+    select_kernel<true><<<n_q, kSelThreads, 0, st>>>(n_chunks, cap, topk, trivial_len, only_trivial, row_range, cand_key, cand_idx, cand_cnt,
                                                     idx_out, score_out, status);
   else
-    select_kernel<false><<<n_q, kSelThreads, 0, st>>>(n_chunks, cap, topk, trivial_len, row_range, cand_key, cand_idx, cand_cnt,
+    select_kernel<false><<<n_q, kSelThreads, 0, st>>>(n_chunks, cap, topk, trivial_len, only_trivial, row_range, cand_key, cand_idx, cand_cnt,
                                                      idx_out, score_out, status);
   return cudaGetLastError();
 }

@@ -97,6 +97,7 @@ struct ACfg {
 struct AShared {
   uint64_t full[2], empty[2];   // per tile slot set (nine 64-dim blocks)
   uint64_t q_full, q_empty, s_full[2], s_empty[2], p_full, o_done[2], o_free;   // o_done[g & 1]: PV(g) complete
+  uint64_t mma_done;            // both MMA warps' last commits: nothing of theirs in flight
   uint32_t tmem_base, abort_flag, soft_abort;
   uint32_t prod_ok;
   alignas(16) float red[4][64];
@@ -218,7 +219,8 @@ __global__ void __launch_bounds__(ACfg<HB, HD>::THREADS, 1)
                        const int32_t* __restrict__ ks, const PagedRows pg, const int32_t* __restrict__ row_nt,
                        const int2* __restrict__ block_range, const uint32_t* __restrict__ block_mask,
                        uint16_t* __restrict__ out, float* __restrict__ lse, int n_q, int n_kv, int H, int topk,
-                       float scale_log2, uint32_t* status, uint32_t* bad_count) {
+                       float scale_log2, uint32_t* status, uint32_t* bad_count, unsigned long long wait_ns,
+                       int stop_after) {
   using C = ACfg<HB, HD>;
   constexpr bool DENSE = C::DENSE;
   constexpr int B = C::B;
@@ -255,6 +257,7 @@ __global__ void __launch_bounds__(ACfg<HB, HD>::THREADS, 1)
     mbar_init(&sh.o_done[0], 1);
     mbar_init(&sh.o_done[1], 1);
     mbar_init(&sh.o_free, C::SW);
+    mbar_init(&sh.mma_done, 2);
     sh.abort_flag = 0;
     sh.soft_abort = 0;
     fence_mbar_init();
@@ -291,7 +294,7 @@ __global__ void __launch_bounds__(ACfg<HB, HD>::THREADS, 1)
       if (I.nt == 0) continue;
       bool w_ok = true;
       if (tid == 0) {
-        if (it > 0) w_ok = mbar_wait(&sh.q_empty, (it - 1) & 1, &sh.abort_flag, status);
+        if (it > 0) w_ok = mbar_wait_for(&sh.q_empty, (it - 1) & 1, &sh.abort_flag, status, wait_ns);
         if (w_ok) {
           // the item's HB consecutive (token, head) rows of q, as nine boxes of HB x 64 dims;
           // rows past the end of q read as zeros, and columns past the last head are never stored
@@ -309,8 +312,12 @@ __global__ void __launch_bounds__(ACfg<HB, HD>::THREADS, 1)
         if (tid == 0) {
           for (int i = 0; i < I.nt && ok; ++i, ++g) {
             const int s = g & 1;
+            if (stop_after >= 0 && g >= static_cast<uint32_t>(stop_after)) {
+              ok = false;   // test hook: stop feeding the pipeline; the waits behind it run out
+              break;
+            }
             if (g >= 2) {
-              ok = mbar_wait(&sh.empty[s], ((g >> 1) - 1) & 1, &sh.abort_flag, status);
+              ok = mbar_wait_for(&sh.empty[s], ((g >> 1) - 1) & 1, &sh.abort_flag, status, wait_ns);
               if (!ok) break;
             }
             mbar_arrive_expect_tx(&sh.full[s], kKB * kBlkBytes);
@@ -360,9 +367,10 @@ __global__ void __launch_bounds__(ACfg<HB, HD>::THREADS, 1)
 #pragma unroll
             for (int m = 0; m < 8; ++m) crow[m] = row_of(i * kRows + (tid >> 3) + 8 * m, false);
           }
-          w_ok = true;
-          if (tid == 0) {
-            if (g >= 2) w_ok = mbar_wait(&sh.empty[g & 1], ((g >> 1) - 1) & 1, &sh.abort_flag, status);
+          // test hook: stop feeding the pipeline; the waits behind it run out
+          w_ok = stop_after < 0 || g < static_cast<uint32_t>(stop_after);
+          if (tid == 0 && w_ok) {
+            if (g >= 2) w_ok = mbar_wait_for(&sh.empty[g & 1], ((g >> 1) - 1) & 1, &sh.abort_flag, status, wait_ns);
             if (w_ok) mbar_arrive_expect_tx(&sh.full[g & 1], kTmaBlocks * kBlkBytes);
           }
           ok = sync_ok(w_ok);
@@ -387,6 +395,13 @@ __global__ void __launch_bounds__(ACfg<HB, HD>::THREADS, 1)
         }
       }
       ++it;
+    }
+    // let every copy this CTA started land before its shared memory can be released
+    // (bounded; after a normal run everything has landed already)
+    if constexpr (!DENSE && kCpBlocks > 0) cp_async_wait<0>();
+    if (tid == 0) {
+      if (it > 0) mbar_drain(&sh.q_full, (it - 1) & 1, 200000000ull);
+      for (uint32_t j = g > 2 ? g - 2 : 0; j < g; ++j) mbar_drain(&sh.full[j & 1], (j >> 1) & 1, 200000000ull);
     }
   } else if ((warp >= 3 && warp < 7) || warp >= 8) {
     // ---------------------------------------------------------------- softmax + epilogue
@@ -463,7 +478,7 @@ __global__ void __launch_bounds__(ACfg<HB, HD>::THREADS, 1)
             rv1 = j1 >= 0 && kst + j1 >= 0 && kst + j1 < n_kv;
           }
         }
-        bool ok = mbar_wait(&sh.s_full[sb], (g >> 1) & 1, &sh.abort_flag, status);
+        bool ok = mbar_wait_for(&sh.s_full[sb], (g >> 1) & 1, &sh.abort_flag, status, wait_ns);
         ok = __all_sync(0xffffffffu, ok);
         float sc[4 * NR];   // [4k + j]: j = 0,1 row r0 columns 8k+cq, +1;  j = 2,3 row r0 + 8
         bool need = false;
@@ -515,7 +530,7 @@ __global__ void __launch_bounds__(ACfg<HB, HD>::THREADS, 1)
             }
             // O^T may only be rescaled once the previous tile's PV has finished
             if (i > 0) {
-              ok = mbar_wait(&sh.o_done[(g - 1) & 1], ((g - 1) >> 1) & 1, &sh.abort_flag, status);
+              ok = mbar_wait_for(&sh.o_done[(g - 1) & 1], ((g - 1) >> 1) & 1, &sh.abort_flag, status, wait_ns);
               ok = __all_sync(0xffffffffu, ok);
               if (!ok && lane == 0) sh.soft_abort = 1;
             }
@@ -613,7 +628,7 @@ __global__ void __launch_bounds__(ACfg<HB, HD>::THREADS, 1)
           if (lane < 4) sh.red[qd][c_off + 8 * kk + cq + e] = x;
         }
       }
-      bool ok = mbar_wait(&sh.o_done[(g - 1) & 1], ((g - 1) >> 1) & 1, &sh.abort_flag, status);
+      bool ok = mbar_wait_for(&sh.o_done[(g - 1) & 1], ((g - 1) >> 1) & 1, &sh.abort_flag, status, wait_ns);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok && lane == 0) sh.soft_abort = 1;
       named_bar_sync(1, kSoft);
@@ -676,7 +691,7 @@ __global__ void __launch_bounds__(ACfg<HB, HD>::THREADS, 1)
     uint32_t g = 0, it = 0;
     bool ok = true;
     auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
-      return __all_sync(0xffffffffu, mbar_wait(bar, parity, &sh.abort_flag, status));
+      return __all_sync(0xffffffffu, mbar_wait_for(bar, parity, &sh.abort_flag, status, wait_ns));
     };
     const bool qk_warp = warp == 2;
     const uint64_t dq0 = sdesc_sw128(smem_u32(sQ), 16, 1024);       // Q: B operand of S^T, K-major
@@ -732,6 +747,9 @@ __global__ void __launch_bounds__(ACfg<HB, HD>::THREADS, 1)
       }
       ++it;
     }
+    // every MMA this warp issued has completed before TMEM is released
+    umma_commit_elect(&sh.mma_done);
+    mbar_drain(&sh.mma_done, 0, 200000000ull);
   }
   tc_fence_before();
   __syncthreads();
@@ -862,11 +880,13 @@ cudaError_t launch_cfg(const CUtensorMap& tmap, const CUtensorMap& tmap_q, int n
   if (e != cudaSuccess) return e;
   const int n_items = C::DENSE ? (n_q + C::B - 1) / C::B : n_q * ((H + HB - 1) / HB);
   const int grid = n_items < device_sm_count() ? n_items : device_sm_count();
+  const PipelineDebug dbg = pipeline_debug();
   const int ps = prof_begin(kProfAttn, st);
   kern<<<grid, C::THREADS, C::DYN_SMEM, st>>>(tmap, tmap_q, static_cast<const uint16_t*>(kv), idx, ks, pg, row_nt,
                                             block_range, block_mask,
                                             static_cast<uint16_t*>(out), lse, n_q, n_kv, H, topk,
-                                            scale * 1.4426950408889634f, status, status + 1);
+                                            scale * 1.4426950408889634f, status, status + 1, dbg.wait_ns,
+                                            dbg.stop_after_tiles);
   prof_end(ps, st);
   return cudaGetLastError();
 }

@@ -421,6 +421,19 @@ typedef struct dsa_profile_record {
 } dsa_profile_record;
 dsa_status dsa_profile_read(dsa_profile_record* out, int32_t cap, int32_t* n);
 
+/* ------------------------------------------------------------------ testing --------- */
+
+/* Test hook for the bounded pipeline waits (the pages have no counterpart).  Every
+ * mbarrier wait inside the library's pipelined kernels gives up after wait_ns nanoseconds of
+ * device time (0 restores the default, 2 s): the waiting warp records a timeout in the
+ * workspace status word (DSA_ERR_TIMEOUT from dsa_workspace_status), every other warp of its
+ * block stops at its next wait, copies already in flight are allowed to land, and the kernel
+ * returns -- the context stays usable.  stop_after_tiles >= 0 makes the TMA producer of the
+ * indexer and sparse-attention kernels stop after that many tiles, so that the waits behind
+ * it run out; -1 (the default) never stops.  Process-wide; applies to calls made after it.
+ * Meant for tests only.  Errors: DSA_ERR_ARG (stop_after_tiles < -1). */
+dsa_status dsa_debug_pipeline(int32_t stop_after_tiles, uint64_t wait_ns);
+
 #ifdef __cplusplus
 }
 #endif
