@@ -748,7 +748,12 @@ def run_native(args):
         with ClockSampler(local) as clk2:
             for name in extras:
                 wx = synth.WORKLOADS[name]
-                r, _ = measure(D, wx, max(3, args.steps // 2), args.warmup, dev, stream, flush, rank, world)
+                try:
+                    r, _ = measure(D, wx, max(3, args.steps // 2), args.warmup, dev, stream, flush, rank, world)
+                except Exception as exc:   # keep the headline line; say what failed
+                    line["workloads"][name] = {"error": f"{type(exc).__name__}: {exc}"}
+                    torch.cuda.empty_cache()
+                    continue
                 line["workloads"][name] = {
                     "value": r["value"], "ms_per_step": r["ms_per_step"], "config": r["config"],
                     "gpu_launches": r["gpu_launches"], "roofline": r["roofline"],

@@ -620,7 +620,16 @@ __global__ void __launch_bounds__(Cfg<HI, DI, G>::THREADS, 1)
       const int u = snake_unit(k);
       if (u >= n_units) continue;
       const UnitInfo ui = unit_info(u, A.n_groups, A.chunk_len, A.group_range);
-      if (ui.n_tiles == 0) continue;
+      if (ui.n_tiles == 0) {
+        // an empty chunk still tells the final select that it holds no candidates
+        if (!final_here && lane == 0) {
+          for (int g = tw; g < G; g += NT) {
+            const int t = ui.group * G + g;
+            if (t < A.n_q) A.cand_cnt[static_cast<size_t>(t) * A.n_chunks + ui.chunk] = 0u;
+          }
+        }
+        continue;
+      }
       // per owned query: key range within this unit, count, threshold, key extremes
       int qa[QPT], qb[QPT], cnt[QPT];
       uint32_t tau[QPT], lmin[QPT], lmax[QPT];
