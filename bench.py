@@ -71,6 +71,8 @@ def parse(argv=None):
                          "shuffled) against the contiguous calls on the same data, under 'paged'")
     ap.add_argument("--only", choices=["attn", "indexer"], default=None,
                     help="run just one kernel call of the workload (for profiler captures); prints nothing")
+    ap.add_argument("--n-q", type=int, default=0,
+                    help="with --only: that many query rows of the workload instead of all (a smaller capture)")
     return ap.parse_args(argv)
 
 
@@ -697,6 +699,8 @@ def run_native(args):
     w = synth.WORKLOADS[args.workload]
     stream = torch.cuda.current_stream(dev)
     if args.only is not None:
+        if args.n_q > 0:
+            w = w.replace(n_q=args.n_q)
         return run_only(D, w, args, dev, stream)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     hbm, tc_burst, tc_sus, peak_kind = peaks()

@@ -180,7 +180,7 @@ bool supported_heads(int h) { return h == 4 || h == 8 || h == 16 || h == 32 || h
 
 struct IndexerLayout {
   IndexerPlan plan{};
-  size_t off_q = 0, off_k = 0, off_rr = 0, off_gr = 0, off_cnt = 0, off_key = 0, off_idx = 0, total = 0;
+  size_t off_q = 0, off_k = 0, off_rr = 0, off_gr = 0, off_cnt = 0, off_edge = 0, off_key = 0, off_idx = 0, total = 0;
 };
 
 dsa_status check_indexer_desc(const dsa_indexer_desc* d) {
@@ -209,7 +209,9 @@ IndexerLayout indexer_layout(const dsa_indexer_desc* d, int sms) {
   p.n_heads = d->n_heads;
   p.head_dim = d->head_dim;
   p.topk = d->topk;
-  p.group = indep ? (d->n_heads >= 64 ? 1 : 64 / d->n_heads) : 256 / d->n_heads;
+  // G rows share a key stream: N = G * H_I <= 256 MMA columns, at most 16 rows (the score ring
+  // of a unit holds one tile's scores of every row); independent rows fill only 64 columns
+  p.group = indep ? (d->n_heads >= 64 ? 1 : 64 / d->n_heads) : std::min(256 / d->n_heads, 16);
   p.n_groups = (d->n_q + p.group - 1) / p.group;
   const long long max_len = d->max_len > 0 ? d->max_len : 1;
   // keys one group's union of row ranges can span: a row's own range for prefill-like rows
@@ -228,8 +230,12 @@ IndexerLayout indexer_layout(const dsa_indexer_desc* d, int sms) {
   chunk = (chunk + 127) / 128 * 128;
   p.chunk = static_cast<int>(chunk);
   p.n_chunks = static_cast<int>((span + chunk - 1) / chunk);
-  const int cap0 = 2 * d->topk + 128;   // rows of up to 2k keys never need a cut-back
-  p.cap = (cap0 + 127) / 128 * 128;
+  // candidates per (row, chunk): every key of a chunk when it has at most 16K, else 16K (the
+  // streaming threshold keeps about k (1 + ln(chunk / k)) of them; more only for scores that
+  // keep rising along the keys, which the kernel handles by cutting the buffer back)
+  const long long span_keys = std::min<long long>(chunk, span);
+  p.cap = static_cast<int>(std::min<long long>((span_keys + 127) / 128 * 128, 16384));
+  if (p.cap < 2 * d->topk + 256 && span_keys > p.cap) p.cap = (2 * d->topk + 256 + 127) / 128 * 128;
   const long long units = static_cast<long long>(p.n_groups) * p.n_chunks;
   p.grid = static_cast<int>(units < sms ? units : sms);
   if (p.grid < 1) p.grid = 1;
@@ -247,6 +253,8 @@ IndexerLayout indexer_layout(const dsa_indexer_desc* d, int sms) {
   off += align_up(static_cast<size_t>(p.n_groups) * 8);
   const size_t slots = static_cast<size_t>(d->n_q) * p.n_chunks;
   L.off_cnt = off;
+  off += align_up(slots * 4);
+  L.off_edge = off;
   off += align_up(slots * 4);
   L.off_key = off;
   off += align_up(slots * p.cap * 4);
@@ -320,6 +328,7 @@ dsa_status run_indexer(const dsa_indexer_desc* d, const void* q_idx, const void*
   if (e != cudaSuccess) return cuda_fail(e, "key ranges");
   if (pe) (void)cudaEventRecord(pe->ev[2], st);
   uint32_t* cnt = reinterpret_cast<uint32_t*>(base + L.off_cnt);
+  uint32_t* edge = reinterpret_cast<uint32_t*>(base + L.off_edge);
   uint32_t* ck = reinterpret_cast<uint32_t*>(base + L.off_key);
   int32_t* ci = reinterpret_cast<int32_t*>(base + L.off_idx);
   if (d->n_kv > 0) {
@@ -336,18 +345,17 @@ dsa_status run_indexer(const dsa_indexer_desc* d, const void* q_idx, const void*
     const int k_split = rk ? rope_split_blocks(d->head_dim, d->rope_dim) : 0;
     ps = prof_begin(kProfIndexer, st);
     e = launch_indexer(p, tq, tk, tqi, tki, q_split, k_split, pg ? *pg : PagedRows{}, w, d->n_q, rr, gr, trivial_len,
-                       ck, ci, cnt, idx_out, score_out, status, pipeline_debug(), st);
+                       ck, ci, cnt, edge, status, pipeline_debug(), st);
     prof_end(ps, st);
     if (e != cudaSuccess) return cuda_fail(e, "indexer kernel");
   } else {
-    if ((e = cudaMemsetAsync(cnt, 0, static_cast<size_t>(d->n_q) * p.n_chunks * 4, st)) != cudaSuccess)
+    if ((e = cudaMemsetAsync(cnt, 0, static_cast<size_t>(d->n_q) * p.n_chunks * 4, st)) != cudaSuccess ||
+        (e = cudaMemsetAsync(edge, 0, static_cast<size_t>(d->n_q) * p.n_chunks * 4, st)) != cudaSuccess)
       return cuda_fail(e, "clear counts");
   }
   if (pe) (void)cudaEventRecord(pe->ev[3], st);
   ps = prof_begin(kProfSelect, st);
-  // one key chunk per row: the indexer kernel already wrote every scored row
-  const bool only_trivial = d->n_kv > 0 && p.n_chunks == 1;
-  e = launch_select(d->n_q, p.n_chunks, p.cap, d->topk, trivial_len, only_trivial, rr, ck, ci, cnt, idx_out, score_out,
+  e = launch_select(d->n_q, p.n_chunks, p.cap, d->topk, trivial_len, rr, edge, ck, ci, cnt, idx_out, score_out,
                     status, st);
   prof_end(ps, st);
   if (e != cudaSuccess) return cuda_fail(e, "top-k select");

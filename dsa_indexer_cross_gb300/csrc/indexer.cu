@@ -12,25 +12,29 @@
 //     S^T[key, (g, h)] = K_tile[key, :] . Q_group[(g, h), :]
 // into one of two TMEM accumulators.
 //
+// Candidates.  Every (row, chunk) has a buffer of `cap` (order-preserving score key, key
+// index) entries in key order; launch_select later picks each row's exact top-k from them.
+// A row whose key range in the chunk fits the buffer is written DIRECTLY: every key's score at
+// its offset.  A longer one is FILTERED: a key is kept only if its score is at or above the
+// lower edge tau of the histogram bin that holds the row's k-th largest kept score so far
+// (bins of a fixed log-spaced map of the score key), because every key below that edge has at
+// least k kept keys above it; the expected number kept over N keys is about k (1 + ln(N/k)).
+//
 // Warp roles (no role waits on a CTA-wide barrier inside the tile loop):
 //   warp 0            TMA producer: Q of the unit once, K tiles through a STAGES-deep ring;
 //   warp 1            MMA issuer (owns TMEM);
 //   head-sum warps    NE = 4 or 8: a warp owns one TMEM lane quarter (32 keys) and half or
 //                     all of the group's queries; it reduces the heads of each query in
-//                     registers (ReLU * w with packed fp32 FMAs) and writes one fp32 score per
-//                     (query, key) into a shared-memory score ring of RING tiles;
-//   top-k warps       NT <= 8: a warp owns queries g = warp, warp + NT, ...; per tile it reads
-//                     its queries' 128 scores from the ring and appends those that beat the
-//                     query's running threshold tau to the query's candidate buffer (order-
-//                     preserving score key + key index, in key order, in the workspace).  When
-//                     a buffer could overflow on the next tile the warp cuts it back alone to a
-//                     superset of its top-k (one 512-bin pass linear in score; the exact radix
-//                     select when the boundary bin is crowded) and raises tau to the smallest
-//                     kept key.  When the unit covers the whole row (one key chunk per row),
-//                     the warp also makes the row's exact final selection and writes the
-//                     indices (ascending offsets, -1 padded) itself.
-// The score matrix is never written anywhere.  Keys of a unit are visited in increasing
-// index order, so "beats tau" is a strict comparison (ties go to the lower index).
+//                     registers (ReLU * w with packed fp32 FMAs).  Direct rows: it stores
+//                     the scores itself.  Filtered rows: it writes the tile's scores and, per
+//                     lane quarter, the mask of keys at or above tau into a shared-memory
+//                     ring slot;
+//   top-k warps       NT <= 4, filtered rows only: a warp owns queries g = warp, warp + NT, ...;
+//                     per tile it appends the marked keys of its queries in key order, counts
+//                     them in the query's histogram, raises tau and publishes it.  Should a
+//                     buffer still fill up (scores rising along the keys), the warp cuts it
+//                     back to exactly the top-k and rebuilds the histogram.
+// The score matrix is never written anywhere.
 #include <cuda_bf16.h>
 
 #include <cstddef>
@@ -43,9 +47,13 @@ namespace dsa {
 namespace {
 
 constexpr int kKeyTile = 128;
-constexpr int kBins = 512;        // value-linear bins of a warp's cut-back / final select
-constexpr int kBoundary = 128;    // boundary-bin entries ranked directly by a warp
+constexpr int kBins = 256;        // value-linear bins of a warp's cut-back
+constexpr int kBoundary = 64;     // boundary-bin entries ranked directly by a warp
 constexpr int kLoadsInFlight = 16;
+constexpr int kLog2Span = 5;      // the threshold histogram covers 2^kLog2Span octaves of scores ...
+constexpr int kLowExp = 127 - 16; // ... starting at 2^-16 (lower scores share the bottom bin)
+
+constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
 
 template <int HI, int DI, int G>
 struct Cfg {
@@ -59,27 +67,47 @@ struct Cfg {
   static constexpr int NE = 4 * HALVES;
   static constexpr int GH = G / HALVES;                  // queries per half
   static constexpr int NH = N / HALVES;                  // TMEM columns per half
-  static constexpr int NT = G < 8 ? G : 8;               // top-k warps
+  static constexpr int NT = G < 4 ? G : 4;               // top-k warps
   static constexpr int QPT = (G + NT - 1) / NT;          // queries per top-k warp
   static constexpr int THREADS = 32 * (2 + NE + NT);
-  static constexpr int RING_SLOT = G * kKeyTile * 4;     // one tile's scores of the group
+  // threshold histogram: NB bins per query (16 KB in all), log-spaced over 2^kLog2Span octaves
+  static constexpr int NB = 4096 / G < 1024 ? 4096 / G : 1024;
+  static constexpr int SHIFT = 23 + ilog2(1 << kLog2Span) - ilog2(NB);   // key bits below the bin index
+  static constexpr uint32_t BASE = (0x80000000u | (static_cast<uint32_t>(kLowExp) << 23)) >> SHIFT;
+  // ring slot: the tile's scores of every query, then one keep-mask per (query, lane quarter)
+  static constexpr int RING_SCORES = G * kKeyTile * 4;
+  static constexpr int RING_SLOT = RING_SCORES + G * 4 * 4;
   static constexpr int SMEM_MAX = 232448;                // dynamic + static per CTA
-  static constexpr int STATIC_EST = 2048 + NT * (kBins * 4 + kBoundary * 8 + 16) + NE * NH * 4;
+  static constexpr int STATIC_EST = 2048 + NE * NH * 4 + G * NB * 4 + NT * 1600 + G * 8;
   static constexpr int AVAIL = SMEM_MAX - STATIC_EST - 1024 - Q_BYTES;
-  // K stages first (up to 4), then as many ring slots as fit (2 .. 16)
-  static constexpr int STAGES_FIT = (AVAIL - 2 * RING_SLOT) / K_STAGE_BYTES;
-  static constexpr int STAGES = STAGES_FIT > 4 ? 4 : STAGES_FIT;
+  static constexpr int RING_RESERVE = RING_SLOT <= 8192 ? 4 : 2;
+  static constexpr int STAGES_FIT = (AVAIL - RING_RESERVE * RING_SLOT) / K_STAGE_BYTES;
+  static constexpr int STAGES = STAGES_FIT > 6 ? 6 : STAGES_FIT;
   static constexpr int RING_FIT = (AVAIL - STAGES * K_STAGE_BYTES) / RING_SLOT;
   static constexpr int RING = RING_FIT > 16 ? 16 : RING_FIT;
   static constexpr int DYN_SMEM = 1024 + Q_BYTES + STAGES * K_STAGE_BYTES + RING * RING_SLOT;
   static constexpr uint32_t TMEM_COLS = (2 * N <= 32) ? 32 : (2 * N <= 64) ? 64 : (2 * N <= 128) ? 128 : (2 * N <= 256) ? 256 : 512;
   static_assert(N % 64 == 0 && N >= 64 && N <= 256, "MMA N");
-  static_assert(NH % 64 == 0 || NH == 64, "head-sum reads 64 columns at a time");
+  static_assert(NH % 64 == 0, "head-sum reads 64 columns at a time");
   static_assert(GH * HI == NH, "a half holds whole queries");
   static_assert(STAGES >= 2 && RING >= 2, "shared memory");
+  static_assert((1 << (SHIFT + ilog2(NB))) == (1 << (23 + kLog2Span)), "NB bins span 2^kLog2Span octaves");
 };
 
-// Per top-k warp scratch: histogram bins, then the boundary bin's entries.
+// Threshold-histogram bin of a score key under Cfg C's map (monotone non-decreasing; scores
+// below 2^-16, negative ones included, share bin 0; scores above the span share the top bin)
+// and the smallest key of a bin.
+template <class C>
+__device__ __forceinline__ int hist_bin(uint32_t key) {
+  const int b = static_cast<int>(key >> C::SHIFT) - static_cast<int>(C::BASE);
+  return b < 0 ? 0 : (b >= C::NB ? C::NB - 1 : b);
+}
+template <class C>
+__device__ __forceinline__ uint32_t bin_edge_key(int b) {
+  return static_cast<uint32_t>(b + static_cast<int>(C::BASE)) << C::SHIFT;
+}
+
+// Per top-k warp scratch of a cut-back: histogram bins, then the boundary bin's entries.
 struct WarpScratch {
   uint32_t hist[kBins];
   uint32_t bkey[kBoundary];
@@ -87,16 +115,18 @@ struct WarpScratch {
   int bc[4];
 };
 
-template <int NT, int NE, int NH>
+template <int G, int NT, int NE, int NH, int NB>
 struct Shared {
-  uint64_t k_full[4], k_empty[4];
+  uint64_t k_full[6], k_empty[6];
   uint64_t q_full, q_empty;
   uint64_t t_full[2], t_empty[2];
   uint64_t r_full[16], r_empty[16];
   uint64_t mma_done;
   uint32_t tmem_base;
   uint32_t abort_flag;
+  uint64_t tau[G];                 // per query: (unit ordinal << 32) | threshold key, published by its top-k warp
   alignas(16) float w_s[NE][NH];   // head weights of the unit, one private copy per head-sum warp
+  uint32_t hist[G][NB];            // threshold histograms (filtered rows)
   WarpScratch ws[NT];
 };
 
@@ -117,13 +147,31 @@ __device__ __forceinline__ UnitInfo unit_info(int u, int n_groups, int chunk_len
   return ui;
 }
 
+// A query's key range within a unit and whether it is scored (rows of at most trivial_len
+// keys are left to the select pass) and filtered (longer than direct_max keys).
+struct QueryRange {
+  int a, b;
+  bool live, filtered;
+};
+__device__ __forceinline__ QueryRange query_range(const int2* row_range, int t, int n_q, const UnitInfo& ui,
+                                                  int trivial_len, int direct_max) {
+  QueryRange r;
+  int2 rr = make_int2(0, 0);
+  if (t < n_q) rr = row_range[t];
+  r.live = t < n_q && rr.y - rr.x > trivial_len;
+  r.a = max(rr.x, ui.kbeg);
+  r.b = r.live ? min(rr.y, ui.kend) : r.a;
+  if (r.b < r.a) r.b = r.a;
+  r.filtered = r.b - r.a > direct_max;
+  return r;
+}
+
 // Warp-uniform bounded wait (every lane polls; the result is agreed across the warp).
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag,
                                           uint32_t* status, unsigned long long limit_ns) {
   const bool ok = mbar_wait_for(bar, parity, abort_flag, status, limit_ns);
   return __all_sync(0xffffffffu, ok);
 }
-
 
 // ------------------------------------------------------------------ warp-level top-k helpers
 // A top-k warp works on one candidate buffer at a time (keys[], idxs[] of n entries in the
@@ -328,38 +376,6 @@ __device__ int warp_cut_back(uint32_t* keys, int32_t* idxs, int n, int K, int ca
                       kmax);
 }
 
-// Final exact selection of one row from its single candidate buffer: the min(topk, L)
-// largest, ties to the lower index, written as ascending offsets from ks (the buffer is in
-// key order) and -1 padding to width topk; scores too when requested.
-__device__ void warp_final_select(const uint32_t* keys, const int32_t* idxs, int n, int Kt, int ks, int topk,
-                                  uint32_t kmin, uint32_t kmax, int32_t* out, float* score_out, WarpScratch& ws,
-                                  int* bc, uint32_t* status) {
-  const int lane = threadIdx.x & 31;
-  uint32_t v = 0, cut = 0x7FFFFFFFu;
-  const bool all = n <= Kt;
-  if (!all) warp_exact_threshold(keys, idxs, n, Kt, kmin, kmax, ws, bc, v, cut);
-  int written = 0;
-  warp_for_each<true>(keys, idxs, n, [&](bool ok, uint32_t key, int32_t idx) {
-    const bool kp = ok && (all || topk_keep(key, idx, v, cut));
-    const uint32_t m = __ballot_sync(0xffffffffu, kp);
-    if (kp) {
-      const int p = written + __popc(m & ((1u << lane) - 1u));
-      if (p < topk) {
-        out[p] = idx - ks;
-        if (score_out) score_out[p] = key_float(key);
-      }
-    }
-    written += __popc(m);
-  });
-  if (written != min(Kt, n) || n < Kt) {
-    if (lane == 0) atomicOr(status, DEV_ERR_OVERFLOW);
-  }
-  for (int p = written + lane; p < topk; p += 32) {
-    out[p] = -1;
-    if (score_out) score_out[p] = -__int_as_float(0x7f800000);
-  }
-}
-
 // ------------------------------------------------------------------ the kernel
 struct IndexerArgs {
   const float* w;
@@ -367,11 +383,11 @@ struct IndexerArgs {
   const int2* row_range;
   const int2* group_range;
   int n_groups, n_chunks, chunk_len, cap, topk, trivial_len;
+  int direct_max;               // rows with at most this many keys in a chunk are stored whole
   uint32_t* cand_key;
   int32_t* cand_idx;
   uint32_t* cand_cnt;
-  int32_t* idx_out;       // final indices, written here when every row is one key chunk
-  float* score_out;
+  uint32_t* cand_edge;          // per (row, chunk): a key below which no entry can be in the row's top-k (0: none)
   uint32_t* status;
   unsigned long long wait_ns;   // bound of every pipeline wait
   int stop_after;               // test hook: the producer stops after this many key tiles (< 0: never)
@@ -385,20 +401,29 @@ __global__ void __launch_bounds__(Cfg<HI, DI, G>::THREADS, 1)
   using C = Cfg<HI, DI, G>;
   constexpr int N = C::N, KB = C::KB, STAGES = C::STAGES, RING = C::RING, NE = C::NE, NT = C::NT, NH = C::NH;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ Shared<NT, NE, NH> sh;
+  __shared__ Shared<G, NT, NE, NH, C::NB> sh;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
   uint8_t* sK = smem + C::Q_BYTES;
-  float* ring = reinterpret_cast<float*>(sK + STAGES * C::K_STAGE_BYTES);   // [RING][G][128]
+  uint8_t* ring = sK + STAGES * C::K_STAGE_BYTES;   // [RING] x (scores [G][128] fp32, masks [G][4])
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int n_units = A.n_groups * A.n_chunks;
   uint32_t* status = A.status;
+  const int cap = A.cap;
   // k-th unit of this CTA, in "snake" order: forward on even rounds, backward on odd ones,
   // so a CTA that drew a long unit in one round draws a short one in the next.
   auto snake_unit = [&](int k) {
     const int g = static_cast<int>(gridDim.x), b = static_cast<int>(blockIdx.x);
     return k * g + ((k & 1) ? (g - 1 - b) : b);
+  };
+  // whether any row of the unit is filtered (the ring is used only then); every role derives
+  // it from the same row ranges
+  auto unit_filtered = [&](const UnitInfo& ui) {
+    bool f = false;
+    for (int g = 0; g < G; ++g)
+      f = f || query_range(A.row_range, ui.group * G + g, A.n_q, ui, A.trivial_len, A.direct_max).filtered;
+    return f;
   };
 
   if (threadIdx.x == 0) {
@@ -417,6 +442,7 @@ __global__ void __launch_bounds__(Cfg<HI, DI, G>::THREADS, 1)
       mbar_init(&sh.r_empty[r], NT);
     }
     mbar_init(&sh.mma_done, 1);
+    for (int g = 0; g < G; ++g) sh.tau[g] = 0xFFFFFFFF00000000ull;   // no unit yet: no threshold
     sh.abort_flag = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
@@ -528,38 +554,49 @@ __global__ void __launch_bounds__(Cfg<HI, DI, G>::THREADS, 1)
     }
   } else if (warp < 2 + NE) {
     // ------------------------------------------------------------------ head-sum warps
+    constexpr int GH = C::GH;
     const int hw = warp - 2;
     const int quarter = warp & 3;              // TMEM lane quarter this warp may access
     const int half = hw >> 2;                  // queries [half * GH, half * GH + GH)
-    const int g0 = half * C::GH;
+    const int g0 = half * GH;
     const int row = quarter * 32 + lane;       // key within the tile
     const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
     float* w_s = sh.w_s[hw];
-    uint32_t tile = 0;
+    uint32_t tile = 0, rtile = 0, unit_ord = 0;
     bool ok = true;
     for (int k = 0; k * static_cast<int>(gridDim.x) < n_units && ok; ++k) {
       const int u = snake_unit(k);
       if (u >= n_units) continue;
       const UnitInfo ui = unit_info(u, A.n_groups, A.chunk_len, A.group_range);
       if (ui.n_tiles == 0) continue;
-      // this warp's private copy of the head weights of its queries
+      const bool uses_ring = unit_filtered(ui);
+      // this warp's private copy of the head weights of its queries, and their key ranges
       const int t0 = ui.group * G + g0;
       for (int i = lane; i < NH; i += 32) {
         const int t = t0 + i / HI;
         w_s[i] = t < A.n_q ? __ldg(A.w + static_cast<size_t>(t) * HI + (i % HI)) : 0.f;
       }
+      int qa[GH], qb[GH];
+      bool qf[GH];
+#pragma unroll
+      for (int g = 0; g < GH; ++g) {
+        const QueryRange r = query_range(A.row_range, t0 + g, A.n_q, ui, A.trivial_len, A.direct_max);
+        qa[g] = r.a;
+        qb[g] = r.b;
+        qf[g] = r.filtered;
+      }
       __syncwarp();
       for (int i = 0; i < ui.n_tiles; ++i, ++tile) {
         const int buf = tile & 1;
-        const int slot = tile % RING;
+        const int slot = rtile % RING;
         ok = warp_wait(&sh.t_full[buf], (tile >> 1) & 1, &sh.abort_flag, status, wait_ns);
-        if (ok && tile >= RING) ok = warp_wait(&sh.r_empty[slot], ((tile / RING) - 1) & 1, &sh.abort_flag, status, wait_ns);
+        if (ok && uses_ring && rtile >= RING)
+          ok = warp_wait(&sh.r_empty[slot], ((rtile / RING) - 1) & 1, &sh.abort_flag, status, wait_ns);
         if (!ok) break;
         tc_fence_after();
         // head sum of this half's queries with NP independent partial sums per query (breaks
         // the dependent FMA chain); TMEM read 64 columns per wait
         constexpr int NP = HI >= 16 ? 4 : 1;
-        constexpr int GH = C::GH;
         float part[GH][NP];
 #pragma unroll
         for (int g = 0; g < GH; ++g)
@@ -594,27 +631,49 @@ __global__ void __launch_bounds__(Cfg<HI, DI, G>::THREADS, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh.t_empty[buf]);
-        float* rs = ring + static_cast<size_t>(slot) * G * kKeyTile;
+        const int j = ui.kbeg + i * kKeyTile + row;
+        float* rs = reinterpret_cast<float*>(ring + static_cast<size_t>(slot) * C::RING_SLOT);
+        uint32_t* rm = reinterpret_cast<uint32_t*>(ring + static_cast<size_t>(slot) * C::RING_SLOT + C::RING_SCORES);
 #pragma unroll
         for (int g = 0; g < GH; ++g) {
           float acc;
           if constexpr (NP == 4) acc = (part[g][0] + part[g][1]) + (part[g][2] + part[g][3]);
           else acc = part[g][0];
-          rs[(g0 + g) * kKeyTile + row] = acc;
+          const bool in = j >= qa[g] && j < qb[g];
+          if (!qf[g]) {
+            // direct: every key of the range at its offset
+            if (in) {
+              const size_t off = (static_cast<size_t>(t0 + g) * A.n_chunks + ui.chunk) * cap + (j - qa[g]);
+              A.cand_key[off] = float_key(acc);
+              A.cand_idx[off] = j;
+            }
+            if (uses_ring && lane == 0) rm[(g0 + g) * 4 + quarter] = 0u;
+          } else {
+            // filtered: the score and whether it reaches the query's published threshold
+            const uint64_t tv = *reinterpret_cast<volatile uint64_t*>(&sh.tau[g0 + g]);
+            const uint32_t tk = static_cast<uint32_t>(tv >> 32) == unit_ord ? static_cast<uint32_t>(tv) : 0u;
+            const uint32_t m = __ballot_sync(0xffffffffu, in && float_key(acc) >= tk);
+            rs[(g0 + g) * kKeyTile + row] = acc;
+            if (lane == 0) rm[(g0 + g) * 4 + quarter] = m;
+          }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sh.r_full[slot]);
+        if (uses_ring) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh.r_full[slot]);
+          ++rtile;
+        }
       }
+      ++unit_ord;
     }
   } else {
     // ------------------------------------------------------------------ top-k warps
+    using Cf = C;
     const int tw = warp - 2 - NE;               // queries tw, tw + NT, ...
     constexpr int QPT = C::QPT;
     WarpScratch& ws = sh.ws[tw];
     const uint32_t below = (1u << lane) - 1u;
-    const int cap = A.cap, topk = A.topk;
-    const bool final_here = A.n_chunks == 1;
-    uint32_t tile = 0;
+    const int topk = A.topk;
+    uint32_t rtile = 0, unit_ord = 0;
     bool ok = true;
     for (int k = 0; k * static_cast<int>(gridDim.x) < n_units && ok; ++k) {
       const int u = snake_unit(k);
@@ -622,106 +681,153 @@ __global__ void __launch_bounds__(Cfg<HI, DI, G>::THREADS, 1)
       const UnitInfo ui = unit_info(u, A.n_groups, A.chunk_len, A.group_range);
       if (ui.n_tiles == 0) {
         // an empty chunk still tells the final select that it holds no candidates
-        if (!final_here && lane == 0) {
+        if (lane == 0)
           for (int g = tw; g < G; g += NT) {
             const int t = ui.group * G + g;
-            if (t < A.n_q) A.cand_cnt[static_cast<size_t>(t) * A.n_chunks + ui.chunk] = 0u;
+            if (t < A.n_q) {
+              A.cand_cnt[static_cast<size_t>(t) * A.n_chunks + ui.chunk] = 0u;
+              A.cand_edge[static_cast<size_t>(t) * A.n_chunks + ui.chunk] = 0u;
+            }
           }
-        }
         continue;
       }
-      // per owned query: key range within this unit, count, threshold, key extremes
-      int qa[QPT], qb[QPT], cnt[QPT];
-      uint32_t tau[QPT], lmin[QPT], lmax[QPT];
-      bool live[QPT];
+      const bool uses_ring = unit_filtered(ui);
+      // per owned query: range, filtered or not, count, threshold bin, entries at or above it
+      int qa[QPT], qb[QPT], cnt[QPT], bstar[QPT], above[QPT];
+      uint32_t lmin[QPT], lmax[QPT];   // per lane: extremes of the keys it appended
+      bool qf[QPT];
 #pragma unroll
       for (int qi = 0; qi < QPT; ++qi) {
         const int g = tw + qi * NT;
-        const int t = ui.group * G + g;
-        int2 rr = make_int2(0, 0);
-        if (g < G && t < A.n_q) rr = A.row_range[t];
-        live[qi] = g < G && t < A.n_q && rr.y - rr.x > A.trivial_len;
-        qa[qi] = max(rr.x, ui.kbeg);
-        qb[qi] = live[qi] ? min(rr.y, ui.kend) : qa[qi];
+        const QueryRange r = query_range(A.row_range, ui.group * G + g, A.n_q, ui, A.trivial_len, A.direct_max);
+        qa[qi] = r.a;
+        qb[qi] = r.b;
+        qf[qi] = g < G && r.filtered;
         cnt[qi] = 0;
-        tau[qi] = 0u;
+        bstar[qi] = 0;
+        above[qi] = 0;
         lmin[qi] = 0xFFFFFFFFu;
         lmax[qi] = 0u;
-      }
-      for (int i = 0; i < ui.n_tiles; ++i, ++tile) {
-        const int slot = tile % RING;
-        ok = warp_wait(&sh.r_full[slot], (tile / RING) & 1, &sh.abort_flag, status, wait_ns);
-        if (!ok) break;
-        const float* rs = ring + static_cast<size_t>(slot) * G * kKeyTile;
-        const int tile0 = ui.kbeg + i * kKeyTile;
-#pragma unroll
-        for (int qi = 0; qi < QPT; ++qi) {
-          const int g = tw + qi * NT;
-          if (g >= G) continue;
-          if (tile0 >= qb[qi] || tile0 + kKeyTile <= qa[qi]) continue;   // warp-uniform
-          const size_t off = (static_cast<size_t>(ui.group * G + g) * A.n_chunks + ui.chunk) * cap;
-          uint32_t* ck = A.cand_key + off;
-          int32_t* ci = A.cand_idx + off;
-#pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            const int j = tile0 + r * 32 + lane;
-            const uint32_t key = float_key(rs[g * kKeyTile + r * 32 + lane]);
-            const bool pass = j >= qa[qi] && j < qb[qi] && key > tau[qi];
-            const uint32_t m = __ballot_sync(0xffffffffu, pass);
-            if (pass) {
-              const int p = cnt[qi] + __popc(m & below);
-              if (p < cap) {
-                ck[p] = key;
-                ci[p] = j;
-              }
-              lmin[qi] = min(lmin[qi], key);
-              lmax[qi] = max(lmax[qi], key);
-            }
-            cnt[qi] += __popc(m);
-          }
+        if (qf[qi]) {
+          for (int b = lane; b < C::NB; b += 32) sh.hist[g][b] = 0u;
+          if (lane == 0) *reinterpret_cast<volatile uint64_t*>(&sh.tau[g]) = static_cast<uint64_t>(unit_ord) << 32;
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sh.r_empty[slot]);
-        // cut back any buffer that could overflow on the next tile
+      }
+      __syncwarp();
+      if (uses_ring) {
+        for (int i = 0; i < ui.n_tiles; ++i, ++rtile) {
+          const int slot = rtile % RING;
+          ok = warp_wait(&sh.r_full[slot], (rtile / RING) & 1, &sh.abort_flag, status, wait_ns);
+          if (!ok) break;
+          const float* rs = reinterpret_cast<const float*>(ring + static_cast<size_t>(slot) * C::RING_SLOT);
+          const uint32_t* rm = reinterpret_cast<const uint32_t*>(ring + static_cast<size_t>(slot) * C::RING_SLOT + C::RING_SCORES);
+          const int tile0 = ui.kbeg + i * kKeyTile;
 #pragma unroll
-        for (int qi = 0; qi < QPT; ++qi) {
-          const int g = tw + qi * NT;
-          if (g >= G || cnt[qi] <= cap - kKeyTile) continue;
-          const size_t off = (static_cast<size_t>(ui.group * G + g) * A.n_chunks + ui.chunk) * cap;
-          if (cnt[qi] > cap) {
-            if (lane == 0) atomicOr(status, DEV_ERR_OVERFLOW);
-            cnt[qi] = cap;
+          for (int qi = 0; qi < QPT; ++qi) {
+            const int g = tw + qi * NT;
+            if (!qf[qi]) continue;
+            const uint4 m4 = *reinterpret_cast<const uint4*>(&rm[g * 4]);
+            if ((m4.x | m4.y | m4.z | m4.w) == 0u) continue;
+            const size_t off = (static_cast<size_t>(ui.group * G + g) * A.n_chunks + ui.chunk) * cap;
+            const uint32_t mq[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+              const uint32_t m = mq[r];
+              if (m == 0u) continue;
+              const bool pass = (m >> lane) & 1u;
+              int bin = -1;
+              if (pass) {
+                const uint32_t key = float_key(rs[g * kKeyTile + r * 32 + lane]);
+                const int p = cnt[qi] + __popc(m & below);
+                if (p < cap) {
+                  A.cand_key[off + p] = key;
+                  A.cand_idx[off + p] = tile0 + r * 32 + lane;
+                }
+                bin = hist_bin<Cf>(key);
+                atomicAdd(&sh.hist[g][bin], 1u);
+                lmin[qi] = min(lmin[qi], key);
+                lmax[qi] = max(lmax[qi], key);
+              }
+              // entries at or above the current boundary bin count towards it (a threshold
+              // published late lets a few lower ones in: they are kept, not counted)
+              above[qi] += __popc(__ballot_sync(0xffffffffu, bin >= bstar[qi]));
+              cnt[qi] += __popc(m);
+            }
+            __syncwarp();
+            // raise the boundary bin while the entries strictly above it are k or more
+            int b = bstar[qi], ab = above[qi];
+            while (b < C::NB - 1) {
+              const int h = static_cast<int>(sh.hist[g][b]);
+              if (ab - h < topk) break;
+              ab -= h;
+              ++b;
+            }
+            if (b != bstar[qi]) {
+              bstar[qi] = b;
+              above[qi] = ab;
+              if (lane == 0)
+                *reinterpret_cast<volatile uint64_t*>(&sh.tau[g]) =
+                    (static_cast<uint64_t>(unit_ord) << 32) | bin_edge_key<Cf>(b);
+            }
           }
-          __syncwarp();   // this warp's appends are visible to all its lanes
-          uint32_t kmin = __reduce_min_sync(0xffffffffu, lmin[qi]), kmax = __reduce_max_sync(0xffffffffu, lmax[qi]);
-          cnt[qi] = warp_cut_back(A.cand_key + off, A.cand_idx + off, cnt[qi], topk, cap, kmin, kmax, ws, ws.bc);
-          tau[qi] = kmin;
-          lmin[qi] = kmin;
-          lmax[qi] = kmax;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh.r_empty[slot]);
+          // a buffer that could overflow on the next tile: cut it back to exactly the top-k
+          // (rare: only when scores keep rising along the keys) and rebuild its histogram
+#pragma unroll 1
+          for (int qi = 0; qi < QPT; ++qi) {
+            const int g = tw + qi * NT;
+            if (!qf[qi] || cnt[qi] <= cap - kKeyTile) continue;
+            const size_t off = (static_cast<size_t>(ui.group * G + g) * A.n_chunks + ui.chunk) * cap;
+            if (cnt[qi] > cap) {
+              if (lane == 0) atomicOr(status, DEV_ERR_OVERFLOW);
+              cnt[qi] = cap;
+            }
+            __syncwarp();   // this warp's appends are visible to all its lanes
+            uint32_t kmin = __reduce_min_sync(0xffffffffu, lmin[qi]), kmax = __reduce_max_sync(0xffffffffu, lmax[qi]);
+            uint32_t v = 0, cutv = 0;
+            warp_exact_threshold(A.cand_key + off, A.cand_idx + off, cnt[qi], topk, kmin, kmax, ws, ws.bc, v, cutv);
+            cnt[qi] = warp_compact(A.cand_key + off, A.cand_idx + off, cnt[qi],
+                                   [&](uint32_t key, int32_t idx) { return topk_keep(key, idx, v, cutv); }, kmin, kmax);
+            lmin[qi] = kmin;
+            lmax[qi] = kmax;
+            for (int b = lane; b < C::NB; b += 32) sh.hist[g][b] = 0u;
+            __syncwarp();
+            warp_for_each<false>(A.cand_key + off, A.cand_idx + off, cnt[qi], [&](bool okk, uint32_t key, int32_t) {
+              if (okk) atomicAdd(&sh.hist[g][hist_bin<Cf>(key)], 1u);
+            });
+            __syncwarp();
+            int b = 0, ab = cnt[qi];
+            while (b < C::NB - 1) {
+              const int h = static_cast<int>(sh.hist[g][b]);
+              if (ab - h < topk) break;
+              ab -= h;
+              ++b;
+            }
+            bstar[qi] = b;
+            above[qi] = ab;
+            if (lane == 0)
+              *reinterpret_cast<volatile uint64_t*>(&sh.tau[g]) =
+                  (static_cast<uint64_t>(unit_ord) << 32) | (b > 0 ? bin_edge_key<Cf>(b) : 0u);
+          }
         }
       }
       if (!ok) break;
-      // the unit is done: final selection of rows finished here, else the chunk's count
-#pragma unroll 1
-      for (int qi = 0; qi < QPT; ++qi) {
-        const int g = tw + qi * NT;
-        const int t = ui.group * G + g;
-        if (g >= G || t >= A.n_q) continue;
-        const size_t off = (static_cast<size_t>(t) * A.n_chunks + ui.chunk) * cap;
-        const int n = min(cnt[qi], cap);
-        __syncwarp();
-        if (!final_here) {
-          if (lane == 0) A.cand_cnt[static_cast<size_t>(t) * A.n_chunks + ui.chunk] = static_cast<uint32_t>(n);
-          continue;
+      // the unit is done: each row's count in this chunk, and the lower edge of its boundary
+      // bin when at least k entries lie at or above it (no entry below can make the top-k)
+      if (lane == 0) {
+#pragma unroll
+        for (int qi = 0; qi < QPT; ++qi) {
+          const int g = tw + qi * NT;
+          const int t = ui.group * G + g;
+          if (g >= G || t >= A.n_q) continue;
+          const int n = qf[qi] ? min(cnt[qi], cap) : qb[qi] - qa[qi];
+          A.cand_cnt[static_cast<size_t>(t) * A.n_chunks + ui.chunk] = static_cast<uint32_t>(n);
+          A.cand_edge[static_cast<size_t>(t) * A.n_chunks + ui.chunk] =
+              qf[qi] && bstar[qi] > 0 && above[qi] >= topk ? bin_edge_key<Cf>(bstar[qi]) : 0u;
         }
-        if (!live[qi]) continue;   // trivial and empty rows are written by the select pass
-        const int2 rr = A.row_range[t];
-        const int Kt = min(topk, rr.y - rr.x);
-        const uint32_t kmin = __reduce_min_sync(0xffffffffu, lmin[qi]), kmax = __reduce_max_sync(0xffffffffu, lmax[qi]);
-        warp_final_select(A.cand_key + off, A.cand_idx + off, n, Kt, rr.x, topk, kmin, kmax,
-                          A.idx_out + static_cast<size_t>(t) * topk,
-                          A.score_out ? A.score_out + static_cast<size_t>(t) * topk : nullptr, ws, ws.bc, status);
       }
+      ++unit_ord;
     }
   }
 
@@ -755,8 +861,7 @@ cudaError_t launch_t(const IndexerPlan& p, const CUtensorMap& tq, const CUtensor
 cudaError_t launch_indexer(const IndexerPlan& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tqi,
                            const CUtensorMap& tki, int q_split, int k_split, const PagedRows& pg, const float* w, int n_q,
                            const int2* row_range, const int2* group_range, int trivial_len, uint32_t* ck, int32_t* ci,
-                           uint32_t* cc, int32_t* idx_out, float* score_out, uint32_t* status,
-                           const PipelineDebug& dbg, cudaStream_t st) {
+                           uint32_t* cc, uint32_t* ce, uint32_t* status, const PipelineDebug& dbg, cudaStream_t st) {
   if (p.n_groups * p.n_chunks == 0) return cudaSuccess;
   if (pg.block_table && (p.group != 1 || p.chunk % kPageRows != 0)) return cudaErrorInvalidValue;
   IndexerArgs A;
@@ -768,35 +873,33 @@ cudaError_t launch_indexer(const IndexerPlan& p, const CUtensorMap& tq, const CU
   A.n_chunks = p.n_chunks;
   A.chunk_len = p.chunk;
   A.cap = p.cap;
+  A.direct_max = p.cap < 4096 ? p.cap : 4096;
   A.topk = p.topk;
   A.trivial_len = trivial_len;
   A.cand_key = ck;
   A.cand_idx = ci;
   A.cand_cnt = cc;
-  A.idx_out = idx_out;
-  A.score_out = score_out;
+  A.cand_edge = ce;
   A.status = status;
   A.wait_ns = dbg.wait_ns;
   A.stop_after = dbg.stop_after_tiles;
 #define DSA_IDX_CASE(HI_, DI_, G_)                                                                      \
   if (p.n_heads == HI_ && p.head_dim == DI_ && p.group == G_)                                           \
     return launch_t<HI_, DI_, G_>(p, tq, tk, tqi, tki, q_split, k_split, pg, A, st);
-  DSA_IDX_CASE(4, 64, 64)
-  DSA_IDX_CASE(8, 64, 32)
+  DSA_IDX_CASE(4, 64, 16)
+  DSA_IDX_CASE(8, 64, 16)
   DSA_IDX_CASE(16, 64, 16)
   DSA_IDX_CASE(32, 64, 8)
   DSA_IDX_CASE(64, 64, 4)
-  DSA_IDX_CASE(4, 128, 64)
-  DSA_IDX_CASE(8, 128, 32)
+  DSA_IDX_CASE(4, 128, 16)
+  DSA_IDX_CASE(8, 128, 16)
   DSA_IDX_CASE(16, 128, 16)
   DSA_IDX_CASE(32, 128, 8)
   DSA_IDX_CASE(64, 128, 4)
-  DSA_IDX_CASE(4, 64, 16)
   DSA_IDX_CASE(8, 64, 8)
   DSA_IDX_CASE(16, 64, 4)
   DSA_IDX_CASE(32, 64, 2)
   DSA_IDX_CASE(64, 64, 1)
-  DSA_IDX_CASE(4, 128, 16)
   DSA_IDX_CASE(8, 128, 8)
   DSA_IDX_CASE(16, 128, 4)
   DSA_IDX_CASE(32, 128, 2)

@@ -60,11 +60,11 @@ struct PipelineDebug {
 };
 PipelineDebug pipeline_debug();
 
-// Scores + streaming top-k.  tmap_q covers rotated q as [(n_q*H_I) x d_I] bf16, tmap_k covers
-// rotated k as [n_kv x d_I] bf16, both 128-byte swizzled, boxes {64, N} and {64, 128}.
-// With one key chunk per row (p.n_chunks == 1) the kernel also makes every non-trivial row's
-// final selection (idx_out, score_out); otherwise it leaves per-chunk candidates and counts
-// for launch_select.  Rows of at most trivial_len keys are left to launch_select either way.
+// Scores + streaming top-k candidates.  tmap_q covers rotated q as [(n_q*H_I) x d_I] bf16,
+// tmap_k covers rotated k as [n_kv x d_I] bf16, both 128-byte swizzled, boxes {64, N} and
+// {64, 128}.  Per (row, chunk) it leaves up to p.cap candidates in key order, their count and
+// an edge key (no entry below it can be in the row's top-k; 0 when unknown) for
+// launch_select.  Rows of at most trivial_len keys are not scored (count 0).
 inline int rope_split_blocks(int d, int rope) { return rope > 0 ? (d - rope) / 64 : 0; }
 // tmap_q / tmap_k: rotated copies; tmap_q_in / tmap_k_in: the unrotated inputs, read for the
 // 64-dim blocks below q_split / k_split.
@@ -72,14 +72,14 @@ cudaError_t launch_indexer(const IndexerPlan& p, const CUtensorMap& tmap_q, cons
                            const CUtensorMap& tmap_q_in, const CUtensorMap& tmap_k_in, int q_split, int k_split,
                            const PagedRows& pg, const float* w, int n_q, const int2* row_range,
                            const int2* group_range, int trivial_len, uint32_t* cand_key, int32_t* cand_idx,
-                           uint32_t* cand_cnt, int32_t* idx_out, float* score_out, uint32_t* status,
-                           const PipelineDebug& dbg, cudaStream_t st);
+                           uint32_t* cand_cnt, uint32_t* cand_edge, uint32_t* status, const PipelineDebug& dbg,
+                           cudaStream_t st);
 
 // Exact top-k of every row from its candidates; writes offsets (ascending) and -1 padding.
-// Rows of at most trivial_len keys are written as 0..L-1 without reading candidates; with
-// only_trivial set, the other rows (already written by the indexer) are left alone.
-cudaError_t launch_select(int n_q, int n_chunks, int cap, int topk, int trivial_len, bool only_trivial,
-                          const int2* row_range,
+// Rows of at most trivial_len keys are written as 0..L-1 without reading candidates; entries
+// below the largest of a row's chunk edges are skipped.
+cudaError_t launch_select(int n_q, int n_chunks, int cap, int topk, int trivial_len, const int2* row_range,
+                          const uint32_t* cand_edge,
                           const uint32_t* cand_key,
                           const int32_t* cand_idx, const uint32_t* cand_cnt, int32_t* idx_out, float* score_out,
                           uint32_t* status, cudaStream_t st);

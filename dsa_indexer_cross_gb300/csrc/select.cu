@@ -129,8 +129,8 @@ __device__ bool linear_threshold(const ForEach& fe, int tid, int K, LinearSmem& 
 
 template <bool kRegs>
 __global__ void __launch_bounds__(kSelThreads) select_kernel(int n_chunks, int cap, int topk, int trivial_len,
-                                                             bool only_trivial,
                                                              const int2* __restrict__ row_range,
+                                                             const uint32_t* __restrict__ cand_edge,
                                                              const uint32_t* __restrict__ cand_key,
                                                              const int32_t* __restrict__ cand_idx,
                                                              const uint32_t* __restrict__ cand_cnt,
@@ -144,7 +144,6 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(int n_chunks, int c
   const int t = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int2 r = row_range[t];
-  if (only_trivial && r.y - r.x > trivial_len) return;   // written by the indexer kernel
   if (r.y - r.x <= trivial_len) {
     // the whole range is selected: offsets 0 .. L-1 in order, no candidates read.  The host
     // passes trivial_len = 0 whenever scores are requested, so only empty rows get here then.
@@ -159,15 +158,22 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(int n_chunks, int c
   }
   const size_t base = static_cast<size_t>(t) * n_chunks * cap;
   const uint32_t* cnt_row = cand_cnt + static_cast<size_t>(t) * n_chunks;
+  __shared__ uint32_t s_edge;
   if (tid == 0) {
     int s = 0;
+    uint32_t e = 0u;
     for (int c = 0; c < n_chunks; ++c) {
       start[c] = s;
       s += min(static_cast<int>(cnt_row[c]), cap);
+      e = max(e, __ldg(cand_edge + static_cast<size_t>(t) * n_chunks + c));
     }
     start[n_chunks] = s;
+    s_edge = e;
   }
   __syncthreads();
+  // a chunk's edge has at least k of that chunk's entries at or above it, so nothing below the
+  // largest edge can be in the row's top-k: the threshold passes skip those entries
+  const uint32_t edge = s_edge;
   const int total = start[n_chunks];
   int kt = min(topk, r.y - r.x);
   if (total < kt) {
@@ -205,7 +211,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(int n_chunks, int c
     auto fe = [&](auto&& f) {
 #pragma unroll
       for (int i = 0; i < kSelPer; ++i)
-        if (p0 + i < p1) f(rk[i], ri[i]);
+        if (p0 + i < p1 && rk[i] >= edge) f(rk[i], ri[i]);
     };
     if (kt > 0 && !take_all && !linear_threshold(fe, tid, kt, lin, v, cut)) {
       __syncthreads();
@@ -257,7 +263,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(int n_chunks, int c
           }
 #pragma unroll
           for (int u = 0; u < 4; ++u)
-            if (e0 + u * kSelThreads < n) f(kk[u], ii[u]);
+            if (e0 + u * kSelThreads < n && kk[u] >= edge) f(kk[u], ii[u]);
         }
       }
     };
@@ -334,18 +340,18 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(int n_chunks, int c
 
 }  // namespace
 
-cudaError_t launch_select(int n_q, int n_chunks, int cap, int topk, int trivial_len, bool only_trivial,
-                          const int2* row_range,
+cudaError_t launch_select(int n_q, int n_chunks, int cap, int topk, int trivial_len, const int2* row_range,
+                          const uint32_t* cand_edge,
                           const uint32_t* cand_key,
                           const int32_t* cand_idx, const uint32_t* cand_cnt, int32_t* idx_out, float* score_out,
                           uint32_t* status, cudaStream_t st) {
   if (n_q <= 0) return cudaSuccess;
   if (n_chunks > kMaxChunks) return cudaErrorInvalidValue;
   if (static_cast<long long>(n_chunks) * cap <= static_cast<long long>(kSelThreads) * kSelPer)
-    select_kernel<true><<<n_q, kSelThreads, 0, st>>>(n_chunks, cap, topk, trivial_len, only_trivial, row_range, cand_key, cand_idx, cand_cnt,
+    select_kernel<true><<<n_q, kSelThreads, 0, st>>>(n_chunks, cap, topk, trivial_len, row_range, cand_edge, cand_key, cand_idx, cand_cnt,
                                                     idx_out, score_out, status);
   else
-    select_kernel<false><<<n_q, kSelThreads, 0, st>>>(n_chunks, cap, topk, trivial_len, only_trivial, row_range, cand_key, cand_idx, cand_cnt,
+    select_kernel<false><<<n_q, kSelThreads, 0, st>>>(n_chunks, cap, topk, trivial_len, row_range, cand_edge, cand_key, cand_idx, cand_cnt,
                                                      idx_out, score_out, status);
   return cudaGetLastError();
 }

@@ -191,3 +191,34 @@ def test_attention_gather_walk_for_small_heads(H):
     e_o, e_l = attn_errors(out, lse, o_ref, lse_ref, range(n_q))
     assert e_o <= ATOL_OUT and e_l <= ATOL_LSE, (e_o, e_l)
     assert torch.all(out[5] == 0) and torch.all(torch.isneginf(lse[5]))
+
+
+def test_indexer_rising_scores_cut_back_the_buffer():
+    """Scores that rise along the keys beat every streaming threshold, so a long row's
+    candidate buffer fills up and has to be cut back to its exact top-k (ties to the lower
+    key index) again and again; the result is still exactly the oracle's set.  Here every
+    head sees s_j = k_j[0], which rises with j in steps of bf16 rounding, so long runs of
+    equal scores exercise the tie rule as well."""
+    from oracle import dsa_oracle as O
+    n_q, n_kv, H, d, topk = 2432, 40000, 64, 128, 2048   # 608 groups of 4 rows: one chunk per row
+    q = torch.zeros((n_q, H, d), dtype=torch.float32)
+    q[:, :, 0] = 1.0
+    k = torch.zeros((n_kv, d), dtype=torch.float32)
+    k[:, 0] = (torch.arange(n_kv, dtype=torch.float32) + 1.0) / n_kv
+    q, k = q.to(torch.bfloat16), k.to(torch.bfloat16)
+    w = torch.full((n_q, H), 1.0 / 64.0, dtype=torch.float32)
+    ks = np.zeros(n_q, np.int32)
+    ke = (n_kv - (np.arange(n_q) % 7) * 1000).astype(np.int32)
+    pos = np.arange(n_kv, dtype=np.int32)
+    q_pos = (ke - 1).astype(np.int32)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+    desc = D.indexer_desc(n_q, n_kv, H, d, 0, topk, n_kv, 0)
+    idx = torch.empty((n_q, topk), dtype=torch.int32, device=DEV)
+    ws = D.dsa_indexer_topk(desc, q.to(DEV), k.to(DEV), w.to(DEV), dev(q_pos), dev(pos), dev(ks), dev(ke), None, idx)
+    assert D.dsa_workspace_status(ws) == 0
+    rows = [0, 1, 6, 1000, n_q - 1]
+    ref = O.indexer_topk(synth.to_f64(q), synth.to_f64(k), synth.to_f64(w), q_pos, pos, ks, ke, 0, 1e4, topk,
+                         rope_q=False, rope_k=False, rows=rows)
+    got = idx.cpu().numpy()
+    for n, t in enumerate(rows):
+        assert np.array_equal(got[t], ref[n]), f"row {t}"
