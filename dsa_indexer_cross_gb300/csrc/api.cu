@@ -230,12 +230,12 @@ IndexerLayout indexer_layout(const dsa_indexer_desc* d, int sms) {
   chunk = (chunk + 127) / 128 * 128;
   p.chunk = static_cast<int>(chunk);
   p.n_chunks = static_cast<int>((span + chunk - 1) / chunk);
-  // candidates per (row, chunk): every key of a chunk when it has at most 16K, else 16K (the
-  // streaming threshold keeps about k (1 + ln(chunk / k)) of them; more only for scores that
-  // keep rising along the keys, which the kernel handles by cutting the buffer back)
+  // candidates per (row, chunk), in kSub sub-buffers: every key of the chunk when a row's part
+  // of it has at most kDirectMax keys, else 16K (the streaming threshold keeps about
+  // k (1 + ln(chunk / k)) of them; more only for scores that keep rising along the keys, which
+  // the kernel handles by cutting a sub-buffer back to its top-k)
   const long long span_keys = std::min<long long>(chunk, span);
-  p.cap = static_cast<int>(std::min<long long>((span_keys + 127) / 128 * 128, 16384));
-  if (p.cap < 2 * d->topk + 256 && span_keys > p.cap) p.cap = (2 * d->topk + 256 + 127) / 128 * 128;
+  p.cap = span_keys > kDirectMax ? 16384 : static_cast<int>((span_keys + 127) / 128 * 128);
   const long long units = static_cast<long long>(p.n_groups) * p.n_chunks;
   p.grid = static_cast<int>(units < sms ? units : sms);
   if (p.grid < 1) p.grid = 1;
@@ -253,7 +253,7 @@ IndexerLayout indexer_layout(const dsa_indexer_desc* d, int sms) {
   off += align_up(static_cast<size_t>(p.n_groups) * 8);
   const size_t slots = static_cast<size_t>(d->n_q) * p.n_chunks;
   L.off_cnt = off;
-  off += align_up(slots * 4);
+  off += align_up(slots * kSub * 4);
   L.off_edge = off;
   off += align_up(slots * 4);
   L.off_key = off;
@@ -349,7 +349,7 @@ dsa_status run_indexer(const dsa_indexer_desc* d, const void* q_idx, const void*
     prof_end(ps, st);
     if (e != cudaSuccess) return cuda_fail(e, "indexer kernel");
   } else {
-    if ((e = cudaMemsetAsync(cnt, 0, static_cast<size_t>(d->n_q) * p.n_chunks * 4, st)) != cudaSuccess ||
+    if ((e = cudaMemsetAsync(cnt, 0, static_cast<size_t>(d->n_q) * p.n_chunks * kSub * 4, st)) != cudaSuccess ||
         (e = cudaMemsetAsync(edge, 0, static_cast<size_t>(d->n_q) * p.n_chunks * 4, st)) != cudaSuccess)
       return cuda_fail(e, "clear counts");
   }

@@ -12,28 +12,28 @@
 //     S^T[key, (g, h)] = K_tile[key, :] . Q_group[(g, h), :]
 // into one of two TMEM accumulators.
 //
-// Candidates.  Every (row, chunk) has a buffer of `cap` (order-preserving score key, key
-// index) entries in key order; launch_select later picks each row's exact top-k from them.
-// A row whose key range in the chunk fits the buffer is written DIRECTLY: every key's score at
-// its offset.  A longer one is FILTERED: a key is kept only if its score is at or above the
-// lower edge tau of the histogram bin that holds the row's k-th largest kept score so far
-// (bins of a fixed log-spaced map of the score key), because every key below that edge has at
-// least k kept keys above it; the expected number kept over N keys is about k (1 + ln(N/k)).
+// Candidates.  Every (row, chunk) has kSub sub-buffers of cap / kSub (order-preserving score
+// key, key index) entries, one per TMEM lane quarter (keys j with (j - chunk start) % 128 in
+// [32 q, 32 q + 32)), each in key order; launch_select later picks each row's exact top-k from
+// them.  A row keeps a key only if its score is at or above the row's threshold tau: minus
+// infinity for rows of at most direct_max keys in the chunk (every key is kept), else the lower
+// edge of the bin of a log-spaced score histogram that holds the row's k-th largest kept
+// score -- every key below that edge has at least k kept keys above it.  The expected number
+// kept over N keys is about k (1 + ln(N/k)).
 //
 // Warp roles (no role waits on a CTA-wide barrier inside the tile loop):
 //   warp 0            TMA producer: Q of the unit once, K tiles through a STAGES-deep ring;
 //   warp 1            MMA issuer (owns TMEM);
 //   head-sum warps    NE = 4 or 8: a warp owns one TMEM lane quarter (32 keys) and half or
 //                     all of the group's queries; it reduces the heads of each query in
-//                     registers (ReLU * w with packed fp32 FMAs).  Direct rows: it stores
-//                     the scores itself.  Filtered rows: it writes the tile's scores and, per
-//                     lane quarter, the mask of keys at or above tau into a shared-memory
-//                     ring slot;
-//   top-k warps       NT <= 4, filtered rows only: a warp owns queries g = warp, warp + NT, ...;
-//                     per tile it appends the marked keys of its queries in key order, counts
-//                     them in the query's histogram, raises tau and publishes it.  Should a
-//                     buffer still fill up (scores rising along the keys), the warp cuts it
-//                     back to exactly the top-k and rebuilds the histogram.
+//                     registers (ReLU * w with packed fp32 FMAs), keeps the keys at or above
+//                     the query's tau in its own sub-buffer (no other warp writes there) and
+//                     counts them in the query's histogram.  A sub-buffer that could overflow
+//                     (scores that keep rising along the keys) is cut back by its warp to
+//                     exactly its top-k, which still holds every key of the row's top-k that
+//                     lies in it;
+//   threshold warp    keeps raising each filtered query's tau from its histogram while the
+//                     unit runs; histograms and taus are double-buffered by unit parity.
 // The score matrix is never written anywhere.
 #include <cuda_bf16.h>
 
@@ -67,31 +67,25 @@ struct Cfg {
   static constexpr int NE = 4 * HALVES;
   static constexpr int GH = G / HALVES;                  // queries per half
   static constexpr int NH = N / HALVES;                  // TMEM columns per half
-  static constexpr int NT = G < 4 ? G : 4;               // top-k warps
-  static constexpr int QPT = (G + NT - 1) / NT;          // queries per top-k warp
-  static constexpr int THREADS = 32 * (2 + NE + NT);
-  // threshold histogram: NB bins per query (16 KB in all), log-spaced over 2^kLog2Span octaves
-  static constexpr int NB = 4096 / G < 1024 ? 4096 / G : 1024;
-  static constexpr int SHIFT = 23 + ilog2(1 << kLog2Span) - ilog2(NB);   // key bits below the bin index
+  static constexpr int THREADS = 32 * (3 + NE);          // + producer, MMA, threshold warps
+  // threshold histograms: NB bins per query per unit parity (16 KB in all), log-spaced over
+  // 2^kLog2Span octaves
+  static constexpr int NB = 2048 / G < 512 ? 2048 / G : 512;
+  static constexpr int SHIFT = 23 + kLog2Span - ilog2(NB);   // key bits below the bin index
   static constexpr uint32_t BASE = (0x80000000u | (static_cast<uint32_t>(kLowExp) << 23)) >> SHIFT;
-  // ring slot: the tile's scores of every query, then one keep-mask per (query, lane quarter)
-  static constexpr int RING_SCORES = G * kKeyTile * 4;
-  static constexpr int RING_SLOT = RING_SCORES + G * 4 * 4;
   static constexpr int SMEM_MAX = 232448;                // dynamic + static per CTA
-  static constexpr int STATIC_EST = 2048 + NE * NH * 4 + G * NB * 4 + NT * 1600 + G * 8;
+  static constexpr int STATIC_EST = 1024 + NE * NH * 4 + 2 * G * NB * 4 + NE * 1600 + 4 * G * 4;
   static constexpr int AVAIL = SMEM_MAX - STATIC_EST - 1024 - Q_BYTES;
-  static constexpr int RING_RESERVE = RING_SLOT <= 8192 ? 4 : 2;
-  static constexpr int STAGES_FIT = (AVAIL - RING_RESERVE * RING_SLOT) / K_STAGE_BYTES;
+  static constexpr int STAGES_FIT = AVAIL / K_STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT > 6 ? 6 : STAGES_FIT;
-  static constexpr int RING_FIT = (AVAIL - STAGES * K_STAGE_BYTES) / RING_SLOT;
-  static constexpr int RING = RING_FIT > 16 ? 16 : RING_FIT;
-  static constexpr int DYN_SMEM = 1024 + Q_BYTES + STAGES * K_STAGE_BYTES + RING * RING_SLOT;
+  static constexpr int DYN_SMEM = 1024 + Q_BYTES + STAGES * K_STAGE_BYTES;
   static constexpr uint32_t TMEM_COLS = (2 * N <= 32) ? 32 : (2 * N <= 64) ? 64 : (2 * N <= 128) ? 128 : (2 * N <= 256) ? 256 : 512;
   static_assert(N % 64 == 0 && N >= 64 && N <= 256, "MMA N");
   static_assert(NH % 64 == 0, "head-sum reads 64 columns at a time");
   static_assert(GH * HI == NH, "a half holds whole queries");
-  static_assert(STAGES >= 2 && RING >= 2, "shared memory");
-  static_assert((1 << (SHIFT + ilog2(NB))) == (1 << (23 + kLog2Span)), "NB bins span 2^kLog2Span octaves");
+  static_assert(G <= 16, "the threshold warp keeps one query per lane, at most 16");
+  static_assert(STAGES >= 2, "shared memory");
+  static_assert(SHIFT + ilog2(NB) == 23 + kLog2Span, "NB bins span 2^kLog2Span octaves");
 };
 
 // Threshold-histogram bin of a score key under Cfg C's map (monotone non-decreasing; scores
@@ -115,19 +109,19 @@ struct WarpScratch {
   int bc[4];
 };
 
-template <int G, int NT, int NE, int NH, int NB>
+template <int G, int NE, int NH, int NB>
 struct Shared {
   uint64_t k_full[6], k_empty[6];
   uint64_t q_full, q_empty;
   uint64_t t_full[2], t_empty[2];
-  uint64_t r_full[16], r_empty[16];
+  uint64_t u_done[2], u_ready[2];  // per unit parity: head-sum warps done / histograms reset
   uint64_t mma_done;
   uint32_t tmem_base;
   uint32_t abort_flag;
-  uint64_t tau[G];                 // per query: (unit ordinal << 32) | threshold key, published by its top-k warp
+  uint32_t tau[2][G];              // per unit parity and query: threshold key (0: keep every key)
   alignas(16) float w_s[NE][NH];   // head weights of the unit, one private copy per head-sum warp
-  uint32_t hist[G][NB];            // threshold histograms (filtered rows)
-  WarpScratch ws[NT];
+  uint32_t hist[2][G][NB];         // threshold histograms of the filtered queries
+  WarpScratch ws[NE];              // cut-back scratch of each head-sum warp
 };
 
 struct UnitInfo {
@@ -383,15 +377,35 @@ struct IndexerArgs {
   const int2* row_range;
   const int2* group_range;
   int n_groups, n_chunks, chunk_len, cap, topk, trivial_len;
-  int direct_max;               // rows with at most this many keys in a chunk are stored whole
+  int direct_max;               // rows with at most this many keys in a chunk keep every key
   uint32_t* cand_key;
   int32_t* cand_idx;
-  uint32_t* cand_cnt;
+  uint32_t* cand_cnt;           // [row][chunk][kSub]
   uint32_t* cand_edge;          // per (row, chunk): a key below which no entry can be in the row's top-k (0: none)
   uint32_t* status;
   unsigned long long wait_ns;   // bound of every pipeline wait
   int stop_after;               // test hook: the producer stops after this many key tiles (< 0: never)
 };
+
+// Raise query g's boundary bin while the entries strictly above it number k or more; returns
+// the new boundary bin and (in *above) the entries at or above it.  Histogram counts only grow
+// while this runs, so a stale read can only stop the climb early.
+template <int NB>
+__device__ __forceinline__ int climb(const uint32_t* hist, int b, int topk, int* above) {
+  const int lane = threadIdx.x & 31;
+  // entries at or above b, summed by the whole warp
+  int s = 0;
+  for (int i = b + lane; i < NB; i += 32) s += static_cast<int>(*reinterpret_cast<const volatile uint32_t*>(&hist[i]));
+  s = __reduce_add_sync(0xffffffffu, s);
+  while (b < NB - 1) {
+    const int h = static_cast<int>(*reinterpret_cast<const volatile uint32_t*>(&hist[b]));
+    if (s - h < topk) break;
+    s -= h;
+    ++b;
+  }
+  *above = s;
+  return b;
+}
 
 template <int HI, int DI, int G>
 __global__ void __launch_bounds__(Cfg<HI, DI, G>::THREADS, 1)
@@ -399,31 +413,22 @@ __global__ void __launch_bounds__(Cfg<HI, DI, G>::THREADS, 1)
                    const __grid_constant__ CUtensorMap tmap_q_in, const __grid_constant__ CUtensorMap tmap_k_in,
                    int q_split, int k_split, const PagedRows pg, const IndexerArgs A) {
   using C = Cfg<HI, DI, G>;
-  constexpr int N = C::N, KB = C::KB, STAGES = C::STAGES, RING = C::RING, NE = C::NE, NT = C::NT, NH = C::NH;
+  constexpr int N = C::N, KB = C::KB, STAGES = C::STAGES, NE = C::NE, NH = C::NH, NB = C::NB;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ Shared<G, NT, NE, NH, C::NB> sh;
+  __shared__ Shared<G, NE, NH, NB> sh;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
   uint8_t* sK = smem + C::Q_BYTES;
-  uint8_t* ring = sK + STAGES * C::K_STAGE_BYTES;   // [RING] x (scores [G][128] fp32, masks [G][4])
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int n_units = A.n_groups * A.n_chunks;
   uint32_t* status = A.status;
-  const int cap = A.cap;
+  const int cap4 = A.cap / kSub;
   // k-th unit of this CTA, in "snake" order: forward on even rounds, backward on odd ones,
   // so a CTA that drew a long unit in one round draws a short one in the next.
   auto snake_unit = [&](int k) {
     const int g = static_cast<int>(gridDim.x), b = static_cast<int>(blockIdx.x);
     return k * g + ((k & 1) ? (g - 1 - b) : b);
-  };
-  // whether any row of the unit is filtered (the ring is used only then); every role derives
-  // it from the same row ranges
-  auto unit_filtered = [&](const UnitInfo& ui) {
-    bool f = false;
-    for (int g = 0; g < G; ++g)
-      f = f || query_range(A.row_range, ui.group * G + g, A.n_q, ui, A.trivial_len, A.direct_max).filtered;
-    return f;
   };
 
   if (threadIdx.x == 0) {
@@ -436,17 +441,17 @@ __global__ void __launch_bounds__(Cfg<HI, DI, G>::THREADS, 1)
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sh.t_full[b], 1);
       mbar_init(&sh.t_empty[b], NE);     // one arrive per head-sum warp
-    }
-    for (int r = 0; r < RING; ++r) {
-      mbar_init(&sh.r_full[r], NE);
-      mbar_init(&sh.r_empty[r], NT);
+      mbar_init(&sh.u_done[b], NE);
+      mbar_init(&sh.u_ready[b], 1);
     }
     mbar_init(&sh.mma_done, 1);
-    for (int g = 0; g < G; ++g) sh.tau[g] = 0xFFFFFFFF00000000ull;   // no unit yet: no threshold
     sh.abort_flag = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
   }
+  // both parities start reset: units 0 and 1 may begin at once
+  for (int i = threadIdx.x; i < 2 * G * NB; i += blockDim.x) (&sh.hist[0][0][0])[i] = 0u;
+  for (int i = threadIdx.x; i < 2 * G; i += blockDim.x) (&sh.tau[0][0])[i] = 0u;
   if (warp == 1) {
     tmem_alloc(&sh.tmem_base, C::TMEM_COLS);
     tmem_relinquish();
@@ -454,6 +459,10 @@ __global__ void __launch_bounds__(Cfg<HI, DI, G>::THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (threadIdx.x == 0) {
+    mbar_arrive(&sh.u_ready[0]);
+    mbar_arrive(&sh.u_ready[1]);
+  }
   const uint32_t tmem = sh.tmem_base;
   const unsigned long long wait_ns = A.wait_ns;
 
@@ -561,22 +570,28 @@ __global__ void __launch_bounds__(Cfg<HI, DI, G>::THREADS, 1)
     const int g0 = half * GH;
     const int row = quarter * 32 + lane;       // key within the tile
     const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t below = (1u << lane) - 1u;
     float* w_s = sh.w_s[hw];
-    uint32_t tile = 0, rtile = 0, unit_ord = 0;
+    WarpScratch& ws = sh.ws[hw];
+    uint32_t tile = 0, unit_ord = 0;
     bool ok = true;
     for (int k = 0; k * static_cast<int>(gridDim.x) < n_units && ok; ++k) {
       const int u = snake_unit(k);
       if (u >= n_units) continue;
       const UnitInfo ui = unit_info(u, A.n_groups, A.chunk_len, A.group_range);
       if (ui.n_tiles == 0) continue;
-      const bool uses_ring = unit_filtered(ui);
+      const int par = unit_ord & 1;
+      // this unit's histograms and thresholds have been reset
+      ok = warp_wait(&sh.u_ready[par], (unit_ord >> 1) & 1, &sh.abort_flag, status, wait_ns);
+      if (!ok) break;
       // this warp's private copy of the head weights of its queries, and their key ranges
       const int t0 = ui.group * G + g0;
       for (int i = lane; i < NH; i += 32) {
         const int t = t0 + i / HI;
         w_s[i] = t < A.n_q ? __ldg(A.w + static_cast<size_t>(t) * HI + (i % HI)) : 0.f;
       }
-      int qa[GH], qb[GH];
+      int qa[GH], qb[GH], cnt[GH];
+      uint32_t lmin[GH], lmax[GH];   // per lane: extremes of the keys it kept
       bool qf[GH];
 #pragma unroll
       for (int g = 0; g < GH; ++g) {
@@ -584,14 +599,14 @@ __global__ void __launch_bounds__(Cfg<HI, DI, G>::THREADS, 1)
         qa[g] = r.a;
         qb[g] = r.b;
         qf[g] = r.filtered;
+        cnt[g] = 0;
+        lmin[g] = 0xFFFFFFFFu;
+        lmax[g] = 0u;
       }
       __syncwarp();
       for (int i = 0; i < ui.n_tiles; ++i, ++tile) {
         const int buf = tile & 1;
-        const int slot = rtile % RING;
         ok = warp_wait(&sh.t_full[buf], (tile >> 1) & 1, &sh.abort_flag, status, wait_ns);
-        if (ok && uses_ring && rtile >= RING)
-          ok = warp_wait(&sh.r_empty[slot], ((rtile / RING) - 1) & 1, &sh.abort_flag, status, wait_ns);
         if (!ok) break;
         tc_fence_after();
         // head sum of this half's queries with NP independent partial sums per query (breaks
@@ -632,48 +647,66 @@ __global__ void __launch_bounds__(Cfg<HI, DI, G>::THREADS, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh.t_empty[buf]);
         const int j = ui.kbeg + i * kKeyTile + row;
-        float* rs = reinterpret_cast<float*>(ring + static_cast<size_t>(slot) * C::RING_SLOT);
-        uint32_t* rm = reinterpret_cast<uint32_t*>(ring + static_cast<size_t>(slot) * C::RING_SLOT + C::RING_SCORES);
 #pragma unroll
         for (int g = 0; g < GH; ++g) {
           float acc;
           if constexpr (NP == 4) acc = (part[g][0] + part[g][1]) + (part[g][2] + part[g][3]);
           else acc = part[g][0];
-          const bool in = j >= qa[g] && j < qb[g];
-          if (!qf[g]) {
-            // direct: every key of the range at its offset
-            if (in) {
-              const size_t off = (static_cast<size_t>(t0 + g) * A.n_chunks + ui.chunk) * cap + (j - qa[g]);
-              A.cand_key[off] = float_key(acc);
-              A.cand_idx[off] = j;
+          const uint32_t key = float_key(acc);
+          const uint32_t tk = qf[g] ? *reinterpret_cast<volatile uint32_t*>(&sh.tau[par][g0 + g]) : 0u;
+          const bool keep = j >= qa[g] && j < qb[g] && key >= tk;
+          const uint32_t m = __ballot_sync(0xffffffffu, keep);
+          if (m == 0u) continue;
+          const size_t off = ((static_cast<size_t>(t0 + g) * A.n_chunks + ui.chunk) * kSub + quarter) * cap4;
+          if (keep) {
+            const int p = cnt[g] + __popc(m & below);
+            if (p < cap4) {
+              A.cand_key[off + p] = key;
+              A.cand_idx[off + p] = j;
             }
-            if (uses_ring && lane == 0) rm[(g0 + g) * 4 + quarter] = 0u;
-          } else {
-            // filtered: the score and whether it reaches the query's published threshold
-            const uint64_t tv = *reinterpret_cast<volatile uint64_t*>(&sh.tau[g0 + g]);
-            const uint32_t tk = static_cast<uint32_t>(tv >> 32) == unit_ord ? static_cast<uint32_t>(tv) : 0u;
-            const uint32_t m = __ballot_sync(0xffffffffu, in && float_key(acc) >= tk);
-            rs[(g0 + g) * kKeyTile + row] = acc;
-            if (lane == 0) rm[(g0 + g) * 4 + quarter] = m;
+            if (qf[g]) {
+              atomicAdd(&sh.hist[par][g0 + g][hist_bin<C>(key)], 1u);
+              lmin[g] = min(lmin[g], key);
+              lmax[g] = max(lmax[g], key);
+            }
+          }
+          cnt[g] += __popc(m);
+          if (qf[g] && cnt[g] > cap4 - 32) {
+            // this sub-buffer could overflow on the next tile (scores rising along the keys):
+            // cut it back to exactly its own top-k, which keeps every key of the row's top-k in it
+            if (cnt[g] > cap4) {
+              if (lane == 0) atomicOr(status, DEV_ERR_OVERFLOW);
+              cnt[g] = cap4;
+            }
+            __syncwarp();   // this warp's stores are visible to all its lanes
+            uint32_t kmin = __reduce_min_sync(0xffffffffu, lmin[g]), kmax = __reduce_max_sync(0xffffffffu, lmax[g]);
+            uint32_t v = 0, cutv = 0;
+            warp_exact_threshold(A.cand_key + off, A.cand_idx + off, cnt[g], A.topk, kmin, kmax, ws, ws.bc, v, cutv);
+            cnt[g] = warp_compact(A.cand_key + off, A.cand_idx + off, cnt[g],
+                                  [&](uint32_t kk, int32_t ix) { return topk_keep(kk, ix, v, cutv); }, kmin, kmax);
+            lmin[g] = kmin;
+            lmax[g] = kmax;
           }
         }
-        if (uses_ring) {
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sh.r_full[slot]);
-          ++rtile;
+      }
+      if (!ok) break;
+      // this warp's count of each of its queries in this chunk
+      if (lane == 0) {
+#pragma unroll
+        for (int g = 0; g < GH; ++g) {
+          const int t = t0 + g;
+          if (t < A.n_q)
+            A.cand_cnt[(static_cast<size_t>(t) * A.n_chunks + ui.chunk) * kSub + quarter] =
+                static_cast<uint32_t>(min(cnt[g], cap4));
         }
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.u_done[par]);
       ++unit_ord;
     }
   } else {
-    // ------------------------------------------------------------------ top-k warps
-    using Cf = C;
-    const int tw = warp - 2 - NE;               // queries tw, tw + NT, ...
-    constexpr int QPT = C::QPT;
-    WarpScratch& ws = sh.ws[tw];
-    const uint32_t below = (1u << lane) - 1u;
-    const int topk = A.topk;
-    uint32_t rtile = 0, unit_ord = 0;
+    // ------------------------------------------------------------------ threshold warp
+    uint32_t unit_ord = 0;
     bool ok = true;
     for (int k = 0; k * static_cast<int>(gridDim.x) < n_units && ok; ++k) {
       const int u = snake_unit(k);
@@ -681,152 +714,70 @@ __global__ void __launch_bounds__(Cfg<HI, DI, G>::THREADS, 1)
       const UnitInfo ui = unit_info(u, A.n_groups, A.chunk_len, A.group_range);
       if (ui.n_tiles == 0) {
         // an empty chunk still tells the final select that it holds no candidates
-        if (lane == 0)
-          for (int g = tw; g < G; g += NT) {
-            const int t = ui.group * G + g;
-            if (t < A.n_q) {
-              A.cand_cnt[static_cast<size_t>(t) * A.n_chunks + ui.chunk] = 0u;
-              A.cand_edge[static_cast<size_t>(t) * A.n_chunks + ui.chunk] = 0u;
-            }
-          }
+        for (int e = lane; e < G * kSub; e += 32) {
+          const int t = ui.group * G + e / kSub;
+          if (t < A.n_q) A.cand_cnt[(static_cast<size_t>(t) * A.n_chunks + ui.chunk) * kSub + (e % kSub)] = 0u;
+        }
+        for (int g = lane; g < G; g += 32) {
+          const int t = ui.group * G + g;
+          if (t < A.n_q) A.cand_edge[static_cast<size_t>(t) * A.n_chunks + ui.chunk] = 0u;
+        }
         continue;
       }
-      const bool uses_ring = unit_filtered(ui);
-      // per owned query: range, filtered or not, count, threshold bin, entries at or above it
-      int qa[QPT], qb[QPT], cnt[QPT], bstar[QPT], above[QPT];
-      uint32_t lmin[QPT], lmax[QPT];   // per lane: extremes of the keys it appended
-      bool qf[QPT];
-#pragma unroll
-      for (int qi = 0; qi < QPT; ++qi) {
-        const int g = tw + qi * NT;
-        const QueryRange r = query_range(A.row_range, ui.group * G + g, A.n_q, ui, A.trivial_len, A.direct_max);
-        qa[qi] = r.a;
-        qb[qi] = r.b;
-        qf[qi] = g < G && r.filtered;
-        cnt[qi] = 0;
-        bstar[qi] = 0;
-        above[qi] = 0;
-        lmin[qi] = 0xFFFFFFFFu;
-        lmax[qi] = 0u;
-        if (qf[qi]) {
-          for (int b = lane; b < C::NB; b += 32) sh.hist[g][b] = 0u;
-          if (lane == 0) *reinterpret_cast<volatile uint64_t*>(&sh.tau[g]) = static_cast<uint64_t>(unit_ord) << 32;
-        }
-      }
-      __syncwarp();
-      if (uses_ring) {
-        for (int i = 0; i < ui.n_tiles; ++i, ++rtile) {
-          const int slot = rtile % RING;
-          ok = warp_wait(&sh.r_full[slot], (rtile / RING) & 1, &sh.abort_flag, status, wait_ns);
-          if (!ok) break;
-          const float* rs = reinterpret_cast<const float*>(ring + static_cast<size_t>(slot) * C::RING_SLOT);
-          const uint32_t* rm = reinterpret_cast<const uint32_t*>(ring + static_cast<size_t>(slot) * C::RING_SLOT + C::RING_SCORES);
-          const int tile0 = ui.kbeg + i * kKeyTile;
-#pragma unroll
-          for (int qi = 0; qi < QPT; ++qi) {
-            const int g = tw + qi * NT;
-            if (!qf[qi]) continue;
-            const uint4 m4 = *reinterpret_cast<const uint4*>(&rm[g * 4]);
-            if ((m4.x | m4.y | m4.z | m4.w) == 0u) continue;
-            const size_t off = (static_cast<size_t>(ui.group * G + g) * A.n_chunks + ui.chunk) * cap;
-            const uint32_t mq[4] = {m4.x, m4.y, m4.z, m4.w};
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-              const uint32_t m = mq[r];
-              if (m == 0u) continue;
-              const bool pass = (m >> lane) & 1u;
-              int bin = -1;
-              if (pass) {
-                const uint32_t key = float_key(rs[g * kKeyTile + r * 32 + lane]);
-                const int p = cnt[qi] + __popc(m & below);
-                if (p < cap) {
-                  A.cand_key[off + p] = key;
-                  A.cand_idx[off + p] = tile0 + r * 32 + lane;
-                }
-                bin = hist_bin<Cf>(key);
-                atomicAdd(&sh.hist[g][bin], 1u);
-                lmin[qi] = min(lmin[qi], key);
-                lmax[qi] = max(lmax[qi], key);
-              }
-              // entries at or above the current boundary bin count towards it (a threshold
-              // published late lets a few lower ones in: they are kept, not counted)
-              above[qi] += __popc(__ballot_sync(0xffffffffu, bin >= bstar[qi]));
-              cnt[qi] += __popc(m);
-            }
-            __syncwarp();
-            // raise the boundary bin while the entries strictly above it are k or more
-            int b = bstar[qi], ab = above[qi];
-            while (b < C::NB - 1) {
-              const int h = static_cast<int>(sh.hist[g][b]);
-              if (ab - h < topk) break;
-              ab -= h;
-              ++b;
-            }
-            if (b != bstar[qi]) {
-              bstar[qi] = b;
-              above[qi] = ab;
-              if (lane == 0)
-                *reinterpret_cast<volatile uint64_t*>(&sh.tau[g]) =
-                    (static_cast<uint64_t>(unit_ord) << 32) | bin_edge_key<Cf>(b);
-            }
+      const int par = unit_ord & 1;
+      // per filtered query (lane g holds query g's state)
+      bool filt = false;
+      if (lane < G) filt = query_range(A.row_range, ui.group * G + lane, A.n_q, ui, A.trivial_len, A.direct_max).filtered;
+      const uint32_t fmask = __ballot_sync(0xffffffffu, filt);
+      int bstar = 0, above = 0;   // lane g: query g's boundary bin and entries at or above it
+      const uint64_t t0 = globaltimer_ns();
+      while (true) {
+        const bool done = mbar_try_wait(&sh.u_done[par], (unit_ord >> 1) & 1);
+        // raise the threshold of every filtered query (the whole warp sums one histogram)
+        for (uint32_t fm = fmask; fm; fm &= fm - 1) {
+          const int g = __ffs(fm) - 1;
+          const int b0 = __shfl_sync(0xffffffffu, bstar, g);
+          int ab = 0;
+          const int b = climb<NB>(sh.hist[par][g], b0, A.topk, &ab);
+          if (lane == g) {
+            bstar = b;
+            above = ab;
           }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sh.r_empty[slot]);
-          // a buffer that could overflow on the next tile: cut it back to exactly the top-k
-          // (rare: only when scores keep rising along the keys) and rebuild its histogram
-#pragma unroll 1
-          for (int qi = 0; qi < QPT; ++qi) {
-            const int g = tw + qi * NT;
-            if (!qf[qi] || cnt[qi] <= cap - kKeyTile) continue;
-            const size_t off = (static_cast<size_t>(ui.group * G + g) * A.n_chunks + ui.chunk) * cap;
-            if (cnt[qi] > cap) {
-              if (lane == 0) atomicOr(status, DEV_ERR_OVERFLOW);
-              cnt[qi] = cap;
-            }
-            __syncwarp();   // this warp's appends are visible to all its lanes
-            uint32_t kmin = __reduce_min_sync(0xffffffffu, lmin[qi]), kmax = __reduce_max_sync(0xffffffffu, lmax[qi]);
-            uint32_t v = 0, cutv = 0;
-            warp_exact_threshold(A.cand_key + off, A.cand_idx + off, cnt[qi], topk, kmin, kmax, ws, ws.bc, v, cutv);
-            cnt[qi] = warp_compact(A.cand_key + off, A.cand_idx + off, cnt[qi],
-                                   [&](uint32_t key, int32_t idx) { return topk_keep(key, idx, v, cutv); }, kmin, kmax);
-            lmin[qi] = kmin;
-            lmax[qi] = kmax;
-            for (int b = lane; b < C::NB; b += 32) sh.hist[g][b] = 0u;
-            __syncwarp();
-            warp_for_each<false>(A.cand_key + off, A.cand_idx + off, cnt[qi], [&](bool okk, uint32_t key, int32_t) {
-              if (okk) atomicAdd(&sh.hist[g][hist_bin<Cf>(key)], 1u);
-            });
-            __syncwarp();
-            int b = 0, ab = cnt[qi];
-            while (b < C::NB - 1) {
-              const int h = static_cast<int>(sh.hist[g][b]);
-              if (ab - h < topk) break;
-              ab -= h;
-              ++b;
-            }
-            bstar[qi] = b;
-            above[qi] = ab;
-            if (lane == 0)
-              *reinterpret_cast<volatile uint64_t*>(&sh.tau[g]) =
-                  (static_cast<uint64_t>(unit_ord) << 32) | (b > 0 ? bin_edge_key<Cf>(b) : 0u);
-          }
+          if (b != b0 && lane == 0)
+            *reinterpret_cast<volatile uint32_t*>(&sh.tau[par][g]) = b > 0 ? bin_edge_key<C>(b) : 0u;
         }
+        if (__all_sync(0xffffffffu, done)) break;
+        if (sh.abort_flag) {
+          ok = false;
+          break;
+        }
+        // the head-sum warps' own bounded waits end a stalled unit (abort flag above); this
+        // bound is only a safety net
+        if (globaltimer_ns() - t0 > 100ull * wait_ns) {
+          if (lane == 0) {
+            sh.abort_flag = 1u;
+            atomicOr(status, DEV_ERR_TIMEOUT);
+          }
+          ok = false;
+          break;
+        }
+        __nanosleep(fmask ? 256 : 2048);
       }
       if (!ok) break;
-      // the unit is done: each row's count in this chunk, and the lower edge of its boundary
-      // bin when at least k entries lie at or above it (no entry below can make the top-k)
-      if (lane == 0) {
-#pragma unroll
-        for (int qi = 0; qi < QPT; ++qi) {
-          const int g = tw + qi * NT;
-          const int t = ui.group * G + g;
-          if (g >= G || t >= A.n_q) continue;
-          const int n = qf[qi] ? min(cnt[qi], cap) : qb[qi] - qa[qi];
-          A.cand_cnt[static_cast<size_t>(t) * A.n_chunks + ui.chunk] = static_cast<uint32_t>(n);
+      // the unit is done: each row's edge in this chunk (the lower edge of its boundary bin
+      // when at least k entries lie at or above it: nothing below can make the row's top-k)
+      if (lane < G) {
+        const int t = ui.group * G + lane;
+        if (t < A.n_q)
           A.cand_edge[static_cast<size_t>(t) * A.n_chunks + ui.chunk] =
-              qf[qi] && bstar[qi] > 0 && above[qi] >= topk ? bin_edge_key<Cf>(bstar[qi]) : 0u;
-        }
+              filt && bstar > 0 && above >= A.topk ? bin_edge_key<C>(bstar) : 0u;
       }
+      // reset this parity for the unit after next, then let its head-sum warps start
+      for (int i = lane; i < G * NB; i += 32) (&sh.hist[par][0][0])[i] = 0u;
+      if (lane < G) sh.tau[par][lane] = 0u;
+      __syncwarp();
+      __threadfence_block();
+      if (lane == 0) mbar_arrive(&sh.u_ready[par]);
       ++unit_ord;
     }
   }
@@ -873,7 +824,7 @@ cudaError_t launch_indexer(const IndexerPlan& p, const CUtensorMap& tq, const CU
   A.n_chunks = p.n_chunks;
   A.chunk_len = p.chunk;
   A.cap = p.cap;
-  A.direct_max = p.cap < 4096 ? p.cap : 4096;
+  A.direct_max = kDirectMax;
   A.topk = p.topk;
   A.trivial_len = trivial_len;
   A.cand_key = ck;

@@ -36,6 +36,12 @@ cudaError_t launch_rope_rows(const void* in, void* out, const int32_t* pos, int6
                              int rope, const float* cs, int n_pos, uint32_t* status, cudaStream_t st);
 
 // ---------------------------------------------------------------------------- indexer
+// Candidate buffers: per (row, key chunk) kSub sub-buffers of cap / kSub entries, one per
+// lane quarter of the indexer's 128-key tiles (keys j with (j - chunk start) % 128 in
+// [32 q, 32 q + 32) go to sub-buffer q, in key order).
+constexpr int kSub = 4;
+// Rows with at most kDirectMax keys in a chunk keep every key (no streaming threshold).
+constexpr int kDirectMax = 4096;
 struct IndexerPlan {
   int n_heads, head_dim, group;      // group = query rows sharing one key stream (G)
   int n_groups, n_chunks, chunk;     // key chunking of every group's range
