@@ -346,26 +346,13 @@ __device__ __forceinline__ int warp_compact(uint32_t* keys, int32_t* idxs, int n
   return written;
 }
 
-// Cut a candidate buffer back to a superset of its top-K.  Coarse when it frees enough room:
-// every entry in the boundary bin or above is kept (>= K entries, everything dropped scores
-// below everything kept).  Otherwise exact: exactly K kept.  Either way the new threshold is
-// the smallest kept key: a later key at or below it has at least K earlier keys at or above
-// it and loses to them (ties go to the lower index).
-__device__ int warp_cut_back(uint32_t* keys, int32_t* idxs, int n, int K, int cap, uint32_t& kmin, uint32_t& kmax,
-                             WarpScratch& ws, int* bc) {
-  const int lane = threadIdx.x & 31;
-  const BinMap bin(kmin, kmax);
-  for (int i = lane; i < kBins; i += 32) ws.hist[i] = 0u;
-  __syncwarp();
-  warp_for_each<false>(keys, idxs, n, [&](bool ok, uint32_t key, int32_t) { warp_hist_add(ws.hist, ok ? bin(key) : -1); });
-  __syncwarp();
-  const Boundary bd = warp_boundary(ws.hist, K);
-  const int kept = bd.above + bd.hb;
-  __syncwarp();
-  if (kept <= K + (cap - K) / 2 && kept + kKeyTile <= cap)
-    return warp_compact(keys, idxs, n, [&](uint32_t key, int32_t) { return bin(key) >= bd.b; }, kmin, kmax);
+// Cut a candidate buffer back to exactly its top-K (ties to the lower index), keeping the
+// survivors in key order; returns the count and updates [kmin, kmax] to the kept keys.  Kept
+// out of line: it runs only when scores keep rising along the keys.
+__device__ __noinline__ int warp_cut_to_topk(uint32_t* keys, int32_t* idxs, int n, int K, uint32_t& kmin,
+                                             uint32_t& kmax, WarpScratch& ws) {
   uint32_t v = 0, cut = 0;
-  warp_exact_threshold(keys, idxs, n, K, kmin, kmax, ws, bc, v, cut);
+  warp_exact_threshold(keys, idxs, n, K, kmin, kmax, ws, ws.bc, v, cut);
   return warp_compact(keys, idxs, n, [&](uint32_t key, int32_t idx) { return topk_keep(key, idx, v, cut); }, kmin,
                       kmax);
 }
@@ -604,43 +591,109 @@ __global__ void __launch_bounds__(Cfg<HI, DI, G>::THREADS, 1)
         lmax[g] = 0u;
       }
       __syncwarp();
+      // With 8 or more heads per query the TMEM tile is read in the 16x256b shape: thread t
+      // holds keys t/4 + 8 r (r < 4) of its lane quarter and, of every group of 8 columns, the
+      // two columns 2 (t % 4) and 2 (t % 4) + 1 -- so it needs only NH / 4 head weights, which
+      // stay in registers for the whole unit.
+      constexpr bool kWide = HI >= 8;
+      constexpr int NG = NH / 8;                 // column groups of this warp
+      float2 wr[kWide ? NG : 1];
+      if constexpr (kWide) {
+#pragma unroll
+        for (int k = 0; k < NG; ++k) wr[k] = *reinterpret_cast<const float2*>(&w_s[8 * k + 2 * (lane & 3)]);
+      }
       for (int i = 0; i < ui.n_tiles; ++i, ++tile) {
         const int buf = tile & 1;
         ok = warp_wait(&sh.t_full[buf], (tile >> 1) & 1, &sh.abort_flag, status, wait_ns);
         if (!ok) break;
         tc_fence_after();
-        // head sum of this half's queries with NP independent partial sums per query (breaks
-        // the dependent FMA chain); TMEM read 64 columns per wait
-        constexpr int NP = HI >= 16 ? 4 : 1;
-        float part[GH][NP];
+        float accs[GH];   // this lane's key (row of the quarter): its score for every query of the half
+        if constexpr (kWide) {
+          constexpr int GPQ = HI / 8;              // column groups per query
+          float part[4][GH][2];
 #pragma unroll
-        for (int g = 0; g < GH; ++g)
+          for (int r = 0; r < 4; ++r)
 #pragma unroll
-          for (int p = 0; p < NP; ++p) part[g][p] = 0.f;
+            for (int g = 0; g < GH; ++g) part[r][g][0] = part[r][g][1] = 0.f;
 #pragma unroll
-        for (int c0 = 0; c0 < NH; c0 += 64) {
-          const int cc = half * NH + c0;   // TMEM column of this chunk
-          uint32_t v[64];
-          tmem_ld32(tmem + t_lane + buf * N + cc, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-          tmem_ld32(tmem + t_lane + buf * N + cc + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-          tmem_ld_wait();
+          for (int c0 = 0; c0 < NH; c0 += 32) {
+            uint32_t v[2][16];
 #pragma unroll
-          for (int j = 0; j < 64; j += 4) {
-            const float4 wv = *reinterpret_cast<const float4*>(&w_s[c0 + j]);
-            const float r0 = fmaxf(__uint_as_float(v[j]), 0.f), r1 = fmaxf(__uint_as_float(v[j + 1]), 0.f);
-            const float r2 = fmaxf(__uint_as_float(v[j + 2]), 0.f), r3 = fmaxf(__uint_as_float(v[j + 3]), 0.f);
-            const int gl = (c0 + j) / HI;   // query within the half
-            if constexpr (NP == 4) {
-              fma2(part[gl][0], part[gl][1], wv.x, wv.y, r0, r1);
-              fma2(part[gl][2], part[gl][3], wv.z, wv.w, r2, r3);
-            } else {
-              const float wj[4] = {wv.x, wv.y, wv.z, wv.w}, rj[4] = {r0, r1, r2, r3};
+            for (int h16 = 0; h16 < 2; ++h16)
+              tmem_ld_16x256b<4>(tmem + (static_cast<uint32_t>(quarter * 32 + h16 * 16) << 16) + buf * N + half * NH + c0,
+                                 v[h16]);
+            tmem_ld_wait();
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                float& acc_e = part[(c0 + j + e) / HI][0];
-                acc_e = fmaf(wj[e], rj[e], acc_e);
+            for (int h16 = 0; h16 < 2; ++h16)
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const int kk = c0 / 8 + k;         // column group within the half
+                const int gl = kk / GPQ;           // query within the half
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) {
+                  const float a = fmaxf(__uint_as_float(v[h16][4 * k + 2 * rr]), 0.f);
+                  const float b = fmaxf(__uint_as_float(v[h16][4 * k + 2 * rr + 1]), 0.f);
+                  fma2(part[2 * h16 + rr][gl][0], part[2 * h16 + rr][gl][1], wr[kk].x, wr[kk].y, a, b);
+                }
+              }
+          }
+          // complete each key's sum over the four threads that share it, then move key L's score
+          // to lane L
+#pragma unroll
+          for (int g = 0; g < GH; ++g) {
+            float sr[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+              float x = part[r][g][0] + part[r][g][1];
+              x += __shfl_xor_sync(0xffffffffu, x, 1);
+              x += __shfl_xor_sync(0xffffffffu, x, 2);
+              sr[r] = x;
+            }
+            const int src = 4 * (lane & 7);
+            const float x0 = __shfl_sync(0xffffffffu, sr[0], src), x1 = __shfl_sync(0xffffffffu, sr[1], src);
+            const float x2 = __shfl_sync(0xffffffffu, sr[2], src), x3 = __shfl_sync(0xffffffffu, sr[3], src);
+            const int rsel = lane >> 3;
+            accs[g] = rsel == 0 ? x0 : rsel == 1 ? x1 : rsel == 2 ? x2 : x3;
+          }
+        } else {
+          // head sum of this half's queries with NP independent partial sums per query (breaks
+          // the dependent FMA chain); TMEM read 64 columns per wait
+          constexpr int NP = HI >= 16 ? 4 : 1;
+          float part[GH][NP];
+#pragma unroll
+          for (int g = 0; g < GH; ++g)
+#pragma unroll
+            for (int p = 0; p < NP; ++p) part[g][p] = 0.f;
+#pragma unroll
+          for (int c0 = 0; c0 < NH; c0 += 64) {
+            const int cc = half * NH + c0;   // TMEM column of this chunk
+            uint32_t v[64];
+            tmem_ld32(tmem + t_lane + buf * N + cc, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+            tmem_ld32(tmem + t_lane + buf * N + cc + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 64; j += 4) {
+              const float4 wv = *reinterpret_cast<const float4*>(&w_s[c0 + j]);
+              const float r0 = fmaxf(__uint_as_float(v[j]), 0.f), r1 = fmaxf(__uint_as_float(v[j + 1]), 0.f);
+              const float r2 = fmaxf(__uint_as_float(v[j + 2]), 0.f), r3 = fmaxf(__uint_as_float(v[j + 3]), 0.f);
+              const int gl = (c0 + j) / HI;   // query within the half
+              if constexpr (NP == 4) {
+                fma2(part[gl][0], part[gl][1], wv.x, wv.y, r0, r1);
+                fma2(part[gl][2], part[gl][3], wv.z, wv.w, r2, r3);
+              } else {
+                const float wj[4] = {wv.x, wv.y, wv.z, wv.w}, rj[4] = {r0, r1, r2, r3};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  float& acc_e = part[(c0 + j + e) / HI][0];
+                  acc_e = fmaf(wj[e], rj[e], acc_e);
+                }
               }
             }
+          }
+#pragma unroll
+          for (int g = 0; g < GH; ++g) {
+            if constexpr (NP == 4) accs[g] = (part[g][0] + part[g][1]) + (part[g][2] + part[g][3]);
+            else accs[g] = part[g][0];
           }
         }
         tc_fence_before();
@@ -649,10 +702,7 @@ __global__ void __launch_bounds__(Cfg<HI, DI, G>::THREADS, 1)
         const int j = ui.kbeg + i * kKeyTile + row;
 #pragma unroll
         for (int g = 0; g < GH; ++g) {
-          float acc;
-          if constexpr (NP == 4) acc = (part[g][0] + part[g][1]) + (part[g][2] + part[g][3]);
-          else acc = part[g][0];
-          const uint32_t key = float_key(acc);
+          const uint32_t key = float_key(accs[g]);
           const uint32_t tk = qf[g] ? *reinterpret_cast<volatile uint32_t*>(&sh.tau[par][g0 + g]) : 0u;
           const bool keep = j >= qa[g] && j < qb[g] && key >= tk;
           const uint32_t m = __ballot_sync(0xffffffffu, keep);
@@ -680,10 +730,7 @@ __global__ void __launch_bounds__(Cfg<HI, DI, G>::THREADS, 1)
             }
             __syncwarp();   // this warp's stores are visible to all its lanes
             uint32_t kmin = __reduce_min_sync(0xffffffffu, lmin[g]), kmax = __reduce_max_sync(0xffffffffu, lmax[g]);
-            uint32_t v = 0, cutv = 0;
-            warp_exact_threshold(A.cand_key + off, A.cand_idx + off, cnt[g], A.topk, kmin, kmax, ws, ws.bc, v, cutv);
-            cnt[g] = warp_compact(A.cand_key + off, A.cand_idx + off, cnt[g],
-                                  [&](uint32_t kk, int32_t ix) { return topk_keep(kk, ix, v, cutv); }, kmin, kmax);
+            cnt[g] = warp_cut_to_topk(A.cand_key + off, A.cand_idx + off, cnt[g], A.topk, kmin, kmax, ws);
             lmin[g] = kmin;
             lmax[g] = kmax;
           }
