@@ -24,16 +24,18 @@
 // Warp roles (no role waits on a CTA-wide barrier inside the tile loop):
 //   warp 0            TMA producer: Q of the unit once, K tiles through a STAGES-deep ring;
 //   warp 1            MMA issuer (owns TMEM);
-//   head-sum warps    NE = 4 or 8: a warp owns one TMEM lane quarter (32 keys) and half or
-//                     all of the group's queries; it reduces the heads of each query in
-//                     registers (ReLU * w with packed fp32 FMAs), keeps the keys at or above
-//                     the query's tau in its own sub-buffer (no other warp writes there) and
-//                     counts them in the query's histogram.  A sub-buffer that could overflow
-//                     (scores that keep rising along the keys) is cut back by its warp to
-//                     exactly its top-k, which still holds every key of the row's top-k that
-//                     lies in it;
-//   threshold warp    keeps raising each filtered query's tau from its histogram while the
-//                     unit runs; histograms and taus are double-buffered by unit parity.
+//   warp 2            threshold warp: keeps raising each filtered query's tau from its
+//                     histogram while the unit runs; histograms and taus are double-buffered
+//                     by unit parity;
+//   warp 3            idle (completes warpgroup 0, which gives registers to the head-sum warps);
+//   warps 4..         NE = 4 or 8 head-sum warps: a warp owns one TMEM lane quarter (32 keys)
+//                     and half or all of the group's queries; it reduces the heads of each
+//                     query with the head weights held in registers (ReLU * w with packed fp32
+//                     FMAs), keeps the keys at or above the query's tau in its own sub-buffer
+//                     (no other warp writes there) and counts them in the query's histogram.
+//                     A sub-buffer that could overflow (scores that keep rising along the
+//                     keys) is cut back by its warp to exactly its top-k, which still holds
+//                     every key of the row's top-k that lies in it.
 // The score matrix is never written anywhere.
 #include <cuda_bf16.h>
 
@@ -67,7 +69,14 @@ struct Cfg {
   static constexpr int NE = 4 * HALVES;
   static constexpr int GH = G / HALVES;                  // queries per half
   static constexpr int NH = N / HALVES;                  // TMEM columns per half
-  static constexpr int THREADS = 32 * (3 + NE);          // + producer, MMA, threshold warps
+  // warpgroup 0: producer, MMA, threshold and one idle warp; then NE / 4 head-sum warpgroups
+  static constexpr int THREADS = 32 * (4 + NE);
+  // With two head-sum warpgroups (384 threads, 168 registers a thread at launch) warpgroup 0
+  // hands registers to the head-sum warps, which keep all NH head weights of their queries in
+  // registers: 128 * REG_LOW + 256 * REG_HIGH stays within the 384 * 168 the block holds.
+  static constexpr bool REG_SPLIT = NE == 8;
+  static constexpr int REG_LAUNCH = 168, REG_LOW = 56, REG_HIGH = 224;
+  static_assert(!REG_SPLIT || 128 * REG_LOW + 256 * REG_HIGH <= THREADS * REG_LAUNCH, "register split");
   // threshold histograms: NB bins per query per unit parity (16 KB in all), log-spaced over
   // 2^kLog2Span octaves
   static constexpr int NB = 2048 / G < 512 ? 2048 / G : 512;
@@ -81,7 +90,7 @@ struct Cfg {
   static constexpr int DYN_SMEM = 1024 + Q_BYTES + STAGES * K_STAGE_BYTES;
   static constexpr uint32_t TMEM_COLS = (2 * N <= 32) ? 32 : (2 * N <= 64) ? 64 : (2 * N <= 128) ? 128 : (2 * N <= 256) ? 256 : 512;
   static_assert(N % 64 == 0 && N >= 64 && N <= 256, "MMA N");
-  static_assert(NH % 64 == 0, "head-sum reads 64 columns at a time");
+  static_assert(NH % 32 == 0 && NH <= 128, "head-sum reads 32 columns at a time, weights in registers");
   static_assert(GH * HI == NH, "a half holds whole queries");
   static_assert(G <= 16, "the threshold warp keeps one query per lane, at most 16");
   static_assert(STAGES >= 2, "shared memory");
@@ -452,106 +461,11 @@ __global__ void __launch_bounds__(Cfg<HI, DI, G>::THREADS, 1)
   }
   const uint32_t tmem = sh.tmem_base;
   const unsigned long long wait_ns = A.wait_ns;
-
-  if (warp == 0) {
-    // ------------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      tma_prefetch_desc(&tmap_q);
-      tma_prefetch_desc(&tmap_k);
-      tma_prefetch_desc(&tmap_q_in);
-      tma_prefetch_desc(&tmap_k_in);
-      uint32_t kstage = 0, q_uses = 0;
-      bool ok = true;
-      for (int k = 0; k * static_cast<int>(gridDim.x) < n_units && ok; ++k) {
-        const int u = snake_unit(k);
-        if (u >= n_units) continue;
-        const UnitInfo ui = unit_info(u, A.n_groups, A.chunk_len, A.group_range);
-        if (ui.n_tiles == 0) continue;
-        if (q_uses > 0) ok = mbar_wait_for(&sh.q_empty, (q_uses - 1) & 1, &sh.abort_flag, status, wait_ns);
-        if (!ok) break;
-        mbar_arrive_expect_tx(&sh.q_full, C::Q_BYTES);
-        // 64-dim blocks without rotary dims come from the unrotated input
-        for (int b = 0; b < KB; ++b)
-          tma_load_2d(sQ + b * N * 128, b < q_split ? &tmap_q_in : &tmap_q, &sh.q_full, b * 64, ui.group * N);
-        ++q_uses;
-        for (int i = 0; i < ui.n_tiles; ++i, ++kstage) {
-          if (A.stop_after >= 0 && kstage >= static_cast<uint32_t>(A.stop_after)) {
-            ok = false;   // test hook: stop feeding the pipeline; its waits then run out
-            break;
-          }
-          const int s = kstage % STAGES;
-          if (kstage >= STAGES) {
-            ok = mbar_wait_for(&sh.k_empty[s], ((kstage / STAGES) - 1) & 1, &sh.abort_flag, status, wait_ns);
-            if (!ok) break;
-          }
-          mbar_arrive_expect_tx(&sh.k_full[s], C::K_STAGE_BYTES);
-          uint8_t* dst = sK + s * C::K_STAGE_BYTES;
-          // cache row of the tile's first key: contiguous, or its page (one 128-key tile per
-          // page; a group is one row in paged mode).  A page outside the cache is flagged and
-          // row 0 read instead (the tile's scores are then meaningless, the status says so).
-          int krow = ui.kbeg + i * kKeyTile;
-          if (pg.block_table) {
-            const int lp = krow >> kPageShift;
-            const int page = lp < pg.max_pages ? __ldg(pg.block_table + static_cast<size_t>(ui.group) * pg.max_pages + lp) : -1;
-            if (page < 0 || page >= pg.n_pages) {
-              atomicOr(status, DEV_ERR_BAD_INDEX);
-              krow = 0;
-            } else {
-              krow = page << kPageShift;
-            }
-          }
-          for (int b = 0; b < KB; ++b)
-            tma_load_2d(dst + b * kKeyTile * 128, b < k_split ? &tmap_k_in : &tmap_k, &sh.k_full[s], b * 64, krow);
-        }
-      }
-      // let copies still in flight land before the CTA can exit (bounded; normally all done)
-      if (q_uses > 0) mbar_drain(&sh.q_full, (q_uses - 1) & 1, 200000000ull);
-      for (uint32_t j = kstage > STAGES ? kstage - STAGES : 0; j < kstage; ++j)
-        mbar_drain(&sh.k_full[j % STAGES], (j / STAGES) & 1, 200000000ull);
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(128, N, 0, 0);
-      uint32_t kstage = 0, q_uses = 0, tile = 0;
-      bool ok = true;
-      for (int k = 0; k * static_cast<int>(gridDim.x) < n_units && ok; ++k) {
-        const int u = snake_unit(k);
-        if (u >= n_units) continue;
-        const UnitInfo ui = unit_info(u, A.n_groups, A.chunk_len, A.group_range);
-        if (ui.n_tiles == 0) continue;
-        ok = mbar_wait_for(&sh.q_full, q_uses & 1, &sh.abort_flag, status, wait_ns);
-        if (!ok) break;
-        ++q_uses;
-        for (int i = 0; i < ui.n_tiles; ++i, ++kstage, ++tile) {
-          const int s = kstage % STAGES;
-          const int buf = tile & 1;
-          ok = mbar_wait_for(&sh.k_full[s], (kstage / STAGES) & 1, &sh.abort_flag, status, wait_ns);
-          if (ok && tile >= 2) ok = mbar_wait_for(&sh.t_empty[buf], ((tile >> 1) - 1) & 1, &sh.abort_flag, status, wait_ns);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t a0 = smem_u32(sK + s * C::K_STAGE_BYTES);
-          const uint32_t b0 = smem_u32(sQ);
-#pragma unroll
-          for (int k = 0; k < DI / 16; ++k) {
-            const int kb = k >> 2, sub = k & 3;
-            const uint64_t ad = sdesc_sw128(a0 + kb * kKeyTile * 128 + sub * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(b0 + kb * N * 128 + sub * 32, 16, 1024);
-            umma_bf16(tmem + buf * N, ad, bd, idesc, k > 0 ? 1u : 0u);
-          }
-          umma_commit(&sh.k_empty[s]);
-          umma_commit(&sh.t_full[buf]);
-        }
-        if (ok) umma_commit(&sh.q_empty);
-      }
-      // every MMA issued has completed before TMEM is released
-      umma_commit(&sh.mma_done);
-      mbar_drain(&sh.mma_done, 0, 200000000ull);
-    }
-  } else if (warp < 2 + NE) {
+  if (warp >= 4) {
+    if constexpr (C::REG_SPLIT) setmaxnreg_inc<C::REG_HIGH>();
     // ------------------------------------------------------------------ head-sum warps
     constexpr int GH = C::GH;
-    const int hw = warp - 2;
+    const int hw = warp - 4;
     const int quarter = warp & 3;              // TMEM lane quarter this warp may access
     const int half = hw >> 2;                  // queries [half * GH, half * GH + GH)
     const int g0 = half * GH;
@@ -591,122 +505,73 @@ __global__ void __launch_bounds__(Cfg<HI, DI, G>::THREADS, 1)
         lmax[g] = 0u;
       }
       __syncwarp();
-      // With 8 or more heads per query the TMEM tile is read in the 16x256b shape: thread t
-      // holds keys t/4 + 8 r (r < 4) of its lane quarter and, of every group of 8 columns, the
-      // two columns 2 (t % 4) and 2 (t % 4) + 1 -- so it needs only NH / 4 head weights, which
-      // stay in registers for the whole unit.
-      constexpr bool kWide = HI >= 8;
-      constexpr int NG = NH / 8;                 // column groups of this warp
-      float2 wr[kWide ? NG : 1];
-      if constexpr (kWide) {
+      // every head weight of the warp's queries stays in registers for the whole unit: read from
+      // shared memory per tile, each weight would cost a broadcast load into all 32 lanes of all
+      // eight warps, 1024 cycles of load bandwidth per tile, as long as the tile's MMAs
+      float wreg[NH];
 #pragma unroll
-        for (int k = 0; k < NG; ++k) wr[k] = *reinterpret_cast<const float2*>(&w_s[8 * k + 2 * (lane & 3)]);
+      for (int c = 0; c < NH; c += 4) {
+        const float4 wv = *reinterpret_cast<const float4*>(&w_s[c]);
+        wreg[c] = wv.x;
+        wreg[c + 1] = wv.y;
+        wreg[c + 2] = wv.z;
+        wreg[c + 3] = wv.w;
       }
+      // partial sums per query: four with 16 or more heads (breaks the dependent FMA chain),
+      // two below (the half's many queries already give independent chains)
+      constexpr int NP = HI >= 16 ? 4 : 2;
       for (int i = 0; i < ui.n_tiles; ++i, ++tile) {
         const int buf = tile & 1;
         ok = warp_wait(&sh.t_full[buf], (tile >> 1) & 1, &sh.abort_flag, status, wait_ns);
         if (!ok) break;
         tc_fence_after();
+        float part[GH][NP];
+#pragma unroll
+        for (int g = 0; g < GH; ++g)
+#pragma unroll
+          for (int p = 0; p < NP; ++p) part[g][p] = 0.f;
+        const uint32_t tbase = tmem + t_lane + buf * N + half * NH;
+#pragma unroll
+        for (int c0 = 0; c0 < NH; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld32(tbase + c0, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; j += 4) {
+            const int gl = (c0 + j) / HI;   // query within the half (HI is a multiple of 4)
+            const float r0 = fmaxf(__uint_as_float(v[j]), 0.f), r1 = fmaxf(__uint_as_float(v[j + 1]), 0.f);
+            const float r2 = fmaxf(__uint_as_float(v[j + 2]), 0.f), r3 = fmaxf(__uint_as_float(v[j + 3]), 0.f);
+            fma2(part[gl][0], part[gl][1], wreg[c0 + j], wreg[c0 + j + 1], r0, r1);
+            if constexpr (NP == 4) fma2(part[gl][2], part[gl][3], wreg[c0 + j + 2], wreg[c0 + j + 3], r2, r3);
+            else fma2(part[gl][0], part[gl][1], wreg[c0 + j + 2], wreg[c0 + j + 3], r2, r3);
+          }
+        }
         float accs[GH];   // this lane's key (row of the quarter): its score for every query of the half
-        if constexpr (kWide) {
-          constexpr int GPQ = HI / 8;              // column groups per query
-          float part[4][GH][2];
 #pragma unroll
-          for (int r = 0; r < 4; ++r)
-#pragma unroll
-            for (int g = 0; g < GH; ++g) part[r][g][0] = part[r][g][1] = 0.f;
-#pragma unroll
-          for (int c0 = 0; c0 < NH; c0 += 32) {
-            uint32_t v[2][16];
-#pragma unroll
-            for (int h16 = 0; h16 < 2; ++h16)
-              tmem_ld_16x256b<4>(tmem + (static_cast<uint32_t>(quarter * 32 + h16 * 16) << 16) + buf * N + half * NH + c0,
-                                 v[h16]);
-            tmem_ld_wait();
-#pragma unroll
-            for (int h16 = 0; h16 < 2; ++h16)
-#pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const int kk = c0 / 8 + k;         // column group within the half
-                const int gl = kk / GPQ;           // query within the half
-#pragma unroll
-                for (int rr = 0; rr < 2; ++rr) {
-                  const float a = fmaxf(__uint_as_float(v[h16][4 * k + 2 * rr]), 0.f);
-                  const float b = fmaxf(__uint_as_float(v[h16][4 * k + 2 * rr + 1]), 0.f);
-                  fma2(part[2 * h16 + rr][gl][0], part[2 * h16 + rr][gl][1], wr[kk].x, wr[kk].y, a, b);
-                }
-              }
-          }
-          // complete each key's sum over the four threads that share it, then move key L's score
-          // to lane L
-#pragma unroll
-          for (int g = 0; g < GH; ++g) {
-            float sr[4];
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-              float x = part[r][g][0] + part[r][g][1];
-              x += __shfl_xor_sync(0xffffffffu, x, 1);
-              x += __shfl_xor_sync(0xffffffffu, x, 2);
-              sr[r] = x;
-            }
-            const int src = 4 * (lane & 7);
-            const float x0 = __shfl_sync(0xffffffffu, sr[0], src), x1 = __shfl_sync(0xffffffffu, sr[1], src);
-            const float x2 = __shfl_sync(0xffffffffu, sr[2], src), x3 = __shfl_sync(0xffffffffu, sr[3], src);
-            const int rsel = lane >> 3;
-            accs[g] = rsel == 0 ? x0 : rsel == 1 ? x1 : rsel == 2 ? x2 : x3;
-          }
-        } else {
-          // head sum of this half's queries with NP independent partial sums per query (breaks
-          // the dependent FMA chain); TMEM read 64 columns per wait
-          constexpr int NP = HI >= 16 ? 4 : 1;
-          float part[GH][NP];
-#pragma unroll
-          for (int g = 0; g < GH; ++g)
-#pragma unroll
-            for (int p = 0; p < NP; ++p) part[g][p] = 0.f;
-#pragma unroll
-          for (int c0 = 0; c0 < NH; c0 += 64) {
-            const int cc = half * NH + c0;   // TMEM column of this chunk
-            uint32_t v[64];
-            tmem_ld32(tmem + t_lane + buf * N + cc, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-            tmem_ld32(tmem + t_lane + buf * N + cc + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-            tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 64; j += 4) {
-              const float4 wv = *reinterpret_cast<const float4*>(&w_s[c0 + j]);
-              const float r0 = fmaxf(__uint_as_float(v[j]), 0.f), r1 = fmaxf(__uint_as_float(v[j + 1]), 0.f);
-              const float r2 = fmaxf(__uint_as_float(v[j + 2]), 0.f), r3 = fmaxf(__uint_as_float(v[j + 3]), 0.f);
-              const int gl = (c0 + j) / HI;   // query within the half
-              if constexpr (NP == 4) {
-                fma2(part[gl][0], part[gl][1], wv.x, wv.y, r0, r1);
-                fma2(part[gl][2], part[gl][3], wv.z, wv.w, r2, r3);
-              } else {
-                const float wj[4] = {wv.x, wv.y, wv.z, wv.w}, rj[4] = {r0, r1, r2, r3};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  float& acc_e = part[(c0 + j + e) / HI][0];
-                  acc_e = fmaf(wj[e], rj[e], acc_e);
-                }
-              }
-            }
-          }
-#pragma unroll
-          for (int g = 0; g < GH; ++g) {
-            if constexpr (NP == 4) accs[g] = (part[g][0] + part[g][1]) + (part[g][2] + part[g][3]);
-            else accs[g] = part[g][0];
-          }
+        for (int g = 0; g < GH; ++g) {
+          if constexpr (NP == 4) accs[g] = (part[g][0] + part[g][1]) + (part[g][2] + part[g][3]);
+          else accs[g] = part[g][0] + part[g][1];
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh.t_empty[buf]);
         const int j = ui.kbeg + i * kKeyTile + row;
+        // every query's keep mask first (independent work), then the stores where one is set
+        uint32_t keys[GH], masks[GH], any = 0u;
 #pragma unroll
         for (int g = 0; g < GH; ++g) {
-          const uint32_t key = float_key(accs[g]);
+          keys[g] = float_key(accs[g]);
           const uint32_t tk = qf[g] ? *reinterpret_cast<volatile uint32_t*>(&sh.tau[par][g0 + g]) : 0u;
-          const bool keep = j >= qa[g] && j < qb[g] && key >= tk;
-          const uint32_t m = __ballot_sync(0xffffffffu, keep);
+          masks[g] = __ballot_sync(0xffffffffu, j >= qa[g] && j < qb[g] && keys[g] >= tk);
+          any |= masks[g];
+        }
+        if (any == 0u) continue;
+#pragma unroll
+        for (int g = 0; g < GH; ++g) {
+          const uint32_t m = masks[g];
           if (m == 0u) continue;
+          const uint32_t key = keys[g];
+          const bool keep = (m >> lane) & 1u;
           const size_t off = ((static_cast<size_t>(t0 + g) * A.n_chunks + ui.chunk) * kSub + quarter) * cap4;
           if (keep) {
             const int p = cnt[g] + __popc(m & below);
@@ -752,80 +617,184 @@ __global__ void __launch_bounds__(Cfg<HI, DI, G>::THREADS, 1)
       ++unit_ord;
     }
   } else {
-    // ------------------------------------------------------------------ threshold warp
-    uint32_t unit_ord = 0;
-    bool ok = true;
-    for (int k = 0; k * static_cast<int>(gridDim.x) < n_units && ok; ++k) {
-      const int u = snake_unit(k);
-      if (u >= n_units) continue;
-      const UnitInfo ui = unit_info(u, A.n_groups, A.chunk_len, A.group_range);
-      if (ui.n_tiles == 0) {
-        // an empty chunk still tells the final select that it holds no candidates
-        for (int e = lane; e < G * kSub; e += 32) {
-          const int t = ui.group * G + e / kSub;
-          if (t < A.n_q) A.cand_cnt[(static_cast<size_t>(t) * A.n_chunks + ui.chunk) * kSub + (e % kSub)] = 0u;
-        }
-        for (int g = lane; g < G; g += 32) {
-          const int t = ui.group * G + g;
-          if (t < A.n_q) A.cand_edge[static_cast<size_t>(t) * A.n_chunks + ui.chunk] = 0u;
-        }
-        continue;
-      }
-      const int par = unit_ord & 1;
-      // per filtered query (lane g holds query g's state)
-      bool filt = false;
-      if (lane < G) filt = query_range(A.row_range, ui.group * G + lane, A.n_q, ui, A.trivial_len, A.direct_max).filtered;
-      const uint32_t fmask = __ballot_sync(0xffffffffu, filt);
-      int bstar = 0, above = 0;   // lane g: query g's boundary bin and entries at or above it
-      const uint64_t t0 = globaltimer_ns();
-      while (true) {
-        const bool done = mbar_try_wait(&sh.u_done[par], (unit_ord >> 1) & 1);
-        // raise the threshold of every filtered query (the whole warp sums one histogram)
-        for (uint32_t fm = fmask; fm; fm &= fm - 1) {
-          const int g = __ffs(fm) - 1;
-          const int b0 = __shfl_sync(0xffffffffu, bstar, g);
-          int ab = 0;
-          const int b = climb<NB>(sh.hist[par][g], b0, A.topk, &ab);
-          if (lane == g) {
-            bstar = b;
-            above = ab;
+    // warpgroup 0
+    if constexpr (C::REG_SPLIT) setmaxnreg_dec<C::REG_LOW>();
+    if (warp == 0) {
+      // ------------------------------------------------------------------ TMA producer
+      if (lane == 0) {
+        tma_prefetch_desc(&tmap_q);
+        tma_prefetch_desc(&tmap_k);
+        tma_prefetch_desc(&tmap_q_in);
+        tma_prefetch_desc(&tmap_k_in);
+        uint32_t kstage = 0, q_uses = 0;
+        bool ok = true;
+        for (int k = 0; k * static_cast<int>(gridDim.x) < n_units && ok; ++k) {
+          const int u = snake_unit(k);
+          if (u >= n_units) continue;
+          const UnitInfo ui = unit_info(u, A.n_groups, A.chunk_len, A.group_range);
+          if (ui.n_tiles == 0) continue;
+          if (q_uses > 0) ok = mbar_wait_for(&sh.q_empty, (q_uses - 1) & 1, &sh.abort_flag, status, wait_ns);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&sh.q_full, C::Q_BYTES);
+          // 64-dim blocks without rotary dims come from the unrotated input
+          for (int b = 0; b < KB; ++b)
+            tma_load_2d(sQ + b * N * 128, b < q_split ? &tmap_q_in : &tmap_q, &sh.q_full, b * 64, ui.group * N);
+          ++q_uses;
+          for (int i = 0; i < ui.n_tiles; ++i, ++kstage) {
+            if (A.stop_after >= 0 && kstage >= static_cast<uint32_t>(A.stop_after)) {
+              ok = false;   // test hook: stop feeding the pipeline; its waits then run out
+              break;
+            }
+            const int s = kstage % STAGES;
+            if (kstage >= STAGES) {
+              ok = mbar_wait_for(&sh.k_empty[s], ((kstage / STAGES) - 1) & 1, &sh.abort_flag, status, wait_ns);
+              if (!ok) break;
+            }
+            mbar_arrive_expect_tx(&sh.k_full[s], C::K_STAGE_BYTES);
+            uint8_t* dst = sK + s * C::K_STAGE_BYTES;
+            // cache row of the tile's first key: contiguous, or its page (one 128-key tile per
+            // page; a group is one row in paged mode).  A page outside the cache is flagged and
+            // row 0 read instead (the tile's scores are then meaningless, the status says so).
+            int krow = ui.kbeg + i * kKeyTile;
+            if (pg.block_table) {
+              const int lp = krow >> kPageShift;
+              const int page = lp < pg.max_pages ? __ldg(pg.block_table + static_cast<size_t>(ui.group) * pg.max_pages + lp) : -1;
+              if (page < 0 || page >= pg.n_pages) {
+                atomicOr(status, DEV_ERR_BAD_INDEX);
+                krow = 0;
+              } else {
+                krow = page << kPageShift;
+              }
+            }
+            for (int b = 0; b < KB; ++b)
+              tma_load_2d(dst + b * kKeyTile * 128, b < k_split ? &tmap_k_in : &tmap_k, &sh.k_full[s], b * 64, krow);
           }
-          if (b != b0 && lane == 0)
-            *reinterpret_cast<volatile uint32_t*>(&sh.tau[par][g]) = b > 0 ? bin_edge_key<C>(b) : 0u;
         }
-        if (__all_sync(0xffffffffu, done)) break;
-        if (sh.abort_flag) {
-          ok = false;
-          break;
-        }
-        // the head-sum warps' own bounded waits end a stalled unit (abort flag above); this
-        // bound is only a safety net
-        if (globaltimer_ns() - t0 > 100ull * wait_ns) {
-          if (lane == 0) {
-            sh.abort_flag = 1u;
-            atomicOr(status, DEV_ERR_TIMEOUT);
+        // let copies still in flight land before the CTA can exit (bounded; normally all done)
+        if (q_uses > 0) mbar_drain(&sh.q_full, (q_uses - 1) & 1, 200000000ull);
+        for (uint32_t j = kstage > STAGES ? kstage - STAGES : 0; j < kstage; ++j)
+          mbar_drain(&sh.k_full[j % STAGES], (j / STAGES) & 1, 200000000ull);
+      }
+    } else if (warp == 1) {
+      // ------------------------------------------------------------------ MMA issuer
+      // The whole warp runs the loop (descriptors stay warp-uniform, built once per tile as a
+      // base plus compile-time offsets) and one elected lane issues each instruction: issuing
+      // from a single thread with descriptors rebuilt per MMA cost about 110 cycles per MMA,
+      // enough to leave the tensor pipe idle a third of the time.
+      constexpr uint32_t idesc = idesc_bf16_f32(128, N, 0, 0);
+      const uint64_t qd0 = sdesc_sw128(smem_u32(sQ), 16, 1024);
+      auto wait = [&](uint64_t* bar, uint32_t parity) {
+        return __all_sync(0xffffffffu, mbar_wait_for(bar, parity, &sh.abort_flag, status, wait_ns));
+      };
+      uint32_t kstage = 0, q_uses = 0, tile = 0;
+      bool ok = true;
+      for (int k = 0; k * static_cast<int>(gridDim.x) < n_units && ok; ++k) {
+        const int u = snake_unit(k);
+        if (u >= n_units) continue;
+        const UnitInfo ui = unit_info(u, A.n_groups, A.chunk_len, A.group_range);
+        if (ui.n_tiles == 0) continue;
+        ok = wait(&sh.q_full, q_uses & 1);
+        if (!ok) break;
+        ++q_uses;
+        for (int i = 0; i < ui.n_tiles; ++i, ++kstage, ++tile) {
+          const int s = kstage % STAGES;
+          const int buf = tile & 1;
+          ok = wait(&sh.k_full[s], (kstage / STAGES) & 1);
+          if (ok && tile >= 2) ok = wait(&sh.t_empty[buf], ((tile >> 1) - 1) & 1);
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t kd0 = sdesc_sw128(smem_u32(sK + s * C::K_STAGE_BYTES), 16, 1024);
+  #pragma unroll
+          for (int k = 0; k < DI / 16; ++k) {
+            const int kb = k >> 2, sub = k & 3;
+            umma_bf16_elect(tmem + buf * N, kd0 + static_cast<uint64_t>((kb * kKeyTile * 128 + sub * 32) >> 4),
+                            qd0 + static_cast<uint64_t>((kb * N * 128 + sub * 32) >> 4), idesc, k > 0 ? 1u : 0u);
           }
-          ok = false;
-          break;
+          umma_commit_elect(&sh.k_empty[s]);
+          umma_commit_elect(&sh.t_full[buf]);
         }
-        __nanosleep(fmask ? 256 : 2048);
+        if (ok) umma_commit_elect(&sh.q_empty);
       }
-      if (!ok) break;
-      // the unit is done: each row's edge in this chunk (the lower edge of its boundary bin
-      // when at least k entries lie at or above it: nothing below can make the row's top-k)
-      if (lane < G) {
-        const int t = ui.group * G + lane;
-        if (t < A.n_q)
-          A.cand_edge[static_cast<size_t>(t) * A.n_chunks + ui.chunk] =
-              filt && bstar > 0 && above >= A.topk ? bin_edge_key<C>(bstar) : 0u;
-      }
-      // reset this parity for the unit after next, then let its head-sum warps start
-      for (int i = lane; i < G * NB; i += 32) (&sh.hist[par][0][0])[i] = 0u;
-      if (lane < G) sh.tau[par][lane] = 0u;
+      // every MMA issued has completed before TMEM is released
+      umma_commit_elect(&sh.mma_done);
+      mbar_drain(&sh.mma_done, 0, 200000000ull);
       __syncwarp();
-      __threadfence_block();
-      if (lane == 0) mbar_arrive(&sh.u_ready[par]);
-      ++unit_ord;
+    } else if (warp == 2) {
+      // ------------------------------------------------------------------ threshold warp
+      uint32_t unit_ord = 0;
+      bool ok = true;
+      for (int k = 0; k * static_cast<int>(gridDim.x) < n_units && ok; ++k) {
+        const int u = snake_unit(k);
+        if (u >= n_units) continue;
+        const UnitInfo ui = unit_info(u, A.n_groups, A.chunk_len, A.group_range);
+        if (ui.n_tiles == 0) {
+          // an empty chunk still tells the final select that it holds no candidates
+          for (int e = lane; e < G * kSub; e += 32) {
+            const int t = ui.group * G + e / kSub;
+            if (t < A.n_q) A.cand_cnt[(static_cast<size_t>(t) * A.n_chunks + ui.chunk) * kSub + (e % kSub)] = 0u;
+          }
+          for (int g = lane; g < G; g += 32) {
+            const int t = ui.group * G + g;
+            if (t < A.n_q) A.cand_edge[static_cast<size_t>(t) * A.n_chunks + ui.chunk] = 0u;
+          }
+          continue;
+        }
+        const int par = unit_ord & 1;
+        // per filtered query (lane g holds query g's state)
+        bool filt = false;
+        if (lane < G) filt = query_range(A.row_range, ui.group * G + lane, A.n_q, ui, A.trivial_len, A.direct_max).filtered;
+        const uint32_t fmask = __ballot_sync(0xffffffffu, filt);
+        int bstar = 0, above = 0;   // lane g: query g's boundary bin and entries at or above it
+        const uint64_t t0 = globaltimer_ns();
+        while (true) {
+          const bool done = mbar_try_wait(&sh.u_done[par], (unit_ord >> 1) & 1);
+          // raise the threshold of every filtered query (the whole warp sums one histogram)
+          for (uint32_t fm = fmask; fm; fm &= fm - 1) {
+            const int g = __ffs(fm) - 1;
+            const int b0 = __shfl_sync(0xffffffffu, bstar, g);
+            int ab = 0;
+            const int b = climb<NB>(sh.hist[par][g], b0, A.topk, &ab);
+            if (lane == g) {
+              bstar = b;
+              above = ab;
+            }
+            if (b != b0 && lane == 0)
+              *reinterpret_cast<volatile uint32_t*>(&sh.tau[par][g]) = b > 0 ? bin_edge_key<C>(b) : 0u;
+          }
+          if (__all_sync(0xffffffffu, done)) break;
+          if (sh.abort_flag) {
+            ok = false;
+            break;
+          }
+          // the head-sum warps' own bounded waits end a stalled unit (abort flag above); this
+          // bound is only a safety net
+          if (globaltimer_ns() - t0 > 100ull * wait_ns) {
+            if (lane == 0) {
+              sh.abort_flag = 1u;
+              atomicOr(status, DEV_ERR_TIMEOUT);
+            }
+            ok = false;
+            break;
+          }
+          __nanosleep(fmask ? 256 : 2048);
+        }
+        if (!ok) break;
+        // the unit is done: each row's edge in this chunk (the lower edge of its boundary bin
+        // when at least k entries lie at or above it: nothing below can make the row's top-k)
+        if (lane < G) {
+          const int t = ui.group * G + lane;
+          if (t < A.n_q)
+            A.cand_edge[static_cast<size_t>(t) * A.n_chunks + ui.chunk] =
+                filt && bstar > 0 && above >= A.topk ? bin_edge_key<C>(bstar) : 0u;
+        }
+        // reset this parity for the unit after next, then let its head-sum warps start
+        for (int i = lane; i < G * NB; i += 32) (&sh.hist[par][0][0])[i] = 0u;
+        if (lane < G) sh.tau[par][lane] = 0u;
+        __syncwarp();
+        __threadfence_block();
+        if (lane == 0) mbar_arrive(&sh.u_ready[par]);
+        ++unit_ord;
+      }
     }
   }
 
@@ -847,6 +816,14 @@ cudaError_t launch_t(const IndexerPlan& p, const CUtensorMap& tq, const CUtensor
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::DYN_SMEM);
     if (e != cudaSuccess) return e;
+    if constexpr (C::REG_SPLIT) {
+      // the head-sum warpgroups' setmaxnreg.inc waits for registers the block must hold from
+      // launch: refuse to launch a build whose register count would leave it waiting
+      cudaFuncAttributes fa{};
+      e = cudaFuncGetAttributes(&fa, kern);
+      if (e != cudaSuccess) return e;
+      if (fa.numRegs < C::REG_LAUNCH) return cudaErrorInvalidConfiguration;
+    }
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   kern<<<p.grid, C::THREADS, C::DYN_SMEM, st>>>(tq, tk, tqi, tki, q_split, k_split, pg, A);

@@ -214,6 +214,19 @@ __device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, f
       : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
+// Per-warpgroup register reallocation (all four warps of a warpgroup execute the same one): dec
+// returns registers to the block's pool, inc waits until the pool can grant the new count.
+template <int R>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  static_assert(R >= 24 && R <= 256 && R % 8 == 0, "setmaxnreg count");
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(R));
+}
+template <int R>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  static_assert(R >= 24 && R <= 256 && R % 8 == 0, "setmaxnreg count");
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(R));
+}
+
 // Warp-wide TMEM load: thread i gets lane (lane_base + i), 32 consecutive 32-bit columns.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
