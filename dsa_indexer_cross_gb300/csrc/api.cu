@@ -231,11 +231,13 @@ IndexerLayout indexer_layout(const dsa_indexer_desc* d, int sms) {
   p.chunk = static_cast<int>(chunk);
   p.n_chunks = static_cast<int>((span + chunk - 1) / chunk);
   // candidates per (row, chunk), in kSub sub-buffers: every key of the chunk when a row's part
-  // of it has at most kDirectMax keys, else 16K (the streaming threshold keeps about
-  // k (1 + ln(chunk / k)) of them; more only for scores that keep rising along the keys, which
-  // the kernel handles by cutting a sub-buffer back to its top-k)
+  // of it has at most kDirectMax keys, else 16K, or 32K for chunks over 64K keys.  The streaming
+  // threshold keeps about k (1 + ln(chunk / k)) keys with an exact threshold (12K of a 256K
+  // chunk at k = 2048) and some 40 % more with its 1/16-octave histogram bins; a sub-buffer that
+  // fills anyway (scores that keep rising along the keys) is cut back to its top-k by its warp,
+  // a pass that holds up the whole CTA, so the buffers are sized to make that rare.
   const long long span_keys = std::min<long long>(chunk, span);
-  p.cap = span_keys > kDirectMax ? 16384 : static_cast<int>((span_keys + 127) / 128 * 128);
+  p.cap = span_keys > kDirectMax ? (span_keys > 65536 ? 32768 : 16384) : static_cast<int>((span_keys + 127) / 128 * 128);
   const long long units = static_cast<long long>(p.n_groups) * p.n_chunks;
   p.grid = static_cast<int>(units < sms ? units : sms);
   if (p.grid < 1) p.grid = 1;

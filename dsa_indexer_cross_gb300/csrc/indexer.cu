@@ -52,10 +52,20 @@ constexpr int kKeyTile = 128;
 constexpr int kBins = 256;        // value-linear bins of a warp's cut-back
 constexpr int kBoundary = 64;     // boundary-bin entries ranked directly by a warp
 constexpr int kLoadsInFlight = 16;
-constexpr int kLog2Span = 5;      // the threshold histogram covers 2^kLog2Span octaves of scores ...
-constexpr int kLowExp = 127 - 16; // ... starting at 2^-16 (lower scores share the bottom bin)
+constexpr int kLog2Span = 5;      // each sign's half of the threshold histogram covers 2^kLog2Span
+constexpr int kLowExp = 127 - 16; // octaves of |score| from 2^-16 (smaller magnitudes share a bin)
 
 constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
+
+// Per head-sum warp scratch of a cut-back: histogram bins, then the boundary bin's entries.  (In
+// global memory instead, the call into the cut-back made the compiler keep the head-sum state
+// in local memory and halved the kernel's speed.)
+struct WarpScratch {
+  uint32_t hist[kBins];
+  uint32_t bkey[kBoundary];
+  int32_t bidx[kBoundary];
+  int bc[4];
+};
 
 template <int HI, int DI, int G>
 struct Cfg {
@@ -77,13 +87,19 @@ struct Cfg {
   static constexpr bool REG_SPLIT = NE == 8;
   static constexpr int REG_LAUNCH = 168, REG_LOW = 56, REG_HIGH = 224;
   static_assert(!REG_SPLIT || 128 * REG_LOW + 256 * REG_HIGH <= THREADS * REG_LAUNCH, "register split");
-  // threshold histograms: NB bins per query per unit parity (16 KB in all), log-spaced over
-  // 2^kLog2Span octaves
-  static constexpr int NB = 2048 / G < 512 ? 2048 / G : 512;
-  static constexpr int SHIFT = 23 + kLog2Span - ilog2(NB);   // key bits below the bin index
-  static constexpr uint32_t BASE = (0x80000000u | (static_cast<uint32_t>(kLowExp) << 23)) >> SHIFT;
+  // threshold histograms: NB bins per query per unit parity (32 KB in all for G >= 4); bins
+  // [0, NBH) hold negative scores and [NBH, NB) positive ones, each half log-spaced over
+  // 2^kLog2Span octaves of |score| (a row whose k-th largest score is negative -- head weights
+  // of mostly one sign -- still gets a rising threshold)
+  static constexpr int NB = 4096 / G < 1024 ? 4096 / G : 1024;
+  static constexpr int NBH = NB / 2;
+  static constexpr int SHIFT = 23 + kLog2Span - ilog2(NBH);  // key bits below the bin index
+  // key >> SHIFT of +2^-16 and of -2^(2^kLog2Span - 16): the lowest bin of each half
+  static constexpr uint32_t BASE_POS = (0x80000000u | (static_cast<uint32_t>(kLowExp) << 23)) >> SHIFT;
+  static constexpr uint32_t BASE_NEG =
+      (~(0x80000000u | (static_cast<uint32_t>(kLowExp + (1 << kLog2Span)) << 23))) >> SHIFT;
   static constexpr int SMEM_MAX = 232448;                // dynamic + static per CTA
-  static constexpr int STATIC_EST = 1024 + NE * NH * 4 + 2 * G * NB * 4 + NE * 1600 + 4 * G * 4;
+  static constexpr int STATIC_EST = 1024 + 2 * G * NB * 4 + 4 * G * 4 + NE * static_cast<int>(sizeof(WarpScratch));
   static constexpr int AVAIL = SMEM_MAX - STATIC_EST - 1024 - Q_BYTES;
   static constexpr int STAGES_FIT = AVAIL / K_STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT > 6 ? 6 : STAGES_FIT;
@@ -94,31 +110,30 @@ struct Cfg {
   static_assert(GH * HI == NH, "a half holds whole queries");
   static_assert(G <= 16, "the threshold warp keeps one query per lane, at most 16");
   static_assert(STAGES >= 2, "shared memory");
-  static_assert(SHIFT + ilog2(NB) == 23 + kLog2Span, "NB bins span 2^kLog2Span octaves");
+  static_assert(SHIFT + ilog2(NBH) == 23 + kLog2Span, "NB / 2 bins span 2^kLog2Span octaves");
+  static_assert(kLowExp + (1 << kLog2Span) < 255, "histogram range within the float exponents");
 };
 
-// Threshold-histogram bin of a score key under Cfg C's map (monotone non-decreasing; scores
-// below 2^-16, negative ones included, share bin 0; scores above the span share the top bin)
-// and the smallest key of a bin.
+// Threshold-histogram bin of a score key under Cfg C's map (monotone non-decreasing in the key):
+// negative scores below -2^(2^kLog2Span - 16) share bin 0, negative magnitudes under 2^-16 share
+// bin NBH - 1, positive scores under 2^-16 (and +0) share bin NBH, scores above the span the
+// top bin.  bin_edge_key(b) is the smallest key of bin b.
 template <class C>
 __device__ __forceinline__ int hist_bin(uint32_t key) {
-  const int b = static_cast<int>(key >> C::SHIFT) - static_cast<int>(C::BASE);
-  return b < 0 ? 0 : (b >= C::NB ? C::NB - 1 : b);
+  const int hi = static_cast<int>(key >> C::SHIFT);
+  int b = (key & 0x80000000u) ? hi - static_cast<int>(C::BASE_POS) : hi - static_cast<int>(C::BASE_NEG);
+  b = b < 0 ? 0 : (b >= C::NBH ? C::NBH - 1 : b);
+  return (key & 0x80000000u) ? C::NBH + b : b;
 }
 template <class C>
 __device__ __forceinline__ uint32_t bin_edge_key(int b) {
-  return static_cast<uint32_t>(b + static_cast<int>(C::BASE)) << C::SHIFT;
+  if (b >= C::NBH + 1) return static_cast<uint32_t>(b - C::NBH + static_cast<int>(C::BASE_POS)) << C::SHIFT;
+  if (b == C::NBH) return 0x80000000u;
+  return b > 0 ? static_cast<uint32_t>(b + static_cast<int>(C::BASE_NEG)) << C::SHIFT : 0u;
 }
 
-// Per top-k warp scratch of a cut-back: histogram bins, then the boundary bin's entries.
-struct WarpScratch {
-  uint32_t hist[kBins];
-  uint32_t bkey[kBoundary];
-  int32_t bidx[kBoundary];
-  int bc[4];
-};
 
-template <int G, int NE, int NH, int NB>
+template <int G, int NB, int NE>
 struct Shared {
   uint64_t k_full[6], k_empty[6];
   uint64_t q_full, q_empty;
@@ -128,7 +143,6 @@ struct Shared {
   uint32_t tmem_base;
   uint32_t abort_flag;
   uint32_t tau[2][G];              // per unit parity and query: threshold key (0: keep every key)
-  alignas(16) float w_s[NE][NH];   // head weights of the unit, one private copy per head-sum warp
   uint32_t hist[2][G][NB];         // threshold histograms of the filtered queries
   WarpScratch ws[NE];              // cut-back scratch of each head-sum warp
 };
@@ -358,8 +372,16 @@ __device__ __forceinline__ int warp_compact(uint32_t* keys, int32_t* idxs, int n
 // Cut a candidate buffer back to exactly its top-K (ties to the lower index), keeping the
 // survivors in key order; returns the count and updates [kmin, kmax] to the kept keys.  Kept
 // out of line: it runs only when scores keep rising along the keys.
-__device__ __noinline__ int warp_cut_to_topk(uint32_t* keys, int32_t* idxs, int n, int K, uint32_t& kmin,
-                                             uint32_t& kmax, WarpScratch& ws) {
+__device__ __noinline__ int warp_cut_to_topk(uint32_t* keys, int32_t* idxs, int n, int K, WarpScratch& ws) {
+  // extremes of the buffer's keys
+  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+  for (int e = static_cast<int>(threadIdx.x & 31u); e < n; e += 32) {
+    const uint32_t kk = keys[e];
+    kmin = min(kmin, kk);
+    kmax = max(kmax, kk);
+  }
+  kmin = __reduce_min_sync(0xffffffffu, kmin);
+  kmax = __reduce_max_sync(0xffffffffu, kmax);
   uint32_t v = 0, cut = 0;
   warp_exact_threshold(keys, idxs, n, K, kmin, kmax, ws, ws.bc, v, cut);
   return warp_compact(keys, idxs, n, [&](uint32_t key, int32_t idx) { return topk_keep(key, idx, v, cut); }, kmin,
@@ -411,7 +433,7 @@ __global__ void __launch_bounds__(Cfg<HI, DI, G>::THREADS, 1)
   using C = Cfg<HI, DI, G>;
   constexpr int N = C::N, KB = C::KB, STAGES = C::STAGES, NE = C::NE, NH = C::NH, NB = C::NB;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ Shared<G, NE, NH, NB> sh;
+  __shared__ Shared<G, NB, NE> sh;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
   uint8_t* sK = smem + C::Q_BYTES;
@@ -472,8 +494,6 @@ __global__ void __launch_bounds__(Cfg<HI, DI, G>::THREADS, 1)
     const int row = quarter * 32 + lane;       // key within the tile
     const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t below = (1u << lane) - 1u;
-    float* w_s = sh.w_s[hw];
-    WarpScratch& ws = sh.ws[hw];
     uint32_t tile = 0, unit_ord = 0;
     bool ok = true;
     for (int k = 0; k * static_cast<int>(gridDim.x) < n_units && ok; ++k) {
@@ -485,14 +505,16 @@ __global__ void __launch_bounds__(Cfg<HI, DI, G>::THREADS, 1)
       // this unit's histograms and thresholds have been reset
       ok = warp_wait(&sh.u_ready[par], (unit_ord >> 1) & 1, &sh.abort_flag, status, wait_ns);
       if (!ok) break;
-      // this warp's private copy of the head weights of its queries, and their key ranges
+      // the head weights of this warp's queries (lane l loads weights l, l + 32, ...) and their
+      // key ranges
       const int t0 = ui.group * G + g0;
-      for (int i = lane; i < NH; i += 32) {
-        const int t = t0 + i / HI;
-        w_s[i] = t < A.n_q ? __ldg(A.w + static_cast<size_t>(t) * HI + (i % HI)) : 0.f;
+      float wl[NH / 32];
+#pragma unroll
+      for (int c = 0; c < NH / 32; ++c) {
+        const int i = c * 32 + lane;
+        wl[c] = t0 + i / HI < A.n_q ? __ldg(A.w + static_cast<size_t>(t0) * HI + i) : 0.f;
       }
       int qa[GH], qb[GH], cnt[GH];
-      uint32_t lmin[GH], lmax[GH];   // per lane: extremes of the keys it kept
       bool qf[GH];
 #pragma unroll
       for (int g = 0; g < GH; ++g) {
@@ -501,36 +523,38 @@ __global__ void __launch_bounds__(Cfg<HI, DI, G>::THREADS, 1)
         qb[g] = r.b;
         qf[g] = r.filtered;
         cnt[g] = 0;
-        lmin[g] = 0xFFFFFFFFu;
-        lmax[g] = 0u;
       }
-      __syncwarp();
-      // every head weight of the warp's queries stays in registers for the whole unit: read from
-      // shared memory per tile, each weight would cost a broadcast load into all 32 lanes of all
-      // eight warps, 1024 cycles of load bandwidth per tile, as long as the tile's MMAs
+      // every head weight of the warp's queries stays in registers, in every lane, for the whole
+      // unit: read from shared memory per tile, each weight would cost a broadcast load into all
+      // 32 lanes of all eight warps, 1024 cycles of load bandwidth per tile, as long as the
+      // tile's MMAs
       float wreg[NH];
 #pragma unroll
-      for (int c = 0; c < NH; c += 4) {
-        const float4 wv = *reinterpret_cast<const float4*>(&w_s[c]);
-        wreg[c] = wv.x;
-        wreg[c + 1] = wv.y;
-        wreg[c + 2] = wv.z;
-        wreg[c + 3] = wv.w;
-      }
-      // partial sums per query: four with 16 or more heads (breaks the dependent FMA chain),
-      // two below (the half's many queries already give independent chains)
+      for (int c = 0; c < NH; ++c) wreg[c] = __shfl_sync(0xffffffffu, wl[c / 32], c % 32);
+      // this warp's sub-buffer of each query in this chunk
+      size_t sub_off[GH];
+#pragma unroll
+      for (int g = 0; g < GH; ++g)
+        sub_off[g] = ((static_cast<size_t>(t0 + g) * A.n_chunks + ui.chunk) * kSub + quarter) * cap4;
+      // partial sums per query (NP / 2 packed pairs): four with 16 or more heads, two below (the
+      // half's many queries already give independent chains)
       constexpr int NP = HI >= 16 ? 4 : 2;
+      constexpr int NPP = NP / 2;
       for (int i = 0; i < ui.n_tiles; ++i, ++tile) {
         const int buf = tile & 1;
         ok = warp_wait(&sh.t_full[buf], (tile >> 1) & 1, &sh.abort_flag, status, wait_ns);
         if (!ok) break;
         tc_fence_after();
+        const uint32_t tbase = tmem + t_lane + buf * N + half * NH;
+        // thresholds read now (a stale one is lower, which only keeps more), used after the sum
+        uint32_t tk[GH];
+#pragma unroll
+        for (int g = 0; g < GH; ++g) tk[g] = qf[g] ? *reinterpret_cast<volatile uint32_t*>(&sh.tau[par][g0 + g]) : 0u;
         float part[GH][NP];
 #pragma unroll
         for (int g = 0; g < GH; ++g)
 #pragma unroll
           for (int p = 0; p < NP; ++p) part[g][p] = 0.f;
-        const uint32_t tbase = tmem + t_lane + buf * N + half * NH;
 #pragma unroll
         for (int c0 = 0; c0 < NH; c0 += 32) {
           uint32_t v[32];
@@ -538,19 +562,26 @@ __global__ void __launch_bounds__(Cfg<HI, DI, G>::THREADS, 1)
           tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < 32; j += 4) {
-            const int gl = (c0 + j) / HI;   // query within the half (HI is a multiple of 4)
+            const int c = c0 + j;
+            const int gl = c / HI;   // query within the half (HI is a multiple of 4)
+            const int pa = (2 * (c / 4)) % NPP, pb = (2 * (c / 4) + 1) % NPP;
             const float r0 = fmaxf(__uint_as_float(v[j]), 0.f), r1 = fmaxf(__uint_as_float(v[j + 1]), 0.f);
             const float r2 = fmaxf(__uint_as_float(v[j + 2]), 0.f), r3 = fmaxf(__uint_as_float(v[j + 3]), 0.f);
-            fma2(part[gl][0], part[gl][1], wreg[c0 + j], wreg[c0 + j + 1], r0, r1);
-            if constexpr (NP == 4) fma2(part[gl][2], part[gl][3], wreg[c0 + j + 2], wreg[c0 + j + 3], r2, r3);
-            else fma2(part[gl][0], part[gl][1], wreg[c0 + j + 2], wreg[c0 + j + 3], r2, r3);
+            fma2(part[gl][2 * pa], part[gl][2 * pa + 1], wreg[c], wreg[c + 1], r0, r1);
+            fma2(part[gl][2 * pb], part[gl][2 * pb + 1], wreg[c + 2], wreg[c + 3], r2, r3);
           }
         }
         float accs[GH];   // this lane's key (row of the quarter): its score for every query of the half
 #pragma unroll
         for (int g = 0; g < GH; ++g) {
-          if constexpr (NP == 4) accs[g] = (part[g][0] + part[g][1]) + (part[g][2] + part[g][3]);
-          else accs[g] = part[g][0] + part[g][1];
+          float sp[NP];
+#pragma unroll
+          for (int p = 0; p < NP; ++p) sp[p] = part[g][p];
+#pragma unroll
+          for (int w2 = NP / 2; w2 >= 1; w2 /= 2)
+#pragma unroll
+            for (int p = 0; p < w2; ++p) sp[p] += sp[p + w2];
+          accs[g] = sp[0];
         }
         tc_fence_before();
         __syncwarp();
@@ -561,8 +592,7 @@ __global__ void __launch_bounds__(Cfg<HI, DI, G>::THREADS, 1)
 #pragma unroll
         for (int g = 0; g < GH; ++g) {
           keys[g] = float_key(accs[g]);
-          const uint32_t tk = qf[g] ? *reinterpret_cast<volatile uint32_t*>(&sh.tau[par][g0 + g]) : 0u;
-          masks[g] = __ballot_sync(0xffffffffu, j >= qa[g] && j < qb[g] && keys[g] >= tk);
+          masks[g] = __ballot_sync(0xffffffffu, j >= qa[g] && j < qb[g] && keys[g] >= tk[g]);
           any |= masks[g];
         }
         if (any == 0u) continue;
@@ -570,21 +600,13 @@ __global__ void __launch_bounds__(Cfg<HI, DI, G>::THREADS, 1)
         for (int g = 0; g < GH; ++g) {
           const uint32_t m = masks[g];
           if (m == 0u) continue;
-          const uint32_t key = keys[g];
           const bool keep = (m >> lane) & 1u;
-          const size_t off = ((static_cast<size_t>(t0 + g) * A.n_chunks + ui.chunk) * kSub + quarter) * cap4;
-          if (keep) {
-            const int p = cnt[g] + __popc(m & below);
-            if (p < cap4) {
-              A.cand_key[off + p] = key;
-              A.cand_idx[off + p] = j;
-            }
-            if (qf[g]) {
-              atomicAdd(&sh.hist[par][g0 + g][hist_bin<C>(key)], 1u);
-              lmin[g] = min(lmin[g], key);
-              lmax[g] = max(lmax[g], key);
-            }
+          const int p = cnt[g] + __popc(m & below);
+          if (keep && p < cap4) {
+            A.cand_key[sub_off[g] + p] = keys[g];
+            A.cand_idx[sub_off[g] + p] = j;
           }
+          if (keep && qf[g]) atomicAdd(&sh.hist[par][g0 + g][hist_bin<C>(keys[g])], 1u);
           cnt[g] += __popc(m);
           if (qf[g] && cnt[g] > cap4 - 32) {
             // this sub-buffer could overflow on the next tile (scores rising along the keys):
@@ -594,10 +616,7 @@ __global__ void __launch_bounds__(Cfg<HI, DI, G>::THREADS, 1)
               cnt[g] = cap4;
             }
             __syncwarp();   // this warp's stores are visible to all its lanes
-            uint32_t kmin = __reduce_min_sync(0xffffffffu, lmin[g]), kmax = __reduce_max_sync(0xffffffffu, lmax[g]);
-            cnt[g] = warp_cut_to_topk(A.cand_key + off, A.cand_idx + off, cnt[g], A.topk, kmin, kmax, ws);
-            lmin[g] = kmin;
-            lmax[g] = kmax;
+            cnt[g] = warp_cut_to_topk(A.cand_key + sub_off[g], A.cand_idx + sub_off[g], cnt[g], A.topk, sh.ws[hw]);
           }
         }
       }
@@ -704,7 +723,7 @@ __global__ void __launch_bounds__(Cfg<HI, DI, G>::THREADS, 1)
           if (!ok) break;
           tc_fence_after();
           const uint64_t kd0 = sdesc_sw128(smem_u32(sK + s * C::K_STAGE_BYTES), 16, 1024);
-  #pragma unroll
+#pragma unroll
           for (int k = 0; k < DI / 16; ++k) {
             const int kb = k >> 2, sub = k & 3;
             umma_bf16_elect(tmem + buf * N, kd0 + static_cast<uint64_t>((kb * kKeyTile * 128 + sub * 32) >> 4),
