@@ -388,6 +388,12 @@ __device__ __noinline__ int warp_cut_to_topk(uint32_t* keys, int32_t* idxs, int 
                       kmax);
 }
 
+// Drops the entries below key tq from the buffer (in place, order kept); returns the count.
+__device__ __noinline__ int warp_drop_below(uint32_t* keys, int32_t* idxs, int n, uint32_t tq) {
+  uint32_t kmin = 0u, kmax = 0u;
+  return warp_compact(keys, idxs, n, [&](uint32_t key, int32_t) { return key >= tq; }, kmin, kmax);
+}
+
 // ------------------------------------------------------------------ the kernel
 struct IndexerArgs {
   const float* w;
@@ -621,6 +627,16 @@ __global__ void __launch_bounds__(Cfg<HI, DI, G>::THREADS, 1)
         }
       }
       if (!ok) break;
+      // A filtered query's sub-buffer still holds the keys kept while its threshold was lower:
+      // drop those below the threshold as it stands now (no higher than the chunk's final edge,
+      // so no key of the row's top-k goes), while the buffer is still in L2.  The final select
+      // then reads about k entries per chunk instead of k (1 + ln(chunk / k)).
+#pragma unroll
+      for (int g = 0; g < GH; ++g) {
+        const uint32_t tq = qf[g] ? *reinterpret_cast<volatile uint32_t*>(&sh.tau[par][g0 + g]) : 0u;
+        if (tq > 0u && cnt[g] > 0)
+          cnt[g] = warp_drop_below(A.cand_key + sub_off[g], A.cand_idx + sub_off[g], min(cnt[g], cap4), tq);
+      }
       // this warp's count of each of its queries in this chunk
       if (lane == 0) {
 #pragma unroll

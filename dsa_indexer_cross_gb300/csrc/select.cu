@@ -11,9 +11,11 @@
 // One block per row: the entries at or above the edge are gathered into shared memory (in any
 // order), the exact threshold (v, cut) is found there -- one pass of 2048 bins linear in score,
 // then the boundary bin's entries ranked directly, or radix passes when that bin is crowded --
-// and the selected entries are sorted by key index (bitonic sort of <= 2048 pairs) for the
-// ascending output.  Rows with more gathered entries than shared memory holds take the same
-// steps over the buffers in global memory.
+// and the selected entries are put in key-index order by a counting pass over index buckets
+// (at most 2048 buckets over the row; an entry's place is its bucket's start plus the number
+// of smaller indices in its bucket).  Rows with more gathered entries than shared memory holds
+// take the same steps over the buffers in global memory.  Two block shapes: 6144 staged
+// entries and 256 threads where a row's buffers cannot hold more, else 16384 and 512 threads.
 #include "kernels.h"
 #include "ptx.cuh"
 #include "topk.cuh"
@@ -21,18 +23,21 @@
 namespace dsa {
 namespace {
 
-constexpr int kSelThreads = 256;
-constexpr int kStage = 6144;        // candidates gathered into shared memory
 constexpr int kBins = 2048;         // linear bins over the gathered [min, max] key range
 constexpr int kBoundaryMax = 256;   // boundary-bin entries ranked directly; more -> radix passes
 constexpr int kSortMax = 2048;      // topk <= 2048
 constexpr int kMaxSeg = 64 * kSub;  // (chunk, sub-buffer) segments of a row
+constexpr int kSmallStage = 6144, kSmallThreads = 256;
+constexpr int kBigStage = 16384, kBigThreads = 512;
 
+template <int STAGE>
 struct SelSmem {
-  uint32_t key[kStage];
-  int32_t idx[kStage];
+  // staged entries; once the threshold is known, the region holds the bucketed selection
+  // (kSortMax pairs) and the bucket fill counters
+  uint32_t key[STAGE];
+  int32_t idx[STAGE];
   unsigned long long sel[kSortMax];   // (key index << 32) | score key of the selected entries
-  uint32_t hist[kBins];
+  uint32_t hist[kBins];               // threshold bins, then index-bucket counts / starts
   uint32_t bkey[kBoundaryMax];
   int32_t bidx[kBoundaryMax];
   int seg_start[kMaxSeg + 1];
@@ -40,8 +45,9 @@ struct SelSmem {
   uint32_t kmin, kmax, edge;
   int misc[4];
   int bc[4];
-  int wsum[kSelThreads / 32];
+  int wsum[32];
 };
+static_assert(kSmallStage * 8 >= kSortMax * 8 + kBins * 4, "bucketed selection fits the stage region");
 
 // A slot of *counter for every active lane, one shared atomic per warp.
 __device__ __forceinline__ int reserve_slot(int* counter) {
@@ -54,6 +60,31 @@ __device__ __forceinline__ int reserve_slot(int* counter) {
   return base + __popc(m & ((1u << lane) - 1u));
 }
 
+// Exclusive prefix sum of x over the NT threads of the block (returns it; *total gets the sum).
+// Every thread of the block calls it.
+template <int NT>
+__device__ __forceinline__ int block_exclusive_scan(int x, int* wsum, int* total) {
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  int y = x;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int z = __shfl_up_sync(0xffffffffu, y, off);
+    if (lane >= off) y += z;
+  }
+  __syncthreads();   // wsum free for reuse
+  if (lane == 31) wsum[w] = y;
+  __syncthreads();
+  int before = 0, all = 0;
+#pragma unroll
+  for (int i = 0; i < NT / 32; ++i) {
+    const int s = wsum[i];
+    before += i < w ? s : 0;
+    all += s;
+  }
+  *total = all;
+  return before + y - x;
+}
+
 // The (chunk, sub-buffer) segments of one row, in order.
 struct Segs {
   const uint32_t* key;
@@ -64,24 +95,24 @@ struct Segs {
 };
 
 // Calls f(key, idx) for every entry of every segment at or above `edge` (all threads, any order).
-template <class F>
-__device__ __forceinline__ void for_each_global(const Segs& S, const SelSmem& sm, uint32_t edge, F&& f) {
+template <int NT, class Sm, class F>
+__device__ __forceinline__ void for_each_global(const Segs& S, const Sm& sm, uint32_t edge, F&& f) {
   for (int s = 0; s < S.n_seg; ++s) {
     const int n = sm.seg_start[s + 1] - sm.seg_start[s];
     const uint32_t* kp = S.key + S.base(s);
     const int32_t* ip = S.idx + S.base(s);
-    for (int e0 = threadIdx.x; e0 < n; e0 += 4 * kSelThreads) {
+    for (int e0 = threadIdx.x; e0 < n; e0 += 4 * NT) {
       uint32_t kk[4];
       int32_t ii[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const int e = e0 + u * kSelThreads;
+        const int e = e0 + u * NT;
         kk[u] = e < n ? __ldg(kp + e) : 0u;
         ii[u] = e < n ? __ldg(ip + e) : 0;
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u)
-        if (e0 + u * kSelThreads < n && kk[u] >= edge) f(kk[u], ii[u]);
+        if (e0 + u * NT < n && kk[u] >= edge) f(kk[u], ii[u]);
     }
   }
 }
@@ -89,11 +120,11 @@ __device__ __forceinline__ void for_each_global(const Segs& S, const SelSmem& sm
 // Exact threshold (v, cut) over the entries fe visits: exactly K satisfy topk_keep.  One
 // histogram pass of 2048 bins linear in score over [kmin, kmax]; the boundary bin's entries
 // (normally a handful) are ranked directly; a crowded boundary bin takes the radix passes.
-template <class ForEach>
-__device__ void block_threshold(const ForEach& fe, int K, uint32_t kmin, uint32_t kmax, SelSmem& sm, uint32_t& v,
+template <int NT, class Sm, class ForEach>
+__device__ void block_threshold(const ForEach& fe, int K, uint32_t kmin, uint32_t kmax, Sm& sm, uint32_t& v,
                                 uint32_t& cut) {
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  for (int i = tid; i < kBins; i += kSelThreads) sm.hist[i] = 0u;
+  for (int i = tid; i < kBins; i += NT) sm.hist[i] = 0u;
   if (tid == 0) sm.n_bound = 0;
   __syncthreads();
   const float fmin = key_float(kmin), fmax = key_float(kmax);
@@ -105,8 +136,8 @@ __device__ void block_threshold(const ForEach& fe, int K, uint32_t kmin, uint32_
   };
   fe([&](uint32_t key, int32_t) { atomicAdd(&sm.hist[bin_of(key)], 1u); });
   __syncthreads();
-  // thread tid owns the 8 bins [kBins - 8 tid - 8, kBins - 8 tid), visited from the top
-  constexpr int kPerT = kBins / kSelThreads;
+  // thread tid owns the kPerT bins [kBins - kPerT (tid + 1), kBins - kPerT tid), from the top
+  constexpr int kPerT = kBins / NT;
   int h[kPerT], sum = 0;
 #pragma unroll
   for (int j = 0; j < kPerT; ++j) {
@@ -146,7 +177,7 @@ __device__ void block_threshold(const ForEach& fe, int K, uint32_t kmin, uint32_
     });
     __syncthreads();
     const int need = K - above;   // 1 <= need <= hb
-    for (int i = tid; i < hb; i += kSelThreads) {
+    for (int i = tid; i < hb; i += NT) {
       const uint32_t ki = sm.bkey[i];
       const int32_t ii = sm.bidx[i];
       int rank = 0;
@@ -163,42 +194,84 @@ __device__ void block_threshold(const ForEach& fe, int K, uint32_t kmin, uint32_
     return;
   }
   __syncthreads();
-  radix_threshold<kSelThreads>([] { __syncthreads(); }, fe, tid, K, sm.hist, sm.bc, v, cut);
+  radix_threshold<NT>([] { __syncthreads(); }, fe, tid, K, sm.hist, sm.bc, v, cut);
 }
 
-// Ascending bitonic sort of sm.sel[0, n) (n <= kSortMax), padded to a power of two.
-__device__ void block_sort_sel(SelSmem& sm, int n) {
-  int p = 1;
-  while (p < n) p <<= 1;
-  for (int i = n + threadIdx.x; i < p; i += kSelThreads) sm.sel[i] = ~0ull;
-  __syncthreads();
-  for (int size = 2; size <= p; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = threadIdx.x; i < p / 2; i += kSelThreads) {
-        const int lo = 2 * i - (i & (stride - 1));
-        const int hi = lo + stride;
-        const bool asc = (lo & size) == 0;
-        const unsigned long long a = sm.sel[lo], c = sm.sel[hi];
-        if ((a > c) == asc) {
-          sm.sel[lo] = c;
-          sm.sel[hi] = a;
-        }
-      }
-      __syncthreads();
+// Writes the n selected entries of sm.sel in ascending key index (offsets from rx; scores to
+// so when given) into out[0, n), then -1 up to topk.  Key indices lie in [rx, rx + L); one
+// outside (buffers the indexer never filled, after it stopped on an error) is flagged and put
+// in the nearest bucket, so the writes stay in bounds.
+template <int NT, int STAGE>
+__device__ void block_write_ordered(SelSmem<STAGE>& sm, int n, int L, int rx, int topk, int32_t* out, float* so,
+                                    uint32_t* status) {
+  const int tid = threadIdx.x;
+  unsigned long long* tmp = reinterpret_cast<unsigned long long*>(sm.key);   // kSortMax bucketed pairs
+  uint32_t* fill = reinterpret_cast<uint32_t*>(tmp + kSortMax);              // kBins fill counters
+  int sh = 0;
+  while (((L - 1) >> sh) >= kBins) ++sh;   // bucket of offset o: o >> sh < kBins
+  auto bucket = [&](int j) {
+    const int o = j - rx;
+    if (o < 0 || o >= L) {
+      atomicOr(status, DEV_ERR_BAD_INDEX);
+      return o < 0 ? 0 : (L - 1) >> sh;
     }
+    return o >> sh;
+  };
+  for (int i = tid; i < kBins; i += NT) {
+    sm.hist[i] = 0u;
+    fill[i] = 0u;
+  }
+  __syncthreads();
+  for (int e = tid; e < n; e += NT) atomicAdd(&sm.hist[bucket(static_cast<int>(sm.sel[e] >> 32))], 1u);
+  __syncthreads();
+  // exclusive scan of the bucket counts in place: thread tid owns kPerT consecutive buckets
+  constexpr int kPerT = kBins / NT;
+  int h[kPerT], sum = 0;
+#pragma unroll
+  for (int j = 0; j < kPerT; ++j) {
+    h[j] = static_cast<int>(sm.hist[tid * kPerT + j]);
+    sum += h[j];
+  }
+  int total = 0;
+  int c = block_exclusive_scan<NT>(sum, sm.wsum, &total);
+#pragma unroll
+  for (int j = 0; j < kPerT; ++j) {
+    sm.hist[tid * kPerT + j] = static_cast<uint32_t>(c);
+    c += h[j];
+  }
+  __syncthreads();
+  for (int e = tid; e < n; e += NT) {
+    const unsigned long long x = sm.sel[e];
+    const int b = bucket(static_cast<int>(x >> 32));
+    tmp[sm.hist[b] + atomicAdd(&fill[b], 1u)] = x;
+  }
+  __syncthreads();
+  for (int p = tid; p < n; p += NT) {
+    const unsigned long long x = tmp[p];
+    const int j = static_cast<int>(x >> 32);
+    const int b = bucket(j);
+    const int lo = static_cast<int>(sm.hist[b]), m = static_cast<int>(fill[b]);
+    int rank = lo;
+    for (int q = lo; q < lo + m; ++q) rank += static_cast<int>(tmp[q] >> 32) < j ? 1 : 0;
+    out[rank] = j - rx;
+    if (so) so[rank] = key_float(static_cast<uint32_t>(x));
+  }
+  for (int i = n + tid; i < topk; i += NT) {
+    out[i] = -1;
+    if (so) so[i] = -__int_as_float(0x7f800000);
   }
 }
 
-__global__ void __launch_bounds__(kSelThreads) select_kernel(int n_chunks, int cap4, int topk, int trivial_len,
-                                                             const int2* __restrict__ row_range,
-                                                             const uint32_t* __restrict__ cand_edge,
-                                                             const uint32_t* __restrict__ cand_key,
-                                                             const int32_t* __restrict__ cand_idx,
-                                                             const uint32_t* __restrict__ cand_cnt,
-                                                             int32_t* __restrict__ idx_out, float* score_out,
-                                                             uint32_t* status) {
+template <int STAGE, int NT>
+__global__ void __launch_bounds__(NT) select_kernel(int n_chunks, int cap4, int topk, int trivial_len,
+                                                    const int2* __restrict__ row_range,
+                                                    const uint32_t* __restrict__ cand_edge,
+                                                    const uint32_t* __restrict__ cand_key,
+                                                    const int32_t* __restrict__ cand_idx,
+                                                    const uint32_t* __restrict__ cand_cnt, int32_t* __restrict__ idx_out,
+                                                    float* score_out, uint32_t* status) {
   extern __shared__ __align__(16) uint8_t sel_smem_raw[];
-  SelSmem& sm = *reinterpret_cast<SelSmem*>(sel_smem_raw);
+  SelSmem<STAGE>& sm = *reinterpret_cast<SelSmem<STAGE>*>(sel_smem_raw);
   const int t = blockIdx.x;
   const int tid = threadIdx.x;
   const int2 r = row_range[t];
@@ -208,7 +281,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(int n_chunks, int c
   if (L <= trivial_len) {
     // the whole range is selected: offsets 0 .. L-1 in order, no candidates read.  The host
     // passes trivial_len = 0 whenever scores are requested, so only empty rows get here then.
-    for (int i = tid; i < topk; i += kSelThreads) {
+    for (int i = tid; i < topk; i += NT) {
       out[i] = i < L ? i : -1;
       if (so) so[i] = -__int_as_float(0x7f800000);
     }
@@ -216,22 +289,22 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(int n_chunks, int c
   }
   const int n_seg = n_chunks * kSub;
   if (tid == 0) {
-    int s = 0;
-    uint32_t e = 0u;
-    for (int c = 0; c < n_chunks; ++c) {
-      e = max(e, __ldg(cand_edge + static_cast<size_t>(t) * n_chunks + c));
-      for (int q = 0; q < kSub; ++q) {
-        sm.seg_start[c * kSub + q] = s;
-        s += min(static_cast<int>(__ldg(cand_cnt + (static_cast<size_t>(t) * n_chunks + c) * kSub + q)), cap4);
-      }
-    }
-    sm.seg_start[n_seg] = s;
-    sm.edge = e;
+    sm.edge = 0u;
     sm.n_stage = 0;
     sm.n_sel = 0;
     sm.kmin = 0xFFFFFFFFu;
     sm.kmax = 0u;
   }
+  __syncthreads();
+  // segment starts (one thread per segment) and the row's edge (largest chunk edge)
+  const int cnt_s =
+      tid < n_seg ? static_cast<int>(min(__ldg(cand_cnt + static_cast<size_t>(t) * n_seg + tid), static_cast<uint32_t>(cap4)))
+                  : 0;
+  if (tid < n_chunks) atomicMax(&sm.edge, __ldg(cand_edge + static_cast<size_t>(t) * n_chunks + tid));
+  int n_all = 0;
+  const int start_s = block_exclusive_scan<NT>(cnt_s, sm.wsum, &n_all);
+  if (tid < n_seg) sm.seg_start[tid] = start_s;
+  if (tid == 0) sm.seg_start[n_seg] = n_all;
   __syncthreads();
   const uint32_t edge = sm.edge;
   const Segs S{cand_key, cand_idx, n_seg, cap4, static_cast<size_t>(t) * n_seg * cap4};
@@ -239,9 +312,9 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(int n_chunks, int c
 
   // gather the entries at or above the edge into shared memory, with their key range
   uint32_t mn = 0xFFFFFFFFu, mx = 0u;
-  for_each_global(S, sm, edge, [&](uint32_t key, int32_t idx) {
+  for_each_global<NT>(S, sm, edge, [&](uint32_t key, int32_t idx) {
     const int slot = reserve_slot(&sm.n_stage);
-    if (slot < kStage) {
+    if (slot < STAGE) {
       sm.key[slot] = key;
       sm.idx[slot] = idx;
     }
@@ -256,17 +329,17 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(int n_chunks, int c
   }
   __syncthreads();
   const int n = sm.n_stage;
-  const bool staged = n <= kStage;
+  const bool staged = n <= STAGE;
   auto fe_stage = [&](auto&& f) {
-    for (int e = tid; e < n; e += kSelThreads) f(sm.key[e], sm.idx[e]);
+    for (int e = tid; e < n; e += NT) f(sm.key[e], sm.idx[e]);
   };
-  auto fe_global = [&](auto&& f) { for_each_global(S, sm, edge, f); };
+  auto fe_global = [&](auto&& f) { for_each_global<NT>(S, sm, edge, f); };
 
   uint32_t v = 0, cut = 0x7FFFFFFFu;
   const bool all = n <= kt;
   if (!all) {
-    if (staged) block_threshold(fe_stage, kt, sm.kmin, sm.kmax, sm, v, cut);
-    else block_threshold(fe_global, kt, sm.kmin, sm.kmax, sm, v, cut);
+    if (staged) block_threshold<NT>(fe_stage, kt, sm.kmin, sm.kmax, sm, v, cut);
+    else block_threshold<NT>(fe_global, kt, sm.kmin, sm.kmax, sm, v, cut);
   }
   // the selected entries, in any order, as (key index, score key) pairs
   auto take = [&](uint32_t key, int32_t idx) {
@@ -281,17 +354,27 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(int n_chunks, int c
   __syncthreads();
   const int n_sel = min(sm.n_sel, kSortMax);
   if (tid == 0 && sm.n_sel != kt) atomicOr(status, DEV_ERR_OVERFLOW);
-  block_sort_sel(sm, n_sel);
-  for (int i = tid; i < topk; i += kSelThreads) {
-    if (i < n_sel) {
-      const unsigned long long e = sm.sel[i];
-      out[i] = static_cast<int32_t>(e >> 32) - r.x;
-      if (so) so[i] = key_float(static_cast<uint32_t>(e));
-    } else {
-      out[i] = -1;
-      if (so) so[i] = -__int_as_float(0x7f800000);
-    }
+  block_write_ordered<NT>(sm, n_sel, L, r.x, topk, out, so, status);
+}
+
+template <int STAGE, int NT>
+cudaError_t launch_shape(int n_q, int n_chunks, int cap, int topk, int trivial_len, const int2* row_range,
+                         const uint32_t* cand_edge, const uint32_t* cand_key, const int32_t* cand_idx,
+                         const uint32_t* cand_cnt, int32_t* idx_out, float* score_out, uint32_t* status,
+                         cudaStream_t st) {
+  auto kern = select_kernel<STAGE, NT>;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, sizeof(SelSmem<STAGE>));
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
+  kern<<<n_q, NT, sizeof(SelSmem<STAGE>), st>>>(n_chunks, cap / kSub, topk, trivial_len, row_range, cand_edge,
+                                                 cand_key, cand_idx, cand_cnt, idx_out, score_out, status);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -302,19 +385,11 @@ cudaError_t launch_select(int n_q, int n_chunks, int cap, int topk, int trivial_
                           cudaStream_t st) {
   if (n_q <= 0) return cudaSuccess;
   if (n_chunks > kMaxSeg / kSub || topk > kSortMax || cap % kSub) return cudaErrorInvalidValue;
-  static bool attr_set[64] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, sizeof(SelSmem));
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_set[dev] = true;
-  }
-  select_kernel<<<n_q, kSelThreads, sizeof(SelSmem), st>>>(n_chunks, cap / kSub, topk, trivial_len, row_range,
-                                                          cand_edge, cand_key, cand_idx, cand_cnt, idx_out, score_out,
-                                                          status);
-  return cudaGetLastError();
+  if (static_cast<long long>(n_chunks) * cap <= kSmallStage)
+    return launch_shape<kSmallStage, kSmallThreads>(n_q, n_chunks, cap, topk, trivial_len, row_range, cand_edge,
+                                                    cand_key, cand_idx, cand_cnt, idx_out, score_out, status, st);
+  return launch_shape<kBigStage, kBigThreads>(n_q, n_chunks, cap, topk, trivial_len, row_range, cand_edge, cand_key,
+                                              cand_idx, cand_cnt, idx_out, score_out, status, st);
 }
 
 }  // namespace dsa
