@@ -387,3 +387,76 @@ def sparse_attn_backward(q: np.ndarray, kv: np.ndarray, idx: np.ndarray, ks: np.
         contrib[:, :d_v] += p.T @ np.asarray(d_o[t], np.float64)
         np.add.at(dkv, rows, contrib)
     return dq, dkv
+
+
+# --------------------------------------------------------------------------------------
+# lightning-indexer backward (a2 differentiated)
+# --------------------------------------------------------------------------------------
+
+def indexer_backward(q_idx: np.ndarray, k_idx: np.ndarray, w: np.ndarray,
+                     q_pos: np.ndarray, k_pos: np.ndarray, ks: np.ndarray,
+                     idx: np.ndarray, d_score: np.ndarray, rope_dim: int, theta: float,
+                     rope_q: bool = True, rope_k: bool = True, round_rotated: bool = True,
+                     rows: Sequence[int] | None = None, key_rows: Sequence[int] | None = None):
+    """Gradients of the selected indexer scores with respect to q_idx, k_idx and w.
+
+    "GLM-5/5.1/5.2 DSA + LoRA enablement" (Megatron-Bridge pull request), in the commit that
+    vendors the fused lighting_indexer "with fwd/bwd", names this backward without defining
+    it; it is the derivative of indexer_scores_row.  For query t, selected offset j
+    (idx[t, n] = j >= 0, key row ks_t + j) and upstream gradient g = d_score[t, n]:
+        x_h = q~[t, h] . k~[ks_t + j],    s = sum_h w[t, h] max(0, x_h)
+        dw[t, h]        += g max(0, x_h)
+        dq~[t, h]       += g w[t, h] [x_h > 0] k~[ks_t + j]
+        dk~[ks_t + j]   += g sum_h w[t, h] [x_h > 0] q~[t, h]
+    (ReLU'(0) = 0), then back through the rotation: dq = R(q_pos)^T dq~ when rope_q,
+    dk = R(k_pos)^T dk~ when rope_k, R^T being the rotation by the negated angle.  The bf16
+    rounding of the rotated values is taken as the identity in the derivative; with
+    round_rotated=False the forward it differentiates has no rounding at all (the form the
+    finite-difference pin uses).
+
+    rows: the query rows whose dq / dw to return (default all); key_rows: the key rows whose
+    dk to return (default all).  dk sums over EVERY query of idx whatever ``rows`` is.
+    Returns (dq [len(rows), H_I, d], dk [len(key_rows), d], dw [len(rows), H_I]).
+    """
+    rot = (lambda x, p: apply_index_rope(x, p, rope_dim, theta)) if round_rotated else \
+          (lambda x, p: rope_rotate_f64(x, p, rope_dim, theta))
+    q_idx = np.asarray(q_idx, np.float64)
+    k_idx = np.asarray(k_idx, np.float64)
+    w = np.asarray(w, np.float64)
+    n_q, H, d = q_idx.shape
+    rows = list(range(n_q)) if rows is None else list(rows)
+    key_rows = list(range(k_idx.shape[0])) if key_rows is None else list(key_rows)
+    k_rot = rot(k_idx, k_pos) if rope_k else k_idx
+    want_key = {int(j): n for n, j in enumerate(key_rows)}
+    want_row = {int(t): n for n, t in enumerate(rows)}
+    dq_rot = np.zeros((len(rows), H, d))
+    dk_rot = np.zeros((len(key_rows), d))
+    dw = np.zeros((len(rows), H))
+    for t in range(n_q):
+        sel_n = np.nonzero(idx[t] >= 0)[0]
+        if sel_n.size == 0:
+            continue
+        keys = int(ks[t]) + idx[t][sel_n]
+        hit = [m for m, j in enumerate(keys) if int(j) in want_key]
+        if t not in want_row and not hit:
+            continue
+        q_rot = rot(q_idx[t], np.full(H, q_pos[t])) if rope_q else q_idx[t]
+        K = k_rot[keys]                                  # [n, d]
+        g = np.asarray(d_score[t], np.float64)[sel_n]    # [n]
+        x = q_rot @ K.T                                  # [H, n]
+        G = (x > 0) * w[t][:, None] * g[None, :]         # [H, n]
+        if t in want_row:
+            r = want_row[t]
+            dw[r] = np.maximum(x, 0.0) @ g
+            dq_rot[r] = G @ K
+        for m in hit:
+            dk_rot[want_key[int(keys[m])]] += G[:, m] @ q_rot
+    if rope_q:
+        dq = rope_rotate_f64(dq_rot, -np.asarray(q_pos, np.float64)[rows][:, None], rope_dim, theta)
+    else:
+        dq = dq_rot
+    if rope_k:
+        dk = rope_rotate_f64(dk_rot, -np.asarray(k_pos, np.float64)[key_rows], rope_dim, theta)
+    else:
+        dk = dk_rot
+    return dq, dk, dw

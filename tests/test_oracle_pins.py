@@ -477,3 +477,105 @@ def test_rope_inverse_frequencies_closed_form():
         np.testing.assert_allclose(f[-1], theta ** (-(r - 2) / r), rtol=1e-14)
     with pytest.raises(ValueError):
         O.rope_inv_freq(63, 1e4)
+
+
+# ---------------------------------------------------------------------------- indexer backward
+
+def _indexer_bwd_case(seed, n_q=5, n_kv=14, H=3, d=8, r=4, k=6):
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((n_q, H, d))
+    kk = rng.standard_normal((n_kv, d))
+    w = rng.standard_normal((n_q, H))
+    q_pos = rng.integers(0, 50, n_q)
+    k_pos = rng.integers(0, 50, n_kv)
+    ks = rng.integers(0, 3, n_q)
+    idx = np.full((n_q, k), -1)
+    for t in range(n_q):
+        n = int(rng.integers(1, k + 1))
+        idx[t, :n] = np.sort(rng.choice(n_kv - ks[t], size=n, replace=False))
+    g = rng.standard_normal((n_q, k))
+    return q, kk, w, q_pos, k_pos, ks, idx, g
+
+
+def _indexer_loss(q, kk, w, q_pos, k_pos, ks, idx, g, r, theta):
+    # L = sum over selected entries of g * s, through the oracle's own forward (no rounding)
+    k_rot = O.rope_rotate_f64(kk, k_pos, r, theta)
+    total = 0.0
+    for t in range(q.shape[0]):
+        q_rot = O.rope_rotate_f64(q[t], np.full(q.shape[1], q_pos[t]), r, theta)
+        s = O.indexer_scores_row(q_rot, k_rot[ks[t]:], w[t])
+        for n, j in enumerate(idx[t]):
+            if j >= 0:
+                total += g[t, n] * s[j]
+    return total
+
+
+def test_indexer_backward_matches_finite_differences():
+    # central differences of sum g * s through indexer_scores_row and the rotation, keys shared
+    # by several queries (the scatter of dk) and -1 padding included
+    r, theta = 4, 1e4
+    q, kk, w, q_pos, k_pos, ks, idx, g = _indexer_bwd_case(7)
+    args = (q_pos, k_pos, ks, idx, g, r, theta)
+    dq, dk, dw = O.indexer_backward(q, kk, w, q_pos, k_pos, ks, idx, g, r, theta, round_rotated=False)
+    h = 1e-6
+    num = []
+    for arr, pos in ((q, 0), (kk, 1), (w, 2)):
+        f = np.zeros_like(arr)
+        for i in np.ndindex(arr.shape):
+            ap, am = arr.copy(), arr.copy()
+            ap[i] += h
+            am[i] -= h
+            vp = [q, kk, w]
+            vm = [q, kk, w]
+            vp[pos], vm[pos] = ap, am
+            f[i] = (_indexer_loss(*vp, *args) - _indexer_loss(*vm, *args)) / (2 * h)
+        num.append(f)
+    np.testing.assert_allclose(dq, num[0], rtol=1e-6, atol=1e-7)
+    np.testing.assert_allclose(dk, num[1], rtol=1e-6, atol=1e-7)
+    np.testing.assert_allclose(dw, num[2], rtol=1e-6, atol=1e-7)
+    used = {int(ks[t]) + int(j) for t in range(q.shape[0]) for j in idx[t] if j >= 0}
+    for row in set(range(kk.shape[0])) - used:
+        assert not dk[row].any()
+
+
+def test_indexer_backward_single_head_is_relu_matmul_autograd():
+    # H_I = 1, w = 1, no RoPE: s = relu(q . k_j), differentiated by torch autograd
+    rng = np.random.default_rng(3)
+    n_q, n_kv, d, k = 4, 9, 6, 5
+    q = rng.standard_normal((n_q, 1, d))
+    kk = rng.standard_normal((n_kv, d))
+    w = np.ones((n_q, 1))
+    ks = np.zeros(n_q, dtype=np.int64)
+    idx = np.stack([np.sort(rng.choice(n_kv, size=k, replace=False)) for _ in range(n_q)])
+    g = rng.standard_normal((n_q, k))
+    dq, dk, dw = O.indexer_backward(q, kk, w, np.zeros(n_q), np.zeros(n_kv), ks, idx, g, 0, 1e4,
+                                    rope_q=False, rope_k=False)
+    tq = torch.tensor(q[:, 0], dtype=torch.float64, requires_grad=True)
+    tk = torch.tensor(kk, dtype=torch.float64, requires_grad=True)
+    s = torch.relu(tq @ tk.T)                                # [n_q, n_kv]
+    sel = torch.gather(s, 1, torch.tensor(idx))
+    (sel * torch.tensor(g)).sum().backward()
+    np.testing.assert_allclose(dq[:, 0], tq.grad.numpy(), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(dk, tk.grad.numpy(), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(dw[:, 0], (torch.gather(s, 1, torch.tensor(idx)).detach().numpy() * g).sum(1),
+                               rtol=1e-12)
+
+
+def test_indexer_backward_euler_identity_and_row_subsets():
+    # s is positively homogeneous of degree 1 in each of q~, k~ and w, so
+    # sum q~.dq~ = sum k~.dk~ = sum w.dw = sum g s; the rotation is orthogonal, so the same
+    # holds for the unrotated q, k and their gradients (no rounding).  Row and key subsets
+    # return the matching slices of the full result.
+    r, theta = 4, 1e4
+    q, kk, w, q_pos, k_pos, ks, idx, g = _indexer_bwd_case(11, n_q=6, n_kv=16, H=4, d=8, k=7)
+    L = _indexer_loss(q, kk, w, q_pos, k_pos, ks, idx, g, r, theta)
+    dq, dk, dw = O.indexer_backward(q, kk, w, q_pos, k_pos, ks, idx, g, r, theta, round_rotated=False)
+    assert abs(float((q * dq).sum()) - L) <= 1e-10 * max(1.0, abs(L))
+    assert abs(float((kk * dk).sum()) - L) <= 1e-10 * max(1.0, abs(L))
+    assert abs(float((w * dw).sum()) - L) <= 1e-10 * max(1.0, abs(L))
+    rows, keys = [4, 1], [3, 0, 15]
+    dq2, dk2, dw2 = O.indexer_backward(q, kk, w, q_pos, k_pos, ks, idx, g, r, theta, round_rotated=False,
+                                       rows=rows, key_rows=keys)
+    np.testing.assert_allclose(dq2, dq[rows], rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(dw2, dw[rows], rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(dk2, dk[keys], rtol=1e-13, atol=1e-15)
