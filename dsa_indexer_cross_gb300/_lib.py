@@ -30,7 +30,8 @@ EXPORTED = ("dsa_status_string", "dsa_last_error", "dsa_donor_table", "dsa_rope_
             "dsa_layers_workspace_size", "indexshare_layers_forward", "dsa_workspace_status",
             "dsa_indexer_topk_static", "dsa_profile_enable", "dsa_profile_indexer_last", "dsa_mtp_indexshare_step",
             "dsa_indexer_topk_paged", "dsa_sparse_attn_paged", "dsa_indexer_projections", "dsa_sparse_attn_backward",
-            "dsa_indexer_static_status", "dsa_profile_read", "dsa_debug_pipeline")
+            "dsa_indexer_static_status", "dsa_profile_read", "dsa_debug_pipeline",
+            "dsa_indexer_backward_workspace_size", "dsa_indexer_backward")
 
 PROFILE_KINDS = {0: "rope", 1: "ranges", 2: "indexer", 3: "select", 4: "attn_prep", 5: "attn", 6: "attn_bwd",
                  7: "proj", 8: "indexer_bwd"}
@@ -118,6 +119,11 @@ def lib() -> C.CDLL:
         L.dsa_profile_read.argtypes = [P(ProfileRecord), i32, P(i32)]
         L.dsa_sparse_attn_backward.restype = st
         L.dsa_sparse_attn_backward.argtypes = [P(AttnDesc), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.dsa_indexer_backward_workspace_size.restype = st
+        L.dsa_indexer_backward_workspace_size.argtypes = [P(IndexerDesc), P(sz)]
+        L.dsa_indexer_backward.restype = st
+        L.dsa_indexer_backward.argtypes = [P(IndexerDesc), vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp,
+                                           sz, vp]
         L.dsa_indexer_projections.restype = st
         L.dsa_indexer_projections.argtypes = [P(ProjDesc), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.dsa_indexer_topk_paged.restype = st
@@ -238,6 +244,31 @@ def dsa_indexer_topk_static(desc: IndexerDesc, q_idx, k_idx, w, q_pos, k_pos, ks
     _check(lib().dsa_indexer_topk_static(C.byref(desc), _ptr(q_idx), _ptr(k_idx), _ptr(w), _ptr(q_pos), _ptr(k_pos),
                                          _ptr(ks), _ptr(ke), _ptr(rope_cs), n_pos, _ptr(idx_out), _ptr(score_out),
                                          _stream(stream)))
+
+
+def dsa_indexer_backward_workspace_size(desc: IndexerDesc) -> int:
+    n = C.c_size_t(0)
+    _check(lib().dsa_indexer_backward_workspace_size(C.byref(desc), C.byref(n)))
+    return n.value
+
+
+def dsa_indexer_backward(desc: IndexerDesc, q_idx, k_idx, w, q_pos, k_pos, ks, ke, rope_cs, idx, d_score, dq_idx,
+                         dk_idx, dw, ws=None, stream=None) -> torch.Tensor:
+    """Gradients of the selected scores: dq_idx (written), dk_idx and dw (zeroed, then
+    accumulated), fp32, for the upstream d_score aligned with the forward's idx."""
+    _indexer_args(desc, q_idx, k_idx, w, q_pos, k_pos, ks, ke, rope_cs, idx, None)
+    n_q, n_kv, H, d, k = desc.n_q, desc.n_kv, desc.n_heads, desc.head_dim, desc.topk
+    f32 = torch.float32
+    for t, n, name in ((d_score, n_q * k, "d_score"), (dq_idx, n_q * H * d, "dq_idx"), (dk_idx, n_kv * d, "dk_idx"),
+                       (dw, n_q * H, "dw")):
+        _want(t, f32, n, name)
+    if ws is None:
+        ws = torch.empty(dsa_indexer_backward_workspace_size(desc), dtype=torch.uint8, device=dq_idx.device)
+    n_pos = rope_cs.shape[0] if rope_cs is not None else 0
+    _check(lib().dsa_indexer_backward(C.byref(desc), _ptr(q_idx), _ptr(k_idx), _ptr(w), _ptr(q_pos), _ptr(k_pos),
+                                      _ptr(ks), _ptr(ke), _ptr(rope_cs), n_pos, _ptr(idx), _ptr(d_score),
+                                      _ptr(dq_idx), _ptr(dk_idx), _ptr(dw), _ptr(ws), ws.numel(), _stream(stream)))
+    return ws
 
 
 # ------------------------------------------------------------------------------ attention

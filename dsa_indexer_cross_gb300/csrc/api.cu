@@ -841,6 +841,109 @@ dsa_status dsa_sparse_attn_backward(const dsa_attn_desc* desc, const void* q, co
   return DSA_OK;
 }
 
+namespace {
+struct IndexerBwdLayout {
+  size_t off_q = 0, off_k = 0, total = 0;
+};
+IndexerBwdLayout indexer_bwd_layout(const dsa_indexer_desc* d) {
+  IndexerBwdLayout L;
+  size_t off = kAlign;   // status header
+  const bool rq = (d->flags & DSA_IDX_ROPE_Q) && d->rope_dim > 0;
+  const bool rk = (d->flags & DSA_IDX_ROPE_K) && d->rope_dim > 0;
+  L.off_q = off;
+  if (rq) off += align_up(static_cast<size_t>(d->n_q) * d->n_heads * d->head_dim * 2);
+  L.off_k = off;
+  if (rk) off += align_up(static_cast<size_t>(d->n_kv) * d->head_dim * 2);
+  L.total = off;
+  return L;
+}
+dsa_status check_indexer_bwd_desc(const dsa_indexer_desc* d) {
+  dsa_status s = check_indexer_desc(d);
+  if (s != DSA_OK) return s;
+  if (d->head_dim != 128)
+    return fail(DSA_ERR_UNSUPPORTED, "indexer backward: head_dim %d, supported value is 128", d->head_dim);
+  if (d->flags & DSA_IDX_INDEPENDENT_ROWS)
+    return fail(DSA_ERR_UNSUPPORTED, "indexer backward: independent rows are not supported");
+  return DSA_OK;
+}
+}  // namespace
+
+dsa_status dsa_indexer_backward_workspace_size(const dsa_indexer_desc* desc, size_t* bytes) {
+  if (!bytes) return fail(DSA_ERR_ARG, "bytes is NULL");
+  dsa_status s = check_indexer_bwd_desc(desc);
+  if (s != DSA_OK) return s;
+  *bytes = indexer_bwd_layout(desc).total;
+  return DSA_OK;
+}
+
+dsa_status dsa_indexer_backward(const dsa_indexer_desc* desc, const void* q_idx, const void* k_idx, const float* w,
+                                const int32_t* q_pos, const int32_t* k_pos, const int32_t* ks, const int32_t* ke,
+                                const float* rope_cs, int32_t rope_n_pos, const int32_t* idx, const float* d_score,
+                                float* dq_idx, float* dk_idx, float* dw, void* ws, size_t ws_bytes, void* stream) {
+  dsa_status s = check_indexer_bwd_desc(desc);
+  if (s != DSA_OK) return s;
+  const dsa_indexer_desc* d = desc;
+  const bool rq = (d->flags & DSA_IDX_ROPE_Q) && d->rope_dim > 0;
+  const bool rk = (d->flags & DSA_IDX_ROPE_K) && d->rope_dim > 0;
+  if (!q_idx || !k_idx || !w || !ks || !ke || !idx || !d_score || !dq_idx || !dk_idx || !dw || !ws)
+    return fail(DSA_ERR_ARG, "q_idx, k_idx, w, ks, ke, idx, d_score, dq_idx, dk_idx, dw and ws must be non-NULL");
+  if ((rq && !q_pos) || (rk && !k_pos) || ((rq || rk) && (!rope_cs || rope_n_pos < 1)))
+    return fail(DSA_ERR_ARG, "RoPE requested but q_pos/k_pos/rope_cs/rope_n_pos missing");
+  if (!aligned16(q_idx) || !aligned16(k_idx) || !aligned16(w) || !aligned16(dq_idx) || !aligned16(dk_idx))
+    return fail(DSA_ERR_ARG, "q_idx, k_idx, w, dq_idx and dk_idx must be 16-byte aligned");
+  if (rope_cs && !aligned16(rope_cs)) return fail(DSA_ERR_ARG, "rope_cs must be 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(ws) % kAlign) return fail(DSA_ERR_ARG, "workspace must be 256-byte aligned");
+  if ((s = check_device()) != DSA_OK) return s;
+  const IndexerBwdLayout L = indexer_bwd_layout(d);
+  if (ws_bytes < L.total)
+    return fail(DSA_ERR_WORKSPACE, "indexer backward workspace too small: %zu < %zu bytes", ws_bytes, L.total);
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  uint32_t* status = reinterpret_cast<uint32_t*>(base);
+  cudaError_t e;
+  if ((e = cudaMemsetAsync(ws, 0, kAlign, st)) != cudaSuccess) return cuda_fail(e, "clear status");
+  if (d->n_kv > 0 &&
+      (e = cudaMemsetAsync(dk_idx, 0, static_cast<size_t>(d->n_kv) * d->head_dim * sizeof(float), st)) != cudaSuccess)
+    return cuda_fail(e, "clear dk_idx");
+  if (d->n_q == 0) return DSA_OK;
+  if ((e = cudaMemsetAsync(dw, 0, static_cast<size_t>(d->n_q) * d->n_heads * sizeof(float), st)) != cudaSuccess)
+    return cuda_fail(e, "clear dw");
+  const void* qr = q_idx;
+  const void* kr = k_idx;
+  const int ps = prof_begin(kProfIndexerBwd, st);
+  if (rq) {
+    e = launch_rope_rows(q_idx, base + L.off_q, q_pos, static_cast<int64_t>(d->n_q) * d->n_heads, d->n_heads,
+                         d->head_dim, d->rope_dim, rope_cs, rope_n_pos, status, st);
+    if (e != cudaSuccess) return cuda_fail(e, "index q RoPE");
+    qr = base + L.off_q;
+  }
+  if (rk && d->n_kv > 0) {
+    e = launch_rope_rows(k_idx, base + L.off_k, k_pos, d->n_kv, 1, d->head_dim, d->rope_dim, rope_cs, rope_n_pos,
+                         status, st);
+    if (e != cudaSuccess) return cuda_fail(e, "index k RoPE");
+    kr = base + L.off_k;
+  }
+  const int q_split = rq ? rope_split_blocks(d->head_dim, d->rope_dim) : 0;
+  const int k_split = rk ? rope_split_blocks(d->head_dim, d->rope_dim) : 0;
+  const DevInfo di = dev_info();
+  e = launch_indexer_bwd(d->n_q, d->n_kv, d->n_heads, d->head_dim, d->topk, qr, q_idx, kr, k_idx, q_split, k_split, w,
+                         ks, ke, idx, d_score, dq_idx, dk_idx, dw, di.sms > 0 ? di.sms : 148, status, pipeline_debug(),
+                         st);
+  if (e != cudaSuccess) return cuda_fail(e, "indexer backward");
+  if (rq) {
+    e = launch_rope_rows_transpose_f32(dq_idx, q_pos, static_cast<int64_t>(d->n_q) * d->n_heads, d->n_heads,
+                                       d->head_dim, d->rope_dim, rope_cs, rope_n_pos, status, st);
+    if (e != cudaSuccess) return cuda_fail(e, "dq RoPE transpose");
+  }
+  if (rk && d->n_kv > 0) {
+    e = launch_rope_rows_transpose_f32(dk_idx, k_pos, d->n_kv, 1, d->head_dim, d->rope_dim, rope_cs, rope_n_pos, status,
+                                       st);
+    if (e != cudaSuccess) return cuda_fail(e, "dk RoPE transpose");
+  }
+  prof_end(ps, st);
+  return DSA_OK;
+}
+
 dsa_status dsa_workspace_status(const void* ws, void* stream, uint32_t* device_bits) {
   if (!ws) return fail(DSA_ERR_ARG, "workspace is NULL");
   WsHeader h{};

@@ -54,6 +54,11 @@ struct IndexerPlan {
 // (0, 0) and flags; group_range[g] = union of the ranges of the group's rows longer than
 // trivial_len (shorter rows keep every key and are not scored), at most span_limit keys long
 // (a longer union is cut there and flagged: the plan's key chunks cover span_limit keys).
+// In-place transpose of the index RoPE on fp32 rows (the backward of launch_rope_rows): the
+// rotated pair (a, b) of dims (d - r + i, d - r/2 + i) becomes (a c + b s, b c - a s).
+cudaError_t launch_rope_rows_transpose_f32(float* x, const int32_t* pos, int64_t n_rows, int rows_per_pos, int d,
+                                           int rope, const float* cs, int n_pos, uint32_t* status, cudaStream_t st);
+
 cudaError_t launch_ranges(const int32_t* ks, const int32_t* ke, int n_q, int group, int n_kv, int max_len,
                           int trivial_len, long long span_limit, int2* row_range, int2* group_range,
                           uint32_t* status, cudaStream_t st);
@@ -65,6 +70,15 @@ struct PipelineDebug {
   int stop_after_tiles = -1;
 };
 PipelineDebug pipeline_debug();
+
+// Lightning-indexer backward (head_dim 128, n_heads a multiple of 4 up to 64): dq~ written,
+// dk~ and dw accumulated (both zeroed by the caller), all fp32.  q_split / k_split: 64-dim
+// blocks read from the unrotated inputs, as in launch_indexer.
+cudaError_t launch_indexer_bwd(int n_q, int n_kv, int n_heads, int head_dim, int topk, const void* q_rot,
+                               const void* q_in, const void* k_rot, const void* k_in, int q_split, int k_split,
+                               const float* w, const int32_t* ks, const int32_t* ke, const int32_t* idx,
+                               const float* d_score, float* dq, float* dk, float* dw, int grid, uint32_t* status,
+                               const PipelineDebug& dbg, cudaStream_t st);
 
 // Scores + streaming top-k candidates.  tmap_q covers rotated q as [(n_q*H_I) x d_I] bf16,
 // tmap_k covers rotated k as [n_kv x d_I] bf16, both 128-byte swizzled, boxes {64, N} and

@@ -152,6 +152,29 @@ __global__ void __launch_bounds__(256) ranges_kernel(const int32_t* __restrict__
   }
 }
 
+// Transposed rotation on fp32 rows in place: one thread per rotated pair.
+__global__ void __launch_bounds__(256) rope_rows_transpose_f32(float* __restrict__ x, const int32_t* __restrict__ pos,
+                                                               int64_t n_rows, int rows_per_pos, int d, int rope,
+                                                               const float* __restrict__ cs, int n_pos,
+                                                               uint32_t* status) {
+  const int half = rope >> 1;
+  const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (gid >= n_rows * half) return;
+  const int64_t row = gid / half;
+  const int i = static_cast<int>(gid - row * half);
+  const int p = __ldg(pos + row / rows_per_pos);
+  if (p < 0 || p >= n_pos) {
+    atomicOr(status, DEV_ERR_BAD_INDEX);
+    return;
+  }
+  const float c = __ldg(cs + (static_cast<int64_t>(p) * half + i) * 2);
+  const float s = __ldg(cs + (static_cast<int64_t>(p) * half + i) * 2 + 1);
+  float* r = x + row * d;
+  const float a = r[d - rope + i], b = r[d - half + i];
+  r[d - rope + i] = a * c + b * s;
+  r[d - half + i] = b * c - a * s;
+}
+
 }  // namespace
 
 cudaError_t launch_rope_rows(const void* in, void* out, const int32_t* pos, int64_t n_rows, int rows_per_pos, int d,
@@ -181,6 +204,15 @@ cudaError_t launch_ranges(const int32_t* ks, const int32_t* ke, int n_q, int gro
   if (group < 1 || 256 % group != 0) return cudaErrorInvalidValue;
   ranges_kernel<<<(n_q + 255) / 256, 256, 0, st>>>(ks, ke, n_q, group, n_kv, max_len, trivial_len, span_limit, row_range,
                                                    group_range, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rope_rows_transpose_f32(float* x, const int32_t* pos, int64_t n_rows, int rows_per_pos, int d,
+                                           int rope, const float* cs, int n_pos, uint32_t* status, cudaStream_t st) {
+  if (n_rows <= 0 || rope <= 0) return cudaSuccess;
+  const int64_t total = n_rows * (rope / 2);
+  rope_rows_transpose_f32<<<static_cast<unsigned>((total + 255) / 256), 256, 0, st>>>(x, pos, n_rows, rows_per_pos, d,
+                                                                                       rope, cs, n_pos, status);
   return cudaGetLastError();
 }
 

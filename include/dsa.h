@@ -308,6 +308,38 @@ dsa_status dsa_sparse_attn_backward(const dsa_attn_desc* desc, const void* q, co
                                     const int32_t* ks, const void* out, const float* lse, const void* d_out,
                                     float* dq, float* dkv, void* ws, size_t ws_bytes, void* stream);
 
+/* Gradients of the indexer scores that dsa_indexer_topk selected.  [MB]'s commit vendoring
+ * the fused lighting_indexer "with fwd/bwd" names this backward without defining it; it is
+ * the exact derivative of the score above.  For row t, slot n < min(topk, ke_t - ks_t) with
+ * idx[t][n] = j >= 0 (key row ks_t + j) and upstream g = d_score[t][n]:
+ *   x_h = rope(q_idx[t, h]) . rope(k_idx[ks_t + j])
+ *   dw[t][h]          += g max(0, x_h)
+ *   dq_idx[t][h]      += R(q_pos_t)^T  g w[t][h] [x_h > 0] rope(k_idx[ks_t + j])
+ *   dk_idx[ks_t + j]  += R(k_pos_j)^T  g sum_h w[t][h] [x_h > 0] rope(q_idx[t, h])
+ * with ReLU'(0) = 0, R^T the rotation by the negated angle (only when the matching ROPE flag
+ * is set), and the bf16 rounding of the rotated inputs taken as the identity.  The products
+ * run on the tensor core with g w [x > 0] rounded to bf16 and fp32 accumulation.  Slots past
+ * min(topk, ke_t - ks_t) are not read; -1 slots are skipped; an offset >= ke_t - ks_t is
+ * skipped and flagged (DSA_ERR_DEVICE).  The loss that produces d_score (for example a KL
+ * term between the indexer's and the attention's distributions) is the caller's: the pages
+ * do not define one.
+ *   desc: as for dsa_indexer_topk; head_dim must be 128, n_heads <= 64, and
+ *         DSA_IDX_INDEPENDENT_ROWS is not supported.
+ *   inputs as for dsa_indexer_topk (w 16-byte aligned), plus
+ *   idx     int32 [n_q][topk]  the forward's idx_out        d_score f32 [n_q][topk]
+ *   outputs f32: dq_idx [n_q][n_heads][head_dim] (written), dk_idx [n_kv][head_dim] and
+ *          dw [n_q][n_heads] (zeroed here, then accumulated; rows of dk_idx selected by
+ *          several queries receive atomic adds, so the order of the additions, and the last
+ *          bits, vary from run to run).  q_idx, k_idx, dq_idx, dk_idx 16-byte aligned.
+ * ws: dsa_indexer_backward_workspace_size bytes, 256-byte aligned.  Errors: DSA_ERR_ARG,
+ * DSA_ERR_UNSUPPORTED, DSA_ERR_WORKSPACE, DSA_ERR_CUDA; device-side faults go to the
+ * workspace status (dsa_workspace_status). */
+dsa_status dsa_indexer_backward_workspace_size(const dsa_indexer_desc* desc, size_t* bytes);
+dsa_status dsa_indexer_backward(const dsa_indexer_desc* desc, const void* q_idx, const void* k_idx, const float* w,
+                                const int32_t* q_pos, const int32_t* k_pos, const int32_t* ks, const int32_t* ke,
+                                const float* rope_cs, int32_t rope_n_pos, const int32_t* idx, const float* d_score,
+                                float* dq_idx, float* dk_idx, float* dw, void* ws, size_t ws_bytes, void* stream);
+
 /* ------------------------------------------------------------------ paged caches ---- */
 
 /* Paged decode caches (a serving layout; the pages describe per-query key ranges only -- the

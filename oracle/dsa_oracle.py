@@ -441,16 +441,18 @@ def indexer_backward(q_idx: np.ndarray, k_idx: np.ndarray, w: np.ndarray,
         if t not in want_row and not hit:
             continue
         q_rot = rot(q_idx[t], np.full(H, q_pos[t])) if rope_q else q_idx[t]
-        K = k_rot[keys]                                  # [n, d]
-        g = np.asarray(d_score[t], np.float64)[sel_n]    # [n]
+        cols = np.arange(keys.size) if t in want_row else np.asarray(hit, dtype=np.int64)
+        K = k_rot[keys[cols]]                            # [n, d]
+        g = np.asarray(d_score[t], np.float64)[sel_n[cols]]
         x = q_rot @ K.T                                  # [H, n]
         G = (x > 0) * w[t][:, None] * g[None, :]         # [H, n]
         if t in want_row:
             r = want_row[t]
             dw[r] = np.maximum(x, 0.0) @ g
             dq_rot[r] = G @ K
-        for m in hit:
-            dk_rot[want_key[int(keys[m])]] += G[:, m] @ q_rot
+        for c, m in enumerate(cols):
+            if int(keys[m]) in want_key:
+                dk_rot[want_key[int(keys[m])]] += G[:, c] @ q_rot
     if rope_q:
         dq = rope_rotate_f64(dq_rot, -np.asarray(q_pos, np.float64)[rows][:, None], rope_dim, theta)
     else:
