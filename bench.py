@@ -609,6 +609,30 @@ def time_bwd(D, w, st, dev, stream, flush, tc_peak, reps: int = 5):
     return out
 
 
+def time_indexer_bwd(D, w, st, dev, stream, flush, tc_peak, reps: int = 5):
+    """Kernel time of dsa_indexer_backward on the first layer's index inputs and selected keys
+    (seeded upstream gradient), from the launch log, L2 flushed before each call.  FLOPs: three
+    products per selected (query, key) pair, 2 H_I d_I each (scores recomputed, dq, dk)."""
+    L0, idx, R = st["layers"][0], st["cache"].buffers[0], st["R"]
+    g = torch.Generator(device=dev)
+    g.manual_seed(9)
+    d_score = torch.randn((w.n_q, w.topk), generator=g, device=dev)
+    dq = torch.empty((w.n_q, w.n_heads_idx, w.head_dim_idx), dtype=torch.float32, device=dev)
+    dk = torch.empty((st["geo"].n_kv, w.head_dim_idx), dtype=torch.float32, device=dev)
+    dw = torch.empty((w.n_q, w.n_heads_idx), dtype=torch.float32, device=dev)
+    desc = st["idesc"]
+    ws = torch.empty(D.dsa_indexer_backward_workspace_size(desc), dtype=torch.uint8, device=dev)
+    m = logged_ms(D, lambda: D.dsa_indexer_backward(desc, L0["q_idx"], L0["k_idx"], L0["w"], st["q_pos"], st["k_pos"],
+                                                    st["ks"], st["ke"], st["rope"], idx, d_score, dq, dk, dw, ws=ws,
+                                                    stream=stream), reps, flush, "indexer_bwd")
+    if D.dsa_workspace_status(ws) != 0:
+        raise RuntimeError("device status set by the indexer backward")
+    flops = 3 * 2.0 * R["rows"] * w.n_heads_idx * w.head_dim_idx
+    return {"ms": m, "flops": flops, "tflops": flops / (m / 1e3) / 1e12,
+            "frac_of_bf16_peak": flops / (m / 1e3) / 1e12 / tc_peak,
+            "kernel": "indexer_bwd_kernel + RoPE transpose passes (launch log; dk and dw cleared before)"}
+
+
 # --------------------------------------------------------------------------- paged caches
 def time_paged(D, synth, w, geo, L0, idx_full, attn_ms_contig, idx_ms_contig, dev, stream, flush, reps: int = 20,
                seed: int = 3):
