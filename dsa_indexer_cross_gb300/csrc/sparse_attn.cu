@@ -23,9 +23,9 @@
 //
 // Two ways to walk the rows (template parameter HD):
 //   HD == 0  "gather": item = (token, block of HB heads); the tile holds the token's next
-//            64 selected rows, fetched as four-row TMA gathers plus cp.async for the last
-//            blocks (an empty slot reads row 0 or zeros and is masked); a paged cache maps
-//            each offset through the token's block table (template parameter PAGED).
+//            64 selected rows, fetched with cp.async (an empty slot reads zeros and is
+//            masked); a paged cache maps each offset through the token's block table
+//            (template parameter PAGED).
 //   HD  > 0  "block-dense": item = HB / HD consecutive tokens with all HD heads; the tile is
 //            64 CONSECUTIVE latent rows of the block's key range, fetched by TMA, and a
 //            per-(token, row) selection bitmask built from the index rows masks S^T.  Used
@@ -41,8 +41,7 @@
 // and are reduced once per item.
 //
 // Warp roles: warps 0-1 load Q and the rows (Q as nine 64-dim TMA boxes; the rows as one
-// 3-D TMA box per tile in block-dense mode, or as four-row TMA gathers plus cp.async for the
-// last blocks in the gather walk); warp 2 issues the S^T products; warps 3-6 (and 8-11 in
+// 3-D TMA box per tile in block-dense mode, or with cp.async in the gather walk); warp 2 issues the S^T products; warps 3-6 (and 8-11 in
 // the block-dense walk) run the softmax and the epilogue; warp 7 owns TMEM and issues the PV
 // products (256 threads, 384 block-dense).  With the two products issued from separate
 // warps, PV(g) goes out as soon as P(g) exists instead of queueing behind S^T(g+1), whose
@@ -62,10 +61,11 @@ constexpr int kKB = kDqk / 64;     // 64-dim blocks per tile (the last one holds
 constexpr int kBlkBytes = kRows * 128;         // one block: 64 rows x 128 B
 constexpr int kSlots = 2 * kKB;                // two tiles in flight
 constexpr int kProd = 64;                      // warps 0-1
-// Gather walk: the last kCpBlocks 64-dim blocks of every tile come through cp.async (the
-// load/store unit) while the other blocks come through four-row TMA gathers, so both copy
-// paths of the SM work on a tile at once (the TMA unit alone takes ~37 cycles per gather).
-constexpr int kCpBlocks = 3;
+// Gather walk: every 64-dim block of a tile comes through cp.async (the load/store unit).
+// Four-row TMA gathers for some of the blocks were slower: the TMA unit takes ~37 cycles per
+// gather, and moving the last of them to cp.async cut the walk's time by a quarter (1M-key
+// chunk) to a third (32K prefill).
+constexpr int kCpBlocks = 9;
 // Warps 0-1 load, warp 2 issues S^T, warps 3-6 (and, block-dense, 8-11) run the softmax,
 // warp 7 owns TMEM and issues PV.
 constexpr int kDenseCols = 64;                 // columns of a block-dense item
@@ -326,19 +326,15 @@ __global__ void __launch_bounds__(ACfg<HB, HD>::THREADS, 1)
         }
         ok = sync_ok(ok);
       } else {
-        // A tile is 64 selected rows x 9 blocks of 64 dims.  Blocks [0, kTmaBlocks) come as
-        // 16 groups of four rows per block through four-row TMA gathers: thread tid handles row
-        // group tid % 16 for blocks tid / 16, tid / 16 + 4, ...  The other blocks come through
-        // cp.async: thread tid copies 16-byte chunk tid % 8 of rows tid / 8 + 8 m (m < 8), so a
-        // warp reads four whole 128-byte row segments per instruction.  Row indices are read
-        // before the slot set is released.  A slot without a selection (-1) reads row 0 (TMA)
-        // or zeros (cp.async) and is masked by the softmax.
-        constexpr int kTmaBlocks = kKB - kCpBlocks;
+        // A tile is 64 selected rows x 9 blocks of 64 dims, copied with cp.async: thread tid
+        // copies 16-byte chunk tid % 8 of rows tid / 8 + 8 m (m < 8) in every block, so a warp
+        // reads four whole 128-byte row segments per instruction.  Row indices are read before
+        // the slot set is released.  A slot without a selection (-1) reads zeros and is masked
+        // by the softmax.
+        static_assert(kCpBlocks == kKB, "the gather walk copies whole rows with cp.async");
         const int t = I.t0;
         const int32_t* irow = idx + static_cast<size_t>(t) * topk;
         const TokenRows trow = token_rows<PAGED>(pg, ks, t);
-        const int grp = tid & 15;
-        const int b0 = tid >> 4;
         auto row_of = [&](int slot, bool count_bad) -> int {
           const int j = slot < topk ? __ldg(irow + slot) : -1;
           long long row;
@@ -359,39 +355,28 @@ __global__ void __launch_bounds__(ACfg<HB, HD>::THREADS, 1)
           return v ? static_cast<int>(row) : -1;
         };
         for (int i = 0; i < I.nt; ++i, ++g) {
-          int rows[4];
+          int crow[8];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) rows[u] = row_of(i * kRows + 4 * grp + u, b0 == 0);
-          int crow[kCpBlocks > 0 ? 8 : 1];
-          if constexpr (kCpBlocks > 0) {
-#pragma unroll
-            for (int m = 0; m < 8; ++m) crow[m] = row_of(i * kRows + (tid >> 3) + 8 * m, false);
-          }
+          for (int m = 0; m < 8; ++m) crow[m] = row_of(i * kRows + (tid >> 3) + 8 * m, (tid & 7) == 0);
           // test hook: stop feeding the pipeline; the waits behind it run out
           w_ok = stop_after < 0 || g < static_cast<uint32_t>(stop_after);
           if (tid == 0 && w_ok) {
             if (g >= 2) w_ok = mbar_wait_for(&sh.empty[g & 1], ((g >> 1) - 1) & 1, &sh.abort_flag, status, wait_ns);
-            if (w_ok) mbar_arrive_expect_tx(&sh.full[g & 1], kTmaBlocks * kBlkBytes);
+            if (w_ok) mbar_arrive(&sh.full[g & 1]);
           }
           ok = sync_ok(w_ok);
           if (!ok) break;
           uint8_t* tile = sT + slot_of(g, 0) * kBlkBytes;
+          const int ch = tid & 7;
 #pragma unroll
-          for (int b = b0; b < kTmaBlocks; b += 4)
-            tma_gather4(tile + b * kBlkBytes + grp * (4 * 128), &tmap_kv, &sh.full[g & 1], b * 64, max(rows[0], 0),
-                        max(rows[1], 0), max(rows[2], 0), max(rows[3], 0));
-          if constexpr (kCpBlocks > 0) {
-            const int ch = tid & 7;
+          for (int m = 0; m < 8; ++m) {
+            const int r = (tid >> 3) + 8 * m;
+            const uint16_t* src = kv + static_cast<size_t>(crow[m] >= 0 ? crow[m] : 0) * kDqk + ch * 8;
 #pragma unroll
-            for (int m = 0; m < 8; ++m) {
-              const int r = (tid >> 3) + 8 * m;
-              const uint16_t* src = kv + static_cast<size_t>(crow[m] >= 0 ? crow[m] : 0) * kDqk + ch * 8;
-#pragma unroll
-              for (int b = kTmaBlocks; b < kKB; ++b)
-                cp_async_16_zfill(smem_u32(tile + b * kBlkBytes + sw128(r, ch)), src + b * 64, crow[m] >= 0);
-            }
-            cp_async_mbar_arrive(&sh.full[g & 1]);
+            for (int b = 0; b < kKB; ++b)
+              cp_async_16_zfill(smem_u32(tile + b * kBlkBytes + sw128(r, ch)), src + b * 64, crow[m] >= 0);
           }
+          cp_async_mbar_arrive(&sh.full[g & 1]);
         }
       }
       ++it;
