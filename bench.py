@@ -53,7 +53,7 @@ def parse(argv=None):
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--extras", default=EXTRA_WORKLOADS,
-                    help="comma-separated workloads also measured (device only) under 'workloads'; '' for none")
+                    help="comma-separated workloads also measured (device only) under 'workloads'; 'none' (or '') for none")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -69,7 +69,7 @@ def parse(argv=None):
     ap.add_argument("--paged", action="store_true",
                     help="decode workloads: also time the paged-cache indexer and attention (128-row pages, "
                          "shuffled) against the contiguous calls on the same data, under 'paged'")
-    ap.add_argument("--only", choices=["attn", "indexer"], default=None,
+    ap.add_argument("--only", choices=["attn", "indexer", "indexer_bwd"], default=None,
                     help="run just one kernel call of the workload (for profiler captures); prints nothing")
     ap.add_argument("--n-q", type=int, default=0,
                     help="with --only: that many query rows of the workload instead of all (a smaller capture)")
@@ -706,6 +706,15 @@ def run_only(D, w, args, dev, stream):
     call_idx()
     if args.only == "attn":
         D.dsa_sparse_attn(adesc, L0["q"], L0["kv"], idx0, ks, L0["out"], L0["lse"], stream=stream)
+    elif args.only == "indexer_bwd":
+        g = torch.Generator(device=dev)
+        g.manual_seed(9)
+        d_score = torch.randn((w.n_q, w.topk), generator=g, device=dev)
+        dq = torch.empty((w.n_q, w.n_heads_idx, w.head_dim_idx), dtype=torch.float32, device=dev)
+        dk = torch.empty((geo.n_kv, w.head_dim_idx), dtype=torch.float32, device=dev)
+        dw = torch.empty((w.n_q, w.n_heads_idx), dtype=torch.float32, device=dev)
+        D.dsa_indexer_backward(idesc, L0["q_idx"], L0["k_idx"], L0["w"], q_pos, k_pos, ks, ke, rope, idx0, d_score, dq,
+                               dk, dw, stream=stream)
     else:
         call_idx()
     torch.cuda.synchronize()
@@ -770,7 +779,7 @@ def run_native(args):
     torch.cuda.empty_cache()
 
     # the other workloads, device-resident, fewer steps
-    extras = [x for x in args.extras.split(",") if x and x != args.workload]
+    extras = [x for x in args.extras.split(",") if x and x not in (args.workload, "none")]
     if extras:
         line["workloads"] = {}
         with ClockSampler(local) as clk2:

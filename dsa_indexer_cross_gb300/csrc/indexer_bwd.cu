@@ -54,6 +54,8 @@ struct BwdShared {
   uint32_t tmem_base;
   uint32_t abort_flag;
   alignas(16) float w[2][kHP];   // head weights of the query in each Q slot (0 past n_heads)
+  int32_t idx[2][2048];           // the query's selected offsets, per Q slot
+  float ds[2][2048];              // and their upstream gradients
 };
 
 struct BwdArgs {
@@ -172,9 +174,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1) indexer_bwd_kernel(const BwdAr
         cp_async_16_zfill(smem_u32(&sh.w[qs][tid * 4]), A.w + static_cast<size_t>(t) * A.n_heads + (valid ? tid * 4 : 0),
                           valid);
       }
+      // the query's selected offsets and upstream gradients, staged once (both roles read them
+      // per tile; from global memory each read was a full memory latency)
+      for (int n = tid; n < kt; n += kProdThreads) {
+        cp_async_4(smem_u32(&sh.idx[qs][n]), A.idx + static_cast<size_t>(t) * A.topk + n);
+        cp_async_4(smem_u32(&sh.ds[qs][n]), A.d_score + static_cast<size_t>(t) * A.topk + n);
+      }
       cp_async_mbar_arrive(&sh.q_full[qs]);
       const int len = __ldg(A.ke + t) - __ldg(A.ks + t);
       const int ks_t = __ldg(A.ks + t);
+      // the offsets staged by all producer threads have landed
+      if (!(ok = mbar_wait_for(&sh.q_full[qs], (qc >> 1) & 1, &sh.abort_flag, status, wait_ns))) break;
       for (int i = 0; i < nt && ok; ++i, ++T) {
         const int s = T % kStagesB;
         if (T >= kStagesB &&
@@ -187,7 +197,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) indexer_bwd_kernel(const BwdAr
         for (int m = 0; m < kBKeys / 4; ++m) {
           const int key = (tid >> 4) + 4 * m;
           const int n = i * kBKeys + key;
-          int j = n < kt ? __ldg(A.idx + static_cast<size_t>(t) * A.topk + n) : -1;
+          int j = n < kt ? sh.idx[qs][n] : -1;
           if (j >= len) {
             if (ch == 0) atomicOr(status, DEV_ERR_BAD_INDEX);
             j = -1;
@@ -304,9 +314,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) indexer_bwd_kernel(const BwdAr
       for (int i = 0; i < nt && ok; ++i, ++T) {
         const int b = T & 1;
         const int n = i * kBKeys + row;
-        int j = n < kt ? __ldg(A.idx + static_cast<size_t>(t) * A.topk + n) : -1;
+        int j = n < kt ? sh.idx[qs][n] : -1;
         if (j >= len) j = -1;   // flagged by the producer
-        const float g = j >= 0 ? __ldg(A.d_score + static_cast<size_t>(t) * A.topk + n) : 0.f;
+        const float g = j >= 0 ? sh.ds[qs][n] : 0.f;
         if (!(ok = warp_all_wait(&sh.x_full[b], (T >> 1) & 1, &sh.abort_flag, status, wait_ns))) break;
         tc_fence_after();
         uint32_t xv[kHP];

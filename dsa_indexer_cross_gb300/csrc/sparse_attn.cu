@@ -335,8 +335,9 @@ __global__ void __launch_bounds__(ACfg<HB, HD>::THREADS, 1)
         const int t = I.t0;
         const int32_t* irow = idx + static_cast<size_t>(t) * topk;
         const TokenRows trow = token_rows<PAGED>(pg, ks, t);
-        auto row_of = [&](int slot, bool count_bad) -> int {
-          const int j = slot < topk ? __ldg(irow + slot) : -1;
+        // the index of a slot (-1 past topk), then its latent row (-1: none, flagged if invalid)
+        auto index_of = [&](int slot) -> int { return slot < topk ? __ldg(irow + slot) : -1; };
+        auto row_of = [&](int j, bool count_bad) -> int {
           long long row;
           bool v, bad;
           if constexpr (PAGED) {
@@ -354,10 +355,19 @@ __global__ void __launch_bounds__(ACfg<HB, HD>::THREADS, 1)
           }
           return v ? static_cast<int>(row) : -1;
         };
+        // each tile's indices are loaded one tile ahead, so their latency hides behind the
+        // previous tile's slot wait and copies
+        int jn[8];
+#pragma unroll
+        for (int m = 0; m < 8; ++m) jn[m] = index_of((tid >> 3) + 8 * m);
         for (int i = 0; i < I.nt; ++i, ++g) {
           int crow[8];
 #pragma unroll
-          for (int m = 0; m < 8; ++m) crow[m] = row_of(i * kRows + (tid >> 3) + 8 * m, (tid & 7) == 0);
+          for (int m = 0; m < 8; ++m) crow[m] = row_of(jn[m], (tid & 7) == 0);
+          if (i + 1 < I.nt) {
+#pragma unroll
+            for (int m = 0; m < 8; ++m) jn[m] = index_of((i + 1) * kRows + (tid >> 3) + 8 * m);
+          }
           // test hook: stop feeding the pipeline; the waits behind it run out
           w_ok = stop_after < 0 || g < static_cast<uint32_t>(stop_after);
           if (tid == 0 && w_ok) {
