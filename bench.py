@@ -216,7 +216,13 @@ def roofline_numbers(w, geo):
 # DRAM bytes (read + write) of one launch, from an ncu capture, keyed by (kernel, workload):
 # (bytes, source file of the kernel, SHA-256 prefix of that file when the counters were taken,
 # where the capture is summarised).  A kernel whose source has changed since reports None.
-MEASURED_TRAFFIC = {}
+# chunk_1m's indexer was captured on a 608-query slice (152 of the 1024 key streams; a whole
+# launch is too long for a full-set capture) and is scaled by the 4096 / 608 units: each
+# group streams the same chunks, so the traffic grows with the number of groups.
+MEASURED_TRAFFIC = {
+    ("indexer", "chunk_1m"): ((5.076836e9 + 0.620970e9) * 4096 / 608, "indexer.cu", "77134f039cdf7027",
+                              "profiles/indexer_chunk_1m.md (608-query slice, scaled by 4096/608)"),
+}
 
 
 def _src_sha(rel: str) -> str:
