@@ -338,17 +338,20 @@ cudaError_t launch_sparse_attn_bwd(int n_q, int n_kv, int n_heads, int topk, flo
                                    const float* lse, const void* dout, float* dq, float* dkv, uint32_t* status,
                                    cudaStream_t st) {
   if (n_q <= 0) return cudaSuccess;
-  auto run = [&](auto kernel, int hb, int smem) {
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
+  auto run = [&](auto kernel, int hb, int smem, cudaError_t attr) {
+    if (attr != cudaSuccess) return attr;
     dim3 grid(n_q, (n_heads + hb - 1) / hb);
     kernel<<<grid, kThreads, smem, st>>>(static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(kv), idx, ks,
                                          static_cast<const uint16_t*>(out), lse, static_cast<const uint16_t*>(dout), dq,
                                          dkv, n_kv, n_heads, topk, scale, status, status + 1);
     return cudaGetLastError();
   };
-  if (n_heads <= 16) return run(sparse_attn_bwd_kernel<16>, 16, static_cast<int>(sizeof(BwdSmem<16>)));
-  return run(sparse_attn_bwd_kernel<32>, 32, static_cast<int>(sizeof(BwdSmem<32>)));
+  if (n_heads <= 16) {
+    constexpr int smem = static_cast<int>(sizeof(BwdSmem<16>));
+    return run(sparse_attn_bwd_kernel<16>, 16, smem, smem_attr_once<sparse_attn_bwd_kernel<16>>(smem));
+  }
+  constexpr int smem = static_cast<int>(sizeof(BwdSmem<32>));
+  return run(sparse_attn_bwd_kernel<32>, 32, smem, smem_attr_once<sparse_attn_bwd_kernel<32>>(smem));
 }
 
 }  // namespace dsa

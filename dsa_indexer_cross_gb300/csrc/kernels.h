@@ -8,6 +8,20 @@
 
 namespace dsa {
 
+// Sets Kern's maximum dynamic shared memory once per device (the attribute persists for the
+// device's context, so later launches skip the driver call).
+template <auto Kern>
+inline cudaError_t smem_attr_once(int bytes) {
+  static bool done[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+  e = cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
+  return e;
+}
+
 // Layout of the 256-byte header at the start of every workspace.
 struct WsHeader {
   uint32_t status;       // DEV_ERR_* bits

@@ -250,7 +250,7 @@ cudaError_t launch_projections(const CUtensorMap* ta, const CUtensorMap* tb, con
         (jb.epi == kProjEpiLayerNormF32 && (jb.n_total % 32 || jb.n_tile < jb.n_total + jb.n2)))
       return cudaErrorInvalidValue;
   }
-  cudaError_t e = cudaFuncSetAttribute(proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPDynSmem);
+  cudaError_t e = smem_attr_once<proj_kernel>(kPDynSmem);
   if (e != cudaSuccess) return e;
   const int units = J.first_unit[J.n_jobs];
   const int grid = units < device_sm_count() ? units : device_sm_count();

@@ -15,7 +15,8 @@
 // (at most 2048 buckets over the row; an entry's place is its bucket's start plus the number
 // of smaller indices in its bucket).  Rows with more gathered entries than shared memory holds
 // take the same steps over the buffers in global memory.  Two block shapes: 6144 staged
-// entries and 256 threads where a row's buffers cannot hold more, else 16384 and 512 threads.
+// entries and 256 threads for single-chunk rows and where a row's buffers cannot hold more,
+// else 24576 and 512 threads.
 #include "kernels.h"
 #include "ptx.cuh"
 #include "topk.cuh"
@@ -28,7 +29,7 @@ constexpr int kBoundaryMax = 256;   // boundary-bin entries ranked directly; mor
 constexpr int kSortMax = 2048;      // topk <= 2048
 constexpr int kMaxSeg = 64 * kSub;  // (chunk, sub-buffer) segments of a row
 constexpr int kSmallStage = 6144, kSmallThreads = 256;
-constexpr int kBigStage = 16384, kBigThreads = 512;
+constexpr int kBigStage = 24576, kBigThreads = 512;
 
 template <int STAGE>
 struct SelSmem {
@@ -385,7 +386,11 @@ cudaError_t launch_select(int n_q, int n_chunks, int cap, int topk, int trivial_
                           cudaStream_t st) {
   if (n_q <= 0) return cudaSuccess;
   if (n_chunks > kMaxSeg / kSub || topk > kSortMax || cap % kSub) return cudaErrorInvalidValue;
-  if (static_cast<long long>(n_chunks) * cap <= kSmallStage)
+  // the small shape (two or three CTAs per SM) when a row's buffers cannot hold more than its
+  // stage, or when a row has one chunk: the indexer leaves a filtered row's chunk compacted to
+  // its entries at or above the final threshold (about k + a bin of them), and a row of at
+  // most 4096 keys keeps at most 4096; a row that still gathers more takes the global path
+  if (static_cast<long long>(n_chunks) * cap <= kSmallStage || n_chunks == 1)
     return launch_shape<kSmallStage, kSmallThreads>(n_q, n_chunks, cap, topk, trivial_len, row_range, cand_edge,
                                                     cand_key, cand_idx, cand_cnt, idx_out, score_out, status, st);
   return launch_shape<kBigStage, kBigThreads>(n_q, n_chunks, cap, topk, trivial_len, row_range, cand_edge, cand_key,

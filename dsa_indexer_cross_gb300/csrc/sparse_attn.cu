@@ -871,7 +871,7 @@ cudaError_t launch_cfg(const CUtensorMap& tmap, const CUtensorMap& tmap_q, int n
                        cudaStream_t st) {
   using C = ACfg<HB, HD>;
   auto kern = sparse_attn_kernel<HB, HD, PAGED>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::DYN_SMEM);
+  cudaError_t e = smem_attr_once<sparse_attn_kernel<HB, HD, PAGED>>(C::DYN_SMEM);
   if (e != cudaSuccess) return e;
   const int n_items = C::DENSE ? (n_q + C::B - 1) / C::B : n_q * ((H + HB - 1) / HB);
   const int grid = n_items < device_sm_count() ? n_items : device_sm_count();

@@ -31,7 +31,8 @@ def _built():
 # buffer alternation and dQ accumulated across chunks, k = 136 a ragged last chunk, and the gap
 # rows an all-empty chunk between two selected ones
 @pytest.mark.parametrize("n_q,n_kv,H,topk", [(48, 200, 16, 64), (30, 120, 40, 48), (17, 90, 4, 40),
-                                             (20, 700, 16, 200), (12, 500, 40, 136)])
+                                             (20, 700, 16, 200), (12, 500, 40, 136),
+                                             (8, 300, 64, 128), (6, 300, 128, 128)])   # decode / chunk head counts
 def test_backward_matches_oracle(n_q, n_kv, H, topk):
     rng = np.random.default_rng(n_q + H)
     ks = rng.integers(0, n_kv // 3, size=n_q).astype(np.int32)
@@ -65,6 +66,18 @@ def test_backward_matches_oracle(n_q, n_kv, H, topk):
     dq_ref, dkv_ref = O.sparse_attn_backward(f(q), f(kv), idx, ks, scale, f(d_out))
     assert np.abs(dq.double().cpu().numpy() - dq_ref).max() <= 2e-2 * np.abs(dq_ref).max()
     assert np.abs(dkv.double().cpu().numpy() - dkv_ref).max() <= 2e-2 * np.abs(dkv_ref).max()
+    # per (token, head) row of dq: relative L2 error (the bound above is relative to the largest
+    # gradient and would hide errors confined to small rows).  A row's error comes from D taken
+    # as dO . O from the bf16 output: an error dD moves every ds_j = p_j (dp_j - D) by -p_j dD,
+    # so dq moves by -tau dD sum_j p_j kv_j, whatever the size of the row's own (possibly
+    # cancelling) sum.  Rows whose norm falls below a quarter of the median row norm compare
+    # against that floor; measured worst rows reach ~3.5e-2, typical ones ~2e-3.
+    got = dq.double().cpu().numpy().reshape(n_q * H, -1)
+    ref = dq_ref.reshape(n_q * H, -1)
+    den = np.linalg.norm(ref, axis=1)
+    floor = 0.25 * float(np.median(den[den > 0])) if (den > 0).any() else 1.0
+    rel = np.linalg.norm(got - ref, axis=1) / np.maximum(den, floor)
+    assert rel.max() <= 5e-2, (float(rel.max()), int(rel.argmax()), float(den[rel.argmax()]), floor)
     # an index past the cache is counted and skipped
     bad = idx.copy()
     bad[0, 0] = n_kv + 5
