@@ -222,3 +222,33 @@ def test_indexer_rising_scores_cut_back_the_buffer():
     got = idx.cpu().numpy()
     for n, t in enumerate(rows):
         assert np.array_equal(got[t], ref[n]), f"row {t}"
+
+
+def test_indexer_negative_scores_use_the_signed_histogram():
+    """Head weights all negative make every score <= 0, so each row's k-th largest score is
+    negative: the streaming threshold must rise through the negative half of the histogram
+    (a positive-only map would keep every key and cut its buffers back again and again).  Long
+    filtered rows (over 4096 keys in their chunk), checked against the oracle on sampled rows
+    with the near-tie rule."""
+    from oracle import dsa_oracle as O
+    n_q, n_kv, H, d, topk = 256, 30000, 64, 128, 512
+    g = torch.Generator()
+    g.manual_seed(21)
+    q = (torch.randn((n_q, H, d), generator=g) / d ** 0.5).to(torch.bfloat16)
+    k = (torch.randn((n_kv, d), generator=g) / d ** 0.5).to(torch.bfloat16)
+    w = -torch.rand((n_q, H), generator=g) - 0.05
+    ks = np.zeros(n_q, np.int32)
+    ke = (n_kv - (np.arange(n_q) * 97) % 9000).astype(np.int32)
+    pos = np.arange(n_kv, dtype=np.int32)
+    q_pos = (ke - 1).astype(np.int32)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+    desc = D.indexer_desc(n_q, n_kv, H, d, 0, topk, n_kv, 0)
+    idx = torch.empty((n_q, topk), dtype=torch.int32, device=DEV)
+    ws = D.dsa_indexer_topk(desc, q.to(DEV), k.to(DEV), w.to(DEV), dev(q_pos), dev(pos), dev(ks), dev(ke), None, idx)
+    assert D.dsa_workspace_status(ws) == 0
+    rows = [0, 1, 77, 128, n_q - 1]
+    _, sr = O.indexer_topk(synth.to_f64(q), synth.to_f64(k), synth.to_f64(w), q_pos, pos, ks, ke, 0, 1e4, topk,
+                           rope_q=False, rope_k=False, rows=rows, return_scores=True)
+    assert all(float(np.sort(s)[-topk]) < 0.0 for s in sr), "the k-th largest score should be negative"
+    bad = check_topk(idx.cpu().numpy(), sr, topk, rows)
+    assert not bad, bad
