@@ -69,7 +69,7 @@ def parse(argv=None):
     ap.add_argument("--paged", action="store_true",
                     help="decode workloads: also time the paged-cache indexer and attention (128-row pages, "
                          "shuffled) against the contiguous calls on the same data, under 'paged'")
-    ap.add_argument("--only", choices=["attn", "indexer", "indexer_bwd"], default=None,
+    ap.add_argument("--only", choices=["attn", "indexer", "indexer_bwd", "attn_bwd"], default=None,
                     help="run just one kernel call of the workload (for profiler captures); prints nothing")
     ap.add_argument("--n-q", type=int, default=0,
                     help="with --only: that many query rows of the workload instead of all (a smaller capture)")
@@ -712,6 +712,15 @@ def run_only(D, w, args, dev, stream):
     call_idx()
     if args.only == "attn":
         D.dsa_sparse_attn(adesc, L0["q"], L0["kv"], idx0, ks, L0["out"], L0["lse"], stream=stream)
+    elif args.only == "attn_bwd":
+        g = torch.Generator(device=dev)
+        g.manual_seed(5)
+        D.dsa_sparse_attn(adesc, L0["q"], L0["kv"], idx0, ks, L0["out"], L0["lse"], stream=stream)
+        d_out = torch.randn(L0["out"].shape, generator=g, device=dev).to(torch.bfloat16)
+        dq = torch.empty((w.n_q, w.n_heads, w.d_qk), dtype=torch.float32, device=dev)
+        dkv = torch.empty((geo.n_kv, w.d_qk), dtype=torch.float32, device=dev)
+        D.dsa_sparse_attn_backward(adesc, L0["q"], L0["kv"], idx0, ks, L0["out"], L0["lse"], d_out, dq, dkv,
+                                   stream=stream)
     elif args.only == "indexer_bwd":
         g = torch.Generator(device=dev)
         g.manual_seed(9)
