@@ -180,7 +180,8 @@ bool supported_heads(int h) { return h == 4 || h == 8 || h == 16 || h == 32 || h
 
 struct IndexerLayout {
   IndexerPlan plan{};
-  size_t off_q = 0, off_k = 0, off_rr = 0, off_gr = 0, off_cnt = 0, off_edge = 0, off_key = 0, off_idx = 0, total = 0;
+  size_t off_q = 0, off_k = 0, off_rr = 0, off_gr = 0, off_units = 0, off_cnt = 0, off_edge = 0,
+         off_key = 0, off_idx = 0, total = 0;
 };
 
 dsa_status check_indexer_desc(const dsa_indexer_desc* d) {
@@ -212,6 +213,10 @@ IndexerLayout indexer_layout(const dsa_indexer_desc* d, int sms) {
   // G rows share a key stream: N = G * H_I <= 256 MMA columns, at most 16 rows (the score ring
   // of a unit holds one tile's scores of every row); independent rows fill only 64 columns
   p.group = indep ? (d->n_heads >= 64 ? 1 : 64 / d->n_heads) : std::min(256 / d->n_heads, 16);
+  // independent rows have ranges of unequal length (decode), whose empty (group, chunk) slots
+  // would leave CTAs idle: the kernel walks a dense list of the units that hold keys.  Shared-
+  // prefix groups leave few slots empty and walk every pair in a computed order.
+  p.unit_list = indep;
   p.n_groups = (d->n_q + p.group - 1) / p.group;
   const long long max_len = d->max_len > 0 ? d->max_len : 1;
   // keys one group's union of row ranges can span: a row's own range for prefill-like rows
@@ -253,6 +258,8 @@ IndexerLayout indexer_layout(const dsa_indexer_desc* d, int sms) {
   off += align_up(static_cast<size_t>(d->n_q) * 8);
   L.off_gr = off;
   off += align_up(static_cast<size_t>(p.n_groups) * 8);
+  L.off_units = off;
+  if (p.unit_list) off += align_up(static_cast<size_t>(p.n_groups) * p.n_chunks * 8);
   const size_t slots = static_cast<size_t>(d->n_q) * p.n_chunks;
   L.off_cnt = off;
   off += align_up(slots * kSub * 4);
@@ -331,6 +338,7 @@ dsa_status run_indexer(const dsa_indexer_desc* d, const void* q_idx, const void*
   if (pe) (void)cudaEventRecord(pe->ev[2], st);
   uint32_t* cnt = reinterpret_cast<uint32_t*>(base + L.off_cnt);
   uint32_t* edge = reinterpret_cast<uint32_t*>(base + L.off_edge);
+  int2* units = reinterpret_cast<int2*>(base + L.off_units);
   uint32_t* ck = reinterpret_cast<uint32_t*>(base + L.off_key);
   int32_t* ci = reinterpret_cast<int32_t*>(base + L.off_idx);
   if (d->n_kv > 0) {
@@ -345,9 +353,17 @@ dsa_status run_indexer(const dsa_indexer_desc* d, const void* q_idx, const void*
     if ((s = tmap_bf16(&tki, k_idx, d->head_dim, d->n_kv, 128)) != DSA_OK) return s;
     const int q_split = rq ? rope_split_blocks(d->head_dim, d->rope_dim) : 0;
     const int k_split = rk ? rope_split_blocks(d->head_dim, d->rope_dim) : 0;
+    if (p.unit_list) {
+      // the units that hold keys, densely (a chunk past a group's range is left out and its
+      // rows' counts are zeroed)
+      ps = prof_begin(kProfRanges, st);
+      e = launch_units(gr, p.n_groups, p.n_chunks, p.chunk, p.group, d->n_q, units, cnt, edge, st);
+      prof_end(ps, st);
+      if (e != cudaSuccess) return cuda_fail(e, "unit list");
+    }
     ps = prof_begin(kProfIndexer, st);
     e = launch_indexer(p, tq, tk, tqi, tki, q_split, k_split, pg ? *pg : PagedRows{}, w, d->n_q, rr, gr, trivial_len,
-                       ck, ci, cnt, edge, status, pipeline_debug(), st);
+                       ck, ci, cnt, edge, p.unit_list ? units : nullptr, status, pipeline_debug(), st);
     prof_end(ps, st);
     if (e != cudaSuccess) return cuda_fail(e, "indexer kernel");
   } else {

@@ -151,19 +151,6 @@ struct UnitInfo {
   int group, chunk, kbeg, kend, n_tiles;
 };
 
-__device__ __forceinline__ UnitInfo unit_info(int u, int n_groups, int chunk_len, const int2* group_range) {
-  UnitInfo ui;
-  ui.chunk = u / n_groups;
-  ui.group = n_groups - 1 - (u - ui.chunk * n_groups);  // later (longer) groups first
-  const int2 gr = group_range[ui.group];
-  const long long b = static_cast<long long>(gr.x) + static_cast<long long>(ui.chunk) * chunk_len;
-  const long long e = min(static_cast<long long>(gr.y), b + chunk_len);
-  ui.kbeg = static_cast<int>(b);
-  ui.kend = static_cast<int>(e > b ? e : b);
-  ui.n_tiles = e > b ? static_cast<int>((e - b + kKeyTile - 1) / kKeyTile) : 0;
-  return ui;
-}
-
 // A query's key range within a unit and whether it is scored (rows of at most trivial_len
 // keys are left to the select pass) and filtered (longer than direct_max keys).
 struct QueryRange {
@@ -406,10 +393,39 @@ struct IndexerArgs {
   int32_t* cand_idx;
   uint32_t* cand_cnt;           // [row][chunk][kSub]
   uint32_t* cand_edge;          // per (row, chunk): a key below which no entry can be in the row's top-k (0: none)
+  const int2* units;            // the dense unit list (launch_units), n_groups * n_chunks entries, or null
   uint32_t* status;
   unsigned long long wait_ns;   // bound of every pipeline wait
   int stop_after;               // test hook: the producer stops after this many key tiles (< 0: never)
 };
+
+// Unit u.  LIST: entry u of the dense list (launch_units: (group, chunk) pairs that hold keys,
+// chunk-major, later groups first, then (-1, -1) entries without tiles).  Otherwise the same
+// order over every pair, empty ones included: chunk u / n_groups, later (longer) groups first.
+template <bool LIST>
+__device__ __forceinline__ UnitInfo unit_info(int u, const IndexerArgs& A) {
+  UnitInfo ui;
+  if constexpr (LIST) {
+    const int2 gc = A.units[u];
+    ui.group = gc.x;
+    ui.chunk = gc.y;
+    if (gc.x < 0) {
+      ui.kbeg = ui.kend = ui.n_tiles = 0;
+      return ui;
+    }
+  } else {
+    ui.chunk = u / A.n_groups;
+    ui.group = A.n_groups - 1 - (u - ui.chunk * A.n_groups);
+  }
+  const int2 gr = A.group_range[ui.group];
+  const long long b = static_cast<long long>(gr.x) + static_cast<long long>(ui.chunk) * A.chunk_len;
+  const long long e = min(static_cast<long long>(gr.y), b + A.chunk_len);
+  ui.kbeg = static_cast<int>(b);
+  ui.kend = static_cast<int>(e > b ? e : b);
+  ui.n_tiles = e > b ? static_cast<int>((e - b + kKeyTile - 1) / kKeyTile) : 0;
+  return ui;
+}
+
 
 // Raise query g's boundary bin while the entries strictly above it number k or more; returns
 // the new boundary bin and (in *above) the entries at or above it.  Histogram counts only grow
@@ -431,7 +447,7 @@ __device__ __forceinline__ int climb(const uint32_t* hist, int b, int topk, int*
   return b;
 }
 
-template <int HI, int DI, int G>
+template <int HI, int DI, int G, bool LIST>
 __global__ void __launch_bounds__(Cfg<HI, DI, G>::THREADS, 1)
     indexer_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                    const __grid_constant__ CUtensorMap tmap_q_in, const __grid_constant__ CUtensorMap tmap_k_in,
@@ -505,7 +521,7 @@ __global__ void __launch_bounds__(Cfg<HI, DI, G>::THREADS, 1)
     for (int k = 0; k * static_cast<int>(gridDim.x) < n_units && ok; ++k) {
       const int u = snake_unit(k);
       if (u >= n_units) continue;
-      const UnitInfo ui = unit_info(u, A.n_groups, A.chunk_len, A.group_range);
+      const UnitInfo ui = unit_info<LIST>(u, A);
       if (ui.n_tiles == 0) continue;
       const int par = unit_ord & 1;
       // this unit's histograms and thresholds have been reset
@@ -666,7 +682,7 @@ __global__ void __launch_bounds__(Cfg<HI, DI, G>::THREADS, 1)
         for (int k = 0; k * static_cast<int>(gridDim.x) < n_units && ok; ++k) {
           const int u = snake_unit(k);
           if (u >= n_units) continue;
-          const UnitInfo ui = unit_info(u, A.n_groups, A.chunk_len, A.group_range);
+          const UnitInfo ui = unit_info<LIST>(u, A);
           if (ui.n_tiles == 0) continue;
           if (q_uses > 0) ok = mbar_wait_for(&sh.q_empty, (q_uses - 1) & 1, &sh.abort_flag, status, wait_ns);
           if (!ok) break;
@@ -726,7 +742,7 @@ __global__ void __launch_bounds__(Cfg<HI, DI, G>::THREADS, 1)
       for (int k = 0; k * static_cast<int>(gridDim.x) < n_units && ok; ++k) {
         const int u = snake_unit(k);
         if (u >= n_units) continue;
-        const UnitInfo ui = unit_info(u, A.n_groups, A.chunk_len, A.group_range);
+        const UnitInfo ui = unit_info<LIST>(u, A);
         if (ui.n_tiles == 0) continue;
         ok = wait(&sh.q_full, q_uses & 1);
         if (!ok) break;
@@ -761,16 +777,19 @@ __global__ void __launch_bounds__(Cfg<HI, DI, G>::THREADS, 1)
       for (int k = 0; k * static_cast<int>(gridDim.x) < n_units && ok; ++k) {
         const int u = snake_unit(k);
         if (u >= n_units) continue;
-        const UnitInfo ui = unit_info(u, A.n_groups, A.chunk_len, A.group_range);
+        const UnitInfo ui = unit_info<LIST>(u, A);
         if (ui.n_tiles == 0) {
-          // an empty chunk still tells the final select that it holds no candidates
-          for (int e = lane; e < G * kSub; e += 32) {
-            const int t = ui.group * G + e / kSub;
-            if (t < A.n_q) A.cand_cnt[(static_cast<size_t>(t) * A.n_chunks + ui.chunk) * kSub + (e % kSub)] = 0u;
-          }
-          for (int g = lane; g < G; g += 32) {
-            const int t = ui.group * G + g;
-            if (t < A.n_q) A.cand_edge[static_cast<size_t>(t) * A.n_chunks + ui.chunk] = 0u;
+          // an empty chunk still tells the final select that it holds no candidates (the
+          // unit list has zeroed those counts already and pads with group -1)
+          if constexpr (!LIST) {
+            for (int e = lane; e < G * kSub; e += 32) {
+              const int t = ui.group * G + e / kSub;
+              if (t < A.n_q) A.cand_cnt[(static_cast<size_t>(t) * A.n_chunks + ui.chunk) * kSub + (e % kSub)] = 0u;
+            }
+            for (int g = lane; g < G; g += 32) {
+              const int t = ui.group * G + g;
+              if (t < A.n_q) A.cand_edge[static_cast<size_t>(t) * A.n_chunks + ui.chunk] = 0u;
+            }
           }
           continue;
         }
@@ -838,12 +857,12 @@ __global__ void __launch_bounds__(Cfg<HI, DI, G>::THREADS, 1)
   if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
-template <int HI, int DI, int G>
+template <int HI, int DI, int G, bool LIST>
 cudaError_t launch_t(const IndexerPlan& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tqi,
                      const CUtensorMap& tki, int q_split, int k_split, const PagedRows& pg, const IndexerArgs& A,
                      cudaStream_t st) {
   using C = Cfg<HI, DI, G>;
-  auto kern = indexer_kernel<HI, DI, G>;
+  auto kern = indexer_kernel<HI, DI, G, LIST>;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -871,7 +890,8 @@ cudaError_t launch_t(const IndexerPlan& p, const CUtensorMap& tq, const CUtensor
 cudaError_t launch_indexer(const IndexerPlan& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tqi,
                            const CUtensorMap& tki, int q_split, int k_split, const PagedRows& pg, const float* w, int n_q,
                            const int2* row_range, const int2* group_range, int trivial_len, uint32_t* ck, int32_t* ci,
-                           uint32_t* cc, uint32_t* ce, uint32_t* status, const PipelineDebug& dbg, cudaStream_t st) {
+                           uint32_t* cc, uint32_t* ce, const int2* units, uint32_t* status,
+                           const PipelineDebug& dbg, cudaStream_t st) {
   if (p.n_groups * p.n_chunks == 0) return cudaSuccess;
   if (pg.block_table && (p.group != 1 || p.chunk % kPageRows != 0)) return cudaErrorInvalidValue;
   IndexerArgs A;
@@ -890,30 +910,35 @@ cudaError_t launch_indexer(const IndexerPlan& p, const CUtensorMap& tq, const CU
   A.cand_idx = ci;
   A.cand_cnt = cc;
   A.cand_edge = ce;
+  A.units = units;
   A.status = status;
   A.wait_ns = dbg.wait_ns;
   A.stop_after = dbg.stop_after_tiles;
-#define DSA_IDX_CASE(HI_, DI_, G_)                                                                      \
-  if (p.n_heads == HI_ && p.head_dim == DI_ && p.group == G_)                                           \
-    return launch_t<HI_, DI_, G_>(p, tq, tk, tqi, tki, q_split, k_split, pg, A, st);
-  DSA_IDX_CASE(4, 64, 16)
-  DSA_IDX_CASE(8, 64, 16)
-  DSA_IDX_CASE(16, 64, 16)
-  DSA_IDX_CASE(32, 64, 8)
-  DSA_IDX_CASE(64, 64, 4)
-  DSA_IDX_CASE(4, 128, 16)
-  DSA_IDX_CASE(8, 128, 16)
-  DSA_IDX_CASE(16, 128, 16)
-  DSA_IDX_CASE(32, 128, 8)
-  DSA_IDX_CASE(64, 128, 4)
-  DSA_IDX_CASE(8, 64, 8)
-  DSA_IDX_CASE(16, 64, 4)
-  DSA_IDX_CASE(32, 64, 2)
-  DSA_IDX_CASE(64, 64, 1)
-  DSA_IDX_CASE(8, 128, 8)
-  DSA_IDX_CASE(16, 128, 4)
-  DSA_IDX_CASE(32, 128, 2)
-  DSA_IDX_CASE(64, 128, 1)
+  // shared-prefix groups (G = min(256 / H_I, 16)) walk every (group, chunk) pair; independent
+  // rows (G = 64 / H_I) read the dense unit list
+#define DSA_IDX_CASE(HI_, DI_, G_, LIST_)                                                              \
+  if (p.n_heads == HI_ && p.head_dim == DI_ && p.group == G_ && p.unit_list == LIST_)                 \
+    return launch_t<HI_, DI_, G_, LIST_>(p, tq, tk, tqi, tki, q_split, k_split, pg, A, st);
+  DSA_IDX_CASE(4, 64, 16, false)
+  DSA_IDX_CASE(8, 64, 16, false)
+  DSA_IDX_CASE(16, 64, 16, false)
+  DSA_IDX_CASE(32, 64, 8, false)
+  DSA_IDX_CASE(64, 64, 4, false)
+  DSA_IDX_CASE(4, 128, 16, false)
+  DSA_IDX_CASE(8, 128, 16, false)
+  DSA_IDX_CASE(16, 128, 16, false)
+  DSA_IDX_CASE(32, 128, 8, false)
+  DSA_IDX_CASE(64, 128, 4, false)
+  DSA_IDX_CASE(4, 64, 16, true)
+  DSA_IDX_CASE(8, 64, 8, true)
+  DSA_IDX_CASE(16, 64, 4, true)
+  DSA_IDX_CASE(32, 64, 2, true)
+  DSA_IDX_CASE(64, 64, 1, true)
+  DSA_IDX_CASE(4, 128, 16, true)
+  DSA_IDX_CASE(8, 128, 8, true)
+  DSA_IDX_CASE(16, 128, 4, true)
+  DSA_IDX_CASE(32, 128, 2, true)
+  DSA_IDX_CASE(64, 128, 1, true)
 #undef DSA_IDX_CASE
   return cudaErrorInvalidValue;
 }

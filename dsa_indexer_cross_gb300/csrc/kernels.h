@@ -62,6 +62,7 @@ struct IndexerPlan {
   int cap;                           // candidate capacity per (row, chunk), multiple of 128
   int grid;                          // persistent CTAs
   int topk;
+  bool unit_list;                    // the kernel reads the dense unit list (independent rows)
 };
 
 // Fills row_range[t] = (ks, ke) when valid (ks == nullptr: every range starts at 0), else
@@ -76,6 +77,14 @@ cudaError_t launch_rope_rows_transpose_f32(float* x, const int32_t* pos, int64_t
 cudaError_t launch_ranges(const int32_t* ks, const int32_t* ke, int n_q, int group, int n_kv, int max_len,
                           int trivial_len, long long span_limit, int2* row_range, int2* group_range,
                           uint32_t* status, cudaStream_t st);
+
+// The indexer's work units, listed densely: every (group, chunk) pair whose chunk holds keys
+// of the group's range, chunk-major, later groups first within a chunk, as int2 (group,
+// chunk), followed by (-1, -1) up to n_groups * n_chunks entries.  The candidate counts and
+// edges of every (row, chunk) pair left out are zeroed, so the final select reads them as
+// empty.  One block.
+cudaError_t launch_units(const int2* group_range, int n_groups, int n_chunks, int chunk_len, int group, int n_q,
+                         int2* units, uint32_t* cand_cnt, uint32_t* cand_edge, cudaStream_t st);
 
 // Bound of every pipeline wait and a test hook that stops a kernel's producer after a number
 // of tiles (so the waits behind it run out); see dsa_debug_pipeline.
@@ -106,8 +115,7 @@ cudaError_t launch_indexer(const IndexerPlan& p, const CUtensorMap& tmap_q, cons
                            const CUtensorMap& tmap_q_in, const CUtensorMap& tmap_k_in, int q_split, int k_split,
                            const PagedRows& pg, const float* w, int n_q, const int2* row_range,
                            const int2* group_range, int trivial_len, uint32_t* cand_key, int32_t* cand_idx,
-                           uint32_t* cand_cnt, uint32_t* cand_edge, uint32_t* status, const PipelineDebug& dbg,
-                           cudaStream_t st);
+                           uint32_t* cand_cnt, uint32_t* cand_edge, const int2* units, uint32_t* status, const PipelineDebug& dbg, cudaStream_t st);
 
 // Exact top-k of every row from its candidates; writes offsets (ascending) and -1 padding.
 // Rows of at most trivial_len keys are written as 0..L-1 without reading candidates; entries

@@ -175,6 +175,60 @@ __global__ void __launch_bounds__(256) rope_rows_transpose_f32(float* __restrict
   r[d - half + i] = b * c - a * s;
 }
 
+// Dense unit list, one block of 1024 threads: for every chunk c (outer) the groups whose
+// range reaches into chunk c, last group first, compacted with a block scan; the list's tail,
+// up to n_groups * n_chunks entries, holds (-1, -1).
+__global__ void __launch_bounds__(1024) units_kernel(const int2* __restrict__ group_range, int n_groups, int n_chunks,
+                                                     int chunk_len, int group, int n_q, int2* __restrict__ units,
+                                                     uint32_t* __restrict__ cand_cnt, uint32_t* __restrict__ cand_edge) {
+  __shared__ int wsum[32];
+  __shared__ int base;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  if (tid == 0) base = 0;
+  __syncthreads();
+  for (int c = 0; c < n_chunks; ++c) {
+    for (int g0 = 0; g0 < n_groups; g0 += 1024) {
+      const int gi = g0 + tid;                  // position in "last group first" order
+      const int g = n_groups - 1 - gi;
+      int has = 0;
+      if (gi < n_groups) {
+        const int2 gr = group_range[g];
+        const long long b = static_cast<long long>(gr.x) + static_cast<long long>(c) * chunk_len;
+        has = b < gr.y ? 1 : 0;
+        if (!has) {
+          // an empty (group, chunk): its rows' counts and edges read as empty
+          for (int r = 0; r < group; ++r) {
+            const int t = g * group + r;
+            if (t >= n_q) break;
+            const size_t rc = static_cast<size_t>(t) * n_chunks + c;
+            for (int q = 0; q < kSub; ++q) cand_cnt[rc * kSub + q] = 0u;
+            cand_edge[rc] = 0u;
+          }
+        }
+      }
+      int x = has;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, off);
+        if (lane >= off) x += y;
+      }
+      if (lane == 31) wsum[w] = x;
+      __syncthreads();
+      int before = 0, all = 0;
+      for (int i = 0; i < 32; ++i) {
+        before += i < w ? wsum[i] : 0;
+        all += wsum[i];
+      }
+      if (has) units[base + before + x - 1] = make_int2(g, c);
+      __syncthreads();
+      if (tid == 0) base += all;
+      __syncthreads();
+    }
+  }
+  const int total = n_groups * n_chunks;
+  for (int i = base + tid; i < total; i += 1024) units[i] = make_int2(-1, -1);
+}
+
 }  // namespace
 
 cudaError_t launch_rope_rows(const void* in, void* out, const int32_t* pos, int64_t n_rows, int rows_per_pos, int d,
@@ -213,6 +267,13 @@ cudaError_t launch_rope_rows_transpose_f32(float* x, const int32_t* pos, int64_t
   const int64_t total = n_rows * (rope / 2);
   rope_rows_transpose_f32<<<static_cast<unsigned>((total + 255) / 256), 256, 0, st>>>(x, pos, n_rows, rows_per_pos, d,
                                                                                        rope, cs, n_pos, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_units(const int2* group_range, int n_groups, int n_chunks, int chunk_len, int group, int n_q,
+                         int2* units, uint32_t* cand_cnt, uint32_t* cand_edge, cudaStream_t st) {
+  if (n_groups <= 0 || n_chunks <= 0) return cudaSuccess;
+  units_kernel<<<1, 1024, 0, st>>>(group_range, n_groups, n_chunks, chunk_len, group, n_q, units, cand_cnt, cand_edge);
   return cudaGetLastError();
 }
 
