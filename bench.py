@@ -220,7 +220,7 @@ def roofline_numbers(w, geo):
 # launch is too long for a full-set capture) and is scaled by the 4096 / 608 units: each
 # group streams the same chunks, so the traffic grows with the number of groups.
 MEASURED_TRAFFIC = {
-    ("indexer", "chunk_1m"): ((5.076836e9 + 0.620970e9) * 4096 / 608, "indexer.cu", "77134f039cdf7027",
+    ("indexer", "chunk_1m"): ((5.244348e9 + 0.620581e9) * 4096 / 608, "indexer.cu", "12bbe372616c92c4",
                               "profiles/indexer_chunk_1m.md (608-query slice, scaled by 4096/608)"),
 }
 
