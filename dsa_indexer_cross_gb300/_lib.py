@@ -31,7 +31,8 @@ EXPORTED = ("dsa_status_string", "dsa_last_error", "dsa_donor_table", "dsa_rope_
             "dsa_indexer_topk_static", "dsa_profile_enable", "dsa_profile_indexer_last", "dsa_mtp_indexshare_step",
             "dsa_indexer_topk_paged", "dsa_sparse_attn_paged", "dsa_indexer_projections", "dsa_sparse_attn_backward",
             "dsa_indexer_static_status", "dsa_profile_read", "dsa_debug_pipeline",
-            "dsa_indexer_backward_workspace_size", "dsa_indexer_backward")
+            "dsa_indexer_backward_workspace_size", "dsa_indexer_backward",
+            "dsa_sparse_attn_backward_workspace_size")
 
 PROFILE_KINDS = {0: "rope", 1: "ranges", 2: "indexer", 3: "select", 4: "attn_prep", 5: "attn", 6: "attn_bwd",
                  7: "proj", 8: "indexer_bwd"}
@@ -118,6 +119,8 @@ def lib() -> C.CDLL:
         L.dsa_profile_read.restype = st
         L.dsa_profile_read.argtypes = [P(ProfileRecord), i32, P(i32)]
         L.dsa_sparse_attn_backward.restype = st
+        L.dsa_sparse_attn_backward_workspace_size.restype = st
+        L.dsa_sparse_attn_backward_workspace_size.argtypes = [P(AttnDesc), P(sz)]
         L.dsa_sparse_attn_backward.argtypes = [P(AttnDesc), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.dsa_indexer_backward_workspace_size.restype = st
         L.dsa_indexer_backward_workspace_size.argtypes = [P(IndexerDesc), P(sz)]
@@ -363,6 +366,12 @@ def indexshare_layers_forward(idesc: IndexerDesc, adesc: AttnDesc, indexer_types
     return ws
 
 
+def dsa_sparse_attn_backward_workspace_size(desc: AttnDesc) -> int:
+    n = C.c_size_t(0)
+    _check(lib().dsa_sparse_attn_backward_workspace_size(C.byref(desc), C.byref(n)))
+    return n.value
+
+
 def dsa_sparse_attn_backward(desc: AttnDesc, q, kv, idx, ks, out, lse, d_out, dq, dkv, ws=None, stream=None):
     """dq (written) and dkv (zeroed, then accumulated), fp32, for the upstream gradient d_out."""
     n_q, n_kv, H, k = desc.n_q, desc.n_kv, desc.n_heads, desc.topk
@@ -373,7 +382,7 @@ def dsa_sparse_attn_backward(desc: AttnDesc, q, kv, idx, ks, out, lse, d_out, dq
                            (dkv, f32, n_kv * desc.d_qk, "dkv")):
         _want(t, dt, n, name)
     if ws is None:
-        ws = torch.zeros(256, dtype=torch.uint8, device=q.device)
+        ws = torch.empty(dsa_sparse_attn_backward_workspace_size(desc), dtype=torch.uint8, device=q.device)
     _check(lib().dsa_sparse_attn_backward(C.byref(desc), _ptr(q), _ptr(kv), _ptr(idx), _ptr(ks), _ptr(out), _ptr(lse),
                                           _ptr(d_out), _ptr(dq), _ptr(dkv), _ptr(ws), ws.numel(), _stream(stream)))
     return ws

@@ -17,7 +17,7 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "-diag-suppress", "177", f"-I{os.path.join(ROOT, 'include')}"]
 SOURCES = ["api.cu", "rope.cu", "indexer.cu", "select.cu", "sparse_attn.cu", "static_scratch.cu", "proj.cu", "attn_bwd.cu",
-           "indexer_bwd.cu"]
+           "attn_bwd_tc.cu", "indexer_bwd.cu"]
 
 
 def nvcc() -> str:

@@ -830,6 +830,24 @@ dsa_status dsa_indexer_projections(const dsa_proj_desc* d, const void* x, const 
   return DSA_OK;
 }
 
+namespace {
+// Backward workspace: the status header, then for the block-dense walk D = d_out . out per
+// (token, head) and the walk's key ranges and selection bitmasks.
+size_t attn_bwd_ws_bytes(const dsa_attn_desc* d) {
+  if (!sparse_attn_dense_heads(d->n_heads, d->n_kv, d->topk)) return kAlign;
+  return kAlign + align_up(sparse_attn_bwd_dense_delta_bytes(d->n_q, d->n_heads)) +
+         align_up(sparse_attn_ws_bytes(d->n_q, d->n_heads, d->n_kv, d->topk));
+}
+}  // namespace
+
+dsa_status dsa_sparse_attn_backward_workspace_size(const dsa_attn_desc* desc, size_t* bytes) {
+  dsa_status s = check_attn_desc(desc);
+  if (s != DSA_OK) return s;
+  if (!bytes) return fail(DSA_ERR_ARG, "bytes is NULL");
+  *bytes = attn_bwd_ws_bytes(desc);
+  return DSA_OK;
+}
+
 dsa_status dsa_sparse_attn_backward(const dsa_attn_desc* desc, const void* q, const void* kv, const int32_t* idx,
                                     const int32_t* ks, const void* out, const float* lse, const void* d_out,
                                     float* dq, float* dkv, void* ws, size_t ws_bytes, void* stream) {
@@ -840,7 +858,8 @@ dsa_status dsa_sparse_attn_backward(const dsa_attn_desc* desc, const void* q, co
   if (!aligned16(q) || !aligned16(kv) || !aligned16(out) || !aligned16(d_out) || !aligned16(dq) || !aligned16(dkv))
     return fail(DSA_ERR_ARG, "q, kv, out, d_out, dq and dkv must be 16-byte aligned");
   if (reinterpret_cast<uintptr_t>(ws) % kAlign) return fail(DSA_ERR_ARG, "workspace must be 256-byte aligned");
-  if (ws_bytes < kAlign) return fail(DSA_ERR_WORKSPACE, "backward workspace too small: %zu < %zu bytes", ws_bytes, kAlign);
+  const size_t need = attn_bwd_ws_bytes(desc);
+  if (ws_bytes < need) return fail(DSA_ERR_WORKSPACE, "backward workspace too small: %zu < %zu bytes", ws_bytes, need);
   if ((s = check_device()) != DSA_OK) return s;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
@@ -849,9 +868,27 @@ dsa_status dsa_sparse_attn_backward(const dsa_attn_desc* desc, const void* q, co
       (e = cudaMemsetAsync(dkv, 0, static_cast<size_t>(desc->n_kv) * 576 * sizeof(float), st)) != cudaSuccess)
     return cuda_fail(e, "clear dkv");
   if (desc->n_q == 0) return DSA_OK;
+  uint32_t* status = static_cast<uint32_t*>(ws);
+  const int hd = sparse_attn_dense_heads(desc->n_heads, desc->n_kv, desc->topk);
+  if (hd) {
+    // block-dense walk on tcgen05: kv as whole 64-row tiles, q and d_out as 64-row boxes
+    CUtensorMap tkv, tq, tdo;
+    std::memset(&tkv, 0, sizeof(tkv));
+    if (desc->n_kv > 0 && (s = tmap_kv_tiles(&tkv, kv, desc->n_kv)) != DSA_OK) return s;
+    const uint64_t rows = static_cast<uint64_t>(desc->n_q) * desc->n_heads;
+    if ((s = tmap_bf16(&tq, q, 576, rows, kDenseCols)) != DSA_OK) return s;
+    if ((s = tmap_bf16(&tdo, d_out, 512, rows, kDenseCols)) != DSA_OK) return s;
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    float* delta = reinterpret_cast<float*>(base + kAlign);
+    void* scratch = base + kAlign + align_up(sparse_attn_bwd_dense_delta_bytes(desc->n_q, desc->n_heads));
+    e = launch_sparse_attn_bwd_dense(hd, tkv, tq, tdo, desc->n_q, desc->n_kv, desc->topk, desc->softmax_scale, idx, ks,
+                                     out, lse, d_out, dq, dkv, status, delta, scratch, st);
+    if (e != cudaSuccess) return cuda_fail(e, "sparse attention backward (block-dense)");
+    return DSA_OK;
+  }
   const int ps = prof_begin(kProfAttnBwd, st);
   e = launch_sparse_attn_bwd(desc->n_q, desc->n_kv, desc->n_heads, desc->topk, desc->softmax_scale, q, kv, idx, ks, out,
-                             lse, d_out, dq, dkv, static_cast<uint32_t*>(ws), st);
+                             lse, d_out, dq, dkv, status, st);
   prof_end(ps, st);
   if (e != cudaSuccess) return cuda_fail(e, "sparse attention backward");
   return DSA_OK;

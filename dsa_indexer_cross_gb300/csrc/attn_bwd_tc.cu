@@ -1,0 +1,512 @@
+// Backward of the MLA-absorbed sparse attention on the block-dense walk, on tcgen05.
+//
+// The same gradients as the per-token kernel (attn_bwd.cu): for column c = (token, head) and a
+// selected latent row j,
+//   p = exp(tau q_c . kv_j - lse_c),  dp = d_o_c . kv_j[:512],  ds' = tau p (dp - D_c),
+//   dq_c += ds' kv_j,  dkv_j += ds' q_c + p d_o_c (first 512 dims),
+// with D_c = d_o_c . o_c from the forward's output.  ("GLM-5/5.1/5.2 DSA + LoRA enablement",
+// Megatron-Bridge pull request #15, names a backward for the fused sparse-MLA kernel without
+// defining it; this is the exact gradient of the forward.)
+//
+// Work item = the forward's block-dense item: 64 columns (64 / H consecutive tokens with all
+// H heads) and the union of their key ranges, walked in tiles of 64 consecutive latent rows
+// (one 72 KB 3-D TMA box) with the per-(token, row) selection bitmask of the pre-pass.  Per
+// tile, with the rows on the M side wherever the columns are too few for it:
+//   S^T  [64 rows x 64 cols]  = Rows . Q^T           M = 64,  N = 64, K = 576   (TMEM)
+//   dP^T [64 rows x 64 cols]  = Rows[:, :512] . dO^T M = 64,  N = 64, K = 512   (TMEM)
+//   softmax warps: P and dS' per (row, col), bf16, into two 8 KB blocks laid out [row][col]
+//   dQ^T [576 dims x 64 cols] += Rows^T . dS'^T      M = 128 per dim chunk, K = 64 rows
+//   dKV^T piece [128 dims x 32 rows] = Q^T . dS' (+ dO^T . P)   K = 64 cols
+// The [row][col] blocks are read as the MN-major B of dQ^T and as the K-major B of the dKV^T
+// pieces (the same bytes); Q and dO stay in shared memory as K-major B operands of the first
+// two products and as MN-major A operands of the pieces.  576 dims are five 128-dim chunks,
+// the last one starting at dim 448 (its first 64 lanes repeat chunk 3 and are ignored), so
+// no operand reads past its tile.  dQ^T (320 TMEM columns) accumulates over the item and is
+// written once; each dKV^T piece (two 32-column TMEM slots) is drained by four warps with
+// fp32 reductions into dkv, the 64 columns of the item summed first.  TMEM: S^T 64 + dP^T 64
+// + dQ^T 320 + pieces 64 = 512 columns; shared memory: Q 72 KB + dO 64 KB + tile 72 KB + P
+// and dS' 16 KB.
+//
+// Warp roles (512 threads): warp 0 loads (TMA), warp 1 owns TMEM and issues every MMA, warps
+// 4-7 drain the dKV^T pieces and dQ^T, warps 8-15 run the softmax (two per TMEM lane quarter,
+// 32 columns each).  Every wait is bounded; a timeout sets the CTA's abort flag and the
+// device status, and every role then leaves its loop.
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace dsa {
+namespace {
+
+constexpr int kR = 64;                      // latent rows per tile
+constexpr int kC = kDenseCols;              // columns per item
+constexpr int kDqk = 576, kDv = 512;
+constexpr int kQB = kDqk / 64, kVB = kDv / 64;
+constexpr int kBlk = 64 * 128;              // one 64 x 128-byte block
+constexpr int kMaskWords = kDenseMaskBytes / 4;
+static_assert(kC == 64, "the [row][col] blocks hold 64 columns in one 128-byte row");
+
+constexpr uint32_t kColS = 0, kColDP = 64, kColDQ = 128, kColKV = 448, kTmemCols = 512;
+
+constexpr int kOffQ = 0;
+constexpr int kOffDO = kOffQ + kQB * kBlk;
+constexpr int kOffR = kOffDO + kVB * kBlk;
+constexpr int kOffP = kOffR + kQB * kBlk;
+constexpr int kOffDS = kOffP + kBlk;
+constexpr int kDynSmem = 1024 + kOffDS + kBlk;   // + alignment slack for the 1024-byte swizzle atoms
+
+constexpr int kThreads = 512;
+constexpr int kSoftWarps = 8, kDrainWarps = 4;
+
+struct BShared {
+  uint64_t q_full, q_empty, full, empty, s_full, s_empty, p_full;
+  uint64_t kv_full[2], kv_empty[2], dq_full, dq_empty, mma_done;
+  uint32_t tmem_base, abort_flag;
+};
+static_assert(kDynSmem + sizeof(BShared) <= 232448, "backward tile set must fit in shared memory");
+
+// first dim of 128-dim chunk m (the last chunk overlaps the previous one by 64 dims)
+__device__ __forceinline__ constexpr int chunk_dim0(int m) { return m < 4 ? 128 * m : 448; }
+
+__device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ void red_add_f32(float* p, float v) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+}
+
+// D = d_out . out per (token, head) row, one warp per row (bf16 inputs, fp32 sum).
+__global__ void __launch_bounds__(256) attn_bwd_delta_kernel(const uint16_t* __restrict__ out,
+                                                             const uint16_t* __restrict__ dout, long long n_rows,
+                                                             float* __restrict__ delta) {
+  const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= n_rows) return;
+  const uint4* o4 = reinterpret_cast<const uint4*>(out + row * kDv);
+  const uint4* d4 = reinterpret_cast<const uint4*>(dout + row * kDv);
+  float acc = 0.f;
+#pragma unroll
+  for (int i = 0; i < kDv / 8 / 32; ++i) {
+    const uint4 a = __ldg(o4 + lane + 32 * i), b = __ldg(d4 + lane + 32 * i);
+    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 x = __bfloat1622float2(a2[k]), y = __bfloat1622float2(b2[k]);
+      acc = fmaf(x.x, y.x, acc);
+      acc = fmaf(x.y, y.y, acc);
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (lane == 0) delta[row] = acc;
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_bwd_dense_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_constant__ CUtensorMap tmap_q,
+                          const __grid_constant__ CUtensorMap tmap_do, const int2* __restrict__ block_range,
+                          const uint32_t* __restrict__ block_mask, const float* __restrict__ lse,
+                          const float* __restrict__ delta, float* __restrict__ dq, float* __restrict__ dkv, int n_q,
+                          float scale, float scale_log2, uint32_t* status, unsigned long long wait_ns) {
+  constexpr int B = kC / HD;                          // tokens per item
+  constexpr int RW = kDenseMaskBytes * 8 / B / 32;    // mask words per token
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ BShared sh;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem + kOffQ;
+  uint8_t* sDO = smem + kOffDO;
+  uint8_t* sR = smem + kOffR;
+  uint8_t* sP = smem + kOffP;
+  uint8_t* sDS = smem + kOffDS;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int n_items = (n_q + B - 1) / B;
+  // causal items grow with their index: alternate directions so the CTAs balance
+  auto snake_item = [&](int k) {
+    const int gdim = static_cast<int>(gridDim.x), b = static_cast<int>(blockIdx.x);
+    return k * gdim + ((k & 1) ? (gdim - 1 - b) : b);
+  };
+  auto item_tiles = [&](int item, int& lo) {
+    const int2 r = __ldg(block_range + item);
+    lo = r.x;
+    return r.y > r.x ? (r.y - r.x + kR - 1) / kR : 0;
+  };
+
+  if (threadIdx.x == 0) {
+    mbar_init(&sh.q_full, 1);
+    mbar_init(&sh.q_empty, 1);
+    mbar_init(&sh.full, 1);
+    mbar_init(&sh.empty, 1);
+    mbar_init(&sh.s_full, 1);
+    mbar_init(&sh.s_empty, kSoftWarps);
+    mbar_init(&sh.p_full, kSoftWarps);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&sh.kv_full[s], 1);
+      mbar_init(&sh.kv_empty[s], kDrainWarps);
+    }
+    mbar_init(&sh.dq_full, 1);
+    mbar_init(&sh.dq_empty, kDrainWarps);
+    mbar_init(&sh.mma_done, 1);
+    sh.abort_flag = 0;
+    fence_mbar_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 1) {
+    tmem_alloc(&sh.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sh.tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ loads (one thread)
+    if (lane == 0) {
+      uint32_t g = 0, it = 0;
+      bool ok = true;
+      for (int k = 0; k * static_cast<int>(gridDim.x) < n_items && ok; ++k) {
+        const int item = snake_item(k);
+        if (item >= n_items) continue;
+        int lo;
+        const int nt = item_tiles(item, lo);
+        if (nt == 0) continue;
+        if (it > 0 && !(ok = mbar_wait_for(&sh.q_empty, (it - 1) & 1, &sh.abort_flag, status, wait_ns))) break;
+        // the item's 64 (token, head) rows of q and d_out; rows past the end read as zeros
+        const int qrow = item * kC;
+        mbar_arrive_expect_tx(&sh.q_full, (kQB + kVB) * kBlk);
+#pragma unroll 1
+        for (int kb = 0; kb < kQB; ++kb) tma_load_2d(sQ + kb * kBlk, &tmap_q, &sh.q_full, kb * 64, qrow);
+#pragma unroll 1
+        for (int kb = 0; kb < kVB; ++kb) tma_load_2d(sDO + kb * kBlk, &tmap_do, &sh.q_full, kb * 64, qrow);
+        for (int i = 0; i < nt; ++i, ++g) {
+          if (g > 0 && !(ok = mbar_wait_for(&sh.empty, (g - 1) & 1, &sh.abort_flag, status, wait_ns))) break;
+          mbar_arrive_expect_tx(&sh.full, kQB * kBlk);
+          tma_load_3d(sR, &tmap_kv, &sh.full, 0, lo + i * kR, 0);
+        }
+        ++it;
+      }
+      // copies in flight land before the CTA's shared memory is released
+      if (it > 0) mbar_drain(&sh.q_full, (it - 1) & 1, 200000000ull);
+      if (g > 0) mbar_drain(&sh.full, (g - 1) & 1, 200000000ull);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    constexpr uint32_t id_s = idesc_bf16_f32(64, kC, 0, 0);
+    constexpr uint32_t id_dq = idesc_bf16_f32(128, kC, 1, 1);
+    constexpr uint32_t id_kv = idesc_bf16_f32(128, 32, 1, 0);
+    const uint64_t dR_k = sdesc_sw128(smem_u32(sR), 16, 1024);      // rows, K-major (A of S^T, dP^T)
+    const uint64_t dQ_k = sdesc_sw128(smem_u32(sQ), 16, 1024);      // q, K-major (B of S^T)
+    const uint64_t dO_k = sdesc_sw128(smem_u32(sDO), 16, 1024);     // d_out, K-major (B of dP^T)
+    const uint64_t dR_mn = sdesc_sw128(smem_u32(sR), kBlk, 1024);   // rows^T, MN-major (A of dQ^T)
+    const uint64_t dDS_mn = sdesc_sw128(smem_u32(sDS), kBlk, 1024); // dS'^T, MN-major (B of dQ^T)
+    const uint64_t dQ_mn = sdesc_sw128(smem_u32(sQ), kBlk, 1024);   // q^T, MN-major (A of dKV^T)
+    const uint64_t dO_mn = sdesc_sw128(smem_u32(sDO), kBlk, 1024);  // d_out^T, MN-major (A of dKV^T)
+    const uint64_t dDS_k = sdesc_sw128(smem_u32(sDS), 16, 1024);    // dS', K-major (B of dKV^T)
+    const uint64_t dP_k = sdesc_sw128(smem_u32(sP), 16, 1024);      // P, K-major (B of dKV^T)
+    auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+      return __all_sync(0xffffffffu, mbar_wait_for(bar, parity, &sh.abort_flag, status, wait_ns));
+    };
+    uint32_t g = 0, it = 0, pc = 0;
+    bool ok = true;
+    for (int k = 0; k * static_cast<int>(gridDim.x) < n_items && ok; ++k) {
+      const int item = snake_item(k);
+      if (item >= n_items) continue;
+      int lo;
+      const int nt = item_tiles(item, lo);
+      if (nt == 0) continue;
+      if (!(ok = wait(&sh.q_full, it & 1))) break;
+      for (int i = 0; i < nt && ok; ++i, ++g) {
+        if (!(ok = wait(&sh.full, g & 1))) break;
+        if (g > 0 && !(ok = wait(&sh.s_empty, (g - 1) & 1))) break;
+        tc_fence_after();
+        // S^T and dP^T share each 64-dim block of the tile
+#pragma unroll
+        for (int kb = 0; kb < kQB; ++kb) {
+#pragma unroll
+          for (int sub = 0; sub < 4; ++sub) {
+            const uint64_t off = static_cast<uint64_t>((kb * kBlk + sub * 32) >> 4);
+            const uint32_t acc = (kb | sub) ? 1u : 0u;
+            umma_bf16_elect(tmem + kColS, dR_k + off, dQ_k + off, id_s, acc);
+            if (kb < kVB) umma_bf16_elect(tmem + kColDP, dR_k + off, dO_k + off, id_s, acc);
+          }
+        }
+        umma_commit_elect(&sh.s_full);
+        if (!(ok = wait(&sh.p_full, g & 1))) break;
+        if (i == 0 && it > 0 && !(ok = wait(&sh.dq_empty, (it - 1) & 1))) break;
+        tc_fence_after();
+        // dQ^T += Rows^T dS'^T, five 128-dim chunks, K = the tile's 64 rows
+#pragma unroll
+        for (int m = 0; m < 5; ++m) {
+#pragma unroll
+          for (int kq = 0; kq < kR / 16; ++kq)
+            umma_bf16_elect(tmem + kColDQ + m * kC,
+                            dR_mn + static_cast<uint64_t>(((chunk_dim0(m) / 64) * kBlk + kq * 2048) >> 4),
+                            dDS_mn + static_cast<uint64_t>((kq * 2048) >> 4), id_dq, (i > 0 || kq > 0) ? 1u : 0u);
+        }
+        umma_commit_elect(&sh.empty);              // the tile may be refilled
+        if (i == nt - 1) umma_commit_elect(&sh.dq_full);
+        // dKV^T pieces: dims chunk m x rows half h, K = the item's 64 columns
+#pragma unroll 1
+        for (int m = 0; m < 5 && ok; ++m) {
+#pragma unroll 1
+          for (int h = 0; h < 2 && ok; ++h, ++pc) {
+            const int slot = pc & 1;
+            if (pc >= 2 && !(ok = wait(&sh.kv_empty[slot], ((pc >> 1) - 1) & 1))) break;
+            tc_fence_after();
+            const uint32_t d_kv = tmem + kColKV + slot * 32;
+            const uint32_t a_off = static_cast<uint32_t>((chunk_dim0(m) / 64) * kBlk);
+#pragma unroll
+            for (int kq = 0; kq < kC / 16; ++kq)
+              umma_bf16_elect(d_kv, dQ_mn + static_cast<uint64_t>((a_off + kq * 2048) >> 4),
+                              dDS_k + static_cast<uint64_t>((h * 32 * 128 + kq * 32) >> 4), id_kv, kq > 0 ? 1u : 0u);
+            if (m < 4) {
+#pragma unroll
+              for (int kq = 0; kq < kC / 16; ++kq)
+                umma_bf16_elect(d_kv, dO_mn + static_cast<uint64_t>((a_off + kq * 2048) >> 4),
+                                dP_k + static_cast<uint64_t>((h * 32 * 128 + kq * 32) >> 4), id_kv, 1u);
+            }
+            umma_commit_elect(&sh.kv_full[slot]);
+          }
+        }
+      }
+      if (ok) umma_commit_elect(&sh.q_empty);      // q and d_out may be replaced once these finish
+      ++it;
+    }
+    // every MMA issued here has completed before TMEM is released
+    umma_commit_elect(&sh.mma_done);
+    mbar_drain(&sh.mma_done, 0, 200000000ull);
+  } else if (warp >= 4 && warp < 8) {
+    // ------------------------------------------------------------------ drains: dKV^T pieces, dQ^T
+    const int qd = warp & 3;
+    const uint32_t t_lane = static_cast<uint32_t>(qd * 32) << 16;
+    uint32_t g = 0, it = 0, pc = 0;
+    bool ok = true;
+    for (int k = 0; k * static_cast<int>(gridDim.x) < n_items && ok; ++k) {
+      const int item = snake_item(k);
+      if (item >= n_items) continue;
+      int lo;
+      const int nt = item_tiles(item, lo);
+      const int n_cols = min(kC, (n_q - item * B) * HD);   // columns of real tokens
+      float* dq_item = dq + static_cast<size_t>(item) * kC * kDqk;
+      if (nt == 0) {
+        // nothing selected: zero gradients for the item's rows of dq
+        for (int e = (warp - 4) * 32 + lane; e < n_cols * kDqk; e += kDrainWarps * 32) dq_item[e] = 0.f;
+        continue;
+      }
+      for (int i = 0; i < nt && ok; ++i, ++g) {
+        // rows of the tile some column selects (the others add nothing to dkv)
+        uint32_t any_lo = 0u, any_hi = 0u;
+        for (int b = lane; b < B; b += 32) {
+          const uint2 w = __ldg(reinterpret_cast<const uint2*>(block_mask + static_cast<size_t>(item) * kMaskWords +
+                                                               b * RW + 2 * i));
+          any_lo |= w.x;
+          any_hi |= w.y;
+        }
+        any_lo = __reduce_or_sync(0xffffffffu, any_lo);
+        any_hi = __reduce_or_sync(0xffffffffu, any_hi);
+        const long long row0 = static_cast<long long>(lo) + static_cast<long long>(i) * kR;
+#pragma unroll 1
+        for (int m = 0; m < 5 && ok; ++m) {
+#pragma unroll 1
+          for (int h = 0; h < 2; ++h, ++pc) {
+            const int slot = pc & 1;
+            ok = __all_sync(0xffffffffu,
+                            mbar_wait_for(&sh.kv_full[slot], (pc >> 1) & 1, &sh.abort_flag, status, wait_ns));
+            if (!ok) break;
+            tc_fence_after();
+            const bool mine = m < 4 || qd >= 2;     // chunk 4's first 64 lanes repeat chunk 3
+            uint32_t v[32];
+            if (mine) {
+              tmem_ld32(tmem + t_lane + kColKV + slot * 32, v);
+              tmem_ld_wait();
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.kv_empty[slot]);
+            if (mine) {
+              const uint32_t any = h ? any_hi : any_lo;
+              float* col = dkv + (row0 + 32 * h) * kDqk + chunk_dim0(m) + 32 * qd + lane;
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if ((any >> j) & 1u) red_add_f32(col + static_cast<size_t>(j) * kDqk, __uint_as_float(v[j]));
+            }
+          }
+        }
+      }
+      if (!ok) break;
+      // the item's dQ^T, written once: lane = dim, TMEM column = (token, head) column
+      ok = __all_sync(0xffffffffu, mbar_wait_for(&sh.dq_full, it & 1, &sh.abort_flag, status, wait_ns));
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll 1
+      for (int m = 0; m < 5; ++m) {
+        if (m == 4 && qd < 2) continue;
+        const int d = chunk_dim0(m) + 32 * qd + lane;
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
+          uint32_t v[32];
+          tmem_ld32(tmem + t_lane + kColDQ + m * kC + half * 32, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int c = half * 32 + j;
+            if (c < n_cols) dq_item[static_cast<size_t>(c) * kDqk + d] = __uint_as_float(v[j]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.dq_empty);
+      ++it;
+    }
+  } else if (warp >= 8) {
+    // ------------------------------------------------------------------ softmax: P and dS'
+    const int qd = warp & 3;                  // TMEM lane quarter
+    const int c_off = warp >= 12 ? 32 : 0;    // this warp's 32 columns
+    const int r0 = qd * 16 + (lane >> 2);     // S^T rows held: r0 and r0 + 8
+    const int cq = 2 * (lane & 3);            // column pair within each group of 8
+    const uint32_t t_lane = static_cast<uint32_t>(qd * 32) << 16;
+    const uint32_t p_base = smem_u32(sP), ds_base = smem_u32(sDS);
+    uint32_t g = 0;
+    bool ok = true;
+    for (int k = 0; k * static_cast<int>(gridDim.x) < n_items && ok; ++k) {
+      const int item = snake_item(k);
+      if (item >= n_items) continue;
+      int lo;
+      const int nt = item_tiles(item, lo);
+      if (nt == 0) continue;
+      // this thread's eight columns: c = c_off + 8 kk + cq + e
+      float l2[8], dd[8];
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int c = c_off + 8 * kk + cq + e;
+          const bool real = item * B + c / HD < n_q;
+          const size_t row = static_cast<size_t>(item) * kC + c;
+          l2[2 * kk + e] = real ? __ldg(lse + row) * 1.4426950408889634f : 0.f;
+          dd[2 * kk + e] = real ? __ldg(delta + row) : 0.f;
+        }
+      }
+      const uint32_t* mrow = block_mask + static_cast<size_t>(item) * kMaskWords;
+      for (int i = 0; i < nt; ++i, ++g) {
+        // selection bits of rows r0 and r0 + 8 for each column's token (e = 0, 1 share a token
+        // unless there is one head)
+        uint2 mw[4][2];
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            if (e == 0 || HD == 1) {
+              const int b = (c_off + 8 * kk + cq + e) / HD;
+              mw[kk][e] = __ldg(reinterpret_cast<const uint2*>(mrow + b * RW + 2 * i));
+            } else {
+              mw[kk][e] = mw[kk][0];
+            }
+          }
+        }
+        ok = __all_sync(0xffffffffu, mbar_wait_for(&sh.s_full, g & 1, &sh.abort_flag, status, wait_ns));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t vs[16], vd[16];
+        tmem_ld_16x256b<4>(tmem + t_lane + kColS + c_off, vs);
+        tmem_ld_16x256b<4>(tmem + t_lane + kColDP + c_off, vd);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.s_empty);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const int chunk = c_off / 8 + kk;   // 16-byte chunk of the 128-byte [row] line
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int r = r0 + 8 * hh;
+            float p[2], ds[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const uint2 w = mw[kk][e];
+              const bool sel = (((r < 32 ? w.x : w.y) >> (r & 31)) & 1u) != 0u;
+              const float s = __uint_as_float(vs[4 * kk + 2 * hh + e]);
+              const float dp = __uint_as_float(vd[4 * kk + 2 * hh + e]);
+              p[e] = sel ? ex2_approx(s * scale_log2 - l2[2 * kk + e]) : 0.f;
+              ds[e] = sel ? scale * p[e] * (dp - dd[2 * kk + e]) : 0.f;
+            }
+            const uint32_t off = static_cast<uint32_t>(r * 128 + ((chunk ^ (r & 7)) << 4) + cq * 2);
+            const __nv_bfloat162 pb = __floats2bfloat162_rn(p[0], p[1]);
+            const __nv_bfloat162 db = __floats2bfloat162_rn(ds[0], ds[1]);
+            st_shared_u32(p_base + off, *reinterpret_cast<const uint32_t*>(&pb));
+            st_shared_u32(ds_base + off, *reinterpret_cast<const uint32_t*>(&db));
+          }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.p_full);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+template <int HD>
+cudaError_t launch_hd(const CUtensorMap& tmap_kv, const CUtensorMap& tmap_q, const CUtensorMap& tmap_do, int n_q,
+                      float scale, const DenseScratch& ds, const float* lse, const float* delta, float* dq, float* dkv,
+                      uint32_t* status, cudaStream_t st) {
+  cudaError_t e = smem_attr_once<attn_bwd_dense_kernel<HD>>(kDynSmem);
+  if (e != cudaSuccess) return e;
+  constexpr int B = kC / HD;
+  const int n_items = (n_q + B - 1) / B;
+  const int grid = n_items < device_sm_count() ? n_items : device_sm_count();
+  attn_bwd_dense_kernel<HD><<<grid, kThreads, kDynSmem, st>>>(tmap_kv, tmap_q, tmap_do, ds.block_range,
+                                                             ds.block_mask, lse, delta, dq, dkv, n_q, scale,
+                                                             scale * 1.4426950408889634f, status,
+                                                             pipeline_debug().wait_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t sparse_attn_bwd_dense_delta_bytes(int n_q, int n_heads) {
+  return static_cast<size_t>(n_q) * static_cast<size_t>(n_heads) * sizeof(float);
+}
+
+cudaError_t launch_sparse_attn_bwd_dense(int hd, const CUtensorMap& tmap_kv, const CUtensorMap& tmap_q,
+                                         const CUtensorMap& tmap_do, int n_q, int n_kv, int topk, float scale,
+                                         const int32_t* idx, const int32_t* ks, const void* out, const float* lse,
+                                         const void* dout, float* dq, float* dkv, uint32_t* status, float* delta,
+                                         void* scratch, cudaStream_t st) {
+  if (n_q <= 0) return cudaSuccess;
+  const DenseScratch ds = dense_scratch(scratch, n_q, hd);
+  const long long n_rows = static_cast<long long>(n_q) * hd;
+  int ps = prof_begin(kProfAttnPrep, st);
+  attn_bwd_delta_kernel<<<static_cast<unsigned>((n_rows + 7) / 8), 256, 0, st>>>(
+      static_cast<const uint16_t*>(out), static_cast<const uint16_t*>(dout), n_rows, delta);
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) e = launch_block_mask(hd, idx, ks, n_q, n_kv, topk, ds, status, st);
+  prof_end(ps, st);
+  if (e != cudaSuccess) return e;
+  ps = prof_begin(kProfAttnBwd, st);
+  switch (hd) {
+    case 1: e = launch_hd<1>(tmap_kv, tmap_q, tmap_do, n_q, scale, ds, lse, delta, dq, dkv, status, st); break;
+    case 2: e = launch_hd<2>(tmap_kv, tmap_q, tmap_do, n_q, scale, ds, lse, delta, dq, dkv, status, st); break;
+    case 4: e = launch_hd<4>(tmap_kv, tmap_q, tmap_do, n_q, scale, ds, lse, delta, dq, dkv, status, st); break;
+    case 8: e = launch_hd<8>(tmap_kv, tmap_q, tmap_do, n_q, scale, ds, lse, delta, dq, dkv, status, st); break;
+    case 16: e = launch_hd<16>(tmap_kv, tmap_q, tmap_do, n_q, scale, ds, lse, delta, dq, dkv, status, st); break;
+    default: e = cudaErrorInvalidValue;
+  }
+  prof_end(ps, st);
+  return e;
+}
+
+}  // namespace dsa

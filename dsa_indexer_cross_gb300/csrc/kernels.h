@@ -127,8 +127,24 @@ cudaError_t launch_select(int n_q, int n_chunks, int cap, int topk, int trivial_
                           uint32_t* status, cudaStream_t st);
 
 // ---------------------------------------------------------------------------- sparse attention
+// Block-dense walk: an item is kDenseCols (token, head) columns, kDenseCols / H consecutive
+// tokens with all H heads, and its tokens' selections over the item's key range are one
+// bitmask of kDenseMaskBytes (kDenseMaskBytes * 8 / tokens bits a token).
+constexpr int kDenseCols = 64;
+constexpr int kDenseMaskBytes = 4096;
 // Heads of the block-dense walk for this shape, or 0 for the per-token gather walk.
 int sparse_attn_dense_heads(int n_heads, int n_kv, int topk);
+// The block-dense pre-pass over idx, one CTA per item (hd = heads of the walk): block_range[b]
+// = [min, max + 1) of the in-range latent rows the item's tokens select ((0, 0) for none),
+// block_mask[b] = per token, bit o set when row min + o is selected.  Bad offsets are counted in
+// status[0..1].  dense_scratch splits a scratch of sparse_attn_ws_bytes into the two arrays.
+struct DenseScratch {
+  int2* block_range;
+  uint32_t* block_mask;
+};
+DenseScratch dense_scratch(void* scratch, int n_q, int hd);
+cudaError_t launch_block_mask(int hd, const int32_t* idx, const int32_t* ks, int n_q, int n_kv, int topk,
+                              const DenseScratch& ds, uint32_t* status, cudaStream_t st);
 // Scratch bytes launch_sparse_attn needs (per-row tile counts, or per-block key ranges and
 // selection bitmasks).
 size_t sparse_attn_ws_bytes(int n_q, int n_heads, int n_kv, int topk);
@@ -179,6 +195,18 @@ cudaError_t launch_sparse_attn_bwd(int n_q, int n_kv, int n_heads, int topk, flo
                                    const void* kv, const int32_t* idx, const int32_t* ks, const void* out,
                                    const float* lse, const void* dout, float* dq, float* dkv, uint32_t* status,
                                    cudaStream_t st);
+
+// The same gradients on the block-dense walk (hd = sparse_attn_dense_heads(...) != 0), on
+// tcgen05: delta [n_q * hd] fp32 scratch for D = d_out . out, scratch of sparse_attn_ws_bytes
+// for the walk's pre-pass.  tmap_kv as for launch_sparse_attn's block-dense walk; tmap_q and
+// tmap_do: q [n_q * hd][576] and dout [n_q * hd][512] bf16 with 128-byte swizzled boxes of
+// {64, kDenseCols}.
+size_t sparse_attn_bwd_dense_delta_bytes(int n_q, int n_heads);
+cudaError_t launch_sparse_attn_bwd_dense(int hd, const CUtensorMap& tmap_kv, const CUtensorMap& tmap_q,
+                                         const CUtensorMap& tmap_do, int n_q, int n_kv, int topk, float scale,
+                                         const int32_t* idx, const int32_t* ks, const void* out, const float* lse,
+                                         const void* dout, float* dq, float* dkv, uint32_t* status, float* delta,
+                                         void* scratch, cudaStream_t st);
 
 int device_sm_count();
 

@@ -68,8 +68,7 @@ constexpr int kProd = 64;                      // warps 0-1
 constexpr int kCpBlocks = 9;
 // Warps 0-1 load, warp 2 issues S^T, warps 3-6 (and, block-dense, 8-11) run the softmax,
 // warp 7 owns TMEM and issues PV.
-constexpr int kDenseCols = 64;                 // columns of a block-dense item
-constexpr int kMaskBytes = 4096;               // selection bitmask budget (block-dense)
+constexpr int kMaskBytes = kDenseMaskBytes;    // selection bitmask budget (block-dense)
 
 template <int HB, int HD>
 struct ACfg {
@@ -911,19 +910,25 @@ template <int HD>
 cudaError_t launch_dense(const CUtensorMap& tmap_kv, const CUtensorMap& tmap_q, int n_q, int n_kv, int n_heads,
                          int topk, float scale, const int32_t* idx, const int32_t* ks, void* out, float* lse,
                          uint32_t* status, void* scratch, cudaStream_t st) {
+  const DenseScratch ds = dense_scratch(scratch, n_q, HD);
+  const int ps = prof_begin(kProfAttnPrep, st);
+  cudaError_t e = launch_block_mask(HD, idx, ks, n_q, n_kv, topk, ds, status, st);
+  prof_end(ps, st);
+  if (e != cudaSuccess) return e;
+  return launch_cfg<kDenseCols, HD>(tmap_kv, tmap_q, n_q, n_kv, n_heads, topk, scale, nullptr, idx, ks, PagedRows{},
+                                    nullptr, ds.block_range, ds.block_mask, out,
+                                    lse, status, st);
+}
+
+template <int HD>
+cudaError_t launch_mask_t(const int32_t* idx, const int32_t* ks, int n_q, int n_kv, int topk, const DenseScratch& ds,
+                          uint32_t* status, cudaStream_t st) {
   using C = ACfg<kDenseCols, HD>;
   static_assert(C::B * (C::MAXR / 32) * 4 == kMaskBytes, "one bitmask per block fills the budget exactly");
   const int n_blk = (n_q + C::B - 1) / C::B;
-  int2* br = static_cast<int2*>(scratch);
-  uint32_t* bm = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(scratch) + dense_mask_offset(n_blk));
-  const int ps = prof_begin(kProfAttnPrep, st);
-  block_mask_kernel<C::B, C::MAXR><<<n_blk, 256, 0, st>>>(idx, ks, n_q, n_kv, topk, br, bm, status, status + 1);
-  prof_end(ps, st);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  return launch_cfg<kDenseCols, HD>(tmap_kv, tmap_q, n_q, n_kv, n_heads, topk, scale, nullptr, idx, ks, PagedRows{},
-                                    nullptr, br, bm, out,
-                                    lse, status, st);
+  block_mask_kernel<C::B, C::MAXR><<<n_blk, 256, 0, st>>>(idx, ks, n_q, n_kv, topk, ds.block_range, ds.block_mask,
+                                                          status, status + 1);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -942,6 +947,28 @@ cudaError_t launch_gather(const CUtensorMap& tmap_kv, const CUtensorMap& tmap_q,
                                   nullptr, out, lse, status, st);
 }
 }  // namespace
+
+DenseScratch dense_scratch(void* scratch, int n_q, int hd) {
+  const int b = kDenseCols / hd;
+  const int n_blk = (n_q + b - 1) / b;
+  DenseScratch ds;
+  ds.block_range = static_cast<int2*>(scratch);
+  ds.block_mask = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(scratch) + dense_mask_offset(n_blk));
+  return ds;
+}
+
+cudaError_t launch_block_mask(int hd, const int32_t* idx, const int32_t* ks, int n_q, int n_kv, int topk,
+                              const DenseScratch& ds, uint32_t* status, cudaStream_t st) {
+  if (n_q <= 0) return cudaSuccess;
+  switch (hd) {
+    case 1: return launch_mask_t<1>(idx, ks, n_q, n_kv, topk, ds, status, st);
+    case 2: return launch_mask_t<2>(idx, ks, n_q, n_kv, topk, ds, status, st);
+    case 4: return launch_mask_t<4>(idx, ks, n_q, n_kv, topk, ds, status, st);
+    case 8: return launch_mask_t<8>(idx, ks, n_q, n_kv, topk, ds, status, st);
+    case 16: return launch_mask_t<16>(idx, ks, n_q, n_kv, topk, ds, status, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
 
 size_t sparse_attn_ws_bytes(int n_q, int n_heads, int n_kv, int topk) {
   const int hd = sparse_attn_dense_heads(n_heads, n_kv, topk);

@@ -301,9 +301,13 @@ dsa_status dsa_indexer_projections(const dsa_proj_desc* desc, const void* x, con
  * bf16.  Outputs fp32: dq [n_q][n_heads][576] (written) and dkv [n_kv][576] (zeroed here, then
  * accumulated; rows shared by several tokens receive atomic adds, so the order of the
  * additions, and the last bits of dkv, vary from run to run).  All tensors 16-byte aligned.
- * Out-of-range indices are counted in the status word and skipped.
- * ws: at least 256 bytes, 256-byte aligned (status word).  Errors: DSA_ERR_ARG,
- * DSA_ERR_UNSUPPORTED (d_qk != 576 or d_v != 512), DSA_ERR_WORKSPACE, DSA_ERR_CUDA. */
+ * Out-of-range indices are counted in the status word and skipped.  Shapes that take the
+ * forward's block-dense walk (at most 16 heads, selections dense in a short key range) run
+ * on the tensor cores with P and dS rounded to bf16; the others take a per-token kernel.
+ * ws: dsa_sparse_attn_backward_workspace_size bytes (at least 256), 256-byte aligned.
+ * Errors: DSA_ERR_ARG, DSA_ERR_UNSUPPORTED (d_qk != 576 or d_v != 512), DSA_ERR_WORKSPACE,
+ * DSA_ERR_CUDA. */
+dsa_status dsa_sparse_attn_backward_workspace_size(const dsa_attn_desc* desc, size_t* bytes);
 dsa_status dsa_sparse_attn_backward(const dsa_attn_desc* desc, const void* q, const void* kv, const int32_t* idx,
                                     const int32_t* ks, const void* out, const float* lse, const void* d_out,
                                     float* dq, float* dkv, void* ws, size_t ws_bytes, void* stream);
