@@ -12,25 +12,32 @@
 // H heads) and the union of their key ranges, walked in tiles of 64 consecutive latent rows
 // (one 72 KB 3-D TMA box) with the per-(token, row) selection bitmask of the pre-pass.  Per
 // tile, with the rows on the M side wherever the columns are too few for it:
-//   S^T  [64 rows x 64 cols]  = Rows . Q^T           M = 64,  N = 64, K = 576   (TMEM)
-//   dP^T [64 rows x 64 cols]  = Rows[:, :512] . dO^T M = 64,  N = 64, K = 512   (TMEM)
+//   [S^T | dP^T] [64 rows x 128] = Rows . [Q | dO]^T   M = 64, N = 128, K = 512, then
+//   S^T += Rows[:, 512:] . Q[:, 512:]^T                 (the rope block, N = 64)
 //   softmax warps: P and dS' per (row, col), bf16, into two 8 KB blocks laid out [row][col]
-//   dQ^T [576 dims x 64 cols] += Rows^T . dS'^T      M = 128 per dim chunk, K = 64 rows
-//   dKV^T piece [128 dims x 32 rows] = Q^T . dS' (+ dO^T . P)   K = 64 cols
-// The [row][col] blocks are read as the MN-major B of dQ^T and as the K-major B of the dKV^T
-// pieces (the same bytes); Q and dO stay in shared memory as K-major B operands of the first
-// two products and as MN-major A operands of the pieces.  576 dims are five 128-dim chunks,
-// the last one starting at dim 448 (its first 64 lanes repeat chunk 3 and are ignored), so
-// no operand reads past its tile.  dQ^T (320 TMEM columns) accumulates over the item and is
-// written once; each dKV^T piece (two 32-column TMEM slots) is drained by four warps with
-// fp32 reductions into dkv, the 64 columns of the item summed first.  TMEM: S^T 64 + dP^T 64
-// + dQ^T 320 + pieces 64 = 512 columns; shared memory: Q 72 KB + dO 64 KB + tile 72 KB + P
-// and dS' 16 KB.
+//   dQ^T [576 dims x 64 cols] += Rows^T . dS'^T         M = 128 per dim chunk, K = 64 rows
+//   dKV^T piece [128 dims x 64 rows] = Q^T . dS' (+ dO^T . P)   K = 64 cols
+// q and d_out sit in shared memory interleaved by 64-dim block, so each block's K-major
+// [q; d_out] operand feeds S^T and dP^T in one N = 128 MMA; the same blocks are the MN-major A
+// operands of the pieces.  The [row][col] blocks are read as the MN-major B of dQ^T and as the
+// K-major B of the pieces (the same bytes).  576 dims are five 128-dim chunks, the last one
+// starting at dim 448 (its first 64 lanes repeat chunk 3 and are ignored), so no operand reads
+// past its tile.  dQ^T (320 TMEM columns) accumulates over the item and is written once.  The
+// five pieces of a tile go to three 64-column TMEM slots: the spare columns and S^T's and
+// dP^T's, free from the softmax's read until the next tile's S^T (which waits for the drains of
+// the pieces parked there; the tile's last piece takes the spare slot, so that wait ends one
+// piece early).  Each piece is drained by eight warps with fp32 reductions into dkv, the item's
+// 64 columns summed first.  These products read two operands of 2-6 KB from shared memory per
+// 16-deep step, so the tensor core runs near its rate only on the N = 128 S^T | dP^T step; and
+// the reductions (147 KB a tile) run close to the L2's reduction throughput.  TMEM: S^T 64 +
+// dP^T 64 + dQ^T 320 + spare 64 = 512 columns; shared memory: q 72 KB + d_out 64 KB + tile
+// 72 KB + P and dS' 16 KB.
 //
-// Warp roles (512 threads): warp 0 loads (TMA), warp 1 owns TMEM and issues every MMA, warps
-// 4-7 drain the dKV^T pieces and dQ^T, warps 8-15 run the softmax (two per TMEM lane quarter,
-// 32 columns each).  Every wait is bounded; a timeout sets the CTA's abort flag and the
-// device status, and every role then leaves its loop.
+// Warp roles (576 threads): warp 0 loads (TMA); warp 1 owns TMEM, takes every wait of the
+// products and has its lane 0 issue them; warps 2-7, 16 and 17 drain the pieces and dQ^T (two
+// per TMEM lane quarter); warps 8-15 run the softmax (two per lane quarter, 32 columns each).
+// Every wait is bounded; a timeout sets the CTA's abort flag and the device status, and every
+// role then leaves its loop.
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -48,20 +55,27 @@ constexpr int kMaskWords = kDenseMaskBytes / 4;
 static_assert(kC == 64, "the [row][col] blocks hold 64 columns in one 128-byte row");
 
 constexpr uint32_t kColS = 0, kColDP = 64, kColDQ = 128, kColKV = 448, kTmemCols = 512;
+// dKV^T piece slots (64 columns each): the spare columns, then S^T's and dP^T's, which are free
+// from the softmax's read of a tile until the next tile's S^T
+__device__ __forceinline__ uint32_t kv_slot_col(int slot) { return slot == 0 ? kColKV : slot == 1 ? kColS : kColDP; }
+// Slot of a tile's piece m: the last piece goes to the spare slot, so the next tile's S^T waits
+// only for the drain of the fourth
+__device__ __forceinline__ int piece_slot(int m) { return m == 0 || m == 3 ? 1 : m == 1 ? 2 : 0; }
 
-constexpr int kOffQ = 0;
-constexpr int kOffDO = kOffQ + kQB * kBlk;
-constexpr int kOffR = kOffDO + kVB * kBlk;
+// q and d_out interleaved by 64-dim block: [q block kb | d_out block kb] for kb < 8, then q's
+// rope block, so one N = 128 K-major operand per block feeds S^T and dP^T together
+constexpr int kOffQD = 0;
+constexpr int kOffR = kOffQD + (kQB + kVB) * kBlk;
 constexpr int kOffP = kOffR + kQB * kBlk;
 constexpr int kOffDS = kOffP + kBlk;
 constexpr int kDynSmem = 1024 + kOffDS + kBlk;   // + alignment slack for the 1024-byte swizzle atoms
 
-constexpr int kThreads = 512;
-constexpr int kSoftWarps = 8, kDrainWarps = 4;
+constexpr int kThreads = 576;
+constexpr int kSoftWarps = 8, kDrainWarps = 8;
 
 struct BShared {
   uint64_t q_full, q_empty, full, empty, s_full, s_empty, p_full;
-  uint64_t kv_full[2], kv_empty[2], dq_full, dq_empty, mma_done;
+  uint64_t kv_full[3], kv_empty[3], dq_full, dq_empty, mma_done;
   uint32_t tmem_base, abort_flag;
 };
 static_assert(kDynSmem + sizeof(BShared) <= 232448, "backward tile set must fit in shared memory");
@@ -120,8 +134,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   __shared__ BShared sh;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = smem + kOffQ;
-  uint8_t* sDO = smem + kOffDO;
+  uint8_t* sQD = smem + kOffQD;
   uint8_t* sR = smem + kOffR;
   uint8_t* sP = smem + kOffP;
   uint8_t* sDS = smem + kOffDS;
@@ -147,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&sh.s_full, 1);
     mbar_init(&sh.s_empty, kSoftWarps);
     mbar_init(&sh.p_full, kSoftWarps);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < 3; ++s) {
       mbar_init(&sh.kv_full[s], 1);
       mbar_init(&sh.kv_empty[s], kDrainWarps);
     }
@@ -183,9 +196,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int qrow = item * kC;
         mbar_arrive_expect_tx(&sh.q_full, (kQB + kVB) * kBlk);
 #pragma unroll 1
-        for (int kb = 0; kb < kQB; ++kb) tma_load_2d(sQ + kb * kBlk, &tmap_q, &sh.q_full, kb * 64, qrow);
+        for (int kb = 0; kb < kQB; ++kb) tma_load_2d(sQD + 2 * kb * kBlk, &tmap_q, &sh.q_full, kb * 64, qrow);
 #pragma unroll 1
-        for (int kb = 0; kb < kVB; ++kb) tma_load_2d(sDO + kb * kBlk, &tmap_do, &sh.q_full, kb * 64, qrow);
+        for (int kb = 0; kb < kVB; ++kb) tma_load_2d(sQD + (2 * kb + 1) * kBlk, &tmap_do, &sh.q_full, kb * 64, qrow);
         for (int i = 0; i < nt; ++i, ++g) {
           if (g > 0 && !(ok = mbar_wait_for(&sh.empty, (g - 1) & 1, &sh.abort_flag, status, wait_ns))) break;
           mbar_arrive_expect_tx(&sh.full, kQB * kBlk);
@@ -200,22 +213,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
-    constexpr uint32_t id_s = idesc_bf16_f32(64, kC, 0, 0);
+    // The whole warp takes every wait; lane 0 alone issues the MMAs and their commits (the
+    // descriptors are bases plus compile-time offsets, so issuing costs little more than the
+    // instruction itself).
+    constexpr uint32_t id_sd = idesc_bf16_f32(64, 2 * kC, 0, 0);   // S^T and dP^T together
+    constexpr uint32_t id_s = idesc_bf16_f32(64, kC, 0, 0);        // S^T alone (rope block)
     constexpr uint32_t id_dq = idesc_bf16_f32(128, kC, 1, 1);
-    constexpr uint32_t id_kv = idesc_bf16_f32(128, 32, 1, 0);
-    const uint64_t dR_k = sdesc_sw128(smem_u32(sR), 16, 1024);      // rows, K-major (A of S^T, dP^T)
-    const uint64_t dQ_k = sdesc_sw128(smem_u32(sQ), 16, 1024);      // q, K-major (B of S^T)
-    const uint64_t dO_k = sdesc_sw128(smem_u32(sDO), 16, 1024);     // d_out, K-major (B of dP^T)
-    const uint64_t dR_mn = sdesc_sw128(smem_u32(sR), kBlk, 1024);   // rows^T, MN-major (A of dQ^T)
-    const uint64_t dDS_mn = sdesc_sw128(smem_u32(sDS), kBlk, 1024); // dS'^T, MN-major (B of dQ^T)
-    const uint64_t dQ_mn = sdesc_sw128(smem_u32(sQ), kBlk, 1024);   // q^T, MN-major (A of dKV^T)
-    const uint64_t dO_mn = sdesc_sw128(smem_u32(sDO), kBlk, 1024);  // d_out^T, MN-major (A of dKV^T)
-    const uint64_t dDS_k = sdesc_sw128(smem_u32(sDS), 16, 1024);    // dS', K-major (B of dKV^T)
-    const uint64_t dP_k = sdesc_sw128(smem_u32(sP), 16, 1024);      // P, K-major (B of dKV^T)
+    constexpr uint32_t id_kv = idesc_bf16_f32(128, kR, 1, 0);
+    const uint64_t dR_k = sdesc_sw128(smem_u32(sR), 16, 1024);             // rows, K-major (A of S^T, dP^T)
+    const uint64_t dQD_k = sdesc_sw128(smem_u32(sQD), 16, 1024);           // [q; d_out], K-major (B)
+    const uint64_t dR_mn = sdesc_sw128(smem_u32(sR), kBlk, 1024);          // rows^T, MN-major (A of dQ^T)
+    const uint64_t dDS_mn = sdesc_sw128(smem_u32(sDS), kBlk, 1024);        // dS'^T, MN-major (B of dQ^T)
+    const uint64_t dQ_mn = sdesc_sw128(smem_u32(sQD), 2 * kBlk, 1024);     // q^T, MN-major (A of dKV^T)
+    const uint64_t dO_mn = sdesc_sw128(smem_u32(sQD + kBlk), 2 * kBlk, 1024);   // d_out^T (A of dKV^T)
+    const uint64_t dDS_k = sdesc_sw128(smem_u32(sDS), 16, 1024);           // dS', K-major (B of dKV^T)
+    const uint64_t dP_k = sdesc_sw128(smem_u32(sP), 16, 1024);             // P, K-major (B of dKV^T)
     auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
       return __all_sync(0xffffffffu, mbar_wait_for(bar, parity, &sh.abort_flag, status, wait_ns));
     };
-    uint32_t g = 0, it = 0, pc = 0;
+    uint32_t g = 0, it = 0;
+    uint32_t su[3] = {0u, 0u, 0u};   // uses of each piece slot so far
     bool ok = true;
     for (int k = 0; k * static_cast<int>(gridDim.x) < n_items && ok; ++k) {
       const int item = snake_item(k);
@@ -227,68 +244,86 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < nt && ok; ++i, ++g) {
         if (!(ok = wait(&sh.full, g & 1))) break;
         if (g > 0 && !(ok = wait(&sh.s_empty, (g - 1) & 1))) break;
+        // S^T and dP^T's columns held pieces of the previous tile: wait for their drains
+        if (su[1] > 0 && !(ok = wait(&sh.kv_empty[1], (su[1] - 1) & 1))) break;
+        if (su[2] > 0 && !(ok = wait(&sh.kv_empty[2], (su[2] - 1) & 1))) break;
         tc_fence_after();
-        // S^T and dP^T share each 64-dim block of the tile
+        if (lane == 0) {
+          // S^T | dP^T = Rows [q | d_out]^T over the eight value blocks, then S^T += the rope block
 #pragma unroll
-        for (int kb = 0; kb < kQB; ++kb) {
+          for (int kb = 0; kb < kVB; ++kb) {
 #pragma unroll
-          for (int sub = 0; sub < 4; ++sub) {
-            const uint64_t off = static_cast<uint64_t>((kb * kBlk + sub * 32) >> 4);
-            const uint32_t acc = (kb | sub) ? 1u : 0u;
-            umma_bf16_elect(tmem + kColS, dR_k + off, dQ_k + off, id_s, acc);
-            if (kb < kVB) umma_bf16_elect(tmem + kColDP, dR_k + off, dO_k + off, id_s, acc);
+            for (int sub = 0; sub < 4; ++sub)
+              umma_bf16(tmem + kColS, dR_k + static_cast<uint64_t>((kb * kBlk + sub * 32) >> 4),
+                        dQD_k + static_cast<uint64_t>((2 * kb * kBlk + sub * 32) >> 4), id_sd, (kb | sub) ? 1u : 0u);
           }
+#pragma unroll
+          for (int sub = 0; sub < 4; ++sub)
+            umma_bf16(tmem + kColS, dR_k + static_cast<uint64_t>((kVB * kBlk + sub * 32) >> 4),
+                      dQD_k + static_cast<uint64_t>((2 * kVB * kBlk + sub * 32) >> 4), id_s, 1u);
+          umma_commit(&sh.s_full);
         }
-        umma_commit_elect(&sh.s_full);
+        __syncwarp();
         if (!(ok = wait(&sh.p_full, g & 1))) break;
         if (i == 0 && it > 0 && !(ok = wait(&sh.dq_empty, (it - 1) & 1))) break;
         tc_fence_after();
-        // dQ^T += Rows^T dS'^T, five 128-dim chunks, K = the tile's 64 rows
+        if (lane == 0) {
+          // dQ^T += Rows^T dS'^T, five 128-dim chunks, K = the tile's 64 rows
 #pragma unroll
-        for (int m = 0; m < 5; ++m) {
+          for (int m = 0; m < 5; ++m) {
 #pragma unroll
-          for (int kq = 0; kq < kR / 16; ++kq)
-            umma_bf16_elect(tmem + kColDQ + m * kC,
-                            dR_mn + static_cast<uint64_t>(((chunk_dim0(m) / 64) * kBlk + kq * 2048) >> 4),
-                            dDS_mn + static_cast<uint64_t>((kq * 2048) >> 4), id_dq, (i > 0 || kq > 0) ? 1u : 0u);
+            for (int kq = 0; kq < kR / 16; ++kq)
+              umma_bf16(tmem + kColDQ + m * kC,
+                        dR_mn + static_cast<uint64_t>(((chunk_dim0(m) / 64) * kBlk + kq * 2048) >> 4),
+                        dDS_mn + static_cast<uint64_t>((kq * 2048) >> 4), id_dq, (i > 0 || kq > 0) ? 1u : 0u);
+          }
+          umma_commit(&sh.empty);                  // the tile may be refilled
+          if (i == nt - 1) umma_commit(&sh.dq_full);
         }
-        umma_commit_elect(&sh.empty);              // the tile may be refilled
-        if (i == nt - 1) umma_commit_elect(&sh.dq_full);
-        // dKV^T pieces: dims chunk m x rows half h, K = the item's 64 columns
-#pragma unroll 1
+        __syncwarp();
+        // dKV^T pieces: dims chunk m x the tile's 64 rows, K = the item's 64 columns
+#pragma unroll
         for (int m = 0; m < 5 && ok; ++m) {
-#pragma unroll 1
-          for (int h = 0; h < 2 && ok; ++h, ++pc) {
-            const int slot = pc & 1;
-            if (pc >= 2 && !(ok = wait(&sh.kv_empty[slot], ((pc >> 1) - 1) & 1))) break;
-            tc_fence_after();
-            const uint32_t d_kv = tmem + kColKV + slot * 32;
-            const uint32_t a_off = static_cast<uint32_t>((chunk_dim0(m) / 64) * kBlk);
+          const int slot = piece_slot(m);
+          if (su[slot] > 0 && !(ok = wait(&sh.kv_empty[slot], (su[slot] - 1) & 1))) break;
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t d_kv = tmem + kv_slot_col(slot);
+            const uint32_t a_off = static_cast<uint32_t>((chunk_dim0(m) / 64) * 2 * kBlk);
 #pragma unroll
             for (int kq = 0; kq < kC / 16; ++kq)
-              umma_bf16_elect(d_kv, dQ_mn + static_cast<uint64_t>((a_off + kq * 2048) >> 4),
-                              dDS_k + static_cast<uint64_t>((h * 32 * 128 + kq * 32) >> 4), id_kv, kq > 0 ? 1u : 0u);
+              umma_bf16(d_kv, dQ_mn + static_cast<uint64_t>((a_off + kq * 2048) >> 4),
+                        dDS_k + static_cast<uint64_t>((kq * 32) >> 4), id_kv, kq > 0 ? 1u : 0u);
             if (m < 4) {
 #pragma unroll
               for (int kq = 0; kq < kC / 16; ++kq)
-                umma_bf16_elect(d_kv, dO_mn + static_cast<uint64_t>((a_off + kq * 2048) >> 4),
-                                dP_k + static_cast<uint64_t>((h * 32 * 128 + kq * 32) >> 4), id_kv, 1u);
+                umma_bf16(d_kv, dO_mn + static_cast<uint64_t>((a_off + kq * 2048) >> 4),
+                          dP_k + static_cast<uint64_t>((kq * 32) >> 4), id_kv, 1u);
             }
-            umma_commit_elect(&sh.kv_full[slot]);
+            umma_commit(&sh.kv_full[slot]);
           }
+          __syncwarp();
+          ++su[slot];
         }
       }
-      if (ok) umma_commit_elect(&sh.q_empty);      // q and d_out may be replaced once these finish
+      if (ok && lane == 0) umma_commit(&sh.q_empty);   // q and d_out may be replaced once these finish
+      __syncwarp();
       ++it;
     }
     // every MMA issued here has completed before TMEM is released
-    umma_commit_elect(&sh.mma_done);
+    if (lane == 0) umma_commit(&sh.mma_done);
+    __syncwarp();
     mbar_drain(&sh.mma_done, 0, 200000000ull);
-  } else if (warp >= 4 && warp < 8) {
+  } else if ((warp >= 2 && warp < 8) || warp >= 16) {
     // ------------------------------------------------------------------ drains: dKV^T pieces, dQ^T
+    // two warps per TMEM lane quarter: set 0 (warps 4-7) takes the first half of every piece's
+    // rows and of dQ^T's columns, set 1 (warps 2, 3, 16, 17) the second half
     const int qd = warp & 3;
+    const int set = (warp >= 4 && warp < 8) ? 0 : 1;
+    const int drain_id = set * 4 + qd;
     const uint32_t t_lane = static_cast<uint32_t>(qd * 32) << 16;
-    uint32_t g = 0, it = 0, pc = 0;
+    uint32_t g = 0, it = 0;
+    uint32_t su[3] = {0u, 0u, 0u};   // uses of each piece slot so far
     bool ok = true;
     for (int k = 0; k * static_cast<int>(gridDim.x) < n_items && ok; ++k) {
       const int item = snake_item(k);
@@ -299,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float* dq_item = dq + static_cast<size_t>(item) * kC * kDqk;
       if (nt == 0) {
         // nothing selected: zero gradients for the item's rows of dq
-        for (int e = (warp - 4) * 32 + lane; e < n_cols * kDqk; e += kDrainWarps * 32) dq_item[e] = 0.f;
+        for (int e = drain_id * 32 + lane; e < n_cols * kDqk; e += kDrainWarps * 32) dq_item[e] = 0.f;
         continue;
       }
       for (int i = 0; i < nt && ok; ++i, ++g) {
@@ -314,31 +349,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         any_lo = __reduce_or_sync(0xffffffffu, any_lo);
         any_hi = __reduce_or_sync(0xffffffffu, any_hi);
         const long long row0 = static_cast<long long>(lo) + static_cast<long long>(i) * kR;
-#pragma unroll 1
-        for (int m = 0; m < 5 && ok; ++m) {
-#pragma unroll 1
-          for (int h = 0; h < 2; ++h, ++pc) {
-            const int slot = pc & 1;
-            ok = __all_sync(0xffffffffu,
-                            mbar_wait_for(&sh.kv_full[slot], (pc >> 1) & 1, &sh.abort_flag, status, wait_ns));
-            if (!ok) break;
-            tc_fence_after();
-            const bool mine = m < 4 || qd >= 2;     // chunk 4's first 64 lanes repeat chunk 3
-            uint32_t v[32];
-            if (mine) {
-              tmem_ld32(tmem + t_lane + kColKV + slot * 32, v);
-              tmem_ld_wait();
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sh.kv_empty[slot]);
-            if (mine) {
-              const uint32_t any = h ? any_hi : any_lo;
-              float* col = dkv + (row0 + 32 * h) * kDqk + chunk_dim0(m) + 32 * qd + lane;
 #pragma unroll
-              for (int j = 0; j < 32; ++j)
-                if ((any >> j) & 1u) red_add_f32(col + static_cast<size_t>(j) * kDqk, __uint_as_float(v[j]));
-            }
+        for (int m = 0; m < 5; ++m) {
+          const int slot = piece_slot(m);
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait_for(&sh.kv_full[slot], su[slot] & 1, &sh.abort_flag, status, wait_ns));
+          if (!ok) break;
+          ++su[slot];
+          tc_fence_after();
+          const bool mine = m < 4 || qd >= 2;     // chunk 4's first 64 lanes repeat chunk 3
+          uint32_t v[32];
+          if (mine) {
+            tmem_ld32(tmem + t_lane + kv_slot_col(slot) + set * 32, v);
+            tmem_ld_wait();
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh.kv_empty[slot]);
+          if (mine) {
+            const uint32_t any = set ? any_hi : any_lo;
+            float* col = dkv + (row0 + 32 * set) * kDqk + chunk_dim0(m) + 32 * qd + lane;
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if ((any >> j) & 1u) red_add_f32(col + static_cast<size_t>(j) * kDqk, __uint_as_float(v[j]));
           }
         }
       }
@@ -351,16 +384,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int m = 0; m < 5; ++m) {
         if (m == 4 && qd < 2) continue;
         const int d = chunk_dim0(m) + 32 * qd + lane;
-#pragma unroll 1
-        for (int half = 0; half < 2; ++half) {
-          uint32_t v[32];
-          tmem_ld32(tmem + t_lane + kColDQ + m * kC + half * 32, v);
-          tmem_ld_wait();
+        uint32_t v[32];
+        tmem_ld32(tmem + t_lane + kColDQ + m * kC + set * 32, v);
+        tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int c = half * 32 + j;
-            if (c < n_cols) dq_item[static_cast<size_t>(c) * kDqk + d] = __uint_as_float(v[j]);
-          }
+        for (int j = 0; j < 32; ++j) {
+          const int c = set * 32 + j;
+          if (c < n_cols) dq_item[static_cast<size_t>(c) * kDqk + d] = __uint_as_float(v[j]);
         }
       }
       tc_fence_before();
@@ -368,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&sh.dq_empty);
       ++it;
     }
-  } else if (warp >= 8) {
+  } else if (warp >= 8 && warp < 16) {
     // ------------------------------------------------------------------ softmax: P and dS'
     const int qd = warp & 3;                  // TMEM lane quarter
     const int c_off = warp >= 12 ? 32 : 0;    // this warp's 32 columns
