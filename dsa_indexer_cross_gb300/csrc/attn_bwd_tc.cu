@@ -141,10 +141,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int n_items = (n_q + B - 1) / B;
-  // causal items grow with their index: alternate directions so the CTAs balance
+  // k-th item of this CTA: causal items grow with their index, so the walk takes them from the
+  // last (largest) down, alternating directions across the CTAs each round; the partial last
+  // round then holds the smallest items.  Past the end: n_items.
   auto snake_item = [&](int k) {
     const int gdim = static_cast<int>(gridDim.x), b = static_cast<int>(blockIdx.x);
-    return k * gdim + ((k & 1) ? (gdim - 1 - b) : b);
+    const int r = k * gdim + ((k & 1) ? (gdim - 1 - b) : b);
+    return r < n_items ? n_items - 1 - r : n_items;
   };
   auto item_tiles = [&](int item, int& lo) {
     const int2 r = __ldg(block_range + item);

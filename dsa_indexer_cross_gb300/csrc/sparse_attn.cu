@@ -235,10 +235,14 @@ __global__ void __launch_bounds__(ACfg<HB, HD>::THREADS, 1)
   const int n_hb = DENSE ? 1 : (H + HB - 1) / HB;
   const int n_items = DENSE ? (n_q + B - 1) / B : n_q * n_hb;
   // k-th item of this CTA in "snake" order (forward on even rounds, backward on odd ones):
-  // causal items grow with their index, so alternating directions balances the CTAs.
+  // causal items grow with their index, so alternating directions balances the CTAs.  The
+  // block-dense walk takes its items from the last (largest) down, so that the partial last
+  // round holds the smallest ones.  Past the end: n_items.
   auto snake_item = [&](int k) {
     const int gdim = static_cast<int>(gridDim.x), b = static_cast<int>(blockIdx.x);
-    return k * gdim + ((k & 1) ? (gdim - 1 - b) : b);
+    const int r = k * gdim + ((k & 1) ? (gdim - 1 - b) : b);
+    if constexpr (DENSE) return r < n_items ? n_items - 1 - r : n_items;
+    return r;
   };
 
   if (threadIdx.x == 0) {
