@@ -601,7 +601,7 @@ def time_bwd(D, w, st, dev, stream, flush, tc_peak, reps: int = 5):
     dq = torch.empty((w.n_q, w.n_heads, w.d_qk), dtype=torch.float32, device=dev)
     dkv = torch.empty((adesc.n_kv, w.d_qk), dtype=torch.float32, device=dev)
     ws = torch.zeros(D.dsa_sparse_attn_backward_workspace_size(adesc), dtype=torch.uint8, device=dev)
-    dense = ws.numel() > 256   # only the block-dense walk needs more than the status words
+    tc = ws.numel() > 256   # the tcgen05 walks need more than the status words
     D.dsa_sparse_attn(adesc, L0["q"], L0["kv"], idx, ks, L0["out"], L0["lse"], stream=stream)
     m = logged_ms(D, lambda: D.dsa_sparse_attn_backward(adesc, L0["q"], L0["kv"], idx, ks, L0["out"], L0["lse"], d_out,
                                                         dq, dkv, ws=ws, stream=stream), reps, flush, "attn_bwd")
@@ -610,8 +610,7 @@ def time_bwd(D, w, st, dev, stream, flush, tc_peak, reps: int = 5):
     flops = 2.5 * R["attn_flops"]
     out = {"attn": {"ms": m, "forward_ms": st["attn_ms"], "flops": flops, "tflops": flops / (m / 1e3) / 1e12,
                     "frac_of_bf16_peak": flops / (m / 1e3) / 1e12 / tc_peak,
-                    "kernel": ("attn_bwd_dense_kernel (tcgen05, block-dense walk" if dense else
-                               "sparse_attn_bwd_kernel (mma.sync, per-token walk") +
+                    "kernel": ("attn_bwd_tc_kernel (tcgen05" if tc else "sparse_attn_bwd_kernel (mma.sync") +
                               "; kernel time from the launch log, dkv cleared before it)"}}
     if hasattr(D, "dsa_indexer_backward"):
         out["indexer"] = time_indexer_bwd(D, w, st, dev, stream, flush, tc_peak, reps)

@@ -831,12 +831,19 @@ dsa_status dsa_indexer_projections(const dsa_proj_desc* d, const void* x, const 
 }
 
 namespace {
-// Backward workspace: the status header, then for the block-dense walk D = d_out . out per
-// (token, head) and the walk's key ranges and selection bitmasks.
+// The tcgen05 backward reads q and d_out in boxes of 64 (token, head) rows: it takes every
+// shape with at least 64 of them; smaller ones take the per-token kernel.
+bool attn_bwd_tc(const dsa_attn_desc* d) { return static_cast<long long>(d->n_q) * d->n_heads >= kDenseCols; }
+
+// Backward workspace: the status header, then (tcgen05) D = d_out . out per (token, head) and
+// the walk's pre-pass arrays (block-dense: key ranges and selection bitmasks; gather: 64-slot
+// tiles per token).
 size_t attn_bwd_ws_bytes(const dsa_attn_desc* d) {
-  if (!sparse_attn_dense_heads(d->n_heads, d->n_kv, d->topk)) return kAlign;
-  return kAlign + align_up(sparse_attn_bwd_dense_delta_bytes(d->n_q, d->n_heads)) +
-         align_up(sparse_attn_ws_bytes(d->n_q, d->n_heads, d->n_kv, d->topk));
+  if (!attn_bwd_tc(d)) return kAlign;
+  const size_t walk = sparse_attn_dense_heads(d->n_heads, d->n_kv, d->topk)
+                          ? sparse_attn_ws_bytes(d->n_q, d->n_heads, d->n_kv, d->topk)
+                          : static_cast<size_t>(d->n_q) * sizeof(int32_t);
+  return kAlign + align_up(sparse_attn_bwd_dense_delta_bytes(d->n_q, d->n_heads)) + align_up(walk);
 }
 }  // namespace
 
@@ -869,21 +876,29 @@ dsa_status dsa_sparse_attn_backward(const dsa_attn_desc* desc, const void* q, co
     return cuda_fail(e, "clear dkv");
   if (desc->n_q == 0) return DSA_OK;
   uint32_t* status = static_cast<uint32_t*>(ws);
-  const int hd = sparse_attn_dense_heads(desc->n_heads, desc->n_kv, desc->topk);
-  if (hd) {
-    // block-dense walk on tcgen05: kv as whole 64-row tiles, q and d_out as 64-row boxes
-    CUtensorMap tkv, tq, tdo;
-    std::memset(&tkv, 0, sizeof(tkv));
-    if (desc->n_kv > 0 && (s = tmap_kv_tiles(&tkv, kv, desc->n_kv)) != DSA_OK) return s;
+  if (attn_bwd_tc(desc)) {
+    // tcgen05: q and d_out as 64-row boxes; block-dense walk: kv as whole 64-row tiles
+    CUtensorMap tq, tdo;
     const uint64_t rows = static_cast<uint64_t>(desc->n_q) * desc->n_heads;
     if ((s = tmap_bf16(&tq, q, 576, rows, kDenseCols)) != DSA_OK) return s;
     if ((s = tmap_bf16(&tdo, d_out, 512, rows, kDenseCols)) != DSA_OK) return s;
     uint8_t* base = static_cast<uint8_t*>(ws);
     float* delta = reinterpret_cast<float*>(base + kAlign);
     void* scratch = base + kAlign + align_up(sparse_attn_bwd_dense_delta_bytes(desc->n_q, desc->n_heads));
-    e = launch_sparse_attn_bwd_dense(hd, tkv, tq, tdo, desc->n_q, desc->n_kv, desc->topk, desc->softmax_scale, idx, ks,
-                                     out, lse, d_out, dq, dkv, status, delta, scratch, st);
-    if (e != cudaSuccess) return cuda_fail(e, "sparse attention backward (block-dense)");
+    const int hd = sparse_attn_dense_heads(desc->n_heads, desc->n_kv, desc->topk);
+    if (hd) {
+      CUtensorMap tkv;
+      std::memset(&tkv, 0, sizeof(tkv));
+      if (desc->n_kv > 0 && (s = tmap_kv_tiles(&tkv, kv, desc->n_kv)) != DSA_OK) return s;
+      e = launch_sparse_attn_bwd_dense(hd, tkv, tq, tdo, desc->n_q, desc->n_kv, desc->topk, desc->softmax_scale, idx,
+                                       ks, out, lse, d_out, dq, dkv, status, delta, scratch, st);
+      if (e != cudaSuccess) return cuda_fail(e, "sparse attention backward (block-dense)");
+    } else {
+      e = launch_sparse_attn_bwd_gather(tq, tdo, desc->n_q, desc->n_kv, desc->n_heads, desc->topk, desc->softmax_scale,
+                                        kv, idx, ks, out, lse, d_out, dq, dkv, status, delta,
+                                        static_cast<int32_t*>(scratch), st);
+      if (e != cudaSuccess) return cuda_fail(e, "sparse attention backward (gather)");
+    }
     return DSA_OK;
   }
   const int ps = prof_begin(kProfAttnBwd, st);

@@ -1,4 +1,5 @@
-// Backward of the MLA-absorbed sparse attention on the block-dense walk, on tcgen05.
+// Backward of the MLA-absorbed sparse attention on tcgen05: the block-dense walk and the gather
+// walk (one token's selected rows per item).
 //
 // The same gradients as the per-token kernel (attn_bwd.cu): for column c = (token, head) and a
 // selected latent row j,
@@ -74,11 +75,18 @@ constexpr int kThreads = 576;
 constexpr int kSoftWarps = 8, kDrainWarps = 8;
 
 struct BShared {
+  int rows[3][kR];   // gather walk: latent row of each slot of the tile (-1: none), three tiles deep
+  uint32_t rows_tag[3];   // the tile whose row list each slot holds (published after the list)
   uint64_t q_full, q_empty, full, empty, s_full, s_empty, p_full;
   uint64_t kv_full[3], kv_empty[3], dq_full, dq_empty, mma_done;
   uint32_t tmem_base, abort_flag;
 };
 static_assert(kDynSmem + sizeof(BShared) <= 232448, "backward tile set must fit in shared memory");
+
+// byte offset of 16-byte chunk `chunk` of row `row` in a 128-byte-swizzled block of 128-byte rows
+__device__ __forceinline__ uint32_t sw128(int row, int chunk) {
+  return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
 
 // first dim of 128-dim chunk m (the last chunk overlaps the previous one by 64 dims)
 __device__ __forceinline__ constexpr int chunk_dim0(int m) { return m < 4 ? 128 * m : 448; }
@@ -122,15 +130,44 @@ __global__ void __launch_bounds__(256) attn_bwd_delta_kernel(const uint16_t* __r
   if (lane == 0) delta[row] = acc;
 }
 
+struct BwdArgs {
+  const int2* block_range;      // block-dense walk: the items' key ranges and selection bitmasks
+  const uint32_t* block_mask;
+  const uint16_t* kv;           // gather walk: the latent cache, selections, row starts and
+  const int32_t* idx;           // 64-slot tiles per token
+  const int32_t* ks;
+  const int32_t* row_nt;
+  const float* lse;
+  const float* delta;           // D = d_out . out per (token, head)
+  float* dq;
+  float* dkv;
+  int n_q, n_kv, H, topk;
+  float scale, scale_log2;
+  uint32_t* status;             // [0] bits, [1] bad-index count
+  unsigned long long wait_ns;
+};
+
+// HD > 0: block-dense walk over items of 64 / HD tokens x HD heads (HD == H).  HD == 0: gather
+// walk, item = (token, 64-head block), the tile = the token's next 64 selected rows, fetched by
+// the load warp with cp.async.
 template <int HD>
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_bwd_dense_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_constant__ CUtensorMap tmap_q,
-                          const __grid_constant__ CUtensorMap tmap_do, const int2* __restrict__ block_range,
-                          const uint32_t* __restrict__ block_mask, const float* __restrict__ lse,
-                          const float* __restrict__ delta, float* __restrict__ dq, float* __restrict__ dkv, int n_q,
-                          float scale, float scale_log2, uint32_t* status, unsigned long long wait_ns) {
-  constexpr int B = kC / HD;                          // tokens per item
-  constexpr int RW = kDenseMaskBytes * 8 / B / 32;    // mask words per token
+    attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_constant__ CUtensorMap tmap_q,
+                          const __grid_constant__ CUtensorMap tmap_do, const BwdArgs A) {
+  constexpr bool GATHER = HD == 0;
+  constexpr int B = GATHER ? 1 : kC / (GATHER ? 1 : HD);          // tokens per item
+  constexpr int RW = kDenseMaskBytes * 8 / B / 32;                 // mask words per token
+  const int2* __restrict__ block_range = A.block_range;
+  const uint32_t* __restrict__ block_mask = A.block_mask;
+  const float* __restrict__ lse = A.lse;
+  const float* __restrict__ delta = A.delta;
+  float* __restrict__ dq = A.dq;
+  float* __restrict__ dkv = A.dkv;
+  const int n_q = A.n_q;
+  const float scale = A.scale, scale_log2 = A.scale_log2;
+  uint32_t* status = A.status;
+  const unsigned long long wait_ns = A.wait_ns;
+  const int n_hb = GATHER ? (A.H + kC - 1) / kC : 1;
   extern __shared__ uint8_t smem_raw[];
   __shared__ BShared sh;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -140,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sDS = smem + kOffDS;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int n_items = (n_q + B - 1) / B;
+  const int n_items = GATHER ? n_q * n_hb : (n_q + B - 1) / B;
   // k-th item of this CTA: causal items grow with their index, so the walk takes them from the
   // last (largest) down, alternating directions across the CTAs each round; the partial last
   // round then holds the smallest items.  Past the end: n_items.
@@ -149,16 +186,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = k * gdim + ((k & 1) ? (gdim - 1 - b) : b);
     return r < n_items ? n_items - 1 - r : n_items;
   };
+  // tiles of an item; block-dense: lo = its first latent row
   auto item_tiles = [&](int item, int& lo) {
-    const int2 r = __ldg(block_range + item);
-    lo = r.x;
-    return r.y > r.x ? (r.y - r.x + kR - 1) / kR : 0;
+    if constexpr (GATHER) {
+      lo = 0;
+      return __ldg(A.row_nt + item / n_hb);
+    } else {
+      const int2 r = __ldg(block_range + item);
+      lo = r.x;
+      return r.y > r.x ? (r.y - r.x + kR - 1) / kR : 0;
+    }
+  };
+  // the item's first (token, head) row of q / d_out / dq and its number of real columns
+  auto item_row0 = [&](int item) -> long long {
+    if constexpr (GATHER) return static_cast<long long>(item / n_hb) * A.H + (item % n_hb) * kC;
+    else return static_cast<long long>(item) * kC;
+  };
+  auto item_cols = [&](int item) -> int {
+    if constexpr (GATHER) return min(kC, A.H - (item % n_hb) * kC);
+    else return min(kC, (n_q - item * B) * HD);
   };
 
   if (threadIdx.x == 0) {
     mbar_init(&sh.q_full, 1);
     mbar_init(&sh.q_empty, 1);
-    mbar_init(&sh.full, 1);
+    mbar_init(&sh.full, GATHER ? 1 + 32 : 1);   // gather: + the load warp's cp.async arrivals
     mbar_init(&sh.empty, 1);
     mbar_init(&sh.s_full, 1);
     mbar_init(&sh.s_empty, kSoftWarps);
@@ -170,6 +222,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&sh.dq_full, 1);
     mbar_init(&sh.dq_empty, kDrainWarps);
     mbar_init(&sh.mma_done, 1);
+    for (int i = 0; i < 3 * kR; ++i) sh.rows[i / kR][i % kR] = -1;
+    for (int i = 0; i < 3; ++i) sh.rows_tag[i] = 0xFFFFFFFFu;
     sh.abort_flag = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
@@ -182,34 +236,115 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sh.tmem_base;
+  // Gather walk: wait (bounded) until the row list of tile g is published; its products are
+  // complete by then in every caller, so this only orders the list's shared-memory writes.
+  auto wait_rows = [&](uint32_t g) -> bool {
+    const volatile uint32_t* tag = &sh.rows_tag[g % 3];
+    if (*tag != g) {
+      const uint64_t t0 = globaltimer_ns();
+      while (*tag != g) {
+        if (sh.abort_flag) return false;
+        if (globaltimer_ns() - t0 > wait_ns) {
+          sh.abort_flag = 1u;
+          atomicOr(status, DEV_ERR_TIMEOUT);
+          return false;
+        }
+      }
+    }
+    __threadfence_block();
+    return true;
+  };
 
   if (warp == 0) {
-    // ------------------------------------------------------------------ loads (one thread)
-    if (lane == 0) {
-      uint32_t g = 0, it = 0;
-      bool ok = true;
-      for (int k = 0; k * static_cast<int>(gridDim.x) < n_items && ok; ++k) {
-        const int item = snake_item(k);
-        if (item >= n_items) continue;
-        int lo;
-        const int nt = item_tiles(item, lo);
-        if (nt == 0) continue;
-        if (it > 0 && !(ok = mbar_wait_for(&sh.q_empty, (it - 1) & 1, &sh.abort_flag, status, wait_ns))) break;
-        // the item's 64 (token, head) rows of q and d_out; rows past the end read as zeros
-        const int qrow = item * kC;
-        mbar_arrive_expect_tx(&sh.q_full, (kQB + kVB) * kBlk);
+    // ------------------------------------------------------------------ loads
+    // Lane 0 takes every wait and issues the TMA copies (q and d_out; block-dense: the tile);
+    // the gather walk's tile rows come through cp.async from all 32 lanes.
+    uint32_t g = 0, it = 0;
+    bool ok = true;
+    for (int k = 0; k * static_cast<int>(gridDim.x) < n_items && ok; ++k) {
+      const int item = snake_item(k);
+      if (item >= n_items) continue;
+      int lo;
+      const int nt = item_tiles(item, lo);
+      if (nt == 0) continue;
+      bool w_ok = true;
+      if (lane == 0) {
+        if (it > 0) w_ok = mbar_wait_for(&sh.q_empty, (it - 1) & 1, &sh.abort_flag, status, wait_ns);
+        if (w_ok) {
+          // the item's 64 (token, head) rows of q and d_out; rows past the end read as zeros
+          const int qrow = static_cast<int>(item_row0(item));
+          mbar_arrive_expect_tx(&sh.q_full, (kQB + kVB) * kBlk);
 #pragma unroll 1
-        for (int kb = 0; kb < kQB; ++kb) tma_load_2d(sQD + 2 * kb * kBlk, &tmap_q, &sh.q_full, kb * 64, qrow);
+          for (int kb = 0; kb < kQB; ++kb) tma_load_2d(sQD + 2 * kb * kBlk, &tmap_q, &sh.q_full, kb * 64, qrow);
 #pragma unroll 1
-        for (int kb = 0; kb < kVB; ++kb) tma_load_2d(sQD + (2 * kb + 1) * kBlk, &tmap_do, &sh.q_full, kb * 64, qrow);
-        for (int i = 0; i < nt; ++i, ++g) {
-          if (g > 0 && !(ok = mbar_wait_for(&sh.empty, (g - 1) & 1, &sh.abort_flag, status, wait_ns))) break;
-          mbar_arrive_expect_tx(&sh.full, kQB * kBlk);
-          tma_load_3d(sR, &tmap_kv, &sh.full, 0, lo + i * kR, 0);
+          for (int kb = 0; kb < kVB; ++kb)
+            tma_load_2d(sQD + (2 * kb + 1) * kBlk, &tmap_do, &sh.q_full, kb * 64, qrow);
         }
-        ++it;
       }
-      // copies in flight land before the CTA's shared memory is released
+      ok = __shfl_sync(0xffffffffu, w_ok, 0);
+      if (!ok) break;
+      if constexpr (GATHER) {
+        // lane l copies 16-byte chunk l % 8 of slots l / 8 + 4 m (m < 16) in all nine blocks;
+        // a slot without a selection (-1, or past topk) reads zeros and is masked
+        const int t = item / n_hb;
+        const int32_t* irow = A.idx + static_cast<size_t>(t) * A.topk;
+        const long long kst = __ldg(A.ks + t);
+        const int ch = lane & 7;
+        for (int i = 0; i < nt; ++i, ++g) {
+          int crow[16];
+#pragma unroll
+          for (int m = 0; m < 16; ++m) {
+            const int slot = i * kR + (lane >> 3) + 4 * m;
+            const int j = slot < A.topk ? __ldg(irow + slot) : -1;
+            const long long row = kst + j;
+            const bool v = j >= 0 && row >= 0 && row < A.n_kv;
+            if (j >= 0 && !v && ch == 0) {
+              atomicOr(status, DEV_ERR_BAD_INDEX);
+              atomicAdd(status + 1, 1u);
+            }
+            crow[m] = v ? static_cast<int>(row) : -1;
+          }
+          if (lane == 0 && g > 0) w_ok = mbar_wait_for(&sh.empty, (g - 1) & 1, &sh.abort_flag, status, wait_ns);
+          ok = __shfl_sync(0xffffffffu, w_ok, 0);
+          if (!ok) break;
+          // the tile's row list (three tiles deep: the drains of tile g - 3 finished before the
+          // products of tile g - 1, which released this slot)
+          if (ch == 0) {
+#pragma unroll
+            for (int m = 0; m < 16; ++m) sh.rows[g % 3][(lane >> 3) + 4 * m] = crow[m];
+          }
+          __syncwarp();
+          if (lane == 0) {
+            __threadfence_block();
+            *reinterpret_cast<volatile uint32_t*>(&sh.rows_tag[g % 3]) = g;
+            mbar_arrive(&sh.full);
+          }
+#pragma unroll
+          for (int m = 0; m < 16; ++m) {
+            const int r = (lane >> 3) + 4 * m;
+            const uint16_t* rowp = A.kv + static_cast<size_t>(crow[m] >= 0 ? crow[m] : 0) * kDqk + ch * 8;
+#pragma unroll
+            for (int b = 0; b < kQB; ++b)
+              cp_async_16_zfill(smem_u32(sR + b * kBlk + sw128(r, ch)), rowp + b * 64, crow[m] >= 0);
+          }
+          cp_async_mbar_arrive(&sh.full);
+        }
+      } else {
+        if (lane == 0) {
+          for (int i = 0; i < nt; ++i, ++g) {
+            if (g > 0 && !(w_ok = mbar_wait_for(&sh.empty, (g - 1) & 1, &sh.abort_flag, status, wait_ns))) break;
+            mbar_arrive_expect_tx(&sh.full, kQB * kBlk);
+            tma_load_3d(sR, &tmap_kv, &sh.full, 0, lo + i * kR, 0);
+          }
+        }
+        g = __shfl_sync(0xffffffffu, g, 0);
+        ok = __shfl_sync(0xffffffffu, w_ok, 0);
+      }
+      ++it;
+    }
+    // copies in flight land before the CTA's shared memory is released
+    if constexpr (GATHER) cp_async_wait<0>();
+    if (lane == 0) {
       if (it > 0) mbar_drain(&sh.q_full, (it - 1) & 1, 200000000ull);
       if (g > 0) mbar_drain(&sh.full, (g - 1) & 1, 200000000ull);
     }
@@ -246,6 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!(ok = wait(&sh.q_full, it & 1))) break;
       for (int i = 0; i < nt && ok; ++i, ++g) {
         if (!(ok = wait(&sh.full, g & 1))) break;
+        if constexpr (GATHER) fence_proxy_async_smem();   // the tile was written by cp.async
         if (g > 0 && !(ok = wait(&sh.s_empty, (g - 1) & 1))) break;
         // S^T and dP^T's columns held pieces of the previous tile: wait for their drains
         if (su[1] > 0 && !(ok = wait(&sh.kv_empty[1], (su[1] - 1) & 1))) break;
@@ -333,24 +469,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (item >= n_items) continue;
       int lo;
       const int nt = item_tiles(item, lo);
-      const int n_cols = min(kC, (n_q - item * B) * HD);   // columns of real tokens
-      float* dq_item = dq + static_cast<size_t>(item) * kC * kDqk;
+      const int n_cols = item_cols(item);   // columns of real (token, head) rows
+      float* dq_item = dq + static_cast<size_t>(item_row0(item)) * kDqk;
       if (nt == 0) {
         // nothing selected: zero gradients for the item's rows of dq
         for (int e = drain_id * 32 + lane; e < n_cols * kDqk; e += kDrainWarps * 32) dq_item[e] = 0.f;
         continue;
       }
       for (int i = 0; i < nt && ok; ++i, ++g) {
-        // rows of the tile some column selects (the others add nothing to dkv)
+        // rows of the tile some column selects (the others add nothing to dkv); gather: read
+        // from the tile's row list once its first piece is complete (below)
         uint32_t any_lo = 0u, any_hi = 0u;
-        for (int b = lane; b < B; b += 32) {
-          const uint2 w = __ldg(reinterpret_cast<const uint2*>(block_mask + static_cast<size_t>(item) * kMaskWords +
-                                                               b * RW + 2 * i));
-          any_lo |= w.x;
-          any_hi |= w.y;
+        int my_row = -1;
+        if constexpr (!GATHER) {
+          for (int b = lane; b < B; b += 32) {
+            const uint2 w = __ldg(reinterpret_cast<const uint2*>(block_mask + static_cast<size_t>(item) * kMaskWords +
+                                                                 b * RW + 2 * i));
+            any_lo |= w.x;
+            any_hi |= w.y;
+          }
+          any_lo = __reduce_or_sync(0xffffffffu, any_lo);
+          any_hi = __reduce_or_sync(0xffffffffu, any_hi);
         }
-        any_lo = __reduce_or_sync(0xffffffffu, any_lo);
-        any_hi = __reduce_or_sync(0xffffffffu, any_hi);
         const long long row0 = static_cast<long long>(lo) + static_cast<long long>(i) * kR;
 #pragma unroll
         for (int m = 0; m < 5; ++m) {
@@ -360,6 +500,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           ++su[slot];
           tc_fence_after();
+          if constexpr (GATHER) {
+            if (m == 0) {
+              // this warp's 32 slots of the tile, lane j holding slot 32 set + j
+              ok = __all_sync(0xffffffffu, wait_rows(g));
+              if (!ok) break;
+              my_row = sh.rows[g % 3][32 * set + lane];
+              const uint32_t bits = __ballot_sync(0xffffffffu, my_row >= 0);
+              any_lo = set ? 0u : bits;
+              any_hi = set ? bits : 0u;
+            }
+          }
           const bool mine = m < 4 || qd >= 2;     // chunk 4's first 64 lanes repeat chunk 3
           uint32_t v[32];
           if (mine) {
@@ -371,10 +522,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) mbar_arrive(&sh.kv_empty[slot]);
           if (mine) {
             const uint32_t any = set ? any_hi : any_lo;
-            float* col = dkv + (row0 + 32 * set) * kDqk + chunk_dim0(m) + 32 * qd + lane;
+            if constexpr (GATHER) {
+              float* col = dkv + chunk_dim0(m) + 32 * qd + lane;
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if ((any >> j) & 1u) red_add_f32(col + static_cast<size_t>(j) * kDqk, __uint_as_float(v[j]));
+              for (int j = 0; j < 32; ++j) {
+                const int row = __shfl_sync(0xffffffffu, my_row, j);
+                if ((any >> j) & 1u) red_add_f32(col + static_cast<size_t>(row) * kDqk, __uint_as_float(v[j]));
+              }
+            } else {
+              float* col = dkv + (row0 + 32 * set) * kDqk + chunk_dim0(m) + 32 * qd + lane;
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if ((any >> j) & 1u) red_add_f32(col + static_cast<size_t>(j) * kDqk, __uint_as_float(v[j]));
+            }
           }
         }
       }
@@ -419,37 +579,50 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (nt == 0) continue;
       // this thread's eight columns: c = c_off + 8 kk + cq + e
       float l2[8], dd[8];
+      const int n_cols = item_cols(item);
+      const long long qrow0 = item_row0(item);
+      uint32_t col_ok = 0u;   // gather: columns of real heads (the others belong to other tokens)
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int c = c_off + 8 * kk + cq + e;
-          const bool real = item * B + c / HD < n_q;
-          const size_t row = static_cast<size_t>(item) * kC + c;
+          const bool real = c < n_cols;
+          const size_t row = static_cast<size_t>(qrow0 + c);
           l2[2 * kk + e] = real ? __ldg(lse + row) * 1.4426950408889634f : 0.f;
           dd[2 * kk + e] = real ? __ldg(delta + row) : 0.f;
+          col_ok |= (real ? 1u : 0u) << (2 * kk + e);
         }
       }
-      const uint32_t* mrow = block_mask + static_cast<size_t>(item) * kMaskWords;
+      const uint32_t* mrow = GATHER ? nullptr : block_mask + static_cast<size_t>(item) * kMaskWords;
       for (int i = 0; i < nt; ++i, ++g) {
         // selection bits of rows r0 and r0 + 8 for each column's token (e = 0, 1 share a token
-        // unless there is one head)
+        // unless there is one head); gather: all columns share the token
         uint2 mw[4][2];
+        if constexpr (!GATHER) {
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
+          for (int kk = 0; kk < 4; ++kk) {
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            if (e == 0 || HD == 1) {
-              const int b = (c_off + 8 * kk + cq + e) / HD;
-              mw[kk][e] = __ldg(reinterpret_cast<const uint2*>(mrow + b * RW + 2 * i));
-            } else {
-              mw[kk][e] = mw[kk][0];
+            for (int e = 0; e < 2; ++e) {
+              if (e == 0 || HD == 1) {
+                const int b = (c_off + 8 * kk + cq + e) / (GATHER ? 1 : HD);
+                mw[kk][e] = __ldg(reinterpret_cast<const uint2*>(mrow + b * RW + 2 * i));
+              } else {
+                mw[kk][e] = mw[kk][0];
+              }
             }
           }
         }
         ok = __all_sync(0xffffffffu, mbar_wait_for(&sh.s_full, g & 1, &sh.abort_flag, status, wait_ns));
         if (!ok) break;
         tc_fence_after();
+        bool rsel[2] = {false, false};   // gather: slots r0 and r0 + 8 hold a selection
+        if constexpr (GATHER) {
+          ok = __all_sync(0xffffffffu, wait_rows(g));
+          if (!ok) break;
+          rsel[0] = sh.rows[g % 3][r0] >= 0;
+          rsel[1] = sh.rows[g % 3][r0 + 8] >= 0;
+        }
         uint32_t vs[16], vd[16];
         tmem_ld_16x256b<4>(tmem + t_lane + kColS + c_off, vs);
         tmem_ld_16x256b<4>(tmem + t_lane + kColDP + c_off, vd);
@@ -466,8 +639,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             float p[2], ds[2];
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-              const uint2 w = mw[kk][e];
-              const bool sel = (((r < 32 ? w.x : w.y) >> (r & 31)) & 1u) != 0u;
+              bool sel;
+              if constexpr (GATHER) {
+                sel = rsel[hh] && ((col_ok >> (2 * kk + e)) & 1u);
+              } else {
+                const uint2 w = mw[kk][e];
+                sel = (((r < 32 ? w.x : w.y) >> (r & 31)) & 1u) != 0u;
+              }
               const float s = __uint_as_float(vs[4 * kk + 2 * hh + e]);
               const float dp = __uint_as_float(vd[4 * kk + 2 * hh + e]);
               p[e] = sel ? ex2_approx(s * scale_log2 - l2[2 * kk + e]) : 0.f;
@@ -493,18 +671,37 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int HD>
-cudaError_t launch_hd(const CUtensorMap& tmap_kv, const CUtensorMap& tmap_q, const CUtensorMap& tmap_do, int n_q,
-                      float scale, const DenseScratch& ds, const float* lse, const float* delta, float* dq, float* dkv,
-                      uint32_t* status, cudaStream_t st) {
-  cudaError_t e = smem_attr_once<attn_bwd_dense_kernel<HD>>(kDynSmem);
+cudaError_t launch_hd(const CUtensorMap& tmap_kv, const CUtensorMap& tmap_q, const CUtensorMap& tmap_do,
+                      const BwdArgs& A, cudaStream_t st) {
+  cudaError_t e = smem_attr_once<attn_bwd_tc_kernel<HD>>(kDynSmem);
   if (e != cudaSuccess) return e;
-  constexpr int B = kC / HD;
-  const int n_items = (n_q + B - 1) / B;
+  const int n_items = HD == 0 ? A.n_q * ((A.H + kC - 1) / kC) : (A.n_q + kC / (HD ? HD : 1) - 1) / (kC / (HD ? HD : 1));
   const int grid = n_items < device_sm_count() ? n_items : device_sm_count();
-  attn_bwd_dense_kernel<HD><<<grid, kThreads, kDynSmem, st>>>(tmap_kv, tmap_q, tmap_do, ds.block_range,
-                                                             ds.block_mask, lse, delta, dq, dkv, n_q, scale,
-                                                             scale * 1.4426950408889634f, status,
-                                                             pipeline_debug().wait_ns);
+  attn_bwd_tc_kernel<HD><<<grid, kThreads, kDynSmem, st>>>(tmap_kv, tmap_q, tmap_do, A);
+  return cudaGetLastError();
+}
+
+BwdArgs bwd_args(int n_q, int n_kv, int H, int topk, float scale, const float* lse, const float* delta, float* dq,
+                 float* dkv, uint32_t* status) {
+  BwdArgs A{};
+  A.lse = lse;
+  A.delta = delta;
+  A.dq = dq;
+  A.dkv = dkv;
+  A.n_q = n_q;
+  A.n_kv = n_kv;
+  A.H = H;
+  A.topk = topk;
+  A.scale = scale;
+  A.scale_log2 = scale * 1.4426950408889634f;
+  A.status = status;
+  A.wait_ns = pipeline_debug().wait_ns;
+  return A;
+}
+
+cudaError_t launch_delta(const void* out, const void* dout, long long n_rows, float* delta, cudaStream_t st) {
+  attn_bwd_delta_kernel<<<static_cast<unsigned>((n_rows + 7) / 8), 256, 0, st>>>(
+      static_cast<const uint16_t*>(out), static_cast<const uint16_t*>(dout), n_rows, delta);
   return cudaGetLastError();
 }
 
@@ -521,23 +718,45 @@ cudaError_t launch_sparse_attn_bwd_dense(int hd, const CUtensorMap& tmap_kv, con
                                          void* scratch, cudaStream_t st) {
   if (n_q <= 0) return cudaSuccess;
   const DenseScratch ds = dense_scratch(scratch, n_q, hd);
-  const long long n_rows = static_cast<long long>(n_q) * hd;
   int ps = prof_begin(kProfAttnPrep, st);
-  attn_bwd_delta_kernel<<<static_cast<unsigned>((n_rows + 7) / 8), 256, 0, st>>>(
-      static_cast<const uint16_t*>(out), static_cast<const uint16_t*>(dout), n_rows, delta);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_delta(out, dout, static_cast<long long>(n_q) * hd, delta, st);
   if (e == cudaSuccess) e = launch_block_mask(hd, idx, ks, n_q, n_kv, topk, ds, status, st);
   prof_end(ps, st);
   if (e != cudaSuccess) return e;
+  BwdArgs A = bwd_args(n_q, n_kv, hd, topk, scale, lse, delta, dq, dkv, status);
+  A.block_range = ds.block_range;
+  A.block_mask = ds.block_mask;
   ps = prof_begin(kProfAttnBwd, st);
   switch (hd) {
-    case 1: e = launch_hd<1>(tmap_kv, tmap_q, tmap_do, n_q, scale, ds, lse, delta, dq, dkv, status, st); break;
-    case 2: e = launch_hd<2>(tmap_kv, tmap_q, tmap_do, n_q, scale, ds, lse, delta, dq, dkv, status, st); break;
-    case 4: e = launch_hd<4>(tmap_kv, tmap_q, tmap_do, n_q, scale, ds, lse, delta, dq, dkv, status, st); break;
-    case 8: e = launch_hd<8>(tmap_kv, tmap_q, tmap_do, n_q, scale, ds, lse, delta, dq, dkv, status, st); break;
-    case 16: e = launch_hd<16>(tmap_kv, tmap_q, tmap_do, n_q, scale, ds, lse, delta, dq, dkv, status, st); break;
+    case 1: e = launch_hd<1>(tmap_kv, tmap_q, tmap_do, A, st); break;
+    case 2: e = launch_hd<2>(tmap_kv, tmap_q, tmap_do, A, st); break;
+    case 4: e = launch_hd<4>(tmap_kv, tmap_q, tmap_do, A, st); break;
+    case 8: e = launch_hd<8>(tmap_kv, tmap_q, tmap_do, A, st); break;
+    case 16: e = launch_hd<16>(tmap_kv, tmap_q, tmap_do, A, st); break;
     default: e = cudaErrorInvalidValue;
   }
+  prof_end(ps, st);
+  return e;
+}
+
+cudaError_t launch_sparse_attn_bwd_gather(const CUtensorMap& tmap_q, const CUtensorMap& tmap_do, int n_q, int n_kv,
+                                          int n_heads, int topk, float scale, const void* kv, const int32_t* idx,
+                                          const int32_t* ks, const void* out, const float* lse, const void* dout,
+                                          float* dq, float* dkv, uint32_t* status, float* delta, int32_t* row_nt,
+                                          cudaStream_t st) {
+  if (n_q <= 0) return cudaSuccess;
+  int ps = prof_begin(kProfAttnPrep, st);
+  cudaError_t e = launch_delta(out, dout, static_cast<long long>(n_q) * n_heads, delta, st);
+  if (e == cudaSuccess) e = launch_row_tiles(idx, n_q, topk, row_nt, st);
+  prof_end(ps, st);
+  if (e != cudaSuccess) return e;
+  BwdArgs A = bwd_args(n_q, n_kv, n_heads, topk, scale, lse, delta, dq, dkv, status);
+  A.kv = static_cast<const uint16_t*>(kv);
+  A.idx = idx;
+  A.ks = ks;
+  A.row_nt = row_nt;
+  ps = prof_begin(kProfAttnBwd, st);
+  e = launch_hd<0>(tmap_q, tmap_q, tmap_do, A, st);   // the gather walk reads no tile map of kv
   prof_end(ps, st);
   return e;
 }

@@ -202,6 +202,16 @@ cudaError_t launch_sparse_attn_bwd(int n_q, int n_kv, int n_heads, int topk, flo
 // tmap_do: q [n_q * hd][576] and dout [n_q * hd][512] bf16 with 128-byte swizzled boxes of
 // {64, kDenseCols}.
 size_t sparse_attn_bwd_dense_delta_bytes(int n_q, int n_heads);
+// The same gradients on the gather walk (every other shape), on tcgen05: item = (token, 64-head
+// block), each 64-slot tile of the token's selections gathered with cp.async.  delta as above;
+// row_nt: n_q int32 scratch (64-slot tiles per token).
+cudaError_t launch_sparse_attn_bwd_gather(const CUtensorMap& tmap_q, const CUtensorMap& tmap_do, int n_q, int n_kv,
+                                          int n_heads, int topk, float scale, const void* kv, const int32_t* idx,
+                                          const int32_t* ks, const void* out, const float* lse, const void* dout,
+                                          float* dq, float* dkv, uint32_t* status, float* delta, int32_t* row_nt,
+                                          cudaStream_t st);
+// row_nt[t] = number of 64-slot tiles of idx row t up to its last index >= 0.
+cudaError_t launch_row_tiles(const int32_t* idx, int n_q, int topk, int32_t* row_nt, cudaStream_t st);
 cudaError_t launch_sparse_attn_bwd_dense(int hd, const CUtensorMap& tmap_kv, const CUtensorMap& tmap_q,
                                          const CUtensorMap& tmap_do, int n_q, int n_kv, int topk, float scale,
                                          const int32_t* idx, const int32_t* ks, const void* out, const float* lse,

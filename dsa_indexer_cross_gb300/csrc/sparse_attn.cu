@@ -952,6 +952,12 @@ cudaError_t launch_gather(const CUtensorMap& tmap_kv, const CUtensorMap& tmap_q,
 }
 }  // namespace
 
+cudaError_t launch_row_tiles(const int32_t* idx, int n_q, int topk, int32_t* row_nt, cudaStream_t st) {
+  if (n_q <= 0) return cudaSuccess;
+  row_tiles_kernel<<<(n_q + 7) / 8, 256, 0, st>>>(idx, n_q, topk, row_nt);
+  return cudaGetLastError();
+}
+
 DenseScratch dense_scratch(void* scratch, int n_q, int hd) {
   const int b = kDenseCols / hd;
   const int n_blk = (n_q + b - 1) / b;

@@ -32,7 +32,8 @@ def _built():
 # rows an all-empty chunk between two selected ones
 @pytest.mark.parametrize("n_q,n_kv,H,topk", [(48, 200, 16, 64), (30, 120, 40, 48), (17, 90, 4, 40),
                                              (20, 700, 16, 200), (12, 500, 40, 136),
-                                             (8, 300, 64, 128), (6, 300, 128, 128)])   # decode / chunk head counts
+                                             (8, 300, 64, 128), (6, 300, 128, 128),   # decode / chunk head counts
+                                             (3, 100, 16, 40)])   # fewer than 64 (token, head) rows: per-token kernel
 def test_backward_matches_oracle(n_q, n_kv, H, topk):
     rng = np.random.default_rng(n_q + H)
     ks = rng.integers(0, n_kv // 3, size=n_q).astype(np.int32)
@@ -200,3 +201,34 @@ def test_backward_prefill_4k_sampled():
     tail = list(range(n_q - 96, n_q))
     _, dkv_ref = O.sparse_attn_backward(q64[tail], kv64, idx[tail], geo.ks[tail], scale, do64[tail])
     assert _rel_rows(dkv[n_q - 96:].double().cpu().numpy(), dkv_ref[n_q - 96:]) <= 5e-2
+
+
+def test_backward_gather_walk_long_rows():
+    # the tcgen05 gather walk: 64 tokens x 64 heads, each selecting up to k = 2048 random rows of
+    # a 20000-row cache (32 tiles of 64 slots, rows shared by a few tokens), some rows shorter
+    # than k, one token selecting nothing
+    n_q, n_kv, H, topk = 64, 20000, 64, 2048
+    rng = np.random.default_rng(29)
+    ks = np.zeros(n_q, dtype=np.int32)
+    idx = np.full((n_q, topk), -1, dtype=np.int32)
+    for t in range(n_q):
+        L = topk if t % 5 else int(rng.integers(1, topk))
+        idx[t, :L] = np.sort(rng.choice(n_kv, size=L, replace=False))
+    idx[9] = -1
+    g = torch.Generator(device=DEV)
+    g.manual_seed(31)
+    q = (torch.randn((n_q, H, 576), generator=g, device=DEV) / 24.0).to(torch.bfloat16)
+    kv = (torch.randn((n_kv, 576), generator=g, device=DEV) / 24.0).to(torch.bfloat16)
+    d_out = torch.randn((n_q, H, 512), generator=g, device=DEV).to(torch.bfloat16)
+    scale = 1.0 / math.sqrt(576)
+    dq, dkv, bits = _fwd_bwd(q, kv, idx, ks, scale, d_out)
+    assert bits == 0
+    f = synth.to_f64
+    dq_ref, dkv_ref = O.sparse_attn_backward(f(q), f(kv), idx, ks, scale, f(d_out))
+    dq_g, dkv_g = dq.double().cpu().numpy(), dkv.double().cpu().numpy()
+    assert _rel_rows(dq_g, dq_ref) <= 5e-2
+    used = np.unique(idx[idx >= 0])
+    assert _rel_rows(dkv_g[used], dkv_ref[used]) <= 5e-2
+    assert not dq_g[9].any()
+    unused = np.setdiff1d(np.arange(n_kv), used)
+    assert not dkv_g[unused].any()
