@@ -48,6 +48,8 @@
 // blocks may still be in flight.  Persistent CTAs.
 #include <cuda_bf16.h>
 
+#include <algorithm>
+
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -149,21 +151,39 @@ __device__ __forceinline__ uint32_t sw128(int row, int chunk) {
   return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
+// Gather walk split over several CTAs per (token, head block) (few tokens, long selections:
+// decode): split s of n walks the token's tiles [s T / n, (s + 1) T / n) and writes its output
+// normalised by its own running sum, in fp32, with its log-sum-exp; a combine pass merges the
+// splits.  n == 1: no split, the kernel writes out and lse itself.
+struct SplitOut {
+  int n;
+  float* o;      // [n][n_q * H][512]
+  float* lse;    // [n][n_q * H]
+};
+
 // Work item description shared by all roles.
 struct Item {
   int t0;        // gather: the token; block-dense: first token of the block
   int hb;        // gather: head block; block-dense: 0
   int nt;        // tiles of 64 rows
   int lo;        // block-dense: first latent row of the block's range
+  int i0;        // gather: first tile of the split
+  int split;     // gather: split index
 };
 
 template <int HB, int HD>
-__device__ __forceinline__ Item item_info(int item, int n_hb, const int32_t* row_nt, const int2* block_range) {
+__device__ __forceinline__ Item item_info(int item, int n_hb, int n_split, const int32_t* row_nt,
+                                          const int2* block_range) {
   Item it{};
   if constexpr (HD == 0) {
-    it.t0 = item / n_hb;
-    it.hb = item - it.t0 * n_hb;
-    it.nt = __ldg(row_nt + it.t0);
+    const int per_tok = n_hb * n_split;
+    it.t0 = item / per_tok;
+    const int r = item - it.t0 * per_tok;
+    it.hb = r / n_split;
+    it.split = r - it.hb * n_split;
+    const int T = __ldg(row_nt + it.t0);
+    it.i0 = (it.split * T) / n_split;
+    it.nt = ((it.split + 1) * T) / n_split - it.i0;
     it.lo = 0;
   } else {
     it.t0 = item * (HB / HD);
@@ -219,7 +239,7 @@ __global__ void __launch_bounds__(ACfg<HB, HD>::THREADS, 1)
                        const int2* __restrict__ block_range, const uint32_t* __restrict__ block_mask,
                        uint16_t* __restrict__ out, float* __restrict__ lse, int n_q, int n_kv, int H, int topk,
                        float scale_log2, uint32_t* status, uint32_t* bad_count, unsigned long long wait_ns,
-                       int stop_after) {
+                       int stop_after, const SplitOut split) {
   using C = ACfg<HB, HD>;
   constexpr bool DENSE = C::DENSE;
   constexpr int B = C::B;
@@ -233,7 +253,8 @@ __global__ void __launch_bounds__(ACfg<HB, HD>::THREADS, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int n_hb = DENSE ? 1 : (H + HB - 1) / HB;
-  const int n_items = DENSE ? (n_q + B - 1) / B : n_q * n_hb;
+  const int n_split = DENSE ? 1 : split.n;
+  const int n_items = DENSE ? (n_q + B - 1) / B : n_q * n_hb * n_split;
   // k-th item of this CTA in "snake" order (forward on even rounds, backward on odd ones):
   // causal items grow with their index, so alternating directions balances the CTAs.  The
   // block-dense walk takes its items from the last (largest) down, so that the partial last
@@ -293,7 +314,7 @@ __global__ void __launch_bounds__(ACfg<HB, HD>::THREADS, 1)
     for (int k = 0; k * static_cast<int>(gridDim.x) < n_items && ok; ++k) {
       const int item = snake_item(k);
       if (item >= n_items) continue;
-      const Item I = item_info<HB, HD>(item, n_hb, row_nt, block_range);
+      const Item I = item_info<HB, HD>(item, n_hb, n_split, row_nt, block_range);
       if (I.nt == 0) continue;
       bool w_ok = true;
       if (tid == 0) {
@@ -362,14 +383,14 @@ __global__ void __launch_bounds__(ACfg<HB, HD>::THREADS, 1)
         // previous tile's slot wait and copies
         int jn[8];
 #pragma unroll
-        for (int m = 0; m < 8; ++m) jn[m] = index_of((tid >> 3) + 8 * m);
+        for (int m = 0; m < 8; ++m) jn[m] = index_of(I.i0 * kRows + (tid >> 3) + 8 * m);
         for (int i = 0; i < I.nt; ++i, ++g) {
           int crow[8];
 #pragma unroll
           for (int m = 0; m < 8; ++m) crow[m] = row_of(jn[m], (tid & 7) == 0);
           if (i + 1 < I.nt) {
 #pragma unroll
-            for (int m = 0; m < 8; ++m) jn[m] = index_of((i + 1) * kRows + (tid >> 3) + 8 * m);
+            for (int m = 0; m < 8; ++m) jn[m] = index_of((I.i0 + i + 1) * kRows + (tid >> 3) + 8 * m);
           }
           // test hook: stop feeding the pipeline; the waits behind it run out
           w_ok = stop_after < 0 || g < static_cast<uint32_t>(stop_after);
@@ -418,12 +439,23 @@ __global__ void __launch_bounds__(ACfg<HB, HD>::THREADS, 1)
     for (int k = 0; k * static_cast<int>(gridDim.x) < n_items && !stop; ++k) {
       const int item = snake_item(k);
       if (item >= n_items) continue;
-      const Item I = item_info<HB, HD>(item, n_hb, row_nt, block_range);
+      const Item I = item_info<HB, HD>(item, n_hb, n_split, row_nt, block_range);
       // column c -> (token, head)
       auto col_token = [&](int c) { return DENSE ? I.t0 + c / (DENSE ? HD : 1) : I.t0; };
       auto col_head = [&](int c) { return DENSE ? c % (DENSE ? HD : 1) : I.hb * HB + c; };
       auto col_ok = [&](int c) { return col_token(c) < n_q && col_head(c) < H; };
       if (I.nt == 0) {
+        if (n_split > 1) {
+          // an empty split: weight zero in the combine
+          const size_t pbase = static_cast<size_t>(I.split) * n_q * H;
+          for (int e = tid; e < HB * kDv; e += kSoft) {
+            const int c = e / kDv;
+            if (col_ok(c))
+              split.o[(pbase + static_cast<size_t>(col_token(c)) * H + col_head(c)) * kDv + (e - c * kDv)] = 0.f;
+          }
+          if (tid < HB && col_ok(tid)) split.lse[pbase + static_cast<size_t>(col_token(tid)) * H + col_head(tid)] = -INFINITY;
+          continue;
+        }
         for (int e = tid; e < HB * kDv; e += kSoft) {
           const int c = e / kDv;
           if (col_ok(c))
@@ -464,7 +496,7 @@ __global__ void __launch_bounds__(ACfg<HB, HD>::THREADS, 1)
         const int sb = g & 1;
         bool rv0 = false, rv1 = false;   // gather: rows r0 / r0 + 8 hold a valid selection
         if constexpr (!DENSE) {
-          const int s0 = i * kRows + r0, s1 = s0 + 8;
+          const int s0 = (I.i0 + i) * kRows + r0, s1 = s0 + 8;
           const int j0 = s0 < topk ? __ldg(irow + s0) : -1;
           const int j1 = s1 < topk ? __ldg(irow + s1) : -1;
           if constexpr (PAGED) {
@@ -654,6 +686,21 @@ __global__ void __launch_bounds__(ACfg<HB, HD>::THREADS, 1)
           for (int b = 0; b < 4; ++b) tmem_ld16(tmem + t_lane + C::O_COL + b * HB + hh * 16, o[b]);
           tmem_ld_wait();
 #pragma unroll
+          if (n_split > 1) {
+            // this split's output, fp32, normalised by its own sum
+            float* pbase = split.o + (static_cast<size_t>(I.split) * n_q * H + row0) * kDv + qd * 32 + lane;
+#pragma unroll
+            for (int h = 0; h < 16; ++h) {
+              const int c = hh * 16 + h;
+              if (c < n_cols) {
+#pragma unroll
+                for (int b = 0; b < 4; ++b)
+                  pbase[static_cast<long long>(c) * kDv + b * 128] = __uint_as_float(o[b][h]) * inv[h];
+              }
+            }
+            continue;
+          }
+#pragma unroll
           for (int h = 0; h < 16; ++h) {
             const int c = hh * 16 + h;
             if (c < n_cols) {
@@ -667,10 +714,15 @@ __global__ void __launch_bounds__(ACfg<HB, HD>::THREADS, 1)
           }
         }
       }
-      if (lse && tid < HB && col_ok(tid)) {
+      if (tid < HB && col_ok(tid)) {
         const float lv = sh.l_run[tid];
-        lse[static_cast<size_t>(col_token(tid)) * H + col_head(tid)] =
-            lv > 0.f ? (sh.m_used[tid] + log2f(lv)) * 0.69314718055994531f : -INFINITY;
+        const float lval = lv > 0.f ? (sh.m_used[tid] + log2f(lv)) * 0.69314718055994531f : -INFINITY;
+        const size_t r = static_cast<size_t>(col_token(tid)) * H + col_head(tid);
+        if (n_split > 1) {
+          split.lse[static_cast<size_t>(I.split) * n_q * H + r] = lval;
+        } else if (lse) {
+          lse[r] = lval;
+        }
       }
       tc_fence_before();
       __syncwarp();
@@ -696,7 +748,7 @@ __global__ void __launch_bounds__(ACfg<HB, HD>::THREADS, 1)
     for (int k = 0; k * static_cast<int>(gridDim.x) < n_items && ok; ++k) {
       const int item = snake_item(k);
       if (item >= n_items) continue;
-      const Item I = item_info<HB, HD>(item, n_hb, row_nt, block_range);
+      const Item I = item_info<HB, HD>(item, n_hb, n_split, row_nt, block_range);
       if (I.nt == 0) continue;
       if (qk_warp) {
         // S^T(g) = tile . Q^T once the whole tile has landed
@@ -866,17 +918,59 @@ __global__ void __launch_bounds__(256) block_mask_kernel(const int32_t* __restri
   for (int i = threadIdx.x; i < kWords / 4; i += blockDim.x) dst[i] = reinterpret_cast<const uint4*>(mask)[i];
 }
 
+// Merge of the gather walk's splits: per (token, head) row, out = sum_s w_s o_s / sum_s w_s
+// with w_s = exp(lse_s - max lse), lse = max + log(sum w_s); a row whose splits are all empty
+// gets zeros and -inf.  One warp per row.
+__global__ void __launch_bounds__(256) split_combine_kernel(const float* __restrict__ po, const float* __restrict__ plse,
+                                                            int n_split, long long n_rows, uint16_t* __restrict__ out,
+                                                            float* __restrict__ lse) {
+  const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= n_rows) return;
+  float m = -INFINITY;
+  for (int s = 0; s < n_split; ++s) m = fmaxf(m, __ldg(plse + s * n_rows + row));
+  float acc[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+  float den = 0.f;
+  if (m > -INFINITY) {
+    for (int s = 0; s < n_split; ++s) {
+      const float ls = __ldg(plse + s * n_rows + row);
+      const float w = ls > -INFINITY ? __expf(ls - m) : 0.f;
+      den += w;
+      const float4* src = reinterpret_cast<const float4*>(po + (s * n_rows + row) * kDv);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float4 v = __ldg(src + lane + 32 * i);
+        acc[4 * i] += w * v.x;
+        acc[4 * i + 1] += w * v.y;
+        acc[4 * i + 2] += w * v.z;
+        acc[4 * i + 3] += w * v.w;
+      }
+    }
+  }
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  uint2* dst = reinterpret_cast<uint2*>(out + row * kDv);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __nv_bfloat162 a = __floats2bfloat162_rn(acc[4 * i] * inv, acc[4 * i + 1] * inv);
+    const __nv_bfloat162 b = __floats2bfloat162_rn(acc[4 * i + 2] * inv, acc[4 * i + 3] * inv);
+    dst[lane + 32 * i] = make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+  }
+  if (lse && lane == 0) lse[row] = den > 0.f ? m + __logf(den) : -INFINITY;
+}
+
 template <int HB, int HD, bool PAGED = false>
 cudaError_t launch_cfg(const CUtensorMap& tmap, const CUtensorMap& tmap_q, int n_q, int n_kv, int H, int topk,
                        float scale, const void* kv, const int32_t* idx, const int32_t* ks, const PagedRows& pg,
                        const int32_t* row_nt,
                        const int2* block_range, const uint32_t* block_mask, void* out, float* lse, uint32_t* status,
-                       cudaStream_t st) {
+                       cudaStream_t st, const SplitOut& split = SplitOut{1, nullptr, nullptr}) {
   using C = ACfg<HB, HD>;
   auto kern = sparse_attn_kernel<HB, HD, PAGED>;
   cudaError_t e = smem_attr_once<sparse_attn_kernel<HB, HD, PAGED>>(C::DYN_SMEM);
   if (e != cudaSuccess) return e;
-  const int n_items = C::DENSE ? (n_q + C::B - 1) / C::B : n_q * ((H + HB - 1) / HB);
+  const int n_items = C::DENSE ? (n_q + C::B - 1) / C::B : n_q * ((H + HB - 1) / HB) * split.n;
   const int grid = n_items < device_sm_count() ? n_items : device_sm_count();
   const PipelineDebug dbg = pipeline_debug();
   const int ps = prof_begin(kProfAttn, st);
@@ -884,10 +978,19 @@ cudaError_t launch_cfg(const CUtensorMap& tmap, const CUtensorMap& tmap_q, int n
                                             block_range, block_mask,
                                             static_cast<uint16_t*>(out), lse, n_q, n_kv, H, topk,
                                             scale * 1.4426950408889634f, status, status + 1, dbg.wait_ns,
-                                            dbg.stop_after_tiles);
+                                            dbg.stop_after_tiles, split);
+  e = cudaGetLastError();
+  if (e == cudaSuccess && !C::DENSE && split.n > 1) {
+    // merge the splits (inside the same launch-log entry: one attention call)
+    const long long rows = static_cast<long long>(n_q) * H;
+    split_combine_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, st>>>(split.o, split.lse, split.n, rows,
+                                                                               static_cast<uint16_t*>(out), lse);
+    e = cudaGetLastError();
+  }
   prof_end(ps, st);
-  return cudaGetLastError();
+  return e;
 }
+
 
 }  // namespace
 
@@ -943,12 +1046,37 @@ template <int HB>
 cudaError_t launch_gather(const CUtensorMap& tmap_kv, const CUtensorMap& tmap_q, int n_q, int n_kv, int n_heads,
                           int topk, float scale, const void* kv, const int32_t* idx, const int32_t* ks,
                           const PagedRows& pg, const int32_t* row_nt, void* out, float* lse, uint32_t* status,
-                          cudaStream_t st) {
+                          const SplitOut& split, cudaStream_t st) {
   if (pg.block_table)
     return launch_cfg<HB, 0, true>(tmap_kv, tmap_q, n_q, n_kv, n_heads, topk, scale, kv, idx, ks, pg, row_nt, nullptr,
-                                   nullptr, out, lse, status, st);
+                                   nullptr, out, lse, status, st, split);
   return launch_cfg<HB, 0, false>(tmap_kv, tmap_q, n_q, n_kv, n_heads, topk, scale, kv, idx, ks, pg, row_nt, nullptr,
-                                  nullptr, out, lse, status, st);
+                                  nullptr, out, lse, status, st, split);
+}
+
+// Splits of each (token, head block) in the gather walk: when the items leave SMs idle, as many
+// as still fit one round of the persistent CTAs (a second round repeats each split's fixed
+// costs -- q, the pipeline fill, its fp32 output -- for no gain), each split keeping at least
+// four 64-row tiles, at most eight.
+int gather_splits(int n_q, int n_heads, int topk) {
+  const int hb = n_heads <= 16 ? 16 : n_heads <= 32 ? 32 : 64;
+  const long long items = static_cast<long long>(n_q) * ((n_heads + hb - 1) / hb);
+  const int sms = device_sm_count();
+  if (items <= 0 || 2 * items > sms) return 1;
+  int ns = static_cast<int>(sms / items);
+  const int tiles = (topk + kRows - 1) / kRows;
+  ns = std::min(ns, std::max(1, tiles / 4));
+  return std::max(1, std::min(ns, 8));
+}
+
+// Gather-walk scratch: row_nt (n_q int32), then for splits the per-split fp32 outputs and
+// log-sum-exps.
+size_t gather_split_offset(int n_q) { return (static_cast<size_t>(n_q) * sizeof(int32_t) + 15) & ~size_t(15); }
+size_t gather_ws_bytes(int n_q, int n_heads, int topk) {
+  const int ns = gather_splits(n_q, n_heads, topk);
+  size_t b = gather_split_offset(n_q);
+  if (ns > 1) b += static_cast<size_t>(ns) * n_q * n_heads * (kDv + 1) * sizeof(float);
+  return b;
 }
 }  // namespace
 
@@ -981,12 +1109,15 @@ cudaError_t launch_block_mask(int hd, const int32_t* idx, const int32_t* ks, int
 }
 
 size_t sparse_attn_ws_bytes(int n_q, int n_heads, int n_kv, int topk) {
+  // the gather walk's needs always (a paged cache takes it whatever the shape), the
+  // block-dense walk's when that applies
+  size_t b = gather_ws_bytes(n_q, n_heads, topk);
   const int hd = sparse_attn_dense_heads(n_heads, n_kv, topk);
   if (hd) {
     const int n_blk = (n_q + kDenseCols / hd - 1) / (kDenseCols / hd);
-    return dense_mask_offset(n_blk) + static_cast<size_t>(n_blk) * kMaskBytes;
+    b = std::max(b, dense_mask_offset(n_blk) + static_cast<size_t>(n_blk) * kMaskBytes);
   }
-  return static_cast<size_t>(n_q) * sizeof(int32_t);
+  return b;
 }
 
 int sparse_attn_q_box_rows(int n_heads, int n_kv, int topk, bool paged) {
@@ -1015,13 +1146,18 @@ cudaError_t launch_sparse_attn(const CUtensorMap& tmap_kv, const CUtensorMap& tm
   prof_end(ps, st);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  SplitOut split{gather_splits(n_q, n_heads, topk), nullptr, nullptr};
+  if (split.n > 1) {
+    split.o = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + gather_split_offset(n_q));
+    split.lse = split.o + static_cast<size_t>(split.n) * n_q * n_heads * kDv;
+  }
   switch (sparse_attn_q_box_rows(n_heads, n_kv, topk, pg.block_table != nullptr)) {
     case 16: return launch_gather<16>(tmap_kv, tmap_q, n_q, n_kv, n_heads, topk, scale, kv, idx, ks, pg, row_nt, out,
-                                      lse, status, st);
+                                      lse, status, split, st);
     case 32: return launch_gather<32>(tmap_kv, tmap_q, n_q, n_kv, n_heads, topk, scale, kv, idx, ks, pg, row_nt, out,
-                                      lse, status, st);
+                                      lse, status, split, st);
     default: return launch_gather<64>(tmap_kv, tmap_q, n_q, n_kv, n_heads, topk, scale, kv, idx, ks, pg, row_nt, out,
-                                      lse, status, st);
+                                      lse, status, split, st);
   }
 }
 

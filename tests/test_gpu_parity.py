@@ -193,6 +193,33 @@ def test_attention_gather_walk_for_small_heads(H):
     assert torch.all(out[5] == 0) and torch.all(torch.isneginf(lse[5]))
 
 
+@pytest.mark.parametrize("H", [64, 128])
+def test_attention_gather_walk_split_over_ctas(H):
+    # few tokens with long index rows: each (token, head block) is split over several CTAs whose
+    # partial outputs a combine pass merges; rows of 1 to 32 tiles give splits with no tile at
+    # all, one token selects nothing
+    rng = np.random.default_rng(200 + H)
+    n_q, n_kv, topk = 5, 9000, 2048
+    ks = rng.integers(0, 500, n_q).astype(np.int32)
+    idx = np.full((n_q, topk), -1, dtype=np.int32)
+    lengths = [2048, 1, 300, 0, 1111]
+    for t, L in enumerate(lengths):
+        idx[t, :L] = rng.permutation(8000)[:L]
+    idx[0, rng.random(topk) < 0.05] = -1     # scattered unused slots
+    geo = synth.Geometry(n_kv, np.zeros(n_q, np.int32), np.zeros(n_kv, np.int32), ks, ks)
+    w = synth.Workload("split", "decode", n_q, ("full", "shared"), 4, 64, 0, 1e4, topk, H)
+    L = synth.layer_inputs(w, geo, 1, device=DEV, attn_scale="unit")
+    out, lse, bits = run_attn(w, geo, L, torch.from_numpy(idx).to(DEV))
+    assert bits == 0
+    o_ref, lse_ref = oracle_attn(w, geo, L, idx, range(n_q))
+    e_o, e_l = attn_errors(out, lse, o_ref, lse_ref, range(n_q))
+    assert e_o <= ATOL_OUT and e_l <= ATOL_LSE, (e_o, e_l)
+    assert torch.all(out[3] == 0) and torch.all(torch.isneginf(lse[3]))
+    # the same call without lse writes the same output
+    out2, _, bits2 = run_attn(w, geo, L, torch.from_numpy(idx).to(DEV), lse=False)
+    assert bits2 == 0 and torch.equal(out, out2)
+
+
 def test_indexer_rising_scores_cut_back_the_buffer():
     """Scores that rise along the keys beat every streaming threshold, so a long row's
     candidate buffer fills up and has to be cut back to its exact top-k (ties to the lower
