@@ -145,6 +145,7 @@ struct BwdArgs {
   float scale, scale_log2;
   uint32_t* status;             // [0] bits, [1] bad-index count
   unsigned long long wait_ns;
+  int stop_after;               // test hook: the load warp stops after this many tiles (< 0: never)
 };
 
 // HD > 0: block-dense walk over items of 64 / HD tokens x HD heads (HD == H).  HD == 0: gather
@@ -159,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const int32_t* __restrict__ row_nt, const float* __restrict__ lse,
                        const float* __restrict__ delta, float* __restrict__ dq, float* __restrict__ dkv, int n_q,
                        int n_kv, int H, int topk, float scale, float scale_log2, uint32_t* status,
-                       unsigned long long wait_ns) {
+                       unsigned long long wait_ns, int stop_after) {
   // (separate __restrict__ parameters: passing them in one struct cost 4% on the block-dense walk)
   constexpr bool GATHER = HD == 0;
   constexpr int B = GATHER ? 1 : kC / (GATHER ? 1 : HD);          // tokens per item
@@ -301,7 +302,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             crow[m] = v ? static_cast<int>(row) : -1;
           }
-          if (lane == 0 && g > 0) w_ok = mbar_wait_for(&sh.empty, (g - 1) & 1, &sh.abort_flag, status, wait_ns);
+          // test hook: stop feeding the pipeline; the waits behind it run out
+          if (stop_after >= 0 && g >= static_cast<uint32_t>(stop_after)) w_ok = false;
+          if (lane == 0 && g > 0 && w_ok)
+            w_ok = mbar_wait_for(&sh.empty, (g - 1) & 1, &sh.abort_flag, status, wait_ns);
           ok = __shfl_sync(0xffffffffu, w_ok, 0);
           if (!ok) break;
           // the tile's row list (three tiles deep: the drains of tile g - 3 finished before the
@@ -329,6 +333,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         if (lane == 0) {
           for (int i = 0; i < nt; ++i, ++g) {
+            if (stop_after >= 0 && g >= static_cast<uint32_t>(stop_after)) {
+              w_ok = false;   // test hook: stop feeding the pipeline; the waits behind it run out
+              break;
+            }
             if (g > 0 && !(w_ok = mbar_wait_for(&sh.empty, (g - 1) & 1, &sh.abort_flag, status, wait_ns))) break;
             mbar_arrive_expect_tx(&sh.full, kQB * kBlk);
             tma_load_3d(sR, &tmap_kv, &sh.full, 0, lo + i * kR, 0);
@@ -676,7 +684,7 @@ cudaError_t launch_hd(const CUtensorMap& tmap_kv, const CUtensorMap& tmap_q, con
   const int grid = n_items < device_sm_count() ? n_items : device_sm_count();
   attn_bwd_tc_kernel<HD><<<grid, kThreads, kDynSmem, st>>>(
       tmap_kv, tmap_q, tmap_do, A.block_range, A.block_mask, A.kv, A.idx, A.ks, A.row_nt, A.lse, A.delta, A.dq, A.dkv,
-      A.n_q, A.n_kv, A.H, A.topk, A.scale, A.scale_log2, A.status, A.wait_ns);
+      A.n_q, A.n_kv, A.H, A.topk, A.scale, A.scale_log2, A.status, A.wait_ns, A.stop_after);
   return cudaGetLastError();
 }
 
@@ -694,7 +702,9 @@ BwdArgs bwd_args(int n_q, int n_kv, int H, int topk, float scale, const float* l
   A.scale = scale;
   A.scale_log2 = scale * 1.4426950408889634f;
   A.status = status;
-  A.wait_ns = pipeline_debug().wait_ns;
+  const PipelineDebug dbg = pipeline_debug();
+  A.wait_ns = dbg.wait_ns;
+  A.stop_after = dbg.stop_after_tiles;
   return A;
 }
 

@@ -102,3 +102,48 @@ def test_attention_wait_runs_out_then_the_workspace_is_clean(hook, heads):
     o_ref, l_ref = oracle_attn(w, geo, L, idx_np, rows)
     got = synth.to_f64(out[torch.as_tensor(rows, device="cuda")])
     assert float(np.abs(got - o_ref).max()) <= 1e-2
+
+
+@pytest.mark.parametrize("heads", [16, 64])   # the backward's block-dense walk (16 heads) and gather walk (64)
+def test_attention_backward_wait_runs_out_then_the_workspace_is_clean(hook, heads):
+    import math
+    n_q, n_kv, topk = 512, 512, 256
+    rng = np.random.default_rng(heads)
+    idx_np = np.full((n_q, topk), -1, dtype=np.int32)
+    for t in range(n_q):
+        k = min(topk, t + 1)
+        idx_np[t, :k] = np.sort(rng.permutation(t + 1)[:k])
+    idx = torch.from_numpy(idx_np).cuda()
+    ks = torch.zeros(n_q, dtype=torch.int32, device="cuda")
+    g = torch.Generator(device="cuda")
+    g.manual_seed(heads)
+    q = (torch.randn((n_q, heads, 576), generator=g, device="cuda") / 24.0).to(torch.bfloat16)
+    kv = (torch.randn((n_kv, 576), generator=g, device="cuda") / 24.0).to(torch.bfloat16)
+    d_out = torch.randn((n_q, heads, 512), generator=g, device="cuda").to(torch.bfloat16)
+    desc = D.attn_desc(n_q, n_kv, heads, topk, 1.0 / math.sqrt(576))
+    out = torch.empty((n_q, heads, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((n_q, heads), dtype=torch.float32, device="cuda")
+    assert D.dsa_workspace_status(D.dsa_sparse_attn(desc, q, kv, idx, ks, out, lse)) == 0
+
+    def bwd(ws=None):
+        dq = torch.full((n_q, heads, 576), 5.0, dtype=torch.float32, device="cuda")
+        dkv = torch.full((n_kv, 576), 7.0, dtype=torch.float32, device="cuda")
+        ws = D.dsa_sparse_attn_backward(desc, q, kv, idx, ks, out, lse, d_out, dq, dkv, ws=ws)
+        return dq, dkv, ws
+
+    dq_ref, dkv_ref, ws_ref = bwd()
+    assert D.dsa_workspace_status(ws_ref) == 0
+    D.dsa_debug_pipeline(stop_after_tiles=2, wait_ns=1_000_000)
+    _, _, ws = bwd()
+    bits = D.dsa_workspace_status(ws, raise_on_fault=False)
+    assert bits & TIMEOUT_BIT, f"status bits 0x{bits:x}: no wait ran out"
+    with pytest.raises(D.DsaError) as e:
+        D.dsa_workspace_status(ws)
+    assert e.value.name == "DSA_ERR_TIMEOUT"
+
+    D.dsa_debug_pipeline(-1, 0)
+    dq2, dkv2, _ = bwd(ws)                       # the same workspace, now a normal call
+    assert D.dsa_workspace_status(ws) == 0
+    assert torch.equal(dq2, dq_ref)              # written once per (token, head) row
+    # fp32 reductions in a different order: last bits of each sum, cancellation included
+    torch.testing.assert_close(dkv2, dkv_ref, rtol=1e-4, atol=1e-5 * float(dkv_ref.abs().max()))
