@@ -15,17 +15,19 @@
 // per tile run on the tensor core, all from tiles that are already in shared memory:
 //     X[j, h]   = K[j, :] . Q[h, :]      M = 128 keys, N = 64 heads, K = d    (A, B K-major)
 //     dK[j, :]  = G[j, :] . Q[:, :]      M = 128 keys, N = d, K = 64 heads     (A K-major, B MN-major)
+//       or its transpose dK^T = Q^T G^T  M = d, N = 128 keys                     (A MN-major, B K-major)
 //     dQ^T[:, h] += K[:, :]^T . G[:, h]  M = d, N = 64 heads, K = 128 keys     (A, B MN-major)
 // Heads are padded to 64 with zero rows of Q and zero weights (so G is one 128-byte row per
 // key).  X and dK are double-buffered in TMEM, dQ^T accumulates over the query's tiles (two
 // buffers, one per query parity).  The epilogue reads X, keeps the per-head dw sums in
-// registers, writes G into shared memory in the 128-byte-swizzled layout, and adds each dK
-// row into dk~ with vector atomics (rows selected by several queries receive several adds:
-// the order, and the last bits of dk, vary between runs).  dq~ is written once per query.
+// registers, writes G into shared memory in the 128-byte-swizzled layout, and adds dK into dk~
+// with fp32 reductions, in one of two forms chosen per call (template parameter TR, below).
+// Rows selected by several queries receive several adds: the order, and the last bits of dk,
+// vary between runs.  dq~ is written once per query.
 //
 // Warp roles (256 threads): warps 0-1 gather Q, w and the selected key rows with cp.async
-// (zero-filled where a slot is empty); warp 2 issues the products; warp 3 owns TMEM; warps
-// 4-7 run the epilogue, one TMEM lane quarter each.  Every wait is bounded.
+// (zero-filled where a slot is empty); warp 2 issues X; warp 3 owns TMEM and issues dK and
+// dQ^T; warps 4-7 run the epilogue, one TMEM lane quarter each.  Every wait is bounded.
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -84,6 +86,9 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   const __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&p);
 }
+__device__ __forceinline__ void red_add_f32(float* addr, float v) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
+}
 __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
                : "memory");
@@ -106,6 +111,11 @@ __device__ __forceinline__ bool warp_all_wait(uint64_t* bar, uint32_t parity, vo
   return __all_sync(0xffffffffu, mbar_wait_for(bar, parity, abort_flag, status, limit_ns));
 }
 
+// TR: dK computed transposed (dK^T, a TMEM lane per dim) and added with 128-byte scalar
+// reductions per key row; else dK (a TMEM lane per key) added with 16-byte reductions, one
+// key row per thread.  The first wins when few queries share a key row (long caches), the
+// second when many do (a short causal prefix, whose rows every query reduces into at once).
+template <bool TR>
 __global__ void __launch_bounds__(kBwdThreads, 1) indexer_bwd_kernel(const BwdArgs A) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ BwdShared sh;
@@ -120,7 +130,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) indexer_bwd_kernel(const BwdAr
   if (threadIdx.x == 0) {
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sh.q_full[b], kProdThreads);
-      mbar_init(&sh.q_empty[b], 1);
+      mbar_init(&sh.q_empty[b], 2);   // both MMA warps read Q
       mbar_init(&sh.x_full[b], 1);
       mbar_init(&sh.x_empty[b], 4);
       mbar_init(&sh.g_full[b], 4);
@@ -132,9 +142,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) indexer_bwd_kernel(const BwdAr
     }
     for (int s = 0; s < kStagesB; ++s) {
       mbar_init(&sh.k_full[s], kProdThreads);
-      mbar_init(&sh.k_empty[s], 1);
+      mbar_init(&sh.k_empty[s], 2);   // X (warp 2) and dQ^T (warp 3) read the K tile
     }
-    mbar_init(&sh.mma_done, 1);
+    mbar_init(&sh.mma_done, 2);
     sh.abort_flag = 0u;
     fence_mbar_init();
   }
@@ -211,80 +221,83 @@ __global__ void __launch_bounds__(kBwdThreads, 1) indexer_bwd_kernel(const BwdAr
       ++qc;
     }
     cp_async_wait<0>();   // every copy has landed before the CTA can exit
-  } else if (warp == 2) {
-    // ------------------------------------------------------------------ MMA issuer
+  } else if (warp == 2 || warp == 3) {
+    // ------------------------------------------------------------------ MMA issuers
+    // Warp 2 issues X for each tile as soon as its keys have landed; warp 3 (which owns TMEM)
+    // issues dK and dQ^T as soon as the tile's G is written.  Issued from one warp, dK of tile i
+    // queued behind X of tile i + 1 and so behind that tile's gather; and the K stages, released
+    // after dQ^T, held the gather back in turn.
     constexpr uint32_t id_x = idesc_bf16_f32(128, kHP, 0, 0);
-    constexpr uint32_t id_dk = idesc_bf16_f32(128, kBD, 0, 1);
+    constexpr uint32_t id_dk = TR ? idesc_bf16_f32(kBD, kBKeys, 1, 0)    // dK^T: M = d, N = keys
+                                  : idesc_bf16_f32(kBKeys, kBD, 0, 1);   // dK: M = keys, N = d
     constexpr uint32_t id_dq = idesc_bf16_f32(128, kHP, 1, 1);
     auto wait = [&](uint64_t* bar, uint32_t parity) {
       return __all_sync(0xffffffffu, mbar_wait_for(bar, parity, &sh.abort_flag, status, wait_ns));
     };
-    uint32_t T = 0, T1 = 0, qc = 0;
+    uint32_t T = 0, qc = 0;
     bool ok = true;
-    // X(T1) = K(T1) Q^T
-    auto mma_x = [&](int qs) {
-      const int s = T1 % kStagesB, b = T1 & 1;
-      if (!(ok = wait(&sh.k_full[s], (T1 / kStagesB) & 1))) return;
-      if (T1 >= 2 && !(ok = wait(&sh.x_empty[b], ((T1 >> 1) - 1) & 1))) return;
-      fence_proxy_async_smem();   // cp.async-written tiles
-      tc_fence_after();
-      const uint64_t da = sdesc_sw128(smem_u32(sK + s * kKBytes), 16, 1024);
-      const uint64_t db = sdesc_sw128(smem_u32(sQ + qs * kQBytes), 16, 1024);
-#pragma unroll
-      for (int k = 0; k < kBD / 16; ++k) {
-        const int kb = k >> 2, sub = k & 3;
-        umma_bf16_elect(tmem + kXCol + b * kHP, da + static_cast<uint64_t>((kb * (kKBytes / 2) + sub * 32) >> 4),
-                        db + static_cast<uint64_t>((kb * (kQBytes / 2) + sub * 32) >> 4), id_x, k > 0 ? 1u : 0u);
-      }
-      umma_commit_elect(&sh.x_full[b]);
-      ++T1;
-    };
     for (int t = blockIdx.x; t < A.n_q && ok; t += gridDim.x) {
       const int kt = row_slots(A, t);
       if (kt == 0) continue;
       const int nt = (kt + kBKeys - 1) / kBKeys;
       const int qs = qc & 1;
       if (!(ok = wait(&sh.q_full[qs], (qc >> 1) & 1))) break;
-      mma_x(qs);
+      const uint32_t q_addr = smem_u32(sQ + qs * kQBytes);
       for (int i = 0; i < nt && ok; ++i, ++T) {
-        if (i + 1 < nt) {
-          mma_x(qs);
-          if (!ok) break;
-        }
         const int s = T % kStagesB, b = T & 1;
-        if (!(ok = wait(&sh.g_full[b], (T >> 1) & 1))) break;
-        if (T >= 2 && !(ok = wait(&sh.dk_empty[b], ((T >> 1) - 1) & 1))) break;
-        if (i == 0 && qc >= 2 && !(ok = wait(&sh.dq_empty[qs], ((qc >> 1) - 1) & 1))) break;
-        fence_proxy_async_smem();   // G written with generic stores
-        tc_fence_after();
-        const uint32_t g_addr = smem_u32(sG + b * kGBytes);
         const uint32_t k_addr = smem_u32(sK + s * kKBytes);
-        const uint32_t q_addr = smem_u32(sQ + qs * kQBytes);
-        // dK = G Q: A = G (K-major over heads), B = Q (MN-major over d: 64-dim blocks 8 KB apart)
-        const uint64_t dga = sdesc_sw128(g_addr, 16, 1024);
-        const uint64_t dqb = sdesc_sw128(q_addr, kQBytes / 2, 1024);
+        if (warp == 2) {
+          // X = K Q^T
+          if (!(ok = wait(&sh.k_full[s], (T / kStagesB) & 1))) break;
+          if (T >= 2 && !(ok = wait(&sh.x_empty[b], ((T >> 1) - 1) & 1))) break;
+          fence_proxy_async_smem();   // cp.async-written tiles
+          tc_fence_after();
+          const uint64_t da = sdesc_sw128(k_addr, 16, 1024);
+          const uint64_t db = sdesc_sw128(q_addr, 16, 1024);
 #pragma unroll
-        for (int k = 0; k < kHP / 16; ++k)
-          umma_bf16_elect(tmem + kDkCol + b * kBD, dga + static_cast<uint64_t>((k * 32) >> 4),
-                          dqb + static_cast<uint64_t>((k * 16 * 128) >> 4), id_dk, k > 0 ? 1u : 0u);
-        umma_commit_elect(&sh.dk_full[b]);
-        // dQ^T += K^T G: A = K tile (MN-major over d: 64-dim blocks 16 KB apart), B = G (MN-major
-        // over heads); 16 keys (2 KB of rows) per step
-        const uint64_t dka = sdesc_sw128(k_addr, kKBytes / 2, 1024);
-        const uint64_t dgb = sdesc_sw128(g_addr, kGBytes, 1024);
+          for (int k = 0; k < kBD / 16; ++k) {
+            const int kb = k >> 2, sub = k & 3;
+            umma_bf16_elect(tmem + kXCol + b * kHP, da + static_cast<uint64_t>((kb * (kKBytes / 2) + sub * 32) >> 4),
+                            db + static_cast<uint64_t>((kb * (kQBytes / 2) + sub * 32) >> 4), id_x, k > 0 ? 1u : 0u);
+          }
+          umma_commit_elect(&sh.x_full[b]);
+          umma_commit_elect(&sh.k_empty[s]);   // this warp's read of the tile
+        } else {
+          if (!(ok = wait(&sh.g_full[b], (T >> 1) & 1))) break;
+          if (T >= 2 && !(ok = wait(&sh.dk_empty[b], ((T >> 1) - 1) & 1))) break;
+          if (i == 0 && qc >= 2 && !(ok = wait(&sh.dq_empty[qs], ((qc >> 1) - 1) & 1))) break;
+          fence_proxy_async_smem();   // G written with generic stores
+          tc_fence_after();
+          const uint32_t g_addr = smem_u32(sG + b * kGBytes);
+          // TR: dK^T = Q^T G^T (A = Q, MN-major over d: 64-dim blocks 8 KB apart; B = G, K-major
+          // over heads); else dK = G Q (A = G, B = Q, the same descriptors); 16 heads per step
+          const uint64_t dq_mn = sdesc_sw128(q_addr, kQBytes / 2, 1024);
+          const uint64_t dg_k = sdesc_sw128(g_addr, 16, 1024);
 #pragma unroll
-        for (int k = 0; k < kBKeys / 16; ++k)
-          umma_bf16_elect(tmem + kDqCol + qs * kHP, dka + static_cast<uint64_t>((k * 16 * 128) >> 4),
-                          dgb + static_cast<uint64_t>((k * 16 * 128) >> 4), id_dq, (i > 0 || k > 0) ? 1u : 0u);
-        umma_commit_elect(&sh.k_empty[s]);
-        umma_commit_elect(&sh.g_empty[b]);
+          for (int k = 0; k < kHP / 16; ++k) {
+            const uint64_t qk = dq_mn + static_cast<uint64_t>((k * 16 * 128) >> 4);
+            const uint64_t gk = dg_k + static_cast<uint64_t>((k * 32) >> 4);
+            umma_bf16_elect(tmem + kDkCol + b * kBKeys, TR ? qk : gk, TR ? gk : qk, id_dk, k > 0 ? 1u : 0u);
+          }
+          umma_commit_elect(&sh.dk_full[b]);
+          // dQ^T += K^T G: A = K tile (MN-major over d: 64-dim blocks 16 KB apart), B = G (MN-major
+          // over heads); 16 keys (2 KB of rows) per step
+          const uint64_t dka = sdesc_sw128(k_addr, kKBytes / 2, 1024);
+          const uint64_t dgb = sdesc_sw128(g_addr, kGBytes, 1024);
+#pragma unroll
+          for (int k = 0; k < kBKeys / 16; ++k)
+            umma_bf16_elect(tmem + kDqCol + qs * kHP, dka + static_cast<uint64_t>((k * 16 * 128) >> 4),
+                            dgb + static_cast<uint64_t>((k * 16 * 128) >> 4), id_dq, (i > 0 || k > 0) ? 1u : 0u);
+          umma_commit_elect(&sh.k_empty[s]);   // this warp's read of the tile
+          umma_commit_elect(&sh.g_empty[b]);
+        }
       }
       if (!ok) break;
-      umma_commit_elect(&sh.dq_full[qs]);
+      if (warp == 3) umma_commit_elect(&sh.dq_full[qs]);
       umma_commit_elect(&sh.q_empty[qs]);
       ++qc;
     }
-    // every product issued has completed before TMEM is released
+    // every product this warp issued has completed before TMEM is released
     umma_commit_elect(&sh.mma_done);
     mbar_drain(&sh.mma_done, 0, 200000000ull);
     __syncwarp();
@@ -350,21 +363,43 @@ __global__ void __launch_bounds__(kBwdThreads, 1) indexer_bwd_kernel(const BwdAr
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh.g_full[b]);
-        // dK row of this key, added into dk~
+        // dK^T into dk~: this thread is dim `row` of the tile's 128 keys (TMEM columns); per chunk
+        // of 32 keys lane c looks up key c's row (-1 when it adds nothing: no selection, or
+        // g = 0) and the warp takes them by shuffle, so no shared-memory read sits between two
+        // reductions
         if (!(ok = warp_all_wait(&sh.dk_full[b], (T >> 1) & 1, &sh.abort_flag, status, wait_ns))) break;
         tc_fence_after();
-        float* dk_row = A.dk + static_cast<size_t>(j >= 0 ? ks_t + j : 0) * kBD;
-        const bool add = j >= 0 && g != 0.f;
+        if constexpr (TR) {
+          float* dk_dim = A.dk + row;
+#pragma unroll 1
+          for (int c0 = 0; c0 < kBKeys; c0 += 32) {
+            uint32_t v[32];
+            tmem_ld32(tmem + t_lane + kDkCol + b * kBKeys + c0, v);
+            const int nk = i * kBKeys + c0 + lane;
+            const int jk = nk < kt ? sh.idx[qs][nk] : -1;
+            const int kr = (jk >= 0 && jk < len && sh.ds[qs][nk] != 0.f) ? ks_t + jk : -1;
+            tmem_ld_wait();
 #pragma unroll
-        for (int c0 = 0; c0 < kBD; c0 += 32) {
-          uint32_t v[32];
-          tmem_ld32(tmem + t_lane + kDkCol + b * kBD + c0, v);
-          tmem_ld_wait();
-          if (add) {
+            for (int c = 0; c < 32; ++c) {
+              const int r = __shfl_sync(0xffffffffu, kr, c);
+              if (r >= 0) red_add_f32(dk_dim + static_cast<size_t>(r) * kBD, __uint_as_float(v[c]));
+            }
+          }
+        } else {
+          // this thread's key row (`row` = key), 16 bytes a reduction
+          float* dk_row = A.dk + static_cast<size_t>(j >= 0 ? ks_t + j : 0) * kBD;
+          const bool add = j >= 0 && g != 0.f;
 #pragma unroll
-            for (int q = 0; q < 32; q += 4)
-              red_add_v4(dk_row + c0 + q, __uint_as_float(v[q]), __uint_as_float(v[q + 1]), __uint_as_float(v[q + 2]),
-                         __uint_as_float(v[q + 3]));
+          for (int c0 = 0; c0 < kBD; c0 += 32) {
+            uint32_t v[32];
+            tmem_ld32(tmem + t_lane + kDkCol + b * kBD + c0, v);
+            tmem_ld_wait();
+            if (add) {
+#pragma unroll
+              for (int q = 0; q < 32; q += 4)
+                red_add_v4(dk_row + c0 + q, __uint_as_float(v[q]), __uint_as_float(v[q + 1]),
+                           __uint_as_float(v[q + 2]), __uint_as_float(v[q + 3]));
+            }
           }
         }
         tc_fence_before();
@@ -423,15 +458,9 @@ cudaError_t launch_indexer_bwd(int n_q, int n_kv, int n_heads, int head_dim, int
                                const PipelineDebug& dbg, cudaStream_t st) {
   if (n_q <= 0) return cudaSuccess;
   if (head_dim != kBD || n_heads < 1 || n_heads > kHP || n_heads % 4 || grid < 1) return cudaErrorInvalidValue;
-  static bool attr_set[64] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  cudaError_t e = smem_attr_once<indexer_bwd_kernel<true>>(kBwdDynSmem);
+  if (e == cudaSuccess) e = smem_attr_once<indexer_bwd_kernel<false>>(kBwdDynSmem);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    e = cudaFuncSetAttribute(indexer_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kBwdDynSmem);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_set[dev] = true;
-  }
   BwdArgs A;
   A.q_rot = static_cast<const uint16_t*>(q_rot);
   A.q_in = static_cast<const uint16_t*>(q_in);
@@ -453,7 +482,14 @@ cudaError_t launch_indexer_bwd(int n_q, int n_kv, int n_heads, int head_dim, int
   A.topk = topk;
   A.status = status;
   A.wait_ns = dbg.wait_ns;
-  indexer_bwd_kernel<<<grid < n_q ? grid : n_q, kBwdThreads, kBwdDynSmem, st>>>(A);
+  // the transposed dK form unless many queries share each key row (about 64 or more
+  // selections per row on average: a short prefix)
+  const bool tr = static_cast<long long>(n_q) * topk <= 64LL * (n_kv > 0 ? n_kv : 1);
+  const int g = grid < n_q ? grid : n_q;
+  if (tr)
+    indexer_bwd_kernel<true><<<g, kBwdThreads, kBwdDynSmem, st>>>(A);
+  else
+    indexer_bwd_kernel<false><<<g, kBwdThreads, kBwdDynSmem, st>>>(A);
   return cudaGetLastError();
 }
 
