@@ -96,14 +96,14 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
 
 // Selected slots of query t: min(topk, ke_t - ks_t); none for an empty range or one outside
 // [0, n_kv) (the producer flags those).
-__device__ __forceinline__ bool range_ok(const BwdArgs& A, int t) {
-  const int a = __ldg(A.ks + t), b = __ldg(A.ke + t);
-  return a >= 0 && b <= A.n_kv && a <= b;
+__device__ __forceinline__ bool range_ok(const int32_t* ks, const int32_t* ke, int n_kv, int t) {
+  const int a = __ldg(ks + t), b = __ldg(ke + t);
+  return a >= 0 && b <= n_kv && a <= b;
 }
-__device__ __forceinline__ int row_slots(const BwdArgs& A, int t) {
-  if (!range_ok(A, t)) return 0;
-  const int len = __ldg(A.ke + t) - __ldg(A.ks + t);
-  return len <= 0 ? 0 : min(A.topk, len);
+__device__ __forceinline__ int row_slots(const int32_t* ks, const int32_t* ke, int n_kv, int topk, int t) {
+  if (!range_ok(ks, ke, n_kv, t)) return 0;
+  const int len = __ldg(ke + t) - __ldg(ks + t);
+  return len <= 0 ? 0 : min(topk, len);
 }
 
 __device__ __forceinline__ bool warp_all_wait(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag,
@@ -116,7 +116,15 @@ __device__ __forceinline__ bool warp_all_wait(uint64_t* bar, uint32_t parity, vo
 // key row per thread.  The first wins when few queries share a key row (long caches), the
 // second when many do (a short causal prefix, whose rows every query reduces into at once).
 template <bool TR>
-__global__ void __launch_bounds__(kBwdThreads, 1) indexer_bwd_kernel(const BwdArgs A) {
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    indexer_bwd_kernel(const uint16_t* __restrict__ q_rot, const uint16_t* __restrict__ q_in,
+                       const uint16_t* __restrict__ k_rot, const uint16_t* __restrict__ k_in, int q_split,
+                       int k_split, const float* __restrict__ w, const int32_t* __restrict__ ks,
+                       const int32_t* __restrict__ ke, const int32_t* __restrict__ idx,
+                       const float* __restrict__ d_score, float* __restrict__ dq, float* __restrict__ dk,
+                       float* __restrict__ dw, int n_q, int n_kv, int n_heads, int topk, uint32_t* status,
+                       unsigned long long wait_ns) {
+  // (separate __restrict__ parameters rather than one struct of them)
   extern __shared__ uint8_t smem_raw[];
   __shared__ BwdShared sh;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -124,8 +132,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1) indexer_bwd_kernel(const BwdAr
   uint8_t* sK = sQ + 2 * kQBytes;                       // kStagesB slots
   uint8_t* sG = sK + kStagesB * kKBytes;                // 2 slots
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  uint32_t* status = A.status;
-  const unsigned long long wait_ns = A.wait_ns;
 
   if (threadIdx.x == 0) {
     for (int b = 0; b < 2; ++b) {
@@ -162,9 +168,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) indexer_bwd_kernel(const BwdAr
     const int tid = threadIdx.x;   // 0 .. 63
     uint32_t T = 0, qc = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < A.n_q && ok; t += gridDim.x) {
-      if (tid == 0 && !range_ok(A, t)) atomicOr(status, DEV_ERR_RANGE);
-      const int kt = row_slots(A, t);
+    for (int t = blockIdx.x; t < n_q && ok; t += gridDim.x) {
+      if (tid == 0 && !range_ok(ks, ke, n_kv, t)) atomicOr(status, DEV_ERR_RANGE);
+      const int kt = row_slots(ks, ke, n_kv, topk, t);
       if (kt == 0) continue;
       const int nt = (kt + kBKeys - 1) / kBKeys;
       const int qs = qc & 1;
@@ -174,25 +180,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1) indexer_bwd_kernel(const BwdAr
       uint8_t* q_dst = sQ + qs * kQBytes;
       for (int c = tid; c < kHP * 16; c += kProdThreads) {
         const int h = c >> 4, ch = c & 15, blk = ch >> 3;
-        const bool valid = h < A.n_heads;
-        const uint16_t* src = (blk < A.q_split ? A.q_in : A.q_rot) +
-                              (static_cast<size_t>(t) * A.n_heads + (valid ? h : 0)) * kBD + ch * 8;
+        const bool valid = h < n_heads;
+        const uint16_t* src = (blk < q_split ? q_in : q_rot) +
+                              (static_cast<size_t>(t) * n_heads + (valid ? h : 0)) * kBD + ch * 8;
         cp_async_16_zfill(smem_u32(q_dst + blk * (kQBytes / 2) + sw128b(h, ch & 7)), src, valid);
       }
       if (tid < kHP / 4) {
-        const bool valid = tid * 4 < A.n_heads;
-        cp_async_16_zfill(smem_u32(&sh.w[qs][tid * 4]), A.w + static_cast<size_t>(t) * A.n_heads + (valid ? tid * 4 : 0),
+        const bool valid = tid * 4 < n_heads;
+        cp_async_16_zfill(smem_u32(&sh.w[qs][tid * 4]), w + static_cast<size_t>(t) * n_heads + (valid ? tid * 4 : 0),
                           valid);
       }
       // the query's selected offsets and upstream gradients, staged once (both roles read them
       // per tile; from global memory each read was a full memory latency)
       for (int n = tid; n < kt; n += kProdThreads) {
-        cp_async_4(smem_u32(&sh.idx[qs][n]), A.idx + static_cast<size_t>(t) * A.topk + n);
-        cp_async_4(smem_u32(&sh.ds[qs][n]), A.d_score + static_cast<size_t>(t) * A.topk + n);
+        cp_async_4(smem_u32(&sh.idx[qs][n]), idx + static_cast<size_t>(t) * topk + n);
+        cp_async_4(smem_u32(&sh.ds[qs][n]), d_score + static_cast<size_t>(t) * topk + n);
       }
       cp_async_mbar_arrive(&sh.q_full[qs]);
-      const int len = __ldg(A.ke + t) - __ldg(A.ks + t);
-      const int ks_t = __ldg(A.ks + t);
+      const int len = __ldg(ke + t) - __ldg(ks + t);
+      const int ks_t = __ldg(ks + t);
       // the offsets staged by all producer threads have landed
       if (!(ok = mbar_wait_for(&sh.q_full[qs], (qc >> 1) & 1, &sh.abort_flag, status, wait_ns))) break;
       for (int i = 0; i < nt && ok; ++i, ++T) {
@@ -202,7 +208,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) indexer_bwd_kernel(const BwdAr
           break;
         uint8_t* k_dst = sK + s * kKBytes;
         const int ch = tid & 15, blk = ch >> 3;
-        const uint16_t* kb = blk < A.k_split ? A.k_in : A.k_rot;
+        const uint16_t* kb = blk < k_split ? k_in : k_rot;
 #pragma unroll 4
         for (int m = 0; m < kBKeys / 4; ++m) {
           const int key = (tid >> 4) + 4 * m;
@@ -236,8 +242,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) indexer_bwd_kernel(const BwdAr
     };
     uint32_t T = 0, qc = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < A.n_q && ok; t += gridDim.x) {
-      const int kt = row_slots(A, t);
+    for (int t = blockIdx.x; t < n_q && ok; t += gridDim.x) {
+      const int kt = row_slots(ks, ke, n_kv, topk, t);
       if (kt == 0) continue;
       const int nt = (kt + kBKeys - 1) / kBKeys;
       const int qs = qc & 1;
@@ -308,18 +314,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1) indexer_bwd_kernel(const BwdAr
     const int row = e * 32 + lane;                           // key within the tile / dim of dQ^T
     uint32_t T = 0, qc = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < A.n_q && ok; t += gridDim.x) {
-      const int kt = row_slots(A, t);
+    for (int t = blockIdx.x; t < n_q && ok; t += gridDim.x) {
+      const int kt = row_slots(ks, ke, n_kv, topk, t);
       if (kt == 0) {
         // nothing selected: dq~ is zero (dw was cleared before the launch)
-        float* dq_t = A.dq + static_cast<size_t>(t) * A.n_heads * kBD;
-        for (int i = threadIdx.x - 128; i < A.n_heads * kBD; i += 128) dq_t[i] = 0.f;
+        float* dq_t = dq + static_cast<size_t>(t) * n_heads * kBD;
+        for (int i = threadIdx.x - 128; i < n_heads * kBD; i += 128) dq_t[i] = 0.f;
         continue;
       }
       const int nt = (kt + kBKeys - 1) / kBKeys;
       const int qs = qc & 1;
-      const int len = __ldg(A.ke + t) - __ldg(A.ks + t);
-      const int ks_t = __ldg(A.ks + t);
+      const int len = __ldg(ke + t) - __ldg(ks + t);
+      const int ks_t = __ldg(ks + t);
       if (!(ok = warp_all_wait(&sh.q_full[qs], (qc >> 1) & 1, &sh.abort_flag, status, wait_ns))) break;
       float dwacc[kHP];
 #pragma unroll
@@ -370,7 +376,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) indexer_bwd_kernel(const BwdAr
         if (!(ok = warp_all_wait(&sh.dk_full[b], (T >> 1) & 1, &sh.abort_flag, status, wait_ns))) break;
         tc_fence_after();
         if constexpr (TR) {
-          float* dk_dim = A.dk + row;
+          float* dk_dim = dk + row;
 #pragma unroll 1
           for (int c0 = 0; c0 < kBKeys; c0 += 32) {
             uint32_t v[32];
@@ -387,7 +393,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) indexer_bwd_kernel(const BwdAr
           }
         } else {
           // this thread's key row (`row` = key), 16 bytes a reduction
-          float* dk_row = A.dk + static_cast<size_t>(j >= 0 ? ks_t + j : 0) * kBD;
+          float* dk_row = dk + static_cast<size_t>(j >= 0 ? ks_t + j : 0) * kBD;
           const bool add = j >= 0 && g != 0.f;
 #pragma unroll
           for (int c0 = 0; c0 < kBD; c0 += 32) {
@@ -421,13 +427,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1) indexer_bwd_kernel(const BwdAr
         }
         if (up) h0 += half;
       }
-      float* dw_t = A.dw + static_cast<size_t>(t) * A.n_heads;
-      if (h0 < A.n_heads) atomicAdd(dw_t + h0, dwacc[0]);
-      if (h0 + 1 < A.n_heads) atomicAdd(dw_t + h0 + 1, dwacc[1]);
+      float* dw_t = dw + static_cast<size_t>(t) * n_heads;
+      if (h0 < n_heads) atomicAdd(dw_t + h0, dwacc[0]);
+      if (h0 + 1 < n_heads) atomicAdd(dw_t + h0 + 1, dwacc[1]);
       // dq~: lane = dim, columns = heads
       if (!(ok = warp_all_wait(&sh.dq_full[qs], (qc >> 1) & 1, &sh.abort_flag, status, wait_ns))) break;
       tc_fence_after();
-      float* dq_t = A.dq + static_cast<size_t>(t) * A.n_heads * kBD;
+      float* dq_t = dq + static_cast<size_t>(t) * n_heads * kBD;
 #pragma unroll
       for (int c0 = 0; c0 < kHP; c0 += 32) {
         uint32_t v[32];
@@ -435,7 +441,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) indexer_bwd_kernel(const BwdAr
         tmem_ld_wait();
 #pragma unroll
         for (int q = 0; q < 32; ++q)
-          if (c0 + q < A.n_heads) dq_t[static_cast<size_t>(c0 + q) * kBD + row] = __uint_as_float(v[q]);
+          if (c0 + q < n_heads) dq_t[static_cast<size_t>(c0 + q) * kBD + row] = __uint_as_float(v[q]);
       }
       tc_fence_before();
       __syncwarp();
@@ -486,10 +492,10 @@ cudaError_t launch_indexer_bwd(int n_q, int n_kv, int n_heads, int head_dim, int
   // selections per row on average: a short prefix)
   const bool tr = static_cast<long long>(n_q) * topk <= 64LL * (n_kv > 0 ? n_kv : 1);
   const int g = grid < n_q ? grid : n_q;
-  if (tr)
-    indexer_bwd_kernel<true><<<g, kBwdThreads, kBwdDynSmem, st>>>(A);
-  else
-    indexer_bwd_kernel<false><<<g, kBwdThreads, kBwdDynSmem, st>>>(A);
+  auto kern = tr ? indexer_bwd_kernel<true> : indexer_bwd_kernel<false>;
+  kern<<<g, kBwdThreads, kBwdDynSmem, st>>>(A.q_rot, A.q_in, A.k_rot, A.k_in, A.q_split, A.k_split, A.w, A.ks, A.ke,
+                                           A.idx, A.d_score, A.dq, A.dk, A.dw, A.n_q, A.n_kv, A.n_heads, A.topk,
+                                           A.status, A.wait_ns);
   return cudaGetLastError();
 }
 
