@@ -393,6 +393,10 @@ cudaError_t launch_select(int n_q, int n_chunks, int cap, int topk, int trivial_
   if (static_cast<long long>(n_chunks) * cap <= kSmallStage || n_chunks == 1)
     return launch_shape<kSmallStage, kSmallThreads>(n_q, n_chunks, cap, topk, trivial_len, row_range, cand_edge,
                                                     cand_key, cand_idx, cand_cnt, idx_out, score_out, status, st);
+  // few rows (decode): one CTA per row leaves most SMs idle, so each row gets 1024 threads
+  if (n_q <= device_sm_count())
+    return launch_shape<kBigStage, 2 * kBigThreads>(n_q, n_chunks, cap, topk, trivial_len, row_range, cand_edge,
+                                                    cand_key, cand_idx, cand_cnt, idx_out, score_out, status, st);
   return launch_shape<kBigStage, kBigThreads>(n_q, n_chunks, cap, topk, trivial_len, row_range, cand_edge, cand_key,
                                               cand_idx, cand_cnt, idx_out, score_out, status, st);
 }
