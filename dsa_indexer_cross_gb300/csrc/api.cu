@@ -404,9 +404,11 @@ size_t attn_ws_bytes(const dsa_attn_desc* d) {
 
 // status: device status header (first two words: bits, bad-index count); row_nt: n_q int32.
 // pg (paged latent cache): ks is unused, offsets map through the block table.
+// reuse_prepass: the workspace already holds the walk's pre-pass results for these index rows
+// (the previous call on it used the same idx, ks and shape: IndexShare's shared layers).
 dsa_status run_attn(const dsa_attn_desc* d, const void* q, const void* kv, const int32_t* idx, const int32_t* ks,
                     void* out, float* lse, void* ws, size_t ws_bytes, cudaStream_t st, bool clear_status,
-                    uint32_t* status_override = nullptr, const PagedRows* pg = nullptr) {
+                    uint32_t* status_override = nullptr, const PagedRows* pg = nullptr, bool reuse_prepass = false) {
   dsa_status s = check_attn_desc(d);
   if (s != DSA_OK) return s;
   if (d->n_q == 0) return DSA_OK;
@@ -441,7 +443,7 @@ dsa_status run_attn(const dsa_attn_desc* d, const void* q, const void* kv, const
     return s;
   e = launch_sparse_attn(tkv, tq, d->n_q, d->n_kv, d->n_heads, d->topk, d->softmax_scale, kv, idx, ks,
                          pg ? *pg : PagedRows{}, out, lse, status,
-                         base + kAlign, st);
+                         base + kAlign, st, reuse_prepass);
   if (e != cudaSuccess) return cuda_fail(e, "sparse attention kernel");
   return DSA_OK;
 }
@@ -688,15 +690,19 @@ dsa_status indexshare_layers_forward(const dsa_indexer_desc* idx_desc, const dsa
   if ((s = check_device()) != DSA_OK) return s;
   cudaError_t e;
   if ((e = cudaMemsetAsync(ws, 0, kAlign, st)) != cudaSuccess) return cuda_fail(e, "clear status");
+  const int32_t* prev_idx = nullptr;   // index rows whose attention pre-pass the workspace holds
   for (int32_t l = 0; l < n_layers; ++l) {
     if (cache->types[l] == DSA_LAYER_FULL) {
       s = run_indexer(idx_desc, io[l].q_idx, io[l].k_idx, io[l].w, q_pos, k_pos, ks, ke, rope_cs, rope_n_pos,
                       cache->buffers[l], nullptr, ws, idx_ws, st, false);
       if (s != DSA_OK) return s;
     }
-    s = run_attn(attn_desc, io[l].q, io[l].kv, cache->buffers[cache->donors[l]], ks, io[l].out, io[l].lse, attn_ws,
-                 ws_bytes - idx_ws, st, false, static_cast<uint32_t*>(ws));
+    // a shared layer reading the same index rows as the layer before reuses its pre-pass
+    const int32_t* idx_l = cache->buffers[cache->donors[l]];
+    s = run_attn(attn_desc, io[l].q, io[l].kv, idx_l, ks, io[l].out, io[l].lse, attn_ws, ws_bytes - idx_ws, st, false,
+                 static_cast<uint32_t*>(ws), nullptr, idx_l == prev_idx);
     if (s != DSA_OK) return s;
+    prev_idx = idx_l;
   }
   return DSA_OK;
 }

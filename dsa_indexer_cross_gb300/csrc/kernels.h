@@ -156,10 +156,12 @@ int sparse_attn_q_box_rows(int n_heads, int n_kv, int topk, bool paged);
 // a 2-D [n_kv][576] tensor with 128-byte swizzled boxes of {64, 1} (four-row gathers).
 // tmap_q: q as a 2-D [n_q * n_heads][576] tensor, 128-byte swizzled boxes of
 // {64, sparse_attn_q_box_rows(...)}.
+// reuse_prepass: the scratch already holds the pre-pass results (tile counts, or key ranges and
+// bitmasks) for these idx and ks rows, from the previous call on the same scratch and shape.
 cudaError_t launch_sparse_attn(const CUtensorMap& tmap_kv, const CUtensorMap& tmap_q, int n_q, int n_kv, int n_heads,
                                int topk, float scale, const void* kv, const int32_t* idx, const int32_t* ks,
                                const PagedRows& pg, void* out, float* lse, uint32_t* status, void* scratch,
-                               cudaStream_t st);
+                               cudaStream_t st, bool reuse_prepass = false);
 
 // ---------------------------------------------------------------------------- indexer projections
 // One GEMM job of the projection kernel, Y = A[T][k] . W^T in N tiles of n_tile weight rows.

@@ -1016,12 +1016,14 @@ size_t dense_mask_offset(int n_blk) { return (static_cast<size_t>(n_blk) * sizeo
 template <int HD>
 cudaError_t launch_dense(const CUtensorMap& tmap_kv, const CUtensorMap& tmap_q, int n_q, int n_kv, int n_heads,
                          int topk, float scale, const int32_t* idx, const int32_t* ks, void* out, float* lse,
-                         uint32_t* status, void* scratch, cudaStream_t st) {
+                         uint32_t* status, void* scratch, cudaStream_t st, bool reuse_prepass) {
   const DenseScratch ds = dense_scratch(scratch, n_q, HD);
-  const int ps = prof_begin(kProfAttnPrep, st);
-  cudaError_t e = launch_block_mask(HD, idx, ks, n_q, n_kv, topk, ds, status, st);
-  prof_end(ps, st);
-  if (e != cudaSuccess) return e;
+  if (!reuse_prepass) {
+    const int ps = prof_begin(kProfAttnPrep, st);
+    cudaError_t e = launch_block_mask(HD, idx, ks, n_q, n_kv, topk, ds, status, st);
+    prof_end(ps, st);
+    if (e != cudaSuccess) return e;
+  }
   return launch_cfg<kDenseCols, HD>(tmap_kv, tmap_q, n_q, n_kv, n_heads, topk, scale, nullptr, idx, ks, PagedRows{},
                                     nullptr, ds.block_range, ds.block_mask, out,
                                     lse, status, st);
@@ -1128,24 +1130,26 @@ int sparse_attn_q_box_rows(int n_heads, int n_kv, int topk, bool paged) {
 cudaError_t launch_sparse_attn(const CUtensorMap& tmap_kv, const CUtensorMap& tmap_q, int n_q, int n_kv, int n_heads,
                                int topk, float scale, const void* kv, const int32_t* idx, const int32_t* ks,
                                const PagedRows& pg, void* out, float* lse, uint32_t* status, void* scratch,
-                               cudaStream_t st) {
+                               cudaStream_t st, bool reuse_prepass) {
   if (n_q <= 0) return cudaSuccess;
   const int hd = pg.block_table ? 0 : sparse_attn_dense_heads(n_heads, n_kv, topk);   // paged: gather walk
   if (hd) {
     switch (hd) {
-      case 1: return launch_dense<1>(tmap_kv, tmap_q, n_q, n_kv, n_heads, topk, scale, idx, ks, out, lse, status, scratch, st);
-      case 2: return launch_dense<2>(tmap_kv, tmap_q, n_q, n_kv, n_heads, topk, scale, idx, ks, out, lse, status, scratch, st);
-      case 4: return launch_dense<4>(tmap_kv, tmap_q, n_q, n_kv, n_heads, topk, scale, idx, ks, out, lse, status, scratch, st);
-      case 8: return launch_dense<8>(tmap_kv, tmap_q, n_q, n_kv, n_heads, topk, scale, idx, ks, out, lse, status, scratch, st);
-      default: return launch_dense<16>(tmap_kv, tmap_q, n_q, n_kv, n_heads, topk, scale, idx, ks, out, lse, status, scratch, st);
+      case 1: return launch_dense<1>(tmap_kv, tmap_q, n_q, n_kv, n_heads, topk, scale, idx, ks, out, lse, status, scratch, st, reuse_prepass);
+      case 2: return launch_dense<2>(tmap_kv, tmap_q, n_q, n_kv, n_heads, topk, scale, idx, ks, out, lse, status, scratch, st, reuse_prepass);
+      case 4: return launch_dense<4>(tmap_kv, tmap_q, n_q, n_kv, n_heads, topk, scale, idx, ks, out, lse, status, scratch, st, reuse_prepass);
+      case 8: return launch_dense<8>(tmap_kv, tmap_q, n_q, n_kv, n_heads, topk, scale, idx, ks, out, lse, status, scratch, st, reuse_prepass);
+      default: return launch_dense<16>(tmap_kv, tmap_q, n_q, n_kv, n_heads, topk, scale, idx, ks, out, lse, status, scratch, st, reuse_prepass);
     }
   }
   int32_t* row_nt = static_cast<int32_t*>(scratch);
-  const int ps = prof_begin(kProfAttnPrep, st);
-  row_tiles_kernel<<<(n_q + 7) / 8, 256, 0, st>>>(idx, n_q, topk, row_nt);
-  prof_end(ps, st);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  if (!reuse_prepass) {
+    const int ps = prof_begin(kProfAttnPrep, st);
+    row_tiles_kernel<<<(n_q + 7) / 8, 256, 0, st>>>(idx, n_q, topk, row_nt);
+    prof_end(ps, st);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   SplitOut split{gather_splits(n_q, n_heads, topk), nullptr, nullptr};
   if (split.n > 1) {
     split.o = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + gather_split_offset(n_q));
