@@ -373,7 +373,7 @@ dsa_status run_indexer(const dsa_indexer_desc* d, const void* q_idx, const void*
   }
   if (pe) (void)cudaEventRecord(pe->ev[3], st);
   ps = prof_begin(kProfSelect, st);
-  e = launch_select(d->n_q, p.n_chunks, p.cap, d->topk, trivial_len, rr, edge, ck, ci, cnt, idx_out, score_out,
+  e = launch_select(d->n_q, p.n_chunks, p.cap, d->topk, trivial_len, d->max_len, rr, edge, ck, ci, cnt, idx_out, score_out,
                     status, st);
   prof_end(ps, st);
   if (e != cudaSuccess) return cuda_fail(e, "top-k select");

@@ -120,7 +120,8 @@ cudaError_t launch_indexer(const IndexerPlan& p, const CUtensorMap& tmap_q, cons
 // Exact top-k of every row from its candidates; writes offsets (ascending) and -1 padding.
 // Rows of at most trivial_len keys are written as 0..L-1 without reading candidates; entries
 // below the largest of a row's chunk edges are skipped.
-cudaError_t launch_select(int n_q, int n_chunks, int cap, int topk, int trivial_len, const int2* row_range,
+// max_len bounds every row's length (the ranges kernel empties longer rows).
+cudaError_t launch_select(int n_q, int n_chunks, int cap, int topk, int trivial_len, int max_len, const int2* row_range,
                           const uint32_t* cand_edge,
                           const uint32_t* cand_key,
                           const int32_t* cand_idx, const uint32_t* cand_cnt, int32_t* idx_out, float* score_out,

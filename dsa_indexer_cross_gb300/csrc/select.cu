@@ -8,15 +8,18 @@
 // top-k.  Each chunk also carries an edge key with at least k of its entries at or above it,
 // so nothing below the largest edge of the row can be selected.
 //
-// One block per row: the entries at or above the edge are gathered into shared memory (in any
-// order), the exact threshold (v, cut) is found there -- one pass of 2048 bins linear in score,
-// then the boundary bin's entries ranked directly, or radix passes when that bin is crowded --
-// and the selected entries are put in key-index order by a counting pass over index buckets
-// (at most 2048 buckets over the row; an entry's place is its bucket's start plus the number
-// of smaller indices in its bucket).  Rows with more gathered entries than shared memory holds
-// take the same steps over the buffers in global memory.  Two block shapes: 6144 staged
-// entries and 256 threads for single-chunk rows and where a row's buffers cannot hold more,
-// else 24576 and 512 threads.
+// One block per row.  When every row has at most 8192 keys, each gathered entry is stored at
+// its offset in the row, the exact threshold (v, cut) is found over them and the kept offsets
+// are written in order by a ballot compaction.  Otherwise the entries at or above the edge are
+// gathered into shared memory (in any order), the threshold is found there -- one pass of 2048
+// bins linear in score, then the boundary bin's entries ranked directly, or radix passes when
+// that bin is crowded -- and the selected entries are put in key-index order by a counting
+// pass over index buckets (at most 2048 buckets over the row; an entry's place is its bucket's
+// start plus the number of smaller indices in its bucket).  Rows with more gathered entries
+// than shared memory holds take the same steps over the buffers in global memory.  Block
+// shapes: 256 threads and 4096 or 8192 score keys for short rows; 6144 staged entries and 256
+// threads for single-chunk rows and where a row's buffers cannot hold more; else 24576 entries
+// and 512 threads (1024 when there are no more rows than SMs).
 #include "kernels.h"
 #include "ptx.cuh"
 #include "topk.cuh"
@@ -30,6 +33,7 @@ constexpr int kSortMax = 2048;      // topk <= 2048
 constexpr int kMaxSeg = 64 * kSub;  // (chunk, sub-buffer) segments of a row
 constexpr int kSmallStage = 6144, kSmallThreads = 256;
 constexpr int kBigStage = 24576, kBigThreads = 512;
+constexpr int kDenseKeys = 4096, kDenseThreads = 256;
 
 template <int STAGE>
 struct SelSmem {
@@ -49,6 +53,21 @@ struct SelSmem {
   int wsum[32];
 };
 static_assert(kSmallStage * 8 >= kSortMax * 8 + kBins * 4, "bucketed selection fits the stage region");
+
+// Rows of at most KEYS keys: one score key per offset of the row, no staging or sort region.
+template <int KEYS>
+struct DenseSmem {
+  uint32_t key[KEYS];
+  uint32_t hist[kBins];
+  uint32_t bkey[kBoundaryMax];
+  int32_t bidx[kBoundaryMax];
+  int seg_start[kMaxSeg + 1];
+  int n_stage, n_sel, n_bound;
+  uint32_t kmin, kmax, edge;
+  int misc[4];
+  int bc[4];
+  int wsum[32];
+};
 
 // A slot of *counter for every active lane, one shared atomic per warp.
 __device__ __forceinline__ int reserve_slot(int* counter) {
@@ -263,54 +282,95 @@ __device__ void block_write_ordered(SelSmem<STAGE>& sm, int n, int L, int rx, in
   }
 }
 
-template <int STAGE, int NT>
-__global__ void __launch_bounds__(NT) select_kernel(int n_chunks, int cap4, int topk, int trivial_len,
-                                                    const int2* __restrict__ row_range,
-                                                    const uint32_t* __restrict__ cand_edge,
-                                                    const uint32_t* __restrict__ cand_key,
-                                                    const int32_t* __restrict__ cand_idx,
-                                                    const uint32_t* __restrict__ cand_cnt, int32_t* __restrict__ idx_out,
-                                                    float* score_out, uint32_t* status) {
-  extern __shared__ __align__(16) uint8_t sel_smem_raw[];
-  SelSmem<STAGE>& sm = *reinterpret_cast<SelSmem<STAGE>*>(sel_smem_raw);
-  const int t = blockIdx.x;
-  const int tid = threadIdx.x;
-  const int2 r = row_range[t];
-  int32_t* out = idx_out + static_cast<size_t>(t) * topk;
-  float* so = score_out ? score_out + static_cast<size_t>(t) * topk : nullptr;
-  const int L = r.y - r.x;
-  if (L <= trivial_len) {
-    // the whole range is selected: offsets 0 .. L-1 in order, no candidates read.  The host
-    // passes trivial_len = 0 whenever scores are requested, so only empty rows get here then.
-    for (int i = tid; i < topk; i += NT) {
-      out[i] = i < L ? i : -1;
-      if (so) so[i] = -__int_as_float(0x7f800000);
+// A row of at most KEYS keys.  Every gathered entry goes to its own offset in the row (0 marks
+// an offset without an entry; a real key of 0 -- the all-ones NaN pattern -- is stored as 1),
+// the exact threshold is found over the present offsets, and the selection is written in
+// offset order by a ballot compaction: warp w walks its own contiguous span of offsets twice,
+// once to count its kept entries, once to write them after the earlier warps'.
+template <int NT, int KEYS>
+__device__ void dense_row(const Segs& S, DenseSmem<KEYS>& sm, uint32_t edge, int L, int rx, int kt, int topk,
+                          int32_t* out, float* so, uint32_t* status) {
+  constexpr int NW = NT / 32;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  uint32_t* dk = sm.key;
+  for (int o = tid; o < L; o += NT) dk[o] = 0u;
+  __syncthreads();
+  int cnt = 0;
+  uint32_t mn = 0xFFFFFFFFu, mx = 0u;
+  for_each_global<NT>(S, sm, edge, [&](uint32_t key, int32_t idx) {
+    const int o = idx - rx;
+    if (o < 0 || o >= L) {
+      atomicOr(status, DEV_ERR_BAD_INDEX);
+      return;
     }
-    return;
-  }
-  const int n_seg = n_chunks * kSub;
-  if (tid == 0) {
-    sm.edge = 0u;
-    sm.n_stage = 0;
-    sm.n_sel = 0;
-    sm.kmin = 0xFFFFFFFFu;
-    sm.kmax = 0u;
+    const uint32_t k1 = key ? key : 1u;
+    dk[o] = k1;
+    ++cnt;
+    mn = min(mn, k1);
+    mx = max(mx, k1);
+  });
+  cnt = __reduce_add_sync(0xffffffffu, cnt);
+  mn = __reduce_min_sync(0xffffffffu, mn);
+  mx = __reduce_max_sync(0xffffffffu, mx);
+  if (lane == 0) {
+    atomicAdd(&sm.n_stage, cnt);
+    atomicMin(&sm.kmin, mn);
+    atomicMax(&sm.kmax, mx);
   }
   __syncthreads();
-  // segment starts (one thread per segment) and the row's edge (largest chunk edge)
-  const int cnt_s =
-      tid < n_seg ? static_cast<int>(min(__ldg(cand_cnt + static_cast<size_t>(t) * n_seg + tid), static_cast<uint32_t>(cap4)))
-                  : 0;
-  if (tid < n_chunks) atomicMax(&sm.edge, __ldg(cand_edge + static_cast<size_t>(t) * n_chunks + tid));
-  int n_all = 0;
-  const int start_s = block_exclusive_scan<NT>(cnt_s, sm.wsum, &n_all);
-  if (tid < n_seg) sm.seg_start[tid] = start_s;
-  if (tid == 0) sm.seg_start[n_seg] = n_all;
+  const bool all = sm.n_stage <= kt;
+  uint32_t v = 0, cut = 0x7FFFFFFFu;
+  if (!all) {
+    auto fe = [&](auto&& f) {
+      for (int o = tid; o < L; o += NT) {
+        const uint32_t k = dk[o];
+        if (k) f(k, rx + o);
+      }
+    };
+    block_threshold<NT>(fe, kt, sm.kmin, sm.kmax, sm, v, cut);
+  }
+  const int span = ((L + NW - 1) / NW + 31) & ~31;
+  const int o0 = w * span, o1 = min(L, o0 + span);
+  auto keep = [&](int o) {
+    const uint32_t k = o < o1 ? dk[o] : 0u;
+    return k != 0u && (all || topk_keep(k, rx + o, v, cut));
+  };
+  int c = 0;
+  for (int b = o0; b < o1; b += 32) c += __popc(__ballot_sync(0xffffffffu, keep(b + lane)));
   __syncthreads();
-  const uint32_t edge = sm.edge;
-  const Segs S{cand_key, cand_idx, n_seg, cap4, static_cast<size_t>(t) * n_seg * cap4};
-  const int kt = min(topk, L);
+  if (lane == 0) sm.wsum[w] = c;
+  __syncthreads();
+  int pre = 0, total = 0;
+#pragma unroll
+  for (int i = 0; i < NW; ++i) {
+    const int s = sm.wsum[i];
+    pre += i < w ? s : 0;
+    total += s;
+  }
+  for (int b = o0; b < o1; b += 32) {
+    const int o = b + lane;
+    const bool kp = keep(o);
+    const uint32_t m = __ballot_sync(0xffffffffu, kp);
+    const int pos = pre + __popc(m & ((1u << lane) - 1u));
+    if (kp && pos < topk) {
+      out[pos] = o;
+      if (so) so[pos] = key_float(dk[o]);
+    }
+    pre += __popc(m);
+  }
+  for (int i = total + tid; i < topk; i += NT) {
+    out[i] = -1;
+    if (so) so[i] = -__int_as_float(0x7f800000);
+  }
+  if (tid == 0 && total != kt) atomicOr(status, DEV_ERR_OVERFLOW);
+}
 
+// A row gathered as (key, index) entries: staged in shared memory when they fit, else read
+// from the buffers in global memory on every pass; threshold, then index-bucket ordering.
+template <int NT, int STAGE>
+__device__ void select_sparse(const Segs& S, SelSmem<STAGE>& sm, uint32_t edge, int L, int rx, int kt, int topk,
+                              int32_t* out, float* so, uint32_t* status) {
+  const int tid = threadIdx.x;
   // gather the entries at or above the edge into shared memory, with their key range
   uint32_t mn = 0xFFFFFFFFu, mx = 0u;
   for_each_global<NT>(S, sm, edge, [&](uint32_t key, int32_t idx) {
@@ -355,50 +415,139 @@ __global__ void __launch_bounds__(NT) select_kernel(int n_chunks, int cap4, int 
   __syncthreads();
   const int n_sel = min(sm.n_sel, kSortMax);
   if (tid == 0 && sm.n_sel != kt) atomicOr(status, DEV_ERR_OVERFLOW);
-  block_write_ordered<NT>(sm, n_sel, L, r.x, topk, out, so, status);
+  block_write_ordered<NT>(sm, n_sel, L, rx, topk, out, so, status);
 }
 
-template <int STAGE, int NT>
+// One row per block.  SM: SelSmem<STAGE> (any row) or DenseSmem<KEYS> (DENSE: rows of at most
+// KEYS keys, which the host guarantees by choosing this shape only when max_len <= KEYS).
+template <class SM, int NT, bool DENSE>
+__device__ __forceinline__ void select_row(int n_chunks, int cap4, int topk, int trivial_len,
+                                           const int2* __restrict__ row_range, const uint32_t* __restrict__ cand_edge,
+                                           const uint32_t* __restrict__ cand_key, const int32_t* __restrict__ cand_idx,
+                                           const uint32_t* __restrict__ cand_cnt, int32_t* __restrict__ idx_out,
+                                           float* score_out, uint32_t* status) {
+  extern __shared__ __align__(16) uint8_t sel_smem_raw[];
+  SM& sm = *reinterpret_cast<SM*>(sel_smem_raw);
+  const int t = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int2 r = row_range[t];
+  int32_t* out = idx_out + static_cast<size_t>(t) * topk;
+  float* so = score_out ? score_out + static_cast<size_t>(t) * topk : nullptr;
+  const int L = r.y - r.x;
+  if (L <= trivial_len) {
+    // the whole range is selected: offsets 0 .. L-1 in order, no candidates read.  The host
+    // passes trivial_len = 0 whenever scores are requested, so only empty rows get here then.
+    for (int i = tid; i < topk; i += NT) {
+      out[i] = i < L ? i : -1;
+      if (so) so[i] = -__int_as_float(0x7f800000);
+    }
+    return;
+  }
+  const int n_seg = n_chunks * kSub;
+  if (tid == 0) {
+    sm.edge = 0u;
+    sm.n_stage = 0;
+    sm.n_sel = 0;
+    sm.kmin = 0xFFFFFFFFu;
+    sm.kmax = 0u;
+  }
+  __syncthreads();
+  // segment starts (one thread per segment) and the row's edge (largest chunk edge)
+  const int cnt_s =
+      tid < n_seg ? static_cast<int>(min(__ldg(cand_cnt + static_cast<size_t>(t) * n_seg + tid), static_cast<uint32_t>(cap4)))
+                  : 0;
+  if (tid < n_chunks) atomicMax(&sm.edge, __ldg(cand_edge + static_cast<size_t>(t) * n_chunks + tid));
+  int n_all = 0;
+  const int start_s = block_exclusive_scan<NT>(cnt_s, sm.wsum, &n_all);
+  if (tid < n_seg) sm.seg_start[tid] = start_s;
+  if (tid == 0) sm.seg_start[n_seg] = n_all;
+  __syncthreads();
+  const uint32_t edge = sm.edge;
+  const Segs S{cand_key, cand_idx, n_seg, cap4, static_cast<size_t>(t) * n_seg * cap4};
+  const int kt = min(topk, L);
+  if constexpr (DENSE) {
+    if (L <= static_cast<int>(sizeof(sm.key) / sizeof(sm.key[0]))) {
+      dense_row<NT>(S, sm, edge, L, r.x, kt, topk, out, so, status);
+    } else {
+      if (tid == 0) atomicOr(status, DEV_ERR_RANGE);
+      for (int i = tid; i < topk; i += NT) {
+        out[i] = -1;
+        if (so) so[i] = -__int_as_float(0x7f800000);
+      }
+    }
+  } else {
+    select_sparse<NT>(S, sm, edge, L, r.x, kt, topk, out, so, status);
+  }
+}
+
+#define DSA_SEL_PARAMS                                                                                        \
+  int n_chunks, int cap4, int topk, int trivial_len, const int2 *__restrict__ row_range,                     \
+      const uint32_t *__restrict__ cand_edge, const uint32_t *__restrict__ cand_key,                         \
+      const int32_t *__restrict__ cand_idx, const uint32_t *__restrict__ cand_cnt, int32_t *__restrict__ idx_out, \
+      float *score_out, uint32_t *status
+#define DSA_SEL_FWD \
+  n_chunks, cap4, topk, trivial_len, row_range, cand_edge, cand_key, cand_idx, cand_cnt, idx_out, score_out, status
+
+template <class SM, int NT>
+__global__ void __launch_bounds__(NT) select_kernel(DSA_SEL_PARAMS) {
+  select_row<SM, NT, false>(DSA_SEL_FWD);
+}
+// six short rows an SM (40 registers a thread)
+template <class SM, int NT>
+__global__ void __launch_bounds__(NT, 6) select_dense_kernel(DSA_SEL_PARAMS) {
+  select_row<SM, NT, true>(DSA_SEL_FWD);
+}
+#undef DSA_SEL_PARAMS
+#undef DSA_SEL_FWD
+
+template <class SM, int NT, bool DENSE>
 cudaError_t launch_shape(int n_q, int n_chunks, int cap, int topk, int trivial_len, const int2* row_range,
                          const uint32_t* cand_edge, const uint32_t* cand_key, const int32_t* cand_idx,
                          const uint32_t* cand_cnt, int32_t* idx_out, float* score_out, uint32_t* status,
                          cudaStream_t st) {
-  auto kern = select_kernel<STAGE, NT>;
+  auto kern = [] {
+    if constexpr (DENSE) return select_dense_kernel<SM, NT>;
+    else return select_kernel<SM, NT>;
+  }();
   static bool attr_set[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, sizeof(SelSmem<STAGE>));
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, sizeof(SM));
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
-  kern<<<n_q, NT, sizeof(SelSmem<STAGE>), st>>>(n_chunks, cap / kSub, topk, trivial_len, row_range, cand_edge,
-                                                 cand_key, cand_idx, cand_cnt, idx_out, score_out, status);
+  kern<<<n_q, NT, sizeof(SM), st>>>(n_chunks, cap / kSub, topk, trivial_len, row_range, cand_edge, cand_key, cand_idx,
+                                    cand_cnt, idx_out, score_out, status);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_select(int n_q, int n_chunks, int cap, int topk, int trivial_len, const int2* row_range,
+cudaError_t launch_select(int n_q, int n_chunks, int cap, int topk, int trivial_len, int max_len, const int2* row_range,
                           const uint32_t* cand_edge, const uint32_t* cand_key, const int32_t* cand_idx,
                           const uint32_t* cand_cnt, int32_t* idx_out, float* score_out, uint32_t* status,
                           cudaStream_t st) {
   if (n_q <= 0) return cudaSuccess;
   if (n_chunks > kMaxSeg / kSub || topk > kSortMax || cap % kSub) return cudaErrorInvalidValue;
-  // the small shape (two or three CTAs per SM) when a row's buffers cannot hold more than its
-  // stage, or when a row has one chunk: the indexer leaves a filtered row's chunk compacted to
-  // its entries at or above the final threshold (about k + a bin of them), and a row of at
-  // most 4096 keys keeps at most 4096; a row that still gathers more takes the global path
+#define DSA_SEL_ARGS                                                                                          \
+  n_q, n_chunks, cap, topk, trivial_len, row_range, cand_edge, cand_key, cand_idx, cand_cnt, idx_out, score_out, \
+      status, st
+  // short rows (prefill of a few thousand keys): one score key per offset, 27 or 43 KB a row,
+  // so six to eight rows share an SM
+  if (max_len <= kDenseKeys) return launch_shape<DenseSmem<kDenseKeys>, kDenseThreads, true>(DSA_SEL_ARGS);
+  if (max_len <= 2 * kDenseKeys) return launch_shape<DenseSmem<2 * kDenseKeys>, kDenseThreads, true>(DSA_SEL_ARGS);
+  // the small shape (two CTAs per SM) when a row's buffers cannot hold more than its stage, or
+  // when a row has one chunk: the indexer leaves a filtered row's chunk compacted to its
+  // entries at or above the final threshold (about k + a bin of them); a row that still
+  // gathers more takes the global path
   if (static_cast<long long>(n_chunks) * cap <= kSmallStage || n_chunks == 1)
-    return launch_shape<kSmallStage, kSmallThreads>(n_q, n_chunks, cap, topk, trivial_len, row_range, cand_edge,
-                                                    cand_key, cand_idx, cand_cnt, idx_out, score_out, status, st);
+    return launch_shape<SelSmem<kSmallStage>, kSmallThreads, false>(DSA_SEL_ARGS);
   // few rows (decode): one CTA per row leaves most SMs idle, so each row gets 1024 threads
-  if (n_q <= device_sm_count())
-    return launch_shape<kBigStage, 2 * kBigThreads>(n_q, n_chunks, cap, topk, trivial_len, row_range, cand_edge,
-                                                    cand_key, cand_idx, cand_cnt, idx_out, score_out, status, st);
-  return launch_shape<kBigStage, kBigThreads>(n_q, n_chunks, cap, topk, trivial_len, row_range, cand_edge, cand_key,
-                                              cand_idx, cand_cnt, idx_out, score_out, status, st);
+  if (n_q <= device_sm_count()) return launch_shape<SelSmem<kBigStage>, 2 * kBigThreads, false>(DSA_SEL_ARGS);
+  return launch_shape<SelSmem<kBigStage>, kBigThreads, false>(DSA_SEL_ARGS);
+#undef DSA_SEL_ARGS
 }
 
 }  // namespace dsa
