@@ -17,7 +17,7 @@
 // pass over index buckets (at most 2048 buckets over the row; an entry's place is its bucket's
 // start plus the number of smaller indices in its bucket).  Rows with more gathered entries
 // than shared memory holds take the same steps over the buffers in global memory.  Block
-// shapes: 256 threads and 4096 or 8192 score keys for short rows; 6144 staged entries and 256
+// shapes: 256 threads and 4096 or 8192 score keys for short rows; 5120 staged entries and 256
 // threads for single-chunk rows and where a row's buffers cannot hold more; else 24576 entries
 // and 512 threads (1024 when there are no more rows than SMs).
 #include "kernels.h"
@@ -31,7 +31,7 @@ constexpr int kBins = 2048;         // linear bins over the gathered [min, max] 
 constexpr int kBoundaryMax = 256;   // boundary-bin entries ranked directly; more -> radix passes
 constexpr int kSortMax = 2048;      // topk <= 2048
 constexpr int kMaxSeg = 64 * kSub;  // (chunk, sub-buffer) segments of a row
-constexpr int kSmallStage = 6144, kSmallThreads = 256;
+constexpr int kSmallStage = 5120, kSmallThreads = 256;
 constexpr int kBigStage = 24576, kBigThreads = 512;
 constexpr int kDenseKeys = 4096, kDenseThreads = 256;
 
@@ -538,7 +538,7 @@ cudaError_t launch_select(int n_q, int n_chunks, int cap, int topk, int trivial_
   // so six to eight rows share an SM
   if (max_len <= kDenseKeys) return launch_shape<DenseSmem<kDenseKeys>, kDenseThreads, true>(DSA_SEL_ARGS);
   if (max_len <= 2 * kDenseKeys) return launch_shape<DenseSmem<2 * kDenseKeys>, kDenseThreads, true>(DSA_SEL_ARGS);
-  // the small shape (two CTAs per SM) when a row's buffers cannot hold more than its stage, or
+  // the small shape (68 KB: three CTAs per SM) when a row's buffers cannot hold more than its stage, or
   // when a row has one chunk: the indexer leaves a filtered row's chunk compacted to its
   // entries at or above the final threshold (about k + a bin of them); a row that still
   // gathers more takes the global path
