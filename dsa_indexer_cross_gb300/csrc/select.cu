@@ -18,8 +18,8 @@
 // start plus the number of smaller indices in its bucket).  Rows with more gathered entries
 // than shared memory holds take the same steps over the buffers in global memory.  Block
 // shapes: 256 threads and 4096 or 8192 score keys for short rows; 5120 staged entries and 256
-// threads for single-chunk rows and where a row's buffers cannot hold more; else 24576 entries
-// and 512 threads (1024 when there are no more rows than SMs).
+// threads for single-chunk rows and where a row's buffers cannot hold more; else 10240 entries
+// and 512 threads, or 24576 entries and 1024 threads when there are no more rows than SMs.
 #include "kernels.h"
 #include "ptx.cuh"
 #include "topk.cuh"
@@ -33,6 +33,7 @@ constexpr int kSortMax = 2048;      // topk <= 2048
 constexpr int kMaxSeg = 64 * kSub;  // (chunk, sub-buffer) segments of a row
 constexpr int kSmallStage = 5120, kSmallThreads = 256;
 constexpr int kBigStage = 24576, kBigThreads = 512;
+constexpr int kMidStage = 10240;   // 107 KB: two rows per SM
 constexpr int kDenseKeys = 4096, kDenseThreads = 256;
 
 template <int STAGE>
@@ -546,7 +547,9 @@ cudaError_t launch_select(int n_q, int n_chunks, int cap, int topk, int trivial_
     return launch_shape<SelSmem<kSmallStage>, kSmallThreads, false>(DSA_SEL_ARGS);
   // few rows (decode): one CTA per row leaves most SMs idle, so each row gets 1024 threads
   if (n_q <= device_sm_count()) return launch_shape<SelSmem<kBigStage>, 2 * kBigThreads, false>(DSA_SEL_ARGS);
-  return launch_shape<SelSmem<kBigStage>, kBigThreads, false>(DSA_SEL_ARGS);
+  // many multi-chunk rows (chunk_1m): the entries at or above the row's edge (the largest of its
+  // chunks' edges) number a few k, so two rows share an SM
+  return launch_shape<SelSmem<kMidStage>, kBigThreads, false>(DSA_SEL_ARGS);
 #undef DSA_SEL_ARGS
 }
 
