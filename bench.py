@@ -220,14 +220,19 @@ def roofline_numbers(w, geo):
 # launch is too long for a full-set capture) and is scaled by the 4096 / 608 units: each
 # group streams the same chunks, so the traffic grows with the number of groups.
 MEASURED_TRAFFIC = {
-    ("indexer", "chunk_1m"): ((5.244348e9 + 0.620581e9) * 4096 / 608, "indexer.cu", "12bbe372616c92c4",
+    ("indexer", "chunk_1m"): ((5.244348e9 + 0.620581e9) * 4096 / 608, ("indexer.cu", "api.cu"), "not-yet-captured",
                               "profiles/indexer_chunk_1m.md (608-query slice, scaled by 4096/608)"),
 }
 
 
-def _src_sha(rel: str) -> str:
-    with open(os.path.join(ROOT, "dsa_indexer_cross_gb300", "csrc", rel), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def _src_sha(rels) -> str:
+    """SHA-256 (first 16 hex digits) over the named csrc files: the kernel and the host code
+    that plans its launch (buffer sizes change its traffic too)."""
+    h = hashlib.sha256()
+    for rel in rels:
+        with open(os.path.join(ROOT, "dsa_indexer_cross_gb300", "csrc", rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def traffic_for(kernel: str, workload: str):
@@ -236,7 +241,7 @@ def traffic_for(kernel: str, workload: str):
         return None, "no ncu capture of the current kernel for this workload"
     nbytes, src, sha, where = t
     if _src_sha(src) != sha:
-        return None, f"{src} changed since the capture in {where}"
+        return None, f"{', '.join(src)} changed since the capture in {where}"
     return nbytes, f"ncu dram__bytes_read.sum + dram__bytes_write.sum, {where}"
 
 

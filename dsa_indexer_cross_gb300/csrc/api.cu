@@ -235,14 +235,18 @@ IndexerLayout indexer_layout(const dsa_indexer_desc* d, int sms) {
   chunk = (chunk + 127) / 128 * 128;
   p.chunk = static_cast<int>(chunk);
   p.n_chunks = static_cast<int>((span + chunk - 1) / chunk);
-  // candidates per (row, chunk), in kSub sub-buffers: every key of the chunk when a row's part
-  // of it has at most kDirectMax keys, else 16K, or 32K for chunks over 64K keys.  The streaming
-  // threshold keeps about k (1 + ln(chunk / k)) keys with an exact threshold (12K of a 256K
-  // chunk at k = 2048) and some 40 % more with its 1/16-octave histogram bins; a sub-buffer that
-  // fills anyway (scores that keep rising along the keys) is cut back to its top-k by its warp,
-  // a pass that holds up the whole CTA, so the buffers are sized to make that rare.
+  // candidates per (row, chunk), in kSub sub-buffers: room for every key of the chunk, up to 64K
+  // entries (chunks of more keys).  Rows longer than kDirectMax keys in the chunk are filtered by
+  // the streaming threshold, which keeps about k (1 + ln(chunk / k)) keys with an exact
+  // threshold (12K of a 256K chunk at k = 2048) and some 40 % more with its 1/16-octave histogram
+  // bins, and the unit's end compacts them to those at or above the final threshold; the room
+  // is for the keys kept before the threshold has risen.  A sub-buffer that fills anyway (scores
+  // rising along the keys) is cut back to its top-k by its warp, a pass that holds up the whole
+  // CTA: with 16K entries for 32K-key chunks and 32K for 256K-key chunks, ~44 K and ~7.5 K
+  // cut-backs a call took long_32k's indexer to 21.0 ms and chunk_1m's to 65.3 ms, against
+  // 11.1 and 51.4 ms with none.
   const long long span_keys = std::min<long long>(chunk, span);
-  p.cap = span_keys > kDirectMax ? (span_keys > 65536 ? 32768 : 16384) : static_cast<int>((span_keys + 127) / 128 * 128);
+  p.cap = static_cast<int>((std::min<long long>(span_keys, 65536) + 127) / 128 * 128);
   const long long units = static_cast<long long>(p.n_groups) * p.n_chunks;
   p.grid = static_cast<int>(units < sms ? units : sms);
   if (p.grid < 1) p.grid = 1;

@@ -225,9 +225,11 @@ def test_indexer_rising_scores_cut_back_the_buffer():
     candidate buffer fills up and has to be cut back to its exact top-k (ties to the lower
     key index) again and again; the result is still exactly the oracle's set.  Here every
     head sees s_j = k_j[0], which rises with j in steps of bf16 rounding, so long runs of
-    equal scores exercise the tie rule as well."""
+    equal scores exercise the tie rule as well.  The buffers have room for every key of a
+    chunk up to 64K keys, so the rows here span one chunk of up to 100K keys: a lane quarter
+    of it (25K keys) overflows its 16K entries."""
     from oracle import dsa_oracle as O
-    n_q, n_kv, H, d, topk = 2432, 40000, 64, 128, 2048   # 608 groups of 4 rows: one chunk per row
+    n_q, n_kv, H, d, topk = 2432, 100000, 64, 128, 2048   # 608 groups of 4 rows: one chunk per row
     q = torch.zeros((n_q, H, d), dtype=torch.float32)
     q[:, :, 0] = 1.0
     k = torch.zeros((n_kv, d), dtype=torch.float32)
