@@ -562,7 +562,11 @@ __global__ void __launch_bounds__(Cfg<HI, DI, G>::THREADS, 1)
       // half's many queries already give independent chains)
       constexpr int NP = HI >= 16 ? 4 : 2;
       constexpr int NPP = NP / 2;
-      for (int i = 0; i < ui.n_tiles; ++i, ++tile) {
+      // the tiles run in an inner loop with no call in it: a sub-buffer that could overflow on
+      // the next tile leaves it, is cut back here, and the tiles go on
+      uint32_t full = 0u;
+      for (int i = 0;;) {
+      for (; i < ui.n_tiles; ++i, ++tile) {
         const int buf = tile & 1;
         ok = warp_wait(&sh.t_full[buf], (tile >> 1) & 1, &sh.abort_flag, status, wait_ns);
         if (!ok) break;
@@ -630,17 +634,27 @@ __global__ void __launch_bounds__(Cfg<HI, DI, G>::THREADS, 1)
           }
           if (keep && qf[g]) atomicAdd(&sh.hist[par][g0 + g][hist_bin<C>(keys[g])], 1u);
           cnt[g] += __popc(m);
-          if (qf[g] && cnt[g] > cap4 - 32) {
-            // this sub-buffer could overflow on the next tile (scores rising along the keys):
-            // cut it back to exactly its own top-k, which keeps every key of the row's top-k in it
-            if (cnt[g] > cap4) {
-              if (lane == 0) atomicOr(status, DEV_ERR_OVERFLOW);
-              cnt[g] = cap4;
-            }
-            __syncwarp();   // this warp's stores are visible to all its lanes
-            cnt[g] = warp_cut_to_topk(A.cand_key + sub_off[g], A.cand_idx + sub_off[g], cnt[g], A.topk, sh.ws[hw]);
-          }
+          full |= (qf[g] && cnt[g] > cap4 - 32) ? 1u << g : 0u;
         }
+        if (full != 0u) {   // warp-uniform: masks and counts are the same in every lane
+          ++i;
+          ++tile;
+          break;
+        }
+      }
+      if (full == 0u) break;   // every tile done, or a wait ran out (ok is false)
+      __syncwarp();            // this warp's stores are visible to all its lanes
+      for (int g = 0; g < GH; ++g) {
+        if (!((full >> g) & 1u)) continue;
+        // scores rising along the keys: cut the sub-buffer back to exactly its own top-k,
+        // which keeps every key of the row's top-k that lies in it
+        if (cnt[g] > cap4) {
+          if (lane == 0) atomicOr(status, DEV_ERR_OVERFLOW);
+          cnt[g] = cap4;
+        }
+        cnt[g] = warp_cut_to_topk(A.cand_key + sub_off[g], A.cand_idx + sub_off[g], cnt[g], A.topk, sh.ws[hw]);
+      }
+      full = 0u;
       }
       if (!ok) break;
       // A filtered query's sub-buffer still holds the keys kept while its threshold was lower:
