@@ -220,7 +220,7 @@ def roofline_numbers(w, geo):
 # launch is too long for a full-set capture) and is scaled by the 4096 / 608 units: each
 # group streams the same chunks, so the traffic grows with the number of groups.
 MEASURED_TRAFFIC = {
-    ("indexer", "chunk_1m"): ((1.010259e9 + 0.596139e9) * 4096 / 608, ("indexer.cu", "api.cu"), "33daf392638edcf8",
+    ("indexer", "chunk_1m"): ((1.029944e9 + 0.616998e9) * 4096 / 608, ("indexer.cu", "api.cu"), "4f4ee760241914ca",
                               "profiles/indexer_chunk_1m.md (608-query slice, scaled by 4096/608)"),
 }
 
