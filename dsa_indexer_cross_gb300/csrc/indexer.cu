@@ -566,95 +566,95 @@ __global__ void __launch_bounds__(Cfg<HI, DI, G>::THREADS, 1)
       // the next tile leaves it, is cut back here, and the tiles go on
       uint32_t full = 0u;
       for (int i = 0;;) {
-      for (; i < ui.n_tiles; ++i, ++tile) {
-        const int buf = tile & 1;
-        ok = warp_wait(&sh.t_full[buf], (tile >> 1) & 1, &sh.abort_flag, status, wait_ns);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t tbase = tmem + t_lane + buf * N + half * NH;
-        // thresholds read now (a stale one is lower, which only keeps more), used after the sum
-        uint32_t tk[GH];
+        for (; i < ui.n_tiles; ++i, ++tile) {
+          const int buf = tile & 1;
+          ok = warp_wait(&sh.t_full[buf], (tile >> 1) & 1, &sh.abort_flag, status, wait_ns);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t tbase = tmem + t_lane + buf * N + half * NH;
+          // thresholds read now (a stale one is lower, which only keeps more), used after the sum
+          uint32_t tk[GH];
 #pragma unroll
-        for (int g = 0; g < GH; ++g) tk[g] = qf[g] ? *reinterpret_cast<volatile uint32_t*>(&sh.tau[par][g0 + g]) : 0u;
-        float part[GH][NP];
+          for (int g = 0; g < GH; ++g) tk[g] = qf[g] ? *reinterpret_cast<volatile uint32_t*>(&sh.tau[par][g0 + g]) : 0u;
+          float part[GH][NP];
 #pragma unroll
-        for (int g = 0; g < GH; ++g)
+          for (int g = 0; g < GH; ++g)
 #pragma unroll
-          for (int p = 0; p < NP; ++p) part[g][p] = 0.f;
+            for (int p = 0; p < NP; ++p) part[g][p] = 0.f;
 #pragma unroll
-        for (int c0 = 0; c0 < NH; c0 += 32) {
-          uint32_t v[32];
-          tmem_ld32(tbase + c0, v);
-          tmem_ld_wait();
+          for (int c0 = 0; c0 < NH; c0 += 32) {
+            uint32_t v[32];
+            tmem_ld32(tbase + c0, v);
+            tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 32; j += 4) {
-            const int c = c0 + j;
-            const int gl = c / HI;   // query within the half (HI is a multiple of 4)
-            const int pa = (2 * (c / 4)) % NPP, pb = (2 * (c / 4) + 1) % NPP;
-            const float r0 = fmaxf(__uint_as_float(v[j]), 0.f), r1 = fmaxf(__uint_as_float(v[j + 1]), 0.f);
-            const float r2 = fmaxf(__uint_as_float(v[j + 2]), 0.f), r3 = fmaxf(__uint_as_float(v[j + 3]), 0.f);
-            fma2(part[gl][2 * pa], part[gl][2 * pa + 1], wreg[c], wreg[c + 1], r0, r1);
-            fma2(part[gl][2 * pb], part[gl][2 * pb + 1], wreg[c + 2], wreg[c + 3], r2, r3);
+            for (int j = 0; j < 32; j += 4) {
+              const int c = c0 + j;
+              const int gl = c / HI;   // query within the half (HI is a multiple of 4)
+              const int pa = (2 * (c / 4)) % NPP, pb = (2 * (c / 4) + 1) % NPP;
+              const float r0 = fmaxf(__uint_as_float(v[j]), 0.f), r1 = fmaxf(__uint_as_float(v[j + 1]), 0.f);
+              const float r2 = fmaxf(__uint_as_float(v[j + 2]), 0.f), r3 = fmaxf(__uint_as_float(v[j + 3]), 0.f);
+              fma2(part[gl][2 * pa], part[gl][2 * pa + 1], wreg[c], wreg[c + 1], r0, r1);
+              fma2(part[gl][2 * pb], part[gl][2 * pb + 1], wreg[c + 2], wreg[c + 3], r2, r3);
+            }
+          }
+          float accs[GH];   // this lane's key (row of the quarter): its score for every query of the half
+#pragma unroll
+          for (int g = 0; g < GH; ++g) {
+            float sp[NP];
+#pragma unroll
+            for (int p = 0; p < NP; ++p) sp[p] = part[g][p];
+#pragma unroll
+            for (int w2 = NP / 2; w2 >= 1; w2 /= 2)
+#pragma unroll
+              for (int p = 0; p < w2; ++p) sp[p] += sp[p + w2];
+            accs[g] = sp[0];
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh.t_empty[buf]);
+          const int j = ui.kbeg + i * kKeyTile + row;
+          // every query's keep mask first (independent work), then the stores where one is set
+          uint32_t keys[GH], masks[GH], any = 0u;
+#pragma unroll
+          for (int g = 0; g < GH; ++g) {
+            keys[g] = float_key(accs[g]);
+            masks[g] = __ballot_sync(0xffffffffu, j >= qa[g] && j < qb[g] && keys[g] >= tk[g]);
+            any |= masks[g];
+          }
+          if (any == 0u) continue;
+#pragma unroll
+          for (int g = 0; g < GH; ++g) {
+            const uint32_t m = masks[g];
+            if (m == 0u) continue;
+            const bool keep = (m >> lane) & 1u;
+            const int p = cnt[g] + __popc(m & below);
+            if (keep && p < cap4) {
+              A.cand_key[sub_off[g] + p] = keys[g];
+              A.cand_idx[sub_off[g] + p] = j;
+            }
+            if (keep && qf[g]) atomicAdd(&sh.hist[par][g0 + g][hist_bin<C>(keys[g])], 1u);
+            cnt[g] += __popc(m);
+            full |= (qf[g] && cnt[g] > cap4 - 32) ? 1u << g : 0u;
+          }
+          if (full != 0u) {   // warp-uniform: masks and counts are the same in every lane
+            ++i;
+            ++tile;
+            break;
           }
         }
-        float accs[GH];   // this lane's key (row of the quarter): its score for every query of the half
-#pragma unroll
+        if (full == 0u) break;   // every tile done, or a wait ran out (ok is false)
+        __syncwarp();            // this warp's stores are visible to all its lanes
         for (int g = 0; g < GH; ++g) {
-          float sp[NP];
-#pragma unroll
-          for (int p = 0; p < NP; ++p) sp[p] = part[g][p];
-#pragma unroll
-          for (int w2 = NP / 2; w2 >= 1; w2 /= 2)
-#pragma unroll
-            for (int p = 0; p < w2; ++p) sp[p] += sp[p + w2];
-          accs[g] = sp[0];
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sh.t_empty[buf]);
-        const int j = ui.kbeg + i * kKeyTile + row;
-        // every query's keep mask first (independent work), then the stores where one is set
-        uint32_t keys[GH], masks[GH], any = 0u;
-#pragma unroll
-        for (int g = 0; g < GH; ++g) {
-          keys[g] = float_key(accs[g]);
-          masks[g] = __ballot_sync(0xffffffffu, j >= qa[g] && j < qb[g] && keys[g] >= tk[g]);
-          any |= masks[g];
-        }
-        if (any == 0u) continue;
-#pragma unroll
-        for (int g = 0; g < GH; ++g) {
-          const uint32_t m = masks[g];
-          if (m == 0u) continue;
-          const bool keep = (m >> lane) & 1u;
-          const int p = cnt[g] + __popc(m & below);
-          if (keep && p < cap4) {
-            A.cand_key[sub_off[g] + p] = keys[g];
-            A.cand_idx[sub_off[g] + p] = j;
+          if (!((full >> g) & 1u)) continue;
+          // scores rising along the keys: cut the sub-buffer back to exactly its own top-k,
+          // which keeps every key of the row's top-k that lies in it
+          if (cnt[g] > cap4) {
+            if (lane == 0) atomicOr(status, DEV_ERR_OVERFLOW);
+            cnt[g] = cap4;
           }
-          if (keep && qf[g]) atomicAdd(&sh.hist[par][g0 + g][hist_bin<C>(keys[g])], 1u);
-          cnt[g] += __popc(m);
-          full |= (qf[g] && cnt[g] > cap4 - 32) ? 1u << g : 0u;
+          cnt[g] = warp_cut_to_topk(A.cand_key + sub_off[g], A.cand_idx + sub_off[g], cnt[g], A.topk, sh.ws[hw]);
         }
-        if (full != 0u) {   // warp-uniform: masks and counts are the same in every lane
-          ++i;
-          ++tile;
-          break;
-        }
-      }
-      if (full == 0u) break;   // every tile done, or a wait ran out (ok is false)
-      __syncwarp();            // this warp's stores are visible to all its lanes
-      for (int g = 0; g < GH; ++g) {
-        if (!((full >> g) & 1u)) continue;
-        // scores rising along the keys: cut the sub-buffer back to exactly its own top-k,
-        // which keeps every key of the row's top-k that lies in it
-        if (cnt[g] > cap4) {
-          if (lane == 0) atomicOr(status, DEV_ERR_OVERFLOW);
-          cnt[g] = cap4;
-        }
-        cnt[g] = warp_cut_to_topk(A.cand_key + sub_off[g], A.cand_idx + sub_off[g], cnt[g], A.topk, sh.ws[hw]);
-      }
-      full = 0u;
+        full = 0u;
       }
       if (!ok) break;
       // A filtered query's sub-buffer still holds the keys kept while its threshold was lower:
