@@ -221,7 +221,7 @@ def roofline_numbers(w, geo):
 # launch is too long for a full-set capture) and is scaled by the 4096 / 608 units: each
 # group streams the same chunks, so the traffic grows with the number of groups.
 MEASURED_TRAFFIC = {
-    ("indexer", "chunk_1m"): ((1.029944e9 + 0.616998e9) * 4096 / 608, ("indexer.cu", "api.cu"), "43cc08bc18f4d9cf",
+    ("indexer", "chunk_1m"): ((1.031415e9 + 0.618000e9) * 4096 / 608, ("indexer.cu", "api.cu"), "ebfe4a38773bb214",
                               "profiles/indexer_chunk_1m.md (608-query slice, scaled by 4096/608)"),
 }
 
