@@ -36,3 +36,22 @@ def test_prefill_4k_selected_pairs():
     R = bench.roofline_numbers(w, synth.geometry(w))
     assert R["rows"] == sum(t + 1 for t in range(2048)) + 2048 * 2048 == 6_292_480
     assert R["attn_flops"] == 2.0 * 6_292_480 * 16 * 1088
+
+
+def test_traffic_figure_is_keyed_to_its_sources(tmp_path, monkeypatch):
+    """The captured DRAM traffic is reported only while the kernel and planner sources are the
+    ones it was captured from; a layout-only change keeps it, any other change drops it."""
+    csrc = tmp_path / "dsa_indexer_cross_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (csrc / "k.cu").write_text("int f(int x) {\n  return x + 1;\n}\n")
+    (csrc / "p.cu").write_text("int g() { return 2; }\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    sha = bench._src_sha(("k.cu", "p.cu"))
+    monkeypatch.setitem(bench.MEASURED_TRAFFIC, ("kern", "wl"), (123.0, ("k.cu", "p.cu"), sha, "a capture"))
+    assert bench.traffic_for("kern", "wl")[0] == 123.0
+    (csrc / "k.cu").write_text("int f(int x)\n{\n    return x + 1;   \n}\n")   # layout only
+    assert bench.traffic_for("kern", "wl")[0] == 123.0
+    (csrc / "p.cu").write_text("int g() { return 3; }\n")
+    nbytes, why = bench.traffic_for("kern", "wl")
+    assert nbytes is None and "changed since the capture" in why
+    assert bench.traffic_for("other", "wl")[0] is None
