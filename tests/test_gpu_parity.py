@@ -82,6 +82,27 @@ def test_indexer_ragged_ranges(H_I, d, r, topk):
     _check_indexer(w, geo, L, list(range(n_q)))
 
 
+@pytest.mark.parametrize("topk", [512, 2048])
+def test_indexer_filtered_rows_in_the_dense_select(topk):
+    """Rows of 4100-8192 keys in one chunk (608 groups of 4 rows: the chunk is the whole row):
+    the indexer filters them (more than 4096 keys in the chunk), so the final select sees only
+    the keys at or above each row's threshold, and since no row is longer than 8192 keys it
+    takes the dense path (one score key per offset of the row), where many offsets hold no
+    entry.  With and without scores requested, the same keys are selected."""
+    rng = np.random.default_rng(31 + topk)
+    n_q, n_kv = 2432, 8192
+    ks = np.zeros(n_q, np.int32)
+    ke = rng.integers(4100, n_kv + 1, n_q).astype(np.int32)
+    ke[3] = n_kv
+    geo = synth.Geometry(n_kv, rng.integers(0, 9000, n_q).astype(np.int32),
+                         rng.integers(0, 9000, n_kv).astype(np.int32), ks, ke)
+    w = synth.Workload("filtered", "prefill", n_q, ("full",), 64, 128, 64, 1e4, topk, 4)
+    L = synth.layer_inputs(w, geo, 0, device=DEV, with_attn=False)
+    idx = _check_indexer(w, geo, L, [0, 3, 100, 777, 1500, n_q - 1] + list(range(5, n_q, 97)))
+    idx2, _, bits = run_indexer(w, geo, L, want_scores=False)
+    assert bits == 0 and torch.equal(idx, idx2)
+
+
 def test_indexer_independent_rows_decode_shape():
     # batched decode: each row is its own sequence in a packed, already-rotated key cache
     w = synth.Workload("decode_small", "decode", 6, ("full",), 64, 128, 64, 8e6, 256, 8, n_seqs=6, len_lo=1,
